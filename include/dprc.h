@@ -1,0 +1,196 @@
+/*
+ * dprc.h - C ABI of libdprc, the GB300 (sm_103a) hot path of DP-SGD with
+ * randomized clipping (DP-SGD-RC): per-sample, per-layer gradient-norm
+ * estimation, clip factors and the Gaussian noise add.
+ *
+ * Source of the method: "Efficient DP-SGD for LLMs with Randomized Clipping"
+ * (ICML 2026, arXiv 2605.24879), as described by the papernotes.org notes
+ * ("Method > Overall framework", "Method > Key design") and the gist.science
+ * technical summary ("Methodologie > Kernmechanisme", "Algorithmische Flow").
+ *
+ * Setting.  For one linear-like layer a forward hook captures the activations
+ * A (B x T x d) and a backward hook the output gradients G (B x T x p).  The
+ * per-sample weight gradient is A_i^T G_i, and its squared Frobenius norm is
+ *     n_i = ||A_i^T G_i||_F^2 = trace(G_i^T A_i A_i^T G_i) = trace(O_i).
+ * The norm-estimation routine returns an estimate n_hat_i^(l) per layer l; the
+ * layerwise sum n_i = sum_l n_hat_i^(l) sets the clip factor min(1, C/sqrt(n_i))
+ * that rescales sample i's loss; after the second backward pass the aggregated
+ * gradient receives sigma*C*N(0, I) noise.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Pointers named as device pointers must point to device memory (or
+ *    managed memory) that stays valid until the enqueued work completes.  The
+ *    library never allocates or frees memory.  Scratch memory is passed in as
+ *    `ws` (see dprc_workspace_bytes); its contents need no initialisation and
+ *    are garbage after a call.
+ *  - `stream` is a cudaStream_t passed as void*; NULL means the legacy default
+ *    stream.  Calls only enqueue work and return; results are ready when the
+ *    stream reaches them.  Calls on different streams may run concurrently
+ *    only if they use different workspaces and outputs.
+ *  - Layouts are dense and row-major: A [B][T][d], G [B][T][p], P and S
+ *    [p][k] (k contiguous), outputs [B].  Element types are given by `dtype`
+ *    (DPRC_F32 = float32, DPRC_BF16 = bfloat16); A, G, P and S share it.
+ *  - Argument errors (null pointers, non-positive or inconsistent sizes,
+ *    misaligned pointers, a workspace that is too small) return an error code
+ *    before anything is enqueued.  A failed kernel launch returns
+ *    DPRC_ERR_CUDA.  Nothing throws across this boundary.
+ *  - Every wait inside a kernel is bounded; a wait that runs out sets the
+ *    device error word that dprc_device_error() reads, and the kernel returns.
+ *  - `accumulate` = 0 overwrites n[i]; `accumulate` != 0 adds to it, which is
+ *    how the layerwise sum is formed across layers.
+ */
+#ifndef DPRC_H
+#define DPRC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DPRC_ABI_VERSION 1
+
+typedef enum {
+    DPRC_OK = 0,
+    DPRC_ERR_NULL = 1,        /* a required pointer is NULL */
+    DPRC_ERR_SHAPE = 2,       /* a size is out of range or inconsistent */
+    DPRC_ERR_DTYPE = 3,       /* unknown dtype */
+    DPRC_ERR_ALIGN = 4,       /* a pointer is not 16-byte aligned */
+    DPRC_ERR_WORKSPACE = 5,   /* ws_bytes < dprc_workspace_bytes(...) or ws NULL */
+    DPRC_ERR_CUDA = 6,        /* a CUDA runtime/driver call failed */
+    DPRC_ERR_NONFINITE = 7,   /* reserved: reported through counters, not returns */
+    DPRC_ERR_DEVICE = 8       /* no usable sm_103 device for this call */
+} dprc_status;
+
+typedef enum { DPRC_F32 = 0, DPRC_BF16 = 1 } dprc_dtype;
+
+typedef enum {
+    DPRC_OP_HUTCH = 1,
+    DPRC_OP_HUTCHPP = 2,
+    DPRC_OP_EXACT = 3
+} dprc_op;
+
+/* Version of this ABI (DPRC_ABI_VERSION of the built library). */
+int dprc_abi_version(void);
+
+/* Short static description of a status code. */
+const char* dprc_status_string(dprc_status s);
+
+/*
+ * Scratch bytes needed by one call of `op` with these sizes (k is the
+ * projection width for DPRC_OP_HUTCH, the sketch width r for
+ * DPRC_OP_HUTCHPP, ignored for DPRC_OP_EXACT).  Returns 0 for invalid sizes.
+ * The size depends on the current device's SM count.
+ */
+size_t dprc_workspace_bytes(dprc_op op, dprc_dtype dtype, int64_t B, int64_t T,
+                            int64_t d, int64_t p, int64_t k);
+
+/*
+ * Hutchinson estimate of each sample's squared gradient norm for one layer:
+ *     n_hat_i = trace(P^T O_i P) = ||A_i^T (G_i P)||_F^2.
+ * (papernotes.org, "Key design > Hutchinson random projection": the sketch
+ *  Y = A^T (G P) is formed without the d x p gradient or any T x T matrix.)
+ *  A  device [B][T][d], G device [B][T][p], P device [p][k], all `dtype`.
+ *     P is one projection shared by the batch, entries N(0, 1/k) drawn by the
+ *     caller (a fresh P per layer and step).
+ *  n  device float [B]: n[i] = (accumulate ? n[i] : 0) + n_hat_i.
+ *  Sizes: B >= 1, T >= 1, d >= 1, p >= 1, 1 <= k <= 256.
+ *  Arithmetic: products and sums in fp32 (bf16 inputs are exact in fp32).
+ *  All pointers 16-byte aligned.  The result is deterministic for fixed
+ *  inputs, sizes and device.
+ */
+dprc_status dprc_norm_hutch(const void* A, const void* G, const void* P, dprc_dtype dtype,
+                            int64_t B, int64_t T, int64_t d, int64_t p, int64_t k,
+                            float* n, int accumulate, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Hutch++ head/tail estimate for one layer (papernotes.org, "Key design >
+ * Hutch++ head-tail decomposition"; gist.science, "Kernmechanisme" item 2):
+ *     Q_i     = orthonormal basis of Col(O_i S)          (p x r, thin QR)
+ *     n_hat_i = ||A_i^T G_i Q_i||_F^2 + (1/r) ||A_i^T G_i (I - Q_i Q_i^T) P||_F^2
+ *  S, P device [p][r], `dtype`, entries N(0, 1) drawn by the caller and shared
+ *  by the batch.  O_i S is formed as G_i^T (A_i (A_i^T (G_i S))); the QR is a
+ *  per-sample Householder QR in fp32.  Sizes as dprc_norm_hutch with
+ *  1 <= r <= 64.  Other arguments as dprc_norm_hutch.
+ */
+dprc_status dprc_norm_hutchpp(const void* A, const void* G, const void* S, const void* P,
+                              dprc_dtype dtype, int64_t B, int64_t T, int64_t d, int64_t p,
+                              int64_t r, float* n, int accumulate, void* ws, size_t ws_bytes,
+                              void* stream);
+
+/*
+ * Exact squared norm by the ghost-clipping identity (the comparison path the
+ * pages set the method against; papernotes.org, "Research background"):
+ *     n_i = sum_{t,s} (A_i A_i^T)_{ts} (G_i G_i^T)_{ts}
+ * computed tile by tile; no T x T matrix is stored.  O(T^2 (d + p)) work.
+ * Arguments as dprc_norm_hutch without P and k.
+ */
+dprc_status dprc_exact_norm(const void* A, const void* G, dprc_dtype dtype, int64_t B,
+                            int64_t T, int64_t d, int64_t p, float* n, int accumulate,
+                            void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Clip factors c_i = min(1, C / sqrt(n_i)) (papernotes.org, "Method > Overall
+ * framework").  n_i = 0 gives 1.  A non-finite or negative n_i gives 0 and is
+ * counted in *nonfinite (device int32, may be NULL; the count is added to it).
+ *  n, c device float [B]; B >= 1; C > 0 and finite.
+ */
+dprc_status dprc_clip_factors(const float* n, int64_t B, float C, float* c,
+                              int32_t* nonfinite, void* stream);
+
+/*
+ * Gaussian noise add on the aggregated gradient: grad[e] += sigma * C * z_e
+ * (papernotes.org, "Method > Overall framework": the aggregated gradient plus
+ * sigma*C*N(0, I)).  z_e comes from the Philox4x32-10 stream of
+ * dprc_philox_words: word (e & 3) of block (e >> 2), Box-Muller on the word
+ * pairs (w0, w1) and (w2, w3) with u1 = ((w_a >> 8) + 1) * 2^-24 and
+ * u2 = (w_b >> 8) * 2^-24:  z_a = sqrt(-2 ln u1) cos(2 pi u2),
+ * z_b = sqrt(-2 ln u1) sin(2 pi u2).  Any 1/B averaging belongs to the caller.
+ *  grad device float [N], in place, 16-byte aligned; N >= 0; sigma >= 0.
+ *  The same (seed, step) gives the same noise on every call and device.
+ */
+dprc_status dprc_add_noise(float* grad, int64_t N, float sigma, float C, uint64_t seed,
+                           uint64_t step, void* stream);
+
+/*
+ * The raw Philox4x32-10 stream behind dprc_add_noise (Salmon et al.,
+ * "Parallel Random Numbers: As Easy as 1, 2, 3", SC'11): block j is the
+ * generator applied to the counter (j_lo, j_hi, step_lo, step_hi) under the
+ * key (seed_lo, seed_hi).  Writes blocks [first_block, first_block + n_blocks)
+ * as out[4*(j - first_block) + w], w = 0..3.
+ *  out device uint32 [4 * n_blocks], 16-byte aligned; n_blocks >= 0.
+ */
+dprc_status dprc_philox_words(uint32_t* out, int64_t n_blocks, uint64_t first_block,
+                              uint64_t seed, uint64_t step, void* stream);
+
+/*
+ * Reads (and, if reset != 0, clears) the device error word of the current
+ * device.  Nonzero means a bounded in-kernel wait ran out (the value encodes
+ * which: see DPRC_DEVERR_*); the affected outputs are invalid.  This call
+ * synchronizes with the device.
+ */
+#define DPRC_DEVERR_PIPE_FULL 1   /* consumer waited too long for a tile */
+#define DPRC_DEVERR_PIPE_EMPTY 2  /* producer waited too long for a free stage */
+#define DPRC_DEVERR_ACCUM 3       /* epilogue waited too long for the accumulator */
+dprc_status dprc_device_error(int32_t* out, int reset);
+
+/*
+ * Timing hook.  With events != NULL, every later call made by this host
+ * thread records events[0] on its stream before its first kernel and
+ * events[s] after its s-th stage (up to n_events - 1 stages; a stage is one
+ * or two kernels: dprc_norm_hutch has 2 - the sketch G P and the projection
+ * with its norm; dprc_norm_hutchpp has 4 - Z, M, the QR step, the final pass).
+ * `events` are cudaEvent_t passed as void*, owned by the caller and valid
+ * while set.  Recording between kernels disables the overlap of dependent
+ * launches, so time whole calls with this hook off.  events = NULL,
+ * n_events = 0 turns it off.
+ */
+dprc_status dprc_set_phase_events(void** events, int n_events);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DPRC_H */

@@ -1,0 +1,30 @@
+"""GB300 (sm_103a) hot path of DP-SGD with randomized clipping (DP-SGD-RC).
+
+The compute lives in libdprc.so (C ABI: include/dprc.h): tensor-core
+Hutchinson and Hutch++ per-sample gradient-norm estimation, the exact
+ghost-clipping norm, clip factors and Philox Gaussian noise.  This package is
+its ctypes binding plus the seeded synthetic workloads used by the tests and
+the benchmark.
+"""
+
+from .binding import (  # noqa: F401
+    DPRC_BF16,
+    DPRC_F32,
+    DPRC_OP_EXACT,
+    DPRC_OP_HUTCH,
+    DPRC_OP_HUTCHPP,
+    EXPORTED,
+    DprcError,
+    dprc_abi_version,
+    dprc_add_noise,
+    dprc_clip_factors,
+    dprc_device_error,
+    dprc_exact_norm,
+    dprc_norm_hutch,
+    dprc_norm_hutchpp,
+    dprc_philox_words,
+    dprc_set_phase_events,
+    dprc_workspace_bytes,
+    lib,
+    workspace,
+)

@@ -1,0 +1,223 @@
+"""ctypes binding of libdprc (include/dprc.h): argument marshalling only.
+
+Every function here takes torch tensors for device memory, passes their data
+pointers and the current CUDA stream to the C ABI of the same name, and raises
+``DprcError`` on a non-zero status.  All arithmetic runs in the library's
+kernels; there is no fallback of any kind: if libdprc.so is missing, loading
+raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+PKG_DIR = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG_DIR, "libdprc.so")
+
+DPRC_F32, DPRC_BF16 = 0, 1
+DPRC_OP_HUTCH, DPRC_OP_HUTCHPP, DPRC_OP_EXACT = 1, 2, 3
+STATUS = {0: "ok", 1: "null pointer", 2: "shape", 3: "dtype", 4: "alignment",
+          5: "workspace", 6: "cuda", 7: "non-finite", 8: "device"}
+
+# The C prototypes of include/dprc.h, as (name, restype, argtypes).
+_c = ctypes
+_PROTOS = [
+    ("dprc_abi_version", _c.c_int, []),
+    ("dprc_status_string", _c.c_char_p, [_c.c_int]),
+    ("dprc_workspace_bytes", _c.c_size_t,
+     [_c.c_int, _c.c_int, _c.c_int64, _c.c_int64, _c.c_int64, _c.c_int64, _c.c_int64]),
+    ("dprc_norm_hutch", _c.c_int,
+     [_c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_int, _c.c_int64, _c.c_int64, _c.c_int64,
+      _c.c_int64, _c.c_int64, _c.c_void_p, _c.c_int, _c.c_void_p, _c.c_size_t, _c.c_void_p]),
+    ("dprc_norm_hutchpp", _c.c_int,
+     [_c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_int, _c.c_int64, _c.c_int64,
+      _c.c_int64, _c.c_int64, _c.c_int64, _c.c_void_p, _c.c_int, _c.c_void_p, _c.c_size_t,
+      _c.c_void_p]),
+    ("dprc_exact_norm", _c.c_int,
+     [_c.c_void_p, _c.c_void_p, _c.c_int, _c.c_int64, _c.c_int64, _c.c_int64, _c.c_int64,
+      _c.c_void_p, _c.c_int, _c.c_void_p, _c.c_size_t, _c.c_void_p]),
+    ("dprc_clip_factors", _c.c_int,
+     [_c.c_void_p, _c.c_int64, _c.c_float, _c.c_void_p, _c.c_void_p, _c.c_void_p]),
+    ("dprc_add_noise", _c.c_int,
+     [_c.c_void_p, _c.c_int64, _c.c_float, _c.c_float, _c.c_uint64, _c.c_uint64, _c.c_void_p]),
+    ("dprc_philox_words", _c.c_int,
+     [_c.c_void_p, _c.c_int64, _c.c_uint64, _c.c_uint64, _c.c_uint64, _c.c_void_p]),
+    ("dprc_device_error", _c.c_int, [_c.c_void_p, _c.c_int]),
+    ("dprc_set_phase_events", _c.c_int, [_c.c_void_p, _c.c_int]),
+]
+EXPORTED = tuple(name for name, _, _ in _PROTOS)
+
+_lib = None
+_lock = threading.Lock()
+
+
+class DprcError(RuntimeError):
+    def __init__(self, fn, status):
+        super().__init__(f"{fn} failed with status {status} ({STATUS.get(status, '?')})")
+        self.status = status
+
+
+def lib():
+    """The loaded libdprc (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        with _lock:
+            if _lib is None:
+                if not os.path.exists(LIB_PATH):
+                    raise RuntimeError(
+                        f"{LIB_PATH} is missing: build it with `python -c "
+                        "\"import __graft_entry__ as g; g.build()\"`")
+                h = ctypes.CDLL(LIB_PATH)
+                for name, res, args in _PROTOS:
+                    f = getattr(h, name)
+                    f.restype = res
+                    f.argtypes = args
+                _lib = h
+    return _lib
+
+
+def _dtype_code(t):
+    if t.dtype == torch.float32:
+        return DPRC_F32
+    if t.dtype == torch.bfloat16:
+        return DPRC_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _stream(t, stream):
+    if stream is not None:
+        return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else stream)
+    return ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _check(fn, status):
+    if status != 0:
+        raise DprcError(fn, status)
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise ValueError("libdprc takes device tensors")
+        if t is not None and not t.is_contiguous():
+            raise ValueError("libdprc takes contiguous tensors")
+
+
+def dprc_abi_version():
+    return lib().dprc_abi_version()
+
+
+def dprc_workspace_bytes(op, dtype_code, B, T, d, p, k):
+    return int(lib().dprc_workspace_bytes(op, dtype_code, B, T, d, p, k))
+
+
+def workspace(op, like, B, T, d, p, k):
+    """A device byte buffer of dprc_workspace_bytes(...) (torch allocation)."""
+    n = dprc_workspace_bytes(op, _dtype_code(like), B, T, d, p, k)
+    if n == 0:
+        raise DprcError("dprc_workspace_bytes", 2)
+    return torch.empty(n, dtype=torch.uint8, device=like.device)
+
+
+def dprc_norm_hutch(A, G, P, n, accumulate=False, ws=None, stream=None):
+    """n[i] (+)= ||A_i^T (G_i P)||_F^2 (see include/dprc.h)."""
+    _need_cuda(A, G, P, n)
+    B, T, d = A.shape
+    p, k = P.shape
+    if ws is None:
+        ws = workspace(DPRC_OP_HUTCH, A, B, T, d, p, k)
+    st = lib().dprc_norm_hutch(_ptr(A), _ptr(G), _ptr(P), _dtype_code(A), B, T, d, p, k,
+                               _ptr(n), int(bool(accumulate)), _ptr(ws), ws.numel(),
+                               _stream(A, stream))
+    _check("dprc_norm_hutch", st)
+    return n
+
+
+def dprc_norm_hutchpp(A, G, S, P, n, accumulate=False, ws=None, stream=None):
+    """n[i] (+)= Hutch++ head + tail / r (see include/dprc.h)."""
+    _need_cuda(A, G, S, P, n)
+    B, T, d = A.shape
+    p, r = P.shape
+    if ws is None:
+        ws = workspace(DPRC_OP_HUTCHPP, A, B, T, d, p, r)
+    st = lib().dprc_norm_hutchpp(_ptr(A), _ptr(G), _ptr(S), _ptr(P), _dtype_code(A), B, T, d, p,
+                                 r, _ptr(n), int(bool(accumulate)), _ptr(ws), ws.numel(),
+                                 _stream(A, stream))
+    _check("dprc_norm_hutchpp", st)
+    return n
+
+
+def dprc_exact_norm(A, G, n, accumulate=False, ws=None, stream=None):
+    """n[i] (+)= sum_{t,s} (A_i A_i^T)_{ts} (G_i G_i^T)_{ts} (see include/dprc.h)."""
+    _need_cuda(A, G, n)
+    B, T, d = A.shape
+    p = G.shape[2]
+    if ws is None:
+        ws = workspace(DPRC_OP_EXACT, A, B, T, d, p, 0)
+    st = lib().dprc_exact_norm(_ptr(A), _ptr(G), _dtype_code(A), B, T, d, p, _ptr(n),
+                               int(bool(accumulate)), _ptr(ws), ws.numel(), _stream(A, stream))
+    _check("dprc_exact_norm", st)
+    return n
+
+
+def dprc_clip_factors(n, C, c, nonfinite=None, stream=None):
+    """c[i] = min(1, C / sqrt(n[i])); non-finite or negative n gives 0."""
+    _need_cuda(n, c, nonfinite)
+    st = lib().dprc_clip_factors(_ptr(n), n.numel(), float(C), _ptr(c), _ptr(nonfinite),
+                                 _stream(n, stream))
+    _check("dprc_clip_factors", st)
+    return c
+
+
+def dprc_add_noise(grad, sigma, C, seed, step, stream=None):
+    """grad += sigma * C * z (Philox4x32-10 + Box-Muller), in place."""
+    _need_cuda(grad)
+    st = lib().dprc_add_noise(_ptr(grad), grad.numel(), float(sigma), float(C),
+                              int(seed) & (2**64 - 1), int(step) & (2**64 - 1),
+                              _stream(grad, stream))
+    _check("dprc_add_noise", st)
+    return grad
+
+
+def dprc_philox_words(out, first_block, seed, step, stream=None):
+    """Fills out (int32 [n, 4]) with Philox blocks first_block .. first_block + n - 1."""
+    _need_cuda(out)
+    n_blocks = out.numel() // 4
+    st = lib().dprc_philox_words(_ptr(out), n_blocks, int(first_block), int(seed) & (2**64 - 1),
+                                 int(step) & (2**64 - 1), _stream(out, stream))
+    _check("dprc_philox_words", st)
+    return out
+
+
+def dprc_device_error(reset=False):
+    v = ctypes.c_int32(0)
+    st = lib().dprc_device_error(ctypes.byref(v), int(bool(reset)))
+    _check("dprc_device_error", st)
+    return v.value
+
+
+_events_keepalive = None
+
+
+def dprc_set_phase_events(events):
+    """Record these torch.cuda.Event objects between the stages of later calls
+    on this thread (None turns it off)."""
+    global _events_keepalive
+    if not events:
+        _events_keepalive = None
+        _check("dprc_set_phase_events", lib().dprc_set_phase_events(None, 0))
+        return
+    for e in events:
+        if not e.cuda_event:  # torch creates the event on its first record
+            e.record()
+    arr = (ctypes.c_void_p * len(events))(*[ctypes.c_void_p(e.cuda_event) for e in events])
+    _events_keepalive = (arr, events)
+    _check("dprc_set_phase_events", lib().dprc_set_phase_events(arr, len(events)))

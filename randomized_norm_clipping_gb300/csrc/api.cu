@@ -1,0 +1,487 @@
+// libdprc C ABI: argument checks, scratch layout, dispatch to the kernels.
+//
+// Data flow of one Hutchinson call (tensor-core path):
+//   K1 row projection    W = G P             reads G once   (HBM-bound)
+//   K2 column projection Y = A^T W, ||Y||^2  reads A once   (HBM-bound)
+// K2 is launched with programmatic dependent launch so its prologue overlaps
+// the tail of K1.  Hutch++ chains three such pairs with the per-sample QR in
+// the middle; the float32 path runs the same steps on CUDA cores.
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <algorithm>
+
+#include "dprc.h"
+#include "internal.h"
+
+namespace dprc {
+namespace {
+
+constexpr int kDefaultSms = 152;
+constexpr int64_t kMaxT = int64_t(1) << 24;
+constexpr int64_t kMaxWidth = int64_t(1) << 20;
+constexpr int64_t kMaxB = 65535;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+dprc_status cuda_status(cudaError_t e) { return e == cudaSuccess ? DPRC_OK : DPRC_ERR_CUDA; }
+
+// Per-thread optional events recorded between the kernels of a call (timing).
+thread_local void** t_events = nullptr;
+thread_local int t_nevents = 0;
+
+void mark(int idx, cudaStream_t s) {
+  if (t_events != nullptr && idx < t_nevents && t_events[idx] != nullptr)
+    cudaEventRecord(static_cast<cudaEvent_t>(t_events[idx]), s);
+}
+
+bool device_ok() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess)
+    return false;
+  if (cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return false;
+  return major == 10 && minor == 3;
+}
+
+ColprojPlan colproj_geom(int64_t B, int64_t T, int64_t c, int n, int sms) {
+  ColprojPlan p;
+  p.n = n;
+  p.chunk = colproj_stage_chunk();
+  p.nchunks = static_cast<int>((c + p.chunk - 1) / p.chunk);
+  p.kt = static_cast<int>((T + 63) / 64);
+  p.units = B * p.nchunks * p.kt;
+  p.grid = static_cast<int>(std::min<int64_t>(p.units, sms));
+  const int64_t L = (p.units + p.grid - 1) / p.grid;
+  p.max_seg = static_cast<int>((L + p.kt - 1) / p.kt + 1);
+  p.part_bytes = static_cast<size_t>(p.grid) * p.max_seg * p.chunk * n * sizeof(float);
+  p.tick_count = static_cast<size_t>(B) * p.nchunks;
+  return p;
+}
+
+// Control block at the start of every tensor-core workspace:
+//   int32 tickets [B * max_chunks], int32 sample tickets [B],
+//   fp32 chunk norms [B * max_chunks].
+struct Ctrl {
+  size_t tick_off, stick_off, cnorm_off, end, zero_ints;
+};
+
+Ctrl ctrl_layout(int64_t B, int max_chunks) {
+  Ctrl c;
+  c.tick_off = 0;
+  c.stick_off = align_up(static_cast<size_t>(B) * max_chunks * 4, 256);
+  c.cnorm_off = align_up(c.stick_off + static_cast<size_t>(B) * 4, 256);
+  c.end = align_up(c.cnorm_off + static_cast<size_t>(B) * max_chunks * 4, 1024);
+  c.zero_ints = c.cnorm_off / 4;
+  return c;
+}
+
+void attach_ctrl(ColprojPlan& p, const Ctrl& c) {
+  p.tick_off = c.tick_off;
+  p.stick_off = c.stick_off;
+  p.cnorm_off = c.cnorm_off;
+}
+
+int64_t tpad_of(int64_t T) { return (T + 63) / 64 * 64; }
+
+}  // namespace
+
+int device_sm_count() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return kDefaultSms;
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    return kDefaultSms;
+  return n;
+}
+
+bool tc_path_supported(dprc_dtype dt, int64_t d, int64_t p, int64_t k, bool hutchpp) {
+  if (dt != DPRC_BF16) return false;
+  if (d % 8 != 0 || p % 8 != 0) return false;  // TMA row strides: multiples of 16 bytes
+  if (hutchpp) return k == 16 && p >= k;
+  return k == 16 || k == 32 || k == 64;
+}
+
+TcPlan plan_tc(dprc_op op, int64_t B, int64_t T, int64_t d, int64_t p, int64_t k) {
+  TcPlan t;
+  t.B = B;
+  t.T = T;
+  t.d = d;
+  t.p = p;
+  t.k = k;
+  t.tpad = tpad_of(T);
+  const int sms = device_sm_count();
+  const int nch_d = static_cast<int>((d + colproj_stage_chunk() - 1) / colproj_stage_chunk());
+  const int nch_p = static_cast<int>((p + colproj_stage_chunk() - 1) / colproj_stage_chunk());
+  const Ctrl c = ctrl_layout(B, std::max(nch_d, nch_p));
+  t.zero_ints = c.zero_ints;
+  size_t off = c.end;
+  size_t part = 0;
+  if (op == DPRC_OP_HUTCH) {
+    t.cp = colproj_geom(B, T, d, static_cast<int>(k), sms);
+    part = t.cp.part_bytes;
+    t.w_bytes = static_cast<size_t>(B) * 2 * k * t.tpad * 2;
+  } else {
+    const int r = static_cast<int>(k);
+    t.cp = colproj_geom(B, T, d, 2 * r, sms);  // the widest of the three launches
+    part = std::max({colproj_geom(B, T, d, r, sms).part_bytes,
+                     colproj_geom(B, T, p, r, sms).part_bytes, t.cp.part_bytes});
+    t.w_bytes = static_cast<size_t>(B) * 4 * r * t.tpad * 2;
+  }
+  attach_ctrl(t.cp, c);
+  t.w_off = off;
+  off = align_up(off + t.w_bytes, 1024);
+  if (op == DPRC_OP_HUTCHPP) {
+    const int64_t r = k;
+    t.z_off = off;
+    off = align_up(off + static_cast<size_t>(B) * d * 2 * r * 2, 1024);
+    t.m_off = off;
+    off = align_up(off + static_cast<size_t>(B) * p * r * 4, 1024);
+    t.qp_off = off;
+    off = align_up(off + static_cast<size_t>(B) * p * 4 * r * 2, 1024);
+    t.qscratch_off = off;
+    off = align_up(off + static_cast<size_t>(B) * p * r * 4 * 2, 1024);
+  }
+  t.cp.part_off = off;
+  off = align_up(off + part, 1024);
+  t.total = off;
+  return t;
+}
+
+SimtPlan plan_simt(dprc_op op, int64_t B, int64_t T, int64_t d, int64_t p, int64_t k) {
+  SimtPlan s;
+  const int64_t wide = op == DPRC_OP_HUTCHPP ? 2 * k : k;
+  size_t off = 0;
+  s.w_off = off;
+  off = align_up(off + static_cast<size_t>(B) * T * wide * 4, 1024);
+  s.y_off = off;
+  off = align_up(off + static_cast<size_t>(B) * d * wide * 4, 1024);
+  if (op == DPRC_OP_HUTCHPP) {
+    s.z_off = off;
+    off = align_up(off + static_cast<size_t>(B) * d * k * 4, 1024);
+    s.m_off = off;
+    off = align_up(off + static_cast<size_t>(B) * p * k * 4, 1024);
+    s.qp_off = off;
+    off = align_up(off + static_cast<size_t>(B) * p * 2 * k * 4, 1024);
+    s.qscratch_off = off;
+    off = align_up(off + static_cast<size_t>(B) * p * k * 4 * 2, 1024);
+  }
+  s.total = off;
+  return s;
+}
+
+size_t plan_exact_bytes(int64_t B, int64_t T) {
+  const int64_t nt = (T + 31) / 32;
+  return align_up(static_cast<size_t>(B) * nt * nt * 4, 1024);
+}
+
+// ---- tensor maps ------------------------------------------------------------
+namespace {
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = []() -> EncodeTiledFn {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<EncodeTiledFn>(p);
+  }();
+  return fn;
+}
+}  // namespace
+
+bool make_tmap_3d_bf16(CUtensorMap* map, const void* base, uint64_t dim0, uint64_t dim1,
+                       uint64_t dim2, uint64_t stride1_elems, uint64_t stride2_elems,
+                       uint32_t box0, uint32_t box1, int swizzle_bytes) {
+  EncodeTiledFn fn = encode_fn();
+  if (fn == nullptr) return false;
+  const cuuint64_t dims[3] = {dim0, dim1, dim2};
+  const cuuint64_t strides[2] = {stride1_elems * 2, stride2_elems * 2};
+  const cuuint32_t box[3] = {box0, box1, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_NONE;
+  if (swizzle_bytes == 32) swz = CU_TENSOR_MAP_SWIZZLE_32B;
+  if (swizzle_bytes == 64) swz = CU_TENSOR_MAP_SWIZZLE_64B;
+  if (swizzle_bytes == 128) swz = CU_TENSOR_MAP_SWIZZLE_128B;
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace dprc
+
+using namespace dprc;
+
+namespace {
+
+dprc_status check_common(dprc_dtype dt, int64_t B, int64_t T, int64_t d, int64_t p) {
+  if (dt != DPRC_F32 && dt != DPRC_BF16) return DPRC_ERR_DTYPE;
+  if (B < 1 || T < 1 || d < 1 || p < 1) return DPRC_ERR_SHAPE;
+  if (B > kMaxB || T > kMaxT || d > kMaxWidth || p > kMaxWidth) return DPRC_ERR_SHAPE;
+  return DPRC_OK;
+}
+
+size_t hutch_ws(dprc_dtype dt, int64_t B, int64_t T, int64_t d, int64_t p, int64_t k) {
+  return tc_path_supported(dt, d, p, k, false) ? plan_tc(DPRC_OP_HUTCH, B, T, d, p, k).total
+                                               : plan_simt(DPRC_OP_HUTCH, B, T, d, p, k).total;
+}
+
+size_t hutchpp_ws(dprc_dtype dt, int64_t B, int64_t T, int64_t d, int64_t p, int64_t r) {
+  return tc_path_supported(dt, d, p, r, true) ? plan_tc(DPRC_OP_HUTCHPP, B, T, d, p, r).total
+                                              : plan_simt(DPRC_OP_HUTCHPP, B, T, d, p, r).total;
+}
+
+}  // namespace
+
+extern "C" {
+
+int dprc_abi_version(void) { return DPRC_ABI_VERSION; }
+
+const char* dprc_status_string(dprc_status s) {
+  switch (s) {
+    case DPRC_OK: return "ok";
+    case DPRC_ERR_NULL: return "null pointer argument";
+    case DPRC_ERR_SHAPE: return "size out of range or inconsistent";
+    case DPRC_ERR_DTYPE: return "unknown dtype";
+    case DPRC_ERR_ALIGN: return "pointer not 16-byte aligned";
+    case DPRC_ERR_WORKSPACE: return "workspace missing or too small";
+    case DPRC_ERR_CUDA: return "CUDA call failed";
+    case DPRC_ERR_NONFINITE: return "non-finite value";
+    case DPRC_ERR_DEVICE: return "current device is not an sm_103 GPU";
+  }
+  return "unknown status";
+}
+
+size_t dprc_workspace_bytes(dprc_op op, dprc_dtype dtype, int64_t B, int64_t T, int64_t d,
+                            int64_t p, int64_t k) {
+  if (check_common(dtype, B, T, d, p) != DPRC_OK) return 0;
+  switch (op) {
+    case DPRC_OP_HUTCH:
+      if (k < 1 || k > 256) return 0;
+      return hutch_ws(dtype, B, T, d, p, k);
+    case DPRC_OP_HUTCHPP:
+      if (k < 1 || k > 64 || k > p) return 0;
+      return hutchpp_ws(dtype, B, T, d, p, k);
+    case DPRC_OP_EXACT:
+      return plan_exact_bytes(B, T);
+  }
+  return 0;
+}
+
+dprc_status dprc_set_phase_events(void** events, int n_events) {
+  if (n_events < 0 || (n_events > 0 && events == nullptr)) return DPRC_ERR_NULL;
+  t_events = n_events > 0 ? events : nullptr;
+  t_nevents = n_events;
+  return DPRC_OK;
+}
+
+dprc_status dprc_norm_hutch(const void* A, const void* G, const void* P, dprc_dtype dtype,
+                            int64_t B, int64_t T, int64_t d, int64_t p, int64_t k, float* n,
+                            int accumulate, void* ws, size_t ws_bytes, void* stream) {
+  if (!A || !G || !P || !n) return DPRC_ERR_NULL;
+  dprc_status st = check_common(dtype, B, T, d, p);
+  if (st != DPRC_OK) return st;
+  if (k < 1 || k > 256) return DPRC_ERR_SHAPE;
+  if (!aligned16(A) || !aligned16(G) || !aligned16(P) || !aligned16(n)) return DPRC_ERR_ALIGN;
+  if (!ws) return DPRC_ERR_WORKSPACE;
+  if (!aligned16(ws)) return DPRC_ERR_ALIGN;
+  if (!device_ok()) return DPRC_ERR_DEVICE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char* w = static_cast<char*>(ws);
+  if (tc_path_supported(dtype, d, p, k, false)) {
+    const TcPlan t = plan_tc(DPRC_OP_HUTCH, B, T, d, p, k);
+    if (ws_bytes < t.total) return DPRC_ERR_WORKSPACE;
+    mark(0, s);
+    cudaError_t e = launch_tc_rowproj(G, B, T, p, P, false, static_cast<int>(k), false,
+                                      w + t.w_off, t.tpad, reinterpret_cast<int*>(w), t.zero_ints,
+                                      s);
+    if (e != cudaSuccess) return DPRC_ERR_CUDA;
+    mark(1, s);
+    e = launch_tc_colproj(A, B, T, d, w + t.w_off, t.tpad, static_cast<int>(k), t.cp, w,
+                          kColprojNorm, n, accumulate, static_cast<int>(k), 1.0f, nullptr,
+                          nullptr, t_events == nullptr, s);
+    mark(2, s);
+    return cuda_status(e);
+  }
+  const SimtPlan sp = plan_simt(DPRC_OP_HUTCH, B, T, d, p, k);
+  if (ws_bytes < sp.total) return DPRC_ERR_WORKSPACE;
+  float* W = reinterpret_cast<float*>(w + sp.w_off);
+  float* Y = reinterpret_cast<float*>(w + sp.y_off);
+  const int ik = static_cast<int>(k);
+  mark(0, s);
+  cudaError_t e = launch_simt_rowproj(G, dtype, B, T, p, P, dtype, false, ik, W, s);
+  if (e != cudaSuccess) return DPRC_ERR_CUDA;
+  mark(1, s);
+  e = launch_simt_colproj(A, dtype, B, T, d, W, ik, Y, s);
+  if (e != cudaSuccess) return DPRC_ERR_CUDA;
+  e = launch_simt_norm_finish(Y, B, d, ik, ik, 1.0f, n, accumulate, s);
+  mark(2, s);
+  return cuda_status(e);
+}
+
+dprc_status dprc_norm_hutchpp(const void* A, const void* G, const void* S, const void* P,
+                              dprc_dtype dtype, int64_t B, int64_t T, int64_t d, int64_t p,
+                              int64_t r, float* n, int accumulate, void* ws, size_t ws_bytes,
+                              void* stream) {
+  if (!A || !G || !S || !P || !n) return DPRC_ERR_NULL;
+  dprc_status st = check_common(dtype, B, T, d, p);
+  if (st != DPRC_OK) return st;
+  if (r < 1 || r > 64 || r > p) return DPRC_ERR_SHAPE;
+  if (!aligned16(A) || !aligned16(G) || !aligned16(S) || !aligned16(P) || !aligned16(n))
+    return DPRC_ERR_ALIGN;
+  if (!ws) return DPRC_ERR_WORKSPACE;
+  if (!aligned16(ws)) return DPRC_ERR_ALIGN;
+  if (!device_ok()) return DPRC_ERR_DEVICE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char* w = static_cast<char*>(ws);
+  const int ir = static_cast<int>(r);
+  if (tc_path_supported(dtype, d, p, r, true)) {
+    const TcPlan t = plan_tc(DPRC_OP_HUTCHPP, B, T, d, p, r);
+    if (ws_bytes < t.total) return DPRC_ERR_WORKSPACE;
+    const int sms = device_sm_count();
+    const Ctrl c = ctrl_layout(B, std::max(t.cp.nchunks, static_cast<int>((p + 255) / 256)));
+    int* zp = reinterpret_cast<int*>(w);
+    void* W = w + t.w_off;
+    void* Z = w + t.z_off;
+    float* M = reinterpret_cast<float*>(w + t.m_off);
+    void* QP = w + t.qp_off;
+    ColprojPlan cp1 = colproj_geom(B, T, d, ir, sms);
+    ColprojPlan cp2 = colproj_geom(B, T, p, ir, sms);
+    ColprojPlan cp3 = colproj_geom(B, T, d, 2 * ir, sms);
+    for (ColprojPlan* cp : {&cp1, &cp2, &cp3}) {
+      attach_ctrl(*cp, c);
+      cp->part_off = t.cp.part_off;
+    }
+    const bool pdl = t_events == nullptr;
+    mark(0, s);
+    // pass 1: Z = A^T (G S)
+    cudaError_t e = launch_tc_rowproj(G, B, T, p, S, false, ir, false, W, t.tpad, zp, c.zero_ints, s);
+    if (e == cudaSuccess)
+      e = launch_tc_colproj(A, B, T, d, W, t.tpad, ir, cp1, w, kColprojHilo, nullptr, 0, ir,
+                            1.0f, nullptr, Z, pdl, s);
+    mark(1, s);
+    // pass 2: M = G^T (A Z) = O S
+    if (e == cudaSuccess)
+      e = launch_tc_rowproj(A, B, T, d, Z, true, 2 * ir, true, W, t.tpad, zp, c.zero_ints, s);
+    if (e == cudaSuccess)
+      e = launch_tc_colproj(G, B, T, p, W, t.tpad, ir, cp2, w, kColprojF32, nullptr, 0, ir, 1.0f,
+                            M, nullptr, pdl, s);
+    mark(2, s);
+    // Q = qr(M), P' = P - Q Q^T P
+    if (e == cudaSuccess)
+      e = launch_qr_project(M, B, p, ir, P, dtype,
+                            reinterpret_cast<float*>(w + t.qscratch_off), QP, true, s);
+    mark(3, s);
+    // pass 3: Y = A^T G [Q | P'], n = ||Y_head||^2 + ||Y_tail||^2 / r
+    if (e == cudaSuccess)
+      e = launch_tc_rowproj(G, B, T, p, QP, true, 4 * ir, true, W, t.tpad, zp, c.zero_ints, s);
+    if (e == cudaSuccess)
+      e = launch_tc_colproj(A, B, T, d, W, t.tpad, 2 * ir, cp3, w, kColprojNorm, n, accumulate,
+                            ir, 1.0f / static_cast<float>(r), nullptr, nullptr, pdl, s);
+    mark(4, s);
+    return cuda_status(e);
+  }
+  const SimtPlan sp = plan_simt(DPRC_OP_HUTCHPP, B, T, d, p, r);
+  if (ws_bytes < sp.total) return DPRC_ERR_WORKSPACE;
+  float* W = reinterpret_cast<float*>(w + sp.w_off);
+  float* Y = reinterpret_cast<float*>(w + sp.y_off);
+  float* Z = reinterpret_cast<float*>(w + sp.z_off);
+  float* M = reinterpret_cast<float*>(w + sp.m_off);
+  float* QP = reinterpret_cast<float*>(w + sp.qp_off);
+  mark(0, s);
+  cudaError_t e = launch_simt_rowproj(G, dtype, B, T, p, S, dtype, false, ir, W, s);
+  if (e == cudaSuccess) e = launch_simt_colproj(A, dtype, B, T, d, W, ir, Z, s);
+  mark(1, s);
+  if (e == cudaSuccess) e = launch_simt_rowproj(A, dtype, B, T, d, Z, DPRC_F32, true, ir, W, s);
+  if (e == cudaSuccess) e = launch_simt_colproj(G, dtype, B, T, p, W, ir, M, s);
+  mark(2, s);
+  if (e == cudaSuccess)
+    e = launch_qr_project(M, B, p, ir, P, dtype, reinterpret_cast<float*>(w + sp.qscratch_off),
+                          QP, false, s);
+  mark(3, s);
+  if (e == cudaSuccess)
+    e = launch_simt_rowproj(G, dtype, B, T, p, QP, DPRC_F32, true, 2 * ir, W, s);
+  if (e == cudaSuccess) e = launch_simt_colproj(A, dtype, B, T, d, W, 2 * ir, Y, s);
+  if (e == cudaSuccess)
+    e = launch_simt_norm_finish(Y, B, d, 2 * ir, ir, 1.0f / static_cast<float>(r), n, accumulate,
+                                s);
+  mark(4, s);
+  return cuda_status(e);
+}
+
+dprc_status dprc_exact_norm(const void* A, const void* G, dprc_dtype dtype, int64_t B, int64_t T,
+                            int64_t d, int64_t p, float* n, int accumulate, void* ws,
+                            size_t ws_bytes, void* stream) {
+  if (!A || !G || !n) return DPRC_ERR_NULL;
+  dprc_status st = check_common(dtype, B, T, d, p);
+  if (st != DPRC_OK) return st;
+  if (T > 65535 * 32) return DPRC_ERR_SHAPE;
+  if (!aligned16(A) || !aligned16(G) || !aligned16(n)) return DPRC_ERR_ALIGN;
+  if (!ws) return DPRC_ERR_WORKSPACE;
+  if (!aligned16(ws)) return DPRC_ERR_ALIGN;
+  if (ws_bytes < plan_exact_bytes(B, T)) return DPRC_ERR_WORKSPACE;
+  if (!device_ok()) return DPRC_ERR_DEVICE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  mark(0, s);
+  cudaError_t e = launch_exact_ghost(A, G, dtype, B, T, d, p, static_cast<float*>(ws), n,
+                                     accumulate, s);
+  mark(1, s);
+  return cuda_status(e);
+}
+
+dprc_status dprc_clip_factors(const float* n, int64_t B, float C, float* c, int32_t* nonfinite,
+                              void* stream) {
+  if (!n || !c) return DPRC_ERR_NULL;
+  if (B < 1 || B > (int64_t(1) << 31)) return DPRC_ERR_SHAPE;
+  if (!(C > 0.f) || !(C < __builtin_inff())) return DPRC_ERR_SHAPE;
+  if (!aligned16(n) || !aligned16(c)) return DPRC_ERR_ALIGN;
+  if (!device_ok()) return DPRC_ERR_DEVICE;
+  return cuda_status(launch_clip(n, B, C, c, nonfinite, static_cast<cudaStream_t>(stream)));
+}
+
+dprc_status dprc_add_noise(float* grad, int64_t N, float sigma, float C, uint64_t seed,
+                           uint64_t step, void* stream) {
+  if (N < 0) return DPRC_ERR_SHAPE;
+  if (N > 0 && !grad) return DPRC_ERR_NULL;
+  if (!(sigma >= 0.f) || !(sigma < __builtin_inff()) || !(C >= 0.f) || !(C < __builtin_inff()))
+    return DPRC_ERR_SHAPE;
+  if (N > 0 && !aligned16(grad)) return DPRC_ERR_ALIGN;
+  if (N == 0) return DPRC_OK;
+  if (!device_ok()) return DPRC_ERR_DEVICE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  mark(0, s);
+  const cudaError_t e = launch_noise(grad, N, sigma, C, seed, step, s);
+  mark(1, s);
+  return cuda_status(e);
+}
+
+dprc_status dprc_philox_words(uint32_t* out, int64_t n_blocks, uint64_t first_block,
+                              uint64_t seed, uint64_t step, void* stream) {
+  if (n_blocks < 0) return DPRC_ERR_SHAPE;
+  if (n_blocks > 0 && !out) return DPRC_ERR_NULL;
+  if (n_blocks > 0 && !aligned16(out)) return DPRC_ERR_ALIGN;
+  if (n_blocks == 0) return DPRC_OK;
+  if (!device_ok()) return DPRC_ERR_DEVICE;
+  return cuda_status(launch_philox_words(out, n_blocks, first_block, seed, step,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
+dprc_status dprc_device_error(int32_t* out, int reset) {
+  if (!out) return DPRC_ERR_NULL;
+  if (!device_ok()) return DPRC_ERR_DEVICE;
+  return cuda_status(read_device_error(out, reset != 0));
+}
+
+}  // extern "C"

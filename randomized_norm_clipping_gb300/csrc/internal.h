@@ -1,0 +1,124 @@
+// Host-side declarations shared by the libdprc translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "dprc.h"
+
+namespace dprc {
+
+// ---- workspace plan ------------------------------------------------------
+// Offsets (bytes) of every scratch region one call uses.  Computed from the
+// sizes and the device's SM count; the same function sizes the workspace
+// (dprc_workspace_bytes) and carves it inside the call.
+struct ColprojPlan {
+  int grid = 0;          // persistent CTAs of the T-reduction kernel
+  int n = 0;             // output columns (half the MMA N: hi and lo planes)
+  int chunk = 256;       // output rows per work block
+  int nchunks = 0;       // ceil(c / chunk)
+  int kt = 0;            // ceil(T / 64): T tiles per block
+  int64_t units = 0;     // B * nchunks * kt
+  int max_seg = 0;       // blocks a CTA's unit range can touch
+  size_t part_off = 0, part_bytes = 0;    // [grid][max_seg][chunk][n] fp32
+  size_t tick_off = 0, tick_count = 0;    // [B * nchunks] int32
+  size_t stick_off = 0;                   // [B] int32
+  size_t cnorm_off = 0;                   // [B * nchunks] fp32
+};
+
+// Scratch layout of the tensor-core path of one Hutchinson or Hutch++ call.
+struct TcPlan {
+  int64_t B = 0, T = 0, d = 0, p = 0, k = 0;
+  int64_t tpad = 0;           // row stride (elements) of the [B][2n][tpad] sketches
+  size_t w_off = 0;           // sketch G P (or G S, A Z, G [Q|P']) hi/lo bf16
+  size_t w_bytes = 0;
+  size_t z_off = 0;           // Hutch++: Z hi/lo bf16 [B][d][2r]
+  size_t m_off = 0;           // Hutch++: M = O S fp32 [B][p][r]
+  size_t qp_off = 0;          // Hutch++: [Q | P'] hi/lo bf16 [B][p][4r]
+  size_t qscratch_off = 0;    // Hutch++: QR work space fp32 [B][p][r] + [B][p][r]
+  ColprojPlan cp;             // shared by every column-projection launch
+  size_t zero_ints = 0;       // int32 words of the control block to clear per call
+  size_t total = 0;
+};
+
+// Scratch layout of the SIMT (CUDA-core, fp32) path.
+struct SimtPlan {
+  size_t w_off = 0;   // [B][T][n] fp32 sketch
+  size_t y_off = 0;   // [B][c][n] fp32 projection
+  size_t z_off = 0;   // Hutch++ Z / M / [Q|P'] buffers
+  size_t m_off = 0;
+  size_t qp_off = 0;
+  size_t qscratch_off = 0;
+  size_t total = 0;
+};
+
+int device_sm_count();
+int colproj_stage_chunk();
+cudaError_t read_device_error(int32_t* out, bool reset);
+bool tc_path_supported(dprc_dtype dt, int64_t d, int64_t p, int64_t k, bool hutchpp);
+
+TcPlan plan_tc(dprc_op op, int64_t B, int64_t T, int64_t d, int64_t p, int64_t k);
+SimtPlan plan_simt(dprc_op op, int64_t B, int64_t T, int64_t d, int64_t p, int64_t k);
+size_t plan_exact_bytes(int64_t B, int64_t T);
+
+// ---- tensor maps -----------------------------------------------------------
+// 3-D bf16 tensor map over [dim2][dim1][dim0] (dim0 contiguous) with row
+// strides in elements, a box of (box0, box1, 1) and the given swizzle bytes
+// (0, 32, 64 or 128).
+bool make_tmap_3d_bf16(CUtensorMap* map, const void* base, uint64_t dim0, uint64_t dim1,
+                       uint64_t dim2, uint64_t stride1_elems, uint64_t stride2_elems,
+                       uint32_t box0, uint32_t box1, int swizzle_bytes);
+
+// ---- launchers (return cudaSuccess or the launch error) --------------------
+// Row projection on tensor cores: W[i] = X[i] R[i] with X [B][T][c] bf16 and
+// R [Rb][c][nmma] bf16 (Rb = 1: shared by the batch).  With hilo_in the two
+// column halves of R are the hi and lo parts of one fp32 matrix and are
+// summed.  W is written as bf16 hi/lo planes [B][2n][tpad].  CTA 0 also
+// clears `zero_ints` int32 words at `zero_ptr` (the next kernel's tickets).
+cudaError_t launch_tc_rowproj(const void* X, int64_t B, int64_t T, int64_t c, const void* R,
+                              bool r_batched, int nmma, bool hilo_in, void* W, int64_t tpad,
+                              int* zero_ptr, size_t zero_ints, cudaStream_t s);
+
+enum ColprojMode { kColprojNorm = 0, kColprojF32 = 1, kColprojHilo = 2 };
+
+// Column projection on tensor cores, reduced over T: Y[i] = X[i]^T W[i] with
+// X [B][T][c] bf16 and W the hi/lo sketch [B][2n][tpad].  Mode kColprojNorm
+// adds sum_j w_j ||Y[:, j]||^2 (w_j = 1 for j < n_head, w_tail otherwise) into
+// n_out; kColprojF32 writes Y [B][c][n]; kColprojHilo writes Y as bf16 hi/lo
+// [B][c][2n].
+cudaError_t launch_tc_colproj(const void* X, int64_t B, int64_t T, int64_t c, const void* W,
+                              int64_t tpad, int n, const ColprojPlan& plan, char* ws,
+                              ColprojMode mode, float* n_out, int accumulate, int n_head,
+                              float w_tail, float* y_f32, void* y_hilo, bool pdl,
+                              cudaStream_t s);
+
+// SIMT (fp32 CUDA-core) building blocks; Xdt is the dtype of X, Rdt of R.
+cudaError_t launch_simt_rowproj(const void* X, dprc_dtype xdt, int64_t B, int64_t T, int64_t c,
+                                const void* R, dprc_dtype rdt, bool r_batched, int n, float* W,
+                                cudaStream_t s);
+cudaError_t launch_simt_colproj(const void* X, dprc_dtype xdt, int64_t B, int64_t T, int64_t c,
+                                const float* W, int n, float* Y, cudaStream_t s);
+cudaError_t launch_simt_norm_finish(const float* Y, int64_t B, int64_t c, int n, int n_head,
+                                    float w_tail, float* n_out, int accumulate, cudaStream_t s);
+
+// Hutch++ middle step: per-sample Householder QR of M [B][p][r] (fp32),
+// then P' = P - Q (Q^T P); writes [Q | P'] either as bf16 hi/lo [B][p][4r]
+// (hilo = true) or fp32 [B][p][2r].  scratch: fp32 [B][p][r] * 2.
+cudaError_t launch_qr_project(const float* M, int64_t B, int64_t p, int r, const void* P,
+                              dprc_dtype pdt, float* scratch, void* out, bool hilo,
+                              cudaStream_t s);
+
+// Exact (ghost) norm, SIMT fp32, deterministic.
+cudaError_t launch_exact_ghost(const void* A, const void* G, dprc_dtype dt, int64_t B,
+                               int64_t T, int64_t d, int64_t p, float* partials, float* n_out,
+                               int accumulate, cudaStream_t s);
+
+cudaError_t launch_clip(const float* n, int64_t B, float C, float* c, int32_t* nonfinite,
+                        cudaStream_t s);
+cudaError_t launch_noise(float* grad, int64_t N, float sigma, float C, uint64_t seed,
+                         uint64_t step, cudaStream_t s);
+cudaError_t launch_philox_words(uint32_t* out, int64_t n_blocks, uint64_t first_block,
+                                uint64_t seed, uint64_t step, cudaStream_t s);
+
+}  // namespace dprc

@@ -1,0 +1,142 @@
+// Clip factors and the Gaussian noise add of DP-SGD-RC.
+//
+// Clip (papernotes.org, "Method > Overall framework"): each sample's loss is
+// rescaled by c_i = min(1, C / sqrt(n_i)), n_i the layerwise sum of the
+// squared-norm estimates.
+//
+// Noise (same section; the aggregated gradient receives sigma*C*N(0, I)):
+// normals come from the counter-based Philox4x32-10 generator of Salmon,
+// Moraes, Dror and Shaw, "Parallel Random Numbers: As Easy as 1, 2, 3"
+// (SC'11), implemented here from that paper's definition, followed by the
+// Box-Muller transform.  Stream layout: element e uses word (e & 3) of block
+// e >> 2; block j = Philox(counter (j_lo, j_hi, step_lo, step_hi), key
+// (seed_lo, seed_hi)).  The kernel is HBM-bound: 8 bytes of traffic per
+// element (read + write of the fp32 gradient), read with 128-bit loads.
+
+#include "internal.h"
+
+namespace dprc {
+namespace {
+
+constexpr uint32_t kPhiloxM0 = 0xD2511F53u;
+constexpr uint32_t kPhiloxM1 = 0xCD9E8D57u;
+constexpr uint32_t kPhiloxW0 = 0x9E3779B9u;
+constexpr uint32_t kPhiloxW1 = 0xBB67AE85u;
+
+__device__ __forceinline__ uint4 philox4x32_10(uint4 x, uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int round = 0; round < 10; ++round) {
+    const uint32_t hi0 = __umulhi(kPhiloxM0, x.x), lo0 = kPhiloxM0 * x.x;
+    const uint32_t hi1 = __umulhi(kPhiloxM1, x.z), lo1 = kPhiloxM1 * x.z;
+    x = make_uint4(hi1 ^ x.y ^ k0, lo1, hi0 ^ x.w ^ k1, lo0);
+    k0 += kPhiloxW0;
+    k1 += kPhiloxW1;
+  }
+  return x;
+}
+
+__device__ __forceinline__ uint4 philox_block(uint64_t j, uint64_t seed, uint64_t step) {
+  return philox4x32_10(make_uint4(static_cast<uint32_t>(j), static_cast<uint32_t>(j >> 32),
+                                  static_cast<uint32_t>(step), static_cast<uint32_t>(step >> 32)),
+                       static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32));
+}
+
+// Box-Muller on a word pair: u1 = ((a >> 8) + 1) 2^-24 in (0, 1],
+// u2 = (b >> 8) 2^-24 in [0, 1); both exact in fp32.
+__device__ __forceinline__ float2 box_muller(uint32_t a, uint32_t b) {
+  const float u1 = static_cast<float>((a >> 8) + 1u) * 5.9604644775390625e-8f;  // 2^-24
+  const float u2 = static_cast<float>(b >> 8) * 5.9604644775390625e-8f;
+  const float rad = sqrtf(-2.0f * logf(u1));
+  float s, c;
+  sincospif(2.0f * u2, &s, &c);
+  return make_float2(rad * c, rad * s);
+}
+
+__global__ void __launch_bounds__(256) noise_kernel(float* __restrict__ grad, long long n,
+                                                    float scale, uint64_t seed, uint64_t step) {
+  const long long nblk = n >> 2;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  float4* g4 = reinterpret_cast<float4*>(grad);
+  for (long long j = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; j < nblk;
+       j += stride) {
+    const uint4 w = philox_block(static_cast<uint64_t>(j), seed, step);
+    const float2 z01 = box_muller(w.x, w.y);
+    const float2 z23 = box_muller(w.z, w.w);
+    float4 g = g4[j];
+    g.x = fmaf(scale, z01.x, g.x);
+    g.y = fmaf(scale, z01.y, g.y);
+    g.z = fmaf(scale, z23.x, g.z);
+    g.w = fmaf(scale, z23.y, g.w);
+    g4[j] = g;
+  }
+  // ragged tail: the last n & 3 elements, one thread
+  if (blockIdx.x == 0 && threadIdx.x == 0 && (n & 3) != 0) {
+    const uint4 w = philox_block(static_cast<uint64_t>(nblk), seed, step);
+    const float2 z01 = box_muller(w.x, w.y);
+    const float2 z23 = box_muller(w.z, w.w);
+    const float z[4] = {z01.x, z01.y, z23.x, z23.y};
+    for (long long e = nblk * 4; e < n; ++e) grad[e] = fmaf(scale, z[e - nblk * 4], grad[e]);
+  }
+}
+
+__global__ void __launch_bounds__(256) philox_words_kernel(uint4* __restrict__ out, long long n,
+                                                           uint64_t first, uint64_t seed,
+                                                           uint64_t step) {
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long j = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; j < n;
+       j += stride)
+    out[j] = philox_block(first + static_cast<uint64_t>(j), seed, step);
+}
+
+__global__ void clip_kernel(const float* __restrict__ n, long long B, float C,
+                            float* __restrict__ c, int32_t* __restrict__ nonfinite) {
+  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= B) return;
+  const float v = n[i];
+  float out;
+  if (!isfinite(v) || v < 0.f) {
+    out = 0.f;  // unknown norm: the sample contributes nothing
+    if (nonfinite != nullptr) atomicAdd(nonfinite, 1);
+  } else if (v == 0.f) {
+    out = 1.f;
+  } else {
+    out = fminf(1.f, C / sqrtf(v));
+  }
+  c[i] = out;
+}
+
+int grid_for(long long work, int threads) {
+  const int sms = device_sm_count();
+  long long blocks = (work + threads - 1) / threads;
+  const long long cap = static_cast<long long>(sms) * 8;  // 8 x 256 threads per SM
+  if (blocks > cap) blocks = cap;
+  if (blocks < 1) blocks = 1;
+  return static_cast<int>(blocks);
+}
+
+}  // namespace
+
+cudaError_t launch_noise(float* grad, int64_t N, float sigma, float C, uint64_t seed,
+                         uint64_t step, cudaStream_t s) {
+  if (N == 0) return cudaSuccess;
+  noise_kernel<<<grid_for(N / 4 + 1, 256), 256, 0, s>>>(grad, N, sigma * C, seed, step);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_philox_words(uint32_t* out, int64_t n_blocks, uint64_t first_block,
+                                uint64_t seed, uint64_t step, cudaStream_t s) {
+  if (n_blocks == 0) return cudaSuccess;
+  philox_words_kernel<<<grid_for(n_blocks, 256), 256, 0, s>>>(reinterpret_cast<uint4*>(out),
+                                                              n_blocks, first_block, seed, step);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_clip(const float* n, int64_t B, float C, float* c, int32_t* nonfinite,
+                        cudaStream_t s) {
+  const int threads = 128;
+  clip_kernel<<<static_cast<unsigned>((B + threads - 1) / threads), threads, 0, s>>>(n, B, C, c,
+                                                                                   nonfinite);
+  return cudaGetLastError();
+}
+
+}  // namespace dprc

@@ -1,0 +1,131 @@
+"""Host-side checks of the C ABI: the library builds, loads without a GPU, exports
+every symbol include/dprc.h declares, and rejects bad arguments before any
+device work.  No kernel runs here."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dprc.h")
+
+
+@pytest.fixture(scope="session")
+def lib():
+    from randomized_norm_clipping_gb300 import binding, build
+    if not os.path.exists(binding.LIB_PATH):
+        build.build()
+    return binding.lib()
+
+
+def _declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(dprc_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared()
+    for required in ("dprc_norm_hutch", "dprc_norm_hutchpp", "dprc_exact_norm",
+                     "dprc_clip_factors", "dprc_add_noise", "dprc_workspace_bytes"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+    from randomized_norm_clipping_gb300 import binding
+    assert set(binding.EXPORTED) == set(_declared())
+
+
+def test_abi_version_and_status_strings(lib):
+    assert lib.dprc_abi_version() == 1
+    for code in range(9):
+        s = lib.dprc_status_string(code)
+        assert isinstance(s, bytes) and len(s) > 0
+    assert lib.dprc_status_string(99) == b"unknown status"
+
+
+def test_workspace_bytes_host_only(lib):
+    from randomized_norm_clipping_gb300 import binding as b
+    # tensor-core path (bf16, k = 32): sketch hi/lo planes + partial slots
+    ws = b.dprc_workspace_bytes(b.DPRC_OP_HUTCH, b.DPRC_BF16, 8, 4096, 2048, 2048, 32)
+    assert ws >= 8 * 64 * 4096 * 2
+    assert ws < 64 << 20
+    # float32 path
+    ws32 = b.dprc_workspace_bytes(b.DPRC_OP_HUTCH, b.DPRC_F32, 4, 128, 64, 64, 8)
+    assert ws32 >= 4 * 128 * 8 * 4
+    assert b.dprc_workspace_bytes(b.DPRC_OP_HUTCHPP, b.DPRC_BF16, 8, 4096, 2048, 2048, 16) > 0
+    assert b.dprc_workspace_bytes(b.DPRC_OP_EXACT, b.DPRC_BF16, 2, 4096, 64, 64, 0) >= 2 * 128 * 128 * 4
+    # invalid sizes give 0
+    assert b.dprc_workspace_bytes(b.DPRC_OP_HUTCH, b.DPRC_BF16, 0, 4096, 2048, 2048, 32) == 0
+    assert b.dprc_workspace_bytes(b.DPRC_OP_HUTCH, b.DPRC_BF16, 1, 4096, 2048, 2048, 0) == 0
+    assert b.dprc_workspace_bytes(b.DPRC_OP_HUTCH, b.DPRC_BF16, 1, 4096, 2048, 2048, 257) == 0
+    assert b.dprc_workspace_bytes(b.DPRC_OP_HUTCHPP, b.DPRC_BF16, 1, 64, 64, 8, 16) == 0  # r > p
+    assert b.dprc_workspace_bytes(b.DPRC_OP_HUTCH, 7, 1, 64, 64, 64, 8) == 0
+    assert b.dprc_workspace_bytes(9, b.DPRC_BF16, 1, 64, 64, 64, 8) == 0
+
+
+def _vp(x):
+    return ctypes.c_void_p(x)
+
+
+A16 = 0x10000  # fake, aligned, never dereferenced: every call below fails its checks first
+
+
+def test_argument_errors_return_before_device_work(lib):
+    f = lib.dprc_norm_hutch
+    ws = 1 << 30
+    # null pointers
+    assert f(None, _vp(A16), _vp(A16), 1, 1, 1, 8, 8, 16, _vp(A16), 0, _vp(A16), ws, None) == 1
+    assert f(_vp(A16), _vp(A16), _vp(A16), 1, 1, 1, 8, 8, 16, None, 0, _vp(A16), ws, None) == 1
+    # bad dtype, bad shapes
+    assert f(_vp(A16), _vp(A16), _vp(A16), 5, 1, 1, 8, 8, 16, _vp(A16), 0, _vp(A16), ws, None) == 3
+    assert f(_vp(A16), _vp(A16), _vp(A16), 1, 0, 1, 8, 8, 16, _vp(A16), 0, _vp(A16), ws, None) == 2
+    assert f(_vp(A16), _vp(A16), _vp(A16), 1, 1, -3, 8, 8, 16, _vp(A16), 0, _vp(A16), ws, None) == 2
+    assert f(_vp(A16), _vp(A16), _vp(A16), 1, 1, 1, 8, 8, 0, _vp(A16), 0, _vp(A16), ws, None) == 2
+    assert f(_vp(A16), _vp(A16), _vp(A16), 1, 1, 1, 8, 8, 300, _vp(A16), 0, _vp(A16), ws, None) == 2
+    # misaligned pointer
+    assert f(_vp(A16 + 2), _vp(A16), _vp(A16), 1, 1, 1, 8, 8, 16, _vp(A16), 0, _vp(A16), ws, None) == 4
+    assert f(_vp(A16), _vp(A16), _vp(A16), 1, 1, 1, 8, 8, 16, _vp(A16), 0, _vp(A16 + 8), ws, None) == 4
+    # missing workspace
+    assert f(_vp(A16), _vp(A16), _vp(A16), 1, 1, 1, 8, 8, 16, _vp(A16), 0, None, ws, None) == 5
+    g = lib.dprc_norm_hutchpp
+    assert g(_vp(A16), _vp(A16), None, _vp(A16), 1, 1, 1, 8, 8, 4, _vp(A16), 0, _vp(A16), ws, None) == 1
+    assert g(_vp(A16), _vp(A16), _vp(A16), _vp(A16), 1, 1, 1, 8, 8, 16, _vp(A16), 0, _vp(A16), ws, None) == 2
+    e = lib.dprc_exact_norm
+    assert e(_vp(A16), None, 1, 1, 1, 8, 8, _vp(A16), 0, _vp(A16), ws, None) == 1
+    assert e(_vp(A16), _vp(A16), 1, 1, 1, 8, 8, _vp(A16), 0, _vp(A16), 0, None) == 5
+    c = lib.dprc_clip_factors
+    assert c(None, 4, ctypes.c_float(1.0), _vp(A16), None, None) == 1
+    assert c(_vp(A16), 4, ctypes.c_float(0.0), _vp(A16), None, None) == 2
+    assert c(_vp(A16), 4, ctypes.c_float(float("nan")), _vp(A16), None, None) == 2
+    assert c(_vp(A16), 0, ctypes.c_float(1.0), _vp(A16), None, None) == 2
+    n = lib.dprc_add_noise
+    assert n(None, 10, ctypes.c_float(1.0), ctypes.c_float(1.0), 1, 1, None) == 1
+    assert n(_vp(A16), -1, ctypes.c_float(1.0), ctypes.c_float(1.0), 1, 1, None) == 2
+    assert n(_vp(A16 + 4), 10, ctypes.c_float(1.0), ctypes.c_float(1.0), 1, 1, None) == 4
+    assert n(_vp(A16), 10, ctypes.c_float(-1.0), ctypes.c_float(1.0), 1, 1, None) == 2
+    assert n(None, 0, ctypes.c_float(1.0), ctypes.c_float(1.0), 1, 1, None) == 0  # empty: no-op
+    w = lib.dprc_philox_words
+    assert w(None, 4, 0, 1, 1, None) == 1
+    assert w(None, 0, 0, 1, 1, None) == 0
+
+
+def test_valid_calls_without_a_gpu_fail_loudly(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    st = lib.dprc_norm_hutch(_vp(A16), _vp(A16), _vp(A16), 1, 1, 1, 8, 8, 16, _vp(A16), 0,
+                             _vp(A16), 1 << 30, None)
+    assert st == 8  # DPRC_ERR_DEVICE: nothing was launched
+
+
+def test_binding_raises_when_library_missing(monkeypatch, tmp_path):
+    from randomized_norm_clipping_gb300 import binding
+    monkeypatch.setattr(binding, "_lib", None)
+    monkeypatch.setattr(binding, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        binding.lib()

@@ -1,0 +1,251 @@
+"""Parity of the CUDA path (through the C ABI) with the float64 oracle on the
+same seeded inputs.
+
+Tolerances: relative 1e-3 on every per-sample norm estimate and clip factor
+(bf16 inputs, fp32 accumulation); bit-exact Philox words; noise within
+sigma*C*2e-6*max(1,|z|) plus 4 ulp of the gradient (the kernel's logf,
+sqrtf and sincospif against float64).
+"""
+
+import hashlib
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import randomized_norm_clipping_gb300 as rnc
+from randomized_norm_clipping_gb300 import workloads as wl
+from randomized_norm_clipping_gb300.workloads import to_f64
+
+pytestmark = pytest.mark.gpu
+
+RTOL = 1e-3
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from randomized_norm_clipping_gb300 import binding, build
+    if not os.path.exists(binding.LIB_PATH):
+        build.build()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    rnc.dprc_device_error(reset=True)
+    yield
+    torch.cuda.synchronize()
+    assert rnc.dprc_device_error() == 0, "a bounded in-kernel wait ran out"
+
+
+def _rand(shape, seed, dtype, scale=1.0):
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    return (torch.randn(*shape, generator=g) * scale).to(dtype)
+
+
+def _relerr(got, ref):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    return np.max(np.abs(got - ref) / np.maximum(np.abs(ref), 1e-300))
+
+
+def _hutch_case(B, T, d, p, k, dtype, seed, gscale=1.0):
+    A = _rand((B, T, d), seed, dtype)
+    G = _rand((B, T, p), seed + 1, dtype, gscale)
+    P = _rand((p, k), seed + 2, dtype, 1.0 / np.sqrt(k))
+    return A, G, P
+
+
+# ------------------------------------------------------------------ Hutchinson
+
+HUTCH_SHAPES = [
+    # tensor-core path: bf16, k in {16, 32, 64}, widths multiples of 8
+    (2, 64, 256, 256, 32),
+    (3, 200, 320, 256, 32),        # ragged T (not a multiple of 64), d not a multiple of 256
+    (1, 1, 8, 8, 16),              # minimum sizes
+    (2, 1000, 520, 136, 16),
+    (4, 4097, 256, 512, 64),       # T one past a tile; k = 64
+    (1, 130, 1024, 2048, 32),
+    (5, 333, 264, 1032, 32),
+    # float32 / CUDA-core path through the same entry point
+    (4, 128, 64, 64, 8),
+]
+
+
+@pytest.mark.parametrize("B,T,d,p,k", HUTCH_SHAPES)
+def test_hutch_bf16_matches_oracle(B, T, d, p, k):
+    A, G, P = _hutch_case(B, T, d, p, k, torch.bfloat16, seed=B * 1000 + T)
+    n = torch.full((B,), -1.0, device=DEV)
+    rnc.dprc_norm_hutch(A.to(DEV), G.to(DEV), P.to(DEV), n)
+    ref = oracle.hutch_norm(to_f64(A), to_f64(G), to_f64(P))
+    assert _relerr(n.cpu(), ref) < RTOL
+
+
+@pytest.mark.parametrize("B,T,d,p,k", [(4, 128, 64, 64, 8), (2, 77, 30, 17, 5), (3, 64, 64, 64, 32)])
+def test_hutch_fp32_matches_oracle(B, T, d, p, k):
+    A, G, P = _hutch_case(B, T, d, p, k, torch.float32, seed=17 + T)
+    n = torch.zeros(B, device=DEV)
+    rnc.dprc_norm_hutch(A.to(DEV), G.to(DEV), P.to(DEV), n)
+    ref = oracle.hutch_norm(A.double().numpy(), G.double().numpy(), P.double().numpy())
+    assert _relerr(n.cpu(), ref) < 1e-5
+
+
+def test_hutch_bf16_odd_widths_use_cuda_cores():
+    # d, p not multiples of 8 and k = 24: served by the CUDA-core path
+    A, G, P = _hutch_case(2, 90, 37, 45, 24, torch.bfloat16, seed=5)
+    n = torch.zeros(2, device=DEV)
+    rnc.dprc_norm_hutch(A.to(DEV), G.to(DEV), P.to(DEV), n)
+    assert _relerr(n.cpu(), oracle.hutch_norm(to_f64(A), to_f64(G), to_f64(P))) < RTOL
+
+
+def test_hutch_accumulates_layerwise_sum():
+    layers = [_hutch_case(3, 150, d, p, 32, torch.bfloat16, seed=100 + j)
+              for j, (d, p) in enumerate([(256, 512), (512, 256), (128, 128)])]
+    n = torch.zeros(3, device=DEV)
+    for j, (A, G, P) in enumerate(layers):
+        rnc.dprc_norm_hutch(A.to(DEV), G.to(DEV), P.to(DEV), n, accumulate=j > 0)
+    ref = oracle.layer_sum([oracle.hutch_norm(to_f64(A), to_f64(G), to_f64(P))
+                            for A, G, P in layers])
+    assert _relerr(n.cpu(), ref) < RTOL
+
+
+def test_hutch_is_deterministic():
+    A, G, P = _hutch_case(4, 1500, 768, 512, 32, torch.bfloat16, seed=9)
+    A, G, P = A.to(DEV), G.to(DEV), P.to(DEV)
+    n1 = torch.zeros(4, device=DEV)
+    n2 = torch.zeros(4, device=DEV)
+    rnc.dprc_norm_hutch(A, G, P, n1)
+    rnc.dprc_norm_hutch(A, G, P, n2)
+    assert torch.equal(n1, n2)
+
+
+def test_hutch_identity_projection_gives_exact_norm():
+    # P = I_p (k = p = 32) turns the estimate into the exact norm
+    A, G, _ = _hutch_case(2, 300, 128, 32, 32, torch.bfloat16, seed=3)
+    P = torch.eye(32, dtype=torch.bfloat16)
+    n = torch.zeros(2, device=DEV)
+    rnc.dprc_norm_hutch(A.to(DEV), G.to(DEV), P.to(DEV), n)
+    assert _relerr(n.cpu(), oracle.exact_norm(to_f64(A), to_f64(G))) < RTOL
+
+
+# ------------------------------------------------------------------ Hutch++
+
+@pytest.mark.parametrize("B,T,d,p", [(2, 200, 256, 256), (3, 77, 136, 64), (2, 1100, 512, 1024)])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_hutchpp_matches_oracle(B, T, d, p, dtype):
+    r = 16
+    A = _rand((B, T, d), 40 + T, dtype)
+    g = torch.Generator(device="cpu").manual_seed(41 + T)
+    U, V = torch.randn(B, T, 8, generator=g), torch.randn(B, p, 8, generator=g)
+    G = (torch.bmm(U, V.transpose(1, 2)) / np.sqrt(8) + 0.05 * torch.randn(B, T, p, generator=g)).to(dtype)
+    S = _rand((p, r), 42, dtype)
+    P = _rand((p, r), 43, dtype)
+    n = torch.zeros(B, device=DEV)
+    rnc.dprc_norm_hutchpp(A.to(DEV), G.to(DEV), S.to(DEV), P.to(DEV), n)
+    ref = oracle.hutchpp_norm(to_f64(A), to_f64(G), to_f64(S), to_f64(P))
+    assert _relerr(n.cpu(), ref) < RTOL
+
+
+def test_hutchpp_exact_on_low_rank_gradients():
+    B, T, d, p, r = 2, 256, 256, 512, 16
+    A = _rand((B, T, d), 50, torch.bfloat16)
+    g = torch.Generator(device="cpu").manual_seed(51)
+    G = torch.bmm(torch.randn(B, T, 4, generator=g), torch.randn(B, 4, p, generator=g)).to(torch.bfloat16)
+    S, P = _rand((p, r), 52, torch.bfloat16), _rand((p, r), 53, torch.bfloat16)
+    n = torch.zeros(B, device=DEV)
+    rnc.dprc_norm_hutchpp(A.to(DEV), G.to(DEV), S.to(DEV), P.to(DEV), n)
+    assert _relerr(n.cpu(), oracle.exact_norm(to_f64(A), to_f64(G))) < RTOL
+
+
+# ------------------------------------------------------------------ exact norm
+
+@pytest.mark.parametrize("B,T,d,p,dtype", [(4, 128, 64, 64, torch.float32),
+                                           (2, 333, 96, 40, torch.bfloat16),
+                                           (1, 1, 8, 8, torch.bfloat16),
+                                           (2, 1024, 512, 256, torch.bfloat16)])
+def test_exact_norm_matches_oracle(B, T, d, p, dtype):
+    A = _rand((B, T, d), 60 + T, dtype)
+    G = _rand((B, T, p), 61 + T, dtype, 0.05)
+    n = torch.zeros(B, device=DEV)
+    rnc.dprc_exact_norm(A.to(DEV), G.to(DEV), n)
+    assert _relerr(n.cpu(), oracle.exact_norm(to_f64(A), to_f64(G))) < RTOL
+
+
+# ------------------------------------------------------------------ clip
+
+def test_clip_factors_match_oracle_including_edge_cases():
+    vals = np.array([4.0, 0.25, 1.0, 0.0, 100.0, 3.7e-30, 2.5e30, np.nan, np.inf, -1.0, -np.inf,
+                     1.0000001, 0.9999999], dtype=np.float32)
+    n = torch.from_numpy(vals).to(DEV)
+    c = torch.empty_like(n)
+    cnt = torch.zeros(1, dtype=torch.int32, device=DEV)
+    rnc.dprc_clip_factors(n, 1.0, c, cnt)
+    ref = oracle.clip_factors(vals.astype(np.float64), 1.0)
+    got = c.cpu().double().numpy()
+    np.testing.assert_allclose(got, ref, rtol=1e-6, atol=0)
+    assert int(cnt.item()) == 4
+    c2 = torch.empty_like(n)
+    rnc.dprc_clip_factors(n, 3.5, c2)
+    np.testing.assert_allclose(c2.cpu().double().numpy(), oracle.clip_factors(vals.astype(np.float64), 3.5),
+                               rtol=1e-6, atol=0)
+
+
+# ------------------------------------------------------------------ Philox and noise
+
+@pytest.mark.parametrize("first", [0, 12345, (1 << 32) - 7, (1 << 40) + 3])
+def test_philox_words_bit_exact(first):
+    seed, step = 0x0123456789ABCDEF, (5 << 32) | 77
+    out = torch.empty(4096, 4, dtype=torch.int32, device=DEV)
+    rnc.dprc_philox_words(out, first, seed, step)
+    got = out.cpu().numpy().view(np.uint32)
+    assert np.array_equal(got, oracle.philox_words(seed, step, first, 4096))
+
+
+def test_philox_long_stream_hash():
+    n = 1 << 22
+    out = torch.empty(n, 4, dtype=torch.int32, device=DEV)
+    rnc.dprc_philox_words(out, 0, 2024, 9)
+    got = out.cpu().numpy().view(np.uint32)
+    ref = oracle.philox_words(2024, 9, 0, n)
+    assert hashlib.sha256(got.tobytes()).hexdigest() == hashlib.sha256(ref.tobytes()).hexdigest()
+
+
+def _noise_tol(z, g, sigma, C):
+    return sigma * C * 2e-6 * np.maximum(1.0, np.abs(z)) + 4 * np.finfo(np.float32).eps * np.abs(g)
+
+
+@pytest.mark.parametrize("N", [1, 3, 4, 1001, 65536 + 3])
+def test_noise_matches_oracle(N):
+    grad = wl.gradient_buffer(N, seed=N)
+    out = grad.to(DEV)
+    sigma, C = 1.3, 0.7
+    rnc.dprc_add_noise(out, sigma, C, seed=99, step=4)
+    ref = oracle.add_noise(grad.double().numpy(), sigma, C, 99, 4)
+    z = oracle.noise_normals(N, 99, 4)
+    err = np.abs(out.cpu().double().numpy() - ref)
+    assert np.all(err <= _noise_tol(z, grad.double().numpy(), sigma, C))
+
+
+def test_noise_same_seed_step_reproduces_and_differs_otherwise():
+    a = torch.zeros(10000, device=DEV)
+    b = torch.zeros(10000, device=DEV)
+    c = torch.zeros(10000, device=DEV)
+    rnc.dprc_add_noise(a, 1.0, 1.0, seed=1, step=2)
+    rnc.dprc_add_noise(b, 1.0, 1.0, seed=1, step=2)
+    rnc.dprc_add_noise(c, 1.0, 1.0, seed=1, step=3)
+    assert torch.equal(a, b)
+    assert not torch.equal(a, c)
+
+
+@pytest.mark.slow
+def test_noise_full_gradient_buffer_sampled():
+    # the whole Llama-3.2-1B gradient (1.24e9 fp32), checked at sampled elements
+    N = wl.LLAMA32_1B_PARAMS
+    grad = torch.zeros(N, device=DEV)
+    rnc.dprc_add_noise(grad, 1.0, 1.0, seed=31337, step=1)
+    rng = np.random.default_rng(0)
+    idx = np.concatenate([rng.integers(0, N, 4000), np.arange(N - 7, N), np.arange(0, 8)])
+    got = grad[torch.from_numpy(idx).to(DEV)].cpu().double().numpy()
+    ref = np.array([oracle.noise_normals(1, 31337, 1, first_element=int(e))[0] for e in idx])
+    assert np.all(np.abs(got - ref) <= _noise_tol(ref, 0.0, 1.0, 1.0))
+    del grad
+    torch.cuda.empty_cache()
