@@ -61,7 +61,8 @@ typedef enum {
     DPRC_ERR_WORKSPACE = 5,   /* ws_bytes < dprc_workspace_bytes(...) or ws NULL */
     DPRC_ERR_CUDA = 6,        /* a CUDA runtime/driver call failed */
     DPRC_ERR_NONFINITE = 7,   /* reserved: reported through counters, not returns */
-    DPRC_ERR_DEVICE = 8       /* no usable sm_103 device for this call */
+    DPRC_ERR_DEVICE = 8,      /* no usable sm_103 device for this call */
+    DPRC_ERR_TOO_LARGE = 9    /* needs more scratch than the built-in buffer holds */
 } dprc_status;
 
 typedef enum { DPRC_F32 = 0, DPRC_BF16 = 1 } dprc_dtype;
@@ -188,6 +189,37 @@ dprc_status dprc_device_error(int32_t* out, int reset);
  * n_events = 0 turns it off.
  */
 dprc_status dprc_set_phase_events(void** events, int n_events);
+
+/*
+ * dprc_norm_hutch without a workspace argument, for callers that cannot
+ * allocate device memory where they need the norm: code inside a framework
+ * that owns the device allocator and forbids direct cudaMalloc, loops where a
+ * (possibly device-synchronizing) allocation is not acceptable, or hooks and
+ * plugins that are handed only input and output pointers.  The method's
+ * pages have no counterpart to this entry point.
+ *
+ * Scratch: a fixed array of DPRC_NOALLOC_SCRATCH_BYTES in the library's own
+ * device memory (a file-scope __device__ array), held on every GPU that loads
+ * the library until the process exits.  Calls whose dprc_workspace_bytes
+ * (DPRC_OP_HUTCH, ...) exceeds that size return DPRC_ERR_TOO_LARGE before
+ * any device work.  The call itself allocates nothing (no cudaMalloc,
+ * cudaFree or allocating library routine).
+ *
+ * Set-up: the first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current and caches it, so make the
+ * first call on a device before any stream capture.
+ *
+ * Sharing: every call on a device uses the same array, which keeps the last
+ * call's contents; the kernels clear the counters they need at the start of
+ * each call, so no stale state carries over.  Calls that can overlap on the
+ * GPU (different streams, or different host threads) race on the array: the
+ * caller must order them.  Arguments and results otherwise as dprc_norm_hutch.
+ */
+#define DPRC_NOALLOC_SCRATCH_BYTES (48u << 20)
+dprc_status dprc_norm_hutch_noalloc(const void* A, const void* G, const void* P,
+                                    dprc_dtype dtype, int64_t B, int64_t T, int64_t d,
+                                    int64_t p, int64_t k, float* n, int accumulate,
+                                    void* stream);
 
 #ifdef __cplusplus
 }

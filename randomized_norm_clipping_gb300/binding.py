@@ -21,7 +21,7 @@ LIB_PATH = os.path.join(PKG_DIR, "libdprc.so")
 DPRC_F32, DPRC_BF16 = 0, 1
 DPRC_OP_HUTCH, DPRC_OP_HUTCHPP, DPRC_OP_EXACT = 1, 2, 3
 STATUS = {0: "ok", 1: "null pointer", 2: "shape", 3: "dtype", 4: "alignment",
-          5: "workspace", 6: "cuda", 7: "non-finite", 8: "device"}
+          5: "workspace", 6: "cuda", 7: "non-finite", 8: "device", 9: "too large"}
 
 # The C prototypes of include/dprc.h, as (name, restype, argtypes).
 _c = ctypes
@@ -48,6 +48,9 @@ _PROTOS = [
      [_c.c_void_p, _c.c_int64, _c.c_uint64, _c.c_uint64, _c.c_uint64, _c.c_void_p]),
     ("dprc_device_error", _c.c_int, [_c.c_void_p, _c.c_int]),
     ("dprc_set_phase_events", _c.c_int, [_c.c_void_p, _c.c_int]),
+    ("dprc_norm_hutch_noalloc", _c.c_int,
+     [_c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_int, _c.c_int64, _c.c_int64, _c.c_int64,
+      _c.c_int64, _c.c_int64, _c.c_void_p, _c.c_int, _c.c_void_p]),
 ]
 EXPORTED = tuple(name for name, _, _ in _PROTOS)
 
@@ -152,6 +155,18 @@ def dprc_norm_hutchpp(A, G, S, P, n, accumulate=False, ws=None, stream=None):
                                  r, _ptr(n), int(bool(accumulate)), _ptr(ws), ws.numel(),
                                  _stream(A, stream))
     _check("dprc_norm_hutchpp", st)
+    return n
+
+
+def dprc_norm_hutch_noalloc(A, G, P, n, accumulate=False, stream=None):
+    """dprc_norm_hutch with the library's built-in scratch instead of a workspace,
+    for callers that cannot allocate device memory (see include/dprc.h)."""
+    _need_cuda(A, G, P, n)
+    B, T, d = A.shape
+    p, k = P.shape
+    st = lib().dprc_norm_hutch_noalloc(_ptr(A), _ptr(G), _ptr(P), _dtype_code(A), B, T, d, p, k,
+                                       _ptr(n), int(bool(accumulate)), _stream(A, stream))
+    _check("dprc_norm_hutch_noalloc", st)
     return n
 
 

@@ -260,6 +260,7 @@ const char* dprc_status_string(dprc_status s) {
     case DPRC_ERR_CUDA: return "CUDA call failed";
     case DPRC_ERR_NONFINITE: return "non-finite value";
     case DPRC_ERR_DEVICE: return "current device is not an sm_103 GPU";
+    case DPRC_ERR_TOO_LARGE: return "call needs more scratch than the built-in buffer";
   }
   return "unknown status";
 }
