@@ -179,7 +179,7 @@ def cpu_oracle_rate(A, G, P, C, budget_s=12.0):
         oracle.clip_factors(n, C)
         done += 1
         el = time.perf_counter() - t0
-        if el >= budget_s or done >= 64:
+        if el >= budget_s or done >= 20000:
             break
     return done * T / el, done, el
 
@@ -208,19 +208,37 @@ def run_native(args, rank, ws, local):
         step()
     torch.cuda.synchronize(device)
 
+    # Eager rate: one Python call per kernel launch (host overhead included).
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize(device)
+    eager_ms = ev0.elapsed_time(ev1) / args.steps
+
+    # The step captured once as a CUDA graph and replayed: the GPU runs the
+    # kernels back to back; this is the timed region.
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize(device)
+
     # keep the GPU loaded ~1.5 s so the clock samples cover a steady state
     with ClockSampler(local) as clk:
         t_soak = time.perf_counter()
         while time.perf_counter() - t_soak < 1.5:
-            for _ in range(200):
-                step()
+            for _ in range(500):
+                graph.replay()
             torch.cuda.synchronize(device)
         barrier(ws)
         torch.cuda.synchronize(device)
-        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda._sleep(2_000_000)  # queue the replays behind ~1 ms of GPU work
         ev0.record(stream)
         for _ in range(args.steps):
-            step()
+            graph.replay()
         ev1.record(stream)
         torch.cuda.synchronize(device)
         barrier(ws)
@@ -229,21 +247,27 @@ def run_native(args, rank, ws, local):
     ms_per_step = ms / args.steps
     value = ws * B * T / (ms_per_step * 1e-3)
 
-    # per-kernel durations (events between the two kernels of each call)
-    evs = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
-    k1_ms, k2_ms, call_ms = [], [], []
-    rnc.dprc_set_phase_events(evs)
+    # Per-kernel durations: events between the two kernels of each call, with
+    # the calls queued behind a GPU sleep so host launch gaps are not counted.
+    reps = 20
+    sets = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(reps)]
+    for evs in sets:
+        for e in evs:
+            e.record(stream)
+    torch.cuda.synchronize(device)
+    torch.cuda._sleep(20_000_000)
     try:
-        for _ in range(max(10, min(args.steps, 200))):
+        for evs in sets:
+            rnc.dprc_set_phase_events(evs)
             rnc.dprc_norm_hutch(A, G, P, n, accumulate=False, ws=wsbuf)
-            torch.cuda.synchronize(device)
-            k1_ms.append(evs[0].elapsed_time(evs[1]))
-            k2_ms.append(evs[1].elapsed_time(evs[2]))
     finally:
         rnc.dprc_set_phase_events(None)
-    # whole call without the events (programmatic dependent launch active)
+    torch.cuda.synchronize(device)
+    k1_ms = [evs[0].elapsed_time(evs[1]) for evs in sets]
+    k2_ms = [evs[1].elapsed_time(evs[2]) for evs in sets]
+    # whole call (both kernels, dependent launch active), queued the same way
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    reps = max(10, min(args.steps, 200))
+    torch.cuda._sleep(20_000_000)
     e0.record(stream)
     for _ in range(reps):
         rnc.dprc_norm_hutch(A, G, P, n, accumulate=False, ws=wsbuf)
@@ -313,6 +337,8 @@ def run_native(args, rank, ws, local):
             "global_batch": ws * B, "seq_len": T, "d": d, "p": p, "k": k,
             "parallelism": f"replicas x{ws} (samples sharded, no collective)",
             "l2": "inputs (268 MB per rank) larger than the 126 MB L2; no flush",
+            "timed": "step captured as a CUDA graph, K replays queued back to back",
+            "eager_ms_per_step": eager_ms,
         },
         "roofline": {
             "bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,

@@ -23,7 +23,7 @@
  *    managed memory) that stays valid until the enqueued work completes.  The
  *    library never allocates or frees memory.  Scratch memory is passed in as
  *    `ws` (see dprc_workspace_bytes); its contents need no initialisation and
- *    are garbage after a call.
+ *    are garbage after a call (each call clears the counters it uses).
  *  - `stream` is a cudaStream_t passed as void*; NULL means the legacy default
  *    stream.  Calls only enqueue work and return; results are ready when the
  *    stream reaches them.  Calls on different streams may run concurrently
@@ -51,6 +51,7 @@ extern "C" {
 #endif
 
 #define DPRC_ABI_VERSION 1
+
 
 typedef enum {
     DPRC_OK = 0,
@@ -175,6 +176,7 @@ dprc_status dprc_philox_words(uint32_t* out, int64_t n_blocks, uint64_t first_bl
 #define DPRC_DEVERR_PIPE_FULL 1   /* consumer waited too long for a tile */
 #define DPRC_DEVERR_PIPE_EMPTY 2  /* producer waited too long for a free stage */
 #define DPRC_DEVERR_ACCUM 3       /* epilogue waited too long for the accumulator */
+#define DPRC_DEVERR_CLUSTER 4     /* a CTA waited too long for its cluster peers' partials */
 dprc_status dprc_device_error(int32_t* out, int reset);
 
 /*
@@ -210,8 +212,9 @@ dprc_status dprc_set_phase_events(void** events, int n_events);
  * first call on a device before any stream capture.
  *
  * Sharing: every call on a device uses the same array, which keeps the last
- * call's contents; the kernels clear the counters they need at the start of
- * each call, so no stale state carries over.  Calls that can overlap on the
+ * call's contents; nothing in it needs to start at zero (the kernels clear the
+ * counters they use at the start of each call), so no stale state carries
+ * over.  Calls that can overlap on the
  * GPU (different streams, or different host threads) race on the array: the
  * caller must order them.  Arguments and results otherwise as dprc_norm_hutch.
  */

@@ -91,9 +91,14 @@ def _dtype_code(t):
     raise TypeError(f"unsupported dtype {t.dtype}")
 
 
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
 def _stream(t, stream):
     if stream is not None:
         return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else stream)
+    if _raw_stream is not None:  # the current stream's handle without a Stream object
+        return ctypes.c_void_p(_raw_stream(t.device.index))
     return ctypes.c_void_p(torch.cuda.current_stream(t.device).cuda_stream)
 
 
@@ -123,11 +128,12 @@ def dprc_workspace_bytes(op, dtype_code, B, T, d, p, k):
 
 
 def workspace(op, like, B, T, d, p, k):
-    """A device byte buffer of dprc_workspace_bytes(...) (torch allocation)."""
+    """A zeroed device byte buffer of dprc_workspace_bytes(...) (torch
+    allocation); its leading counter block must start at zero."""
     n = dprc_workspace_bytes(op, _dtype_code(like), B, T, d, p, k)
     if n == 0:
         raise DprcError("dprc_workspace_bytes", 2)
-    return torch.empty(n, dtype=torch.uint8, device=like.device)
+    return torch.zeros(n, dtype=torch.uint8, device=like.device)
 
 
 def dprc_norm_hutch(A, G, P, n, accumulate=False, ws=None, stream=None):

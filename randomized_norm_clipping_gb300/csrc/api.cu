@@ -12,6 +12,7 @@
 #include <stdint.h>
 
 #include <algorithm>
+#include <atomic>
 
 #include "dprc.h"
 #include "internal.h"
@@ -39,53 +40,26 @@ void mark(int idx, cudaStream_t s) {
     cudaEventRecord(static_cast<cudaEvent_t>(t_events[idx]), s);
 }
 
+constexpr int kMaxDev = 64;
+std::atomic<int> g_dev_state[kMaxDev];  // 0 unknown, 1 sm_103, 2 other
+std::atomic<int> g_dev_sms[kMaxDev];
+
+// True if the current device is an sm_103 GPU (checked once per device).
 bool device_ok() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  if (dev >= 0 && dev < kMaxDev) {
+    const int st = g_dev_state[dev].load(std::memory_order_acquire);
+    if (st != 0) return st == 1;
+  }
   int major = 0, minor = 0;
   if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess)
     return false;
   if (cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
     return false;
-  return major == 10 && minor == 3;
-}
-
-ColprojPlan colproj_geom(int64_t B, int64_t T, int64_t c, int n, int sms) {
-  ColprojPlan p;
-  p.n = n;
-  p.chunk = colproj_stage_chunk();
-  p.nchunks = static_cast<int>((c + p.chunk - 1) / p.chunk);
-  p.kt = static_cast<int>((T + 63) / 64);
-  p.units = B * p.nchunks * p.kt;
-  p.grid = static_cast<int>(std::min<int64_t>(p.units, sms));
-  const int64_t L = (p.units + p.grid - 1) / p.grid;
-  p.max_seg = static_cast<int>((L + p.kt - 1) / p.kt + 1);
-  p.part_bytes = static_cast<size_t>(p.grid) * p.max_seg * p.chunk * n * sizeof(float);
-  p.tick_count = static_cast<size_t>(B) * p.nchunks;
-  return p;
-}
-
-// Control block at the start of every tensor-core workspace:
-//   int32 tickets [B * max_chunks], int32 sample tickets [B],
-//   fp32 chunk norms [B * max_chunks].
-struct Ctrl {
-  size_t tick_off, stick_off, cnorm_off, end, zero_ints;
-};
-
-Ctrl ctrl_layout(int64_t B, int max_chunks) {
-  Ctrl c;
-  c.tick_off = 0;
-  c.stick_off = align_up(static_cast<size_t>(B) * max_chunks * 4, 256);
-  c.cnorm_off = align_up(c.stick_off + static_cast<size_t>(B) * 4, 256);
-  c.end = align_up(c.cnorm_off + static_cast<size_t>(B) * max_chunks * 4, 1024);
-  c.zero_ints = c.cnorm_off / 4;
-  return c;
-}
-
-void attach_ctrl(ColprojPlan& p, const Ctrl& c) {
-  p.tick_off = c.tick_off;
-  p.stick_off = c.stick_off;
-  p.cnorm_off = c.cnorm_off;
+  const bool ok = major == 10 && minor == 3;
+  if (dev >= 0 && dev < kMaxDev) g_dev_state[dev].store(ok ? 1 : 2, std::memory_order_release);
+  return ok;
 }
 
 int64_t tpad_of(int64_t T) { return (T + 63) / 64 * 64; }
@@ -95,13 +69,52 @@ int64_t tpad_of(int64_t T) { return (T + 63) / 64 * 64; }
 int device_sm_count() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return kDefaultSms;
+  if (dev >= 0 && dev < kMaxDev) {
+    const int c = g_dev_sms[dev].load(std::memory_order_acquire);
+    if (c > 0) return c;
+  }
   int n = 0;
   if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
     return kDefaultSms;
+  if (dev >= 0 && dev < kMaxDev) g_dev_sms[dev].store(n, std::memory_order_release);
   return n;
 }
 
-bool tc_path_supported(dprc_dtype dt, int64_t d, int64_t p, int64_t k, bool hutchpp) {
+BlockSched make_block_sched(int64_t nblocks, int upb, int slots) {
+  BlockSched s;
+  s.nblocks = nblocks;
+  s.upb = upb;
+  if (nblocks * 4 >= static_cast<int64_t>(slots) * 3) {
+    // enough blocks to fill the GPU: whole blocks, as evenly as possible
+    s.cl = 1;
+    s.bpc = static_cast<int>((nblocks + slots - 1) / slots);
+    s.grid = static_cast<int>((nblocks + s.bpc - 1) / s.bpc);
+  } else {
+    // few blocks: split each across a cluster (power of two up to 8)
+    s.cl = 1;
+    while (s.cl < 8 && nblocks * s.cl * 2 <= slots && s.cl * 2 <= upb) s.cl *= 2;
+    s.bpc = 1;
+    s.grid = static_cast<int>(nblocks * s.cl);
+  }
+  return s;
+}
+
+BlockSched rowproj_sched(int64_t B, int64_t T, int64_t c, int nmma) {
+  (void)nmma;
+  return make_block_sched(B * ((T + 127) / 128), static_cast<int>((c + 63) / 64),
+                          device_sm_count() * rowproj_ctas_per_sm());
+}
+
+BlockSched colproj_sched(int64_t B, int64_t T, int64_t c, int nmma) {
+  const int64_t nch = (c + colproj_stage_chunk() - 1) / colproj_stage_chunk();
+  return make_block_sched(B * nch, static_cast<int>((T + colproj_tile_t() - 1) / colproj_tile_t()),
+                          device_sm_count() * colproj_ctas_per_sm(nmma));
+}
+
+bool tc_path_supported(dprc_dtype dt, int64_t B, int64_t T, int64_t d, int64_t p, int64_t k,
+                       bool hutchpp) {
+  (void)B;
+  (void)T;
   if (dt != DPRC_BF16) return false;
   if (d % 8 != 0 || p % 8 != 0) return false;  // TMA row strides: multiples of 16 bytes
   if (hutchpp) return k == 16 && p >= k;
@@ -110,31 +123,14 @@ bool tc_path_supported(dprc_dtype dt, int64_t d, int64_t p, int64_t k, bool hutc
 
 TcPlan plan_tc(dprc_op op, int64_t B, int64_t T, int64_t d, int64_t p, int64_t k) {
   TcPlan t;
-  t.B = B;
-  t.T = T;
-  t.d = d;
-  t.p = p;
-  t.k = k;
   t.tpad = tpad_of(T);
-  const int sms = device_sm_count();
-  const int nch_d = static_cast<int>((d + colproj_stage_chunk() - 1) / colproj_stage_chunk());
-  const int nch_p = static_cast<int>((p + colproj_stage_chunk() - 1) / colproj_stage_chunk());
-  const Ctrl c = ctrl_layout(B, std::max(nch_d, nch_p));
-  t.zero_ints = c.zero_ints;
-  size_t off = c.end;
-  size_t part = 0;
-  if (op == DPRC_OP_HUTCH) {
-    t.cp = colproj_geom(B, T, d, static_cast<int>(k), sms);
-    part = t.cp.part_bytes;
-    t.w_bytes = static_cast<size_t>(B) * 2 * k * t.tpad * 2;
-  } else {
-    const int r = static_cast<int>(k);
-    t.cp = colproj_geom(B, T, d, 2 * r, sms);  // the widest of the three launches
-    part = std::max({colproj_geom(B, T, d, r, sms).part_bytes,
-                     colproj_geom(B, T, p, r, sms).part_bytes, t.cp.part_bytes});
-    t.w_bytes = static_cast<size_t>(B) * 4 * r * t.tpad * 2;
-  }
-  attach_ctrl(t.cp, c);
+  const int64_t nch = (std::max(d, p) + colproj_stage_chunk() - 1) / colproj_stage_chunk();
+  size_t off = 0;
+  t.stick_off = off;
+  off = align_up(off + static_cast<size_t>(B) * 4, 256);
+  t.cnorm_off = off;
+  off = align_up(off + static_cast<size_t>(B) * nch * 4, 1024);
+  t.w_bytes = static_cast<size_t>(B) * (op == DPRC_OP_HUTCH ? 2 * k : 4 * k) * t.tpad * 2;
   t.w_off = off;
   off = align_up(off + t.w_bytes, 1024);
   if (op == DPRC_OP_HUTCHPP) {
@@ -148,8 +144,6 @@ TcPlan plan_tc(dprc_op op, int64_t B, int64_t T, int64_t d, int64_t p, int64_t k
     t.qscratch_off = off;
     off = align_up(off + static_cast<size_t>(B) * p * r * 4 * 2, 1024);
   }
-  t.cp.part_off = off;
-  off = align_up(off + part, 1024);
   t.total = off;
   return t;
 }
@@ -234,12 +228,12 @@ dprc_status check_common(dprc_dtype dt, int64_t B, int64_t T, int64_t d, int64_t
 }
 
 size_t hutch_ws(dprc_dtype dt, int64_t B, int64_t T, int64_t d, int64_t p, int64_t k) {
-  return tc_path_supported(dt, d, p, k, false) ? plan_tc(DPRC_OP_HUTCH, B, T, d, p, k).total
+  return tc_path_supported(dt, B, T, d, p, k, false) ? plan_tc(DPRC_OP_HUTCH, B, T, d, p, k).total
                                                : plan_simt(DPRC_OP_HUTCH, B, T, d, p, k).total;
 }
 
 size_t hutchpp_ws(dprc_dtype dt, int64_t B, int64_t T, int64_t d, int64_t p, int64_t r) {
-  return tc_path_supported(dt, d, p, r, true) ? plan_tc(DPRC_OP_HUTCHPP, B, T, d, p, r).total
+  return tc_path_supported(dt, B, T, d, p, r, true) ? plan_tc(DPRC_OP_HUTCHPP, B, T, d, p, r).total
                                               : plan_simt(DPRC_OP_HUTCHPP, B, T, d, p, r).total;
 }
 
@@ -301,18 +295,20 @@ dprc_status dprc_norm_hutch(const void* A, const void* G, const void* P, dprc_dt
   if (!device_ok()) return DPRC_ERR_DEVICE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   char* w = static_cast<char*>(ws);
-  if (tc_path_supported(dtype, d, p, k, false)) {
+  if (tc_path_supported(dtype, B, T, d, p, k, false)) {
     const TcPlan t = plan_tc(DPRC_OP_HUTCH, B, T, d, p, k);
     if (ws_bytes < t.total) return DPRC_ERR_WORKSPACE;
+    const int ik = static_cast<int>(k);
+    int* stick = reinterpret_cast<int*>(w + t.stick_off);
+    float* cnorm = reinterpret_cast<float*>(w + t.cnorm_off);
     mark(0, s);
-    cudaError_t e = launch_tc_rowproj(G, B, T, p, P, false, static_cast<int>(k), false,
-                                      w + t.w_off, t.tpad, reinterpret_cast<int*>(w), t.zero_ints,
-                                      s);
+    cudaError_t e = launch_tc_rowproj(G, B, T, p, P, false, ik, false, w + t.w_off, t.tpad,
+                                      rowproj_sched(B, T, p, ik), stick, B, s);
     if (e != cudaSuccess) return DPRC_ERR_CUDA;
     mark(1, s);
-    e = launch_tc_colproj(A, B, T, d, w + t.w_off, t.tpad, static_cast<int>(k), t.cp, w,
-                          kColprojNorm, n, accumulate, static_cast<int>(k), 1.0f, nullptr,
-                          nullptr, t_events == nullptr, s);
+    e = launch_tc_colproj(A, B, T, d, w + t.w_off, t.tpad, ik, colproj_sched(B, T, d, 2 * ik),
+                          stick, cnorm, kColprojNorm, n, accumulate, ik, 1.0f, nullptr, nullptr,
+                          t_events == nullptr, s);
     mark(2, s);
     return cuda_status(e);
   }
@@ -348,37 +344,31 @@ dprc_status dprc_norm_hutchpp(const void* A, const void* G, const void* S, const
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   char* w = static_cast<char*>(ws);
   const int ir = static_cast<int>(r);
-  if (tc_path_supported(dtype, d, p, r, true)) {
+  if (tc_path_supported(dtype, B, T, d, p, r, true)) {
     const TcPlan t = plan_tc(DPRC_OP_HUTCHPP, B, T, d, p, r);
     if (ws_bytes < t.total) return DPRC_ERR_WORKSPACE;
-    const int sms = device_sm_count();
-    const Ctrl c = ctrl_layout(B, std::max(t.cp.nchunks, static_cast<int>((p + 255) / 256)));
-    int* zp = reinterpret_cast<int*>(w);
+    int* stick = reinterpret_cast<int*>(w + t.stick_off);
+    float* cnorm = reinterpret_cast<float*>(w + t.cnorm_off);
     void* W = w + t.w_off;
     void* Z = w + t.z_off;
     float* M = reinterpret_cast<float*>(w + t.m_off);
     void* QP = w + t.qp_off;
-    ColprojPlan cp1 = colproj_geom(B, T, d, ir, sms);
-    ColprojPlan cp2 = colproj_geom(B, T, p, ir, sms);
-    ColprojPlan cp3 = colproj_geom(B, T, d, 2 * ir, sms);
-    for (ColprojPlan* cp : {&cp1, &cp2, &cp3}) {
-      attach_ctrl(*cp, c);
-      cp->part_off = t.cp.part_off;
-    }
     const bool pdl = t_events == nullptr;
     mark(0, s);
     // pass 1: Z = A^T (G S)
-    cudaError_t e = launch_tc_rowproj(G, B, T, p, S, false, ir, false, W, t.tpad, zp, c.zero_ints, s);
+    cudaError_t e = launch_tc_rowproj(G, B, T, p, S, false, ir, false, W, t.tpad,
+                                      rowproj_sched(B, T, p, ir), stick, B, s);
     if (e == cudaSuccess)
-      e = launch_tc_colproj(A, B, T, d, W, t.tpad, ir, cp1, w, kColprojHilo, nullptr, 0, ir,
-                            1.0f, nullptr, Z, pdl, s);
+      e = launch_tc_colproj(A, B, T, d, W, t.tpad, ir, colproj_sched(B, T, d, 2 * ir), stick,
+                            cnorm, kColprojHilo, nullptr, 0, ir, 1.0f, nullptr, Z, pdl, s);
     mark(1, s);
     // pass 2: M = G^T (A Z) = O S
     if (e == cudaSuccess)
-      e = launch_tc_rowproj(A, B, T, d, Z, true, 2 * ir, true, W, t.tpad, zp, c.zero_ints, s);
+      e = launch_tc_rowproj(A, B, T, d, Z, true, 2 * ir, true, W, t.tpad,
+                            rowproj_sched(B, T, d, 2 * ir), stick, B, s);
     if (e == cudaSuccess)
-      e = launch_tc_colproj(G, B, T, p, W, t.tpad, ir, cp2, w, kColprojF32, nullptr, 0, ir, 1.0f,
-                            M, nullptr, pdl, s);
+      e = launch_tc_colproj(G, B, T, p, W, t.tpad, ir, colproj_sched(B, T, p, 2 * ir), stick,
+                            cnorm, kColprojF32, nullptr, 0, ir, 1.0f, M, nullptr, pdl, s);
     mark(2, s);
     // Q = qr(M), P' = P - Q Q^T P
     if (e == cudaSuccess)
@@ -387,10 +377,12 @@ dprc_status dprc_norm_hutchpp(const void* A, const void* G, const void* S, const
     mark(3, s);
     // pass 3: Y = A^T G [Q | P'], n = ||Y_head||^2 + ||Y_tail||^2 / r
     if (e == cudaSuccess)
-      e = launch_tc_rowproj(G, B, T, p, QP, true, 4 * ir, true, W, t.tpad, zp, c.zero_ints, s);
+      e = launch_tc_rowproj(G, B, T, p, QP, true, 4 * ir, true, W, t.tpad,
+                            rowproj_sched(B, T, p, 4 * ir), stick, B, s);
     if (e == cudaSuccess)
-      e = launch_tc_colproj(A, B, T, d, W, t.tpad, 2 * ir, cp3, w, kColprojNorm, n, accumulate,
-                            ir, 1.0f / static_cast<float>(r), nullptr, nullptr, pdl, s);
+      e = launch_tc_colproj(A, B, T, d, W, t.tpad, 2 * ir, colproj_sched(B, T, d, 4 * ir), stick,
+                            cnorm, kColprojNorm, n, accumulate, ir, 1.0f / static_cast<float>(r),
+                            nullptr, nullptr, pdl, s);
     mark(4, s);
     return cuda_status(e);
   }

@@ -9,36 +9,30 @@
 
 namespace dprc {
 
-// ---- workspace plan ------------------------------------------------------
-// Offsets (bytes) of every scratch region one call uses.  Computed from the
-// sizes and the device's SM count; the same function sizes the workspace
-// (dprc_workspace_bytes) and carves it inside the call.
-struct ColprojPlan {
-  int grid = 0;          // persistent CTAs of the T-reduction kernel
-  int n = 0;             // output columns (half the MMA N: hi and lo planes)
-  int chunk = 256;       // output rows per work block
-  int nchunks = 0;       // ceil(c / chunk)
-  int kt = 0;            // ceil(T / 64): T tiles per block
-  int64_t units = 0;     // B * nchunks * kt
-  int max_seg = 0;       // blocks a CTA's unit range can touch
-  size_t part_off = 0, part_bytes = 0;    // [grid][max_seg][chunk][n] fp32
-  size_t tick_off = 0, tick_count = 0;    // [B * nchunks] int32
-  size_t stick_off = 0;                   // [B] int32
-  size_t cnorm_off = 0;                   // [B * nchunks] fp32
+// ---- block schedules --------------------------------------------------------
+// How one tensor-core launch assigns its blocks (128 output rows, `upb` units
+// each) to CTAs: whole blocks, `bpc` per CTA (cl == 1), or one block per
+// cluster of `cl` CTAs that split its units and reduce through distributed
+// shared memory.
+struct BlockSched {
+  int cl = 1;
+  int bpc = 1;
+  int64_t nblocks = 0;
+  int upb = 0;
+  int grid = 0;
 };
+BlockSched make_block_sched(int64_t nblocks, int upb, int slots);
 
 // Scratch layout of the tensor-core path of one Hutchinson or Hutch++ call.
 struct TcPlan {
-  int64_t B = 0, T = 0, d = 0, p = 0, k = 0;
   int64_t tpad = 0;           // row stride (elements) of the [B][2n][tpad] sketches
-  size_t w_off = 0;           // sketch G P (or G S, A Z, G [Q|P']) hi/lo bf16
-  size_t w_bytes = 0;
+  size_t stick_off = 0;       // per-sample tickets int32 [B] (cleared by every sketch kernel)
+  size_t cnorm_off = 0;       // per-block squared norms fp32 [B * chunks]
+  size_t w_off = 0, w_bytes = 0;  // sketch G P (or G S, A Z, G [Q|P']) hi/lo bf16
   size_t z_off = 0;           // Hutch++: Z hi/lo bf16 [B][d][2r]
   size_t m_off = 0;           // Hutch++: M = O S fp32 [B][p][r]
   size_t qp_off = 0;          // Hutch++: [Q | P'] hi/lo bf16 [B][p][4r]
-  size_t qscratch_off = 0;    // Hutch++: QR work space fp32 [B][p][r] + [B][p][r]
-  ColprojPlan cp;             // shared by every column-projection launch
-  size_t zero_ints = 0;       // int32 words of the control block to clear per call
+  size_t qscratch_off = 0;    // Hutch++: QR work space fp32 [B][p][r] * 2
   size_t total = 0;
 };
 
@@ -54,9 +48,15 @@ struct SimtPlan {
 };
 
 int device_sm_count();
+int rowproj_ctas_per_sm();
+int colproj_ctas_per_sm(int nmma);
 int colproj_stage_chunk();
+int colproj_tile_t();
 cudaError_t read_device_error(int32_t* out, bool reset);
-bool tc_path_supported(dprc_dtype dt, int64_t d, int64_t p, int64_t k, bool hutchpp);
+bool tc_path_supported(dprc_dtype dt, int64_t B, int64_t T, int64_t d, int64_t p, int64_t k,
+                       bool hutchpp);
+BlockSched rowproj_sched(int64_t B, int64_t T, int64_t c, int nmma);
+BlockSched colproj_sched(int64_t B, int64_t T, int64_t c, int nmma);
 
 TcPlan plan_tc(dprc_op op, int64_t B, int64_t T, int64_t d, int64_t p, int64_t k);
 SimtPlan plan_simt(dprc_op op, int64_t B, int64_t T, int64_t d, int64_t p, int64_t k);
@@ -78,19 +78,21 @@ bool make_tmap_3d_bf16(CUtensorMap* map, const void* base, uint64_t dim0, uint64
 // clears `zero_ints` int32 words at `zero_ptr` (the next kernel's tickets).
 cudaError_t launch_tc_rowproj(const void* X, int64_t B, int64_t T, int64_t c, const void* R,
                               bool r_batched, int nmma, bool hilo_in, void* W, int64_t tpad,
-                              int* zero_ptr, size_t zero_ints, cudaStream_t s);
+                              const BlockSched& bs, int* zero_ptr, size_t zero_ints,
+                              cudaStream_t s);
 
 enum ColprojMode { kColprojNorm = 0, kColprojF32 = 1, kColprojHilo = 2 };
 
 // Column projection on tensor cores, reduced over T: Y[i] = X[i]^T W[i] with
 // X [B][T][c] bf16 and W the hi/lo sketch [B][2n][tpad].  Mode kColprojNorm
 // adds sum_j w_j ||Y[:, j]||^2 (w_j = 1 for j < n_head, w_tail otherwise) into
-// n_out; kColprojF32 writes Y [B][c][n]; kColprojHilo writes Y as bf16 hi/lo
-// [B][c][2n].
+// n_out (per-block squares in chunk_norms, combined in block order by the
+// last block of each sample, found with sample_tickets, which must be zero);
+// kColprojF32 writes Y [B][c][n]; kColprojHilo writes Y as bf16 hi/lo [B][c][2n].
 cudaError_t launch_tc_colproj(const void* X, int64_t B, int64_t T, int64_t c, const void* W,
-                              int64_t tpad, int n, const ColprojPlan& plan, char* ws,
-                              ColprojMode mode, float* n_out, int accumulate, int n_head,
-                              float w_tail, float* y_f32, void* y_hilo, bool pdl,
+                              int64_t tpad, int n, const BlockSched& bs, int* sample_tickets,
+                              float* chunk_norms, ColprojMode mode, float* n_out, int accumulate,
+                              int n_head, float w_tail, float* y_f32, void* y_hilo, bool pdl,
                               cudaStream_t s);
 
 // SIMT (fp32 CUDA-core) building blocks; Xdt is the dtype of X, Rdt of R.

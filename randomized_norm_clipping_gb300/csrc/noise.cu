@@ -23,22 +23,42 @@ constexpr uint32_t kPhiloxM1 = 0xCD9E8D57u;
 constexpr uint32_t kPhiloxW0 = 0x9E3779B9u;
 constexpr uint32_t kPhiloxW1 = 0xBB67AE85u;
 
-__device__ __forceinline__ uint4 philox4x32_10(uint4 x, uint32_t k0, uint32_t k1) {
+// Round keys of Philox4x32-10: the key bumped by (W0, W1) before each round.
+// They depend only on the seed, so a thread computes them once.
+struct RoundKeys {
+  uint32_t k0[10], k1[10];
+};
+
+__device__ __forceinline__ RoundKeys round_keys(uint64_t seed) {
+  RoundKeys rk;
+  uint32_t a = static_cast<uint32_t>(seed), b = static_cast<uint32_t>(seed >> 32);
 #pragma unroll
-  for (int round = 0; round < 10; ++round) {
-    const uint32_t hi0 = __umulhi(kPhiloxM0, x.x), lo0 = kPhiloxM0 * x.x;
-    const uint32_t hi1 = __umulhi(kPhiloxM1, x.z), lo1 = kPhiloxM1 * x.z;
-    x = make_uint4(hi1 ^ x.y ^ k0, lo1, hi0 ^ x.w ^ k1, lo0);
-    k0 += kPhiloxW0;
-    k1 += kPhiloxW1;
+  for (int r = 0; r < 10; ++r) {
+    rk.k0[r] = a;
+    rk.k1[r] = b;
+    a += kPhiloxW0;
+    b += kPhiloxW1;
+  }
+  return rk;
+}
+
+// Ten rounds on the counter x; each round's two 32x32 products are one wide
+// multiply each (high and low words).
+__device__ __forceinline__ uint4 philox4x32_10(uint4 x, const RoundKeys& rk) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    const unsigned long long p0 = static_cast<unsigned long long>(kPhiloxM0) * x.x;
+    const unsigned long long p1 = static_cast<unsigned long long>(kPhiloxM1) * x.z;
+    x = make_uint4(static_cast<uint32_t>(p1 >> 32) ^ x.y ^ rk.k0[r], static_cast<uint32_t>(p1),
+                   static_cast<uint32_t>(p0 >> 32) ^ x.w ^ rk.k1[r], static_cast<uint32_t>(p0));
   }
   return x;
 }
 
-__device__ __forceinline__ uint4 philox_block(uint64_t j, uint64_t seed, uint64_t step) {
+__device__ __forceinline__ uint4 philox_block(uint64_t j, uint64_t step, const RoundKeys& rk) {
   return philox4x32_10(make_uint4(static_cast<uint32_t>(j), static_cast<uint32_t>(j >> 32),
                                   static_cast<uint32_t>(step), static_cast<uint32_t>(step >> 32)),
-                       static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32));
+                       rk);
 }
 
 // Box-Muller on a word pair: u1 = ((a >> 8) + 1) 2^-24 in (0, 1],
@@ -52,26 +72,44 @@ __device__ __forceinline__ float2 box_muller(uint32_t a, uint32_t b) {
   return make_float2(rad * c, rad * s);
 }
 
+__device__ __forceinline__ float4 add_noise4(float4 g, uint4 w, float scale) {
+  const float2 z01 = box_muller(w.x, w.y);
+  const float2 z23 = box_muller(w.z, w.w);
+  g.x = fmaf(scale, z01.x, g.x);
+  g.y = fmaf(scale, z01.y, g.y);
+  g.z = fmaf(scale, z23.x, g.z);
+  g.w = fmaf(scale, z23.y, g.w);
+  return g;
+}
+
+// Each thread keeps kNoiseUnroll 16-byte loads in flight (issued before any
+// arithmetic) so the stream stays busy while the generator runs.
+constexpr int kNoiseUnroll = 4;
+
 __global__ void __launch_bounds__(256) noise_kernel(float* __restrict__ grad, long long n,
                                                     float scale, uint64_t seed, uint64_t step) {
+  const RoundKeys rk = round_keys(seed);
   const long long nblk = n >> 2;
-  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
   float4* g4 = reinterpret_cast<float4*>(grad);
-  for (long long j = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; j < nblk;
-       j += stride) {
-    const uint4 w = philox_block(static_cast<uint64_t>(j), seed, step);
-    const float2 z01 = box_muller(w.x, w.y);
-    const float2 z23 = box_muller(w.z, w.w);
-    float4 g = g4[j];
-    g.x = fmaf(scale, z01.x, g.x);
-    g.y = fmaf(scale, z01.y, g.y);
-    g.z = fmaf(scale, z23.x, g.z);
-    g.w = fmaf(scale, z23.y, g.w);
-    g4[j] = g;
+  const long long tile = static_cast<long long>(blockDim.x) * kNoiseUnroll;
+  for (long long base = static_cast<long long>(blockIdx.x) * tile; base < nblk;
+       base += static_cast<long long>(gridDim.x) * tile) {
+    float4 g[kNoiseUnroll];
+#pragma unroll
+    for (int u = 0; u < kNoiseUnroll; ++u) {
+      const long long j = base + u * blockDim.x + threadIdx.x;
+      if (j < nblk) g[u] = __ldcs(g4 + j);
+    }
+#pragma unroll
+    for (int u = 0; u < kNoiseUnroll; ++u) {
+      const long long j = base + u * blockDim.x + threadIdx.x;
+      if (j < nblk)
+        __stcs(g4 + j, add_noise4(g[u], philox_block(static_cast<uint64_t>(j), step, rk), scale));
+    }
   }
   // ragged tail: the last n & 3 elements, one thread
   if (blockIdx.x == 0 && threadIdx.x == 0 && (n & 3) != 0) {
-    const uint4 w = philox_block(static_cast<uint64_t>(nblk), seed, step);
+    const uint4 w = philox_block(static_cast<uint64_t>(nblk), step, rk);
     const float2 z01 = box_muller(w.x, w.y);
     const float2 z23 = box_muller(w.z, w.w);
     const float z[4] = {z01.x, z01.y, z23.x, z23.y};
@@ -82,10 +120,11 @@ __global__ void __launch_bounds__(256) noise_kernel(float* __restrict__ grad, lo
 __global__ void __launch_bounds__(256) philox_words_kernel(uint4* __restrict__ out, long long n,
                                                            uint64_t first, uint64_t seed,
                                                            uint64_t step) {
+  const RoundKeys rk = round_keys(seed);
   const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
   for (long long j = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; j < n;
        j += stride)
-    out[j] = philox_block(first + static_cast<uint64_t>(j), seed, step);
+    out[j] = philox_block(first + static_cast<uint64_t>(j), step, rk);
 }
 
 __global__ void clip_kernel(const float* __restrict__ n, long long B, float C,
@@ -119,7 +158,8 @@ int grid_for(long long work, int threads) {
 cudaError_t launch_noise(float* grad, int64_t N, float sigma, float C, uint64_t seed,
                          uint64_t step, cudaStream_t s) {
   if (N == 0) return cudaSuccess;
-  noise_kernel<<<grid_for(N / 4 + 1, 256), 256, 0, s>>>(grad, N, sigma * C, seed, step);
+  noise_kernel<<<grid_for(N / 4 / kNoiseUnroll + 1, 256), 256, 0, s>>>(grad, N, sigma * C, seed,
+                                                                     step);
   return cudaGetLastError();
 }
 

@@ -225,12 +225,247 @@ cudaError_t qr_launch(const float* M, int64_t B, int64_t p, int r, const void* P
   return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------
+// Shared-memory variant (p * r * 4 bytes fit in shared memory): the matrix is
+// held column-major in shared memory, each Householder step needs one block
+// reduction, and the thin Q is formed in place from the compact WY form
+//   H_0 H_1 ... H_{r-1} = I - V T V^T,  T upper triangular,
+//   T_jj = 2,  T[0:j, j] = -2 T[0:j, 0:j] (V[:, 0:j]^T v_j)
+// (normalised reflectors v_j, H_j = I - 2 v_j v_j^T), so that
+//   Q = [I_r; 0] - V (T V_top^T),  V_top = the first r rows of V.
+// ---------------------------------------------------------------------------
+constexpr int kQrSmemThreads = 512;
+constexpr int kQrSmemWarps = kQrSmemThreads / 32;
+
+template <int RT, typename TP>
+__global__ void __launch_bounds__(kQrSmemThreads, 1) qr_smem_kernel(const float* __restrict__ M,
+                                                                 int p, int r,
+                                                                 const TP* __restrict__ P,
+                                                                 void* __restrict__ out,
+                                                                 int hilo) {
+  extern __shared__ float V[];  // [r][p], column l at V + l * p
+  __shared__ float part[kQrSmemWarps][RT];
+  __shared__ float coef[RT];
+  __shared__ float gram[RT][RT];
+  __shared__ float Tm[RT][RT];
+  __shared__ float Km[RT][RT];
+  __shared__ float Cm[RT][RT];
+  const int i = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const float* m = M + static_cast<size_t>(i) * p * r;
+
+  // 1. load, then scale every column by 1 / max |column| (span unchanged)
+  float mx[RT];
+#pragma unroll
+  for (int l = 0; l < RT; ++l) mx[l] = 0.f;
+  for (int row = tid; row < p; row += kQrSmemThreads) {
+#pragma unroll
+    for (int l = 0; l < RT; ++l)
+      if (l < r) {
+        const float x = m[static_cast<size_t>(row) * r + l];
+        V[l * p + row] = x;
+        mx[l] = fmaxf(mx[l], fabsf(x));
+      }
+  }
+#pragma unroll
+  for (int l = 0; l < RT; ++l) {
+    float x = mx[l];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, off));
+    if (lane == 0) part[warp][l] = x;
+  }
+  __syncthreads();
+  if (tid < r) {
+    float x = 0.f;
+    for (int w = 0; w < kQrSmemWarps; ++w) x = fmaxf(x, part[w][tid]);
+    coef[tid] = x > 0.f ? 1.f / x : 1.f;
+  }
+  __syncthreads();
+  for (int row = tid; row < p; row += kQrSmemThreads)
+#pragma unroll
+    for (int l = 0; l < RT; ++l)
+      if (l < r) V[l * p + row] *= coef[l];
+  __syncthreads();
+
+  // 2. Householder, one reduction per column: s_l = x . V[:, l] over rows >= j
+  for (int j = 0; j < r; ++j) {
+    const float* x = V + j * p;
+    float s[RT];
+#pragma unroll
+    for (int l = 0; l < RT; ++l) s[l] = 0.f;
+    for (int row = j + tid; row < p; row += kQrSmemThreads) {
+      const float xr = x[row];
+#pragma unroll
+      for (int l = 0; l < RT; ++l)
+        if (l >= j && l < r) s[l] = fmaf(xr, V[l * p + row], s[l]);
+    }
+#pragma unroll
+    for (int l = 0; l < RT; ++l) {
+      if (l < j || l >= r) continue;
+      float t = s[l];
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
+      if (lane == 0) part[warp][l] = t;
+    }
+    __syncthreads();
+    if (warp == 0) {
+      // lane l < r sums column l's partials in warp order
+      float t = 0.f;
+      if (lane >= j && lane < r)
+        for (int w = 0; w < kQrSmemWarps; ++w) t += part[w][lane];
+      const float norm2 = __shfl_sync(0xffffffffu, t, j);
+      const float xj = x[j];
+      const float nrm = sqrtf(norm2);
+      const float alpha = xj >= 0.f ? -nrm : nrm;
+      const float vn2 = 2.f * norm2 + 2.f * fabsf(xj) * nrm;  // ||x - alpha e_j||^2
+      const float inv = vn2 > 0.f ? rsqrtf(vn2) : 0.f;
+      if (lane > j && lane < r)  // 2 (v_hat . V[:, l]) / ||v||, v = x - alpha e_j
+        coef[lane] = 2.f * inv * inv * (t - alpha * V[lane * p + j]);
+      if (lane == j) coef[j] = alpha;
+      if (lane == 0) Km[0][0] = inv;  // scratch: 1 / ||v||
+    }
+    __syncthreads();
+    const float alpha = coef[j], inv = Km[0][0];
+    for (int row = j + tid; row < p; row += kQrSmemThreads) {
+      const float vr = row == j ? x[row] - alpha : x[row];
+#pragma unroll
+      for (int l = 0; l < RT; ++l)
+        if (l > j && l < r) V[l * p + row] = fmaf(-coef[l], vr, V[l * p + row]);
+      V[j * p + row] = vr * inv;  // column j now holds the normalised reflector
+    }
+    __syncthreads();
+  }
+
+  // 3. gram = V^T V over rows (reflector j is zero above row j), by warps
+  for (int pair = warp; pair < r * r; pair += kQrSmemWarps) {
+    const int a = pair / r, b = pair % r;
+    if (a > b) continue;
+    const int r0 = a > b ? a : b;
+    float t = 0.f;
+    for (int row = r0 + lane; row < p; row += 32) t = fmaf(V[a * p + row], V[b * p + row], t);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
+    if (lane == 0) {
+      gram[a][b] = t;
+      gram[b][a] = t;
+    }
+  }
+  __syncthreads();
+  // T (upper triangular), column by column: lane a of warp 0 computes T[a][j]
+  if (warp == 0) {
+    for (int j = 0; j < r; ++j) {
+      float t = 0.f;
+      if (lane < j)
+        for (int b = lane; b < j; ++b) t = fmaf(Tm[lane][b], gram[b][j], t);
+      __syncwarp();
+      if (lane < j) Tm[lane][j] = -2.f * t;
+      if (lane == j) Tm[j][j] = 2.f;
+      if (lane > j && lane < RT) Tm[lane][j] = 0.f;
+      __syncwarp();
+    }
+  }
+  __syncthreads();
+  // K = T V_top^T: K[a][l] = sum_{a <= b <= l} T[a][b] V[l][b-th reflector]
+  for (int e = tid; e < r * r; e += kQrSmemThreads) {
+    const int a = e / r, l = e % r;
+    float t = 0.f;
+    for (int b = a; b <= l; ++b) t = fmaf(Tm[a][b], V[b * p + l], t);
+    Km[a][l] = t;
+  }
+  __syncthreads();
+  // 4. Q = [I_r; 0] - V K, in place (each row only reads its own reflector entries)
+  for (int row = tid; row < p; row += kQrSmemThreads) {
+    float vrow[RT];
+#pragma unroll
+    for (int a = 0; a < RT; ++a) vrow[a] = (a < r && row >= a) ? V[a * p + row] : 0.f;
+#pragma unroll
+    for (int l = 0; l < RT; ++l) {
+      if (l >= r) continue;
+      float q = row == l ? 1.f : 0.f;
+#pragma unroll
+      for (int a = 0; a < RT; ++a)
+        if (a < r) q = fmaf(-vrow[a], Km[a][l], q);
+      V[l * p + row] = q;
+    }
+  }
+  __syncthreads();
+  // 5. C = Q^T P (r x r), by warps; 6. P' = P - Q C, written with Q
+  for (int pair = warp; pair < r * r; pair += kQrSmemWarps) {
+    const int a = pair / r, b = pair % r;
+    float t = 0.f;
+    for (int row = lane; row < p; row += 32)
+      t = fmaf(V[a * p + row], ldp(P + static_cast<size_t>(row) * r + b), t);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
+    if (lane == 0) Cm[a][b] = t;
+  }
+  __syncthreads();
+  for (int row = tid; row < p; row += kQrSmemThreads) {
+    float q[RT];
+#pragma unroll
+    for (int a = 0; a < RT; ++a) q[a] = a < r ? V[a * p + row] : 0.f;
+    if (hilo) {
+      __nv_bfloat16* o =
+          static_cast<__nv_bfloat16*>(out) + (static_cast<size_t>(i) * p + row) * 4 * r;
+#pragma unroll
+      for (int l = 0; l < RT; ++l) {
+        if (l >= r) continue;
+        const __nv_bfloat16 hi = __float2bfloat16_rn(q[l]);
+        o[l] = hi;
+        o[2 * r + l] = __float2bfloat16_rn(q[l] - __bfloat162float(hi));
+        float pv = ldp(P + static_cast<size_t>(row) * r + l);
+#pragma unroll
+        for (int a = 0; a < RT; ++a)
+          if (a < r) pv = fmaf(-q[a], Cm[a][l], pv);
+        const __nv_bfloat16 phi = __float2bfloat16_rn(pv);
+        o[r + l] = phi;
+        o[3 * r + l] = __float2bfloat16_rn(pv - __bfloat162float(phi));
+      }
+    } else {
+      float* o = static_cast<float*>(out) + (static_cast<size_t>(i) * p + row) * 2 * r;
+#pragma unroll
+      for (int l = 0; l < RT; ++l) {
+        if (l >= r) continue;
+        o[l] = q[l];
+        float pv = ldp(P + static_cast<size_t>(row) * r + l);
+#pragma unroll
+        for (int a = 0; a < RT; ++a)
+          if (a < r) pv = fmaf(-q[a], Cm[a][l], pv);
+        o[r + l] = pv;
+      }
+    }
+  }
+}
+
+template <int RT>
+cudaError_t qr_smem_launch(const float* M, int64_t B, int64_t p, int r, const void* P,
+                           dprc_dtype pdt, void* out, bool hilo, cudaStream_t s) {
+  const int smem = static_cast<int>(p * r * sizeof(float));
+  if (pdt == DPRC_F32) {
+    auto k = qr_smem_kernel<RT, float>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    k<<<static_cast<unsigned>(B), kQrSmemThreads, smem, s>>>(M, static_cast<int>(p), r,
+                                                            static_cast<const float*>(P), out,
+                                                            hilo ? 1 : 0);
+  } else {
+    auto k = qr_smem_kernel<RT, __nv_bfloat16>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    k<<<static_cast<unsigned>(B), kQrSmemThreads, smem, s>>>(
+        M, static_cast<int>(p), r, static_cast<const __nv_bfloat16*>(P), out, hilo ? 1 : 0);
+  }
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_qr_project(const float* M, int64_t B, int64_t p, int r, const void* P,
                               dprc_dtype pdt, float* scratch, void* out, bool hilo,
                               cudaStream_t s) {
   if (r < 1 || r > kMaxR) return cudaErrorInvalidValue;
+  // shared-memory variant when the p x r matrix fits (p <= 3328 at r = 16)
+  if (r <= 16 && p * r * static_cast<int64_t>(sizeof(float)) <= 208 * 1024)
+    return qr_smem_launch<16>(M, B, p, r, P, pdt, out, hilo, s);
   float* V = scratch;
   float* Q = scratch + static_cast<size_t>(B) * p * r;
   if (r <= 16) return qr_launch<16>(M, B, p, r, P, pdt, V, Q, out, hilo, s);

@@ -12,10 +12,26 @@
 // exactly once; their arithmetic intensity is ~n flop/byte, so they are
 // HBM-bound and the tensor cores only have to keep up.
 //
+// Work is cut into blocks of 128 output rows (a 128-token tile for the row
+// projection, a (sample, 128-row chunk of c) pair for the column projection),
+// each the sum over `upb` units (64 columns of c, or 128 tokens).  Two CTAs run
+// per SM, each keeping ~64-96 KB of loads in flight - the shape at which plain
+// TMA streaming reaches ~6 TB/s on this GPU.  Blocks are assigned either
+//   (a) whole, `bpc` per CTA, when there are enough of them, or
+//   (b) one block per thread-block cluster of `cl` CTAs, CTA rank r streaming
+//       units [r*upb/cl, (r+1)*upb/cl); the fp32 partials are then reduced
+//       through distributed shared memory: rank q owns rows [q*128/cl, ...),
+//       receives the other ranks' rows of that range and sums them in rank
+//       order, so the result does not depend on timing.
+// Neither case needs a global cross-CTA reduction, so there is no fix-up tail
+// after the last MMA.
+//
 // Precision: X and R are bf16 (exact in fp32); accumulation is fp32 in TMEM.
 // The fp32 sketch W is carried to the second contraction as two bf16 planes
 // W = W_hi + W_lo (|W - W_hi - W_lo| <= 2^-17 |W|), multiplied as one MMA of
 // width 2n whose two column halves are summed in the epilogue.
+
+#include <atomic>
 
 #include "common.cuh"
 #include "internal.h"
@@ -24,9 +40,10 @@ namespace dprc {
 
 namespace {
 
-constexpr int kRowTile = 128;  // tokens per row-projection CTA (MMA M)
-constexpr int kTileC = 64;     // c-columns per row-projection stage (128 B of bf16)
-constexpr int kTileT = 64;     // T-rows per column-projection stage
+constexpr int kRowTile = 128;   // tokens per row-projection tile (MMA M)
+constexpr int kTileC = 64;      // c per row-projection unit (128 B of bf16)
+constexpr int kColChunk = 128;  // output rows per column-projection block (MMA M)
+constexpr int kTileT = 128;     // T rows per column-projection unit
 
 __device__ __forceinline__ uint8_t* align_1024(uint8_t* p) {
   return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
@@ -52,57 +69,195 @@ __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float* v) {
   }
 }
 
+// Block schedule shared by both kernels (see the file comment).
+struct Sched {
+  int cl;             // CTAs per cluster splitting one block (1, 2, 4 or 8)
+  int bpc;            // whole blocks per CTA when cl == 1
+  long long nblocks;  // blocks in the launch
+  int upb;            // units per block
+};
+
+struct CtaWork {
+  long long b0, b1;  // blocks [b0, b1)
+  int ulo, uhi;      // units [ulo, uhi) of each of them
+  int rank;          // rank in the cluster
+};
+
+__device__ __forceinline__ CtaWork cta_work(const Sched& s) {
+  CtaWork w;
+  if (s.cl == 1) {
+    w.rank = 0;
+    w.b0 = static_cast<long long>(blockIdx.x) * s.bpc;
+    w.b1 = w.b0 + s.bpc < s.nblocks ? w.b0 + s.bpc : s.nblocks;
+    w.ulo = 0;
+    w.uhi = s.upb;
+  } else {
+    w.rank = static_cast<int>(cluster_ctarank());
+    w.b0 = blockIdx.x / s.cl;
+    w.b1 = w.b0 + 1;
+    w.ulo = w.rank * s.upb / s.cl;
+    w.uhi = (w.rank + 1) * s.upb / s.cl;
+  }
+  return w;
+}
+
+// Shared memory of the cluster reduction: receive buffer for the rows this
+// rank owns from every other rank, plus two barriers and a small buffer of
+// per-rank partial norms (used by rank 0).
+struct XchgSmem {
+  float* recv;         // [cl-1][128/cl][N] fp32
+  uint64_t* recv_bar;  // expects (cl-1) * 128/cl arrivals
+  uint64_t* norm_bar;  // rank 0: expects cl-1 arrivals
+  float* norms;        // rank 0: [8]
+};
+
+template <int N>
+__host__ __device__ constexpr int xchg_bytes(int cl) {
+  return cl <= 1 ? 0 : (cl - 1) * (128 / cl) * N * 4;
+}
+
+// Reduce-scatter of one 128-row block of fp32 partials across the cluster:
+// every thread holds row `row` in y[]; afterwards the threads whose row is in
+// this rank's range hold the full sum (in rank order) and return true.
+template <int N>
+__device__ __forceinline__ bool cluster_reduce_rows(const XchgSmem& xs, int cl, int rank, int row,
+                                                    float (&y)[N], bool& ok) {
+  const int R = 128 / cl;
+  const int owner = row / R;
+  const int r_in = row - owner * R;
+  if (owner != rank) {
+    const int slot = rank < owner ? rank : rank - 1;  // sender index at the owner
+    const uint32_t dst = map_to_rank(xs.recv + (static_cast<size_t>(slot) * R + r_in) * N, owner);
+#pragma unroll
+    for (int c4 = 0; c4 < N / 4; ++c4)
+      st_cluster_f4(dst + 16 * c4, make_float4(y[4 * c4], y[4 * c4 + 1], y[4 * c4 + 2], y[4 * c4 + 3]));
+    mbar_arrive_remote(map_to_rank(xs.recv_bar, owner));
+    return false;
+  }
+  if (!mbar_wait_cluster(xs.recv_bar, 0, DPRC_DEVERR_CLUSTER)) ok = false;
+  float acc[N];
+#pragma unroll
+  for (int t = 0; t < N; ++t) acc[t] = 0.f;
+  for (int s = 0; s < cl; ++s) {
+    if (s == rank) {
+#pragma unroll
+      for (int t = 0; t < N; ++t) acc[t] += y[t];
+    } else {
+      const int slot = s < rank ? s : s - 1;
+      const float4* src =
+          reinterpret_cast<const float4*>(xs.recv + (static_cast<size_t>(slot) * R + r_in) * N);
+#pragma unroll
+      for (int c4 = 0; c4 < N / 4; ++c4) {
+        const float4 v = src[c4];
+        acc[4 * c4] += v.x;
+        acc[4 * c4 + 1] += v.y;
+        acc[4 * c4 + 2] += v.z;
+        acc[4 * c4 + 3] += v.w;
+      }
+    }
+  }
+#pragma unroll
+  for (int t = 0; t < N; ++t) y[t] = acc[t];
+  return true;
+}
+
+// Shared prologue of both kernels: pipeline barriers, cluster barriers, TMEM.
+template <int kStages>
+__device__ __forceinline__ void init_barriers(uint64_t* full, uint64_t* empty, uint64_t* accf,
+                                              uint64_t* acce, const XchgSmem& xs, int cl) {
+  for (int s = 0; s < kStages; ++s) {
+    mbar_init(&full[s], 1);
+    mbar_init(&empty[s], 1);
+  }
+  for (int b = 0; b < 2; ++b) {
+    mbar_init(&accf[b], 1);
+    mbar_init(&acce[b], 4);
+  }
+  if (cl > 1) {
+    mbar_init(xs.recv_bar, (cl - 1) * (128 / cl));
+    mbar_init(xs.norm_bar, cl - 1);
+  }
+  fence_mbar_init();
+}
+
 // ===========================================================================
-// Row projection: one CTA per 128-token tile, the whole c reduction in TMEM.
-// Warp 0 lane 0: TMA producer.  Warp 1: TMEM allocator; its lane 0 issues
-// the MMAs.  All four warps: epilogue (warp w owns TMEM lanes 32w..32w+31 =
-// tokens t0+32w..t0+32w+31).
+// Row projection.  Block = 128-token tile; unit = 64 columns of c.
+// Warp 0 lane 0: TMA producer.  Warp 1: TMEM allocator, lane 0 issues the
+// MMAs.  Warps 2..5: epilogue; warp w owns TMEM lanes 32*(w%4).. = tokens of
+// the tile.  The accumulator is double-buffered across blocks.
 // ===========================================================================
+struct RowArgs {
+  int T, c, mtiles;
+  Sched sched;
+  int r_batched;
+  __nv_bfloat16* W;
+  long long tpad;
+  int* zero_ptr;
+  int zero_ints;
+};
+
 template <int NMMA, bool HILO_IN>
 struct RowCfg {
-  static constexpr int kStages = 4;
+  static constexpr int kStages = NMMA >= 64 ? 3 : 4;
   static constexpr int kXBytes = kRowTile * kTileC * 2;  // 16 KB
   static constexpr int kRBytes = kTileC * NMMA * 2;      // 2, 4 or 8 KB
   static constexpr int kStageBytes = kXBytes + kRBytes;
   static constexpr int kN = HILO_IN ? NMMA / 2 : NMMA;
-  static constexpr int kTmemCols = NMMA < 32 ? 32 : NMMA;
-  static constexpr int kSmem = kStages * kStageBytes + 1024 + 256;
+  static constexpr int kAcc = NMMA < 32 ? 32 : NMMA;
+  static constexpr int kTmemCols = 2 * kAcc;
+  static constexpr int kBase = kStages * kStageBytes + 1024 + 256;
+  static constexpr int smem(int cl) { return kBase + xchg_bytes<kN>(cl); }
   static_assert(NMMA == 16 || NMMA == 32 || NMMA == 64, "MN-major R atom is one swizzle row");
 };
 
 template <int NMMA, bool HILO_IN>
-__global__ void __launch_bounds__(128, 1)
+__device__ __forceinline__ void write_sketch_row(__nv_bfloat16* wi, long long tpad,
+                                                 const float (&y)[RowCfg<NMMA, HILO_IN>::kN]) {
+  constexpr int kN = RowCfg<NMMA, HILO_IN>::kN;
+#pragma unroll
+  for (int j = 0; j < kN; ++j) {
+    __nv_bfloat16 hi, lo;
+    split_hilo(y[j], hi, lo);
+    wi[static_cast<size_t>(j) * tpad] = hi;
+    wi[static_cast<size_t>(kN + j) * tpad] = lo;
+  }
+}
+
+template <int NMMA, bool HILO_IN>
+__global__ void __launch_bounds__(192, 2)
     tc_rowproj_kernel(const __grid_constant__ CUtensorMap map_x,
-                      const __grid_constant__ CUtensorMap map_r, int T, int c, int r_batched,
-                      int mtiles, __nv_bfloat16* __restrict__ W, long long tpad,
-                      int* __restrict__ zero_ptr, int zero_ints) {
+                      const __grid_constant__ CUtensorMap map_r, const RowArgs a) {
   using Cfg = RowCfg<NMMA, HILO_IN>;
+  constexpr int kN = Cfg::kN;
   extern __shared__ uint8_t smem_raw[];
+
+  const Sched& sc = a.sched;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // The whole grid fits at once: the next kernel may start its prologue.
+  pdl_launch_dependents();
+  if (blockIdx.x == 0 && a.zero_ptr != nullptr)
+    for (int z = threadIdx.x; z < a.zero_ints; z += blockDim.x) a.zero_ptr[z] = 0;
+  const CtaWork wk = cta_work(sc);
+  const int nu = wk.uhi - wk.ulo;
+
   uint8_t* smem = align_1024(smem_raw);
   uint8_t* sx = smem;
   uint8_t* sr = smem + Cfg::kStages * Cfg::kXBytes;
   uint64_t* full = reinterpret_cast<uint64_t*>(sr + Cfg::kStages * Cfg::kRBytes);
   uint64_t* empty = full + Cfg::kStages;
   uint64_t* accf = empty + Cfg::kStages;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accf + 1);
+  uint64_t* acce = accf + 2;
+  XchgSmem xs;
+  xs.recv_bar = acce + 2;
+  xs.norm_bar = acce + 3;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acce + 4);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int i = blockIdx.x / mtiles;
-  const int t0 = (blockIdx.x % mtiles) * kRowTile;
-  const int kc_n = (c + kTileC - 1) / kTileC;
-
-  if (blockIdx.x == 0 && zero_ptr != nullptr)
-    for (int z = threadIdx.x; z < zero_ints; z += blockDim.x) zero_ptr[z] = 0;
+  xs.norms = reinterpret_cast<float*>(tmem_slot + 2);
+  xs.recv = reinterpret_cast<float*>(smem + Cfg::kBase - 1024);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < Cfg::kStages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
-    }
-    mbar_init(accf, 1);
+    init_barriers<Cfg::kStages>(full, empty, accf, acce, xs, sc.cl);
     *abort_flag = 0;
-    fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&map_x);
@@ -114,74 +269,113 @@ __global__ void __launch_bounds__(128, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if (sc.cl > 1) cluster_sync_all();  // peers' barriers exist before any remote arrive
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0 && lane == 0) {
-    int issued = 0;
-    for (int kc = 0; kc < kc_n; ++kc) {
-      const int s = kc % Cfg::kStages;
-      const uint32_t ph = (kc / Cfg::kStages) & 1;
-      if (!mbar_wait(&empty[s], ph ^ 1, DPRC_DEVERR_PIPE_EMPTY)) {
-        *abort_flag = 1;
-        break;
+  if (warp == 0) {
+    if (lane == 0 && wk.b1 > wk.b0) {
+      long long it = 0;
+      bool ok = true;
+      for (long long b = wk.b0; b < wk.b1 && ok; ++b) {
+        const int i = static_cast<int>(b / a.mtiles);
+        const int t0 = static_cast<int>(b - static_cast<long long>(i) * a.mtiles) * kRowTile;
+        for (int kc = wk.ulo; kc < wk.uhi; ++kc, ++it) {
+          const int s = static_cast<int>(it % Cfg::kStages);
+          const uint32_t ph = static_cast<uint32_t>(it / Cfg::kStages) & 1;
+          if (!mbar_wait(&empty[s], ph ^ 1, DPRC_DEVERR_PIPE_EMPTY)) {
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[s], Cfg::kStageBytes);
+          tma_load_3d(sx + s * Cfg::kXBytes, &map_x, &full[s], kc * kTileC, t0, i);
+          tma_load_3d(sr + s * Cfg::kRBytes, &map_r, &full[s], 0, kc * kTileC,
+                      a.r_batched ? i : 0);
+        }
       }
-      mbar_arrive_expect_tx(&full[s], Cfg::kStageBytes);
-      tma_load_3d(sx + s * Cfg::kXBytes, &map_x, &full[s], kc * kTileC, t0, i);
-      tma_load_3d(sr + s * Cfg::kRBytes, &map_r, &full[s], 0, kc * kTileC, r_batched ? i : 0);
-      ++issued;
+      // let the copies this thread issued land before the CTA can exit
+      for (long long k = it - 1; k >= 0 && k >= it - Cfg::kStages; --k)
+        mbar_wait(&full[k % Cfg::kStages], (k / Cfg::kStages) & 1, DPRC_DEVERR_PIPE_FULL);
     }
-    // Let the copies this thread issued land before the CTA can exit.
-    for (int kc = issued - 1; kc >= 0 && kc >= issued - Cfg::kStages; --kc)
-      mbar_wait(&full[kc % Cfg::kStages], (kc / Cfg::kStages) & 1, DPRC_DEVERR_PIPE_FULL);
-  } else if (warp == 1 && lane == 0) {
-    constexpr uint32_t idesc = make_idesc_bf16(128, NMMA, false, true);
-    constexpr uint32_t r_swz = swz_code_for_bytes(2 * NMMA);
-    for (int kc = 0; kc < kc_n; ++kc) {
-      const int s = kc % Cfg::kStages;
-      const uint32_t ph = (kc / Cfg::kStages) & 1;
-      if (!mbar_wait(&full[s], ph, DPRC_DEVERR_PIPE_FULL)) {
-        *abort_flag = 1;
-        break;
+  } else if (warp == 1) {
+    if (lane == 0 && wk.b1 > wk.b0) {
+      constexpr uint32_t idesc = make_idesc_bf16(128, NMMA, false, true);
+      constexpr uint32_t r_swz = swz_code_for_bytes(2 * NMMA);
+      long long it = 0;
+      int seg = 0;
+      bool ok = true;
+      for (long long b = wk.b0; b < wk.b1 && ok; ++b, ++seg) {
+        const int abuf = seg & 1;
+        if (!mbar_wait(&acce[abuf], ((seg >> 1) & 1) ^ 1, DPRC_DEVERR_ACCUM)) {
+          *abort_flag = 1;
+          break;
+        }
+        tc_fence_after();
+        for (int kc = wk.ulo; kc < wk.uhi; ++kc, ++it) {
+          const int s = static_cast<int>(it % Cfg::kStages);
+          const uint32_t ph = static_cast<uint32_t>(it / Cfg::kStages) & 1;
+          if (!mbar_wait(&full[s], ph, DPRC_DEVERR_PIPE_FULL)) {
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t xa = smem_u32(sx + s * Cfg::kXBytes);
+          const uint32_t ra = smem_u32(sr + s * Cfg::kRBytes);
+#pragma unroll
+          for (int kk = 0; kk < kTileC / 16; ++kk) {
+            // X tile: 128 token rows x 64 c, K-major, 128-byte swizzle.
+            const uint64_t ad = make_sdesc(xa + kk * 32, 16, 1024, kSwz128);
+            // R tile: 64 c rows x NMMA columns, MN-major, one swizzle atom
+            // wide; 8-row atoms of 16*NMMA bytes, a K=16 step is 32*NMMA bytes.
+            const uint64_t bd = make_sdesc(ra + kk * 32 * NMMA, 16, 16 * NMMA, r_swz);
+            umma_bf16(tmem + abuf * Cfg::kAcc, ad, bd, idesc,
+                      (kc == wk.ulo && kk == 0) ? 0u : 1u);
+          }
+          umma_commit(&empty[s]);
+        }
+        if (ok) umma_commit(&accf[abuf]);
       }
+    }
+  } else {
+    // ---------------- epilogue warps 2..5 ----------------
+    const int ew = warp - 2;
+    const int q = warp & 3;
+    const int row = q * 32 + lane;  // token within the tile = TMEM lane
+    bool ok = true;
+    int seg = 0;
+    for (long long b = wk.b0; b < wk.b1; ++b, ++seg) {
+      const int abuf = seg & 1;
+      bool live = ok && mbar_wait(&accf[abuf], (seg >> 1) & 1, DPRC_DEVERR_ACCUM) &&
+                  *abort_flag == 0;
+      live = __all_sync(0xffffffffu, live);  // keep the warp's TMEM loads convergent
+      if (!live) ok = false;
       tc_fence_after();
-      const uint32_t xa = smem_u32(sx + s * Cfg::kXBytes);
-      const uint32_t ra = smem_u32(sr + s * Cfg::kRBytes);
+      float y[kN];
 #pragma unroll
-      for (int kk = 0; kk < kTileC / 16; ++kk) {
-        // X tile: 128 token rows x 64 c, K-major, 128-byte swizzle.
-        const uint64_t ad = make_sdesc(xa + kk * 32, 16, 1024, kSwz128);
-        // R tile: 64 c rows x NMMA columns, MN-major, one swizzle atom wide;
-        // 8-row atoms of 16*NMMA bytes, so a K=16 step is 32*NMMA bytes.
-        const uint64_t bd = make_sdesc(ra + kk * 32 * NMMA, 16, 16 * NMMA, r_swz);
-        umma_bf16(tmem, ad, bd, idesc, (kc | kk) != 0 ? 1u : 0u);
+      for (int t = 0; t < kN; ++t) y[t] = 0.f;
+      if (live) {
+        float v[NMMA];
+        tmem_ld_cols<NMMA>(tmem + (static_cast<uint32_t>(q * 32) << 16) + abuf * Cfg::kAcc, v);
+#pragma unroll
+        for (int t = 0; t < kN; ++t) y[t] = HILO_IN ? v[t] + v[kN + t] : v[t];
       }
-      umma_commit(&empty[s]);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acce[abuf]);
+      bool mine = true;
+      if (sc.cl > 1) mine = cluster_reduce_rows<kN>(xs, sc.cl, wk.rank, row, y, ok);
+      const int i = static_cast<int>(b / a.mtiles);
+      const int t = static_cast<int>(b - static_cast<long long>(i) * a.mtiles) * kRowTile + row;
+      if (mine && ok && t < a.T)
+        write_sketch_row<NMMA, HILO_IN>(a.W + static_cast<size_t>(i) * 2 * kN * a.tpad + t,
+                                        a.tpad, y);
     }
-    umma_commit(accf);
+    (void)ew;
   }
-  __syncwarp();
 
-  // ---- epilogue: TMEM -> registers -> bf16 hi/lo planes of W ----
-  const bool ok = __all_sync(0xffffffffu, mbar_wait(accf, 0, DPRC_DEVERR_ACCUM) && *abort_flag == 0);
-  tc_fence_after();
-  pdl_launch_dependents();
-  if (ok) {
-    float v[NMMA];
-    tmem_ld_cols<NMMA>(tmem + (static_cast<uint32_t>(warp * 32) << 16), v);
-    const int t = t0 + warp * 32 + lane;
-    if (t < T) {
-      __nv_bfloat16* wi = W + static_cast<size_t>(i) * 2 * Cfg::kN * tpad + t;
-#pragma unroll
-      for (int j = 0; j < Cfg::kN; ++j) {
-        const float y = HILO_IN ? v[j] + v[Cfg::kN + j] : v[j];
-        __nv_bfloat16 hi, lo;
-        split_hilo(y, hi, lo);
-        wi[static_cast<size_t>(j) * tpad] = hi;
-        wi[static_cast<size_t>(Cfg::kN + j) * tpad] = lo;
-      }
-    }
-  }
+  __syncwarp();  // reconverge each warp before the CTA barrier
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -191,24 +385,15 @@ __global__ void __launch_bounds__(128, 1)
 }
 
 // ===========================================================================
-// Column projection, persistent stream-K over units (block b, T-tile kt),
-// block b = (sample i, chunk of 256 output rows).  CTA j owns the contiguous
-// unit range [j U / G, (j+1) U / G); each maximal run inside one block is a
-// "segment" whose fp32 partial Y goes to a private slot.  A ticket per block
-// finds the CTA that completes it; that CTA sums the block's partial slots in
-// CTA order (deterministic), then applies the mode (norm / fp32 / hi-lo).
-//
-// Warp 0 lane 0: TMA producer.  Warp 1: TMEM allocator + MMA issuer.
-// Warps 2..5: epilogue (warp w may access TMEM lanes 32*(w%4)...).  The
-// accumulator is double-buffered in TMEM so MMAs of the next segment overlap
-// the epilogue of the previous one.
+// Column projection.  Block = (sample i, 128-row chunk of c); unit = 128 T
+// rows.  Stage: two 16 KB boxes of X (128 T x 64 c each; the operand X^T is
+// MN-major) and two boxes of the sketch (64 T x 2n rows each, K-major).  The X
+// loads of the first stages are issued before waiting on the previous kernel
+// (they do not depend on it), so they overlap its tail.
 // ===========================================================================
 struct ColArgs {
-  int T, c, nchunks, kt;
-  long long units;
-  int max_seg;
-  float* part;
-  int* tickets;
+  int T, c, nchunks;
+  Sched sched;
   int* sample_tickets;
   float* chunk_norms;
   int mode;
@@ -222,39 +407,33 @@ struct ColArgs {
 
 template <int NMMA>
 struct ColCfg {
-  static constexpr int kChunk = 256;
-  static constexpr int kMB = kChunk / 128;
-  static constexpr int kXBoxBytes = kTileT * 64 * 2;           // 64 T rows x 64 c = 8 KB
-  static constexpr int kXBytes = kTileT * kChunk * 2;          // 32 KB
-  static constexpr int kWBytes = NMMA * kTileT * 2;            // 4, 8 or 16 KB
+  static constexpr int kXBoxBytes = kTileT * 64 * 2;   // 128 T rows x 64 c = 16 KB
+  static constexpr int kXBytes = 2 * kXBoxBytes;       // 128 c
+  static constexpr int kWBoxBytes = NMMA * 64 * 2;     // NMMA rows x 64 T
+  static constexpr int kWBytes = 2 * kWBoxBytes;       // 128 T
   static constexpr int kStageBytes = kXBytes + kWBytes;
-  static constexpr int kStages = NMMA >= 128 ? 4 : 5;
+  static constexpr int kStages = NMMA >= 128 ? 3 : 2;
+  static constexpr int kCtasPerSm = NMMA >= 128 ? 1 : 2;
   static constexpr int kN = NMMA / 2;
-  static constexpr int kAccCols = kMB * NMMA;
-  static constexpr int kTmemCols = 2 * kAccCols;
-  static constexpr int kSmem = kStages * kStageBytes + 1024 + 512;
-  static_assert(kTmemCols <= 512, "TMEM has 512 columns");
+  static constexpr int kAcc = NMMA;
+  static constexpr int kTmemCols = 2 * kAcc;
+  static constexpr int kBase = kStages * kStageBytes + 1024 + 256;
+  static constexpr int smem(int cl) { return kBase + xchg_bytes<kN>(cl); }
+  static_assert(kTmemCols * kCtasPerSm <= 512, "TMEM has 512 columns");
 };
 
-__device__ __forceinline__ long long cta_of_unit(long long u, long long units, int G) {
-  return ((u + 1) * G - 1) / units;
-}
-
 template <int NMMA>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(192, ColCfg<NMMA>::kCtasPerSm)
     tc_colproj_kernel(const __grid_constant__ CUtensorMap map_x,
                       const __grid_constant__ CUtensorMap map_w, const ColArgs a) {
   using Cfg = ColCfg<NMMA>;
   constexpr int kN = Cfg::kN;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ int s_last;
   __shared__ float s_red[4];
 
-  const int G = gridDim.x, j = blockIdx.x;
-  const long long u0 = static_cast<long long>(j) * a.units / G;
-  const long long u1 = static_cast<long long>(j + 1) * a.units / G;
-  if (u0 >= u1) return;  // uniform across the CTA
-  const int KT = a.kt;
+  const Sched& sc = a.sched;
+  const CtaWork wk = cta_work(sc);
+  const int nu = wk.uhi - wk.ulo;
 
   uint8_t* smem = align_1024(smem_raw);
   uint8_t* sx = smem;
@@ -263,22 +442,19 @@ __global__ void __launch_bounds__(192, 1)
   uint64_t* empty = full + Cfg::kStages;
   uint64_t* accf = empty + Cfg::kStages;  // [2]
   uint64_t* acce = accf + 2;              // [2]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acce + 2);
+  XchgSmem xs;
+  xs.recv_bar = acce + 2;
+  xs.norm_bar = acce + 3;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acce + 4);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  xs.norms = reinterpret_cast<float*>(tmem_slot + 2);
+  xs.recv = reinterpret_cast<float*>(smem + Cfg::kBase - 1024);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < Cfg::kStages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
-    }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&accf[b], 1);
-      mbar_init(&acce[b], 4);
-    }
+    init_barriers<Cfg::kStages>(full, empty, accf, acce, xs, sc.cl);
     *abort_flag = 0;
-    fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&map_x);
@@ -290,181 +466,160 @@ __global__ void __launch_bounds__(192, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if (sc.cl > 1) cluster_sync_all();  // peers' barriers exist before any remote arrive
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // The sketch W and the cleared tickets come from the previous kernel.
-  pdl_wait();
+  const long long total = (wk.b1 - wk.b0) * nu;  // units of this CTA
 
   if (warp == 0) {
-    if (lane == 0) {
-      long long issued = 0;
-      for (long long u = u0; u < u1; ++u) {
-        const int it = static_cast<int>(u - u0);
-        const int s = it % Cfg::kStages;
-        const uint32_t ph = (it / Cfg::kStages) & 1;
+    if (lane == 0 && total > 0) {
+      auto unit = [&](long long it, int& i, int& ch, int& kt) {
+        const long long b = wk.b0 + it / nu;
+        kt = wk.ulo + static_cast<int>(it % nu);
+        i = static_cast<int>(b / a.nchunks);
+        ch = static_cast<int>(b - static_cast<long long>(i) * a.nchunks);
+      };
+      auto load_x = [&](long long it, int s) {
+        int i, ch, kt;
+        unit(it, i, ch, kt);
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+          tma_load_3d(sx + s * Cfg::kXBytes + h * Cfg::kXBoxBytes, &map_x, &full[s],
+                      ch * kColChunk + h * 64, kt * kTileT, i);
+      };
+      auto load_w = [&](long long it, int s) {
+        int i, ch, kt;
+        unit(it, i, ch, kt);
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+          tma_load_3d(sw + s * Cfg::kWBytes + h * Cfg::kWBoxBytes, &map_w, &full[s],
+                      kt * kTileT + h * 64, 0, i);
+      };
+      const int pre = static_cast<int>(total < Cfg::kStages ? total : Cfg::kStages);
+      for (int it = 0; it < pre; ++it) {
+        mbar_arrive_expect_tx(&full[it], Cfg::kStageBytes);
+        load_x(it, it);
+      }
+      pdl_wait();  // the sketch is written by the previous kernel
+      for (int it = 0; it < pre; ++it) load_w(it, it);
+      long long issued = pre;
+      for (long long it = pre; it < total; ++it) {
+        const int s = static_cast<int>(it % Cfg::kStages);
+        const uint32_t ph = static_cast<uint32_t>(it / Cfg::kStages) & 1;
         if (!mbar_wait(&empty[s], ph ^ 1, DPRC_DEVERR_PIPE_EMPTY)) {
           *abort_flag = 1;
           break;
         }
-        const long long b = u / KT;
-        const int kt = static_cast<int>(u - b * KT);
-        const int i = static_cast<int>(b / a.nchunks);
-        const int ch = static_cast<int>(b - static_cast<long long>(i) * a.nchunks);
         mbar_arrive_expect_tx(&full[s], Cfg::kStageBytes);
-        uint8_t* xs = sx + s * Cfg::kXBytes;
-#pragma unroll
-        for (int q = 0; q < Cfg::kChunk / 64; ++q)
-          tma_load_3d(xs + q * Cfg::kXBoxBytes, &map_x, &full[s], ch * Cfg::kChunk + q * 64,
-                      kt * kTileT, i);
-        tma_load_3d(sw + s * Cfg::kWBytes, &map_w, &full[s], kt * kTileT, 0, i);
+        load_x(it, s);
+        load_w(it, s);
         ++issued;
       }
-      for (long long it = issued - 1; it >= 0 && it >= issued - Cfg::kStages; --it)
-        mbar_wait(&full[it % Cfg::kStages], (it / Cfg::kStages) & 1, DPRC_DEVERR_PIPE_FULL);
+      for (long long k = issued - 1; k >= 0 && k >= issued - Cfg::kStages; --k)
+        mbar_wait(&full[k % Cfg::kStages], (k / Cfg::kStages) & 1, DPRC_DEVERR_PIPE_FULL);
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    if (lane == 0 && total > 0) {
       constexpr uint32_t idesc = make_idesc_bf16(128, NMMA, true, false);
+      long long it = 0;
       int seg = 0;
-      for (long long u = u0; u < u1; ++u) {
-        const int it = static_cast<int>(u - u0);
-        const int s = it % Cfg::kStages;
-        const uint32_t ph = (it / Cfg::kStages) & 1;
-        const long long b = u / KT;
-        const int kt = static_cast<int>(u - b * KT);
-        const bool first = (u == u0) || (kt == 0);
-        const bool last = (u == u1 - 1) || (kt == KT - 1);
+      bool ok = true;
+      for (long long b = wk.b0; b < wk.b1 && ok; ++b, ++seg) {
         const int abuf = seg & 1;
-        if (first) {
-          if (!mbar_wait(&acce[abuf], ((seg >> 1) & 1) ^ 1, DPRC_DEVERR_ACCUM)) {
-            *abort_flag = 1;
-            break;
-          }
-          tc_fence_after();
-        }
-        if (!mbar_wait(&full[s], ph, DPRC_DEVERR_PIPE_FULL)) {
+        if (!mbar_wait(&acce[abuf], ((seg >> 1) & 1) ^ 1, DPRC_DEVERR_ACCUM)) {
           *abort_flag = 1;
           break;
         }
         tc_fence_after();
-        const uint32_t xa = smem_u32(sx + s * Cfg::kXBytes);
-        const uint32_t wa = smem_u32(sw + s * Cfg::kWBytes);
-#pragma unroll
-        for (int kk = 0; kk < kTileT / 16; ++kk) {
-          // W tile: NMMA rows x 64 T, K-major, 128-byte swizzle.
-          const uint64_t bd = make_sdesc(wa + kk * 32, 16, 1024, kSwz128);
-#pragma unroll
-          for (int mb = 0; mb < Cfg::kMB; ++mb) {
-            // X tile: T rows of 64 c per 8 KB box; the operand X^T is MN-major
-            // (c contiguous): atoms of 64 c x 8 T = 1 KB, SBO = 1 KB along T,
-            // LBO = one box along c.  A K=16 step is two atoms (2 KB).
-            const uint64_t ad = make_sdesc(xa + mb * 2 * Cfg::kXBoxBytes + kk * 2048,
-                                           Cfg::kXBoxBytes, 1024, kSwz128);
-            umma_bf16(tmem + abuf * Cfg::kAccCols + mb * NMMA, ad, bd, idesc,
-                      (first && kk == 0) ? 0u : 1u);
+        for (int u = 0; u < nu; ++u, ++it) {
+          const int s = static_cast<int>(it % Cfg::kStages);
+          const uint32_t ph = static_cast<uint32_t>(it / Cfg::kStages) & 1;
+          if (!mbar_wait(&full[s], ph, DPRC_DEVERR_PIPE_FULL)) {
+            *abort_flag = 1;
+            ok = false;
+            break;
           }
+          tc_fence_after();
+          const uint32_t xa = smem_u32(sx + s * Cfg::kXBytes);
+          const uint32_t wa = smem_u32(sw + s * Cfg::kWBytes);
+#pragma unroll
+          for (int kk = 0; kk < kTileT / 16; ++kk) {
+            // X^T: 128 c (two 64-c atoms, LBO = one box) x 16 T (two 8-row
+            // atoms, SBO = 1 KB); a K=16 step is 16 rows of 128 B.
+            const uint64_t ad = make_sdesc(xa + kk * 2048, Cfg::kXBoxBytes, 1024, kSwz128);
+            // Sketch: NMMA rows x 64 T per box, K-major, 128-byte swizzle.
+            const uint64_t bd =
+                make_sdesc(wa + (kk >> 2) * Cfg::kWBoxBytes + (kk & 3) * 32, 16, 1024, kSwz128);
+            umma_bf16(tmem + abuf * Cfg::kAcc, ad, bd, idesc, (u == 0 && kk == 0) ? 0u : 1u);
+          }
+          umma_commit(&empty[s]);
         }
-        umma_commit(&empty[s]);
-        if (last) {
-          umma_commit(&accf[abuf]);
-          ++seg;
-        }
+        if (ok) umma_commit(&accf[abuf]);
       }
     }
   } else {
     // ---------------- epilogue warps 2..5 ----------------
+    pdl_wait();  // the sample tickets are cleared by the previous kernel
     const int ew = warp - 2;
     const int q = warp & 3;
-    bool dead = false;
-    const long long b_first = u0 / KT, b_last = (u1 - 1) / KT;
+    const int row = q * 32 + lane;  // row of the 128-row chunk = TMEM lane
+    bool ok = true;
     int seg = 0;
-    for (long long b = b_first; b <= b_last; ++b, ++seg) {
+    for (long long b = wk.b0; b < wk.b1; ++b, ++seg) {
       const int abuf = seg & 1;
-      if (!dead && !mbar_wait(&accf[abuf], (seg >> 1) & 1, DPRC_DEVERR_ACCUM)) dead = true;
-      if (*abort_flag) dead = true;
-      dead = __any_sync(0xffffffffu, dead);  // keep the warp's TMEM loads convergent
+      bool live = ok && mbar_wait(&accf[abuf], (seg >> 1) & 1, DPRC_DEVERR_ACCUM) &&
+                  *abort_flag == 0;
+      live = __all_sync(0xffffffffu, live);  // keep the warp's TMEM loads convergent
+      if (!live) ok = false;
       tc_fence_after();
-      float* slot = a.part + (static_cast<size_t>(j) * a.max_seg + seg) * Cfg::kChunk * kN;
-      if (!dead) {
-#pragma unroll 1
-        for (int mb = 0; mb < Cfg::kMB; ++mb) {
-          const int row = mb * 128 + q * 32 + lane;
-          const uint32_t tb = tmem + (static_cast<uint32_t>(q * 32) << 16) +
-                              abuf * Cfg::kAccCols + mb * NMMA;
-          float hi[kN], lo[kN];
-          tmem_ld_cols<kN>(tb, hi);
-          tmem_ld_cols<kN>(tb + kN, lo);
-          float4* dst = reinterpret_cast<float4*>(slot + static_cast<size_t>(row) * kN);
+      float y[kN];
 #pragma unroll
-          for (int c4 = 0; c4 < kN / 4; ++c4)
-            dst[c4] = make_float4(hi[4 * c4] + lo[4 * c4], hi[4 * c4 + 1] + lo[4 * c4 + 1],
-                                  hi[4 * c4 + 2] + lo[4 * c4 + 2], hi[4 * c4 + 3] + lo[4 * c4 + 3]);
-        }
+      for (int t = 0; t < kN; ++t) y[t] = 0.f;
+      if (live) {
+        const uint32_t tb = tmem + (static_cast<uint32_t>(q * 32) << 16) + abuf * Cfg::kAcc;
+        float hi[kN], lo[kN];
+        tmem_ld_cols<kN>(tb, hi);
+        tmem_ld_cols<kN>(tb + kN, lo);
+#pragma unroll
+        for (int t = 0; t < kN; ++t) y[t] = hi[t] + lo[t];
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acce[abuf]);
-      __threadfence();
-      named_bar_sync(1, 128);
-      if (ew == 0 && lane == 0) {
-        const long long lo_u = b * KT > u0 ? b * KT : u0;
-        const long long hi_u = (b + 1) * KT < u1 ? (b + 1) * KT : u1;
-        const int cnt = static_cast<int>(hi_u - lo_u);
-        const int old = atomicAdd(&a.tickets[b], cnt);
-        s_last = (!dead && old + cnt == KT) ? 1 : 0;
-      }
-      named_bar_sync(1, 128);
-      if (s_last) {
-        __threadfence();
-        const int i = static_cast<int>(b / a.nchunks);
-        const int ch = static_cast<int>(b - static_cast<long long>(i) * a.nchunks);
-        const long long j_first = cta_of_unit(b * KT, a.units, G);
-        const long long j_last = cta_of_unit((b + 1) * KT - 1, a.units, G);
+      bool mine = true;
+      if (sc.cl > 1) mine = cluster_reduce_rows<kN>(xs, sc.cl, wk.rank, row, y, ok);
+      const int i = static_cast<int>(b / a.nchunks);
+      const int ch = static_cast<int>(b - static_cast<long long>(i) * a.nchunks);
+      const int grow = ch * kColChunk + row;
+      if (a.mode == kColprojNorm) {
+        // this CTA's rows: weighted squares, then a fixed-order reduction
         float sq = 0.f;
-#pragma unroll 1
-        for (int mb = 0; mb < Cfg::kMB; ++mb) {
-          const int row = mb * 128 + ew * 32 + lane;
-          const int grow = ch * Cfg::kChunk + row;
-          float acc[kN];
+        if (mine && ok && grow < a.c) {
 #pragma unroll
-          for (int t = 0; t < kN; ++t) acc[t] = 0.f;
-          for (long long jj = j_first; jj <= j_last; ++jj) {
-            const long long uj0 = jj * a.units / G;
-            const int sj = static_cast<int>(b - uj0 / KT);
-            const float4* src = reinterpret_cast<const float4*>(
-                a.part + ((static_cast<size_t>(jj) * a.max_seg + sj) * Cfg::kChunk + row) * kN);
-#pragma unroll
-            for (int c4 = 0; c4 < kN / 4; ++c4) {
-              const float4 v = __ldcg(src + c4);
-              acc[4 * c4] += v.x;
-              acc[4 * c4 + 1] += v.y;
-              acc[4 * c4 + 2] += v.z;
-              acc[4 * c4 + 3] += v.w;
-            }
-          }
-          if (grow < a.c) {
-            if (a.mode == kColprojNorm) {
-#pragma unroll
-              for (int t = 0; t < kN; ++t) sq += (t < a.n_head ? 1.f : a.w_tail) * acc[t] * acc[t];
-            } else if (a.mode == kColprojF32) {
-              float* dst = a.y_f32 + (static_cast<size_t>(i) * a.c + grow) * kN;
-#pragma unroll
-              for (int t = 0; t < kN; ++t) dst[t] = acc[t];
-            } else {
-              __nv_bfloat16* dst = a.y_hilo + (static_cast<size_t>(i) * a.c + grow) * 2 * kN;
-#pragma unroll
-              for (int t = 0; t < kN; ++t) split_hilo(acc[t], dst[t], dst[kN + t]);
-            }
-          }
+          for (int t = 0; t < kN; ++t) sq += (t < a.n_head ? 1.f : a.w_tail) * y[t] * y[t];
         }
-        if (a.mode == kColprojNorm) {
 #pragma unroll
-          for (int off = 16; off > 0; off >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, off);
-          if (lane == 0) s_red[ew] = sq;
-          named_bar_sync(1, 128);
-          if (ew == 0 && lane == 0) {
-            const float tot = (s_red[0] + s_red[1]) + (s_red[2] + s_red[3]);
-            a.chunk_norms[b] = tot;
+        for (int off = 16; off > 0; off >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, off);
+        if (lane == 0) s_red[ew] = sq;
+        named_bar_sync(1, 128);
+        if (ew == 0 && lane == 0) {
+          const float part = (s_red[0] + s_red[1]) + (s_red[2] + s_red[3]);
+          float chunk = part;
+          bool leader = true;
+          if (sc.cl > 1) {
+            if (wk.rank != 0) {
+              st_cluster_f32(map_to_rank(xs.norms + wk.rank, 0), part);
+              mbar_arrive_remote(map_to_rank(xs.norm_bar, 0));
+              leader = false;
+            } else {
+              if (!mbar_wait_cluster(xs.norm_bar, 0, DPRC_DEVERR_CLUSTER)) ok = false;
+              xs.norms[0] = part;
+              chunk = 0.f;
+              for (int s = 0; s < sc.cl; ++s) chunk += xs.norms[s];
+            }
+          }
+          if (leader && ok) {
+            a.chunk_norms[b] = chunk;
             __threadfence();
             const int old = atomicAdd(&a.sample_tickets[i], 1);
             if (old == a.nchunks - 1) {
@@ -473,14 +628,27 @@ __global__ void __launch_bounds__(192, 1)
               for (int c2 = 0; c2 < a.nchunks; ++c2)
                 sum += __ldcg(&a.chunk_norms[static_cast<size_t>(i) * a.nchunks + c2]);
               a.n_out[i] = (a.accumulate ? a.n_out[i] : 0.f) + sum;
+              a.sample_tickets[i] = 0;
             }
           }
         }
+        named_bar_sync(1, 128);
+      } else if (mine && ok && grow < a.c) {
+        if (a.mode == kColprojF32) {
+          float4* d4 = reinterpret_cast<float4*>(a.y_f32 + (static_cast<size_t>(i) * a.c + grow) * kN);
+#pragma unroll
+          for (int c4 = 0; c4 < kN / 4; ++c4)
+            d4[c4] = make_float4(y[4 * c4], y[4 * c4 + 1], y[4 * c4 + 2], y[4 * c4 + 3]);
+        } else {
+          __nv_bfloat16* dst = a.y_hilo + (static_cast<size_t>(i) * a.c + grow) * 2 * kN;
+#pragma unroll
+          for (int t = 0; t < kN; ++t) split_hilo(y[t], dst[t], dst[kN + t]);
+        }
       }
-      named_bar_sync(1, 128);
     }
   }
 
+  __syncwarp();  // reconverge each warp before the CTA barrier
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -489,49 +657,65 @@ __global__ void __launch_bounds__(192, 1)
   }
 }
 
-template <typename K>
-cudaError_t set_smem(K kernel, int bytes) {
-  return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-}
-
-template <int NMMA, bool HILO_IN>
-cudaError_t rowproj_launch(const CUtensorMap& mx, const CUtensorMap& mr, int T, int c,
-                           int r_batched, int B, void* W, long long tpad, int* zero_ptr,
-                           int zero_ints, cudaStream_t s) {
-  using Cfg = RowCfg<NMMA, HILO_IN>;
-  auto kern = tc_rowproj_kernel<NMMA, HILO_IN>;
-  cudaError_t e = set_smem(kern, Cfg::kSmem);
+// Raises a kernel's dynamic shared memory limit once per device (the attribute
+// is per context; setting it on every launch costs host time).  Keyed by the
+// kernel itself: instantiations share a type, not an attribute.
+template <auto Kernel>
+cudaError_t set_smem_once(int bytes) {
+  constexpr int kMaxDev = 64;
+  static std::atomic<int> done[kMaxDev];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  const int mtiles = (T + kRowTile - 1) / kRowTile;
-  kern<<<B * mtiles, 128, Cfg::kSmem, s>>>(mx, mr, T, c, r_batched, mtiles,
-                                            static_cast<__nv_bfloat16*>(W), tpad, zero_ptr,
-                                            zero_ints);
-  return cudaGetLastError();
+  if (dev >= 0 && dev < kMaxDev && done[dev].load(std::memory_order_acquire) >= bytes)
+    return cudaSuccess;
+  e = cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && dev >= 0 && dev < kMaxDev) done[dev].store(bytes, std::memory_order_release);
+  return e;
 }
 
-template <int NMMA>
-cudaError_t colproj_launch(const CUtensorMap& mx, const CUtensorMap& mw, const ColArgs& args,
-                           int grid, bool pdl, cudaStream_t s) {
-  using Cfg = ColCfg<NMMA>;
-  auto kern = tc_colproj_kernel<NMMA>;
-  cudaError_t e = set_smem(kern, Cfg::kSmem);
+template <auto Kernel, typename Args>
+cudaError_t launch_sched(int grid, int cl, int smem, int smem_max, bool pdl, cudaStream_t s,
+                         const CUtensorMap& m0, const CUtensorMap& m1, const Args& args) {
+  cudaError_t e = set_smem_once<Kernel>(smem_max);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(192);
-  cfg.dynamicSmemBytes = Cfg::kSmem;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[na].val.programmaticStreamSerializationAllowed = pdl ? 1 : 0;
+  ++na;
+  if (cl > 1) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = cl;
+    attr[na].val.clusterDim.y = 1;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, mx, mw, args);
+  cfg.numAttrs = na;
+  return cudaLaunchKernelEx(&cfg, Kernel, m0, m1, args);
+}
+
+Sched to_sched(const BlockSched& b) {
+  Sched s;
+  s.cl = b.cl;
+  s.bpc = b.bpc;
+  s.nblocks = b.nblocks;
+  s.upb = b.upb;
+  return s;
 }
 
 }  // namespace
 
-int colproj_stage_chunk() { return ColCfg<32>::kChunk; }
+int rowproj_ctas_per_sm() { return 2; }
+int colproj_ctas_per_sm(int nmma) { return nmma >= 128 ? 1 : 2; }
+int colproj_stage_chunk() { return kColChunk; }
+int colproj_tile_t() { return kTileT; }
 
 cudaError_t read_device_error(int32_t* out, bool reset) {
   int v = 0;
@@ -547,50 +731,57 @@ cudaError_t read_device_error(int32_t* out, bool reset) {
 
 cudaError_t launch_tc_rowproj(const void* X, int64_t B, int64_t T, int64_t c, const void* R,
                               bool r_batched, int nmma, bool hilo_in, void* W, int64_t tpad,
-                              int* zero_ptr, size_t zero_ints, cudaStream_t s) {
+                              const BlockSched& bs, int* zero_ptr, size_t zero_ints,
+                              cudaStream_t s) {
   CUtensorMap mx, mr;
   if (!make_tmap_3d_bf16(&mx, X, c, T, B, c, T * c, kTileC, kRowTile, 128))
     return cudaErrorInvalidValue;
   if (!make_tmap_3d_bf16(&mr, R, nmma, c, r_batched ? B : 1, nmma, c * nmma, nmma, kTileC,
                          2 * nmma))
     return cudaErrorInvalidValue;
-  const int iT = static_cast<int>(T), ic = static_cast<int>(c), iB = static_cast<int>(B);
-  const int zi = static_cast<int>(zero_ints);
-  if (nmma == 16 && !hilo_in)
-    return rowproj_launch<16, false>(mx, mr, iT, ic, r_batched, iB, W, tpad, zero_ptr, zi, s);
-  if (nmma == 32 && !hilo_in)
-    return rowproj_launch<32, false>(mx, mr, iT, ic, r_batched, iB, W, tpad, zero_ptr, zi, s);
-  if (nmma == 64 && !hilo_in)
-    return rowproj_launch<64, false>(mx, mr, iT, ic, r_batched, iB, W, tpad, zero_ptr, zi, s);
-  if (nmma == 32 && hilo_in)
-    return rowproj_launch<32, true>(mx, mr, iT, ic, r_batched, iB, W, tpad, zero_ptr, zi, s);
-  if (nmma == 64 && hilo_in)
-    return rowproj_launch<64, true>(mx, mr, iT, ic, r_batched, iB, W, tpad, zero_ptr, zi, s);
+  RowArgs a;
+  a.T = static_cast<int>(T);
+  a.c = static_cast<int>(c);
+  a.mtiles = static_cast<int>((T + kRowTile - 1) / kRowTile);
+  a.sched = to_sched(bs);
+  a.r_batched = r_batched ? 1 : 0;
+  a.W = static_cast<__nv_bfloat16*>(W);
+  a.tpad = tpad;
+  a.zero_ptr = zero_ptr;
+  a.zero_ints = static_cast<int>(zero_ints);
+#define DPRC_ROW(NM, HL)                                                                 \
+  if (nmma == NM && hilo_in == HL)                                                       \
+    return launch_sched<tc_rowproj_kernel<NM, HL>>(bs.grid, bs.cl,                       \
+                                                   RowCfg<NM, HL>::smem(bs.cl),          \
+                                                   RowCfg<NM, HL>::smem(8), false, s, mx, \
+                                                   mr, a);
+  DPRC_ROW(16, false)
+  DPRC_ROW(32, false)
+  DPRC_ROW(64, false)
+  DPRC_ROW(32, true)
+  DPRC_ROW(64, true)
+#undef DPRC_ROW
   return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_tc_colproj(const void* X, int64_t B, int64_t T, int64_t c, const void* W,
-                              int64_t tpad, int n, const ColprojPlan& plan, char* ws,
-                              ColprojMode mode, float* n_out, int accumulate, int n_head,
-                              float w_tail, float* y_f32, void* y_hilo, bool pdl,
+                              int64_t tpad, int n, const BlockSched& bs, int* sample_tickets,
+                              float* chunk_norms, ColprojMode mode, float* n_out, int accumulate,
+                              int n_head, float w_tail, float* y_f32, void* y_hilo, bool pdl,
                               cudaStream_t s) {
   const int nmma = 2 * n;
   CUtensorMap mx, mw;
   if (!make_tmap_3d_bf16(&mx, X, c, T, B, c, T * c, 64, kTileT, 128))
     return cudaErrorInvalidValue;
-  if (!make_tmap_3d_bf16(&mw, W, T, nmma, B, tpad, nmma * tpad, kTileT, nmma, 128))
+  if (!make_tmap_3d_bf16(&mw, W, T, nmma, B, tpad, nmma * tpad, 64, nmma, 128))
     return cudaErrorInvalidValue;
   ColArgs a;
   a.T = static_cast<int>(T);
   a.c = static_cast<int>(c);
-  a.nchunks = plan.nchunks;
-  a.kt = plan.kt;
-  a.units = plan.units;
-  a.max_seg = plan.max_seg;
-  a.part = reinterpret_cast<float*>(ws + plan.part_off);
-  a.tickets = reinterpret_cast<int*>(ws + plan.tick_off);
-  a.sample_tickets = reinterpret_cast<int*>(ws + plan.stick_off);
-  a.chunk_norms = reinterpret_cast<float*>(ws + plan.cnorm_off);
+  a.nchunks = static_cast<int>((c + kColChunk - 1) / kColChunk);
+  a.sched = to_sched(bs);
+  a.sample_tickets = sample_tickets;
+  a.chunk_norms = chunk_norms;
   a.mode = mode;
   a.n_out = n_out;
   a.accumulate = accumulate;
@@ -598,9 +789,14 @@ cudaError_t launch_tc_colproj(const void* X, int64_t B, int64_t T, int64_t c, co
   a.w_tail = w_tail;
   a.y_f32 = y_f32;
   a.y_hilo = static_cast<__nv_bfloat16*>(y_hilo);
-  if (nmma == 32) return colproj_launch<32>(mx, mw, a, plan.grid, pdl, s);
-  if (nmma == 64) return colproj_launch<64>(mx, mw, a, plan.grid, pdl, s);
-  if (nmma == 128) return colproj_launch<128>(mx, mw, a, plan.grid, pdl, s);
+#define DPRC_COL(NM)                                                                        \
+  if (nmma == NM)                                                                           \
+    return launch_sched<tc_colproj_kernel<NM>>(bs.grid, bs.cl, ColCfg<NM>::smem(bs.cl),     \
+                                               ColCfg<NM>::smem(8), pdl, s, mx, mw, a);
+  DPRC_COL(32)
+  DPRC_COL(64)
+  DPRC_COL(128)
+#undef DPRC_COL
   return cudaErrorInvalidValue;
 }
 

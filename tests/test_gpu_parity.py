@@ -66,6 +66,9 @@ HUTCH_SHAPES = [
     (4, 4097, 256, 512, 64),       # T one past a tile; k = 64
     (1, 130, 1024, 2048, 32),
     (5, 333, 264, 1032, 32),
+    (1, 2048, 1024, 1024, 32),     # few blocks: both kernels split blocks over 8-CTA clusters
+    (3, 4096, 1024, 512, 16),      # two-CTA clusters for the sketch, four for the projection
+    (40, 256, 256, 128, 32),       # many blocks: whole blocks per CTA, several per CTA
     # float32 / CUDA-core path through the same entry point
     (4, 128, 64, 64, 8),
 ]
@@ -95,6 +98,23 @@ def test_hutch_bf16_odd_widths_use_cuda_cores():
     n = torch.zeros(2, device=DEV)
     rnc.dprc_norm_hutch(A.to(DEV), G.to(DEV), P.to(DEV), n)
     assert _relerr(n.cpu(), oracle.hutch_norm(to_f64(A), to_f64(G), to_f64(P))) < RTOL
+
+
+def test_every_tensor_core_variant_back_to_back():
+    # all sketch/projection instantiations in one process, in an order where a
+    # launch-attribute cache keyed on the wrong thing would fail
+    A, G, _ = _hutch_case(2, 300, 256, 256, 16, torch.bfloat16, seed=77)
+    Ad, Gd = A.to(DEV), G.to(DEV)
+    g = torch.Generator(device="cpu").manual_seed(78)
+    S = torch.randn(256, 16, generator=g).to(torch.bfloat16)
+    Pp = torch.randn(256, 16, generator=g).to(torch.bfloat16)
+    n = torch.zeros(2, device=DEV)
+    rnc.dprc_norm_hutchpp(Ad, Gd, S.to(DEV), Pp.to(DEV), n)
+    assert _relerr(n.cpu(), oracle.hutchpp_norm(to_f64(A), to_f64(G), to_f64(S), to_f64(Pp))) < RTOL
+    for k in (64, 16, 32):
+        P = _rand((256, k), 79 + k, torch.bfloat16, 1.0 / np.sqrt(k))
+        rnc.dprc_norm_hutch(Ad, Gd, P.to(DEV), n)
+        assert _relerr(n.cpu(), oracle.hutch_norm(to_f64(A), to_f64(G), to_f64(P))) < RTOL, k
 
 
 def test_hutch_accumulates_layerwise_sum():

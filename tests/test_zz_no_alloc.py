@@ -53,7 +53,7 @@ def _with_workspace(lib, A, G, P, n):
     B, T, d = A.shape
     p, k = P.shape
     nbytes = lib.dprc_workspace_bytes(1, 1, B, T, d, p, k)
-    ws = torch.empty(nbytes, dtype=torch.uint8, device=DEV)
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device=DEV)
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     st = lib.dprc_norm_hutch(_vp(A), _vp(G), _vp(P), 1, B, T, d, p, k, _vp(n), 0, _vp(ws),
                              nbytes, stream)
