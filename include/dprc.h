@@ -149,7 +149,9 @@ dprc_status dprc_clip_factors(const float* n, int64_t B, float C, float* c,
  * dprc_philox_words: word (e & 3) of block (e >> 2), Box-Muller on the word
  * pairs (w0, w1) and (w2, w3) with u1 = ((w_a >> 8) + 1) * 2^-24 and
  * u2 = (w_b >> 8) * 2^-24:  z_a = sqrt(-2 ln u1) cos(2 pi u2),
- * z_b = sqrt(-2 ln u1) sin(2 pi u2).  Any 1/B averaging belongs to the caller.
+ * z_b = sqrt(-2 ln u1) sin(2 pi u2), evaluated in fp32 with the hardware
+ * logarithm, sine and cosine (|error| <= 2e-6 + 1e-6 r, r = sqrt(z_a^2 + z_b^2));
+ * the integer stream itself is exact.  Any 1/B averaging belongs to the caller.
  *  grad device float [N], in place, 16-byte aligned; N >= 0; sigma >= 0.
  *  The same (seed, step) gives the same noise on every call and device.
  */

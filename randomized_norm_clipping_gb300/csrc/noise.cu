@@ -61,15 +61,40 @@ __device__ __forceinline__ uint4 philox_block(uint64_t j, uint64_t step, const R
                        rk);
 }
 
+// -2 ln(u1) for u1 = m 2^-24, m = (a >> 8) + 1 in [1, 2^24].  The hardware
+// logarithm (__logf, absolute error <= 2^-21.41 on [0.5, 2]) loses relative
+// accuracy as u1 -> 1, so for v = 1 - u1 <= 2^-5 (v exact) the Taylor series
+//   -ln(1 - v) = v (1 + v/2 + v^2/3 + ... + v^6/7)
+// is used instead (truncation below 4e-12 relative).  Both are evaluated and
+// one selected, so warps do not diverge.
+__device__ __forceinline__ float neg2log_u1(uint32_t a) {
+  const uint32_t m = (a >> 8) + 1u;
+  const uint32_t w = (1u << 24) - m;  // 2^24 v
+  const float v = static_cast<float>(w) * 5.9604644775390625e-8f;
+  float t = 0.14285714285714285f;     // 1/7
+  t = fmaf(t, v, 0.16666666666666666f);
+  t = fmaf(t, v, 0.2f);
+  t = fmaf(t, v, 0.25f);
+  t = fmaf(t, v, 0.33333333333333333f);
+  t = fmaf(t, v, 0.5f);
+  t = fmaf(t, v, 1.0f);
+  const float series = 2.0f * v * t;
+  const float u1 = static_cast<float>(m) * 5.9604644775390625e-8f;
+  const float hw = -2.0f * __logf(u1);
+  return w <= (1u << 19) ? series : hw;
+}
+
 // Box-Muller on a word pair: u1 = ((a >> 8) + 1) 2^-24 in (0, 1],
-// u2 = (b >> 8) 2^-24 in [0, 1); both exact in fp32.
+// u2 = (b >> 8) 2^-24 in [0, 1):  (r cos 2 pi u2, r sin 2 pi u2),
+// r = sqrt(-2 ln u1).  The angle is taken as x + pi with x = 2 pi (u2 - 1/2)
+// in [-pi, pi), where the hardware sine and cosine have absolute error
+// <= 2^-21.41, hence |error| <= 2e-6 + 1e-6 r for each normal.
 __device__ __forceinline__ float2 box_muller(uint32_t a, uint32_t b) {
-  const float u1 = static_cast<float>((a >> 8) + 1u) * 5.9604644775390625e-8f;  // 2^-24
-  const float u2 = static_cast<float>(b >> 8) * 5.9604644775390625e-8f;
-  const float rad = sqrtf(-2.0f * logf(u1));
+  const float rad = sqrtf(neg2log_u1(a));
+  const float t = static_cast<float>(b >> 8) * 5.9604644775390625e-8f - 0.5f;  // exact
   float s, c;
-  sincospif(2.0f * u2, &s, &c);
-  return make_float2(rad * c, rad * s);
+  __sincosf(6.283185307179586f * t, &s, &c);
+  return make_float2(-rad * c, -rad * s);
 }
 
 __device__ __forceinline__ float4 add_noise4(float4 g, uint4 w, float scale) {
