@@ -11,6 +11,12 @@ all ranks, plus the HBM roofline fraction of the dominant kernel.
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl native|reference]
   torchrun --nproc-per-node N bench.py --gpus N ...      (one rank per GPU)
 
+After the headline, the other configurations of the path are timed the same
+way and reported under "rows" (--rows all|none|c3,c4,c5,noise,exact): the
+112-layer Llama-3.2-1B step with layerwise sum, clip and noise on the
+1,235,814,400-element gradient; Hutch++; the T = 32768 up/down projections;
+the noise kernel alone; and the exact ghost norm.
+
 Ranks shard the batch (weak scaling: every rank runs its own B = 8 samples);
 the norm path has no cross-rank exchange, so the only collectives are the
 barriers and the max-over-ranks of the timed region.
@@ -150,6 +156,32 @@ def measured_peaks():
         return 6800.0, "fallback"
 
 
+def ncu_traffic(kernel):
+    """DRAM bytes per launch of the named headline kernel from the committed ncu
+    capture, or None when the kernel's sources changed since it was taken."""
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic_hutch_q_proj.json")) as f:
+            rec = json.load(f)
+        h = hashlib.sha256()
+        for src in rec["sources"]:
+            with open(os.path.join(ROOT, src), "rb") as f:
+                h.update(f.read())
+        if h.hexdigest() != rec["sources_sha256"]:
+            return None
+        return int(rec["kernels"][kernel]["dram_bytes_per_launch"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+def measured_tflops():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"])
+    except (OSError, KeyError, ValueError):
+        return 1900.0
+
+
 def headline_inputs(wk, rank, device):
     seeded = wl.Workload(**{**wk.__dict__, "seed": shard_seed(wk.seed, rank)})
     return wl.layer_inputs(seeded, 0, device=device)
@@ -281,9 +313,10 @@ def run_native(args, rank, ws, local):
     k2 = float(np.mean(k2_ms))
     peak, peak_kind = measured_peaks()
     if k2 >= k1:
-        dom, dom_ms, dom_bytes = "colproj (A^T W, ||Y||^2)", k2, pj_bytes
+        dom, dom_ms, dom_bytes, dom_key = "colproj (A^T W, ||Y||^2)", k2, pj_bytes, "colproj"
     else:
-        dom, dom_ms, dom_bytes = "rowproj (G P)", k1, sk_bytes
+        dom, dom_ms, dom_bytes, dom_key = "rowproj (G P)", k1, sk_bytes, "rowproj"
+    traffic = ncu_traffic(dom_key)
     achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
     op_achieved = (sk_bytes + pj_bytes) / (call_ms * 1e-3) / 1e9
 
@@ -343,7 +376,7 @@ def run_native(args, rank, ws, local):
         "roofline": {
             "bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
             "peak_kind": peak_kind, "unit": "GB/s", "frac": achieved / peak,
-            "traffic": None, "ms": dom_ms, "algorithmic_bytes": dom_bytes,
+            "traffic": traffic, "ms": dom_ms, "algorithmic_bytes": dom_bytes,
         },
         "roofline_op": {
             "what": "dprc_norm_hutch call (both kernels), algorithmic bytes A + G + P",
@@ -355,6 +388,10 @@ def run_native(args, rank, ws, local):
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk.summary(),
     }
+    which = set() if args.rows == "none" else (
+        {"c3", "c4", "c5", "noise", "exact"} if args.rows == "all" else set(args.rows.split(",")))
+    if which:
+        out["rows"] = measure_rows(which, device, peak, measured_tflops(), 7919 * rank)
     if rank == 0 and not args.no_cpu_baseline:
         rate, done, el = cpu_oracle_rate(A.cpu(), G.cpu(), P.cpu(), wk.C)
         out["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": os.cpu_count(),
@@ -362,6 +399,136 @@ def run_native(args, rank, ws, local):
                                "sample": f"{done} whole samples (T={T}) of the same batch, "
                                          f"{el:.1f} s, float64 numpy (BLAS threads = cores)"}
     return out
+
+
+# ---------------------------------------------------------------- other rows
+
+def graph_ms(fn, device, reps, warmup=3):
+    """Mean device time of fn captured as one CUDA graph and replayed reps times
+    back to back (queued behind a GPU sleep so host launch gaps are hidden)."""
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize(device)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    for _ in range(warmup):
+        g.replay()
+    torch.cuda.synchronize(device)
+    stream = torch.cuda.current_stream(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda._sleep(5_000_000)
+    e0.record(stream)
+    for _ in range(reps):
+        g.replay()
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    del g
+    return e0.elapsed_time(e1) / reps
+
+
+def hbm_entry(ms, nbytes, peak, **extra):
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"ms": ms, "algorithmic_bytes": nbytes, "achieved_gbs": gbs, "frac": gbs / peak,
+            **extra}
+
+
+def hutch_bytes(B, T, d, p, k, eb):
+    return B * T * (d + p) * eb + p * k * eb
+
+
+def measure_rows(which, device, peak, tflops_peak, seed_shift):
+    """Every other configuration of the path, each timed the same way as the
+    headline (a CUDA graph of the whole row, inputs resident in HBM)."""
+    import randomized_norm_clipping_gb300 as rnc
+
+    rows = {}
+
+    def inputs(wk, i):
+        seeded = wl.Workload(**{**wk.__dict__, "seed": wk.seed + seed_shift})
+        return wl.layer_inputs(seeded, i, device=device)
+
+    if "c3" in which or "noise" in which:
+        wk = wl.WORKLOADS["hutch_llama32_1b_112layers_b4_t4096_k32_bf16"]
+        grad = wl.gradient_buffer(wk.noise_elems, device=device)
+        noise_bytes = 8 * wk.noise_elems
+        t_noise = graph_ms(lambda: rnc.dprc_add_noise(grad, wk.sigma, wk.C, 1234, 1), device, 10)
+        rows["noise_1.24e9"] = hbm_entry(t_noise, noise_bytes, peak,
+                                         what="dprc_add_noise on the 1,235,814,400-element "
+                                              "fp32 Llama-3.2-1B gradient (read + write)")
+        if "c3" in which:
+            layers = [inputs(wk, i) for i in range(len(wk.layers))]
+            n = torch.zeros(wk.B, device=device)
+            c = torch.empty(wk.B, device=device)
+            wsz = max(rnc.dprc_workspace_bytes(rnc.DPRC_OP_HUTCH, rnc.DPRC_BF16, wk.B, wk.T,
+                                               lay.d, lay.p, wk.k) for lay in wk.layers)
+            wsbuf = torch.empty(wsz, dtype=torch.uint8, device=device)
+
+            def norms():
+                for i, (A, G, P) in enumerate(layers):
+                    rnc.dprc_norm_hutch(A, G, P, n, accumulate=i > 0, ws=wsbuf)
+
+            def step():
+                norms()
+                rnc.dprc_clip_factors(n, wk.C, c)
+                rnc.dprc_add_noise(grad, wk.sigma, wk.C, 1234, 1)
+
+            norm_bytes = sum(hutch_bytes(wk.B, wk.T, lay.d, lay.p, wk.k, 2) for lay in wk.layers)
+            t_norms = graph_ms(norms, device, 10)
+            t_step = graph_ms(step, device, 10)
+            rows["c3_112layers"] = hbm_entry(
+                t_step, norm_bytes + noise_bytes, peak,
+                what="112 dprc_norm_hutch calls (layerwise sum) + clip + noise, one graph",
+                tokens_per_s_per_layer=wk.B * wk.T * len(wk.layers) / (t_norms * 1e-3),
+                norms=hbm_entry(t_norms, norm_bytes, peak),
+                clip_fraction=float((c < 1).float().mean().item()),
+                launches=2 * len(wk.layers) + 2)
+            del layers, n, c, wsbuf
+        del grad
+        torch.cuda.empty_cache()
+
+    if "c4" in which:
+        wk = wl.WORKLOADS["hutchpp_q_proj_b8_t4096_r16_bf16"]
+        lay = wk.layers[0]
+        A, G, (S, P) = inputs(wk, 0)
+        n = torch.zeros(wk.B, device=device)
+        wsbuf = rnc.workspace(rnc.DPRC_OP_HUTCHPP, A, wk.B, wk.T, lay.d, lay.p, wk.k)
+        t = graph_ms(lambda: rnc.dprc_norm_hutchpp(A, G, S, P, n, ws=wsbuf), device, 20)
+        nb = 3 * wk.B * wk.T * (lay.d + lay.p) * 2 + 2 * lay.p * wk.k * 2
+        rows["c4_hutchpp"] = hbm_entry(t, nb, peak, what="dprc_norm_hutchpp, three passes + QR",
+                                       tokens_per_s=wk.B * wk.T / (t * 1e-3))
+        del A, G, S, P, n, wsbuf
+
+    if "c5" in which:
+        wk = wl.WORKLOADS["hutch_long_b2_t32768_up_down_k32_bf16"]
+        n = torch.zeros(wk.B, device=device)
+        for i, lay in enumerate(wk.layers):
+            A, G, P = inputs(wk, i)
+            wsbuf = rnc.workspace(rnc.DPRC_OP_HUTCH, A, wk.B, wk.T, lay.d, lay.p, wk.k)
+            t = graph_ms(lambda: rnc.dprc_norm_hutch(A, G, P, n, ws=wsbuf), device, 20)
+            rows[f"c5_{lay.name}"] = hbm_entry(
+                t, hutch_bytes(wk.B, wk.T, lay.d, lay.p, wk.k, 2), peak,
+                what=f"dprc_norm_hutch B2 T32768 {lay.d}->{lay.p}",
+                tokens_per_s=wk.B * wk.T / (t * 1e-3))
+            del A, G, P, wsbuf
+        del n
+
+    if "exact" in which:
+        wk = wl.WORKLOADS[wl.HEADLINE]
+        lay = wk.layers[0]
+        A, G, _ = inputs(wk, 0)
+        n = torch.zeros(wk.B, device=device)
+        wsbuf = rnc.workspace(rnc.DPRC_OP_EXACT, A, wk.B, wk.T, lay.d, lay.p, wk.k)
+        t = graph_ms(lambda: rnc.dprc_exact_norm(A, G, n, ws=wsbuf), device, 2, warmup=1)
+        flops = wk.B * 2 * wk.T * wk.T * (lay.d + lay.p)
+        tf = flops / (t * 1e-3) / 1e12
+        rows["exact_c2"] = {"ms": t, "algorithmic_flops": flops, "achieved_tflops": tf,
+                            "bound": "tensor", "frac": tf / tflops_peak,
+                            "what": "dprc_exact_norm (tiled ghost norm) on the q_proj batch; "
+                                    "flops as 2 T^2 (d + p) per sample"}
+        del A, G, n, wsbuf
+    torch.cuda.empty_cache()
+    return rows
 
 
 # ---------------------------------------------------------------- reference arm
@@ -407,6 +574,9 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--rows", default="all",
+                    help="other configurations to time after the headline: all, none, or a "
+                         "comma list of c3,c4,c5,noise,exact")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3

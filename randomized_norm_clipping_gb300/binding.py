@@ -128,8 +128,8 @@ def dprc_workspace_bytes(op, dtype_code, B, T, d, p, k):
 
 
 def workspace(op, like, B, T, d, p, k):
-    """A zeroed device byte buffer of dprc_workspace_bytes(...) (torch
-    allocation); its leading counter block must start at zero."""
+    """A device byte buffer of dprc_workspace_bytes(...) bytes (torch
+    allocation; the library needs no particular initial contents)."""
     n = dprc_workspace_bytes(op, _dtype_code(like), B, T, d, p, k)
     if n == 0:
         raise DprcError("dprc_workspace_bytes", 2)

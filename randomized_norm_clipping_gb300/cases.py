@@ -1,0 +1,107 @@
+"""Run one named case of the library a few times, for profilers.
+
+    python -m randomized_norm_clipping_gb300.cases NAME [--reps R] [--warmup W]
+
+Each case draws its seeded inputs on the current GPU, calls one entry point
+W + R times on the current stream and prints the mean device time of the last
+R calls.  The cases are the benchmark's configurations (or a stated smaller
+slice of one, sized to stay above the 126 MB L2 so DRAM counters still mean
+something), so a profiler run such as
+
+    ncu --set full --clock-control none -k regex:colproj -s 2 -c 1 \\
+        python -m randomized_norm_clipping_gb300.cases hutch_q_proj
+
+captures one launch of the kernel on the workload the benchmark times.
+"""
+
+from __future__ import annotations
+
+import argparse
+
+import torch
+
+from . import binding as rnc
+from . import workloads as wl
+
+
+def _hutch(name, layer=0):
+    wk = wl.WORKLOADS[name]
+    lay = wk.layers[layer]
+    A, G, P = wl.layer_inputs(wk, layer, device="cuda")
+    n = torch.zeros(wk.B, device="cuda")
+    ws = rnc.workspace(rnc.DPRC_OP_HUTCH, A, wk.B, wk.T, lay.d, lay.p, wk.k)
+    return lambda: rnc.dprc_norm_hutch(A, G, P, n, ws=ws)
+
+
+def _hutchpp():
+    wk = wl.WORKLOADS["hutchpp_q_proj_b8_t4096_r16_bf16"]
+    lay = wk.layers[0]
+    A, G, (S, P) = wl.layer_inputs(wk, 0, device="cuda")
+    n = torch.zeros(wk.B, device="cuda")
+    ws = rnc.workspace(rnc.DPRC_OP_HUTCHPP, A, wk.B, wk.T, lay.d, lay.p, wk.k)
+    return lambda: rnc.dprc_norm_hutchpp(A, G, S, P, n, ws=ws)
+
+
+def _noise(n_elems):
+    grad = wl.gradient_buffer(n_elems, device="cuda")
+    return lambda: rnc.dprc_add_noise(grad, 1.0, 1.0, 1234, 1)
+
+
+def _exact(B, T):
+    wk = wl.WORKLOADS[wl.HEADLINE]
+    lay = wk.layers[0]
+    A, G, _ = wl.layer_inputs(wk, 0, device="cuda", B=B, T=T)
+    n = torch.zeros(B, device="cuda")
+    ws = rnc.workspace(rnc.DPRC_OP_EXACT, A, B, T, lay.d, lay.p, wk.k)
+    return lambda: rnc.dprc_exact_norm(A, G, n, ws=ws)
+
+
+def _clip():
+    n = torch.rand(8, device="cuda") * 4.0
+    c = torch.empty(8, device="cuda")
+    return lambda: rnc.dprc_clip_factors(n, 1.0, c)
+
+
+CASES = {
+    # B8 T4096 d = p = 2048 k32 bf16 (268 MB of A and G)
+    "hutch_q_proj": lambda: _hutch("hutch_q_proj_b8_t4096_k32_bf16"),
+    # B2 T32768 2048 -> 8192 and 8192 -> 2048, k32 bf16 (1.34 GB each)
+    "hutch_long_up": lambda: _hutch("hutch_long_b2_t32768_up_down_k32_bf16", 0),
+    "hutch_long_down": lambda: _hutch("hutch_long_b2_t32768_up_down_k32_bf16", 1),
+    # Hutch++ B8 T4096 d = p = 2048 r16 bf16
+    "hutchpp_q_proj": _hutchpp,
+    # the noise kernel on 2^27 fp32 elements (1.07 GB read + written), a slice of
+    # the 1,235,814,400-element gradient: same per-element work, fewer elements
+    "noise_2p27": lambda: _noise(1 << 27),
+    "noise_llama32_1b": lambda: _noise(wl.LLAMA32_1B_PARAMS),
+    # exact ghost norm on 2 samples of the q_proj batch, T = 1024
+    "exact_q_proj_b2_t1024": lambda: _exact(2, 1024),
+    "clip_b8": _clip,
+}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("case", choices=sorted(CASES))
+    ap.add_argument("--reps", type=int, default=3)
+    ap.add_argument("--warmup", type=int, default=2)
+    args = ap.parse_args(argv)
+    fn = CASES[args.case]()
+    for _ in range(args.warmup):
+        fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.reps):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    err = rnc.dprc_device_error()
+    print(f"{args.case}: {e0.elapsed_time(e1) / max(args.reps, 1) * 1e3:.1f} us per call "
+          f"(mean of {args.reps}), device error {err}")
+    if err != 0:
+        raise SystemExit(1)
+
+
+if __name__ == "__main__":
+    main()
