@@ -520,12 +520,16 @@ def measure_rows(which, device, peak, tflops_peak, seed_shift):
         n = torch.zeros(wk.B, device=device)
         wsbuf = rnc.workspace(rnc.DPRC_OP_EXACT, A, wk.B, wk.T, lay.d, lay.p, wk.k)
         t = graph_ms(lambda: rnc.dprc_exact_norm(A, G, n, ws=wsbuf), device, 2, warmup=1)
-        flops = wk.B * 2 * wk.T * wk.T * (lay.d + lay.p)
+        # bf16 q_proj shapes take the direct form A_i^T G_i on tensor cores:
+        # 2 T d p flops per sample (the ghost form would need 2 T^2 (d + p))
+        flops = wk.B * 2 * wk.T * lay.d * lay.p
         tf = flops / (t * 1e-3) / 1e12
         rows["exact_c2"] = {"ms": t, "algorithmic_flops": flops, "achieved_tflops": tf,
-                            "bound": "tensor", "frac": tf / tflops_peak,
-                            "what": "dprc_exact_norm (tiled ghost norm) on the q_proj batch; "
-                                    "flops as 2 T^2 (d + p) per sample"}
+                            "bound": "tensor", "peak_tflops": tflops_peak,
+                            "frac": tf / tflops_peak,
+                            "ghost_form_flops": wk.B * 2 * wk.T * wk.T * (lay.d + lay.p),
+                            "what": "dprc_exact_norm on the q_proj batch, direct form on "
+                                    "tensor cores; flops 2 T d p per sample"}
         del A, G, n, wsbuf
     torch.cuda.empty_cache()
     return rows

@@ -123,11 +123,19 @@ dprc_status dprc_norm_hutchpp(const void* A, const void* G, const void* S, const
                               void* stream);
 
 /*
- * Exact squared norm by the ghost-clipping identity (the comparison path the
- * pages set the method against; papernotes.org, "Research background"):
- *     n_i = sum_{t,s} (A_i A_i^T)_{ts} (G_i G_i^T)_{ts}
- * computed tile by tile; no T x T matrix is stored.  O(T^2 (d + p)) work.
- * Arguments as dprc_norm_hutch without P and k.
+ * Exact squared norm n_i = ||A_i^T G_i||_F^2, the quantity the estimators
+ * approximate (the comparison path the pages set the method against;
+ * papernotes.org, "Research background" and "Key design"), by one of its two
+ * exact forms:
+ *   - bf16 with d and p multiples of 8: the direct form on tensor cores, the
+ *     d x p product A_i^T G_i formed in 128 x 256 tiles in on-chip memory and
+ *     squared there (never stored), O(T d p) work;
+ *   - otherwise the ghost-clipping identity
+ *         n_i = sum_{t,s} (A_i A_i^T)_{ts} (G_i G_i^T)_{ts}
+ *     tile by tile on CUDA cores (no T x T matrix stored), O(T^2 (d + p)).
+ * Both sum in a fixed order (bitwise repeatable).  Arguments as
+ * dprc_norm_hutch without P and k; the workspace size comes from
+ * dprc_workspace_bytes(DPRC_OP_EXACT, ...).
  */
 dprc_status dprc_exact_norm(const void* A, const void* G, dprc_dtype dtype, int64_t B,
                             int64_t T, int64_t d, int64_t p, float* n, int accumulate,

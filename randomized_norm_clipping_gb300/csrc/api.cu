@@ -170,7 +170,15 @@ SimtPlan plan_simt(dprc_op op, int64_t B, int64_t T, int64_t d, int64_t p, int64
   return s;
 }
 
-size_t plan_exact_bytes(int64_t B, int64_t T) {
+// The direct form on tensor cores when the layout allows it (bf16, rows of d
+// and p 16-byte multiples for TMA), else the ghost form on CUDA cores.
+bool exact_direct_tc(dprc_dtype dt, int64_t d, int64_t p) {
+  return dt == DPRC_BF16 && d % 8 == 0 && p % 8 == 0;
+}
+
+size_t plan_exact_bytes(dprc_dtype dt, int64_t B, int64_t T, int64_t d, int64_t p) {
+  if (exact_direct_tc(dt, d, p))
+    return align_up(static_cast<size_t>(fgc_partials(B, d, p)) * 4, 1024);
   const int64_t nt = (T + 31) / 32;
   return align_up(static_cast<size_t>(B) * nt * nt * 4, 1024);
 }
@@ -270,7 +278,7 @@ size_t dprc_workspace_bytes(dprc_op op, dprc_dtype dtype, int64_t B, int64_t T, 
       if (k < 1 || k > 64 || k > p) return 0;
       return hutchpp_ws(dtype, B, T, d, p, k);
     case DPRC_OP_EXACT:
-      return plan_exact_bytes(B, T);
+      return plan_exact_bytes(dtype, B, T, d, p);
   }
   return 0;
 }
@@ -420,16 +428,19 @@ dprc_status dprc_exact_norm(const void* A, const void* G, dprc_dtype dtype, int6
   if (!A || !G || !n) return DPRC_ERR_NULL;
   dprc_status st = check_common(dtype, B, T, d, p);
   if (st != DPRC_OK) return st;
-  if (T > 65535 * 32) return DPRC_ERR_SHAPE;
+  if (!exact_direct_tc(dtype, d, p) && T > 65535 * 32) return DPRC_ERR_SHAPE;  // ghost grid
   if (!aligned16(A) || !aligned16(G) || !aligned16(n)) return DPRC_ERR_ALIGN;
   if (!ws) return DPRC_ERR_WORKSPACE;
   if (!aligned16(ws)) return DPRC_ERR_ALIGN;
-  if (ws_bytes < plan_exact_bytes(B, T)) return DPRC_ERR_WORKSPACE;
+  if (ws_bytes < plan_exact_bytes(dtype, B, T, d, p)) return DPRC_ERR_WORKSPACE;
   if (!device_ok()) return DPRC_ERR_DEVICE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   mark(0, s);
-  cudaError_t e = launch_exact_ghost(A, G, dtype, B, T, d, p, static_cast<float*>(ws), n,
-                                     accumulate, s);
+  cudaError_t e =
+      exact_direct_tc(dtype, d, p)
+          ? launch_tc_exact_direct(A, G, B, T, d, p, static_cast<float*>(ws), n, accumulate, s)
+          : launch_exact_ghost(A, G, dtype, B, T, d, p, static_cast<float*>(ws), n, accumulate,
+                               s);
   mark(1, s);
   return cuda_status(e);
 }

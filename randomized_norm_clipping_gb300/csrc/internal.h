@@ -60,7 +60,7 @@ BlockSched colproj_sched(int64_t B, int64_t T, int64_t c, int nmma);
 
 TcPlan plan_tc(dprc_op op, int64_t B, int64_t T, int64_t d, int64_t p, int64_t k);
 SimtPlan plan_simt(dprc_op op, int64_t B, int64_t T, int64_t d, int64_t p, int64_t k);
-size_t plan_exact_bytes(int64_t B, int64_t T);
+size_t plan_exact_bytes(dprc_dtype dt, int64_t B, int64_t T, int64_t d, int64_t p);
 
 // ---- tensor maps -----------------------------------------------------------
 // 3-D bf16 tensor map over [dim2][dim1][dim0] (dim0 contiguous) with row
@@ -112,6 +112,17 @@ cudaError_t launch_qr_project(const float* M, int64_t B, int64_t p, int r, const
                               cudaStream_t s);
 
 // Exact (ghost) norm, SIMT fp32, deterministic.
+// Exact norm on tensor cores by the direct form: per sample, 128 x 256 tiles
+// of A_i^T G_i accumulated over T in TMEM and squared in the epilogue; one
+// partial per tile (fgc_partials(B, d, p) floats), summed per sample in index
+// order into n_out.  bf16, d and p multiples of 8.
+int64_t fgc_partials(int64_t B, int64_t d, int64_t p);
+cudaError_t launch_tc_exact_direct(const void* A, const void* G, int64_t B, int64_t T, int64_t d,
+                                   int64_t p, float* partials, float* n_out, int accumulate,
+                                   cudaStream_t s);
+// n_out[i] (+)= sum of partials[i * per_sample .. (i + 1) * per_sample), fixed order.
+cudaError_t launch_partials_finish(const float* partials, int64_t B, int64_t per_sample,
+                                   float* n_out, int accumulate, cudaStream_t s);
 cudaError_t launch_exact_ghost(const void* A, const void* G, dprc_dtype dt, int64_t B,
                                int64_t T, int64_t d, int64_t p, float* partials, float* n_out,
                                int accumulate, cudaStream_t s);

@@ -257,6 +257,13 @@ cudaError_t launch_simt_norm_finish(const float* Y, int64_t B, int64_t c, int n,
   return cudaGetLastError();
 }
 
+cudaError_t launch_partials_finish(const float* partials, int64_t B, int64_t per_sample,
+                                   float* n_out, int accumulate, cudaStream_t s) {
+  exact_finish_kernel<<<static_cast<unsigned>(B), 256, 0, s>>>(
+      partials, static_cast<long long>(per_sample), n_out, accumulate);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_exact_ghost(const void* A, const void* G, dprc_dtype dt, int64_t B,
                                int64_t T, int64_t d, int64_t p, float* partials, float* n_out,
                                int accumulate, cudaStream_t s) {

@@ -58,7 +58,12 @@ def test_workspace_bytes_host_only(lib):
     ws32 = b.dprc_workspace_bytes(b.DPRC_OP_HUTCH, b.DPRC_F32, 4, 128, 64, 64, 8)
     assert ws32 >= 4 * 128 * 8 * 4
     assert b.dprc_workspace_bytes(b.DPRC_OP_HUTCHPP, b.DPRC_BF16, 8, 4096, 2048, 2048, 16) > 0
-    assert b.dprc_workspace_bytes(b.DPRC_OP_EXACT, b.DPRC_BF16, 2, 4096, 64, 64, 0) >= 2 * 128 * 128 * 4
+    # exact norm: bf16 with aligned widths takes the direct tensor-core form
+    # (one fp32 partial per 128 x 256 tile of A^T G); fp32 or odd widths the
+    # ghost form (one partial per pair of 32-token tiles)
+    assert b.dprc_workspace_bytes(b.DPRC_OP_EXACT, b.DPRC_BF16, 2, 4096, 2048, 2048, 0) >= 2 * 16 * 8 * 4
+    assert b.dprc_workspace_bytes(b.DPRC_OP_EXACT, b.DPRC_F32, 2, 4096, 64, 64, 0) >= 2 * 128 * 128 * 4
+    assert b.dprc_workspace_bytes(b.DPRC_OP_EXACT, b.DPRC_BF16, 2, 4096, 63, 64, 0) >= 2 * 128 * 128 * 4
     # invalid sizes give 0
     assert b.dprc_workspace_bytes(b.DPRC_OP_HUTCH, b.DPRC_BF16, 0, 4096, 2048, 2048, 32) == 0
     assert b.dprc_workspace_bytes(b.DPRC_OP_HUTCH, b.DPRC_BF16, 1, 4096, 2048, 2048, 0) == 0

@@ -179,15 +179,46 @@ def test_hutchpp_exact_on_low_rank_gradients():
 
 # ------------------------------------------------------------------ exact norm
 
+# bf16 with d, p multiples of 8 takes the tensor-core direct form (128 x 256
+# tiles of A^T G); fp32 or other widths take the ghost form on CUDA cores.
 @pytest.mark.parametrize("B,T,d,p,dtype", [(4, 128, 64, 64, torch.float32),
                                            (2, 333, 96, 40, torch.bfloat16),
+                                           (2, 333, 97, 41, torch.bfloat16),
                                            (1, 1, 8, 8, torch.bfloat16),
-                                           (2, 1024, 512, 256, torch.bfloat16)])
+                                           (2, 1024, 512, 256, torch.bfloat16),
+                                           (3, 1000, 392, 600, torch.bfloat16),
+                                           (1, 4097, 128, 256, torch.bfloat16),
+                                           (5, 64, 1024, 1536, torch.bfloat16)])
 def test_exact_norm_matches_oracle(B, T, d, p, dtype):
     A = _rand((B, T, d), 60 + T, dtype)
     G = _rand((B, T, p), 61 + T, dtype, 0.05)
     n = torch.zeros(B, device=DEV)
     rnc.dprc_exact_norm(A.to(DEV), G.to(DEV), n)
+    assert _relerr(n.cpu(), oracle.exact_norm(to_f64(A), to_f64(G))) < RTOL
+
+
+def test_exact_norm_accumulates_and_repeats():
+    A = _rand((3, 700, 264), 70, torch.bfloat16)
+    G = _rand((3, 700, 520), 71, torch.bfloat16, 0.05)
+    Ad, Gd = A.to(DEV), G.to(DEV)
+    ref = oracle.exact_norm(to_f64(A), to_f64(G))
+    n = torch.full((3,), 2.5, device=DEV)
+    rnc.dprc_exact_norm(Ad, Gd, n, accumulate=True)
+    assert _relerr(n.cpu(), ref + 2.5) < RTOL
+    rnc.dprc_exact_norm(Ad, Gd, n, accumulate=False)
+    once = n.clone()
+    rnc.dprc_exact_norm(Ad, Gd, n, accumulate=False)
+    assert torch.equal(n, once)  # fixed summation order: bitwise repeatable
+    assert _relerr(n.cpu(), ref) < RTOL
+
+
+def test_exact_norm_full_size_samples():
+    # two samples of the q_proj workload (T = 4096, d = p = 2048), the launch
+    # configuration the benchmark's exact-norm row times with B = 8
+    wk = wl.WORKLOADS[wl.HEADLINE]
+    A, G, _ = wl.layer_inputs(wk, 0, device=DEV, B=2)
+    n = torch.zeros(2, device=DEV)
+    rnc.dprc_exact_norm(A, G, n)
     assert _relerr(n.cpu(), oracle.exact_norm(to_f64(A), to_f64(G))) < RTOL
 
 
