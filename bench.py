@@ -462,7 +462,7 @@ def measure_rows(which, device, peak, tflops_peak, seed_shift):
             c = torch.empty(wk.B, device=device)
             wsz = max(rnc.dprc_workspace_bytes(rnc.DPRC_OP_HUTCH, rnc.DPRC_BF16, wk.B, wk.T,
                                                lay.d, lay.p, wk.k) for lay in wk.layers)
-            wsbuf = torch.empty(wsz, dtype=torch.uint8, device=device)
+            wsbuf = torch.zeros(wsz, dtype=torch.uint8, device=device)
 
             def norms():
                 for i, (A, G, P) in enumerate(layers):

@@ -22,8 +22,13 @@
  *  - Pointers named as device pointers must point to device memory (or
  *    managed memory) that stays valid until the enqueued work completes.  The
  *    library never allocates or frees memory.  Scratch memory is passed in as
- *    `ws` (see dprc_workspace_bytes); its contents need no initialisation and
- *    are garbage after a call (each call clears the counters it uses).
+ *    `ws` (see dprc_workspace_bytes).  Zero a workspace once before its first
+ *    use (e.g. cudaMemsetAsync): it starts with a block of per-sample
+ *    counters that must read zero when a call begins.  Every call that ends
+ *    without a device error (dprc_device_error) leaves that block zero again,
+ *    so one workspace serves any sequence of calls of any sizes that fit it;
+ *    after a device error, zero it again.  The rest of its contents are
+ *    scratch.
  *  - `stream` is a cudaStream_t passed as void*; NULL means the legacy default
  *    stream.  Calls only enqueue work and return; results are ready when the
  *    stream reaches them.  Calls on different streams may run concurrently
@@ -187,6 +192,7 @@ dprc_status dprc_philox_words(uint32_t* out, int64_t n_blocks, uint64_t first_bl
 #define DPRC_DEVERR_PIPE_EMPTY 2  /* producer waited too long for a free stage */
 #define DPRC_DEVERR_ACCUM 3       /* epilogue waited too long for the accumulator */
 #define DPRC_DEVERR_CLUSTER 4     /* a CTA waited too long for its cluster peers' partials */
+#define DPRC_DEVERR_READY 5       /* the projection waited too long for a sample's sketch */
 dprc_status dprc_device_error(int32_t* out, int reset);
 
 /*
@@ -222,9 +228,10 @@ dprc_status dprc_set_phase_events(void** events, int n_events);
  * first call on a device before any stream capture.
  *
  * Sharing: every call on a device uses the same array, which keeps the last
- * call's contents; nothing in it needs to start at zero (the kernels clear the
- * counters they use at the start of each call), so no stale state carries
- * over.  Calls that can overlap on the
+ * call's contents.  Its leading counter block must read zero when a call
+ * begins, so each call first clears it on `stream` (cudaMemsetAsync, which
+ * allocates nothing); no stale state from an earlier call, even one that hit
+ * a device error, carries over.  Calls that can overlap on the
  * GPU (different streams, or different host threads) race on the array: the
  * caller must order them.  Arguments and results otherwise as dprc_norm_hutch.
  */

@@ -121,13 +121,18 @@ bool tc_path_supported(dprc_dtype dt, int64_t B, int64_t T, int64_t d, int64_t p
   return k == 16 || k == 32 || k == 64;
 }
 
+// Every plan starts with the same counter block: per-sample tickets and
+// sketch-ready counters, int32 [B] each.  Calls leave it zeroed; the fused
+// Hutchinson kernel relies on that, so no other buffer may overlap it.
+size_t ctrl_bytes(int64_t B) { return align_up(static_cast<size_t>(B) * 8, 256); }
+
 TcPlan plan_tc(dprc_op op, int64_t B, int64_t T, int64_t d, int64_t p, int64_t k) {
   TcPlan t;
   t.tpad = tpad_of(T);
   const int64_t nch = (std::max(d, p) + colproj_stage_chunk() - 1) / colproj_stage_chunk();
-  size_t off = 0;
-  t.stick_off = off;
-  off = align_up(off + static_cast<size_t>(B) * 4, 256);
+  t.stick_off = 0;
+  t.ready_off = static_cast<size_t>(B) * 4;
+  size_t off = ctrl_bytes(B);
   t.cnorm_off = off;
   off = align_up(off + static_cast<size_t>(B) * nch * 4, 1024);
   t.w_bytes = static_cast<size_t>(B) * (op == DPRC_OP_HUTCH ? 2 * k : 4 * k) * t.tpad * 2;
@@ -151,7 +156,7 @@ TcPlan plan_tc(dprc_op op, int64_t B, int64_t T, int64_t d, int64_t p, int64_t k
 SimtPlan plan_simt(dprc_op op, int64_t B, int64_t T, int64_t d, int64_t p, int64_t k) {
   SimtPlan s;
   const int64_t wide = op == DPRC_OP_HUTCHPP ? 2 * k : k;
-  size_t off = 0;
+  size_t off = ctrl_bytes(B);
   s.w_off = off;
   off = align_up(off + static_cast<size_t>(B) * T * wide * 4, 1024);
   s.y_off = off;
@@ -176,11 +181,13 @@ bool exact_direct_tc(dprc_dtype dt, int64_t d, int64_t p) {
   return dt == DPRC_BF16 && d % 8 == 0 && p % 8 == 0;
 }
 
+size_t exact_partials_off(int64_t B) { return align_up(ctrl_bytes(B), 1024); }
+
 size_t plan_exact_bytes(dprc_dtype dt, int64_t B, int64_t T, int64_t d, int64_t p) {
   if (exact_direct_tc(dt, d, p))
-    return align_up(static_cast<size_t>(fgc_partials(B, d, p)) * 4, 1024);
+    return exact_partials_off(B) + align_up(static_cast<size_t>(fgc_partials(B, d, p)) * 4, 1024);
   const int64_t nt = (T + 31) / 32;
-  return align_up(static_cast<size_t>(B) * nt * nt * 4, 1024);
+  return exact_partials_off(B) + align_up(static_cast<size_t>(B) * nt * nt * 4, 1024);
 }
 
 // ---- tensor maps ------------------------------------------------------------
@@ -310,6 +317,19 @@ dprc_status dprc_norm_hutch(const void* A, const void* G, const void* P, dprc_dt
     int* stick = reinterpret_cast<int*>(w + t.stick_off);
     float* cnorm = reinterpret_cast<float*>(w + t.cnorm_off);
     mark(0, s);
+    if (fused_hutch_supported(k)) {
+      // one launch: sketch and projection as two phases of one kernel
+      bool launched = false;
+      cudaError_t e = launch_tc_hutch_fused(A, G, P, B, T, d, p, k, w + t.w_off, t.tpad,
+                                            reinterpret_cast<int*>(w + t.ready_off), stick, cnorm,
+                                            n, accumulate, s, &launched);
+      if (launched) {
+        mark(1, s);
+        mark(2, s);
+        return cuda_status(e);
+      }
+      if (e != cudaSuccess) (void)cudaGetLastError();  // not launched: two kernels below
+    }
     cudaError_t e = launch_tc_rowproj(G, B, T, p, P, false, ik, false, w + t.w_off, t.tpad,
                                       rowproj_sched(B, T, p, ik), stick, B, s);
     if (e != cudaSuccess) return DPRC_ERR_CUDA;
@@ -436,11 +456,11 @@ dprc_status dprc_exact_norm(const void* A, const void* G, dprc_dtype dtype, int6
   if (!device_ok()) return DPRC_ERR_DEVICE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   mark(0, s);
+  float* partials = reinterpret_cast<float*>(static_cast<char*>(ws) + exact_partials_off(B));
   cudaError_t e =
       exact_direct_tc(dtype, d, p)
-          ? launch_tc_exact_direct(A, G, B, T, d, p, static_cast<float*>(ws), n, accumulate, s)
-          : launch_exact_ghost(A, G, dtype, B, T, d, p, static_cast<float*>(ws), n, accumulate,
-                               s);
+          ? launch_tc_exact_direct(A, G, B, T, d, p, partials, n, accumulate, s)
+          : launch_exact_ghost(A, G, dtype, B, T, d, p, partials, n, accumulate, s);
   mark(1, s);
   return cuda_status(e);
 }
@@ -485,7 +505,18 @@ dprc_status dprc_philox_words(uint32_t* out, int64_t n_blocks, uint64_t first_bl
 dprc_status dprc_device_error(int32_t* out, int reset) {
   if (!out) return DPRC_ERR_NULL;
   if (!device_ok()) return DPRC_ERR_DEVICE;
-  return cuda_status(read_device_error(out, reset != 0));
+  cudaError_t (*const readers[])(int32_t*, bool) = {read_device_error_proj,
+                                                     read_device_error_hutch,
+                                                     read_device_error_exact};
+  int32_t first = 0;
+  for (auto rd : readers) {
+    int32_t v = 0;
+    const cudaError_t e = rd(&v, reset != 0);
+    if (e != cudaSuccess) return cuda_status(e);
+    if (first == 0) first = v;
+  }
+  *out = first;
+  return DPRC_OK;
 }
 
 }  // extern "C"

@@ -21,6 +21,21 @@ namespace dprc {
 // ---------------------------------------------------------------------------
 static __device__ int g_device_error = 0;
 
+// Host side: reads (and with `reset` clears) this translation unit's copy of
+// the error word.  Every unit whose kernels wait exposes one of these, and
+// dprc_device_error() combines them.
+static inline cudaError_t read_tu_device_error(int32_t* out, bool reset) {
+  int v = 0;
+  cudaError_t e = cudaMemcpyFromSymbol(&v, g_device_error, sizeof(int));
+  if (e != cudaSuccess) return e;
+  if (reset && v != 0) {
+    const int z = 0;
+    e = cudaMemcpyToSymbol(g_device_error, &z, sizeof(int));
+  }
+  *out = v;
+  return e;
+}
+
 // Upper bound on any single in-kernel wait (ns of %globaltimer).
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
 
@@ -320,6 +335,32 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 __device__ __forceinline__ void split_hilo(float x, __nv_bfloat16& hi, __nv_bfloat16& lo) {
   hi = __float2bfloat16_rn(x);
   lo = __float2bfloat16_rn(x - __bfloat162float(hi));
+}
+
+// Round a shared-memory pointer up to the 1024-byte alignment that 128-byte
+// swizzled tiles need.
+__device__ __forceinline__ uint8_t* align_1024(uint8_t* p) {
+  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+// Loads `NC` consecutive fp32 TMEM columns of this thread's lane.
+template <int NC>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float* v) {
+  static_assert(NC % 16 == 0, "columns in multiples of 16");
+#pragma unroll
+  for (int c0 = 0; c0 < NC; c0 += (NC % 32 == 0 ? 32 : 16)) {
+    if constexpr (NC % 32 == 0) {
+      float t[32];
+      tmem_ld_32cols(taddr + c0, t);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[c0 + j] = t[j];
+    } else {
+      float t[16];
+      tmem_ld_16cols(taddr + c0, t);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) v[c0 + j] = t[j];
+    }
+  }
 }
 
 template <typename T>

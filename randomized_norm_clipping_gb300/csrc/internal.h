@@ -26,7 +26,8 @@ BlockSched make_block_sched(int64_t nblocks, int upb, int slots);
 // Scratch layout of the tensor-core path of one Hutchinson or Hutch++ call.
 struct TcPlan {
   int64_t tpad = 0;           // row stride (elements) of the [B][2n][tpad] sketches
-  size_t stick_off = 0;       // per-sample tickets int32 [B] (cleared by every sketch kernel)
+  size_t stick_off = 0;       // per-sample tickets int32 [B] (zero between calls)
+  size_t ready_off = 0;       // per-sample sketch-ready counters int32 [B] (zero between calls)
   size_t cnorm_off = 0;       // per-block squared norms fp32 [B * chunks]
   size_t w_off = 0, w_bytes = 0;  // sketch G P (or G S, A Z, G [Q|P']) hi/lo bf16
   size_t z_off = 0;           // Hutch++: Z hi/lo bf16 [B][d][2r]
@@ -52,12 +53,18 @@ int rowproj_ctas_per_sm();
 int colproj_ctas_per_sm(int nmma);
 int colproj_stage_chunk();
 int colproj_tile_t();
-cudaError_t read_device_error(int32_t* out, bool reset);
+// Device error words of the translation units whose kernels wait (see
+// common.cuh); dprc_device_error() reports the first nonzero one.
+cudaError_t read_device_error_proj(int32_t* out, bool reset);
+cudaError_t read_device_error_exact(int32_t* out, bool reset);
+cudaError_t read_device_error_hutch(int32_t* out, bool reset);
 bool tc_path_supported(dprc_dtype dt, int64_t B, int64_t T, int64_t d, int64_t p, int64_t k,
                        bool hutchpp);
 BlockSched rowproj_sched(int64_t B, int64_t T, int64_t c, int nmma);
 BlockSched colproj_sched(int64_t B, int64_t T, int64_t c, int nmma);
 
+// Bytes of the counter block every workspace starts with (zero between calls).
+size_t ctrl_bytes(int64_t B);
 TcPlan plan_tc(dprc_op op, int64_t B, int64_t T, int64_t d, int64_t p, int64_t k);
 SimtPlan plan_simt(dprc_op op, int64_t B, int64_t T, int64_t d, int64_t p, int64_t k);
 size_t plan_exact_bytes(dprc_dtype dt, int64_t B, int64_t T, int64_t d, int64_t p);
@@ -117,6 +124,15 @@ cudaError_t launch_qr_project(const float* M, int64_t B, int64_t p, int r, const
 // partial per tile (fgc_partials(B, d, p) floats), summed per sample in index
 // order into n_out.  bf16, d and p multiples of 8.
 int64_t fgc_partials(int64_t B, int64_t d, int64_t p);
+// Fused Hutchinson (sketch and projection as two phases of one cooperative
+// launch), k = 16 or 32.  Returns cudaSuccess with *launched false when the
+// kernel cannot run with this shape or device (the caller then uses the two
+// kernels); ready and tickets must be zero and are zero again afterwards.
+bool fused_hutch_supported(int64_t k);
+cudaError_t launch_tc_hutch_fused(const void* A, const void* G, const void* P, int64_t B,
+                                  int64_t T, int64_t d, int64_t p, int64_t k, void* W,
+                                  int64_t tpad, int* ready, int* tickets, float* chunk_norms,
+                                  float* n_out, int accumulate, cudaStream_t s, bool* launched);
 cudaError_t launch_tc_exact_direct(const void* A, const void* G, int64_t B, int64_t T, int64_t d,
                                    int64_t p, float* partials, float* n_out, int accumulate,
                                    cudaStream_t s);

@@ -18,6 +18,7 @@
 #include <mutex>
 
 #include "dprc.h"
+#include "internal.h"
 
 namespace {
 
@@ -59,6 +60,10 @@ extern "C" dprc_status dprc_norm_hutch_noalloc(const void* A, const void* G, con
   void* ws = nullptr;
   const dprc_status st = scratch_address(&ws);
   if (st != DPRC_OK) return st;
+  // the counters at the front of the scratch must start at zero
+  if (cudaMemsetAsync(ws, 0, dprc::ctrl_bytes(B), static_cast<cudaStream_t>(stream)) !=
+      cudaSuccess)
+    return DPRC_ERR_CUDA;
   return dprc_norm_hutch(A, G, P, dtype, B, T, d, p, k, n, accumulate, ws,
                          static_cast<size_t>(DPRC_NOALLOC_SCRATCH_BYTES), stream);
 }

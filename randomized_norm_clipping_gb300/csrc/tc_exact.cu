@@ -51,10 +51,6 @@ struct FgcArgs {
   float* partials;      // [ntiles]
 };
 
-__device__ __forceinline__ uint8_t* align_1024(uint8_t* p) {
-  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
-}
-
 __global__ void __launch_bounds__(192, 1)
     tc_fgc_norm_kernel(const __grid_constant__ CUtensorMap map_a,
                        const __grid_constant__ CUtensorMap map_g, const FgcArgs a) {
@@ -236,6 +232,10 @@ cudaError_t set_fgc_smem_once() {
 }
 
 }  // namespace
+
+cudaError_t read_device_error_exact(int32_t* out, bool reset) {
+  return read_tu_device_error(out, reset);
+}
 
 int64_t fgc_partials(int64_t B, int64_t d, int64_t p) {
   return B * ((d + kFgcM - 1) / kFgcM) * ((p + kFgcN - 1) / kFgcN);

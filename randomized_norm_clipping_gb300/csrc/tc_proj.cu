@@ -45,30 +45,6 @@ constexpr int kTileC = 64;      // c per row-projection unit (128 B of bf16)
 constexpr int kColChunk = 128;  // output rows per column-projection block (MMA M)
 constexpr int kTileT = 128;     // T rows per column-projection unit
 
-__device__ __forceinline__ uint8_t* align_1024(uint8_t* p) {
-  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
-}
-
-// Loads `NC` consecutive fp32 TMEM columns of this thread's lane.
-template <int NC>
-__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float* v) {
-  static_assert(NC % 16 == 0, "columns in multiples of 16");
-#pragma unroll
-  for (int c0 = 0; c0 < NC; c0 += (NC % 32 == 0 ? 32 : 16)) {
-    if constexpr (NC % 32 == 0) {
-      float t[32];
-      tmem_ld_32cols(taddr + c0, t);
-#pragma unroll
-      for (int j = 0; j < 32; ++j) v[c0 + j] = t[j];
-    } else {
-      float t[16];
-      tmem_ld_16cols(taddr + c0, t);
-#pragma unroll
-      for (int j = 0; j < 16; ++j) v[c0 + j] = t[j];
-    }
-  }
-}
-
 // Block schedule shared by both kernels (see the file comment).
 struct Sched {
   int cl;             // CTAs per cluster splitting one block (1, 2, 4 or 8)
@@ -717,16 +693,8 @@ int colproj_ctas_per_sm(int nmma) { return nmma >= 128 ? 1 : 2; }
 int colproj_stage_chunk() { return kColChunk; }
 int colproj_tile_t() { return kTileT; }
 
-cudaError_t read_device_error(int32_t* out, bool reset) {
-  int v = 0;
-  cudaError_t e = cudaMemcpyFromSymbol(&v, g_device_error, sizeof(int));
-  if (e != cudaSuccess) return e;
-  if (reset && v != 0) {
-    const int z = 0;
-    e = cudaMemcpyToSymbol(g_device_error, &z, sizeof(int));
-  }
-  *out = v;
-  return e;
+cudaError_t read_device_error_proj(int32_t* out, bool reset) {
+  return read_tu_device_error(out, reset);
 }
 
 cudaError_t launch_tc_rowproj(const void* X, int64_t B, int64_t T, int64_t c, const void* R,
