@@ -113,6 +113,18 @@ dprc_status dprc_norm_hutch(const void* A, const void* G, const void* P, dprc_dt
                             float* n, int accumulate, void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * Number of kernels one dprc_norm_hutch call with these arguments enqueues on
+ * the current device: 1 (bf16, k = 16 or 32: sketch and projection as two
+ * phases of one cooperative launch), 2 (other tensor-core shapes: a sketch
+ * kernel and a projection kernel) or 3 (the CUDA-core path: sketch,
+ * projection, reduction).  0 for arguments dprc_norm_hutch would reject or
+ * when no sm_103 device is current.  Enqueues nothing; for launch accounting
+ * and graph builders.  No counterpart on the pages (a library property).
+ */
+int dprc_norm_hutch_launches(dprc_dtype dtype, int64_t B, int64_t T, int64_t d, int64_t p,
+                             int64_t k);
+
+/*
  * Hutch++ head/tail estimate for one layer (papernotes.org, "Key design >
  * Hutch++ head-tail decomposition"; gist.science, "Kernmechanisme" item 2):
  *     Q_i     = orthonormal basis of Col(O_i S)          (p x r, thin QR)

@@ -21,6 +21,7 @@ from .binding import (  # noqa: F401
     dprc_device_error,
     dprc_exact_norm,
     dprc_norm_hutch,
+    dprc_norm_hutch_launches,
     dprc_norm_hutch_noalloc,
     dprc_norm_hutchpp,
     dprc_philox_words,

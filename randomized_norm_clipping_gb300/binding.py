@@ -48,6 +48,8 @@ _PROTOS = [
      [_c.c_void_p, _c.c_int64, _c.c_uint64, _c.c_uint64, _c.c_uint64, _c.c_void_p]),
     ("dprc_device_error", _c.c_int, [_c.c_void_p, _c.c_int]),
     ("dprc_set_phase_events", _c.c_int, [_c.c_void_p, _c.c_int]),
+    ("dprc_norm_hutch_launches", _c.c_int,
+     [_c.c_int, _c.c_int64, _c.c_int64, _c.c_int64, _c.c_int64, _c.c_int64]),
     ("dprc_norm_hutch_noalloc", _c.c_int,
      [_c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_int, _c.c_int64, _c.c_int64, _c.c_int64,
       _c.c_int64, _c.c_int64, _c.c_void_p, _c.c_int, _c.c_void_p]),
@@ -128,12 +130,19 @@ def dprc_workspace_bytes(op, dtype_code, B, T, d, p, k):
 
 
 def workspace(op, like, B, T, d, p, k):
-    """A device byte buffer of dprc_workspace_bytes(...) bytes (torch
-    allocation; the library needs no particular initial contents)."""
+    """A zeroed device byte buffer of dprc_workspace_bytes(...) bytes (torch
+    allocation).  Workspaces must be zero before their first use; calls leave
+    their counter block zero again, so the buffer can be reused."""
     n = dprc_workspace_bytes(op, _dtype_code(like), B, T, d, p, k)
     if n == 0:
         raise DprcError("dprc_workspace_bytes", 2)
     return torch.zeros(n, dtype=torch.uint8, device=like.device)
+
+
+def dprc_norm_hutch_launches(dtype_code, B, T, d, p, k):
+    """Kernels one dprc_norm_hutch call with these sizes enqueues on the
+    current device (1 fused, 2 sketch + projection, 3 CUDA cores; 0 invalid)."""
+    return int(lib().dprc_norm_hutch_launches(dtype_code, B, T, d, p, k))
 
 
 def dprc_norm_hutch(A, G, P, n, accumulate=False, ws=None, stream=None):

@@ -356,6 +356,14 @@ dprc_status dprc_norm_hutch(const void* A, const void* G, const void* P, dprc_dt
   return cuda_status(e);
 }
 
+int dprc_norm_hutch_launches(dprc_dtype dtype, int64_t B, int64_t T, int64_t d, int64_t p,
+                             int64_t k) {
+  if (check_common(dtype, B, T, d, p) != DPRC_OK || k < 1 || k > 256) return 0;
+  if (!device_ok()) return 0;
+  if (!tc_path_supported(dtype, B, T, d, p, k, false)) return 3;
+  return fused_hutch_planned(B, T, d, p, k) ? 1 : 2;
+}
+
 dprc_status dprc_norm_hutchpp(const void* A, const void* G, const void* S, const void* P,
                               dprc_dtype dtype, int64_t B, int64_t T, int64_t d, int64_t p,
                               int64_t r, float* n, int accumulate, void* ws, size_t ws_bytes,

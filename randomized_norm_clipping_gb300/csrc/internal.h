@@ -129,6 +129,9 @@ int64_t fgc_partials(int64_t B, int64_t d, int64_t p);
 // kernel cannot run with this shape or device (the caller then uses the two
 // kernels); ready and tickets must be zero and are zero again afterwards.
 bool fused_hutch_supported(int64_t k);
+// Whether a dprc_norm_hutch call with these sizes takes the fused kernel on
+// the current device (the same decision the launcher makes).
+bool fused_hutch_planned(int64_t B, int64_t T, int64_t d, int64_t p, int64_t k);
 cudaError_t launch_tc_hutch_fused(const void* A, const void* G, const void* P, int64_t B,
                                   int64_t T, int64_t d, int64_t p, int64_t k, void* W,
                                   int64_t tpad, int* ready, int* tickets, float* chunk_norms,

@@ -722,27 +722,28 @@ cudaError_t read_device_error_hutch(int32_t* out, bool reset) {
 
 bool fused_hutch_supported(int64_t k) { return k == 16 || k == 32; }
 
-cudaError_t launch_tc_hutch_fused(const void* A, const void* G, const void* P, int64_t B,
-                                  int64_t T, int64_t d, int64_t p, int64_t k, void* W,
-                                  int64_t tpad, int* ready, int* tickets, float* chunk_norms,
-                                  float* n_out, int accumulate, cudaStream_t s, bool* launched) {
-  *launched = false;
-  // a device on which the cooperative cluster launch was refused once keeps
-  // using the two-kernel path
-  constexpr int kMaxDev = 64;
-  static std::atomic<int> refused[kMaxDev];
+namespace {
+
+// Devices on which the cooperative launch was refused once keep using the
+// two-kernel path.
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_refused[kMaxDevices];
+
+// Schedule of one fused launch (phases, cluster size, grid); false when the
+// kernel cannot run with these sizes on the current device.
+bool plan_fused(int64_t B, int64_t T, int64_t d, int64_t p, int64_t k, HArgs& a, int& grid_out,
+                int& cl_out) {
+  if (!fused_hutch_supported(k)) return false;
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return cudaSuccess;
-  if (refused[dev].load(std::memory_order_acquire)) return cudaSuccess;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+  if (g_refused[dev].load(std::memory_order_acquire)) return false;
   const int ik = static_cast<int>(k);
   const int slots = device_sm_count();  // one CTA per SM
-  HArgs a;
   a.T = static_cast<int>(T);
   a.p = static_cast<int>(p);
   a.d = static_cast<int>(d);
   a.mtiles = static_cast<int>((T + kTok - 1) / kTok);
   a.nchunks = static_cast<int>((d + kRows - 1) / kRows);
-  a.tpad = tpad;
   a.ph1.nblocks = B * a.mtiles;
   a.ph1.upb = static_cast<int>((p + kCol - 1) / kCol);
   a.ph2.nblocks = B * a.nchunks;
@@ -750,10 +751,9 @@ cudaError_t launch_tc_hutch_fused(const void* A, const void* G, const void* P, i
   const int cl1 = want_cl(a.ph1.nblocks, a.ph1.upb, slots);
   const int cl2 = want_cl(a.ph2.nblocks, a.ph2.upb, slots);
   const int cl = cl1 > cl2 ? cl1 : cl2;
-  cudaError_t e = ik == 16 ? set_smem_once<16>() : set_smem_once<32>();
-  if (e != cudaSuccess) return e;
+  if ((ik == 16 ? set_smem_once<16>() : set_smem_once<32>()) != cudaSuccess) return false;
   const int resident = ik == 16 ? resident_ctas<16>(cl) : resident_ctas<32>(cl);
-  if (resident < cl) return cudaSuccess;  // cannot run here: caller uses the two-kernel path
+  if (resident < cl) return false;
   a.ph1.split = cl1 > 1 && a.ph1.upb >= cl ? 1 : 0;
   a.ph2.split = cl2 > 1 && a.ph2.upb >= cl ? 1 : 0;
   // Grid: the multiple of cl (up to what is resident) that minimises the
@@ -773,8 +773,31 @@ cudaError_t launch_tc_hutch_fused(const void* A, const void* G, const void* P, i
       grid = g;
     }
   }
-  if (grid < cl) return cudaSuccess;
+  if (grid < cl) return false;
   a.ready_target = a.mtiles * (a.ph1.split ? cl : 1);
+  grid_out = static_cast<int>(grid);
+  cl_out = cl;
+  return true;
+}
+
+}  // namespace
+
+bool fused_hutch_planned(int64_t B, int64_t T, int64_t d, int64_t p, int64_t k) {
+  HArgs a;
+  int grid = 0, cl = 0;
+  return plan_fused(B, T, d, p, k, a, grid, cl);
+}
+
+cudaError_t launch_tc_hutch_fused(const void* A, const void* G, const void* P, int64_t B,
+                                  int64_t T, int64_t d, int64_t p, int64_t k, void* W,
+                                  int64_t tpad, int* ready, int* tickets, float* chunk_norms,
+                                  float* n_out, int accumulate, cudaStream_t s, bool* launched) {
+  *launched = false;
+  HArgs a;
+  int grid = 0, cl = 0;
+  if (!plan_fused(B, T, d, p, k, a, grid, cl)) return cudaSuccess;
+  const int ik = static_cast<int>(k);
+  a.tpad = tpad;
   a.W = static_cast<__nv_bfloat16*>(W);
   a.ready = ready;
   a.tickets = tickets;
@@ -789,13 +812,15 @@ cudaError_t launch_tc_hutch_fused(const void* A, const void* G, const void* P, i
   if (!make_tmap_3d_bf16(&ma, A, d, T, B, d, T * d, 64, kTok, 128)) return cudaErrorInvalidValue;
   if (!make_tmap_3d_bf16(&mw, W, T, 2 * ik, B, tpad, 2 * ik * tpad, 64, 2 * ik, 128))
     return cudaErrorInvalidValue;
-  e = ik == 16 ? launch_k<16>(mg, mp, ma, mw, a, static_cast<int>(grid), cl, s)
-               : launch_k<32>(mg, mp, ma, mw, a, static_cast<int>(grid), cl, s);
+  const cudaError_t e = ik == 16 ? launch_k<16>(mg, mp, ma, mw, a, grid, cl, s)
+                                 : launch_k<32>(mg, mp, ma, mw, a, grid, cl, s);
   if (e == cudaSuccess) {
     *launched = true;
   } else if (e == cudaErrorCooperativeLaunchTooLarge || e == cudaErrorNotSupported ||
              e == cudaErrorInvalidConfiguration || e == cudaErrorInvalidValue) {
-    refused[dev].store(1, std::memory_order_release);
+    int dev = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < kMaxDevices)
+      g_refused[dev].store(1, std::memory_order_release);
   }
   return e;
 }

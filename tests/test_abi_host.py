@@ -126,6 +126,16 @@ def test_valid_calls_without_a_gpu_fail_loudly(lib):
     st = lib.dprc_norm_hutch(_vp(A16), _vp(A16), _vp(A16), 1, 1, 1, 8, 8, 16, _vp(A16), 0,
                              _vp(A16), 1 << 30, None)
     assert st == 8  # DPRC_ERR_DEVICE: nothing was launched
+    # the launch-count query enqueues nothing and reports 0 without a device
+    assert lib.dprc_norm_hutch_launches(1, 8, 4096, 2048, 2048, 32) == 0
+
+
+def test_launch_count_query_rejects_bad_arguments(lib):
+    q = lib.dprc_norm_hutch_launches
+    assert q(5, 8, 4096, 2048, 2048, 32) == 0   # unknown dtype
+    assert q(1, 0, 4096, 2048, 2048, 32) == 0   # empty batch
+    assert q(1, 8, 4096, 2048, 2048, 0) == 0    # k = 0
+    assert q(1, 8, 4096, 2048, 2048, 300) == 0  # k > 256
 
 
 def test_binding_raises_when_library_missing(monkeypatch, tmp_path):

@@ -139,6 +139,17 @@ def test_hutch_is_deterministic():
     assert torch.equal(n1, n2)
 
 
+def test_launch_count_query_matches_the_path():
+    from randomized_norm_clipping_gb300 import DPRC_BF16, DPRC_F32
+    # bf16 k = 32 on the headline shape: one fused launch
+    assert rnc.dprc_norm_hutch_launches(DPRC_BF16, 8, 4096, 2048, 2048, 32) == 1
+    # k = 64: sketch and projection kernels
+    assert rnc.dprc_norm_hutch_launches(DPRC_BF16, 8, 4096, 2048, 2048, 64) == 2
+    # fp32 or widths that are not multiples of 8: the CUDA-core path
+    assert rnc.dprc_norm_hutch_launches(DPRC_F32, 4, 128, 64, 64, 8) == 3
+    assert rnc.dprc_norm_hutch_launches(DPRC_BF16, 2, 100, 97, 64, 32) == 3
+
+
 def test_hutch_identity_projection_gives_exact_norm():
     # P = I_p (k = p = 32) turns the estimate into the exact norm
     A, G, _ = _hutch_case(2, 300, 128, 32, 32, torch.bfloat16, seed=3)
