@@ -515,7 +515,8 @@ dprc_status dprc_device_error(int32_t* out, int reset) {
   if (!device_ok()) return DPRC_ERR_DEVICE;
   cudaError_t (*const readers[])(int32_t*, bool) = {read_device_error_proj,
                                                      read_device_error_hutch,
-                                                     read_device_error_exact};
+                                                     read_device_error_exact,
+                                                     read_device_error_qr};
   int32_t first = 0;
   for (auto rd : readers) {
     int32_t v = 0;

@@ -58,6 +58,7 @@ int colproj_tile_t();
 cudaError_t read_device_error_proj(int32_t* out, bool reset);
 cudaError_t read_device_error_exact(int32_t* out, bool reset);
 cudaError_t read_device_error_hutch(int32_t* out, bool reset);
+cudaError_t read_device_error_qr(int32_t* out, bool reset);
 bool tc_path_supported(dprc_dtype dt, int64_t B, int64_t T, int64_t d, int64_t p, int64_t k,
                        bool hutchpp);
 BlockSched rowproj_sched(int64_t B, int64_t T, int64_t c, int nmma);
@@ -114,6 +115,11 @@ cudaError_t launch_simt_norm_finish(const float* Y, int64_t B, int64_t c, int n,
 // Hutch++ middle step: per-sample Householder QR of M [B][p][r] (fp32),
 // then P' = P - Q (Q^T P); writes [Q | P'] either as bf16 hi/lo [B][p][4r]
 // (hilo = true) or fp32 [B][p][2r].  scratch: fp32 [B][p][r] * 2.
+// Cluster QR (r = 16, 16 <= p <= 4096): one cluster of 8 CTAs per sample;
+// same output as launch_qr_project.
+bool qr_cluster_supported(int64_t p, int r);
+cudaError_t launch_qr_cluster(const float* M, int64_t B, int64_t p, const void* P, dprc_dtype pdt,
+                              void* out, bool hilo, cudaStream_t s);
 cudaError_t launch_qr_project(const float* M, int64_t B, int64_t p, int r, const void* P,
                               dprc_dtype pdt, float* scratch, void* out, bool hilo,
                               cudaStream_t s);

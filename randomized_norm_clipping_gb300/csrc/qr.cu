@@ -613,6 +613,8 @@ cudaError_t launch_qr_project(const float* M, int64_t B, int64_t p, int r, const
                               dprc_dtype pdt, float* scratch, void* out, bool hilo,
                               cudaStream_t s) {
   if (r < 1 || r > kMaxR) return cudaErrorInvalidValue;
+  // r = 16, p <= 4096: one thread-block cluster per sample
+  if (qr_cluster_supported(p, r)) return launch_qr_cluster(M, B, p, P, pdt, out, hilo, s);
   // shared-memory variant for r = 16 when M (fp32) and P^T fit: p <= 2260
   // with bf16 P, p <= 1696 with fp32 P
   if (r == 16 && p <= 5 * kQrSmemThreads && p * 16 * (4 + (pdt == DPRC_F32 ? 4 : 2)) <= 212 * 1024)

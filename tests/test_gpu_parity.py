@@ -161,7 +161,8 @@ def test_hutch_identity_projection_gives_exact_norm():
 
 # ------------------------------------------------------------------ Hutch++
 
-@pytest.mark.parametrize("B,T,d,p", [(2, 200, 256, 256), (3, 77, 136, 64), (2, 1100, 512, 1024)])
+@pytest.mark.parametrize("B,T,d,p", [(2, 200, 256, 256), (3, 77, 136, 64), (2, 1100, 512, 1024),
+                                     (2, 300, 256, 3000)])
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 def test_hutchpp_matches_oracle(B, T, d, p, dtype):
     r = 16
