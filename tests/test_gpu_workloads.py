@@ -1,0 +1,100 @@
+"""Parity at the benchmark's configurations, in the launch shapes it times.
+
+Each configuration is drawn by `workloads.layer_inputs` on the GPU, run
+through the C ABI with the full batch, and compared with the float64 oracle
+on the same bytes: every sample where the oracle is quick, a sampled subset
+(stated per test) where it is not.  Tolerance: relative 1e-3 on n and on the
+clip factors (bf16 inputs, fp32 accumulation).
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import randomized_norm_clipping_gb300 as rnc
+from randomized_norm_clipping_gb300 import workloads as wl
+from randomized_norm_clipping_gb300.workloads import to_f64
+
+pytestmark = pytest.mark.gpu
+
+RTOL = 1e-3
+DEV = "cuda:0"
+
+
+def _relerr(got, ref):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    return np.max(np.abs(got - ref) / np.maximum(np.abs(ref), 1e-300))
+
+
+def _clip_both_branches(n_gpu, ref):
+    # C = 1 (the workloads' value: every sample clips) and C = the median
+    # sqrt(n), so both branches of min(1, C / sqrt(n)) are exercised
+    for C in (1.0, float(np.median(np.sqrt(ref)))):
+        c = torch.empty_like(n_gpu)
+        rnc.dprc_clip_factors(n_gpu, C, c)
+        assert _relerr(c.cpu(), oracle.clip_factors(ref, C)) < RTOL, C
+
+
+def test_single_fp32_layer_b4_t128():
+    wk = wl.WORKLOADS["hutch_b4_t128_64x64_k8_f32"]
+    A, G, P = wl.layer_inputs(wk, 0, device=DEV)
+    n = torch.zeros(wk.B, device=DEV)
+    rnc.dprc_norm_hutch(A, G, P, n)
+    ref = oracle.hutch_norm(to_f64(A), to_f64(G), to_f64(P))
+    assert _relerr(n.cpu(), ref) < 1e-5  # fp32 inputs, fp32 arithmetic
+    e = torch.zeros(wk.B, device=DEV)
+    rnc.dprc_exact_norm(A, G, e)
+    assert _relerr(e.cpu(), oracle.exact_norm(to_f64(A), to_f64(G))) < 1e-5
+    _clip_both_branches(n, ref)
+
+
+def test_q_proj_b8_t4096_every_sample():
+    wk = wl.WORKLOADS[wl.HEADLINE]
+    A, G, P = wl.layer_inputs(wk, 0, device=DEV)
+    n = torch.zeros(wk.B, device=DEV)
+    rnc.dprc_norm_hutch(A, G, P, n)
+    ref = oracle.hutch_norm(to_f64(A), to_f64(G), to_f64(P))
+    assert _relerr(n.cpu(), ref) < RTOL
+    _clip_both_branches(n, ref)
+    assert rnc.dprc_device_error() == 0
+
+
+def test_llama_block_layerwise_sum_and_clip():
+    # the first decoder block of the 112-layer workload (q, k, v, o, gate, up,
+    # down at B = 4, T = 4096), accumulated into one n as the step does
+    wk = wl.WORKLOADS["hutch_llama32_1b_112layers_b4_t4096_k32_bf16"]
+    n = torch.zeros(wk.B, device=DEV)
+    refs = []
+    for j in range(len(wl.LLAMA32_1B_BLOCK)):
+        A, G, P = wl.layer_inputs(wk, j, device=DEV)
+        rnc.dprc_norm_hutch(A, G, P, n, accumulate=j > 0)
+        refs.append(oracle.hutch_norm(to_f64(A), to_f64(G), to_f64(P)))
+        del A, G, P
+    ref = oracle.layer_sum(refs)
+    assert _relerr(n.cpu(), ref) < RTOL
+    _clip_both_branches(n, ref)
+
+
+def test_hutchpp_q_proj_b8_t4096_every_sample():
+    wk = wl.WORKLOADS["hutchpp_q_proj_b8_t4096_r16_bf16"]
+    A, G, (S, P) = wl.layer_inputs(wk, 0, device=DEV)
+    n = torch.zeros(wk.B, device=DEV)
+    rnc.dprc_norm_hutchpp(A, G, S, P, n)
+    ref = oracle.hutchpp_norm(to_f64(A), to_f64(G), to_f64(S), to_f64(P))
+    assert _relerr(n.cpu(), ref) < RTOL
+    assert rnc.dprc_device_error() == 0
+
+
+@pytest.mark.parametrize("layer", [0, 1])
+def test_long_context_b2_t32768_sampled(layer):
+    # the full B = 2 launch; the oracle checks sample 0 (one sample of
+    # T = 32768 widened to float64 is 2.7 GB)
+    wk = wl.WORKLOADS["hutch_long_b2_t32768_up_down_k32_bf16"]
+    A, G, P = wl.layer_inputs(wk, layer, device=DEV)
+    n = torch.zeros(wk.B, device=DEV)
+    rnc.dprc_norm_hutch(A, G, P, n)
+    ref0 = oracle.hutch_norm(to_f64(A[:1]), to_f64(G[:1]), to_f64(P))
+    assert _relerr(n[:1].cpu(), ref0) < RTOL
+    assert np.all(np.isfinite(n.cpu().numpy())) and torch.all(n > 0)
