@@ -152,8 +152,12 @@ __global__ void __launch_bounds__(256) philox_words_kernel(uint4* __restrict__ o
     out[j] = philox_block(first + static_cast<uint64_t>(j), step, rk);
 }
 
+// Launched as a programmatic dependent of the norm kernel before it: the
+// launch overlaps that kernel, and griddepcontrol.wait holds the reads of n
+// until it has completed and its writes are visible.
 __global__ void clip_kernel(const float* __restrict__ n, long long B, float C,
                             float* __restrict__ c, int32_t* __restrict__ nonfinite) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= B) return;
   const float v = n[i];
@@ -199,9 +203,16 @@ cudaError_t launch_philox_words(uint32_t* out, int64_t n_blocks, uint64_t first_
 cudaError_t launch_clip(const float* n, int64_t B, float C, float* c, int32_t* nonfinite,
                         cudaStream_t s) {
   const int threads = 128;
-  clip_kernel<<<static_cast<unsigned>((B + threads - 1) / threads), threads, 0, s>>>(n, B, C, c,
-                                                                                   nonfinite);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((B + threads - 1) / threads));
+  cfg.blockDim = dim3(threads);
+  cfg.stream = s;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, clip_kernel, n, static_cast<long long>(B), C, c, nonfinite);
 }
 
 }  // namespace dprc

@@ -260,6 +260,9 @@ __global__ void __launch_bounds__(192, 1)
   xs.recv = reinterpret_cast<float*>(ring + Cfg::kRing + Cfg::kCtrl);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // a dependent launch (the clip factors) may start now; it waits for this
+  // grid's completion before reading anything
+  pdl_launch_dependents();
   const int rank = cl > 1 ? static_cast<int>(cluster_ctarank()) : 0;
   const Mine m1 = mine(a.ph1, cl, rank);
   const Mine m2 = mine(a.ph2, cl, rank);
