@@ -399,7 +399,8 @@ def run_native(args, rank, ws, local):
         "clocks": clk.summary(),
     }
     which = set() if args.rows == "none" else (
-        {"c3", "c4", "c5", "noise", "exact"} if args.rows == "all" else set(args.rows.split(",")))
+        {"c3", "c4", "c5", "noise", "exact", "step"} if args.rows == "all"
+        else set(args.rows.split(",")))
     if which:
         out["rows"] = measure_rows(which, device, peak, measured_tflops(), 7919 * rank)
     if rank == 0 and not args.no_cpu_baseline:
@@ -541,8 +542,54 @@ def measure_rows(which, device, peak, tflops_peak, seed_shift):
                             "what": "dprc_exact_norm on the q_proj batch, direct form on "
                                     "tensor cores; flops 2 T d p per sample"}
         del A, G, n, wsbuf
+    if "step" in which:
+        rows["dpsgd_rc_step_mlp"] = measure_step(device)
     torch.cuda.empty_cache()
     return rows
+
+
+def measure_step(device, B=4, T=4096):
+    """One DP-SGD-RC step (randomized_norm_clipping_gb300.step) on a Llama-3.2-1B
+    MLP-shaped bias-free block (2048 -> 8192 -> 2048, bf16, B x T tokens),
+    against the same forward with an ordinary backward."""
+    from randomized_norm_clipping_gb300.step import RandomizedClippingStep
+    torch.manual_seed(0)
+    model = torch.nn.Sequential(torch.nn.Linear(2048, 8192, bias=False), torch.nn.SiLU(),
+                                torch.nn.Linear(8192, 2048, bias=False)).to(device, torch.bfloat16)
+    x = torch.randn(B, T, 2048, device=device).to(torch.bfloat16)
+
+    def losses():
+        return (model(x).float() ** 2).mean(dim=(1, 2))
+
+    step = RandomizedClippingStep(model, C=1.0, sigma=1.0, k=32, seed=1)
+
+    def dp():
+        step(losses(), step=0)
+
+    def plain():
+        for m in model:
+            if isinstance(m, torch.nn.Linear):
+                m.weight.grad = None
+        losses().sum().backward()
+
+    def timed(fn, reps=10):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize(device)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize(device)
+        return e0.elapsed_time(e1) / reps
+
+    t_dp, t_plain = timed(dp), timed(plain)
+    step.close()
+    return {"ms": t_dp, "plain_backward_ms": t_plain, "overhead": t_dp / t_plain,
+            "what": "forward + first backward to the layer outputs + dprc_norm_hutch per layer "
+                    "+ clip + rescaled second backward + noise, B4 T4096 bf16 2048->8192->2048 "
+                    "(eager, host launch time included), against forward + plain backward"}
 
 
 # ---------------------------------------------------------------- reference arm
@@ -590,7 +637,7 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--rows", default="all",
                     help="other configurations to time after the headline: all, none, or a "
-                         "comma list of c3,c4,c5,noise,exact")
+                         "comma list of c3,c4,c5,noise,exact,step")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3

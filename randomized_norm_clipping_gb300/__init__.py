@@ -30,3 +30,4 @@ from .binding import (  # noqa: F401
     lib,
     workspace,
 )
+from .step import RandomizedClippingStep  # noqa: F401,E402
