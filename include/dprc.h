@@ -76,7 +76,8 @@ typedef enum { DPRC_F32 = 0, DPRC_BF16 = 1 } dprc_dtype;
 typedef enum {
     DPRC_OP_HUTCH = 1,
     DPRC_OP_HUTCHPP = 2,
-    DPRC_OP_EXACT = 3
+    DPRC_OP_EXACT = 3,
+    DPRC_OP_HUTCH_LAYERS = 4
 } dprc_op;
 
 /* Version of this ABI (DPRC_ABI_VERSION of the built library). */
@@ -111,6 +112,26 @@ size_t dprc_workspace_bytes(dprc_op op, dprc_dtype dtype, int64_t B, int64_t T,
 dprc_status dprc_norm_hutch(const void* A, const void* G, const void* P, dprc_dtype dtype,
                             int64_t B, int64_t T, int64_t d, int64_t p, int64_t k,
                             float* n, int accumulate, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Layerwise sum of Hutchinson estimates over the L linear layers of a model
+ * (papernotes.org, "Method > Overall framework": n_i = sum_l n_hat_i^(l)):
+ *     n[i] (+)= sum_l || A_l,i^T (G_l,i P_l) ||_F^2
+ *  A, G, P: host arrays of L device pointers, layer l holding A [B][T][d[l]],
+ *  G [B][T][p[l]] and P [p[l]][k]; d, p: host arrays of L sizes.  B, T, k and
+ *  dtype are shared by all layers.  The result equals L dprc_norm_hutch calls
+ *  with accumulate set after the first, except that the layer sum is added in
+ *  layer order after all layers (a fixed order: bitwise repeatable).  For bf16
+ *  and k = 16 or 32 the layers run in one persistent launch per 56 layers, so
+ *  one layer's start-up and tail overlap its neighbours' streaming; otherwise
+ *  they run one call at a time.  Workspace: dprc_workspace_bytes(
+ *  DPRC_OP_HUTCH_LAYERS, dtype, B, T, max_l d[l], max_l p[l], k).  Errors as
+ *  dprc_norm_hutch (checked for every layer before anything is enqueued).
+ */
+dprc_status dprc_norm_hutch_layers(int64_t L, const void* const* A, const void* const* G,
+                                   const void* const* P, const int64_t* d, const int64_t* p,
+                                   dprc_dtype dtype, int64_t B, int64_t T, int64_t k, float* n,
+                                   int accumulate, void* ws, size_t ws_bytes, void* stream);
 
 /*
  * Number of kernels one dprc_norm_hutch call with these arguments enqueues on

@@ -12,6 +12,7 @@ from .binding import (  # noqa: F401
     DPRC_F32,
     DPRC_OP_EXACT,
     DPRC_OP_HUTCH,
+    DPRC_OP_HUTCH_LAYERS,
     DPRC_OP_HUTCHPP,
     EXPORTED,
     DprcError,
@@ -22,6 +23,7 @@ from .binding import (  # noqa: F401
     dprc_exact_norm,
     dprc_norm_hutch,
     dprc_norm_hutch_launches,
+    dprc_norm_hutch_layers,
     dprc_norm_hutch_noalloc,
     dprc_norm_hutchpp,
     dprc_philox_words,

@@ -19,7 +19,7 @@ PKG_DIR = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG_DIR, "libdprc.so")
 
 DPRC_F32, DPRC_BF16 = 0, 1
-DPRC_OP_HUTCH, DPRC_OP_HUTCHPP, DPRC_OP_EXACT = 1, 2, 3
+DPRC_OP_HUTCH, DPRC_OP_HUTCHPP, DPRC_OP_EXACT, DPRC_OP_HUTCH_LAYERS = 1, 2, 3, 4
 STATUS = {0: "ok", 1: "null pointer", 2: "shape", 3: "dtype", 4: "alignment",
           5: "workspace", 6: "cuda", 7: "non-finite", 8: "device", 9: "too large"}
 
@@ -48,6 +48,10 @@ _PROTOS = [
      [_c.c_void_p, _c.c_int64, _c.c_uint64, _c.c_uint64, _c.c_uint64, _c.c_void_p]),
     ("dprc_device_error", _c.c_int, [_c.c_void_p, _c.c_int]),
     ("dprc_set_phase_events", _c.c_int, [_c.c_void_p, _c.c_int]),
+    ("dprc_norm_hutch_layers", _c.c_int,
+     [_c.c_int64, _c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_int,
+      _c.c_int64, _c.c_int64, _c.c_int64, _c.c_void_p, _c.c_int, _c.c_void_p, _c.c_size_t,
+      _c.c_void_p]),
     ("dprc_norm_hutch_launches", _c.c_int,
      [_c.c_int, _c.c_int64, _c.c_int64, _c.c_int64, _c.c_int64, _c.c_int64]),
     ("dprc_norm_hutch_noalloc", _c.c_int,
@@ -137,6 +141,28 @@ def workspace(op, like, B, T, d, p, k):
     if n == 0:
         raise DprcError("dprc_workspace_bytes", 2)
     return torch.zeros(n, dtype=torch.uint8, device=like.device)
+
+
+def dprc_norm_hutch_layers(As, Gs, Ps, n, accumulate=False, ws=None, stream=None):
+    """n[i] (+)= sum_l ||A_l,i^T (G_l,i P_l)||_F^2 over the layers (see include/dprc.h)."""
+    L = len(As)
+    if not (L == len(Gs) == len(Ps)) or L == 0:
+        raise ValueError("As, Gs and Ps must be non-empty lists of the same length")
+    _need_cuda(*As, *Gs, *Ps, n)
+    B, T = As[0].shape[0], As[0].shape[1]
+    k = Ps[0].shape[1]
+    d = (ctypes.c_int64 * L)(*[a.shape[2] for a in As])
+    p = (ctypes.c_int64 * L)(*[g.shape[2] for g in Gs])
+    ap = (ctypes.c_void_p * L)(*[_ptr(a) for a in As])
+    gp = (ctypes.c_void_p * L)(*[_ptr(g) for g in Gs])
+    pp = (ctypes.c_void_p * L)(*[_ptr(x) for x in Ps])
+    if ws is None:
+        ws = workspace(DPRC_OP_HUTCH_LAYERS, As[0], B, T, max(d), max(p), k)
+    st = lib().dprc_norm_hutch_layers(L, ap, gp, pp, d, p, _dtype_code(As[0]), B, T, k, _ptr(n),
+                                      int(bool(accumulate)), _ptr(ws), ws.numel(),
+                                      _stream(As[0], stream))
+    _check("dprc_norm_hutch_layers", st)
+    return n
 
 
 def dprc_norm_hutch_launches(dtype_code, B, T, d, p, k):

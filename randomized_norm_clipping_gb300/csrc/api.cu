@@ -121,23 +121,39 @@ bool tc_path_supported(dprc_dtype dt, int64_t B, int64_t T, int64_t d, int64_t p
   return k == 16 || k == 32 || k == 64;
 }
 
-// Every plan starts with the same counter block: per-sample tickets and
-// sketch-ready counters, int32 [B] each.  Calls leave it zeroed; the fused
-// Hutchinson kernel relies on that, so no other buffer may overlap it.
-size_t ctrl_bytes(int64_t B) { return align_up(static_cast<size_t>(B) * 8, 256); }
+// Every plan starts with the same counter block: tickets and sketch-ready
+// counters per (layer slot, sample), layers finished per sample, projection
+// blocks finished per layer slot, and one CTA-exit count.  Calls leave it
+// zeroed; the fused Hutchinson kernel relies on that, so no other buffer may
+// overlap it.
+size_t ctrl_bytes(int64_t B) {
+  const size_t ints = 2 * static_cast<size_t>(kMaxFusedLayers) * B + B + kMaxFusedLayers + 1;
+  return align_up(ints * 4, 256);
+}
 
-TcPlan plan_tc(dprc_op op, int64_t B, int64_t T, int64_t d, int64_t p, int64_t k) {
+TcPlan plan_tc(dprc_op op, int64_t B, int64_t T, int64_t d, int64_t p, int64_t k, int layers) {
   TcPlan t;
   t.tpad = tpad_of(T);
   const int64_t nch = (std::max(d, p) + colproj_stage_chunk() - 1) / colproj_stage_chunk();
+  const size_t LB = static_cast<size_t>(kMaxFusedLayers) * B;
   t.stick_off = 0;
-  t.ready_off = static_cast<size_t>(B) * 4;
+  t.ready_off = LB * 4;
+  t.lticket_off = 2 * LB * 4;
+  t.done2_off = t.lticket_off + static_cast<size_t>(B) * 4;
+  t.exit_off = t.done2_off + static_cast<size_t>(kMaxFusedLayers) * 4;
   size_t off = ctrl_bytes(B);
   t.cnorm_off = off;
-  off = align_up(off + static_cast<size_t>(B) * nch * 4, 1024);
+  off = align_up(off + static_cast<size_t>(layers) * B * nch * 4, 1024);
+  t.nl_off = off;
+  off = align_up(off + static_cast<size_t>(layers) * B * 4, 1024);
   t.w_bytes = static_cast<size_t>(B) * (op == DPRC_OP_HUTCH ? 2 * k : 4 * k) * t.tpad * 2;
   t.w_off = off;
   off = align_up(off + t.w_bytes, 1024);
+  t.w2_off = t.w_off;
+  if (layers > 1) {
+    t.w2_off = off;
+    off = align_up(off + t.w_bytes, 1024);
+  }
   if (op == DPRC_OP_HUTCHPP) {
     const int64_t r = k;
     t.z_off = off;
@@ -151,6 +167,21 @@ TcPlan plan_tc(dprc_op op, int64_t B, int64_t T, int64_t d, int64_t p, int64_t k
   }
   t.total = off;
   return t;
+}
+
+FusedScratch fused_scratch(const TcPlan& t, char* w) {
+  FusedScratch f;
+  f.W[0] = w + t.w_off;
+  f.W[1] = w + t.w2_off;
+  f.tpad = t.tpad;
+  f.tickets = reinterpret_cast<int*>(w + t.stick_off);
+  f.ready = reinterpret_cast<int*>(w + t.ready_off);
+  f.lticket = reinterpret_cast<int*>(w + t.lticket_off);
+  f.done2 = reinterpret_cast<int*>(w + t.done2_off);
+  f.exit_count = reinterpret_cast<int*>(w + t.exit_off);
+  f.chunk_norms = reinterpret_cast<float*>(w + t.cnorm_off);
+  f.nl = reinterpret_cast<float*>(w + t.nl_off);
+  return f;
 }
 
 SimtPlan plan_simt(dprc_op op, int64_t B, int64_t T, int64_t d, int64_t p, int64_t k) {
@@ -286,6 +317,10 @@ size_t dprc_workspace_bytes(dprc_op op, dprc_dtype dtype, int64_t B, int64_t T, 
       return hutchpp_ws(dtype, B, T, d, p, k);
     case DPRC_OP_EXACT:
       return plan_exact_bytes(dtype, B, T, d, p);
+    case DPRC_OP_HUTCH_LAYERS:
+      if (k < 1 || k > 256) return 0;
+      return std::max(hutch_ws(dtype, B, T, d, p, k),
+                      plan_tc(DPRC_OP_HUTCH, B, T, d, p, k, kMaxFusedLayers).total);
   }
   return 0;
 }
@@ -320,9 +355,8 @@ dprc_status dprc_norm_hutch(const void* A, const void* G, const void* P, dprc_dt
     if (fused_hutch_supported(k)) {
       // one launch: sketch and projection as two phases of one kernel
       bool launched = false;
-      cudaError_t e = launch_tc_hutch_fused(A, G, P, B, T, d, p, k, w + t.w_off, t.tpad,
-                                            reinterpret_cast<int*>(w + t.ready_off), stick, cnorm,
-                                            n, accumulate, s, &launched);
+      cudaError_t e = launch_tc_hutch_layers(1, &A, &G, &P, &d, &p, B, T, k, fused_scratch(t, w),
+                                             n, accumulate, s, &launched);
       if (launched) {
         mark(1, s);
         mark(2, s);
@@ -354,6 +388,55 @@ dprc_status dprc_norm_hutch(const void* A, const void* G, const void* P, dprc_dt
   e = launch_simt_norm_finish(Y, B, d, ik, ik, 1.0f, n, accumulate, s);
   mark(2, s);
   return cuda_status(e);
+}
+
+dprc_status dprc_norm_hutch_layers(int64_t L, const void* const* A, const void* const* G,
+                                   const void* const* P, const int64_t* d, const int64_t* p,
+                                   dprc_dtype dtype, int64_t B, int64_t T, int64_t k, float* n,
+                                   int accumulate, void* ws, size_t ws_bytes, void* stream) {
+  if (!A || !G || !P || !d || !p || !n) return DPRC_ERR_NULL;
+  if (L < 1 || L > (int64_t(1) << 20)) return DPRC_ERR_SHAPE;
+  if (k < 1 || k > 256) return DPRC_ERR_SHAPE;
+  int64_t dmax = 0, pmax = 0;
+  bool fused = fused_hutch_supported(k);
+  for (int64_t l = 0; l < L; ++l) {
+    if (!A[l] || !G[l] || !P[l]) return DPRC_ERR_NULL;
+    const dprc_status st = check_common(dtype, B, T, d[l], p[l]);
+    if (st != DPRC_OK) return st;
+    if (!aligned16(A[l]) || !aligned16(G[l]) || !aligned16(P[l])) return DPRC_ERR_ALIGN;
+    dmax = std::max(dmax, d[l]);
+    pmax = std::max(pmax, p[l]);
+    fused = fused && tc_path_supported(dtype, B, T, d[l], p[l], k, false);
+  }
+  if (!aligned16(n)) return DPRC_ERR_ALIGN;
+  if (!ws) return DPRC_ERR_WORKSPACE;
+  if (!aligned16(ws)) return DPRC_ERR_ALIGN;
+  if (ws_bytes < dprc_workspace_bytes(DPRC_OP_HUTCH_LAYERS, dtype, B, T, dmax, pmax, k))
+    return DPRC_ERR_WORKSPACE;
+  if (!device_ok()) return DPRC_ERR_DEVICE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int64_t l0 = 0;
+  if (fused) {
+    const TcPlan t = plan_tc(DPRC_OP_HUTCH, B, T, dmax, pmax, k, kMaxFusedLayers);
+    const FusedScratch f = fused_scratch(t, static_cast<char*>(ws));
+    for (; l0 < L; l0 += kMaxFusedLayers) {
+      const int Lc = static_cast<int>(std::min<int64_t>(kMaxFusedLayers, L - l0));
+      bool launched = false;
+      const cudaError_t e = launch_tc_hutch_layers(Lc, A + l0, G + l0, P + l0, d + l0, p + l0, B,
+                                                   T, k, f, n, accumulate || l0 > 0, s,
+                                                   &launched);
+      if (!launched) {
+        if (e != cudaSuccess) (void)cudaGetLastError();
+        break;  // the remaining layers one call at a time
+      }
+    }
+  }
+  for (int64_t l = l0; l < L; ++l) {
+    const dprc_status st = dprc_norm_hutch(A[l], G[l], P[l], dtype, B, T, d[l], p[l], k, n,
+                                           accumulate || l > 0, ws, ws_bytes, stream);
+    if (st != DPRC_OK) return st;
+  }
+  return DPRC_OK;
 }
 
 int dprc_norm_hutch_launches(dprc_dtype dtype, int64_t B, int64_t T, int64_t d, int64_t p,

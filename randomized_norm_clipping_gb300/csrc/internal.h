@@ -24,12 +24,24 @@ struct BlockSched {
 BlockSched make_block_sched(int64_t nblocks, int upb, int slots);
 
 // Scratch layout of the tensor-core path of one Hutchinson or Hutch++ call.
+// Most layers one fused Hutchinson launch takes (the per-layer tensor maps
+// travel in the kernel parameters); calls with more layers use several
+// launches.
+constexpr int kMaxFusedLayers = 56;
+
 struct TcPlan {
   int64_t tpad = 0;           // row stride (elements) of the [B][2n][tpad] sketches
-  size_t stick_off = 0;       // per-sample tickets int32 [B] (zero between calls)
-  size_t ready_off = 0;       // per-sample sketch-ready counters int32 [B] (zero between calls)
-  size_t cnorm_off = 0;       // per-block squared norms fp32 [B * chunks]
+  // counter block (zero between calls), the same for every plan:
+  size_t stick_off = 0;       // tickets int32 [kMaxFusedLayers][B] (row 0: per-sample tickets)
+  size_t ready_off = 0;       // sketch-ready counters int32 [kMaxFusedLayers][B]
+  size_t lticket_off = 0;     // layers finished per sample int32 [B]
+  size_t done2_off = 0;       // projection blocks finished per layer int32 [kMaxFusedLayers]
+  size_t exit_off = 0;        // CTAs finished int32 [1]
+  // scratch:
+  size_t cnorm_off = 0;       // per-block squared norms fp32 [layers][B][chunks]
+  size_t nl_off = 0;          // per-layer norms fp32 [layers][B]
   size_t w_off = 0, w_bytes = 0;  // sketch G P (or G S, A Z, G [Q|P']) hi/lo bf16
+  size_t w2_off = 0;          // second sketch buffer (multi-layer calls; = w_off otherwise)
   size_t z_off = 0;           // Hutch++: Z hi/lo bf16 [B][d][2r]
   size_t m_off = 0;           // Hutch++: M = O S fp32 [B][p][r]
   size_t qp_off = 0;          // Hutch++: [Q | P'] hi/lo bf16 [B][p][4r]
@@ -66,7 +78,10 @@ BlockSched colproj_sched(int64_t B, int64_t T, int64_t c, int nmma);
 
 // Bytes of the counter block every workspace starts with (zero between calls).
 size_t ctrl_bytes(int64_t B);
-TcPlan plan_tc(dprc_op op, int64_t B, int64_t T, int64_t d, int64_t p, int64_t k);
+// `layers`: layer slots of the per-layer scratch (1 for single-layer calls,
+// kMaxFusedLayers with two sketch buffers for dprc_norm_hutch_layers).
+TcPlan plan_tc(dprc_op op, int64_t B, int64_t T, int64_t d, int64_t p, int64_t k,
+               int layers = 1);
 SimtPlan plan_simt(dprc_op op, int64_t B, int64_t T, int64_t d, int64_t p, int64_t k);
 size_t plan_exact_bytes(dprc_dtype dt, int64_t B, int64_t T, int64_t d, int64_t p);
 
@@ -130,18 +145,32 @@ cudaError_t launch_qr_project(const float* M, int64_t B, int64_t p, int r, const
 // partial per tile (fgc_partials(B, d, p) floats), summed per sample in index
 // order into n_out.  bf16, d and p multiples of 8.
 int64_t fgc_partials(int64_t B, int64_t d, int64_t p);
-// Fused Hutchinson (sketch and projection as two phases of one cooperative
-// launch), k = 16 or 32.  Returns cudaSuccess with *launched false when the
-// kernel cannot run with this shape or device (the caller then uses the two
-// kernels); ready and tickets must be zero and are zero again afterwards.
+// Fused Hutchinson: sketch and projection of 1..kMaxFusedLayers layers as
+// phases of one cooperative launch (bf16, k = 16 or 32, one B and T for all
+// layers).  n_out (+)= the layer sum.  Returns cudaSuccess with *launched
+// false when the kernel cannot run with these shapes on this device (the
+// caller then uses the two-kernel path); the counters must be zero and are
+// zero again afterwards.
+struct FusedScratch {
+  void* W[2];           // sketch buffers (layer parity); W[1] may equal W[0] for one layer
+  int64_t tpad;
+  int* ready;           // [kMaxFusedLayers][B]
+  int* tickets;         // [kMaxFusedLayers][B]
+  int* lticket;         // [B]
+  int* done2;           // [kMaxFusedLayers]
+  int* exit_count;      // [1]
+  float* chunk_norms;   // [layers][B][chunks]
+  float* nl;            // [layers][B]
+};
+FusedScratch fused_scratch(const TcPlan& t, char* ws);
 bool fused_hutch_supported(int64_t k);
 // Whether a dprc_norm_hutch call with these sizes takes the fused kernel on
 // the current device (the same decision the launcher makes).
 bool fused_hutch_planned(int64_t B, int64_t T, int64_t d, int64_t p, int64_t k);
-cudaError_t launch_tc_hutch_fused(const void* A, const void* G, const void* P, int64_t B,
-                                  int64_t T, int64_t d, int64_t p, int64_t k, void* W,
-                                  int64_t tpad, int* ready, int* tickets, float* chunk_norms,
-                                  float* n_out, int accumulate, cudaStream_t s, bool* launched);
+cudaError_t launch_tc_hutch_layers(int L, const void* const* A, const void* const* G,
+                                   const void* const* P, const int64_t* d, const int64_t* p,
+                                   int64_t B, int64_t T, int64_t k, const FusedScratch& ws,
+                                   float* n_out, int accumulate, cudaStream_t s, bool* launched);
 cudaError_t launch_tc_exact_direct(const void* A, const void* G, int64_t B, int64_t T, int64_t d,
                                    int64_t p, float* partials, float* n_out, int accumulate,
                                    cudaStream_t s);

@@ -1,49 +1,55 @@
-// One-launch Hutchinson estimate on tensor cores:
+// Hutchinson estimates of one or many layers in one launch, on tensor cores:
 //
-//   n_i (+)= || A_i^T (G_i P) ||_F^2
+//   n_i (+)= sum_l || A_l,i^T (G_l,i P_l) ||_F^2
 //
 // ("Efficient DP-SGD for LLMs with Randomized Clipping", papernotes.org,
 // "Key design > Hutchinson": the sketch G P first, then Y = A^T (G P), then
-// its squared Frobenius norm).
+// its squared Frobenius norm; "Overall framework": the layerwise sum).
 //
-// The two contractions of tc_proj.cu (the sketch W_i = G_i P and the
-// projection Y_i = A_i^T W_i) run as two phases of one persistent kernel
-// instead of two launches:
+// Each layer is two contractions (those of tc_proj.cu): the sketch
+// W_i = G_i P and the projection Y_i = A_i^T W_i.  One persistent cooperative
+// kernel runs them as phases, layer after layer:
 //
-//   phase 1  every CTA takes sketch blocks (128 tokens of one sample) and
-//            writes W_i as bf16 hi/lo planes [B][2k][T_pad]; after each block
-//            it adds one to the per-sample counter ready[i] (release);
-//   phase 2  every CTA takes projection blocks (sample i, 128 rows of d);
-//            its TMA producer issues the A tiles at once, waits until
-//            ready[i] has reached the number of sketch blocks of sample i
-//            (acquire), then loads the W tiles; the epilogue squares Y and
-//            a per-sample ticket sums the blocks in order into n_i.
+//   phase 1 (sketch)      CTAs take blocks of 128 tokens of one sample and write
+//                         W_i as bf16 hi/lo planes; each block then adds one to
+//                         the counter ready[l][i] (release);
+//   phase 2 (projection)  CTAs take blocks (sample i, 128 rows of d); the TMA
+//                         producer issues the A tiles at once, waits until
+//                         ready[l][i] is complete (acquire), then loads W; the
+//                         epilogue squares Y and a per-(layer, sample) ticket
+//                         sums the blocks in order.
 //
-// This removes the second launch, the wait for the first grid to drain and
-// the projection's pipeline ramp, and lets the A stream of phase 2 start
-// while the last sketch tiles are still in flight.  The cross-CTA waits are
-// safe because the launch is cooperative (every CTA is resident) and phase 1
-// never waits on another CTA; every wait is bounded (2 s) and records a code
-// in the device error word when it runs out.
+// A CTA that finishes its share of layer l moves straight on to layer l + 1,
+// so one layer's start-up and tail overlap its neighbours' streaming.  The
+// sketch is double-buffered by layer parity: before phase 1 of layer l writes
+// buffer l % 2, it waits until every projection block of layer l - 2 (the
+// previous user of that buffer) has finished.  Per-layer results go to
+// n_l[l][i]; the last layer to finish sample i adds them in layer order
+// (deterministic) into n_i.
+//
+// The cross-CTA waits are safe because the launch is cooperative (every CTA
+// is resident) and every wait is on work that comes earlier in the one order
+// all CTAs follow (layer, then phase); every wait is bounded (2 s) and
+// records a code in the device error word when it runs out.
 //
 // Each phase assigns blocks either whole, strided over the CTAs, or one at a
 // time to a thread-block cluster whose CTAs split the block's units and
 // reduce the fp32 partials through distributed shared memory (credits make
-// the receive buffer reusable across blocks and phases).
+// the receive buffer reusable across blocks, phases and layers).
 //
-// Counters: the last block of sample i (ticket) resets ready[i] and the
-// ticket to zero, so the counter block is zero after every call and must be
-// zero before the first.
+// Counters (ready, tickets, per-sample layer tickets, per-layer projection
+// counts) are reset by their last user, so they are zero after every call and
+// must be zero before the first.
 //
-// One CTA per SM (the driver counts tensor-memory kernels at one CTA per SM,
-// and a cooperative launch cannot exceed that), with a 192 KB shared-memory
-// ring so that each SM keeps as many bytes in flight as two CTAs of the
-// two-kernel path.  Both phases use four slots of R/4 bytes; phase-2 slot c
-// overlays phase-1 slot c and is first filled once that has been consumed.
-// A sketch stage is 128 tokens x 128 p of G (two TMA boxes, 256 contiguous
-// bytes per row) plus 128 rows of P; a projection stage 128 tokens x 128 d
-// of A plus the matching 128 tokens of the sketch.  TMEM: phase-1 accumulators (2 x 32
-// columns) and phase-2 accumulators (2 x 2k columns), 256 columns.
+// One CTA per SM: the driver counts tensor-memory kernels at one CTA per SM,
+// and a cooperative launch cannot exceed that.  The shared-memory ring has 4
+// slots of 48 KB used by both phases: a sketch stage is 128 tokens x 128 p of
+// G (two TMA boxes, 256 contiguous bytes per row) plus 128 rows of P; a
+// projection stage 128 tokens x 128 d of A plus the matching 128 tokens of the
+// sketch.  TMEM: sketch accumulators (2 x 32 columns) and projection
+// accumulators (2 x 2k columns), 256 columns.  Per-layer tensor maps travel as
+// kernel parameters (at most kMaxLayers per launch; more layers take several
+// launches that accumulate).
 
 #include <atomic>
 
@@ -57,13 +63,12 @@ namespace {
 constexpr int kTok = 128;   // tokens per sketch block; tokens per projection unit
 constexpr int kCol = 128;   // columns of p per sketch unit (two 64-column boxes)
 constexpr int kRows = 128;  // rows of d per projection block
+constexpr int kStages = 4;  // ring slots
 
 template <int K>
 struct HCfg {
   static constexpr int kNR = K;       // sketch MMA N
   static constexpr int kNC = 2 * K;   // projection MMA N (hi | lo)
-  static constexpr int kRowStages = 4;
-  static constexpr int kColStages = 4;
   static constexpr int kRowGBox = kTok * 64 * 2;     // 16 KB: 128 tokens x 64 p
   static constexpr int kRowG = 2 * kRowGBox;         // 128 p
   static constexpr int kRowP = kCol * kNR * 2;       // 128 p x K
@@ -73,19 +78,16 @@ struct HCfg {
   static constexpr int kColWBox = kNC * 64 * 2;      // 2K rows x 64 tokens
   static constexpr int kColW = 2 * kColWBox;
   static constexpr int kColStage = kColA + kColW;
-  static constexpr int kRing = kColStages * kColStage;
-  static constexpr int kRowSlot = kRing / kRowStages;
-  static constexpr int kColSlot = kRing / kColStages;
+  static constexpr int kSlot = kColStage > kRowStage ? kColStage : kRowStage;
+  static constexpr int kRing = kStages * kSlot;
   static constexpr int kAccR = K < 32 ? 32 : K;
   static constexpr int kColAcc0 = 2 * kAccR;
   static constexpr int kTmemCols = 256;
-  static constexpr int kBars = 2 * kRowStages + 2 * kColStages + 8 + 4;  // + exchange
+  static constexpr int kBars = 2 * kStages + 8 + 4;  // ring, accumulators, exchange
   static constexpr int xchg(int cl) { return cl <= 1 ? 0 : (cl - 1) * (kRows / cl) * K * 4; }
   static constexpr int kCtrl = 1024;  // barriers, TMEM slot, flags, norms
   static constexpr int smem(int cl) { return 1024 + kRing + kCtrl + xchg(cl); }
-  static_assert(kRowSlot >= kRowStage && kRowSlot % 1024 == 0, "sketch slot");
-  static_assert(kRowStages % kColStages == 0, "projection slots overlay whole sketch slots");
-  static_assert(kColSlot % 1024 == 0, "projection slot");
+  static_assert(kSlot % 1024 == 0, "slots keep the 1024-byte alignment of swizzled tiles");
   static_assert(kColAcc0 + 2 * kNC <= kTmemCols, "TMEM columns");
   static_assert(K == 16 || K == 32, "k = 16 or 32");
 };
@@ -94,21 +96,6 @@ struct Phase {
   int split;          // 1: one block per cluster, units split by rank
   long long nblocks;  // blocks of this phase
   int upb;            // units per block
-};
-
-struct HArgs {
-  int T, p, d;
-  int mtiles;    // sketch blocks per sample
-  int nchunks;   // projection blocks per sample
-  long long tpad;
-  Phase ph1, ph2;
-  int ready_target;  // ready[i] value meaning "W_i complete"
-  __nv_bfloat16* W;
-  int* ready;        // [B]
-  int* tickets;      // [B]
-  float* chunk_norms;  // [B * nchunks]
-  float* n_out;
-  int accumulate;
 };
 
 // Blocks and units of this CTA in one phase.
@@ -229,27 +216,48 @@ __device__ __forceinline__ bool xchg_rows(const Xchg& xs, int cl, int rank, int 
   return mine_row;
 }
 
-template <int K>
-__global__ void __launch_bounds__(192, 1)
-    tc_hutch_kernel(const __grid_constant__ CUtensorMap map_g,
-                    const __grid_constant__ CUtensorMap map_p,
-                    const __grid_constant__ CUtensorMap map_a,
-                    const __grid_constant__ CUtensorMap map_w, const HArgs a, const int cl) {
+// One layer of a launch.  The tensor maps live in the kernel parameters.
+struct LayerDesc {
+  CUtensorMap mg, mp, ma;  // G [B][T][p], P [p][k], A [B][T][d]
+  int d, p, nchunks;       // nchunks = projection blocks per sample
+  int ready_target;        // ready[l][i] value meaning "W_l,i complete"
+  Phase ph1, ph2;
+};
+
+template <int CAP>
+struct HParams {
+  CUtensorMap mw[2];       // the two sketch buffers, [B][2k][T_pad]
+  int L, B, T, mtiles;     // layers; batch; tokens; sketch blocks per sample
+  int cl;                  // cluster size of the launch
+  int maxch;               // stride of chunk_norms per (layer, sample)
+  long long tpad;
+  __nv_bfloat16* W[2];
+  int* ready;              // [L][B]
+  int* tickets;            // [L][B]
+  int* lticket;            // [B]   layers finished per sample
+  int* done2;              // [L]   projection blocks finished per layer
+  int* exit_count;         // [1]
+  float* chunk_norms;      // [L][B][maxch]
+  float* nl;               // [L][B]
+  float* n_out;
+  int accumulate;
+  LayerDesc layer[CAP];     // CAP = 1 for single-layer calls: a small parameter block
+};
+
+template <int K, int CAP>
+__global__ void __launch_bounds__(192, 1) tc_hutch_kernel(const __grid_constant__ HParams<CAP> a) {
   using Cfg = HCfg<K>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ float s_red[4];
 
   uint8_t* ring = align_1024(smem_raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(ring + Cfg::kRing);
-  constexpr int RS = Cfg::kRowStages, CS = Cfg::kColStages;
-  uint64_t* full_r = bars;              // [RS]
-  uint64_t* empty_r = full_r + RS;      // [RS]
-  uint64_t* full_c = empty_r + RS;      // [CS]
-  uint64_t* empty_c = full_c + CS;      // [CS]
-  uint64_t* accf_r = empty_c + CS;      // [2]
-  uint64_t* acce_r = accf_r + 2;        // [2]
-  uint64_t* accf_c = acce_r + 2;        // [2]
-  uint64_t* acce_c = accf_c + 2;        // [2]
+  uint64_t* full = bars;                  // [kStages]
+  uint64_t* empty = full + kStages;       // [kStages]
+  uint64_t* accf_r = empty + kStages;     // [2]
+  uint64_t* acce_r = accf_r + 2;          // [2]
+  uint64_t* accf_c = acce_r + 2;          // [2]
+  uint64_t* acce_c = accf_c + 2;          // [2]
   Xchg xs;
   xs.recv_bar = acce_c + 2;
   xs.free_bar = acce_c + 3;
@@ -263,22 +271,14 @@ __global__ void __launch_bounds__(192, 1)
   // a dependent launch (the clip factors) may start now; it waits for this
   // grid's completion before reading anything
   pdl_launch_dependents();
+  const int nlayers = CAP == 1 ? 1 : a.L;  // a constant for single-layer launches
+  const int cl = a.cl;
   const int rank = cl > 1 ? static_cast<int>(cluster_ctarank()) : 0;
-  const Mine m1 = mine(a.ph1, cl, rank);
-  const Mine m2 = mine(a.ph2, cl, rank);
-  const long long nb1 = count_blocks(a.ph1, m1);
-  const long long nb2 = count_blocks(a.ph2, m2);
-  const int nu1 = m1.uhi - m1.ulo;
-  const int nu2 = m2.uhi - m2.ulo;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < RS; ++s) {
-      mbar_init(&full_r[s], 1);
-      mbar_init(&empty_r[s], 1);
-    }
-    for (int s = 0; s < CS; ++s) {
-      mbar_init(&full_c[s], 1);
-      mbar_init(&empty_c[s], 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&accf_r[s], 1);
@@ -295,10 +295,14 @@ __global__ void __launch_bounds__(192, 1)
     *abort_flag = 0;
   }
   if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&map_g);
-    tma_prefetch_desc(&map_p);
-    tma_prefetch_desc(&map_a);
-    tma_prefetch_desc(&map_w);
+    tma_prefetch_desc(&a.mw[0]);
+    tma_prefetch_desc(&a.mw[1]);
+    for (int l = 0; l < nlayers && l < 4; ++l) {
+      const LayerDesc& Ld = a.layer[CAP == 1 ? 0 : l];
+      tma_prefetch_desc(&Ld.mg);
+      tma_prefetch_desc(&Ld.mp);
+      tma_prefetch_desc(&Ld.ma);
+    }
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, Cfg::kTmemCols);
@@ -314,178 +318,193 @@ __global__ void __launch_bounds__(192, 1)
     // ---------------- TMA producer ----------------
     if (lane == 0) {
       bool ok = true;
-      long long it1 = 0;
-      for (long long j = 0; j < nb1 && ok; ++j) {
-        const long long b = m1.first + j * m1.step;
-        const int i = static_cast<int>(b / a.mtiles);
-        const int t0 = static_cast<int>(b - static_cast<long long>(i) * a.mtiles) * kTok;
-        for (int u = m1.ulo; u < m1.uhi; ++u, ++it1) {
-          const int s = static_cast<int>(it1 % RS);
-          if (!mbar_wait(&empty_r[s], (static_cast<uint32_t>(it1 / RS) & 1) ^ 1,
-                         DPRC_DEVERR_PIPE_EMPTY)) {
-            ok = false;
-            *abort_flag = 1;
-            break;
-          }
-          uint8_t* slot = ring + s * Cfg::kRowSlot;
-          mbar_arrive_expect_tx(&full_r[s], Cfg::kRowStage);
+      long long it = 0;  // stages issued (both phases, all layers)
+      auto take_slot = [&](long long i) -> int {
+        const int s = static_cast<int>(i % kStages);
+        if (!mbar_wait(&empty[s], (static_cast<uint32_t>(i / kStages) & 1) ^ 1,
+                       DPRC_DEVERR_PIPE_EMPTY))
+          ok = false;
+        return s;
+      };
+      for (int l = 0; l < nlayers && ok; ++l) {
+        const LayerDesc& Ld = a.layer[CAP == 1 ? 0 : l];
+        if (CAP > 1 && l + 4 < nlayers) {
+          const LayerDesc& Ln = a.layer[CAP == 1 ? 0 : l + 4];
+          tma_prefetch_desc(&Ln.mg);
+          tma_prefetch_desc(&Ln.mp);
+          tma_prefetch_desc(&Ln.ma);
+        }
+        // phase 1: G and P tiles
+        const Mine m1 = mine(Ld.ph1, cl, rank);
+        const long long nb1 = count_blocks(Ld.ph1, m1);
+        for (long long j = 0; j < nb1 && ok; ++j) {
+          const long long b = m1.first + j * m1.step;
+          const int i = static_cast<int>(b / a.mtiles);
+          const int t0 = static_cast<int>(b - static_cast<long long>(i) * a.mtiles) * kTok;
+          for (int u = m1.ulo; u < m1.uhi; ++u) {
+            const int s = take_slot(it);
+            if (!ok) break;
+            uint8_t* slot = ring + s * Cfg::kSlot;
+            mbar_arrive_expect_tx(&full[s], Cfg::kRowStage);
 #pragma unroll
-          for (int h = 0; h < 2; ++h)
-            tma_load_3d(slot + h * Cfg::kRowGBox, &map_g, &full_r[s], u * kCol + h * 64, t0, i);
-          tma_load_3d(slot + Cfg::kRowG, &map_p, &full_r[s], 0, u * kCol, 0);
+            for (int h = 0; h < 2; ++h)
+              tma_load_3d(slot + h * Cfg::kRowGBox, &Ld.mg, &full[s], u * kCol + h * 64, t0, i);
+            tma_load_3d(slot + Cfg::kRowG, &Ld.mp, &full[s], 0, u * kCol, 0);
+            ++it;
+          }
         }
-      }
-      // Phase 2.  The A tiles do not depend on phase 1: before waiting for a
-      // new sample's sketch, up to CS stages of A are put in flight; otherwise
-      // the A and W tiles of a stage go out together.  Two cursors walk the
-      // stages (one division per block, not per stage: this thread paces the
-      // whole pipeline).
-      struct Cursor {
-        long long j = 0;  // block index within this CTA's list
-        int u = 0, i = 0, ch = 0;
-      };
-      auto seek = [&](Cursor& c) {
-        const long long b = m2.first + c.j * m2.step;
-        c.i = static_cast<int>(b / a.nchunks);
-        c.ch = static_cast<int>(b - static_cast<long long>(c.i) * a.nchunks);
-      };
-      auto advance = [&](Cursor& c) {
-        if (++c.u == m2.uhi) {
-          c.u = m2.ulo;
-          ++c.j;
-          if (c.j < nb2) seek(c);
+        // phase 2: A tiles, then, once sample i's sketch is complete, W tiles.
+        // Before waiting for a new sample's sketch, up to kStages stages of A
+        // go out; otherwise the A and W tiles of a stage go out together.  Two
+        // cursors walk the stages (one division per block: this thread paces
+        // the whole pipeline).
+        const Mine m2 = mine(Ld.ph2, cl, rank);
+        const long long nb2 = count_blocks(Ld.ph2, m2);
+        const int nu2 = m2.uhi - m2.ulo;
+        const long long total2 = nb2 * nu2;
+        struct Cursor {
+          long long j = 0;
+          int u = 0, i = 0, ch = 0;
+        };
+        auto seek = [&](Cursor& c) {
+          const long long b = m2.first + c.j * m2.step;
+          c.i = static_cast<int>(b / Ld.nchunks);
+          c.ch = static_cast<int>(b - static_cast<long long>(c.i) * Ld.nchunks);
+        };
+        auto advance = [&](Cursor& c) {
+          if (++c.u == m2.uhi) {
+            c.u = m2.ulo;
+            ++c.j;
+            if (c.j < nb2) seek(c);
+          }
+        };
+        Cursor ca, cw;
+        ca.u = cw.u = m2.ulo;
+        if (nb2 > 0) {
+          seek(ca);
+          seek(cw);
         }
-      };
-      const long long total2 = nb2 * nu2;
-      Cursor ca, cw;
-      ca.u = cw.u = m2.ulo;
-      if (nb2 > 0) {
-        seek(ca);
-        seek(cw);
-      }
-      long long it2 = 0, w_ptr = 0;  // stages with A issued / with W issued
-      int ready_i = -1;
-      while (w_ptr < total2) {
-        const bool need_wait = ok && cw.i != ready_i;
-        const long long ahead = need_wait ? CS : 1;
-        const long long a_to = w_ptr + ahead < total2 ? w_ptr + ahead : total2;
-        while (ok && it2 < a_to) {
-          const int s = static_cast<int>(it2 % CS);
-          if (it2 < CS) {
-            // first use of this slot: the sketch slots under it are consumed
-            constexpr int kPer = RS / CS;
-            for (int q = kPer * s; q < kPer * s + kPer && ok; ++q) {
-              const long long uses = it1 > q ? (it1 - 1 - q) / RS + 1 : 0;
-              if (uses > 0 && !mbar_wait(&empty_r[q], static_cast<uint32_t>(uses - 1) & 1,
-                                         DPRC_DEVERR_PIPE_EMPTY))
-                ok = false;
+        const long long base = it;     // global index of this phase's first stage
+        long long w_done = 0;          // stages of this phase with W issued
+        int ready_i = -1;
+        while (w_done < total2) {
+          const bool need_wait = ok && cw.i != ready_i;
+          const long long ahead = need_wait ? kStages : 1;
+          const long long a_to = w_done + ahead < total2 ? w_done + ahead : total2;
+          while (ok && it - base < a_to) {
+            const int s = take_slot(it);
+            if (!ok) break;
+            uint8_t* slot = ring + s * Cfg::kSlot;
+            mbar_arrive_expect_tx(&full[s], Cfg::kColStage);
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+              tma_load_3d(slot + h * Cfg::kColABox, &Ld.ma, &full[s], ca.ch * kRows + h * 64,
+                          ca.u * kTok, ca.i);
+            ++it;
+            advance(ca);
+          }
+          if (w_done >= it - base) break;  // nothing left to complete (after an error)
+          if (need_wait) {
+            if (wait_geq(&a.ready[l * a.B + cw.i], Ld.ready_target)) {
+              fence_proxy_async_global();
+              ready_i = cw.i;
+            } else {
+              ok = false;  // still load W so the issued stages complete; results are void
             }
-          } else if (!mbar_wait(&empty_c[s], (static_cast<uint32_t>(it2 / CS) & 1) ^ 1,
-                                DPRC_DEVERR_PIPE_EMPTY)) {
-            ok = false;
           }
-          if (!ok) break;
-          uint8_t* slot = ring + s * Cfg::kColSlot;
-          mbar_arrive_expect_tx(&full_c[s], Cfg::kColStage);
+          const long long g = base + w_done;
+          const int s = static_cast<int>(g % kStages);
+          uint8_t* slot = ring + s * Cfg::kSlot;
 #pragma unroll
           for (int h = 0; h < 2; ++h)
-            tma_load_3d(slot + h * Cfg::kColABox, &map_a, &full_c[s], ca.ch * kRows + h * 64,
-                        ca.u * kTok, ca.i);
-          ++it2;
-          advance(ca);
+            tma_load_3d(slot + Cfg::kColA + h * Cfg::kColWBox, &a.mw[l & 1], &full[s],
+                        cw.u * kTok + h * 64, 0, cw.i);
+          ++w_done;
+          advance(cw);
         }
-        if (w_ptr >= it2) break;  // nothing left to complete (after an error)
-        if (need_wait && ok) {
-          if (wait_geq(&a.ready[cw.i], a.ready_target)) {
-            fence_proxy_async_global();
-            ready_i = cw.i;
-          } else {
-            ok = false;  // still load W so the issued stages complete; results are void
-          }
-        }
-        const int s = static_cast<int>(w_ptr % CS);
-        uint8_t* slot = ring + s * Cfg::kColSlot;
-#pragma unroll
-        for (int h = 0; h < 2; ++h)
-          tma_load_3d(slot + Cfg::kColA + h * Cfg::kColWBox, &map_w, &full_c[s],
-                      cw.u * kTok + h * 64, 0, cw.i);
-        ++w_ptr;
-        advance(cw);
       }
       if (!ok) *abort_flag = 1;
       // let every copy this thread issued land before the CTA can exit
-      for (long long k = it1 - 1; k >= 0 && k >= it1 - RS; --k)
-        mbar_wait(&full_r[k % RS], static_cast<uint32_t>(k / RS) & 1, DPRC_DEVERR_PIPE_FULL);
-      for (long long k = it2 - 1; k >= 0 && k >= it2 - CS; --k)
-        mbar_wait(&full_c[k % CS], static_cast<uint32_t>(k / CS) & 1, DPRC_DEVERR_PIPE_FULL);
+      for (long long k = it - 1; k >= 0 && k >= it - kStages; --k)
+        mbar_wait(&full[k % kStages], static_cast<uint32_t>(k / kStages) & 1,
+                  DPRC_DEVERR_PIPE_FULL);
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
       bool ok = true;
-      long long it1 = 0;
+      long long it = 0, seg1 = 0, seg2 = 0;
       constexpr uint32_t idesc1 = make_idesc_bf16(128, Cfg::kNR, false, true);
       constexpr uint32_t p_swz = swz_code_for_bytes(2 * Cfg::kNR);
-      for (long long j = 0; j < nb1 && ok; ++j) {
-        const int abuf = static_cast<int>(j & 1);
-        if (!mbar_wait(&acce_r[abuf], (static_cast<uint32_t>(j >> 1) & 1) ^ 1, DPRC_DEVERR_ACCUM)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        for (int u = 0; u < nu1; ++u, ++it1) {
-          const int s = static_cast<int>(it1 % RS);
-          if (!mbar_wait(&full_r[s], static_cast<uint32_t>(it1 / RS) & 1, DPRC_DEVERR_PIPE_FULL)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t ga = smem_u32(ring + s * Cfg::kRowSlot);
-          const uint32_t pa = ga + Cfg::kRowG;
-#pragma unroll
-          for (int kk = 0; kk < kCol / 16; ++kk) {
-            // G tile: two boxes of 128 token rows x 64 p, K-major, 128-byte swizzle.
-            const uint64_t ad =
-                make_sdesc(ga + (kk >> 2) * Cfg::kRowGBox + (kk & 3) * 32, 16, 1024, kSwz128);
-            // P tile: 128 p rows x K columns, MN-major, one swizzle atom wide.
-            const uint64_t bd = make_sdesc(pa + kk * 32 * Cfg::kNR, 16, 16 * Cfg::kNR, p_swz);
-            umma_bf16(tmem + abuf * Cfg::kAccR, ad, bd, idesc1, (u == 0 && kk == 0) ? 0u : 1u);
-          }
-          umma_commit(&empty_r[s]);
-        }
-        if (ok) umma_commit(&accf_r[abuf]);
-      }
-      long long it2 = 0;
       constexpr uint32_t idesc2 = make_idesc_bf16(128, Cfg::kNC, true, false);
-      for (long long j = 0; j < nb2 && ok; ++j) {
-        const int abuf = static_cast<int>(j & 1);
-        if (!mbar_wait(&acce_c[abuf], (static_cast<uint32_t>(j >> 1) & 1) ^ 1, DPRC_DEVERR_ACCUM)) {
+      auto wait_full = [&](long long i) -> int {
+        const int s = static_cast<int>(i % kStages);
+        if (!mbar_wait(&full[s], static_cast<uint32_t>(i / kStages) & 1, DPRC_DEVERR_PIPE_FULL))
           ok = false;
-          break;
-        }
-        tc_fence_after();
-        for (int u = 0; u < nu2; ++u, ++it2) {
-          const int s = static_cast<int>(it2 % CS);
-          if (!mbar_wait(&full_c[s], static_cast<uint32_t>(it2 / CS) & 1, DPRC_DEVERR_PIPE_FULL)) {
+        return s;
+      };
+      for (int l = 0; l < nlayers && ok; ++l) {
+        const LayerDesc& Ld = a.layer[CAP == 1 ? 0 : l];
+        const Mine m1 = mine(Ld.ph1, cl, rank);
+        const long long nb1 = count_blocks(Ld.ph1, m1);
+        for (long long j = 0; j < nb1 && ok; ++j, ++seg1) {
+          const int abuf = static_cast<int>(seg1 & 1);
+          if (!mbar_wait(&acce_r[abuf], (static_cast<uint32_t>(seg1 >> 1) & 1) ^ 1,
+                         DPRC_DEVERR_ACCUM)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t xa = smem_u32(ring + s * Cfg::kColSlot);
-          const uint32_t wa = xa + Cfg::kColA;
+          for (int u = m1.ulo; u < m1.uhi; ++u, ++it) {
+            const int s = wait_full(it);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t ga = smem_u32(ring + s * Cfg::kSlot);
+            const uint32_t pa = ga + Cfg::kRowG;
 #pragma unroll
-          for (int kk = 0; kk < kTok / 16; ++kk) {
-            // A^T: 128 d (two 64-d atoms, LBO = one box) x 16 tokens (SBO 1 KB).
-            const uint64_t ad = make_sdesc(xa + kk * 2048, Cfg::kColABox, 1024, kSwz128);
-            // Sketch: 2K rows x 64 tokens per box, K-major, 128-byte swizzle.
-            const uint64_t bd =
-                make_sdesc(wa + (kk >> 2) * Cfg::kColWBox + (kk & 3) * 32, 16, 1024, kSwz128);
-            umma_bf16(tmem + Cfg::kColAcc0 + abuf * Cfg::kNC, ad, bd, idesc2,
-                      (u == 0 && kk == 0) ? 0u : 1u);
+            for (int kk = 0; kk < kCol / 16; ++kk) {
+              // G: two boxes of 128 token rows x 64 p, K-major, 128-byte swizzle.
+              const uint64_t ad =
+                  make_sdesc(ga + (kk >> 2) * Cfg::kRowGBox + (kk & 3) * 32, 16, 1024, kSwz128);
+              // P: 128 p rows x K columns, MN-major, one swizzle atom wide.
+              const uint64_t bd = make_sdesc(pa + kk * 32 * Cfg::kNR, 16, 16 * Cfg::kNR, p_swz);
+              umma_bf16(tmem + abuf * Cfg::kAccR, ad, bd, idesc1,
+                        (u == m1.ulo && kk == 0) ? 0u : 1u);
+            }
+            umma_commit(&empty[s]);
           }
-          umma_commit(&empty_c[s]);
+          if (ok) umma_commit(&accf_r[abuf]);
         }
-        if (ok) umma_commit(&accf_c[abuf]);
+        const Mine m2 = mine(Ld.ph2, cl, rank);
+        const long long nb2 = count_blocks(Ld.ph2, m2);
+        for (long long j = 0; j < nb2 && ok; ++j, ++seg2) {
+          const int abuf = static_cast<int>(seg2 & 1);
+          if (!mbar_wait(&acce_c[abuf], (static_cast<uint32_t>(seg2 >> 1) & 1) ^ 1,
+                         DPRC_DEVERR_ACCUM)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          for (int u = m2.ulo; u < m2.uhi; ++u, ++it) {
+            const int s = wait_full(it);
+            if (!ok) break;
+            tc_fence_after();
+            const uint32_t xa = smem_u32(ring + s * Cfg::kSlot);
+            const uint32_t wa = xa + Cfg::kColA;
+#pragma unroll
+            for (int kk = 0; kk < kTok / 16; ++kk) {
+              // A^T: 128 d (two 64-d atoms, LBO = one box) x 16 tokens (SBO 1 KB).
+              const uint64_t ad = make_sdesc(xa + kk * 2048, Cfg::kColABox, 1024, kSwz128);
+              // Sketch: 2K rows x 64 tokens per box, K-major, 128-byte swizzle.
+              const uint64_t bd =
+                  make_sdesc(wa + (kk >> 2) * Cfg::kColWBox + (kk & 3) * 32, 16, 1024, kSwz128);
+              umma_bf16(tmem + Cfg::kColAcc0 + abuf * Cfg::kNC, ad, bd, idesc2,
+                        (u == m2.ulo && kk == 0) ? 0u : 1u);
+            }
+            umma_commit(&empty[s]);
+          }
+          if (ok) umma_commit(&accf_c[abuf]);
+        }
       }
       if (!ok) *abort_flag = 1;
     }
@@ -496,126 +515,187 @@ __global__ void __launch_bounds__(192, 1)
     const int row = q * 32 + lane;  // row of the 128-row tile = TMEM lane
     const uint32_t lane_base = static_cast<uint32_t>(q * 32) << 16;
     bool ok = true;
+    long long seg1 = 0, seg2 = 0;
+    // split projection blocks so far: the same sequence on every rank of the
+    // cluster (seg2 also counts whole blocks, whose number differs by CTA)
+    long long nsplit2 = 0;
     int rnd = 0;  // cluster exchange rounds so far
-    const int rounds = (a.ph1.split ? static_cast<int>(nb1) : 0) +
-                       (a.ph2.split ? static_cast<int>(nb2) : 0);
-    // phase 1: sketch rows -> W hi/lo, then count the block done
-    for (long long j = 0; j < nb1; ++j) {
-      const int abuf = static_cast<int>(j & 1);
-      bool live = ok &&
-                  mbar_wait(&accf_r[abuf], static_cast<uint32_t>(j >> 1) & 1, DPRC_DEVERR_ACCUM) &&
-                  *abort_flag == 0;
-      live = __all_sync(0xffffffffu, live);  // keep the warp's TMEM loads convergent
-      if (!live) ok = false;
-      tc_fence_after();
-      float y[K];
-#pragma unroll
-      for (int t = 0; t < K; ++t) y[t] = 0.f;
-      if (live) tmem_ld_cols<K>(tmem + lane_base + abuf * Cfg::kAccR, y);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&acce_r[abuf]);
-      bool mine_row = true;
-      if (a.ph1.split) {
-        mine_row = xchg_rows<K>(xs, cl, rank, row, rnd, rnd + 1 == rounds, y, ok);
-        ++rnd;
-      }
-      const long long b = m1.first + j * m1.step;
-      const int i = static_cast<int>(b / a.mtiles);
-      const int t = static_cast<int>(b - static_cast<long long>(i) * a.mtiles) * kTok + row;
-      if (mine_row && ok && t < a.T) {
-        __nv_bfloat16* wi = a.W + static_cast<size_t>(i) * 2 * K * a.tpad + t;
-#pragma unroll
-        for (int c = 0; c < K; ++c) {
-          __nv_bfloat16 hi, lo;
-          split_hilo(y[c], hi, lo);
-          wi[static_cast<size_t>(c) * a.tpad] = hi;
-          wi[static_cast<size_t>(K + c) * a.tpad] = lo;
-        }
-      }
-      fence_proxy_async_global();  // these rows are read by TMA (async proxy)
-      named_bar_sync(1, 128);
-      if (ew == 0 && lane == 0 && ok) {
-        __threadfence();
-        atomicAdd(&a.ready[i], 1);
-      }
+    int rounds = 0;
+    for (int l = 0; l < nlayers; ++l) {
+      const LayerDesc& Ld = a.layer[CAP == 1 ? 0 : l];
+      if (Ld.ph1.split) rounds += static_cast<int>(count_blocks(Ld.ph1, mine(Ld.ph1, cl, rank)));
+      if (Ld.ph2.split) rounds += static_cast<int>(count_blocks(Ld.ph2, mine(Ld.ph2, cl, rank)));
     }
-    // phase 2: squared norms of the projection blocks
-    for (long long j = 0; j < nb2; ++j) {
-      const int abuf = static_cast<int>(j & 1);
-      bool live = ok &&
-                  mbar_wait(&accf_c[abuf], static_cast<uint32_t>(j >> 1) & 1, DPRC_DEVERR_ACCUM) &&
-                  *abort_flag == 0;
-      live = __all_sync(0xffffffffu, live);
-      if (!live) ok = false;
-      tc_fence_after();
-      float y[K];
-#pragma unroll
-      for (int t = 0; t < K; ++t) y[t] = 0.f;
-      if (live) {
-        const uint32_t tb = tmem + lane_base + Cfg::kColAcc0 + abuf * Cfg::kNC;
-        float hi[K], lo[K];
-        tmem_ld_cols<K>(tb, hi);
-        tmem_ld_cols<K>(tb + K, lo);
-#pragma unroll
-        for (int t = 0; t < K; ++t) y[t] = hi[t] + lo[t];
+    for (int l = 0; l < nlayers; ++l) {
+      const LayerDesc& Ld = a.layer[CAP == 1 ? 0 : l];
+      __nv_bfloat16* W = a.W[l & 1];
+      // phase 1: sketch rows -> W hi/lo, then count the block done
+      const Mine m1 = mine(Ld.ph1, cl, rank);
+      const long long nb1 = count_blocks(Ld.ph1, m1);
+      if (CAP > 1 && nb1 > 0 && l >= 2) {
+        // the previous user of this sketch buffer (layer l - 2) must be done
+        if (threadIdx.x == 64 && ok &&
+            !wait_geq(&a.done2[l - 2], static_cast<int>(a.layer[CAP == 1 ? 0 : l - 2].ph2.nblocks)))
+          *abort_flag = 1;
+        named_bar_sync(1, 128);
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&acce_c[abuf]);
-      bool mine_row = true;
-      if (a.ph2.split) {
-        mine_row = xchg_rows<K>(xs, cl, rank, row, rnd, rnd + 1 == rounds, y, ok);
-        ++rnd;
-      }
-      const long long b = m2.first + j * m2.step;
-      const int i = static_cast<int>(b / a.nchunks);
-      const int ch = static_cast<int>(b - static_cast<long long>(i) * a.nchunks);
-      float sq = 0.f;
-      if (mine_row && ok && ch * kRows + row < a.d) {
+      for (long long j = 0; j < nb1; ++j, ++seg1) {
+        const int abuf = static_cast<int>(seg1 & 1);
+        bool live = ok &&
+                    mbar_wait(&accf_r[abuf], static_cast<uint32_t>(seg1 >> 1) & 1,
+                              DPRC_DEVERR_ACCUM) &&
+                    *abort_flag == 0;
+        live = __all_sync(0xffffffffu, live);  // keep the warp's TMEM loads convergent
+        if (!live) ok = false;
+        tc_fence_after();
+        float y[K];
 #pragma unroll
-        for (int t = 0; t < K; ++t) sq = fmaf(y[t], y[t], sq);
-      }
+        for (int t = 0; t < K; ++t) y[t] = 0.f;
+        if (live) tmem_ld_cols<K>(tmem + lane_base + abuf * Cfg::kAccR, y);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acce_r[abuf]);
+        bool mine_row = true;
+        if (Ld.ph1.split) {
+          mine_row = xchg_rows<K>(xs, cl, rank, row, rnd, rnd + 1 == rounds, y, ok);
+          ++rnd;
+        }
+        const long long b = m1.first + j * m1.step;
+        const int i = static_cast<int>(b / a.mtiles);
+        const int t = static_cast<int>(b - static_cast<long long>(i) * a.mtiles) * kTok + row;
+        if (mine_row && ok && t < a.T) {
+          __nv_bfloat16* wi = W + static_cast<size_t>(i) * 2 * K * a.tpad + t;
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, off);
-      if (lane == 0) s_red[ew] = sq;
-      named_bar_sync(1, 128);
-      if (ew == 0 && lane == 0) {
-        const float part = (s_red[0] + s_red[1]) + (s_red[2] + s_red[3]);
-        float chunk = part;
-        bool leader = true;
-        if (a.ph2.split) {
-          float* nb = xs.norms + (j & 1) * 8;
-          if (rank != 0) {
-            st_cluster_f32(map_to_rank(nb + rank, 0), part);
-            mbar_arrive_remote(map_to_rank(&xs.norm_bar[j & 1], 0));
-            leader = false;
-          } else {
-            if (!mbar_wait_cluster(&xs.norm_bar[j & 1], static_cast<uint32_t>(j >> 1) & 1,
-                                   DPRC_DEVERR_CLUSTER))
-              ok = false;
-            nb[0] = part;
-            chunk = 0.f;
-            for (int s = 0; s < cl; ++s) chunk += nb[s];
+          for (int c = 0; c < K; ++c) {
+            __nv_bfloat16 hi, lo;
+            split_hilo(y[c], hi, lo);
+            wi[static_cast<size_t>(c) * a.tpad] = hi;
+            wi[static_cast<size_t>(K + c) * a.tpad] = lo;
           }
         }
-        if (leader && ok) {
-          a.chunk_norms[b] = chunk;
+        fence_proxy_async_global();  // these rows are read by TMA (async proxy)
+        named_bar_sync(1, 128);
+        if (ew == 0 && lane == 0 && ok) {
           __threadfence();
-          const int old = atomicAdd(&a.tickets[i], 1);
-          if (old == a.nchunks - 1) {
-            // last block of sample i: sum its blocks in order, reset the counters
-            __threadfence();
-            float sum = 0.f;
-            for (int c = 0; c < a.nchunks; ++c)
-              sum += __ldcg(&a.chunk_norms[static_cast<size_t>(i) * a.nchunks + c]);
-            a.n_out[i] = (a.accumulate ? a.n_out[i] : 0.f) + sum;
-            a.tickets[i] = 0;
-            a.ready[i] = 0;
-          }
+          atomicAdd(&a.ready[l * a.B + i], 1);
         }
       }
-      named_bar_sync(1, 128);
+      // phase 2: squared norms of the projection blocks
+      const Mine m2 = mine(Ld.ph2, cl, rank);
+      const long long nb2 = count_blocks(Ld.ph2, m2);
+      for (long long j = 0; j < nb2; ++j, ++seg2) {
+        const int abuf = static_cast<int>(seg2 & 1);
+        bool live = ok &&
+                    mbar_wait(&accf_c[abuf], static_cast<uint32_t>(seg2 >> 1) & 1,
+                              DPRC_DEVERR_ACCUM) &&
+                    *abort_flag == 0;
+        live = __all_sync(0xffffffffu, live);
+        if (!live) ok = false;
+        tc_fence_after();
+        float y[K];
+#pragma unroll
+        for (int t = 0; t < K; ++t) y[t] = 0.f;
+        if (live) {
+          const uint32_t tb = tmem + lane_base + Cfg::kColAcc0 + abuf * Cfg::kNC;
+          float hi[K], lo[K];
+          tmem_ld_cols<K>(tb, hi);
+          tmem_ld_cols<K>(tb + K, lo);
+#pragma unroll
+          for (int t = 0; t < K; ++t) y[t] = hi[t] + lo[t];
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&acce_c[abuf]);
+        bool mine_row = true;
+        if (Ld.ph2.split) {
+          mine_row = xchg_rows<K>(xs, cl, rank, row, rnd, rnd + 1 == rounds, y, ok);
+          ++rnd;
+        }
+        const long long b = m2.first + j * m2.step;
+        const int i = static_cast<int>(b / Ld.nchunks);
+        const int ch = static_cast<int>(b - static_cast<long long>(i) * Ld.nchunks);
+        float sq = 0.f;
+        if (mine_row && ok && ch * kRows + row < Ld.d) {
+#pragma unroll
+          for (int t = 0; t < K; ++t) sq = fmaf(y[t], y[t], sq);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, off);
+        if (lane == 0) s_red[ew] = sq;
+        named_bar_sync(1, 128);
+        if (ew == 0) {
+          // warp 2: lane 0 gathers the block's norm; the whole warp finishes
+          // a sample (the chunk and layer sums read many L2 lines: one per lane)
+          const float part = (s_red[0] + s_red[1]) + (s_red[2] + s_red[3]);
+          float chunk = part;
+          int leader = 1;
+          if (lane == 0 && Ld.ph2.split) {
+            float* nb = xs.norms + (nsplit2 & 1) * 8;
+            if (rank != 0) {
+              st_cluster_f32(map_to_rank(nb + rank, 0), part);
+              mbar_arrive_remote(map_to_rank(&xs.norm_bar[nsplit2 & 1], 0));
+              leader = 0;
+            } else {
+              if (!mbar_wait_cluster(&xs.norm_bar[nsplit2 & 1],
+                                     static_cast<uint32_t>(nsplit2 >> 1) & 1, DPRC_DEVERR_CLUSTER))
+                ok = false;
+              nb[0] = part;
+              chunk = 0.f;
+              for (int s = 0; s < cl; ++s) chunk += nb[s];
+            }
+          }
+          leader = __shfl_sync(0xffffffffu, leader, 0);
+          const bool lok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+          if (!lok) ok = false;
+          if (leader && lok) {
+            const size_t li = static_cast<size_t>(l) * a.B + i;
+            int last = 0;
+            if (lane == 0) {
+              a.chunk_norms[li * a.maxch + ch] = chunk;
+              __threadfence();
+              last = atomicAdd(&a.tickets[li], 1) == Ld.nchunks - 1;
+            }
+            if (__shfl_sync(0xffffffffu, last, 0)) {
+              // last block of (layer l, sample i): its norm, summed in a fixed order
+              __threadfence();
+              float sum = 0.f;
+              for (int c = lane; c < Ld.nchunks; c += 32) sum += __ldcg(&a.chunk_norms[li * a.maxch + c]);
+#pragma unroll
+              for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+              int final_layer = 0;
+              if (lane == 0) {
+                a.tickets[li] = 0;
+                a.ready[li] = 0;
+                if (CAP == 1) {
+                  // one layer: no layer sum to wait for
+                  a.n_out[i] = (a.accumulate ? a.n_out[i] : 0.f) + sum;
+                } else {
+                  a.nl[li] = sum;
+                  __threadfence();
+                  final_layer = atomicAdd(&a.lticket[i], 1) == a.L - 1;
+                }
+              }
+              if (CAP > 1 && __shfl_sync(0xffffffffu, final_layer, 0)) {
+                // last layer of sample i: the layer sum, in a fixed order
+                __threadfence();
+                float tot = 0.f;
+                for (int ll = lane; ll < a.L; ll += 32)
+                  tot += __ldcg(&a.nl[static_cast<size_t>(ll) * a.B + i]);
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, off);
+                if (lane == 0) {
+                  a.n_out[i] = (a.accumulate ? a.n_out[i] : 0.f) + tot;
+                  a.lticket[i] = 0;
+                }
+              }
+            }
+            // this block no longer reads the sketch buffer of layer l
+            if (CAP > 1 && lane == 0) atomicAdd(&a.done2[l], 1);
+          }
+        }
+        named_bar_sync(1, 128);
+        if (Ld.ph2.split) ++nsplit2;
+      }
     }
   }
 
@@ -627,9 +707,17 @@ __global__ void __launch_bounds__(192, 1)
     tmem_dealloc(tmem, Cfg::kTmemCols);
   }
   if (cl > 1) cluster_sync_all();  // no peer still addresses this CTA's shared memory
+  if (CAP > 1 && threadIdx.x == 0) {
+    // the last CTA out clears the per-layer projection counts for the next call
+    __threadfence();
+    if (atomicAdd(a.exit_count, 1) == static_cast<int>(gridDim.x) - 1) {
+      for (int l = 0; l < a.L; ++l) a.done2[l] = 0;
+      *a.exit_count = 0;
+    }
+  }
 }
 
-template <int K>
+template <int K, int CAP>
 cudaError_t set_smem_once() {
   constexpr int kMaxDev = 64;
   static std::atomic<int> done[kMaxDev];
@@ -637,7 +725,7 @@ cudaError_t set_smem_once() {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 0 && dev < kMaxDev && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
-  e = cudaFuncSetAttribute(tc_hutch_kernel<K>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  e = cudaFuncSetAttribute(tc_hutch_kernel<K, CAP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            HCfg<K>::smem(8));
   if (e == cudaSuccess && dev >= 0 && dev < kMaxDev) done[dev].store(1, std::memory_order_release);
   return e;
@@ -646,7 +734,7 @@ cudaError_t set_smem_once() {
 // CTAs of this kernel that may run at once in one cooperative launch with
 // clusters of cl: the driver's occupancy figures (one CTA per SM: the
 // tensor-memory kernels are counted as such), cached per device and cl.
-template <int K>
+template <int K, int CAP>
 int resident_ctas(int cl) {
   constexpr int kMaxDev = 64;
   static std::atomic<int> cache[kMaxDev][4];
@@ -658,8 +746,8 @@ int resident_ctas(int cl) {
   const int smem = HCfg<K>::smem(cl);
   if (cl == 1) {
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, tc_hutch_kernel<K>, 192, smem) !=
-        cudaSuccess)
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, tc_hutch_kernel<K, CAP>, 192,
+                                                      smem) != cudaSuccess)
       return 0;
     v = per_sm * device_sm_count();
   } else {
@@ -675,36 +763,36 @@ int resident_ctas(int cl) {
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     int ncl = 0;
-    if (cudaOccupancyMaxActiveClusters(&ncl, tc_hutch_kernel<K>, &cfg) != cudaSuccess) return 0;
+    if (cudaOccupancyMaxActiveClusters(&ncl, tc_hutch_kernel<K, CAP>, &cfg) != cudaSuccess)
+      return 0;
     v = ncl * cl;
   }
   cache[dev][ci].store(v, std::memory_order_release);
   return v;
 }
 
-template <int K>
-cudaError_t launch_k(const CUtensorMap& mg, const CUtensorMap& mp, const CUtensorMap& ma,
-                     const CUtensorMap& mw, const HArgs& a, int grid, int cl, cudaStream_t s) {
+template <int K, int CAP>
+cudaError_t launch_k(const HParams<CAP>& a, int grid, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(192);
-  cfg.dynamicSmemBytes = HCfg<K>::smem(cl);
+  cfg.dynamicSmemBytes = HCfg<K>::smem(a.cl);
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
   int na = 0;
   attr[na].id = cudaLaunchAttributeCooperative;
   attr[na].val.cooperative = 1;
   ++na;
-  if (cl > 1) {
+  if (a.cl > 1) {
     attr[na].id = cudaLaunchAttributeClusterDimension;
-    attr[na].val.clusterDim.x = cl;
+    attr[na].val.clusterDim.x = a.cl;
     attr[na].val.clusterDim.y = 1;
     attr[na].val.clusterDim.z = 1;
     ++na;
   }
   cfg.attrs = attr;
   cfg.numAttrs = na;
-  return cudaLaunchKernelEx(&cfg, tc_hutch_kernel<K>, mg, mp, ma, mw, a, cl);
+  return cudaLaunchKernelEx(&cfg, tc_hutch_kernel<K, CAP>, a);
 }
 
 // Cluster size a phase of `nblocks` blocks of `upb` units wants on `slots`
@@ -717,6 +805,78 @@ int want_cl(long long nblocks, int upb, int slots) {
   return cl;
 }
 
+// Devices on which the cooperative launch was refused once keep using the
+// two-kernel path.
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_refused[kMaxDevices];
+
+// Schedule of one launch over layers [0, L): the phases of every layer, the
+// cluster size and the grid.  False when the kernel cannot run here.
+template <int CAP>
+bool plan_fused(int L, const int64_t* d, const int64_t* p, int64_t B, int64_t T, int64_t k,
+                HParams<CAP>& a, int& grid_out) {
+  if (!fused_hutch_supported(k) || L < 1 || L > CAP) return false;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+  if (g_refused[dev].load(std::memory_order_acquire)) return false;
+  const int ik = static_cast<int>(k);
+  const int slots = device_sm_count();  // one CTA per SM
+  a.L = L;
+  a.B = static_cast<int>(B);
+  a.T = static_cast<int>(T);
+  a.mtiles = static_cast<int>((T + kTok - 1) / kTok);
+  int cl = 1, maxch = 1;
+  for (int l = 0; l < L; ++l) {
+    LayerDesc& Ld = a.layer[l];
+    Ld.d = static_cast<int>(d[l]);
+    Ld.p = static_cast<int>(p[l]);
+    Ld.nchunks = static_cast<int>((d[l] + kRows - 1) / kRows);
+    Ld.ph1.nblocks = B * a.mtiles;
+    Ld.ph1.upb = static_cast<int>((p[l] + kCol - 1) / kCol);
+    Ld.ph2.nblocks = B * Ld.nchunks;
+    Ld.ph2.upb = a.mtiles;
+    const int c1 = want_cl(Ld.ph1.nblocks, Ld.ph1.upb, slots);
+    const int c2 = want_cl(Ld.ph2.nblocks, Ld.ph2.upb, slots);
+    Ld.ph1.split = c1;  // the wanted cluster size, until cl is known
+    Ld.ph2.split = c2;
+    cl = c1 > cl ? c1 : cl;
+    cl = c2 > cl ? c2 : cl;
+    maxch = Ld.nchunks > maxch ? Ld.nchunks : maxch;
+  }
+  if ((ik == 16 ? set_smem_once<16, CAP>() : set_smem_once<32, CAP>()) != cudaSuccess) return false;
+  const int resident = ik == 16 ? resident_ctas<16, CAP>(cl) : resident_ctas<32, CAP>(cl);
+  if (resident < cl) return false;
+  for (int l = 0; l < L; ++l) {
+    LayerDesc& Ld = a.layer[l];
+    Ld.ph1.split = Ld.ph1.split > 1 && Ld.ph1.upb >= cl ? 1 : 0;
+    Ld.ph2.split = Ld.ph2.split > 1 && Ld.ph2.upb >= cl ? 1 : 0;
+    Ld.ready_target = a.mtiles * (Ld.ph1.split ? cl : 1);
+  }
+  // Grid: the multiple of cl (up to what is resident) that minimises the
+  // bytes the busiest CTA streams over all phases of all layers (a sketch
+  // unit is 32 KB of G, a projection unit 32 KB of A); ties go to the smaller
+  // grid.
+  long long grid = 0, best = -1;
+  for (long long ncl = 1; ncl * cl <= resident; ++ncl) {
+    const long long g = ncl * cl;
+    auto busiest = [&](const Phase& ph) {
+      if (ph.split) return (ph.nblocks + ncl - 1) / ncl * ((ph.upb + cl - 1) / cl);
+      return (ph.nblocks + g - 1) / g * ph.upb;
+    };
+    long long cost = 0;
+    for (int l = 0; l < L; ++l) cost += busiest(a.layer[l].ph1) + busiest(a.layer[l].ph2);
+    if (best < 0 || cost < best) {
+      best = cost;
+      grid = g;
+    }
+  }
+  if (grid < cl) return false;
+  a.cl = cl;
+  a.maxch = maxch;
+  grid_out = static_cast<int>(grid);
+  return true;
+}
+
 }  // namespace
 
 cudaError_t read_device_error_hutch(int32_t* out, bool reset) {
@@ -725,98 +885,47 @@ cudaError_t read_device_error_hutch(int32_t* out, bool reset) {
 
 bool fused_hutch_supported(int64_t k) { return k == 16 || k == 32; }
 
+bool fused_hutch_planned(int64_t B, int64_t T, int64_t d, int64_t p, int64_t k) {
+  HParams<1> a;
+  int grid = 0;
+  return plan_fused(1, &d, &p, B, T, k, a, grid);
+}
+
 namespace {
 
-// Devices on which the cooperative launch was refused once keep using the
-// two-kernel path.
-constexpr int kMaxDevices = 64;
-std::atomic<int> g_refused[kMaxDevices];
-
-// Schedule of one fused launch (phases, cluster size, grid); false when the
-// kernel cannot run with these sizes on the current device.
-bool plan_fused(int64_t B, int64_t T, int64_t d, int64_t p, int64_t k, HArgs& a, int& grid_out,
-                int& cl_out) {
-  if (!fused_hutch_supported(k)) return false;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
-  if (g_refused[dev].load(std::memory_order_acquire)) return false;
+template <int CAP>
+cudaError_t launch_cap(int L, const void* const* A, const void* const* G, const void* const* P,
+                       const int64_t* d, const int64_t* p, int64_t B, int64_t T, int64_t k,
+                       const FusedScratch& ws, float* n_out, int accumulate, cudaStream_t s,
+                       bool* launched) {
+  static thread_local HParams<CAP> a;  // up to ~26 KB: kept off the stack
+  int grid = 0;
+  if (!plan_fused(L, d, p, B, T, k, a, grid)) return cudaSuccess;
   const int ik = static_cast<int>(k);
-  const int slots = device_sm_count();  // one CTA per SM
-  a.T = static_cast<int>(T);
-  a.p = static_cast<int>(p);
-  a.d = static_cast<int>(d);
-  a.mtiles = static_cast<int>((T + kTok - 1) / kTok);
-  a.nchunks = static_cast<int>((d + kRows - 1) / kRows);
-  a.ph1.nblocks = B * a.mtiles;
-  a.ph1.upb = static_cast<int>((p + kCol - 1) / kCol);
-  a.ph2.nblocks = B * a.nchunks;
-  a.ph2.upb = a.mtiles;
-  const int cl1 = want_cl(a.ph1.nblocks, a.ph1.upb, slots);
-  const int cl2 = want_cl(a.ph2.nblocks, a.ph2.upb, slots);
-  const int cl = cl1 > cl2 ? cl1 : cl2;
-  if ((ik == 16 ? set_smem_once<16>() : set_smem_once<32>()) != cudaSuccess) return false;
-  const int resident = ik == 16 ? resident_ctas<16>(cl) : resident_ctas<32>(cl);
-  if (resident < cl) return false;
-  a.ph1.split = cl1 > 1 && a.ph1.upb >= cl ? 1 : 0;
-  a.ph2.split = cl2 > 1 && a.ph2.upb >= cl ? 1 : 0;
-  // Grid: the multiple of cl (up to what is resident) that minimises the
-  // bytes the busiest CTA streams in the two phases (a sketch unit is 32 KB of
-  // G, a projection unit 32 KB of A); ties go to the smaller grid.
-  long long grid = 0, best = -1;
-  for (long long ncl = 1; ncl * cl <= resident; ++ncl) {
-    const long long g = ncl * cl;
-    auto busiest = [&](const Phase& ph, long long unit_bytes) {
-      if (ph.split)
-        return (ph.nblocks + ncl - 1) / ncl * ((ph.upb + cl - 1) / cl) * unit_bytes;
-      return (ph.nblocks + g - 1) / g * ph.upb * unit_bytes;
-    };
-    const long long cost = busiest(a.ph1, 32) + busiest(a.ph2, 32);
-    if (best < 0 || cost < best) {
-      best = cost;
-      grid = g;
-    }
-  }
-  if (grid < cl) return false;
-  a.ready_target = a.mtiles * (a.ph1.split ? cl : 1);
-  grid_out = static_cast<int>(grid);
-  cl_out = cl;
-  return true;
-}
-
-}  // namespace
-
-bool fused_hutch_planned(int64_t B, int64_t T, int64_t d, int64_t p, int64_t k) {
-  HArgs a;
-  int grid = 0, cl = 0;
-  return plan_fused(B, T, d, p, k, a, grid, cl);
-}
-
-cudaError_t launch_tc_hutch_fused(const void* A, const void* G, const void* P, int64_t B,
-                                  int64_t T, int64_t d, int64_t p, int64_t k, void* W,
-                                  int64_t tpad, int* ready, int* tickets, float* chunk_norms,
-                                  float* n_out, int accumulate, cudaStream_t s, bool* launched) {
-  *launched = false;
-  HArgs a;
-  int grid = 0, cl = 0;
-  if (!plan_fused(B, T, d, p, k, a, grid, cl)) return cudaSuccess;
-  const int ik = static_cast<int>(k);
-  a.tpad = tpad;
-  a.W = static_cast<__nv_bfloat16*>(W);
-  a.ready = ready;
-  a.tickets = tickets;
-  a.chunk_norms = chunk_norms;
+  a.tpad = ws.tpad;
+  a.W[0] = static_cast<__nv_bfloat16*>(ws.W[0]);
+  a.W[1] = static_cast<__nv_bfloat16*>(ws.W[1]);
+  a.ready = ws.ready;
+  a.tickets = ws.tickets;
+  a.lticket = ws.lticket;
+  a.done2 = ws.done2;
+  a.exit_count = ws.exit_count;
+  a.chunk_norms = ws.chunk_norms;
+  a.nl = ws.nl;
   a.n_out = n_out;
   a.accumulate = accumulate;
-
-  CUtensorMap mg, mp, ma, mw;
-  if (!make_tmap_3d_bf16(&mg, G, p, T, B, p, T * p, 64, kTok, 128)) return cudaErrorInvalidValue;
-  if (!make_tmap_3d_bf16(&mp, P, ik, p, 1, ik, p * ik, ik, kCol, 2 * ik))
-    return cudaErrorInvalidValue;
-  if (!make_tmap_3d_bf16(&ma, A, d, T, B, d, T * d, 64, kTok, 128)) return cudaErrorInvalidValue;
-  if (!make_tmap_3d_bf16(&mw, W, T, 2 * ik, B, tpad, 2 * ik * tpad, 64, 2 * ik, 128))
-    return cudaErrorInvalidValue;
-  const cudaError_t e = ik == 16 ? launch_k<16>(mg, mp, ma, mw, a, grid, cl, s)
-                                 : launch_k<32>(mg, mp, ma, mw, a, grid, cl, s);
+  for (int b = 0; b < 2; ++b)
+    if (!make_tmap_3d_bf16(&a.mw[b], ws.W[b], T, 2 * ik, B, ws.tpad, 2 * ik * ws.tpad, 64,
+                           2 * ik, 128))
+      return cudaErrorInvalidValue;
+  for (int l = 0; l < L; ++l) {
+    LayerDesc& Ld = a.layer[l];
+    if (!make_tmap_3d_bf16(&Ld.mg, G[l], p[l], T, B, p[l], T * p[l], 64, kTok, 128) ||
+        !make_tmap_3d_bf16(&Ld.mp, P[l], ik, p[l], 1, ik, p[l] * ik, ik, kCol, 2 * ik) ||
+        !make_tmap_3d_bf16(&Ld.ma, A[l], d[l], T, B, d[l], T * d[l], 64, kTok, 128))
+      return cudaErrorInvalidValue;
+  }
+  const cudaError_t e = ik == 16 ? launch_k<16, CAP>(a, grid, s) : launch_k<32, CAP>(a, grid, s);
   if (e == cudaSuccess) {
     *launched = true;
   } else if (e == cudaErrorCooperativeLaunchTooLarge || e == cudaErrorNotSupported ||
@@ -826,6 +935,20 @@ cudaError_t launch_tc_hutch_fused(const void* A, const void* G, const void* P, i
       g_refused[dev].store(1, std::memory_order_release);
   }
   return e;
+}
+
+}  // namespace
+
+cudaError_t launch_tc_hutch_layers(int L, const void* const* A, const void* const* G,
+                                   const void* const* P, const int64_t* d, const int64_t* p,
+                                   int64_t B, int64_t T, int64_t k, const FusedScratch& ws,
+                                   float* n_out, int accumulate, cudaStream_t s,
+                                   bool* launched) {
+  *launched = false;
+  if (L == 1)
+    return launch_cap<1>(L, A, G, P, d, p, B, T, k, ws, n_out, accumulate, s, launched);
+  return launch_cap<kMaxFusedLayers>(L, A, G, P, d, p, B, T, k, ws, n_out, accumulate, s,
+                                     launched);
 }
 
 }  // namespace dprc

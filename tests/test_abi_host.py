@@ -114,6 +114,16 @@ def test_argument_errors_return_before_device_work(lib):
     assert n(_vp(A16 + 4), 10, ctypes.c_float(1.0), ctypes.c_float(1.0), 1, 1, None) == 4
     assert n(_vp(A16), 10, ctypes.c_float(-1.0), ctypes.c_float(1.0), 1, 1, None) == 2
     assert n(None, 0, ctypes.c_float(1.0), ctypes.c_float(1.0), 1, 1, None) == 0  # empty: no-op
+    L2 = ctypes.c_void_p * 2
+    I2 = ctypes.c_int64 * 2
+    ptrs, bad = L2(A16, A16), L2(A16, A16 + 2)
+    sizes = I2(8, 8)
+    hl = lib.dprc_norm_hutch_layers
+    assert hl(2, None, ptrs, ptrs, sizes, sizes, 1, 1, 1, 16, _vp(A16), 0, _vp(A16), ws, None) == 1
+    assert hl(0, ptrs, ptrs, ptrs, sizes, sizes, 1, 1, 1, 16, _vp(A16), 0, _vp(A16), ws, None) == 2
+    assert hl(2, ptrs, bad, ptrs, sizes, sizes, 1, 1, 1, 16, _vp(A16), 0, _vp(A16), ws, None) == 4
+    assert hl(2, ptrs, ptrs, ptrs, I2(8, 0), sizes, 1, 1, 1, 16, _vp(A16), 0, _vp(A16), ws, None) == 2
+    assert hl(2, ptrs, ptrs, ptrs, sizes, sizes, 1, 1, 1, 16, _vp(A16), 0, _vp(A16), 16, None) == 5
     w = lib.dprc_philox_words
     assert w(None, 4, 0, 1, 1, None) == 1
     assert w(None, 0, 0, 1, 1, None) == 0

@@ -328,3 +328,44 @@ def test_noise_full_gradient_buffer_sampled():
     assert np.all(np.abs(got - ref) <= _noise_tol(ref, 0.0, 1.0, 1.0, rad))
     del grad
     torch.cuda.empty_cache()
+
+
+# ------------------------------------------------------------------ many layers in one call
+
+def _layers(shapes, B, T, k, seed):
+    As, Gs, Ps = [], [], []
+    for j, (d, p) in enumerate(shapes):
+        A, G, P = _hutch_case(B, T, d, p, k, torch.bfloat16, seed=seed + 7 * j, gscale=0.1)
+        As.append(A)
+        Gs.append(G)
+        Ps.append(P)
+    return As, Gs, Ps
+
+
+@pytest.mark.parametrize("shapes,B,T,k", [
+    ([(256, 512), (512, 256), (128, 128), (256, 1024), (1024, 256)], 3, 300, 32),  # one launch
+    ([(128, 64), (64, 128)] * 31, 2, 130, 16),                                     # 62 layers: two launches
+    ([(256, 256), (512, 128)], 2, 200, 64),                                        # k = 64: layer by layer
+])
+def test_hutch_layers_matches_layer_sum(shapes, B, T, k):
+    As, Gs, Ps = _layers(shapes, B, T, k, seed=300 + T)
+    n = torch.full((B,), 0.5, device=DEV)
+    rnc.dprc_norm_hutch_layers([a.to(DEV) for a in As], [g.to(DEV) for g in Gs],
+                               [p_.to(DEV) for p_ in Ps], n, accumulate=True)
+    ref = oracle.layer_sum([oracle.hutch_norm(to_f64(A), to_f64(G), to_f64(P))
+                            for A, G, P in zip(As, Gs, Ps)])
+    assert _relerr(n.cpu() - 0.5, ref) < RTOL
+    assert rnc.dprc_device_error() == 0
+
+
+def test_hutch_layers_repeats_bitwise_and_reuses_its_workspace():
+    shapes = [(256, 512), (512, 512), (512, 256)] * 3
+    As, Gs, Ps = _layers(shapes, 4, 1000, 32, seed=11)
+    As, Gs, Ps = [a.to(DEV) for a in As], [g.to(DEV) for g in Gs], [p_.to(DEV) for p_ in Ps]
+    ws = rnc.workspace(rnc.DPRC_OP_HUTCH_LAYERS, As[0], 4, 1000, 512, 512, 32)
+    n1 = torch.zeros(4, device=DEV)
+    n2 = torch.zeros(4, device=DEV)
+    rnc.dprc_norm_hutch_layers(As, Gs, Ps, n1, ws=ws)
+    rnc.dprc_norm_hutch(As[0], Gs[0], Ps[0], torch.zeros(4, device=DEV), ws=ws)  # same workspace
+    rnc.dprc_norm_hutch_layers(As, Gs, Ps, n2, ws=ws)
+    assert torch.equal(n1, n2)
