@@ -33,6 +33,17 @@ def _hutch(name, layer=0):
     return lambda: rnc.dprc_norm_hutch(A, G, P, n, ws=ws)
 
 
+def _hutch_layers(B, T):
+    wk = wl.WORKLOADS["hutch_llama32_1b_112layers_b4_t4096_k32_bf16"]
+    nl = len(wl.LLAMA32_1B_BLOCK)
+    layers = [wl.layer_inputs(wk, j, device="cuda", B=B, T=T) for j in range(nl)]
+    As, Gs, Ps = [x[0] for x in layers], [x[1] for x in layers], [x[2] for x in layers]
+    n = torch.zeros(B, device="cuda")
+    ws = rnc.workspace(rnc.DPRC_OP_HUTCH_LAYERS, As[0], B, T, max(a.shape[2] for a in As),
+                       max(g.shape[2] for g in Gs), wk.k)
+    return lambda: rnc.dprc_norm_hutch_layers(As, Gs, Ps, n, ws=ws)
+
+
 def _hutchpp():
     wk = wl.WORKLOADS["hutchpp_q_proj_b8_t4096_r16_bf16"]
     lay = wk.layers[0]
@@ -68,6 +79,9 @@ CASES = {
     # B2 T32768 2048 -> 8192 and 8192 -> 2048, k32 bf16 (1.34 GB each)
     "hutch_long_up": lambda: _hutch("hutch_long_b2_t32768_up_down_k32_bf16", 0),
     "hutch_long_down": lambda: _hutch("hutch_long_b2_t32768_up_down_k32_bf16", 1),
+    # one Llama-3.2-1B decoder block (q, k, v, o, gate, up, down) in one
+    # dprc_norm_hutch_layers call, B2 T2048 (0.37 GB of A and G)
+    "hutch_layers_block_b2_t2048": lambda: _hutch_layers(2, 2048),
     # Hutch++ B8 T4096 d = p = 2048 r16 bf16
     "hutchpp_q_proj": _hutchpp,
     # the noise kernel on 2^27 fp32 elements (1.07 GB read + written), a slice of
