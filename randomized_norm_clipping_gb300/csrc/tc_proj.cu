@@ -578,15 +578,17 @@ __global__ void __launch_bounds__(192, ColCfg<NMMA>::kCtasPerSm)
         for (int off = 16; off > 0; off >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, off);
         if (lane == 0) s_red[ew] = sq;
         named_bar_sync(1, 128);
-        if (ew == 0 && lane == 0) {
+        if (ew == 0) {
+          // warp 2: lane 0 gathers the chunk's norm; the whole warp sums a
+          // finished sample's chunks (one L2 line per lane, fixed order)
           const float part = (s_red[0] + s_red[1]) + (s_red[2] + s_red[3]);
           float chunk = part;
-          bool leader = true;
-          if (sc.cl > 1) {
+          int leader = 1;
+          if (lane == 0 && sc.cl > 1) {
             if (wk.rank != 0) {
               st_cluster_f32(map_to_rank(xs.norms + wk.rank, 0), part);
               mbar_arrive_remote(map_to_rank(xs.norm_bar, 0));
-              leader = false;
+              leader = 0;
             } else {
               if (!mbar_wait_cluster(xs.norm_bar, 0, DPRC_DEVERR_CLUSTER)) ok = false;
               xs.norms[0] = part;
@@ -594,17 +596,27 @@ __global__ void __launch_bounds__(192, ColCfg<NMMA>::kCtasPerSm)
               for (int s = 0; s < sc.cl; ++s) chunk += xs.norms[s];
             }
           }
-          if (leader && ok) {
-            a.chunk_norms[b] = chunk;
-            __threadfence();
-            const int old = atomicAdd(&a.sample_tickets[i], 1);
-            if (old == a.nchunks - 1) {
+          leader = __shfl_sync(0xffffffffu, leader, 0);
+          const bool lok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+          if (!lok) ok = false;
+          if (leader && lok) {
+            int last = 0;
+            if (lane == 0) {
+              a.chunk_norms[b] = chunk;
+              __threadfence();
+              last = atomicAdd(&a.sample_tickets[i], 1) == a.nchunks - 1;
+            }
+            if (__shfl_sync(0xffffffffu, last, 0)) {
               __threadfence();
               float sum = 0.f;
-              for (int c2 = 0; c2 < a.nchunks; ++c2)
+              for (int c2 = lane; c2 < a.nchunks; c2 += 32)
                 sum += __ldcg(&a.chunk_norms[static_cast<size_t>(i) * a.nchunks + c2]);
-              a.n_out[i] = (a.accumulate ? a.n_out[i] : 0.f) + sum;
-              a.sample_tickets[i] = 0;
+#pragma unroll
+              for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+              if (lane == 0) {
+                a.n_out[i] = (a.accumulate ? a.n_out[i] : 0.f) + sum;
+                a.sample_tickets[i] = 0;
+              }
             }
           }
         }
