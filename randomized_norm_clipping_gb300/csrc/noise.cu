@@ -107,9 +107,15 @@ __device__ __forceinline__ float4 add_noise4(float4 g, uint4 w, float scale) {
   return g;
 }
 
-// Each thread keeps kNoiseUnroll 16-byte loads in flight (issued before any
-// arithmetic) so the stream stays busy while the generator runs.
-constexpr int kNoiseUnroll = 4;
+// Each thread issues kNoiseUnroll 16-byte loads before any arithmetic, and
+// the grid holds kNoiseCtasPerSm CTAs per SM (eight resident at a time) that
+// stride over the buffer.  A sweep on GB300 (unroll 1-16, 128-512 threads,
+// 8 CTAs per SM up to one CTA per tile) put the optimum at two loads per
+// thread and 64-96 CTAs per SM: enough independent warps to hide the load
+// latency behind the generator, without the register cost of deeper unrolls
+// or the tail of one-tile CTAs.
+constexpr int kNoiseUnroll = 2;
+constexpr int kNoiseCtasPerSm = 64;
 
 __global__ void __launch_bounds__(256) noise_kernel(float* __restrict__ grad, long long n,
                                                     float scale, uint64_t seed, uint64_t step) {
@@ -173,10 +179,10 @@ __global__ void clip_kernel(const float* __restrict__ n, long long B, float C,
   c[i] = out;
 }
 
-int grid_for(long long work, int threads) {
+int grid_for(long long work, int threads, int ctas_per_sm = 8) {
   const int sms = device_sm_count();
   long long blocks = (work + threads - 1) / threads;
-  const long long cap = static_cast<long long>(sms) * 8;  // 8 x 256 threads per SM
+  const long long cap = static_cast<long long>(sms) * ctas_per_sm;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
   return static_cast<int>(blocks);
@@ -187,8 +193,8 @@ int grid_for(long long work, int threads) {
 cudaError_t launch_noise(float* grad, int64_t N, float sigma, float C, uint64_t seed,
                          uint64_t step, cudaStream_t s) {
   if (N == 0) return cudaSuccess;
-  noise_kernel<<<grid_for(N / 4 / kNoiseUnroll + 1, 256), 256, 0, s>>>(grad, N, sigma * C, seed,
-                                                                     step);
+  noise_kernel<<<grid_for(N / 4 / kNoiseUnroll + 1, 256, kNoiseCtasPerSm), 256, 0, s>>>(
+      grad, N, sigma * C, seed, step);
   return cudaGetLastError();
 }
 
