@@ -16,6 +16,7 @@ norms   exact norm (direct, ghost, trace forms), Hutchinson, Hutch++, layerwise
         sum, clip factors.
 philox  Philox4x32-10 counter-based generator (Salmon et al., SC'11), the
         uniform -> normal transform and the Gaussian noise add.
+rademacher  the +-1 projection variant (signs from the Philox stream, 1/k scale).
 cost    the analytic FLOP / memory counts behind the pages' efficiency table.
 
 Parity status: every function here is pinned by a ``-m "not gpu"`` test against
@@ -40,5 +41,10 @@ from .philox import (  # noqa: F401
     normals_from_words,
     noise_normals,
     add_noise,
+)
+from .rademacher import (  # noqa: F401
+    rademacher_signs,
+    hutch_norm_rademacher,
+    rademacher_variance,
 )
 from . import cost  # noqa: F401

@@ -379,3 +379,53 @@ def test_noise_stream_is_offset_consistent():
     # a different step or seed gives an independent stream
     other = oracle.noise_normals(1001, seed=3, step=10)
     assert abs(np.corrcoef(full, other)[0, 1]) < 0.15
+
+
+# ---------------------------------------------------------------------------
+# +-1 (Rademacher) projection variant
+# ---------------------------------------------------------------------------
+
+def test_rademacher_bit_layout_follows_the_philox_words():
+    # k = 32: row u of S is word u of the stream, least significant bit first
+    S = oracle.rademacher_signs(seed=5, step=3, p=8, k=32)
+    w = oracle.philox_words(5, 3, 0, 2).reshape(-1)  # 8 words
+    for u in range(8):
+        bits = [(int(w[u]) >> b) & 1 for b in range(32)]
+        assert list(S[u]) == [1.0 - 2.0 * b for b in bits]
+    # k = 16: two rows per word, the even row in the low half
+    S16 = oracle.rademacher_signs(seed=5, step=3, p=4, k=16)
+    assert list(S16[1]) == [1.0 - 2.0 * ((int(w[0]) >> (16 + b)) & 1) for b in range(16)]
+
+
+def test_rademacher_signs_are_balanced_and_plus_minus_one():
+    S = oracle.rademacher_signs(seed=11, step=0, p=1024, k=1024)
+    assert set(np.unique(S)) == {-1.0, 1.0}
+    assert abs(S.mean()) < 4.0 / np.sqrt(S.size)
+
+
+def test_rademacher_estimate_is_exact_when_o_is_diagonal():
+    # G = I_p and A with orthogonal rows make O = A A^T diagonal; then
+    # (1/k) sum_v s_v^T O s_v = trace(O) for any signs
+    rng = np.random.default_rng(3)
+    p, d, k = 12, 5, 8
+    A = np.diag(rng.uniform(0.5, 2.0, size=p)) @ np.eye(p)[:, :d]  # T = p, A A^T diagonal
+    G = np.eye(p)
+    S = oracle.rademacher_signs(seed=1, step=1, p=p, k=k)
+    got = oracle.hutch_norm_rademacher(A[None], G[None], S)[0]
+    assert abs(got - oracle.exact_norm(A[None], G[None])[0]) <= 1e-12 * got
+
+
+def test_rademacher_estimate_is_unbiased_with_its_variance_law():
+    rng = np.random.default_rng(4)
+    T, d, p, k, draws = 6, 5, 7, 4, 4000
+    A = rng.standard_normal((1, T, d))
+    G = rng.standard_normal((1, T, p))
+    exact = oracle.exact_norm(A, G)[0]
+    vals = np.array([oracle.hutch_norm_rademacher(A, G, oracle.rademacher_signs(s, 0, p, k))[0]
+                     for s in range(draws)])
+    var = oracle.rademacher_variance(A[0], G[0], k)
+    assert abs(vals.mean() - exact) < 4.0 * np.sqrt(var / draws)
+    assert abs(vals.var() / var - 1.0) < 0.15
+    # smaller than the Gaussian law 2 ||O||_F^2 / k whenever O has a diagonal
+    O = G[0].T @ A[0] @ A[0].T @ G[0]
+    assert var < 2.0 / k * np.sum(O * O)
