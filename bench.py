@@ -399,7 +399,7 @@ def run_native(args, rank, ws, local):
         "clocks": clk.summary(),
     }
     which = set() if args.rows == "none" else (
-        {"c3", "c4", "c5", "noise", "exact", "step"} if args.rows == "all"
+        {"c3", "c4", "c5", "noise", "exact", "step", "pm1"} if args.rows == "all"
         else set(args.rows.split(",")))
     if which:
         out["rows"] = measure_rows(which, device, peak, measured_tflops(), 7919 * rank)
@@ -535,6 +535,20 @@ def measure_rows(which, device, peak, tflops_peak, seed_shift):
             del A, G, P, wsbuf
         del n
 
+    if "pm1" in which:
+        wk = wl.WORKLOADS[wl.HEADLINE]
+        lay = wk.layers[0]
+        A, G, _ = inputs(wk, 0)
+        n = torch.zeros(wk.B, device=device)
+        wsbuf = rnc.workspace(rnc.DPRC_OP_HUTCH_PM1, A, wk.B, wk.T, lay.d, lay.p, wk.k)
+        t = graph_ms(lambda: rnc.dprc_norm_hutch_pm1(A, G, wk.k, 99, 1, n, ws=wsbuf), device, 20)
+        rows["pm1_q_proj"] = hbm_entry(
+            t, wk.B * wk.T * (lay.d + lay.p) * 2, peak,
+            what="dprc_norm_hutch_pm1 on the q_proj batch: +-1 projection generated in the "
+                 "kernel (no P in memory), one launch",
+            tokens_per_s=wk.B * wk.T / (t * 1e-3))
+        del A, G, n, wsbuf
+
     if "exact" in which:
         wk = wl.WORKLOADS[wl.HEADLINE]
         lay = wk.layers[0]
@@ -646,7 +660,7 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--rows", default="all",
                     help="other configurations to time after the headline: all, none, or a "
-                         "comma list of c3,c4,c5,noise,exact,step")
+                         "comma list of c3,c4,c5,noise,exact,step,pm1")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3

@@ -77,7 +77,8 @@ typedef enum {
     DPRC_OP_HUTCH = 1,
     DPRC_OP_HUTCHPP = 2,
     DPRC_OP_EXACT = 3,
-    DPRC_OP_HUTCH_LAYERS = 4
+    DPRC_OP_HUTCH_LAYERS = 4,
+    DPRC_OP_HUTCH_PM1 = 5
 } dprc_op;
 
 /* Version of this ABI (DPRC_ABI_VERSION of the built library). */
@@ -112,6 +113,25 @@ size_t dprc_workspace_bytes(dprc_op op, dprc_dtype dtype, int64_t B, int64_t T,
 dprc_status dprc_norm_hutch(const void* A, const void* G, const void* P, dprc_dtype dtype,
                             int64_t B, int64_t T, int64_t d, int64_t p, int64_t k,
                             float* n, int accumulate, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Hutchinson estimate with a +-1 projection generated from a seed (the {-1, +1}
+ * one-bit projection the notes name as the way to cut P's memory further;
+ * papernotes.org, "Experiments > Ablation".  The pages give no formula and
+ * say its privacy analysis would have to be redone):
+ *     n[i] (+)= (1/k) || A_i^T (G_i S) ||_F^2,   S [p][k] in {-1, +1}
+ *  Entry (u, v) of S is bit (e & 31) of word ((e >> 5) & 3) of block (e >> 7),
+ *  e = u k + v, of the Philox4x32-10 stream of (seed, step) (the block layout
+ *  of dprc_philox_words); bit 1 gives -1.  For bf16 with k = 16 or 32 the
+ *  signs are generated inside the kernel and never stored; other shapes write
+ *  S into the workspace first.  The 1/k scale is exact for powers of two.
+ *  Workspace: dprc_workspace_bytes(DPRC_OP_HUTCH_PM1, ...).  Other arguments
+ *  and errors as dprc_norm_hutch.
+ */
+dprc_status dprc_norm_hutch_pm1(const void* A, const void* G, uint64_t seed, uint64_t step,
+                                dprc_dtype dtype, int64_t B, int64_t T, int64_t d, int64_t p,
+                                int64_t k, float* n, int accumulate, void* ws, size_t ws_bytes,
+                                void* stream);
 
 /*
  * Layerwise sum of Hutchinson estimates over the L linear layers of a model

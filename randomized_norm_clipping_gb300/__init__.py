@@ -13,6 +13,7 @@ from .binding import (  # noqa: F401
     DPRC_OP_EXACT,
     DPRC_OP_HUTCH,
     DPRC_OP_HUTCH_LAYERS,
+    DPRC_OP_HUTCH_PM1,
     DPRC_OP_HUTCHPP,
     EXPORTED,
     DprcError,
@@ -24,6 +25,7 @@ from .binding import (  # noqa: F401
     dprc_norm_hutch,
     dprc_norm_hutch_launches,
     dprc_norm_hutch_layers,
+    dprc_norm_hutch_pm1,
     dprc_norm_hutch_noalloc,
     dprc_norm_hutchpp,
     dprc_philox_words,

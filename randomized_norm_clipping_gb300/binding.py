@@ -19,7 +19,8 @@ PKG_DIR = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG_DIR, "libdprc.so")
 
 DPRC_F32, DPRC_BF16 = 0, 1
-DPRC_OP_HUTCH, DPRC_OP_HUTCHPP, DPRC_OP_EXACT, DPRC_OP_HUTCH_LAYERS = 1, 2, 3, 4
+DPRC_OP_HUTCH, DPRC_OP_HUTCHPP, DPRC_OP_EXACT, DPRC_OP_HUTCH_LAYERS, DPRC_OP_HUTCH_PM1 = (
+    1, 2, 3, 4, 5)
 STATUS = {0: "ok", 1: "null pointer", 2: "shape", 3: "dtype", 4: "alignment",
           5: "workspace", 6: "cuda", 7: "non-finite", 8: "device", 9: "too large"}
 
@@ -48,6 +49,10 @@ _PROTOS = [
      [_c.c_void_p, _c.c_int64, _c.c_uint64, _c.c_uint64, _c.c_uint64, _c.c_void_p]),
     ("dprc_device_error", _c.c_int, [_c.c_void_p, _c.c_int]),
     ("dprc_set_phase_events", _c.c_int, [_c.c_void_p, _c.c_int]),
+    ("dprc_norm_hutch_pm1", _c.c_int,
+     [_c.c_void_p, _c.c_void_p, _c.c_uint64, _c.c_uint64, _c.c_int, _c.c_int64, _c.c_int64,
+      _c.c_int64, _c.c_int64, _c.c_int64, _c.c_void_p, _c.c_int, _c.c_void_p, _c.c_size_t,
+      _c.c_void_p]),
     ("dprc_norm_hutch_layers", _c.c_int,
      [_c.c_int64, _c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_int,
       _c.c_int64, _c.c_int64, _c.c_int64, _c.c_void_p, _c.c_int, _c.c_void_p, _c.c_size_t,
@@ -141,6 +146,22 @@ def workspace(op, like, B, T, d, p, k):
     if n == 0:
         raise DprcError("dprc_workspace_bytes", 2)
     return torch.zeros(n, dtype=torch.uint8, device=like.device)
+
+
+def dprc_norm_hutch_pm1(A, G, k, seed, step, n, accumulate=False, ws=None, stream=None):
+    """n[i] (+)= (1/k) ||A_i^T (G_i S)||_F^2 with the +-1 projection S of
+    (seed, step) (see include/dprc.h)."""
+    _need_cuda(A, G, n)
+    B, T, d = A.shape
+    p = G.shape[2]
+    if ws is None:
+        ws = workspace(DPRC_OP_HUTCH_PM1, A, B, T, d, p, k)
+    st = lib().dprc_norm_hutch_pm1(_ptr(A), _ptr(G), int(seed) & (2**64 - 1),
+                                   int(step) & (2**64 - 1), _dtype_code(A), B, T, d, p, k,
+                                   _ptr(n), int(bool(accumulate)), _ptr(ws), ws.numel(),
+                                   _stream(A, stream))
+    _check("dprc_norm_hutch_pm1", st)
+    return n
 
 
 def dprc_norm_hutch_layers(As, Gs, Ps, n, accumulate=False, ws=None, stream=None):

@@ -283,6 +283,47 @@ size_t hutchpp_ws(dprc_dtype dt, int64_t B, int64_t T, int64_t d, int64_t p, int
                                               : plan_simt(DPRC_OP_HUTCHPP, B, T, d, p, r).total;
 }
 
+
+// Sketch and projection as separate kernels (tensor cores for bf16 with
+// aligned widths and k in {16, 32, 64}, CUDA cores otherwise), with the
+// squared columns of Y weighted 1 for the first n_head and w_tail after.
+cudaError_t hutch_kernels(const void* A, const void* G, const void* P, dprc_dtype dtype, int64_t B,
+                          int64_t T, int64_t d, int64_t p, int64_t k, float* n, int accumulate,
+                          char* w, int n_head, float w_tail, cudaStream_t s) {
+  const int ik = static_cast<int>(k);
+  if (tc_path_supported(dtype, B, T, d, p, k, false)) {
+    const TcPlan t = plan_tc(DPRC_OP_HUTCH, B, T, d, p, k);
+    int* stick = reinterpret_cast<int*>(w + t.stick_off);
+    float* cnorm = reinterpret_cast<float*>(w + t.cnorm_off);
+    cudaError_t e = launch_tc_rowproj(G, B, T, p, P, false, ik, false, w + t.w_off, t.tpad,
+                                      rowproj_sched(B, T, p, ik), stick, B, s);
+    if (e != cudaSuccess) return e;
+    mark(1, s);
+    e = launch_tc_colproj(A, B, T, d, w + t.w_off, t.tpad, ik, colproj_sched(B, T, d, 2 * ik),
+                          stick, cnorm, kColprojNorm, n, accumulate, n_head, w_tail, nullptr,
+                          nullptr, t_events == nullptr, s);
+    mark(2, s);
+    return e;
+  }
+  const SimtPlan sp = plan_simt(DPRC_OP_HUTCH, B, T, d, p, k);
+  float* W = reinterpret_cast<float*>(w + sp.w_off);
+  float* Y = reinterpret_cast<float*>(w + sp.y_off);
+  cudaError_t e = launch_simt_rowproj(G, dtype, B, T, p, P, dtype, false, ik, W, s);
+  if (e != cudaSuccess) return e;
+  mark(1, s);
+  e = launch_simt_colproj(A, dtype, B, T, d, W, ik, Y, s);
+  if (e != cudaSuccess) return e;
+  e = launch_simt_norm_finish(Y, B, d, ik, n_head, w_tail, n, accumulate, s);
+  mark(2, s);
+  return e;
+}
+
+// Workspace of dprc_norm_hutch_pm1: the Hutchinson plan, then room for S.
+size_t pm1_ws(dprc_dtype dt, int64_t B, int64_t T, int64_t d, int64_t p, int64_t k) {
+  return align_up(hutch_ws(dt, B, T, d, p, k), 1024) +
+         align_up(static_cast<size_t>(p) * k * (dt == DPRC_F32 ? 4 : 2), 1024);
+}
+
 }  // namespace
 
 extern "C" {
@@ -317,6 +358,9 @@ size_t dprc_workspace_bytes(dprc_op op, dprc_dtype dtype, int64_t B, int64_t T, 
       return hutchpp_ws(dtype, B, T, d, p, k);
     case DPRC_OP_EXACT:
       return plan_exact_bytes(dtype, B, T, d, p);
+    case DPRC_OP_HUTCH_PM1:
+      if (k < 1 || k > 256) return 0;
+      return pm1_ws(dtype, B, T, d, p, k);
     case DPRC_OP_HUTCH_LAYERS:
       if (k < 1 || k > 256) return 0;
       return std::max(hutch_ws(dtype, B, T, d, p, k),
@@ -343,51 +387,58 @@ dprc_status dprc_norm_hutch(const void* A, const void* G, const void* P, dprc_dt
   if (!ws) return DPRC_ERR_WORKSPACE;
   if (!aligned16(ws)) return DPRC_ERR_ALIGN;
   if (!device_ok()) return DPRC_ERR_DEVICE;
+  if (ws_bytes < hutch_ws(dtype, B, T, d, p, k)) return DPRC_ERR_WORKSPACE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   char* w = static_cast<char*>(ws);
-  if (tc_path_supported(dtype, B, T, d, p, k, false)) {
-    const TcPlan t = plan_tc(DPRC_OP_HUTCH, B, T, d, p, k);
-    if (ws_bytes < t.total) return DPRC_ERR_WORKSPACE;
-    const int ik = static_cast<int>(k);
-    int* stick = reinterpret_cast<int*>(w + t.stick_off);
-    float* cnorm = reinterpret_cast<float*>(w + t.cnorm_off);
-    mark(0, s);
-    if (fused_hutch_supported(k)) {
-      // one launch: sketch and projection as two phases of one kernel
-      bool launched = false;
-      cudaError_t e = launch_tc_hutch_layers(1, &A, &G, &P, &d, &p, B, T, k, fused_scratch(t, w),
-                                             n, accumulate, s, &launched);
-      if (launched) {
-        mark(1, s);
-        mark(2, s);
-        return cuda_status(e);
-      }
-      if (e != cudaSuccess) (void)cudaGetLastError();  // not launched: two kernels below
-    }
-    cudaError_t e = launch_tc_rowproj(G, B, T, p, P, false, ik, false, w + t.w_off, t.tpad,
-                                      rowproj_sched(B, T, p, ik), stick, B, s);
-    if (e != cudaSuccess) return DPRC_ERR_CUDA;
-    mark(1, s);
-    e = launch_tc_colproj(A, B, T, d, w + t.w_off, t.tpad, ik, colproj_sched(B, T, d, 2 * ik),
-                          stick, cnorm, kColprojNorm, n, accumulate, ik, 1.0f, nullptr, nullptr,
-                          t_events == nullptr, s);
-    mark(2, s);
-    return cuda_status(e);
-  }
-  const SimtPlan sp = plan_simt(DPRC_OP_HUTCH, B, T, d, p, k);
-  if (ws_bytes < sp.total) return DPRC_ERR_WORKSPACE;
-  float* W = reinterpret_cast<float*>(w + sp.w_off);
-  float* Y = reinterpret_cast<float*>(w + sp.y_off);
-  const int ik = static_cast<int>(k);
   mark(0, s);
-  cudaError_t e = launch_simt_rowproj(G, dtype, B, T, p, P, dtype, false, ik, W, s);
+  if (tc_path_supported(dtype, B, T, d, p, k, false) && fused_hutch_supported(k)) {
+    // one launch: sketch and projection as two phases of one kernel
+    const TcPlan t = plan_tc(DPRC_OP_HUTCH, B, T, d, p, k);
+    bool launched = false;
+    const cudaError_t e = launch_tc_hutch_layers(1, &A, &G, &P, &d, &p, B, T, k,
+                                                 fused_scratch(t, w), n, accumulate, s, &launched);
+    if (launched) {
+      mark(1, s);
+      mark(2, s);
+      return cuda_status(e);
+    }
+    if (e != cudaSuccess) (void)cudaGetLastError();  // not launched: two kernels below
+  }
+  return cuda_status(hutch_kernels(A, G, P, dtype, B, T, d, p, k, n, accumulate, w,
+                                   static_cast<int>(k), 1.0f, s));
+}
+
+dprc_status dprc_norm_hutch_pm1(const void* A, const void* G, uint64_t seed, uint64_t step,
+                                dprc_dtype dtype, int64_t B, int64_t T, int64_t d, int64_t p,
+                                int64_t k, float* n, int accumulate, void* ws, size_t ws_bytes,
+                                void* stream) {
+  if (!A || !G || !n) return DPRC_ERR_NULL;
+  dprc_status st = check_common(dtype, B, T, d, p);
+  if (st != DPRC_OK) return st;
+  if (k < 1 || k > 256) return DPRC_ERR_SHAPE;
+  if (!aligned16(A) || !aligned16(G) || !aligned16(n)) return DPRC_ERR_ALIGN;
+  if (!ws) return DPRC_ERR_WORKSPACE;
+  if (!aligned16(ws)) return DPRC_ERR_ALIGN;
+  if (ws_bytes < pm1_ws(dtype, B, T, d, p, k)) return DPRC_ERR_WORKSPACE;
+  if (!device_ok()) return DPRC_ERR_DEVICE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char* w = static_cast<char*>(ws);
+  if (tc_path_supported(dtype, B, T, d, p, k, false) && fused_hutch_supported(k)) {
+    // the signs are generated inside the kernel: S never exists in memory
+    const TcPlan t = plan_tc(DPRC_OP_HUTCH, B, T, d, p, k);
+    bool launched = false;
+    const cudaError_t e = launch_tc_hutch_pm1(A, G, B, T, d, p, k, seed, step, fused_scratch(t, w),
+                                              n, accumulate, s, &launched);
+    if (launched) return cuda_status(e);
+    if (e != cudaSuccess) (void)cudaGetLastError();
+  }
+  // other shapes: the signs into the workspace, then the usual kernels with
+  // every column weighted 1/k
+  char* S = w + align_up(hutch_ws(dtype, B, T, d, p, k), 1024);
+  cudaError_t e = launch_pm1_signs(S, dtype, p * k, seed, step, s);
   if (e != cudaSuccess) return DPRC_ERR_CUDA;
-  mark(1, s);
-  e = launch_simt_colproj(A, dtype, B, T, d, W, ik, Y, s);
-  if (e != cudaSuccess) return DPRC_ERR_CUDA;
-  e = launch_simt_norm_finish(Y, B, d, ik, ik, 1.0f, n, accumulate, s);
-  mark(2, s);
-  return cuda_status(e);
+  return cuda_status(hutch_kernels(A, G, S, dtype, B, T, d, p, k, n, accumulate, w, 0,
+                                   1.0f / static_cast<float>(k), s));
 }
 
 dprc_status dprc_norm_hutch_layers(int64_t L, const void* const* A, const void* const* G,

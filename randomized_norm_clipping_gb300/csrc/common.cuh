@@ -337,6 +337,56 @@ __device__ __forceinline__ void split_hilo(float x, __nv_bfloat16& hi, __nv_bflo
   lo = __float2bfloat16_rn(x - __bfloat162float(hi));
 }
 
+// ---------------------------------------------------------------------------
+// Philox4x32-10 (Salmon, Moraes, Dror and Shaw, "Parallel Random Numbers: As
+// Easy as 1, 2, 3", SC'11), written from that paper's definition.  Block j of
+// the stream of (seed, step) is Philox applied to the counter
+// (j_lo, j_hi, step_lo, step_hi) under the key (seed_lo, seed_hi).
+// ---------------------------------------------------------------------------
+constexpr uint32_t kPhiloxM0 = 0xD2511F53u;
+constexpr uint32_t kPhiloxM1 = 0xCD9E8D57u;
+constexpr uint32_t kPhiloxW0 = 0x9E3779B9u;
+constexpr uint32_t kPhiloxW1 = 0xBB67AE85u;
+
+// Round keys of Philox4x32-10: the key bumped by (W0, W1) before each round.
+// They depend only on the seed, so a thread computes them once.
+struct RoundKeys {
+  uint32_t k0[10], k1[10];
+};
+
+__device__ __forceinline__ RoundKeys round_keys(uint64_t seed) {
+  RoundKeys rk;
+  uint32_t a = static_cast<uint32_t>(seed), b = static_cast<uint32_t>(seed >> 32);
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    rk.k0[r] = a;
+    rk.k1[r] = b;
+    a += kPhiloxW0;
+    b += kPhiloxW1;
+  }
+  return rk;
+}
+
+// Ten rounds on the counter x; each round's two 32x32 products are one wide
+// multiply each (high and low words).
+__device__ __forceinline__ uint4 philox4x32_10(uint4 x, const RoundKeys& rk) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    const unsigned long long p0 = static_cast<unsigned long long>(kPhiloxM0) * x.x;
+    const unsigned long long p1 = static_cast<unsigned long long>(kPhiloxM1) * x.z;
+    x = make_uint4(static_cast<uint32_t>(p1 >> 32) ^ x.y ^ rk.k0[r], static_cast<uint32_t>(p1),
+                   static_cast<uint32_t>(p0 >> 32) ^ x.w ^ rk.k1[r], static_cast<uint32_t>(p0));
+  }
+  return x;
+}
+
+__device__ __forceinline__ uint4 philox_block(uint64_t j, uint64_t step, const RoundKeys& rk) {
+  return philox4x32_10(make_uint4(static_cast<uint32_t>(j), static_cast<uint32_t>(j >> 32),
+                                  static_cast<uint32_t>(step), static_cast<uint32_t>(step >> 32)),
+                       rk);
+}
+
+
 // Round a shared-memory pointer up to the 1024-byte alignment that 128-byte
 // swizzled tiles need.
 __device__ __forceinline__ uint8_t* align_1024(uint8_t* p) {

@@ -171,6 +171,16 @@ cudaError_t launch_tc_hutch_layers(int L, const void* const* A, const void* cons
                                    const void* const* P, const int64_t* d, const int64_t* p,
                                    int64_t B, int64_t T, int64_t k, const FusedScratch& ws,
                                    float* n_out, int accumulate, cudaStream_t s, bool* launched);
+// The +-1 projection variant on the fused kernel (bf16, k = 16 or 32, one
+// layer): the signs are generated in the kernel from (seed, step); the norm is
+// scaled by 1/k.  *launched false: not possible here (use the signs below).
+cudaError_t launch_tc_hutch_pm1(const void* A, const void* G, int64_t B, int64_t T, int64_t d,
+                                int64_t p, int64_t k, uint64_t seed, uint64_t step,
+                                const FusedScratch& ws, float* n_out, int accumulate,
+                                cudaStream_t s, bool* launched);
+// S [p][k] in {-1, +1} (n = p k entries) written as dt, from the same stream.
+cudaError_t launch_pm1_signs(void* out, dprc_dtype dt, int64_t n, uint64_t seed, uint64_t step,
+                             cudaStream_t s);
 cudaError_t launch_tc_exact_direct(const void* A, const void* G, int64_t B, int64_t T, int64_t d,
                                    int64_t p, float* partials, float* n_out, int accumulate,
                                    cudaStream_t s);

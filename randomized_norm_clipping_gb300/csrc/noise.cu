@@ -13,53 +13,11 @@
 // (seed_lo, seed_hi)).  The kernel is HBM-bound: 8 bytes of traffic per
 // element (read + write of the fp32 gradient), read with 128-bit loads.
 
+#include "common.cuh"
 #include "internal.h"
 
 namespace dprc {
 namespace {
-
-constexpr uint32_t kPhiloxM0 = 0xD2511F53u;
-constexpr uint32_t kPhiloxM1 = 0xCD9E8D57u;
-constexpr uint32_t kPhiloxW0 = 0x9E3779B9u;
-constexpr uint32_t kPhiloxW1 = 0xBB67AE85u;
-
-// Round keys of Philox4x32-10: the key bumped by (W0, W1) before each round.
-// They depend only on the seed, so a thread computes them once.
-struct RoundKeys {
-  uint32_t k0[10], k1[10];
-};
-
-__device__ __forceinline__ RoundKeys round_keys(uint64_t seed) {
-  RoundKeys rk;
-  uint32_t a = static_cast<uint32_t>(seed), b = static_cast<uint32_t>(seed >> 32);
-#pragma unroll
-  for (int r = 0; r < 10; ++r) {
-    rk.k0[r] = a;
-    rk.k1[r] = b;
-    a += kPhiloxW0;
-    b += kPhiloxW1;
-  }
-  return rk;
-}
-
-// Ten rounds on the counter x; each round's two 32x32 products are one wide
-// multiply each (high and low words).
-__device__ __forceinline__ uint4 philox4x32_10(uint4 x, const RoundKeys& rk) {
-#pragma unroll
-  for (int r = 0; r < 10; ++r) {
-    const unsigned long long p0 = static_cast<unsigned long long>(kPhiloxM0) * x.x;
-    const unsigned long long p1 = static_cast<unsigned long long>(kPhiloxM1) * x.z;
-    x = make_uint4(static_cast<uint32_t>(p1 >> 32) ^ x.y ^ rk.k0[r], static_cast<uint32_t>(p1),
-                   static_cast<uint32_t>(p0 >> 32) ^ x.w ^ rk.k1[r], static_cast<uint32_t>(p0));
-  }
-  return x;
-}
-
-__device__ __forceinline__ uint4 philox_block(uint64_t j, uint64_t step, const RoundKeys& rk) {
-  return philox4x32_10(make_uint4(static_cast<uint32_t>(j), static_cast<uint32_t>(j >> 32),
-                                  static_cast<uint32_t>(step), static_cast<uint32_t>(step >> 32)),
-                       rk);
-}
 
 // -2 ln(u1) for u1 = m 2^-24, m = (a >> 8) + 1 in [1, 2^24].  The hardware
 // logarithm (__logf, absolute error <= 2^-21.41 on [0.5, 2]) loses relative
@@ -161,6 +119,27 @@ __global__ void __launch_bounds__(256) philox_words_kernel(uint4* __restrict__ o
 // Launched as a programmatic dependent of the norm kernel before it: the
 // launch overlaps that kernel, and griddepcontrol.wait holds the reads of n
 // until it has completed and its writes are visible.
+// S [n] in {-1, +1} (n = p k, row-major [p][k]) as TO: entry e is bit (e & 31)
+// of word (e >> 5) & 3 of Philox block e >> 7 of the stream of (seed, step);
+// bit 1 gives -1.  One thread per block of 128 entries.
+template <typename TO>
+__global__ void __launch_bounds__(256) pm1_signs_kernel(TO* __restrict__ out, long long n,
+                                                        uint64_t seed, uint64_t step) {
+  const RoundKeys rk = round_keys(seed);
+  const long long nblk = (n + 127) / 128;
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long j = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; j < nblk;
+       j += stride) {
+    const uint4 w = philox_block(static_cast<uint64_t>(j), step, rk);
+    const uint32_t words[4] = {w.x, w.y, w.z, w.w};
+    for (int q = 0; q < 4; ++q)
+      for (int b = 0; b < 32; ++b) {
+        const long long e = j * 128 + q * 32 + b;
+        if (e < n) out[e] = static_cast<TO>(((words[q] >> b) & 1u) ? -1.0f : 1.0f);
+      }
+  }
+}
+
 __global__ void clip_kernel(const float* __restrict__ n, long long B, float C,
                             float* __restrict__ c, int32_t* __restrict__ nonfinite) {
   asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -203,6 +182,17 @@ cudaError_t launch_philox_words(uint32_t* out, int64_t n_blocks, uint64_t first_
   if (n_blocks == 0) return cudaSuccess;
   philox_words_kernel<<<grid_for(n_blocks, 256), 256, 0, s>>>(reinterpret_cast<uint4*>(out),
                                                               n_blocks, first_block, seed, step);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pm1_signs(void* out, dprc_dtype dt, int64_t n, uint64_t seed, uint64_t step,
+                             cudaStream_t s) {
+  const int grid = grid_for((n + 127) / 128, 256);
+  if (dt == DPRC_F32)
+    pm1_signs_kernel<float><<<grid, 256, 0, s>>>(static_cast<float*>(out), n, seed, step);
+  else
+    pm1_signs_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(static_cast<__nv_bfloat16*>(out), n,
+                                                         seed, step);
   return cudaGetLastError();
 }
 

@@ -241,11 +241,75 @@ struct HParams {
   float* nl;               // [L][B]
   float* n_out;
   int accumulate;
+  float norm_scale;                // 1, or 1/k for the +-1 projection
+  unsigned long long seed, step;   // +-1 projection: its Philox stream
   LayerDesc layer[CAP];     // CAP = 1 for single-layer calls: a small parameter block
 };
 
-template <int K, int CAP>
-__global__ void __launch_bounds__(192, 1) tc_hutch_kernel(const __grid_constant__ HParams<CAP> a) {
+// The +-1 projection (reading of papernotes.org, "Experiments > Ablation": a
+// {-1, +1} one-bit P instead of a Gaussian one): rows [128 u, 128 u + 128) of
+// S [p][K] written by one warp as bf16 +-1 into the P tile of a sketch stage,
+// in the layout the TMA gives that tile: MN-major, 2K-byte rows, 64-byte
+// swizzle for K = 32 (16-byte chunk c of row r lands at chunk c ^ ((r>>1)&3)),
+// 32-byte for K = 16 (chunk c ^ ((r>>2)&1)).  Entry (R, v) is bit (e & 31) of
+// word (e >> 5) & 3 of Philox block e >> 7, e = R K + v; bit 1 gives -1.
+// part: which of the two writer warps calls (each writes half of every row's
+// 16-byte chunks; both compute the same Philox blocks).
+template <int K>
+__device__ __forceinline__ void gen_sign_tile(uint8_t* tile, int u, int lane, int part,
+                                              const RoundKeys& rk, uint64_t step) {
+  auto pack = [](uint32_t bits8, int m) {  // two bf16 signs from bits 2m, 2m+1
+    const uint32_t b0 = (bits8 >> (2 * m)) & 1u, b1 = (bits8 >> (2 * m + 1)) & 1u;
+    return (0x3F80u | (b0 << 15)) | ((0x3F80u | (b1 << 15)) << 16);
+  };
+  if constexpr (K == 32) {
+    // lane l: block 32 u + l = rows 4 l .. 4 l + 3, one word per row
+    const uint4 w = philox_block(static_cast<uint64_t>(u) * 32 + lane, step, rk);
+    const uint32_t words[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int r = 4 * lane + q;
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        const int c = 2 * part + cc;
+        const uint32_t b8 = (words[q] >> (8 * c)) & 0xFFu;
+        const int pc = c ^ ((r >> 1) & 3);
+        *reinterpret_cast<uint4*>(tile + r * 64 + pc * 16) =
+            make_uint4(pack(b8, 0), pack(b8, 1), pack(b8, 2), pack(b8, 3));
+      }
+    }
+  } else {
+    // lanes 0..15: block 16 u + l = rows 8 l .. 8 l + 7, two rows per word
+    if (lane < 16) {
+      const uint4 w = philox_block(static_cast<uint64_t>(u) * 16 + lane, step, rk);
+      const uint32_t words[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int r = 8 * lane + 2 * q + h;
+          {
+            const int c = part;
+            const uint32_t b8 = (words[q] >> (16 * h + 8 * c)) & 0xFFu;
+            const int pc = c ^ ((r >> 2) & 1);
+            *reinterpret_cast<uint4*>(tile + r * 32 + pc * 16) =
+                make_uint4(pack(b8, 0), pack(b8, 1), pack(b8, 2), pack(b8, 3));
+          }
+        }
+      }
+    }
+  }
+}
+
+// Threads per CTA: TMA producer, MMA issuer, four epilogue warps, and with the
+// +-1 projection two more warps that write the sign tiles.
+template <bool PM1>
+constexpr int hutch_threads() { return PM1 ? 256 : 192; }
+
+template <int K, int CAP, bool PM1>
+__global__ void __launch_bounds__(hutch_threads<PM1>(), 1)
+    tc_hutch_kernel(const __grid_constant__ HParams<CAP> a) {
+  static_assert(!PM1 || CAP == 1, "the +-1 projection runs one layer per launch");
   using Cfg = HCfg<K>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ float s_red[4];
@@ -277,7 +341,8 @@ __global__ void __launch_bounds__(192, 1) tc_hutch_kernel(const __grid_constant_
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], 1);
+      // with the +-1 projection a stage also waits for the two sign-tile halves
+      mbar_init(&full[s], PM1 ? 3 : 1);
       mbar_init(&empty[s], 1);
     }
     for (int s = 0; s < 2; ++s) {
@@ -300,7 +365,7 @@ __global__ void __launch_bounds__(192, 1) tc_hutch_kernel(const __grid_constant_
     for (int l = 0; l < nlayers && l < 4; ++l) {
       const LayerDesc& Ld = a.layer[CAP == 1 ? 0 : l];
       tma_prefetch_desc(&Ld.mg);
-      tma_prefetch_desc(&Ld.mp);
+      if (!PM1) tma_prefetch_desc(&Ld.mp);
       tma_prefetch_desc(&Ld.ma);
     }
   }
@@ -345,11 +410,12 @@ __global__ void __launch_bounds__(192, 1) tc_hutch_kernel(const __grid_constant_
             const int s = take_slot(it);
             if (!ok) break;
             uint8_t* slot = ring + s * Cfg::kSlot;
-            mbar_arrive_expect_tx(&full[s], Cfg::kRowStage);
+            // (+-1 projection: the sign tile comes from the generator warp)
+            mbar_arrive_expect_tx(&full[s], PM1 ? Cfg::kRowG : Cfg::kRowStage);
 #pragma unroll
             for (int h = 0; h < 2; ++h)
               tma_load_3d(slot + h * Cfg::kRowGBox, &Ld.mg, &full[s], u * kCol + h * 64, t0, i);
-            tma_load_3d(slot + Cfg::kRowG, &Ld.mp, &full[s], 0, u * kCol, 0);
+            if (!PM1) tma_load_3d(slot + Cfg::kRowG, &Ld.mp, &full[s], 0, u * kCol, 0);
             ++it;
           }
         }
@@ -396,6 +462,10 @@ __global__ void __launch_bounds__(192, 1) tc_hutch_kernel(const __grid_constant_
             if (!ok) break;
             uint8_t* slot = ring + s * Cfg::kSlot;
             mbar_arrive_expect_tx(&full[s], Cfg::kColStage);
+            if (PM1) {  // no sign tile in a projection stage
+              mbar_arrive(&full[s]);
+              mbar_arrive(&full[s]);
+            }
 #pragma unroll
             for (int h = 0; h < 2; ++h)
               tma_load_3d(slot + h * Cfg::kColABox, &Ld.ma, &full[s], ca.ch * kRows + h * 64,
@@ -508,7 +578,33 @@ __global__ void __launch_bounds__(192, 1) tc_hutch_kernel(const __grid_constant_
       }
       if (!ok) *abort_flag = 1;
     }
-  } else {
+  } else if (PM1 && warp >= 6) {
+    // ---------------- sign-tile writers (+-1 projection, one layer) ----------------
+    // Walks the sketch stages in the producer's order; once a slot is free it
+    // writes that stage's signs, makes them visible to the tensor cores (async
+    // proxy) and gives the stage's second arrival.
+    const RoundKeys rk = round_keys(a.seed);
+    const LayerDesc& Ld = a.layer[0];
+    const Mine m1 = mine(Ld.ph1, cl, rank);
+    const long long nb1 = count_blocks(Ld.ph1, m1);
+    long long it = 0;
+    bool ok = true;
+    for (long long j = 0; j < nb1 && ok; ++j) {
+      for (int u = m1.ulo; u < m1.uhi; ++u, ++it) {
+        const int s = static_cast<int>(it % kStages);
+        bool free_ok = true;
+        if (lane == 0)
+          free_ok = mbar_wait(&empty[s], (static_cast<uint32_t>(it / kStages) & 1) ^ 1,
+                              DPRC_DEVERR_PIPE_EMPTY);
+        ok = __shfl_sync(0xffffffffu, free_ok ? 1 : 0, 0) != 0 && *abort_flag == 0;
+        if (!ok) break;
+        gen_sign_tile<K>(ring + s * Cfg::kSlot + Cfg::kRowG, u, lane, warp - 6, rk, a.step);
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&full[s]);
+      }
+    }
+  } else if (warp < 6) {
     // ---------------- epilogue warps 2..5 ----------------
     const int ew = warp - 2;
     const int q = warp & 3;         // TMEM lane quadrant of this warp
@@ -618,6 +714,7 @@ __global__ void __launch_bounds__(192, 1) tc_hutch_kernel(const __grid_constant_
         if (mine_row && ok && ch * kRows + row < Ld.d) {
 #pragma unroll
           for (int t = 0; t < K; ++t) sq = fmaf(y[t], y[t], sq);
+          sq *= a.norm_scale;  // 1, or 1/k (a power of two: exact)
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, off);
@@ -717,7 +814,7 @@ __global__ void __launch_bounds__(192, 1) tc_hutch_kernel(const __grid_constant_
   }
 }
 
-template <int K, int CAP>
+template <int K, int CAP, bool PM1>
 cudaError_t set_smem_once() {
   constexpr int kMaxDev = 64;
   static std::atomic<int> done[kMaxDev];
@@ -725,7 +822,7 @@ cudaError_t set_smem_once() {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev >= 0 && dev < kMaxDev && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
-  e = cudaFuncSetAttribute(tc_hutch_kernel<K, CAP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  e = cudaFuncSetAttribute(tc_hutch_kernel<K, CAP, PM1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            HCfg<K>::smem(8));
   if (e == cudaSuccess && dev >= 0 && dev < kMaxDev) done[dev].store(1, std::memory_order_release);
   return e;
@@ -734,7 +831,7 @@ cudaError_t set_smem_once() {
 // CTAs of this kernel that may run at once in one cooperative launch with
 // clusters of cl: the driver's occupancy figures (one CTA per SM: the
 // tensor-memory kernels are counted as such), cached per device and cl.
-template <int K, int CAP>
+template <int K, int CAP, bool PM1>
 int resident_ctas(int cl) {
   constexpr int kMaxDev = 64;
   static std::atomic<int> cache[kMaxDev][4];
@@ -746,14 +843,15 @@ int resident_ctas(int cl) {
   const int smem = HCfg<K>::smem(cl);
   if (cl == 1) {
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, tc_hutch_kernel<K, CAP>, 192,
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, tc_hutch_kernel<K, CAP, PM1>,
+                                                      hutch_threads<PM1>(),
                                                       smem) != cudaSuccess)
       return 0;
     v = per_sm * device_sm_count();
   } else {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(cl * device_sm_count());
-    cfg.blockDim = dim3(192);
+    cfg.blockDim = dim3(hutch_threads<PM1>());
     cfg.dynamicSmemBytes = smem;
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeClusterDimension;
@@ -763,7 +861,7 @@ int resident_ctas(int cl) {
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
     int ncl = 0;
-    if (cudaOccupancyMaxActiveClusters(&ncl, tc_hutch_kernel<K, CAP>, &cfg) != cudaSuccess)
+    if (cudaOccupancyMaxActiveClusters(&ncl, tc_hutch_kernel<K, CAP, PM1>, &cfg) != cudaSuccess)
       return 0;
     v = ncl * cl;
   }
@@ -771,11 +869,11 @@ int resident_ctas(int cl) {
   return v;
 }
 
-template <int K, int CAP>
+template <int K, int CAP, bool PM1>
 cudaError_t launch_k(const HParams<CAP>& a, int grid, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(192);
+  cfg.blockDim = dim3(hutch_threads<PM1>());
   cfg.dynamicSmemBytes = HCfg<K>::smem(a.cl);
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
@@ -792,7 +890,7 @@ cudaError_t launch_k(const HParams<CAP>& a, int grid, cudaStream_t s) {
   }
   cfg.attrs = attr;
   cfg.numAttrs = na;
-  return cudaLaunchKernelEx(&cfg, tc_hutch_kernel<K, CAP>, a);
+  return cudaLaunchKernelEx(&cfg, tc_hutch_kernel<K, CAP, PM1>, a);
 }
 
 // Cluster size a phase of `nblocks` blocks of `upb` units wants on `slots`
@@ -812,7 +910,7 @@ std::atomic<int> g_refused[kMaxDevices];
 
 // Schedule of one launch over layers [0, L): the phases of every layer, the
 // cluster size and the grid.  False when the kernel cannot run here.
-template <int CAP>
+template <int CAP, bool PM1>
 bool plan_fused(int L, const int64_t* d, const int64_t* p, int64_t B, int64_t T, int64_t k,
                 HParams<CAP>& a, int& grid_out) {
   if (!fused_hutch_supported(k) || L < 1 || L > CAP) return false;
@@ -843,8 +941,10 @@ bool plan_fused(int L, const int64_t* d, const int64_t* p, int64_t B, int64_t T,
     cl = c2 > cl ? c2 : cl;
     maxch = Ld.nchunks > maxch ? Ld.nchunks : maxch;
   }
-  if ((ik == 16 ? set_smem_once<16, CAP>() : set_smem_once<32, CAP>()) != cudaSuccess) return false;
-  const int resident = ik == 16 ? resident_ctas<16, CAP>(cl) : resident_ctas<32, CAP>(cl);
+  if ((ik == 16 ? set_smem_once<16, CAP, PM1>() : set_smem_once<32, CAP, PM1>()) != cudaSuccess)
+    return false;
+  const int resident =
+      ik == 16 ? resident_ctas<16, CAP, PM1>(cl) : resident_ctas<32, CAP, PM1>(cl);
   if (resident < cl) return false;
   for (int l = 0; l < L; ++l) {
     LayerDesc& Ld = a.layer[l];
@@ -888,19 +988,19 @@ bool fused_hutch_supported(int64_t k) { return k == 16 || k == 32; }
 bool fused_hutch_planned(int64_t B, int64_t T, int64_t d, int64_t p, int64_t k) {
   HParams<1> a;
   int grid = 0;
-  return plan_fused(1, &d, &p, B, T, k, a, grid);
+  return plan_fused<1, false>(1, &d, &p, B, T, k, a, grid);
 }
 
 namespace {
 
-template <int CAP>
+template <int CAP, bool PM1>
 cudaError_t launch_cap(int L, const void* const* A, const void* const* G, const void* const* P,
                        const int64_t* d, const int64_t* p, int64_t B, int64_t T, int64_t k,
-                       const FusedScratch& ws, float* n_out, int accumulate, cudaStream_t s,
-                       bool* launched) {
+                       const FusedScratch& ws, float* n_out, int accumulate, uint64_t seed,
+                       uint64_t step, cudaStream_t s, bool* launched) {
   static thread_local HParams<CAP> a;  // up to ~26 KB: kept off the stack
   int grid = 0;
-  if (!plan_fused(L, d, p, B, T, k, a, grid)) return cudaSuccess;
+  if (!plan_fused<CAP, PM1>(L, d, p, B, T, k, a, grid)) return cudaSuccess;
   const int ik = static_cast<int>(k);
   a.tpad = ws.tpad;
   a.W[0] = static_cast<__nv_bfloat16*>(ws.W[0]);
@@ -914,6 +1014,9 @@ cudaError_t launch_cap(int L, const void* const* A, const void* const* G, const 
   a.nl = ws.nl;
   a.n_out = n_out;
   a.accumulate = accumulate;
+  a.norm_scale = PM1 ? 1.0f / static_cast<float>(k) : 1.0f;
+  a.seed = seed;
+  a.step = step;
   for (int b = 0; b < 2; ++b)
     if (!make_tmap_3d_bf16(&a.mw[b], ws.W[b], T, 2 * ik, B, ws.tpad, 2 * ik * ws.tpad, 64,
                            2 * ik, 128))
@@ -921,11 +1024,12 @@ cudaError_t launch_cap(int L, const void* const* A, const void* const* G, const 
   for (int l = 0; l < L; ++l) {
     LayerDesc& Ld = a.layer[l];
     if (!make_tmap_3d_bf16(&Ld.mg, G[l], p[l], T, B, p[l], T * p[l], 64, kTok, 128) ||
-        !make_tmap_3d_bf16(&Ld.mp, P[l], ik, p[l], 1, ik, p[l] * ik, ik, kCol, 2 * ik) ||
+        (!PM1 && !make_tmap_3d_bf16(&Ld.mp, P[l], ik, p[l], 1, ik, p[l] * ik, ik, kCol, 2 * ik)) ||
         !make_tmap_3d_bf16(&Ld.ma, A[l], d[l], T, B, d[l], T * d[l], 64, kTok, 128))
       return cudaErrorInvalidValue;
   }
-  const cudaError_t e = ik == 16 ? launch_k<16, CAP>(a, grid, s) : launch_k<32, CAP>(a, grid, s);
+  const cudaError_t e =
+      ik == 16 ? launch_k<16, CAP, PM1>(a, grid, s) : launch_k<32, CAP, PM1>(a, grid, s);
   if (e == cudaSuccess) {
     *launched = true;
   } else if (e == cudaErrorCooperativeLaunchTooLarge || e == cudaErrorNotSupported ||
@@ -946,9 +1050,20 @@ cudaError_t launch_tc_hutch_layers(int L, const void* const* A, const void* cons
                                    bool* launched) {
   *launched = false;
   if (L == 1)
-    return launch_cap<1>(L, A, G, P, d, p, B, T, k, ws, n_out, accumulate, s, launched);
-  return launch_cap<kMaxFusedLayers>(L, A, G, P, d, p, B, T, k, ws, n_out, accumulate, s,
-                                     launched);
+    return launch_cap<1, false>(L, A, G, P, d, p, B, T, k, ws, n_out, accumulate, 0, 0, s,
+                                launched);
+  return launch_cap<kMaxFusedLayers, false>(L, A, G, P, d, p, B, T, k, ws, n_out, accumulate, 0,
+                                            0, s, launched);
+}
+
+cudaError_t launch_tc_hutch_pm1(const void* A, const void* G, int64_t B, int64_t T, int64_t d,
+                                int64_t p, int64_t k, uint64_t seed, uint64_t step,
+                                const FusedScratch& ws, float* n_out, int accumulate,
+                                cudaStream_t s, bool* launched) {
+  *launched = false;
+  const void* P = nullptr;
+  return launch_cap<1, true>(1, &A, &G, &P, &d, &p, B, T, k, ws, n_out, accumulate, seed, step, s,
+                             launched);
 }
 
 }  // namespace dprc

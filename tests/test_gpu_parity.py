@@ -369,3 +369,37 @@ def test_hutch_layers_repeats_bitwise_and_reuses_its_workspace():
     rnc.dprc_norm_hutch(As[0], Gs[0], Ps[0], torch.zeros(4, device=DEV), ws=ws)  # same workspace
     rnc.dprc_norm_hutch_layers(As, Gs, Ps, n2, ws=ws)
     assert torch.equal(n1, n2)
+
+
+# ------------------------------------------------------------------ +-1 projection
+
+@pytest.mark.parametrize("B,T,d,p,k,dtype", [
+    (3, 300, 256, 512, 32, torch.bfloat16),   # signs generated in the kernel (k = 32)
+    (2, 1000, 520, 264, 16, torch.bfloat16),  # in the kernel, k = 16, ragged widths
+    (8, 4096, 2048, 2048, 32, torch.bfloat16),  # the q_proj launch shape
+    (2, 200, 256, 256, 64, torch.bfloat16),   # k = 64: signs in the workspace, two kernels
+    (3, 77, 30, 17, 8, torch.float32),        # fp32: CUDA cores
+    (2, 90, 37, 45, 24, torch.bfloat16),      # odd widths: CUDA cores
+])
+def test_pm1_projection_matches_oracle(B, T, d, p, k, dtype):
+    A = _rand((B, T, d), 500 + T, dtype)
+    G = _rand((B, T, p), 501 + T, dtype, 0.1)
+    seed, step = 0x1234_5678_9ABC, 17 + k
+    n = torch.full((B,), 1.5, device=DEV)
+    rnc.dprc_norm_hutch_pm1(A.to(DEV), G.to(DEV), k, seed, step, n, accumulate=True)
+    S = oracle.rademacher_signs(seed, step, p, k)
+    ref = oracle.hutch_norm_rademacher(to_f64(A), to_f64(G), S)
+    tol = 1e-5 if dtype == torch.float32 else RTOL
+    assert _relerr(n.cpu() - 1.5, ref) < tol
+    assert rnc.dprc_device_error() == 0
+
+
+def test_pm1_projection_is_deterministic_and_seeded():
+    A = _rand((4, 700, 512), 5, torch.bfloat16).to(DEV)
+    G = _rand((4, 700, 512), 6, torch.bfloat16, 0.1).to(DEV)
+    n1, n2, n3 = (torch.zeros(4, device=DEV) for _ in range(3))
+    rnc.dprc_norm_hutch_pm1(A, G, 32, 9, 1, n1)
+    rnc.dprc_norm_hutch_pm1(A, G, 32, 9, 1, n2)
+    rnc.dprc_norm_hutch_pm1(A, G, 32, 9, 2, n3)  # another step: other signs
+    assert torch.equal(n1, n2)
+    assert not torch.equal(n1, n3)
