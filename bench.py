@@ -399,7 +399,7 @@ def run_native(args, rank, ws, local):
         "clocks": clk.summary(),
     }
     which = set() if args.rows == "none" else (
-        {"c3", "c4", "c5", "noise", "exact", "step", "pm1"} if args.rows == "all"
+        {"c3", "c4", "c5", "noise", "exact", "step", "pm1", "lora"} if args.rows == "all"
         else set(args.rows.split(",")))
     if which:
         out["rows"] = measure_rows(which, device, peak, measured_tflops(), 7919 * rank)
@@ -549,6 +549,30 @@ def measure_rows(which, device, peak, tflops_peak, seed_shift):
             tokens_per_s=wk.B * wk.T / (t * 1e-3))
         del A, G, n, wsbuf
 
+    if "lora" in which:
+        # LoRA adapters of the q_proj batch (B8 T4096, rank 16): the down map
+        # 2048 -> 16 and the up map 16 -> 2048, by the estimate and the exact norm
+        wk = wl.WORKLOADS[wl.HEADLINE]
+        g = torch.Generator(device=device)
+        g.manual_seed(4242 + seed_shift)
+        r = 16
+        for name, (d, p) in (("down", (2048, r)), ("up", (r, 2048))):
+            A = torch.randn(wk.B, wk.T, d, generator=g, device=device).to(torch.bfloat16)
+            G = (torch.randn(wk.B, wk.T, p, generator=g, device=device) * 0.02).to(torch.bfloat16)
+            P = (torch.randn(p, wk.k, generator=g, device=device) / wk.k ** 0.5).to(torch.bfloat16)
+            n = torch.zeros(wk.B, device=device)
+            wsh = rnc.workspace(rnc.DPRC_OP_HUTCH, A, wk.B, wk.T, d, p, wk.k)
+            wse = rnc.workspace(rnc.DPRC_OP_EXACT, A, wk.B, wk.T, d, p, wk.k)
+            nbytes = wk.B * wk.T * (d + p) * 2
+            th = graph_ms(lambda: rnc.dprc_norm_hutch(A, G, P, n, ws=wsh), device, 20)
+            te = graph_ms(lambda: rnc.dprc_exact_norm(A, G, n, ws=wse), device, 20)
+            rows[f"lora_{name}_r16"] = hbm_entry(
+                th, nbytes, peak, exact_ms=te,
+                exact_frac=nbytes / (te * 1e-3) / 1e9 / peak,
+                what=f"LoRA {name} map {d} -> {p} on B8 T4096: dprc_norm_hutch (k=32) and "
+                     "dprc_exact_norm; at rank <= k the exact norm moves the same bytes")
+            del A, G, P, n, wsh, wse
+
     if "exact" in which:
         wk = wl.WORKLOADS[wl.HEADLINE]
         lay = wk.layers[0]
@@ -660,7 +684,7 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--rows", default="all",
                     help="other configurations to time after the headline: all, none, or a "
-                         "comma list of c3,c4,c5,noise,exact,step,pm1")
+                         "comma list of c3,c4,c5,noise,exact,step,pm1,lora")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3

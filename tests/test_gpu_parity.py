@@ -70,6 +70,11 @@ HUTCH_SHAPES = [
     (1, 2048, 1024, 1024, 32),     # few blocks: both kernels split blocks over 8-CTA clusters
     (3, 4096, 1024, 512, 16),      # two-CTA clusters for the sketch, four for the projection
     (40, 256, 256, 128, 32),       # many blocks: whole blocks per CTA, several per CTA
+    # LoRA adapters (rank r = 8 .. 64): d_in -> r and r -> d_out
+    (4, 1000, 2048, 16, 32),
+    (4, 1000, 16, 2048, 32),
+    (2, 300, 8, 512, 16),
+    (2, 300, 512, 64, 32),
     # float32 / CUDA-core path through the same entry point
     (4, 128, 64, 64, 8),
 ]
@@ -200,7 +205,9 @@ def test_hutchpp_exact_on_low_rank_gradients():
                                            (2, 1024, 512, 256, torch.bfloat16),
                                            (3, 1000, 392, 600, torch.bfloat16),
                                            (1, 4097, 128, 256, torch.bfloat16),
-                                           (5, 64, 1024, 1536, torch.bfloat16)])
+                                           (5, 64, 1024, 1536, torch.bfloat16),
+                                           (4, 1000, 2048, 16, torch.bfloat16),   # LoRA down
+                                           (4, 1000, 16, 2048, torch.bfloat16)])  # LoRA up
 def test_exact_norm_matches_oracle(B, T, d, p, dtype):
     A = _rand((B, T, d), 60 + T, dtype)
     G = _rand((B, T, p), 61 + T, dtype, 0.05)
@@ -380,6 +387,7 @@ def test_hutch_layers_repeats_bitwise_and_reuses_its_workspace():
     (2, 200, 256, 256, 64, torch.bfloat16),   # k = 64: signs in the workspace, two kernels
     (3, 77, 30, 17, 8, torch.float32),        # fp32: CUDA cores
     (2, 90, 37, 45, 24, torch.bfloat16),      # odd widths: CUDA cores
+    (4, 1000, 2048, 16, 32, torch.bfloat16),  # LoRA down, in the kernel
 ])
 def test_pm1_projection_matches_oracle(B, T, d, p, k, dtype):
     A = _rand((B, T, d), 500 + T, dtype)
