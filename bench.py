@@ -546,7 +546,8 @@ def measure_rows(which, device, peak, tflops_peak, seed_shift):
             t, wk.B * wk.T * (lay.d + lay.p) * 2, peak,
             what="dprc_norm_hutch_pm1 on the q_proj batch: +-1 projection generated in the "
                  "kernel (no P in memory), one launch",
-            tokens_per_s=wk.B * wk.T / (t * 1e-3))
+            tokens_per_s=wk.B * wk.T / (t * 1e-3),
+            ncu_traffic_bytes=ncu_traffic("pm1"))
         del A, G, n, wsbuf
 
     if "lora" in which:

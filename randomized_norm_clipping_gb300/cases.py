@@ -44,6 +44,15 @@ def _hutch_layers(B, T):
     return lambda: rnc.dprc_norm_hutch_layers(As, Gs, Ps, n, ws=ws)
 
 
+def _hutch_pm1(name):
+    wk = wl.WORKLOADS[name]
+    lay = wk.layers[0]
+    A, G, _ = wl.layer_inputs(wk, 0, device="cuda")
+    n = torch.zeros(wk.B, device="cuda")
+    ws = rnc.workspace(rnc.DPRC_OP_HUTCH_PM1, A, wk.B, wk.T, lay.d, lay.p, wk.k)
+    return lambda: rnc.dprc_norm_hutch_pm1(A, G, wk.k, 1234, 1, n, ws=ws)
+
+
 def _hutchpp():
     wk = wl.WORKLOADS["hutchpp_q_proj_b8_t4096_r16_bf16"]
     lay = wk.layers[0]
@@ -77,6 +86,8 @@ CASES = {
     # B8 T4096 d = p = 2048 k32 bf16 (268 MB of A and G)
     "hutch_q_proj": lambda: _hutch("hutch_q_proj_b8_t4096_k32_bf16"),
     # B2 T32768 2048 -> 8192 and 8192 -> 2048, k32 bf16 (1.34 GB each)
+    # the same batch with the +-1 projection generated in the kernel
+    "hutch_pm1_q_proj": lambda: _hutch_pm1("hutch_q_proj_b8_t4096_k32_bf16"),
     "hutch_long_up": lambda: _hutch("hutch_long_b2_t32768_up_down_k32_bf16", 0),
     "hutch_long_down": lambda: _hutch("hutch_long_b2_t32768_up_down_k32_bf16", 1),
     # one Llama-3.2-1B decoder block (q, k, v, o, gate, up, down) in one
