@@ -592,6 +592,41 @@ def measure_rows(which, device, peak, tflops_peak, seed_shift):
                             "what": "dprc_exact_norm on the q_proj batch, direct form on "
                                     "tensor cores; flops 2 T d p per sample"}
         del A, G, n, wsbuf
+        # short sequences: the q_proj widths at T = 1024 with B = 32 (the same
+        # 268 MB of A and G), where the ghost form sum_{t,s} (A A^T)(G G^T) does
+        # half the direct form's work; both forms timed, the automatic choice
+        # named
+        B, T = 32, 1024
+        A, G, _ = wl.layer_inputs(wl.Workload(**{**wk.__dict__, "seed": wk.seed + seed_shift}),
+                                  0, device=device, B=B, T=T)
+        n = torch.zeros(B, device=device)
+        wsbuf = rnc.workspace(rnc.DPRC_OP_EXACT, A, B, T, lay.d, lay.p, wk.k)
+        auto = rnc.dprc_exact_norm_plan(rnc.DPRC_BF16, B, T, lay.d, lay.p)
+        nt = (T + 127) // 128
+        flops_ghost = B * T * (T + 1) * (lay.d + lay.p)  # Gram entries t <= s, 2 (d + p) each
+        forms = {}
+        for name, form in (("ghost_n128", rnc.DPRC_EXACT_GHOST_N128),
+                           ("ghost_n256", rnc.DPRC_EXACT_GHOST_N256),
+                           ("direct", rnc.DPRC_EXACT_DIRECT)):
+            t = graph_ms(lambda: rnc.dprc_exact_norm(A, G, n, ws=wsbuf, form=form), device, 5,
+                         warmup=2)
+            fl = B * 2 * T * lay.d * lay.p if name == "direct" else flops_ghost
+            mma = (B * 2 * T * lay.d * lay.p if name == "direct"
+                   else B * nt * (nt + 1) // 2 * 2 * 128 * 128 * (lay.d + lay.p))
+            forms[name] = {"ms": t, "algorithmic_flops": fl, "mma_flops": mma,
+                           "achieved_tflops": fl / (t * 1e-3) / 1e12,
+                           "frac": fl / (t * 1e-3) / 1e12 / tflops_peak}
+        names = {rnc.DPRC_EXACT_DIRECT: "direct", rnc.DPRC_EXACT_GHOST_N128: "ghost_n128",
+                 rnc.DPRC_EXACT_GHOST_N256: "ghost_n256"}
+        best = min(forms, key=lambda k: forms[k]["ms"])
+        rows["exact_q_proj_b32_t1024"] = {
+            "forms": forms, "auto": names.get(auto, str(auto)), "fastest": best,
+            "bound": "tensor", "peak_tflops": tflops_peak,
+            "what": "dprc_exact_norm on q_proj widths at T = 1024, B = 32, each form; the "
+                    "ghost form's algorithmic flops count the Gram entries t <= s, "
+                    "T (T + 1) (d + p) per sample; mma_flops adds the diagonal blocks' "
+                    "lower halves"}
+        del A, G, n, wsbuf
     torch.cuda.empty_cache()
     return rows
 

@@ -183,21 +183,58 @@ dprc_status dprc_norm_hutchpp(const void* A, const void* G, const void* S, const
 /*
  * Exact squared norm n_i = ||A_i^T G_i||_F^2, the quantity the estimators
  * approximate (the comparison path the pages set the method against;
- * papernotes.org, "Research background" and "Key design"), by one of its two
- * exact forms:
- *   - bf16 with d and p multiples of 8: the direct form on tensor cores, the
- *     d x p product A_i^T G_i formed in 128 x 256 tiles in on-chip memory and
- *     squared there (never stored), O(T d p) work;
- *   - otherwise the ghost-clipping identity
- *         n_i = sum_{t,s} (A_i A_i^T)_{ts} (G_i G_i^T)_{ts}
- *     tile by tile on CUDA cores (no T x T matrix stored), O(T^2 (d + p)).
- * Both sum in a fixed order (bitwise repeatable).  Arguments as
+ * papernotes.org, "Research background" and "Key design"; the pages weigh the
+ * full-gradient form, O(T d p) per sample, against ghost clipping,
+ * O(T^2 (d + p))).  Two exact forms:
+ *   - direct: the d x p product A_i^T G_i formed in 128 x 256 tiles in
+ *     on-chip memory and squared there (never stored);
+ *   - ghost:  n_i = sum_{t,s} (A_i A_i^T)_{ts} (G_i G_i^T)_{ts}, tile by tile
+ *     over the upper triangle of 128-token blocks (no T x T matrix stored).
+ * bf16 with d and p multiples of 8 runs both on tensor cores (the ghost form
+ * up to T = 65536); other layouts run the ghost form on CUDA cores (fp32,
+ * T <= 2097120).  dprc_exact_norm takes the form with less tensor work for
+ * these sizes on the current device (ghost when T < 2 d p / (d + p) and the
+ * batch has enough 128-token blocks to keep every SM busy);
+ * dprc_exact_norm_form lets the caller choose.  Both sum in a fixed order
+ * (bitwise repeatable for fixed inputs, sizes, form and device).  Both
+ * accumulate in fp32; the ghost form adds T^2 signed products whose sum can
+ * be much smaller than its terms, so its rounding error scales with
+ * (sum_t ||A_i[t]|| ||G_i[t]||)^2 rather than with n_i (a sum that rounding
+ * takes below zero is returned as 0).  Arguments as
  * dprc_norm_hutch without P and k; the workspace size comes from
- * dprc_workspace_bytes(DPRC_OP_EXACT, ...).
+ * dprc_workspace_bytes(DPRC_OP_EXACT, ...) and covers every form.
  */
 dprc_status dprc_exact_norm(const void* A, const void* G, dprc_dtype dtype, int64_t B,
                             int64_t T, int64_t d, int64_t p, float* n, int accumulate,
                             void* ws, size_t ws_bytes, void* stream);
+
+typedef enum {
+    DPRC_EXACT_AUTO = 0,        /* the form dprc_exact_norm takes */
+    DPRC_EXACT_DIRECT = 1,      /* A_i^T G_i; tensor-core layout only */
+    DPRC_EXACT_GHOST = 2,       /* sum_{t,s} (A A^T)_{ts} (G G^T)_{ts} */
+    DPRC_EXACT_GHOST_N128 = 3,  /* ghost, Gram tiles 128 x 128 (tensor cores) */
+    DPRC_EXACT_GHOST_N256 = 4   /* ghost, Gram tiles 128 x 256 (tensor cores) */
+} dprc_exact_form;
+
+/*
+ * dprc_exact_norm with the form chosen by the caller (a dprc_exact_form).
+ * GHOST takes the tile width with less work for these sizes; GHOST_N128 and
+ * GHOST_N256 fix it (tensor-core layout only).  DPRC_ERR_SHAPE for an unknown
+ * form, for DIRECT or a fixed tile width outside the tensor-core layout and
+ * for a ghost form beyond its T limit.  Other errors as dprc_exact_norm.
+ */
+dprc_status dprc_exact_norm_form(const void* A, const void* G, dprc_dtype dtype, int64_t B,
+                                 int64_t T, int64_t d, int64_t p, int form, float* n,
+                                 int accumulate, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * The form a dprc_exact_norm_form call with these arguments runs on the
+ * current device: DPRC_EXACT_DIRECT, DPRC_EXACT_GHOST_N128 or
+ * DPRC_EXACT_GHOST_N256 on tensor cores, DPRC_EXACT_GHOST on CUDA cores; 0
+ * when it would be rejected or no sm_103 device is current.  Enqueues nothing.
+ */
+int dprc_exact_norm_plan(dprc_dtype dtype, int64_t B, int64_t T, int64_t d, int64_t p,
+                         int form);
 
 /*
  * Clip factors c_i = min(1, C / sqrt(n_i)) (papernotes.org, "Method > Overall

@@ -1,14 +1,19 @@
 """GB300 (sm_103a) hot path of DP-SGD with randomized clipping (DP-SGD-RC).
 
 The compute lives in libdprc.so (C ABI: include/dprc.h): tensor-core
-Hutchinson and Hutch++ per-sample gradient-norm estimation, the exact
-ghost-clipping norm, clip factors and Philox Gaussian noise.  This package is
-its ctypes binding plus the seeded synthetic workloads used by the tests and
-the benchmark.
+Hutchinson and Hutch++ per-sample gradient-norm estimation, the exact norm
+(direct and ghost-clipping forms), clip factors and Philox Gaussian noise.
+This package is its ctypes binding plus the seeded synthetic workloads used by
+the tests and the benchmark.
 """
 
 from .binding import (  # noqa: F401
     DPRC_BF16,
+    DPRC_EXACT_AUTO,
+    DPRC_EXACT_DIRECT,
+    DPRC_EXACT_GHOST,
+    DPRC_EXACT_GHOST_N128,
+    DPRC_EXACT_GHOST_N256,
     DPRC_F32,
     DPRC_OP_EXACT,
     DPRC_OP_HUTCH,
@@ -22,6 +27,7 @@ from .binding import (  # noqa: F401
     dprc_clip_factors,
     dprc_device_error,
     dprc_exact_norm,
+    dprc_exact_norm_plan,
     dprc_norm_hutch,
     dprc_norm_hutch_launches,
     dprc_norm_hutch_layers,

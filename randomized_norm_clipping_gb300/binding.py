@@ -21,6 +21,8 @@ LIB_PATH = os.path.join(PKG_DIR, "libdprc.so")
 DPRC_F32, DPRC_BF16 = 0, 1
 DPRC_OP_HUTCH, DPRC_OP_HUTCHPP, DPRC_OP_EXACT, DPRC_OP_HUTCH_LAYERS, DPRC_OP_HUTCH_PM1 = (
     1, 2, 3, 4, 5)
+(DPRC_EXACT_AUTO, DPRC_EXACT_DIRECT, DPRC_EXACT_GHOST, DPRC_EXACT_GHOST_N128,
+ DPRC_EXACT_GHOST_N256) = (0, 1, 2, 3, 4)
 STATUS = {0: "ok", 1: "null pointer", 2: "shape", 3: "dtype", 4: "alignment",
           5: "workspace", 6: "cuda", 7: "non-finite", 8: "device", 9: "too large"}
 
@@ -59,6 +61,11 @@ _PROTOS = [
       _c.c_void_p]),
     ("dprc_norm_hutch_launches", _c.c_int,
      [_c.c_int, _c.c_int64, _c.c_int64, _c.c_int64, _c.c_int64, _c.c_int64]),
+    ("dprc_exact_norm_form", _c.c_int,
+     [_c.c_void_p, _c.c_void_p, _c.c_int, _c.c_int64, _c.c_int64, _c.c_int64, _c.c_int64,
+      _c.c_int, _c.c_void_p, _c.c_int, _c.c_void_p, _c.c_size_t, _c.c_void_p]),
+    ("dprc_exact_norm_plan", _c.c_int,
+     [_c.c_int, _c.c_int64, _c.c_int64, _c.c_int64, _c.c_int64, _c.c_int]),
     ("dprc_norm_hutch_noalloc", _c.c_int,
      [_c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_int, _c.c_int64, _c.c_int64, _c.c_int64,
       _c.c_int64, _c.c_int64, _c.c_void_p, _c.c_int, _c.c_void_p]),
@@ -232,17 +239,34 @@ def dprc_norm_hutch_noalloc(A, G, P, n, accumulate=False, stream=None):
     return n
 
 
-def dprc_exact_norm(A, G, n, accumulate=False, ws=None, stream=None):
-    """n[i] (+)= sum_{t,s} (A_i A_i^T)_{ts} (G_i G_i^T)_{ts} (see include/dprc.h)."""
+def dprc_exact_norm(A, G, n, accumulate=False, ws=None, stream=None, form=DPRC_EXACT_AUTO):
+    """n[i] (+)= ||A_i^T G_i||_F^2 exactly, by the direct form A_i^T G_i or the
+    ghost form sum_{t,s} (A_i A_i^T)_{ts} (G_i G_i^T)_{ts} (form: one of
+    DPRC_EXACT_*; AUTO takes the one with less work, see include/dprc.h)."""
     _need_cuda(A, G, n)
     B, T, d = A.shape
     p = G.shape[2]
     if ws is None:
         ws = workspace(DPRC_OP_EXACT, A, B, T, d, p, 0)
-    st = lib().dprc_exact_norm(_ptr(A), _ptr(G), _dtype_code(A), B, T, d, p, _ptr(n),
-                               int(bool(accumulate)), _ptr(ws), ws.numel(), _stream(A, stream))
-    _check("dprc_exact_norm", st)
+    if form == DPRC_EXACT_AUTO:
+        st = lib().dprc_exact_norm(_ptr(A), _ptr(G), _dtype_code(A), B, T, d, p, _ptr(n),
+                                   int(bool(accumulate)), _ptr(ws), ws.numel(),
+                                   _stream(A, stream))
+        _check("dprc_exact_norm", st)
+    else:
+        st = lib().dprc_exact_norm_form(_ptr(A), _ptr(G), _dtype_code(A), B, T, d, p, int(form),
+                                        _ptr(n), int(bool(accumulate)), _ptr(ws), ws.numel(),
+                                        _stream(A, stream))
+        _check("dprc_exact_norm_form", st)
     return n
+
+
+def dprc_exact_norm_plan(dtype, B, T, d, p, form=DPRC_EXACT_AUTO):
+    """The form (DPRC_EXACT_DIRECT, _GHOST_N128 or _GHOST_N256 on tensor cores,
+    _GHOST on CUDA cores) an exact-norm call with these sizes runs on the
+    current device, 0 if it would be rejected."""
+    code = dtype if isinstance(dtype, int) else _dtype_code(torch.empty(0, dtype=dtype))
+    return lib().dprc_exact_norm_plan(code, B, T, d, p, int(form))
 
 
 def dprc_clip_factors(n, C, c, nonfinite=None, stream=None):

@@ -67,13 +67,13 @@ def _noise(n_elems):
     return lambda: rnc.dprc_add_noise(grad, 1.0, 1.0, 1234, 1)
 
 
-def _exact(B, T):
+def _exact(B, T, form=rnc.DPRC_EXACT_AUTO):
     wk = wl.WORKLOADS[wl.HEADLINE]
     lay = wk.layers[0]
     A, G, _ = wl.layer_inputs(wk, 0, device="cuda", B=B, T=T)
     n = torch.zeros(B, device="cuda")
     ws = rnc.workspace(rnc.DPRC_OP_EXACT, A, B, T, lay.d, lay.p, wk.k)
-    return lambda: rnc.dprc_exact_norm(A, G, n, ws=ws)
+    return lambda: rnc.dprc_exact_norm(A, G, n, ws=ws, form=form)
 
 
 def _clip():
@@ -101,6 +101,10 @@ CASES = {
     "noise_llama32_1b": lambda: _noise(wl.LLAMA32_1B_PARAMS),
     # exact ghost norm on 2 samples of the q_proj batch, T = 1024
     "exact_q_proj_b2_t1024": lambda: _exact(2, 1024),
+    # the ghost form on q_proj widths at T = 1024, B = 32 (268 MB of A and G),
+    # Gram tiles 128 x 256 and 128 x 128
+    "exact_ghost_n256_q_proj_b32_t1024": lambda: _exact(32, 1024, rnc.DPRC_EXACT_GHOST_N256),
+    "exact_ghost_n128_q_proj_b32_t1024": lambda: _exact(32, 1024, rnc.DPRC_EXACT_GHOST_N128),
     "clip_b8": _clip,
 }
 

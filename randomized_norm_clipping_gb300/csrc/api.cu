@@ -206,19 +206,90 @@ SimtPlan plan_simt(dprc_op op, int64_t B, int64_t T, int64_t d, int64_t p, int64
   return s;
 }
 
-// The direct form on tensor cores when the layout allows it (bf16, rows of d
-// and p 16-byte multiples for TMA), else the ghost form on CUDA cores.
+// Tensor-core layout of the exact norm: bf16 with rows of d and p 16-byte
+// multiples (TMA).  Both exact forms run there; other layouts take the ghost
+// form on CUDA cores.
 bool exact_direct_tc(dprc_dtype dt, int64_t d, int64_t p) {
   return dt == DPRC_BF16 && d % 8 == 0 && p % 8 == 0;
 }
 
 size_t exact_partials_off(int64_t B) { return align_up(ctrl_bytes(B), 1024); }
 
+namespace {
+// Longest T the tensor-core ghost form takes (its partials grow as T^2).
+constexpr int64_t kGhostTcMaxT = 65536;
+// Longest T of the CUDA-core ghost form (its grid has T / 32 rows).
+constexpr int64_t kGhostSimtMaxT = int64_t(65535) * 32;
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Time of a persistent one-CTA-per-SM launch in units of one 128 x 256 x 64
+// MMA stage of the ghost kernel, for the busiest CTA.  Direct form:
+// B ceil(d/128) ceil(p/256) equal tiles of ceil(T/64) stages, dealt out with
+// a stride of the grid.  Ghost form: B S_W(nt) units of (d + p) / 64 stages;
+// a unit's time does not depend on its width (a 128 x 128 MMA takes about as
+// long as a 128 x 256 one on this part), so the busiest CTA runs
+// ceil(units / SMs) of them.  Relative stage rates measured on GB300: the
+// direct kernel's stage 1.06, a 128 x 128 ghost stage 0.92 of a 128 x 256 one.
+double exact_cost_direct(int64_t B, int64_t T, int64_t d, int64_t p, int sms) {
+  const int64_t tiles = B * cdiv(d, 128) * cdiv(p, 256);
+  return static_cast<double>(cdiv(tiles, sms)) * static_cast<double>(cdiv(T, 64)) * 1.06;
+}
+
+double exact_cost_ghost(int64_t B, int64_t T, int64_t d, int64_t p, int W, int sms) {
+  const int64_t units = ghost_partials(B, T, W);
+  const double stages = static_cast<double>(cdiv(d, 64) + cdiv(p, 64));
+  return static_cast<double>(cdiv(units, sms)) * stages * (W == 1 ? 0.92 : 1.0);
+}
+}  // namespace
+
+ExactPlan plan_exact(dprc_dtype dt, int64_t B, int64_t T, int64_t d, int64_t p, int form) {
+  ExactPlan e;
+  if (form < DPRC_EXACT_AUTO || form > DPRC_EXACT_GHOST_N256) return e;
+  if (!exact_direct_tc(dt, d, p)) {
+    if (form == DPRC_EXACT_DIRECT || form == DPRC_EXACT_GHOST_N128 ||
+        form == DPRC_EXACT_GHOST_N256 || T > kGhostSimtMaxT)
+      return e;
+    e.kind = ExactPlan::kGhostSimt;
+    e.per_sample = cdiv(T, 32) * cdiv(T, 32);
+    return e;
+  }
+  const int sms = device_sm_count() > 0 ? device_sm_count() : 1;
+  const double cd = exact_cost_direct(B, T, d, p, sms);
+  double cg = -1.0;
+  int wg = 2;
+  if (T <= kGhostTcMaxT) {
+    const double c1 = exact_cost_ghost(B, T, d, p, 1, sms);
+    const double c2 = exact_cost_ghost(B, T, d, p, 2, sms);
+    wg = form == DPRC_EXACT_GHOST_N128 ? 1 : (form == DPRC_EXACT_GHOST_N256 ? 2 : (c1 < c2 ? 1 : 2));
+    cg = wg == 1 ? c1 : c2;
+  }
+  const bool ghost = form == DPRC_EXACT_GHOST || form == DPRC_EXACT_GHOST_N128 ||
+                     form == DPRC_EXACT_GHOST_N256 ||
+                     (form == DPRC_EXACT_AUTO && cg >= 0 && cg < cd);
+  if (ghost) {
+    if (cg < 0) return e;
+    e.kind = ExactPlan::kGhostTc;
+    e.W = wg;
+    e.per_sample = ghost_partials(1, T, wg);
+  } else {
+    e.kind = ExactPlan::kDirectTc;
+    e.per_sample = fgc_partials(1, d, p);
+  }
+  return e;
+}
+
 size_t plan_exact_bytes(dprc_dtype dt, int64_t B, int64_t T, int64_t d, int64_t p) {
-  if (exact_direct_tc(dt, d, p))
-    return exact_partials_off(B) + align_up(static_cast<size_t>(fgc_partials(B, d, p)) * 4, 1024);
-  const int64_t nt = (T + 31) / 32;
-  return exact_partials_off(B) + align_up(static_cast<size_t>(B) * nt * nt * 4, 1024);
+  // room for whichever form and span width a call takes (W = 1 has the most
+  // ghost units), independent of the device
+  int64_t most = 0;
+  if (exact_direct_tc(dt, d, p)) {
+    most = fgc_partials(1, d, p);
+    if (T <= kGhostTcMaxT) most = std::max(most, ghost_partials(1, T, 1));
+  } else {
+    most = cdiv(T, 32) * cdiv(T, 32);
+  }
+  return exact_partials_off(B) + align_up(static_cast<size_t>(B) * most * 4, 1024);
 }
 
 // ---- tensor maps ------------------------------------------------------------
@@ -584,27 +655,56 @@ dprc_status dprc_norm_hutchpp(const void* A, const void* G, const void* S, const
   return cuda_status(e);
 }
 
-dprc_status dprc_exact_norm(const void* A, const void* G, dprc_dtype dtype, int64_t B, int64_t T,
-                            int64_t d, int64_t p, float* n, int accumulate, void* ws,
-                            size_t ws_bytes, void* stream) {
+dprc_status dprc_exact_norm_form(const void* A, const void* G, dprc_dtype dtype, int64_t B,
+                                 int64_t T, int64_t d, int64_t p, int form, float* n,
+                                 int accumulate, void* ws, size_t ws_bytes, void* stream) {
   if (!A || !G || !n) return DPRC_ERR_NULL;
   dprc_status st = check_common(dtype, B, T, d, p);
   if (st != DPRC_OK) return st;
-  if (!exact_direct_tc(dtype, d, p) && T > 65535 * 32) return DPRC_ERR_SHAPE;  // ghost grid
   if (!aligned16(A) || !aligned16(G) || !aligned16(n)) return DPRC_ERR_ALIGN;
   if (!ws) return DPRC_ERR_WORKSPACE;
   if (!aligned16(ws)) return DPRC_ERR_ALIGN;
+  if (plan_exact(dtype, B, T, d, p, form).kind == ExactPlan::kNone) return DPRC_ERR_SHAPE;
   if (ws_bytes < plan_exact_bytes(dtype, B, T, d, p)) return DPRC_ERR_WORKSPACE;
   if (!device_ok()) return DPRC_ERR_DEVICE;
+  const ExactPlan e = plan_exact(dtype, B, T, d, p, form);  // with this device's SM count
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   mark(0, s);
   float* partials = reinterpret_cast<float*>(static_cast<char*>(ws) + exact_partials_off(B));
-  cudaError_t e =
-      exact_direct_tc(dtype, d, p)
-          ? launch_tc_exact_direct(A, G, B, T, d, p, partials, n, accumulate, s)
-          : launch_exact_ghost(A, G, dtype, B, T, d, p, partials, n, accumulate, s);
+  cudaError_t err = cudaSuccess;
+  switch (e.kind) {
+    case ExactPlan::kDirectTc:
+      err = launch_tc_exact_direct(A, G, B, T, d, p, partials, n, accumulate, s);
+      break;
+    case ExactPlan::kGhostTc:
+      // the work queue's counters sit at the front of the zeroed counter block
+      err = launch_tc_exact_ghost(A, G, B, T, d, p, e.W, ws, partials, n, accumulate, s);
+      break;
+    default:
+      err = launch_exact_ghost(A, G, dtype, B, T, d, p, partials, n, accumulate, s);
+  }
   mark(1, s);
-  return cuda_status(e);
+  return cuda_status(err);
+}
+
+dprc_status dprc_exact_norm(const void* A, const void* G, dprc_dtype dtype, int64_t B, int64_t T,
+                            int64_t d, int64_t p, float* n, int accumulate, void* ws,
+                            size_t ws_bytes, void* stream) {
+  return dprc_exact_norm_form(A, G, dtype, B, T, d, p, DPRC_EXACT_AUTO, n, accumulate, ws,
+                              ws_bytes, stream);
+}
+
+int dprc_exact_norm_plan(dprc_dtype dtype, int64_t B, int64_t T, int64_t d, int64_t p,
+                         int form) {
+  if (check_common(dtype, B, T, d, p) != DPRC_OK) return 0;
+  if (!device_ok()) return 0;
+  const ExactPlan e = plan_exact(dtype, B, T, d, p, form);
+  switch (e.kind) {
+    case ExactPlan::kDirectTc: return DPRC_EXACT_DIRECT;
+    case ExactPlan::kGhostTc: return e.W == 1 ? DPRC_EXACT_GHOST_N128 : DPRC_EXACT_GHOST_N256;
+    case ExactPlan::kGhostSimt: return DPRC_EXACT_GHOST;
+    default: return 0;
+  }
 }
 
 dprc_status dprc_clip_factors(const float* n, int64_t B, float C, float* c, int32_t* nonfinite,

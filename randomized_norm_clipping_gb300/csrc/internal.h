@@ -83,6 +83,14 @@ size_t ctrl_bytes(int64_t B);
 TcPlan plan_tc(dprc_op op, int64_t B, int64_t T, int64_t d, int64_t p, int64_t k,
                int layers = 1);
 SimtPlan plan_simt(dprc_op op, int64_t B, int64_t T, int64_t d, int64_t p, int64_t k);
+// Which kernel an exact-norm call runs (form: dprc_exact_form).
+struct ExactPlan {
+  enum Kind { kNone = 0, kDirectTc, kGhostTc, kGhostSimt };
+  Kind kind = kNone;
+  int W = 0;               // span width of the tensor-core ghost form
+  int64_t per_sample = 0;  // partials per sample
+};
+ExactPlan plan_exact(dprc_dtype dt, int64_t B, int64_t T, int64_t d, int64_t p, int form);
 size_t plan_exact_bytes(dprc_dtype dt, int64_t B, int64_t T, int64_t d, int64_t p);
 
 // ---- tensor maps -----------------------------------------------------------
@@ -139,7 +147,6 @@ cudaError_t launch_qr_project(const float* M, int64_t B, int64_t p, int r, const
                               dprc_dtype pdt, float* scratch, void* out, bool hilo,
                               cudaStream_t s);
 
-// Exact (ghost) norm, SIMT fp32, deterministic.
 // Exact norm on tensor cores by the direct form: per sample, 128 x 256 tiles
 // of A_i^T G_i accumulated over T in TMEM and squared in the epilogue; one
 // partial per tile (fgc_partials(B, d, p) floats), summed per sample in index
@@ -184,9 +191,21 @@ cudaError_t launch_pm1_signs(void* out, dprc_dtype dt, int64_t n, uint64_t seed,
 cudaError_t launch_tc_exact_direct(const void* A, const void* G, int64_t B, int64_t T, int64_t d,
                                    int64_t p, float* partials, float* n_out, int accumulate,
                                    cudaStream_t s);
+// Exact norm on tensor cores by the ghost form: per sample, 128-token row
+// blocks against spans of W = 1 or 2 column blocks (upper triangle), the Gram
+// tiles of A and of G in TMEM and their weighted dot product in the epilogue;
+// one partial per unit (ghost_partials(B, T, W) floats), summed per sample in
+// index order into n_out.  bf16, d and p multiples of 8.  `counters`: 16
+// bytes, 8-byte aligned, zero on entry and left zero (the work queue).
+int64_t ghost_partials(int64_t B, int64_t T, int W);
+cudaError_t launch_tc_exact_ghost(const void* A, const void* G, int64_t B, int64_t T, int64_t d,
+                                  int64_t p, int W, void* counters, float* partials,
+                                  float* n_out, int accumulate, cudaStream_t s);
 // n_out[i] (+)= sum of partials[i * per_sample .. (i + 1) * per_sample), fixed order.
 cudaError_t launch_partials_finish(const float* partials, int64_t B, int64_t per_sample,
                                    float* n_out, int accumulate, cudaStream_t s);
+// Exact norm by the ghost form on CUDA cores (fp32 arithmetic, any layout),
+// deterministic.
 cudaError_t launch_exact_ghost(const void* A, const void* G, dprc_dtype dt, int64_t B,
                                int64_t T, int64_t d, int64_t p, float* partials, float* n_out,
                                int accumulate, cudaStream_t s);

@@ -144,6 +144,9 @@ __global__ void __launch_bounds__(256) simt_norm_finish_kernel(const float* __re
     s = fmaf((j < n_head ? 1.f : w_tail) * y, y, s);
   }
   s = block_sum_256(s, red);
+  // a squared norm is never negative: a ghost-form sum that rounding in heavy
+  // cancellation took below zero is returned as 0 (a NaN stays NaN)
+  if (s < 0.f) s = 0.f;
   if (threadIdx.x == 0) n_out[i] = (accumulate ? n_out[i] : 0.f) + s;
 }
 
@@ -208,6 +211,9 @@ __global__ void __launch_bounds__(256) exact_finish_kernel(const float* __restri
   float s = 0.f;
   for (long long e = threadIdx.x; e < per_sample; e += 256) s += pi[e];
   s = block_sum_256(s, red);
+  // a squared norm is never negative: a ghost-form sum that rounding in heavy
+  // cancellation took below zero is returned as 0 (a NaN stays NaN)
+  if (s < 0.f) s = 0.f;
   if (threadIdx.x == 0) n_out[i] = (accumulate ? n_out[i] : 0.f) + s;
 }
 

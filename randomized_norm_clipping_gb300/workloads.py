@@ -109,12 +109,18 @@ def _gen(device, seed):
     return g
 
 
-def sample_scales(wl: Workload, device="cpu"):
-    """Per-sample gradient scales s_i (float32 [B])."""
+def sample_scales(wl: Workload, device="cpu", B=None):
+    """Per-sample gradient scales s_i (float32 [B], B = the workload's batch by
+    default; a larger B appends draws from a second seed, so the first
+    samples keep their scales)."""
+    B = wl.B if B is None else B
     if wl.g_scale != "lognormal":
-        return torch.ones(wl.B, dtype=torch.float32, device=device)
+        return torch.ones(B, dtype=torch.float32, device=device)
     z = torch.randn(wl.B, generator=_gen(device, wl.seed + 7), device=device)
-    return torch.exp(-4.0 + z)
+    if B > wl.B:
+        extra = torch.randn(B - wl.B, generator=_gen(device, wl.seed + 8), device=device)
+        z = torch.cat([z, extra])
+    return torch.exp(-4.0 + z[:B])
 
 
 def layer_inputs(wl: Workload, layer_index: int, device="cpu", B=None, T=None):
@@ -136,7 +142,7 @@ def layer_inputs(wl: Workload, layer_index: int, device="cpu", B=None, T=None):
         G = (torch.bmm(U, V.transpose(1, 2)) / math.sqrt(8.0) + 0.05 * E).to(dt)
         del U, V, E
     else:
-        s = sample_scales(wl, device)[:B]
+        s = sample_scales(wl, device, B)
         G = (torch.randn(B, T, p, generator=_gen(device, base + 2), device=device)
              * s.view(B, 1, 1)).to(dt)
     if wl.method == "hutchpp":

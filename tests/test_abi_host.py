@@ -58,10 +58,14 @@ def test_workspace_bytes_host_only(lib):
     ws32 = b.dprc_workspace_bytes(b.DPRC_OP_HUTCH, b.DPRC_F32, 4, 128, 64, 64, 8)
     assert ws32 >= 4 * 128 * 8 * 4
     assert b.dprc_workspace_bytes(b.DPRC_OP_HUTCHPP, b.DPRC_BF16, 8, 4096, 2048, 2048, 16) > 0
-    # exact norm: bf16 with aligned widths takes the direct tensor-core form
-    # (one fp32 partial per 128 x 256 tile of A^T G); fp32 or odd widths the
-    # ghost form (one partial per pair of 32-token tiles)
+    # exact norm: bf16 with aligned widths runs both forms on tensor cores
+    # (one fp32 partial per 128 x 256 tile of A^T G, or per 128-token row
+    # block and span of the ghost form: T (T + 1) / 2 blocks of 128 for
+    # single-block spans); fp32 or odd widths the ghost form on CUDA cores (one
+    # partial per pair of 32-token tiles)
     assert b.dprc_workspace_bytes(b.DPRC_OP_EXACT, b.DPRC_BF16, 2, 4096, 2048, 2048, 0) >= 2 * 16 * 8 * 4
+    assert b.dprc_workspace_bytes(b.DPRC_OP_EXACT, b.DPRC_BF16, 2, 4096, 2048, 2048, 0) >= 2 * 32 * 33 // 2 * 4
+    assert b.dprc_workspace_bytes(b.DPRC_OP_EXACT, b.DPRC_BF16, 3, 1000, 64, 16, 0) >= 3 * 8 * 9 // 2 * 4
     assert b.dprc_workspace_bytes(b.DPRC_OP_EXACT, b.DPRC_F32, 2, 4096, 64, 64, 0) >= 2 * 128 * 128 * 4
     assert b.dprc_workspace_bytes(b.DPRC_OP_EXACT, b.DPRC_BF16, 2, 4096, 63, 64, 0) >= 2 * 128 * 128 * 4
     # invalid sizes give 0
@@ -103,6 +107,16 @@ def test_argument_errors_return_before_device_work(lib):
     e = lib.dprc_exact_norm
     assert e(_vp(A16), None, 1, 1, 1, 8, 8, _vp(A16), 0, _vp(A16), ws, None) == 1
     assert e(_vp(A16), _vp(A16), 1, 1, 1, 8, 8, _vp(A16), 0, _vp(A16), 0, None) == 5
+    ef = lib.dprc_exact_norm_form
+    assert ef(_vp(A16), _vp(A16), 1, 1, 1, 8, 8, 5, _vp(A16), 0, _vp(A16), ws, None) == 2  # form
+    assert ef(_vp(A16), _vp(A16), 0, 1, 1, 8, 8, 3, _vp(A16), 0, _vp(A16), ws, None) == 2
+    # the direct form needs bf16 rows of 16-byte multiples
+    assert ef(_vp(A16), _vp(A16), 0, 1, 1, 8, 8, 1, _vp(A16), 0, _vp(A16), ws, None) == 2
+    assert ef(_vp(A16), _vp(A16), 1, 1, 1, 12, 8, 1, _vp(A16), 0, _vp(A16), ws, None) == 2
+    # the tensor-core ghost form stops at T = 65536
+    assert ef(_vp(A16), _vp(A16), 1, 1, 65537, 8, 8, 2, _vp(A16), 0, _vp(A16), ws, None) == 2
+    assert ef(_vp(A16), _vp(A16), 1, 1, 64, 8, 8, 2, _vp(A16), 0, _vp(A16), 0, None) == 5
+    assert lib.dprc_exact_norm_plan(1, 1, 64, 8, 8, 5) == 0
     c = lib.dprc_clip_factors
     assert c(None, 4, ctypes.c_float(1.0), _vp(A16), None, None) == 1
     assert c(_vp(A16), 4, ctypes.c_float(0.0), _vp(A16), None, None) == 2

@@ -196,8 +196,9 @@ def test_hutchpp_exact_on_low_rank_gradients():
 
 # ------------------------------------------------------------------ exact norm
 
-# bf16 with d, p multiples of 8 takes the tensor-core direct form (128 x 256
-# tiles of A^T G); fp32 or other widths take the ghost form on CUDA cores.
+# The automatic choice: bf16 with d, p multiples of 8 takes a tensor-core form
+# (direct A^T G in 128 x 256 tiles, or ghost for short T); fp32 or other widths
+# take the ghost form on CUDA cores.
 @pytest.mark.parametrize("B,T,d,p,dtype", [(4, 128, 64, 64, torch.float32),
                                            (2, 333, 96, 40, torch.bfloat16),
                                            (2, 333, 97, 41, torch.bfloat16),
@@ -239,6 +240,99 @@ def test_exact_norm_full_size_samples():
     n = torch.zeros(2, device=DEV)
     rnc.dprc_exact_norm(A, G, n)
     assert _relerr(n.cpu(), oracle.exact_norm(to_f64(A), to_f64(G))) < RTOL
+
+
+# Both exact forms on tensor cores at fixed forms and tile widths: T from one
+# token to several 128-token blocks with ragged tails (odd and even block
+# counts, so spans of two blocks end both full and half), ragged d and p, and
+# LoRA-shaped widths.
+EXACT_FORMS = [rnc.DPRC_EXACT_DIRECT, rnc.DPRC_EXACT_GHOST_N128, rnc.DPRC_EXACT_GHOST_N256]
+EXACT_FORM_SHAPES = [(1, 1, 8, 8), (2, 100, 64, 72), (2, 129, 96, 40), (3, 257, 200, 136),
+                     (2, 384, 64, 64), (2, 1000, 392, 600), (1, 2048, 128, 256),
+                     (4, 640, 2048, 16), (4, 640, 16, 2048)]
+
+
+@pytest.mark.parametrize("form", EXACT_FORMS)
+@pytest.mark.parametrize("B,T,d,p", EXACT_FORM_SHAPES)
+def test_exact_forms_match_oracle(B, T, d, p, form):
+    A = _rand((B, T, d), 80 + T, torch.bfloat16)
+    G = _rand((B, T, p), 81 + T, torch.bfloat16, 0.05)
+    n = torch.zeros(B, device=DEV)
+    rnc.dprc_exact_norm(A.to(DEV), G.to(DEV), n, form=form)
+    assert _relerr(n.cpu(), oracle.exact_norm(to_f64(A), to_f64(G))) < RTOL
+
+
+def test_exact_forms_agree_with_the_ghost_oracle_and_repeat():
+    A = _rand((3, 700, 264), 90, torch.bfloat16)
+    G = _rand((3, 700, 520), 91, torch.bfloat16, 0.05)
+    Ad, Gd = A.to(DEV), G.to(DEV)
+    ref = oracle.ghost_norm(to_f64(A), to_f64(G))
+    for form in (rnc.DPRC_EXACT_GHOST_N128, rnc.DPRC_EXACT_GHOST_N256):
+        n = torch.full((3,), 1.5, device=DEV)
+        rnc.dprc_exact_norm(Ad, Gd, n, accumulate=True, form=form)
+        assert _relerr(n.cpu(), ref + 1.5) < RTOL
+        rnc.dprc_exact_norm(Ad, Gd, n, form=form)
+        once = n.clone()
+        rnc.dprc_exact_norm(Ad, Gd, n, form=form)
+        assert torch.equal(n, once)  # fixed summation order: bitwise repeatable
+
+
+def test_ghost_form_under_cancellation():
+    # nearly collinear token rows and alternating-sign gradients: the T^2
+    # Gram products are large and cancel, so n_i is small against them.  The
+    # ghost form's error must stay within fp32 rounding of the scale
+    # (sum_t ||a_t|| ||g_t||)^2 (each Gram entry is accurate to a few ulp of
+    # ||a_t|| ||a_s||), its result must not be negative, and the direct form,
+    # a sum of squares, stays accurate relative to n_i.
+    B, T, d, p = 2, 512, 256, 128
+    gen = torch.Generator().manual_seed(5)
+    a = torch.randn(B, 1, d, generator=gen)
+    g = torch.randn(B, 1, p, generator=gen)
+    sign = (-1.0) ** torch.arange(T).reshape(1, T, 1)
+    A = (a + 0.01 * torch.randn(B, T, d, generator=gen)).to(torch.bfloat16)
+    G = (sign * g + 0.01 * torch.randn(B, T, p, generator=gen)).to(torch.bfloat16)
+    ref = oracle.exact_norm(to_f64(A), to_f64(G))
+    Af, Gf = to_f64(A), to_f64(G)
+    scale = np.array([(np.linalg.norm(Af[i], axis=1) * np.linalg.norm(Gf[i], axis=1)).sum() ** 2
+                      for i in range(B)])
+    assert np.all(ref < 1e-3 * scale)  # the case really cancels
+    for form in (rnc.DPRC_EXACT_GHOST_N128, rnc.DPRC_EXACT_GHOST_N256):
+        n = torch.zeros(B, device=DEV)
+        rnc.dprc_exact_norm(A.to(DEV), G.to(DEV), n, form=form)
+        got = n.cpu().numpy().astype(np.float64)
+        assert np.all(got >= 0)
+        assert np.all(np.abs(got - ref) <= 1e-5 * scale)
+    n = torch.zeros(B, device=DEV)
+    rnc.dprc_exact_norm(A.to(DEV), G.to(DEV), n, form=rnc.DPRC_EXACT_DIRECT)
+    assert _relerr(n.cpu(), ref) < RTOL
+
+
+def test_exact_auto_takes_the_form_with_less_work():
+    bf = rnc.DPRC_BF16
+    # q_proj widths: ghost below T = 2 d p / (d + p) = 2048 when the batch has
+    # enough 128-token blocks to fill the GPU, direct above
+    assert rnc.dprc_exact_norm_plan(bf, 32, 512, 2048, 2048) in (rnc.DPRC_EXACT_GHOST_N128,
+                                                                  rnc.DPRC_EXACT_GHOST_N256)
+    assert rnc.dprc_exact_norm_plan(bf, 32, 1024, 2048, 2048) in (rnc.DPRC_EXACT_GHOST_N128,
+                                                                   rnc.DPRC_EXACT_GHOST_N256)
+    assert rnc.dprc_exact_norm_plan(bf, 8, 4096, 2048, 2048) == rnc.DPRC_EXACT_DIRECT
+    # LoRA widths: the d x p product is tiny, always direct
+    assert rnc.dprc_exact_norm_plan(bf, 8, 512, 2048, 16) == rnc.DPRC_EXACT_DIRECT
+    # fixed forms are reported as asked; fp32 has only the CUDA-core ghost form
+    assert rnc.dprc_exact_norm_plan(bf, 8, 512, 2048, 2048, rnc.DPRC_EXACT_DIRECT) == \
+        rnc.DPRC_EXACT_DIRECT
+    assert rnc.dprc_exact_norm_plan(bf, 8, 512, 64, 64, rnc.DPRC_EXACT_GHOST_N128) == \
+        rnc.DPRC_EXACT_GHOST_N128
+    assert rnc.dprc_exact_norm_plan(rnc.DPRC_F32, 2, 64, 64, 64) == rnc.DPRC_EXACT_GHOST
+    assert rnc.dprc_exact_norm_plan(rnc.DPRC_F32, 2, 64, 64, 64, rnc.DPRC_EXACT_DIRECT) == 0
+    # the automatic call is bitwise the call of the form it reports
+    A = _rand((4, 300, 512), 95, torch.bfloat16).to(DEV)
+    G = _rand((4, 300, 384), 96, torch.bfloat16, 0.05).to(DEV)
+    form = rnc.dprc_exact_norm_plan(bf, 4, 300, 512, 384)
+    n0, n1 = torch.zeros(4, device=DEV), torch.zeros(4, device=DEV)
+    rnc.dprc_exact_norm(A, G, n0)
+    rnc.dprc_exact_norm(A, G, n1, form=form)
+    assert torch.equal(n0, n1)
 
 
 # ------------------------------------------------------------------ clip

@@ -87,6 +87,25 @@ def test_hutchpp_q_proj_b8_t4096_every_sample():
     assert rnc.dprc_device_error() == 0
 
 
+def test_exact_both_forms_q_proj_b32_t1024_sampled():
+    # the short-sequence exact-norm row of the benchmark: q_proj widths at
+    # T = 1024, B = 32, where the ghost form does half the direct form's work;
+    # every form on the full batch, the oracle on every fourth sample
+    wk = wl.WORKLOADS[wl.HEADLINE]
+    lay = wk.layers[0]
+    B, T = 32, 1024
+    A, G, _ = wl.layer_inputs(wk, 0, device=DEV, B=B, T=T)
+    idx = list(range(0, B, 4))
+    ref = oracle.exact_norm(to_f64(A[idx]), to_f64(G[idx]))
+    assert rnc.dprc_exact_norm_plan(rnc.DPRC_BF16, B, T, lay.d, lay.p) != rnc.DPRC_EXACT_DIRECT
+    for form in (rnc.DPRC_EXACT_AUTO, rnc.DPRC_EXACT_DIRECT, rnc.DPRC_EXACT_GHOST_N128,
+                 rnc.DPRC_EXACT_GHOST_N256):
+        n = torch.zeros(B, device=DEV)
+        rnc.dprc_exact_norm(A, G, n, form=form)
+        assert _relerr(n[idx].cpu(), ref) < RTOL, form
+    assert rnc.dprc_device_error() == 0
+
+
 @pytest.mark.parametrize("layer", [0, 1])
 def test_long_context_b2_t32768_sampled(layer):
     # the full B = 2 launch; the oracle checks sample 0 (one sample of
