@@ -135,6 +135,20 @@ __device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
 
+// Asynchronous 16-byte store into another CTA's shared memory whose arrival
+// is counted, as transaction bytes, on an mbarrier of that CTA (the receiver
+// announces the bytes it expects with mbar_arrive_expect_tx and waits on its
+// own barrier; the sender needs no fence).
+__device__ __forceinline__ void st_async_f4(uint32_t cluster_addr, float4 v,
+                                            uint32_t cluster_bar) {
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, "
+      "[%5];" ::"r"(cluster_addr),
+      "r"(__float_as_uint(v.x)), "r"(__float_as_uint(v.y)), "r"(__float_as_uint(v.z)),
+      "r"(__float_as_uint(v.w)), "r"(cluster_bar)
+      : "memory");
+}
+
 // Arrive (release at cluster scope) on an mbarrier of another CTA.
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)

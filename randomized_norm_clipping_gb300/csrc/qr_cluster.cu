@@ -16,9 +16,9 @@
 //   every CTA reduces its rows' 16 dot products s_l = x . V[:, l] (a warp
 //   butterfly, then the warps in order), warp 0 stores them, together with the
 //   pivot row (held by rank 0, zeros elsewhere), into a slot of every CTA of
-//   the cluster and arrives on that CTA's barrier; each CTA then sums the 8
-//   slots in rank order, so every CTA holds the same totals and applies the
-//   reflector to its own rows.
+//   the cluster with asynchronous stores counted on that CTA's barrier; each
+//   CTA then sums the 8 slots in rank order, so every CTA holds the same
+//   totals and applies the reflector to its own rows.
 //
 // The same exchange serves the column scaling before the steps and the
 // 16 x 16 product C = Q^T P after them.  Every CTA rebuilds, from the
@@ -105,26 +105,27 @@ struct Exchange {
 
 // Round `rnd` of the cluster all-gather, called by warp 0 once this CTA's
 // `n` values (a multiple of 4) sit in the local buffer slot [rnd & 1][rank]:
-// lane r < kCl copies them with 16-byte stores into the same slot of CTA r
-// (its own slot is already in place) and arrives on that CTA's barrier, so
-// the kCl destinations are served in parallel, one arrival each.
+// lane 0 announces the (kCl - 1) n floats this CTA will receive (the one
+// arrival the barrier counts; it also publishes the local slot), and lane
+// r < kCl, r != rank, copies the slot into the same slot of CTA r with
+// asynchronous 16-byte stores that complete on that CTA's barrier.  A peer can
+// be at most one round ahead (it needs this CTA's data of the current round
+// first), so two buffers and two barriers suffice.
 __device__ __forceinline__ void xch_send(const Exchange& x, int rnd, int n, int lane) {
   const int b = rnd & 1;
   __syncwarp();
-  if (lane < kCl) {
+  if (lane == 0) mbar_arrive_expect_tx(&x.bar[b], static_cast<uint32_t>((kCl - 1) * n * 4));
+  if (lane < kCl && lane != x.rank) {
     const float4* src = reinterpret_cast<const float4*>(&x.buf[b][x.rank][0]);
-    if (lane != x.rank) {
-      const uint32_t dst = map_to_rank(&x.buf[b][x.rank][0], lane);
-      for (int q = 0; q < n / 4; ++q) st_cluster_f4(dst + 16 * q, src[q]);
-    }
-    mbar_arrive_remote(map_to_rank(&x.bar[b], lane));
+    const uint32_t dst = map_to_rank(&x.buf[b][x.rank][0], lane);
+    const uint32_t rbar = map_to_rank(&x.bar[b], lane);
+    for (int q = 0; q < n / 4; ++q) st_async_f4(dst + 16 * q, src[q], rbar);
   }
 }
 
 // Every thread: wait until all CTAs' slots of round `rnd` have arrived.
 __device__ __forceinline__ bool xch_wait(const Exchange& x, int rnd) {
-  return mbar_wait_cluster(&x.bar[rnd & 1], static_cast<uint32_t>(rnd >> 1) & 1,
-                           DPRC_DEVERR_CLUSTER);
+  return mbar_wait(&x.bar[rnd & 1], static_cast<uint32_t>(rnd >> 1) & 1, DPRC_DEVERR_CLUSTER);
 }
 
 template <int RPT, typename TP>
@@ -153,8 +154,8 @@ __global__ void __launch_bounds__(kCt, 1)
   bool ok = true;
 
   if (tid == 0) {
-    mbar_init(&xbar[0], kCl);
-    mbar_init(&xbar[1], kCl);
+    mbar_init(&xbar[0], 1);
+    mbar_init(&xbar[1], 1);
     fence_mbar_init();
   }
   __syncthreads();
