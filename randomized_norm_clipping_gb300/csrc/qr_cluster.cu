@@ -44,6 +44,10 @@ constexpr int kR = 16;       // columns (r)
 constexpr int kCl = 8;       // CTAs per sample
 constexpr int kCt = 256;     // threads per CTA
 constexpr int kCw = kCt / 32;
+constexpr int kE = kR * kR;  // entries of a 16 x 16 matrix
+constexpr int kEpt = kCt >= kE ? 1 : kE / kCt;       // of them per thread
+constexpr int kCrows = kR / kCw > 0 ? kR / kCw : 1;  // rows of C = Q^T P per warp
+static_assert((kCt >= kE || kE % kCt == 0) && (kR % kCw == 0 || kCw % kR == 0), "CTA size");
 constexpr int kXch = 256;    // floats per rank slot of the exchange buffer
 
 template <typename TP>
@@ -161,7 +165,7 @@ __global__ void __launch_bounds__(kCt, 1)
   __syncthreads();
   cluster_sync_all();  // every CTA's barriers exist before the first remote arrive
 
-  // rows of this thread: k * (kCl * kCt) + rank * kCt + tid (rank 0 holds rows 0..255)
+  // rows of this thread: k * (kCl * kCt) + rank * kCt + tid (rank 0 holds rows 0..kCt-1)
   auto row_of = [&](int k) { return k * (kCl * kCt) + rank * kCt + tid; };
   float v[RPT][kR];
 #pragma unroll
@@ -303,32 +307,60 @@ __global__ void __launch_bounds__(kCt, 1)
   //   T = 2 (I + X)^-1 = 2 (I - X)(I + X^2)(I + X^4)(I + X^8):
   // six 16 x 16 products, one entry per thread.  Then K = T V_top^T.
   {
-    const int a = tid >> 4, l = tid & 15;
+    // entries e = tid + kCt m (m < kEpt) of each 16 x 16 matrix; threads
+    // beyond the 256 entries only keep step
+    const bool ent = tid < kE;
     float* X = &Tm[0][0];   // X, then its powers
     float* Y = &Km[0][0];   // running product
-    X[tid] = l > a ? 2.f * gram[a][l] : 0.f;
-    Y[tid] = (l == a ? 1.f : 0.f) - (l > a ? 2.f * gram[a][l] : 0.f);  // I - X
+#pragma unroll
+    for (int m = 0; m < kEpt; ++m) {
+      const int e = tid + kCt * m, a = (e >> 4) & (kR - 1), l = e & 15;
+      if (ent) {
+        X[e] = l > a ? 2.f * gram[a][l] : 0.f;
+        Y[e] = (l == a ? 1.f : 0.f) - (l > a ? 2.f * gram[a][l] : 0.f);  // I - X
+      }
+    }
     __syncthreads();
     for (int sq = 0; sq < 3; ++sq) {
       // X <- X^2 (X^2, X^4, X^8), then Y <- Y (I + X)
-      float t = 0.f;
+      float t[kEpt];
 #pragma unroll
-      for (int b = 0; b < kR; ++b) t = fmaf(X[a * kR + b], X[b * kR + l], t);
-      __syncthreads();
-      X[tid] = t;
-      __syncthreads();
-      float u = Y[tid];
+      for (int m = 0; m < kEpt; ++m) {
+        const int e = tid + kCt * m, a = (e >> 4) & (kR - 1), l = e & 15;
+        t[m] = 0.f;
 #pragma unroll
-      for (int b = 0; b < kR; ++b) u = fmaf(Y[a * kR + b], X[b * kR + l], u);
+        for (int b = 0; b < kR; ++b) t[m] = fmaf(X[a * kR + b], X[b * kR + l], t[m]);
+      }
       __syncthreads();
-      Y[tid] = u;
+#pragma unroll
+      for (int m = 0; m < kEpt; ++m)
+        if (ent) X[tid + kCt * m] = t[m];
+      __syncthreads();
+#pragma unroll
+      for (int m = 0; m < kEpt; ++m) {
+        const int e = tid + kCt * m, a = (e >> 4) & (kR - 1), l = e & 15;
+        t[m] = Y[a * kR + l];
+#pragma unroll
+        for (int b = 0; b < kR; ++b) t[m] = fmaf(Y[a * kR + b], X[b * kR + l], t[m]);
+      }
+      __syncthreads();
+#pragma unroll
+      for (int m = 0; m < kEpt; ++m)
+        if (ent) Y[tid + kCt * m] = t[m];
       __syncthreads();
     }
     // T = 2 Y (upper triangular); K[a][l] = sum_{a <= b <= l} T[a][b] V_top[l][b]
-    float t = 0.f;
-    for (int b = a; b <= l; ++b) t = fmaf(2.f * Y[a * kR + b], vtop[l][b], t);
+    float t[kEpt];
+#pragma unroll
+    for (int m = 0; m < kEpt; ++m) {
+      const int e = tid + kCt * m, a = (e >> 4) & (kR - 1), l = e & 15;
+      t[m] = 0.f;
+      for (int b = a; b <= l; ++b) t[m] = fmaf(2.f * Y[a * kR + b], vtop[l][b], t[m]);
+    }
     __syncthreads();
-    Km[a][l] = t;
+#pragma unroll
+    for (int m = 0; m < kEpt; ++m)
+      if (ent) (&Km[0][0])[tid + kCt * m] = t[m];
   }
   __syncthreads();
 
@@ -356,40 +388,51 @@ __global__ void __launch_bounds__(kCt, 1)
   }
   __syncthreads();
 
-  // this CTA's part of C = Q^T P: warp w owns rows a = 2w, 2w + 1 of C
-  {
-    float c[2][kR];
+  // this CTA's part of C = Q^T P: warp w owns rows kCrows w .. of C
+  if (warp * kCrows < kR) {
+    float c[kCrows][kR];
 #pragma unroll
-    for (int x2 = 0; x2 < 2; ++x2)
+    for (int x2 = 0; x2 < kCrows; ++x2)
 #pragma unroll
       for (int l = 0; l < kR; ++l) c[x2][l] = 0.f;
     for (int loc = lane; loc < kCt * RPT; loc += 32) {
-      const float q0 = Qs[loc * 17 + 2 * warp], q1 = Qs[loc * 17 + 2 * warp + 1];
+      float qa[kCrows];
+#pragma unroll
+      for (int x2 = 0; x2 < kCrows; ++x2) qa[x2] = Qs[loc * 17 + kCrows * warp + x2];
 #pragma unroll
       for (int l = 0; l < kR; ++l) {
         const float pl = Ps[loc * 17 + l];
-        c[0][l] = fmaf(q0, pl, c[0][l]);
-        c[1][l] = fmaf(q1, pl, c[1][l]);
+#pragma unroll
+        for (int x2 = 0; x2 < kCrows; ++x2) c[x2][l] = fmaf(qa[x2], pl, c[x2][l]);
       }
     }
 #pragma unroll
-    for (int x2 = 0; x2 < 2; ++x2) {
+    for (int x2 = 0; x2 < kCrows; ++x2) {
       int idx;
       const float w = warp_scatter16<false>(c[x2], lane, idx);
-      if ((lane & 1) == 0) Cm[(2 * warp + x2) * kR + idx] = w;
+      if ((lane & 1) == 0) Cm[(kCrows * warp + x2) * kR + idx] = w;
     }
   }
   __syncthreads();
-  // round 17: all-gather the 256 partials; every thread sums its entry
-  xbuf[(1 + kR) & 1][rank][tid] = Cm[tid];
+  // round 17: all-gather the 256 partials; every thread sums its entries
+#pragma unroll
+  for (int m = 0; m < kEpt; ++m)
+    if (tid < kE) xbuf[(1 + kR) & 1][rank][tid + kCt * m] = Cm[tid + kCt * m];
   __syncthreads();
-  if (warp == 0) xch_send(x, 1 + kR, kR * kR, lane);
+  if (warp == 0) xch_send(x, 1 + kR, kE, lane);
   if (!xch_wait(x, 1 + kR)) ok = false;
   {
-    float t = 0.f;
-    for (int r = 0; r < kCl; ++r) t += xbuf[(1 + kR) & 1][r][tid];
+    float t[kEpt];
+#pragma unroll
+    for (int m = 0; m < kEpt; ++m) {
+      t[m] = 0.f;
+      if (tid < kE)
+        for (int r = 0; r < kCl; ++r) t[m] += xbuf[(1 + kR) & 1][r][tid + kCt * m];
+    }
     __syncthreads();  // everyone has read this CTA's partial of Cm
-    Cm[tid] = t;
+#pragma unroll
+    for (int m = 0; m < kEpt; ++m)
+      if (tid < kE) Cm[tid + kCt * m] = t[m];
   }
   __syncthreads();
 
@@ -456,6 +499,10 @@ cudaError_t launch_rpt(const float* M, int64_t B, int64_t p, const void* P, void
   if (dev < 0 || dev >= kMaxDev || !done[dev].load(std::memory_order_acquire)) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
+    if (kCl > 8) {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      if (e != cudaSuccess) return e;
+    }
     if (dev >= 0 && dev < kMaxDev) done[dev].store(1, std::memory_order_release);
   }
   cudaLaunchConfig_t cfg = {};
