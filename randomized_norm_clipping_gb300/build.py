@@ -20,7 +20,7 @@ BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_NAME = "libdprc.so"
 LIB_PATH = os.path.join(PKG_DIR, LIB_NAME)
 
-SOURCES = ["api.cu", "tc_proj.cu", "tc_exact.cu", "tc_hutch.cu", "simt.cu", "qr.cu", "qr_cluster.cu", "noise.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "tc_proj.cu", "tc_exact.cu", "tc_narrow.cu", "tc_hutch.cu", "simt.cu", "qr.cu", "qr_cluster.cu", "noise.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

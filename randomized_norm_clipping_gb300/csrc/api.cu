@@ -254,6 +254,14 @@ ExactPlan plan_exact(dprc_dtype dt, int64_t B, int64_t T, int64_t d, int64_t p, 
     e.per_sample = cdiv(T, 32) * cdiv(T, 32);
     return e;
   }
+  if (form != DPRC_EXACT_GHOST && form != DPRC_EXACT_GHOST_N128 &&
+      form != DPRC_EXACT_GHOST_N256 && narrow_supported(dt, d, p)) {
+    // one width <= 64: the direct form in one pass, no tile padding (and
+    // always less work than the ghost form's T^2 (d + p) when T >= 128)
+    e.kind = ExactPlan::kNarrowTc;
+    e.per_sample = narrow_partials(1, d, p);
+    return e;
+  }
   const int sms = device_sm_count() > 0 ? device_sm_count() : 1;
   const double cd = exact_cost_direct(B, T, d, p, sms);
   double cg = -1.0;
@@ -285,6 +293,7 @@ size_t plan_exact_bytes(dprc_dtype dt, int64_t B, int64_t T, int64_t d, int64_t 
   int64_t most = 0;
   if (exact_direct_tc(dt, d, p)) {
     most = fgc_partials(1, d, p);
+    if (narrow_supported(dt, d, p)) most = std::max(most, narrow_partials(1, d, p));
     if (T <= kGhostTcMaxT) most = std::max(most, ghost_partials(1, T, 1));
   } else {
     most = cdiv(T, 32) * cdiv(T, 32);
@@ -344,9 +353,17 @@ dprc_status check_common(dprc_dtype dt, int64_t B, int64_t T, int64_t d, int64_t
   return DPRC_OK;
 }
 
+// Narrow layers keep one fp32 partial per tile after the counter block.
+size_t narrow_part_off(int64_t B) { return align_up(ctrl_bytes(B), 1024); }
+size_t narrow_ws(int64_t B, int64_t d, int64_t p) {
+  return narrow_part_off(B) + align_up(static_cast<size_t>(narrow_partials(B, d, p)) * 4, 1024);
+}
+
 size_t hutch_ws(dprc_dtype dt, int64_t B, int64_t T, int64_t d, int64_t p, int64_t k) {
-  return tc_path_supported(dt, B, T, d, p, k, false) ? plan_tc(DPRC_OP_HUTCH, B, T, d, p, k).total
-                                               : plan_simt(DPRC_OP_HUTCH, B, T, d, p, k).total;
+  const size_t base = tc_path_supported(dt, B, T, d, p, k, false)
+                          ? plan_tc(DPRC_OP_HUTCH, B, T, d, p, k).total
+                          : plan_simt(DPRC_OP_HUTCH, B, T, d, p, k).total;
+  return narrow_proj_supported(dt, d, p, k) ? std::max(base, narrow_ws(B, d, p)) : base;
 }
 
 size_t hutchpp_ws(dprc_dtype dt, int64_t B, int64_t T, int64_t d, int64_t p, int64_t r) {
@@ -462,6 +479,15 @@ dprc_status dprc_norm_hutch(const void* A, const void* G, const void* P, dprc_dt
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   char* w = static_cast<char*>(ws);
   mark(0, s);
+  if (narrow_proj_supported(dtype, d, p, k)) {
+    // p <= 64: X_i = A_i^T G_i in one pass, each row of it times P in the epilogue
+    const cudaError_t e =
+        launch_narrow_hutch(A, G, P, B, T, d, p, k, 1.0f, 0, 0,
+                            reinterpret_cast<float*>(w + narrow_part_off(B)), n, accumulate, s);
+    mark(1, s);
+    mark(2, s);
+    return cuda_status(e);
+  }
   if (tc_path_supported(dtype, B, T, d, p, k, false) && fused_hutch_supported(k)) {
     // one launch: sketch and projection as two phases of one kernel
     const TcPlan t = plan_tc(DPRC_OP_HUTCH, B, T, d, p, k);
@@ -494,6 +520,14 @@ dprc_status dprc_norm_hutch_pm1(const void* A, const void* G, uint64_t seed, uin
   if (!device_ok()) return DPRC_ERR_DEVICE;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   char* w = static_cast<char*>(ws);
+  if (narrow_proj_supported(dtype, d, p, k)) {
+    // p <= 64: X_i = A_i^T G_i in one pass, then (1/k) ||X_i S||^2 with the
+    // signs generated in the kernel's shared memory
+    return cuda_status(launch_narrow_hutch(A, G, nullptr, B, T, d, p, k,
+                                           1.0f / static_cast<float>(k), seed, step,
+                                           reinterpret_cast<float*>(w + narrow_part_off(B)), n,
+                                           accumulate, s));
+  }
   if (tc_path_supported(dtype, B, T, d, p, k, false) && fused_hutch_supported(k)) {
     // the signs are generated inside the kernel: S never exists in memory
     const TcPlan t = plan_tc(DPRC_OP_HUTCH, B, T, d, p, k);
@@ -565,6 +599,7 @@ int dprc_norm_hutch_launches(dprc_dtype dtype, int64_t B, int64_t T, int64_t d, 
                              int64_t k) {
   if (check_common(dtype, B, T, d, p) != DPRC_OK || k < 1 || k > 256) return 0;
   if (!device_ok()) return 0;
+  if (narrow_proj_supported(dtype, d, p, k)) return 2;
   if (!tc_path_supported(dtype, B, T, d, p, k, false)) return 3;
   return fused_hutch_planned(B, T, d, p, k) ? 1 : 2;
 }
@@ -680,6 +715,9 @@ dprc_status dprc_exact_norm_form(const void* A, const void* G, dprc_dtype dtype,
       // the work queue's counters sit at the front of the zeroed counter block
       err = launch_tc_exact_ghost(A, G, B, T, d, p, e.W, ws, partials, n, accumulate, s);
       break;
+    case ExactPlan::kNarrowTc:
+      err = launch_narrow_norm(A, G, B, T, d, p, partials, n, accumulate, s);
+      break;
     default:
       err = launch_exact_ghost(A, G, dtype, B, T, d, p, partials, n, accumulate, s);
   }
@@ -700,7 +738,8 @@ int dprc_exact_norm_plan(dprc_dtype dtype, int64_t B, int64_t T, int64_t d, int6
   if (!device_ok()) return 0;
   const ExactPlan e = plan_exact(dtype, B, T, d, p, form);
   switch (e.kind) {
-    case ExactPlan::kDirectTc: return DPRC_EXACT_DIRECT;
+    case ExactPlan::kDirectTc:
+    case ExactPlan::kNarrowTc: return DPRC_EXACT_DIRECT;
     case ExactPlan::kGhostTc: return e.W == 1 ? DPRC_EXACT_GHOST_N128 : DPRC_EXACT_GHOST_N256;
     case ExactPlan::kGhostSimt: return DPRC_EXACT_GHOST;
     default: return 0;
@@ -750,7 +789,8 @@ dprc_status dprc_device_error(int32_t* out, int reset) {
   cudaError_t (*const readers[])(int32_t*, bool) = {read_device_error_proj,
                                                      read_device_error_hutch,
                                                      read_device_error_exact,
-                                                     read_device_error_qr};
+                                                     read_device_error_qr,
+                                                     read_device_error_narrow};
   int32_t first = 0;
   for (auto rd : readers) {
     int32_t v = 0;

@@ -85,7 +85,7 @@ TcPlan plan_tc(dprc_op op, int64_t B, int64_t T, int64_t d, int64_t p, int64_t k
 SimtPlan plan_simt(dprc_op op, int64_t B, int64_t T, int64_t d, int64_t p, int64_t k);
 // Which kernel an exact-norm call runs (form: dprc_exact_form).
 struct ExactPlan {
-  enum Kind { kNone = 0, kDirectTc, kGhostTc, kGhostSimt };
+  enum Kind { kNone = 0, kDirectTc, kGhostTc, kGhostSimt, kNarrowTc };
   Kind kind = kNone;
   int W = 0;               // span width of the tensor-core ghost form
   int64_t per_sample = 0;  // partials per sample
@@ -201,6 +201,23 @@ int64_t ghost_partials(int64_t B, int64_t T, int W);
 cudaError_t launch_tc_exact_ghost(const void* A, const void* G, int64_t B, int64_t T, int64_t d,
                                   int64_t p, int W, void* counters, float* partials,
                                   float* n_out, int accumulate, cudaStream_t s);
+// Narrow layers (bf16, d and p multiples of 8, min(d, p) <= 64): the gradient
+// X_i = A_i^T G_i formed tile by tile in one streaming tensor-core pass.
+// launch_narrow_norm: n_out (+)= ||X_i||^2; launch_narrow_hutch (p <= 64,
+// 1 <= k <= 256): n_out (+)= scale ||X_i P||^2 with P [p][k] bf16, or with the
+// +-1 signs of (seed, step) when P is null.  Both use narrow_partials(B, d, p)
+// floats of partials.
+bool narrow_supported(dprc_dtype dt, int64_t d, int64_t p);
+bool narrow_proj_supported(dprc_dtype dt, int64_t d, int64_t p, int64_t k);
+int64_t narrow_partials(int64_t B, int64_t d, int64_t p);
+cudaError_t read_device_error_narrow(int32_t* out, bool reset);
+cudaError_t launch_narrow_norm(const void* A, const void* G, int64_t B, int64_t T, int64_t d,
+                               int64_t p, float* partials, float* n_out, int accumulate,
+                               cudaStream_t s);
+cudaError_t launch_narrow_hutch(const void* A, const void* G, const void* P, int64_t B,
+                                int64_t T, int64_t d, int64_t p, int64_t k, float scale,
+                                uint64_t seed, uint64_t step, float* partials, float* n_out,
+                                int accumulate, cudaStream_t s);
 // n_out[i] (+)= sum of partials[i * per_sample .. (i + 1) * per_sample), fixed order.
 cudaError_t launch_partials_finish(const float* partials, int64_t B, int64_t per_sample,
                                    float* n_out, int accumulate, cudaStream_t s);

@@ -1,0 +1,414 @@
+// Narrow layers (one width <= 64, e.g. the two maps of a low-rank adapter):
+// the per-sample weight gradient itself is small, so it is formed once.
+//
+// "Efficient DP-SGD for LLMs with Randomized Clipping" (papernotes.org,
+// "Key design > Hutchinson") sketches the d x p gradient A_i^T G_i with a
+// p x k projection because forming it costs O(T d p) and its memory is d p
+// per sample.  When min(d, p) <= 64 (adapters of rank 8..64: the notes run
+// LoRA fine-tuning beside full fine-tuning, "Experiments") that product is no
+// more work than the sketch, and X_i = A_i^T G_i arrives tile by tile in
+// on-chip memory.  One streaming pass over A and G then gives
+//
+//   exact norm   n_i = ||X_i||_F^2                   (any orientation)
+//   Hutchinson   n_i = scale ||X_i P||_F^2, p <= 64   (each row of X_i times P)
+//
+// the second equal to the sketch path's ||A_i^T (G_i P)||^2 up to rounding
+// (the product is associative, and rows of X_i P depend on rows of X_i only).
+// For the +-1 projection P = S, its p k signs are generated from the Philox
+// stream into shared memory; S never exists in global memory.
+//
+// tc_narrow_kernel: tiles of 128 columns of the wide operand (the one whose
+// width is > 64, or A when both are narrow) against all columns of the narrow
+// operand, K = T in 64-token stages, accumulated in fp32 TMEM by tcgen05.mma.
+// Both operands are MN-major, read as stored: the wide tile as two 64-column
+// boxes with a 128-byte swizzle, the narrow one as one box N columns wide
+// (N = 16, 32 or 64, the narrow width rounded up; the TMA fills the columns
+// past it with zeros) with a 2N-byte swizzle.  A stage is 18 to 24 KB, so
+// eight of them keep 144 to 192 KB per SM in flight.  The accumulator is
+// double buffered.  The epilogue (one TMEM lane, i.e. one row of the tile, per
+// thread) squares and sums the row, or first multiplies it by P (staged in
+// shared memory in bf16), and writes one partial per tile; a finishing kernel
+// sums a sample's partials in index order.
+
+#include <atomic>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace dprc {
+
+namespace {
+
+constexpr int kNwM = 128;                    // wide columns per tile (MMA M)
+constexpr int kNwK = 64;                     // tokens per stage
+constexpr int kNwStages = 8;
+constexpr int kNwBox = kNwK * 64 * 2;        // 64 tokens x 64 wide columns, 8 KB
+constexpr int kNwWide = (kNwM / 64) * kNwBox;  // 16 KB
+
+template <int N>
+struct NwCfg {
+  static constexpr int kNarrow = kNwK * N * 2;       // 64 tokens x N narrow columns
+  static constexpr int kStage = kNwWide + kNarrow;   // 18, 20 or 24 KB
+  static constexpr int kTmemCols = 2 * N < 32 ? 32 : 2 * N;
+  static constexpr int kCtrl = 256;
+  static constexpr int kBase = 1024 + kNwStages * kStage + kCtrl;
+  // P (bf16, at most 64 x 256) in shared memory after the barriers
+  static constexpr int smem(int proj_bytes) { return kBase + proj_bytes; }
+  static_assert(kStage % 1024 == 0, "stages keep the 1024-byte alignment of swizzled tiles");
+};
+
+enum NwMode { kNwNorm = 0, kNwProj = 1 };
+
+struct NwArgs {
+  int T;
+  int wide, narrow;   // widths of the wide and narrow operands
+  int mt;             // wide tiles per sample
+  long long ntiles;   // B * mt
+  float* partials;    // [ntiles]
+  // projection mode (the narrow operand is G, narrow = p):
+  const void* P;      // [p][k] in the input type, or null for the +-1 signs
+  int k, kp;          // kp: k rounded up to a multiple of 16 (shared-memory rows)
+  float scale;
+  uint64_t seed, step;  // the signs' Philox stream when P is null
+};
+
+template <int N, int MODE, typename TP>
+__global__ void __launch_bounds__(192, 1)
+    tc_narrow_kernel(const __grid_constant__ CUtensorMap map_w,
+                     const __grid_constant__ CUtensorMap map_n, const NwArgs a) {
+  using Cfg = NwCfg<N>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ float s_red[4];
+
+  uint8_t* ring = align_1024(smem_raw);
+  TP* Ps = reinterpret_cast<TP*>(ring + kNwStages * Cfg::kStage + Cfg::kCtrl);
+  uint64_t* full = reinterpret_cast<uint64_t*>(ring + kNwStages * Cfg::kStage);
+  uint64_t* empty = full + kNwStages;
+  uint64_t* accf = empty + kNwStages;  // [2]
+  uint64_t* acce = accf + 2;           // [2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acce + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nu = (a.T + kNwK - 1) / kNwK;  // stages per tile
+  const long long my_tiles =
+      a.ntiles > blockIdx.x ? (a.ntiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kNwStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&accf[b], 1);
+      mbar_init(&acce[b], 4);
+    }
+    fence_mbar_init();
+    *abort_flag = 0;
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&map_w);
+    tma_prefetch_desc(&map_n);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, Cfg::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0 && my_tiles > 0) {
+      long long it = 0;
+      bool ok = true;
+      for (long long j = 0; j < my_tiles && ok; ++j) {
+        const long long tile = blockIdx.x + j * gridDim.x;
+        const int i = static_cast<int>(tile / a.mt);
+        const int m = static_cast<int>(tile - static_cast<long long>(i) * a.mt);
+        for (int u = 0; u < nu; ++u, ++it) {
+          const int s = static_cast<int>(it % kNwStages);
+          const uint32_t ph = static_cast<uint32_t>(it / kNwStages) & 1;
+          if (!mbar_wait(&empty[s], ph ^ 1, DPRC_DEVERR_PIPE_EMPTY)) {
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+          uint8_t* st = ring + s * Cfg::kStage;
+          mbar_arrive_expect_tx(&full[s], Cfg::kStage);
+#pragma unroll
+          for (int h = 0; h < kNwM / 64; ++h)
+            tma_load_3d(st + h * kNwBox, &map_w, &full[s], m * kNwM + h * 64, u * kNwK, i);
+          tma_load_3d(st + kNwWide, &map_n, &full[s], 0, u * kNwK, i);
+        }
+      }
+      // let the copies this thread issued land before the CTA can exit
+      for (long long k = it - 1; k >= 0 && k >= it - kNwStages; --k)
+        mbar_wait(&full[k % kNwStages], (k / kNwStages) & 1, DPRC_DEVERR_PIPE_FULL);
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && my_tiles > 0) {
+      constexpr uint32_t idesc = make_idesc_bf16(kNwM, N, true, true);
+      constexpr uint32_t nswz = swz_code_for_bytes(2 * N);
+      long long it = 0;
+      bool ok = true;
+      for (long long j = 0; j < my_tiles && ok; ++j) {
+        const int abuf = static_cast<int>(j & 1);
+        if (!mbar_wait(&acce[abuf], static_cast<uint32_t>((j >> 1) & 1) ^ 1, DPRC_DEVERR_ACCUM)) {
+          *abort_flag = 1;
+          break;
+        }
+        tc_fence_after();
+        for (int u = 0; u < nu; ++u, ++it) {
+          const int s = static_cast<int>(it % kNwStages);
+          const uint32_t ph = static_cast<uint32_t>(it / kNwStages) & 1;
+          if (!mbar_wait(&full[s], ph, DPRC_DEVERR_PIPE_FULL)) {
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t wa = smem_u32(ring + s * Cfg::kStage);
+          const uint32_t na = wa + kNwWide;
+#pragma unroll
+          for (int kk = 0; kk < kNwK / 16; ++kk) {
+            // wide tile: MN-major, 128-byte swizzle; a K = 16 step is 16 token
+            // rows of 128 B, 8-row atoms 1 KB apart (SBO), the two 64-column
+            // atoms one box apart (LBO)
+            const uint64_t ad = make_sdesc(wa + kk * 2048, kNwBox, 1024, kSwz128);
+            // narrow tile: MN-major, one swizzle atom wide (2N bytes); a K = 16
+            // step is 16 rows of 2N bytes, 8-row atoms 16N bytes apart
+            const uint64_t bd = make_sdesc(na + kk * 32 * N, 16, 16 * N, nswz);
+            umma_bf16(tmem + abuf * N, ad, bd, idesc, (u == 0 && kk == 0) ? 0u : 1u);
+          }
+          umma_commit(&empty[s]);
+        }
+        if (ok) umma_commit(&accf[abuf]);
+      }
+    }
+  } else {
+    // ---------------- epilogue warps 2..5 ----------------
+    const int ew = warp - 2;
+    const int q = warp & 3;  // TMEM lane quadrant this warp may read
+    const int et = threadIdx.x - 64;
+    if (MODE == kNwProj) {
+      // P (or the +-1 signs) into shared memory, once
+      // rows of kp = k rounded up to 16 columns, zeros past k
+      const int pk = a.narrow * a.k;
+      for (int e = et; e < a.narrow * a.kp; e += 128) Ps[e] = static_cast<TP>(0.f);
+      named_bar_sync(1, 128);
+      if (a.P != nullptr) {
+        const TP* P = static_cast<const TP*>(a.P);
+        for (int e = et; e < pk; e += 128) Ps[(e / a.k) * a.kp + e % a.k] = P[e];
+      } else {
+        // entry e of S: bit (e & 31) of word ((e >> 5) & 3) of block e >> 7
+        const RoundKeys rk = round_keys(a.seed);
+        for (int j = et; j * 128 < pk; j += 128) {
+          const uint4 w = philox_block(static_cast<uint64_t>(j), a.step, rk);
+          const uint32_t words[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+          for (int wq = 0; wq < 4; ++wq)
+            for (int b = 0; b < 32; ++b) {
+              const int e = j * 128 + wq * 32 + b;
+              if (e < pk)
+                Ps[(e / a.k) * a.kp + e % a.k] =
+                    static_cast<TP>(((words[wq] >> b) & 1u) ? -1.0f : 1.0f);
+            }
+        }
+      }
+      named_bar_sync(1, 128);
+    }
+    bool ok = true;
+    for (long long j = 0; j < my_tiles; ++j) {
+      const long long tile = blockIdx.x + j * gridDim.x;
+      const int abuf = static_cast<int>(j & 1);
+      bool live = ok && mbar_wait(&accf[abuf], static_cast<uint32_t>((j >> 1) & 1),
+                                  DPRC_DEVERR_ACCUM) &&
+                  *abort_flag == 0;
+      live = __all_sync(0xffffffffu, live);  // keep the warp's TMEM loads convergent
+      if (!live) ok = false;
+      tc_fence_after();
+      float v[N];
+      if (live) {
+        const uint32_t tb = tmem + (static_cast<uint32_t>(q * 32) << 16) + abuf * N;
+#pragma unroll
+        for (int c0 = 0; c0 < N; c0 += 16) {
+          float t[16];
+          tmem_ld_16cols(tb + c0, t);
+#pragma unroll
+          for (int c = 0; c < 16; ++c) v[c0 + c] = t[c];
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acce[abuf]);
+      float sq = 0.f;
+      if (live) {
+        if (MODE == kNwNorm) {
+          float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+          for (int c = 0; c < N; c += 2) {
+            s0 = fmaf(v[c], v[c], s0);
+            s1 = fmaf(v[c + 1], v[c + 1], s1);
+          }
+          sq = s0 + s1;
+        } else {
+          // ||x P||^2 for this row x (columns past p are zero), 16 columns of
+          // x P at a time; every thread reads the same P entries (broadcast),
+          // 8 bf16 per 16-byte load (P's rows are padded to kp columns)
+          for (int c0 = 0; c0 < a.k; c0 += 16) {
+            float y[16];
+#pragma unroll
+            for (int c = 0; c < 16; ++c) y[c] = 0.f;
+#pragma unroll
+            for (int b = 0; b < N; ++b) {
+              if (b < a.narrow) {
+                const uint4* pr = reinterpret_cast<const uint4*>(Ps + b * a.kp + c0);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                  const uint4 w = pr[h];
+                  const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                  for (int c2 = 0; c2 < 4; ++c2) {
+                    const float lo = __uint_as_float(ws[c2] << 16);
+                    const float hi = __uint_as_float(ws[c2] & 0xFFFF0000u);
+                    y[8 * h + 2 * c2] = fmaf(v[b], lo, y[8 * h + 2 * c2]);
+                    y[8 * h + 2 * c2 + 1] = fmaf(v[b], hi, y[8 * h + 2 * c2 + 1]);
+                  }
+                }
+              }
+            }
+#pragma unroll
+            for (int c = 0; c < 16; ++c) sq = fmaf(y[c], y[c], sq);
+          }
+          sq *= a.scale;
+        }
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, off);
+      if (lane == 0) s_red[ew] = sq;
+      named_bar_sync(1, 128);
+      if (ew == 0 && lane == 0 && ok)
+        a.partials[tile] = (s_red[0] + s_red[1]) + (s_red[2] + s_red[3]);
+      named_bar_sync(1, 128);
+    }
+  }
+
+  __syncwarp();  // reconverge each warp before the CTA barrier
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, Cfg::kTmemCols);
+  }
+}
+
+template <int N, int MODE, typename TP>
+cudaError_t launch_n(const CUtensorMap& mw, const CUtensorMap& mn, const NwArgs& a,
+                     int proj_bytes, cudaStream_t s) {
+  auto kern = tc_narrow_kernel<N, MODE, TP>;
+  constexpr int kMaxDev = 64;
+  static std::atomic<int> done[kMaxDev];  // largest shared-memory size set so far
+  const int smem = NwCfg<N>::smem(proj_bytes);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDev || done[dev].load(std::memory_order_acquire) < smem) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < kMaxDev) done[dev].store(smem, std::memory_order_release);
+  }
+  const long long grid = a.ntiles < device_sm_count() ? a.ntiles : device_sm_count();
+  kern<<<static_cast<unsigned>(grid), 192, smem, s>>>(mw, mn, a);
+  return cudaGetLastError();
+}
+
+template <int MODE, typename TP>
+cudaError_t launch_mode(int N, const CUtensorMap& mw, const CUtensorMap& mn, const NwArgs& a,
+                        int proj_bytes, cudaStream_t s) {
+  return N == 16 ? launch_n<16, MODE, TP>(mw, mn, a, proj_bytes, s)
+                 : (N == 32 ? launch_n<32, MODE, TP>(mw, mn, a, proj_bytes, s)
+                            : launch_n<64, MODE, TP>(mw, mn, a, proj_bytes, s));
+}
+
+// Operands of X = A^T G as (wide, narrow): A is the wide one unless only d
+// is narrow.
+bool narrow_setup(const void* A, const void* G, int64_t B, int64_t T, int64_t d, int64_t p,
+                  CUtensorMap& mw, CUtensorMap& mn, NwArgs& a, int& N) {
+  const bool swap = d <= 64 && p > 64;
+  const void* W = swap ? G : A;
+  const void* Nr = swap ? A : G;
+  const int64_t wide = swap ? p : d, narrow = swap ? d : p;
+  N = narrow <= 16 ? 16 : (narrow <= 32 ? 32 : 64);
+  if (!make_tmap_3d_bf16(&mw, W, wide, T, B, wide, T * wide, 64, kNwK, 128)) return false;
+  if (!make_tmap_3d_bf16(&mn, Nr, narrow, T, B, narrow, T * narrow, N, kNwK, 2 * N))
+    return false;
+  a.T = static_cast<int>(T);
+  a.wide = static_cast<int>(wide);
+  a.narrow = static_cast<int>(narrow);
+  a.mt = static_cast<int>((wide + kNwM - 1) / kNwM);
+  a.ntiles = B * a.mt;
+  a.partials = nullptr;
+  a.P = nullptr;
+  a.k = a.kp = 0;
+  a.scale = 1.f;
+  a.seed = a.step = 0;
+  return true;
+}
+
+}  // namespace
+
+cudaError_t read_device_error_narrow(int32_t* out, bool reset) {
+  return read_tu_device_error(out, reset);
+}
+
+bool narrow_supported(dprc_dtype dt, int64_t d, int64_t p) {
+  return dt == DPRC_BF16 && d % 8 == 0 && p % 8 == 0 && (d <= 64 || p <= 64);
+}
+
+bool narrow_proj_supported(dprc_dtype dt, int64_t d, int64_t p, int64_t k) {
+  return dt == DPRC_BF16 && d % 8 == 0 && p % 8 == 0 && p <= 64 && k >= 1 && k <= 256;
+}
+
+int64_t narrow_partials(int64_t B, int64_t d, int64_t p) {
+  const int64_t wide = d <= 64 && p > 64 ? p : d;
+  return B * ((wide + kNwM - 1) / kNwM);
+}
+
+cudaError_t launch_narrow_norm(const void* A, const void* G, int64_t B, int64_t T, int64_t d,
+                               int64_t p, float* partials, float* n_out, int accumulate,
+                               cudaStream_t s) {
+  CUtensorMap mw, mn;
+  NwArgs a;
+  int N = 16;
+  if (!narrow_setup(A, G, B, T, d, p, mw, mn, a, N)) return cudaErrorInvalidValue;
+  a.partials = partials;
+  const cudaError_t e = launch_mode<kNwNorm, float>(N, mw, mn, a, 0, s);
+  if (e != cudaSuccess) return e;
+  return launch_partials_finish(partials, B, a.mt, n_out, accumulate, s);
+}
+
+cudaError_t launch_narrow_hutch(const void* A, const void* G, const void* P, int64_t B,
+                                int64_t T, int64_t d, int64_t p, int64_t k, float scale,
+                                uint64_t seed, uint64_t step, float* partials, float* n_out,
+                                int accumulate, cudaStream_t s) {
+  if (p > 64 || k < 1 || k > 256) return cudaErrorInvalidValue;
+  CUtensorMap mw, mn;
+  NwArgs a;
+  int N = 16;
+  if (!narrow_setup(A, G, B, T, d, p, mw, mn, a, N)) return cudaErrorInvalidValue;
+  a.partials = partials;
+  a.P = P;
+  a.k = static_cast<int>(k);
+  a.kp = static_cast<int>((k + 15) / 16 * 16);
+  a.scale = scale;
+  a.seed = seed;
+  a.step = step;
+  const int proj_bytes = static_cast<int>(p * a.kp * 2);
+  const cudaError_t e = launch_mode<kNwProj, __nv_bfloat16>(N, mw, mn, a, proj_bytes, s);
+  if (e != cudaSuccess) return e;
+  return launch_partials_finish(partials, B, a.mt, n_out, accumulate, s);
+}
+
+}  // namespace dprc

@@ -89,6 +89,52 @@ def test_hutch_bf16_matches_oracle(B, T, d, p, k):
     assert _relerr(n.cpu(), ref) < RTOL
 
 
+# Narrow layers (a width <= 64): X_i = A_i^T G_i in one tensor-core pass; the
+# exact norm for both orientations (the wide operand A or G), the estimate
+# ||X_i P||^2 from the rows of X_i when p <= 64 (d-narrow maps take the
+# sketch path).  Both widths narrow, narrow widths padded to 16, 32 and 64
+# columns, ragged T, k from 8 to 256 (P up to 64 x 256 in shared memory).
+NARROW_SHAPES = [
+    (3, 1000, 2048, 16, 32),   # adapter down map: p narrow
+    (3, 1000, 16, 2048, 32),   # adapter up map: d narrow, G is the wide operand
+    (2, 1, 512, 8, 16),        # one token
+    (2, 129, 24, 1000, 8),     # narrow width 24 (padded to 32), ragged wide width
+    (2, 4097, 40, 136, 64),    # narrow width 40 (padded to 64), T one past a tile
+    (4, 300, 64, 64, 256),     # both narrow; P 64 x 256 in shared memory
+    (1, 640, 32, 16, 128),     # both narrow, d > p
+    (5, 257, 1024, 64, 32),
+]
+
+
+@pytest.mark.parametrize("B,T,d,p,k", NARROW_SHAPES)
+def test_hutch_narrow_matches_oracle(B, T, d, p, k):
+    A, G, P = _hutch_case(B, T, d, p, k, torch.bfloat16, seed=B * 7 + T + d)
+    n = torch.full((B,), 0.25, device=DEV)
+    rnc.dprc_norm_hutch(A.to(DEV), G.to(DEV), P.to(DEV), n, accumulate=True)
+    ref = oracle.hutch_norm(to_f64(A), to_f64(G), to_f64(P))
+    assert _relerr(n.cpu(), ref + 0.25) < RTOL
+    e = torch.zeros(B, device=DEV)
+    rnc.dprc_exact_norm(A.to(DEV), G.to(DEV), e)
+    assert _relerr(e.cpu(), oracle.exact_norm(to_f64(A), to_f64(G))) < RTOL
+    assert rnc.dprc_exact_norm_plan(rnc.DPRC_BF16, B, T, d, p) == rnc.DPRC_EXACT_DIRECT
+
+
+def test_hutch_narrow_identity_projection_is_exact_and_repeats():
+    # P = I_p turns ||X P||^2 into ||X||^2: the two narrow outputs agree with
+    # each other and with the oracle's exact norm; a rerun is bitwise equal
+    B, T, d, p = 3, 700, 1536, 32
+    A, G, _ = _hutch_case(B, T, d, p, 32, torch.bfloat16, seed=91)
+    Ad, Gd = A.to(DEV), G.to(DEV)
+    eye = torch.eye(p, dtype=torch.bfloat16, device=DEV)
+    n1, n2, e = (torch.zeros(B, device=DEV) for _ in range(3))
+    rnc.dprc_norm_hutch(Ad, Gd, eye, n1)
+    rnc.dprc_norm_hutch(Ad, Gd, eye, n2)
+    rnc.dprc_exact_norm(Ad, Gd, e)
+    assert torch.equal(n1, n2)
+    ref = oracle.exact_norm(to_f64(A), to_f64(G))
+    assert _relerr(n1.cpu(), ref) < RTOL and _relerr(e.cpu(), ref) < RTOL
+
+
 @pytest.mark.parametrize("B,T,d,p,k", [(4, 128, 64, 64, 8), (2, 77, 30, 17, 5), (3, 64, 64, 64, 32)])
 def test_hutch_fp32_matches_oracle(B, T, d, p, k):
     A, G, P = _hutch_case(B, T, d, p, k, torch.float32, seed=17 + T)
@@ -153,6 +199,10 @@ def test_launch_count_query_matches_the_path():
     # fp32 or widths that are not multiples of 8: the CUDA-core path
     assert rnc.dprc_norm_hutch_launches(DPRC_F32, 4, 128, 64, 64, 8) == 3
     assert rnc.dprc_norm_hutch_launches(DPRC_BF16, 2, 100, 97, 64, 32) == 3
+    # p <= 64: X = A^T G formed in one pass with its rows times P, then the
+    # per-sample sum of the tile partials
+    assert rnc.dprc_norm_hutch_launches(DPRC_BF16, 8, 4096, 2048, 16, 32) == 2
+    assert rnc.dprc_norm_hutch_launches(DPRC_BF16, 8, 4096, 64, 48, 256) == 2
 
 
 def test_hutch_identity_projection_gives_exact_norm():
@@ -481,7 +531,8 @@ def test_hutch_layers_repeats_bitwise_and_reuses_its_workspace():
     (2, 200, 256, 256, 64, torch.bfloat16),   # k = 64: signs in the workspace, two kernels
     (3, 77, 30, 17, 8, torch.float32),        # fp32: CUDA cores
     (2, 90, 37, 45, 24, torch.bfloat16),      # odd widths: CUDA cores
-    (4, 1000, 2048, 16, 32, torch.bfloat16),  # LoRA down, in the kernel
+    (4, 1000, 2048, 16, 32, torch.bfloat16),  # adapter down map: X = A^T G, then X S
+    (4, 1000, 16, 2048, 32, torch.bfloat16),  # adapter up map, d narrow
 ])
 def test_pm1_projection_matches_oracle(B, T, d, p, k, dtype):
     A = _rand((B, T, d), 500 + T, dtype)
