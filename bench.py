@@ -3,7 +3,9 @@
 One step = one pass of the hot path over one batch of the headline workload
 (Llama-3.2-1B q_proj shape: B = 8 per GPU, T = 4096, d = p = 2048, k = 32,
 bf16): the Hutchinson estimate n_hat_i = ||A_i^T (G_i P)||_F^2 (sketch and
-projection kernels) followed by the clip factors min(1, C / sqrt(n_i)).
+projection as two phases of one launch) and the clip factors
+min(1, C / sqrt(n_i)) (in that launch's finishing step), one call of
+dprc_norm_hutch_clip.
 
 Metric: norm-estimation tokens/s (B*T per second per layer), whole job over
 all ranks, plus the HBM roofline fraction of the dominant kernel.
@@ -232,13 +234,13 @@ def run_native(args, rank, ws, local):
     stream = torch.cuda.current_stream(device)
 
     def step():
-        rnc.dprc_norm_hutch(A, G, P, n, accumulate=False, ws=wsbuf)
-        rnc.dprc_clip_factors(n, wk.C, c)
+        # the layer's norms and the clip factors: one call
+        rnc.dprc_norm_hutch_clip(A, G, P, n, wk.C, c, accumulate=False, ws=wsbuf)
 
-    # kernels per step: the norm call (one fused launch, or sketch + projection)
-    # and the clip factors
+    # kernels per step: one fused launch (the clip factors in its finishing
+    # step), or sketch + projection + clip
     norm_launches = rnc.dprc_norm_hutch_launches(rnc.DPRC_BF16, B, T, d, p, k)
-    launches_per_step = norm_launches + 1
+    launches_per_step = norm_launches if norm_launches == 1 else norm_launches + 1
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(device)
@@ -305,7 +307,7 @@ def run_native(args, rank, ws, local):
     torch.cuda._sleep(20_000_000)
     e0.record(stream)
     for _ in range(reps):
-        rnc.dprc_norm_hutch(A, G, P, n, accumulate=False, ws=wsbuf)
+        rnc.dprc_norm_hutch_clip(A, G, P, n, wk.C, c, accumulate=False, ws=wsbuf)
     e1.record(stream)
     torch.cuda.synchronize(device)
     call_ms = e0.elapsed_time(e1) / reps
@@ -344,8 +346,7 @@ def run_native(args, rank, ws, local):
         Ad.copy_(Ah, non_blocking=True)
         Gd.copy_(Gh, non_blocking=True)
         Pd.copy_(Ph, non_blocking=True)
-        rnc.dprc_norm_hutch(Ad, Gd, Pd, n, accumulate=False, ws=wsbuf)
-        rnc.dprc_clip_factors(n, wk.C, c)
+        rnc.dprc_norm_hutch_clip(Ad, Gd, Pd, n, wk.C, c, accumulate=False, ws=wsbuf)
         ch.copy_(c, non_blocking=True)
 
     e2e_step()

@@ -115,6 +115,24 @@ dprc_status dprc_norm_hutch(const void* A, const void* G, const void* P, dprc_dt
                             float* n, int accumulate, void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * dprc_norm_hutch followed by the clip factors of the updated n (the next
+ * step of the method, papernotes.org, "Method > Overall framework"):
+ *     n[i] (+)= || A_i^T (G_i P) ||_F^2,   c[i] = min(1, C / sqrt(n[i]))
+ * with the rule of dprc_clip_factors (n = 0 gives 1; a non-finite or
+ * negative n gives 0 and is counted in *nonfinite, which may be NULL).  Use
+ * it for the last layer of a step.  When dprc_norm_hutch_launches reports one
+ * launch, the clip factors are written by that launch's finishing step (no
+ * second kernel); otherwise the clip kernel follows on the same stream.  The
+ * results equal dprc_norm_hutch then dprc_clip_factors bit for bit.
+ *  c device float [B], 16-byte aligned; C > 0 and finite.  Other arguments,
+ *  the workspace and errors as dprc_norm_hutch.
+ */
+dprc_status dprc_norm_hutch_clip(const void* A, const void* G, const void* P, dprc_dtype dtype,
+                                 int64_t B, int64_t T, int64_t d, int64_t p, int64_t k,
+                                 float* n, int accumulate, float C, float* c,
+                                 int32_t* nonfinite, void* ws, size_t ws_bytes, void* stream);
+
+/*
  * Hutchinson estimate with a +-1 projection generated from a seed (the {-1, +1}
  * one-bit projection the notes name as the way to cut P's memory further;
  * papernotes.org, "Experiments > Ablation".  The pages give no formula and

@@ -29,6 +29,7 @@ from .binding import (  # noqa: F401
     dprc_exact_norm,
     dprc_exact_norm_plan,
     dprc_norm_hutch,
+    dprc_norm_hutch_clip,
     dprc_norm_hutch_launches,
     dprc_norm_hutch_layers,
     dprc_norm_hutch_pm1,

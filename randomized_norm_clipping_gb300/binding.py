@@ -66,6 +66,10 @@ _PROTOS = [
       _c.c_int, _c.c_void_p, _c.c_int, _c.c_void_p, _c.c_size_t, _c.c_void_p]),
     ("dprc_exact_norm_plan", _c.c_int,
      [_c.c_int, _c.c_int64, _c.c_int64, _c.c_int64, _c.c_int64, _c.c_int]),
+    ("dprc_norm_hutch_clip", _c.c_int,
+     [_c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_int, _c.c_int64, _c.c_int64, _c.c_int64,
+      _c.c_int64, _c.c_int64, _c.c_void_p, _c.c_int, _c.c_float, _c.c_void_p, _c.c_void_p,
+      _c.c_void_p, _c.c_size_t, _c.c_void_p]),
     ("dprc_norm_hutch_noalloc", _c.c_int,
      [_c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_int, _c.c_int64, _c.c_int64, _c.c_int64,
       _c.c_int64, _c.c_int64, _c.c_void_p, _c.c_int, _c.c_void_p]),
@@ -153,6 +157,23 @@ def workspace(op, like, B, T, d, p, k):
     if n == 0:
         raise DprcError("dprc_workspace_bytes", 2)
     return torch.zeros(n, dtype=torch.uint8, device=like.device)
+
+
+def dprc_norm_hutch_clip(A, G, P, n, C, c, accumulate=False, nonfinite=None, ws=None,
+                         stream=None):
+    """n[i] (+)= ||A_i^T (G_i P)||_F^2, then c[i] = min(1, C / sqrt(n[i]))
+    (see include/dprc.h)."""
+    _need_cuda(A, G, P, n, c, nonfinite)
+    B, T, d = A.shape
+    p, k = P.shape
+    if ws is None:
+        ws = workspace(DPRC_OP_HUTCH, A, B, T, d, p, k)
+    st = lib().dprc_norm_hutch_clip(_ptr(A), _ptr(G), _ptr(P), _dtype_code(A), B, T, d, p, k,
+                                    _ptr(n), int(bool(accumulate)), float(C), _ptr(c),
+                                    _ptr(nonfinite) if nonfinite is not None else None,
+                                    _ptr(ws), ws.numel(), _stream(A, stream))
+    _check("dprc_norm_hutch_clip", st)
+    return n, c
 
 
 def dprc_norm_hutch_pm1(A, G, k, seed, step, n, accumulate=False, ws=None, stream=None):

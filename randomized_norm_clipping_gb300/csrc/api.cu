@@ -414,6 +414,63 @@ size_t pm1_ws(dprc_dtype dt, int64_t B, int64_t T, int64_t d, int64_t p, int64_t
 
 }  // namespace
 
+namespace {
+// dprc_norm_hutch, with the clip factors of the updated n when `clip` is set
+// (in the fused kernel's finishing step, else by the clip kernel afterwards).
+dprc_status norm_hutch_impl(const void* A, const void* G, const void* P, dprc_dtype dtype,
+                            int64_t B, int64_t T, int64_t d, int64_t p, int64_t k, float* n,
+                            int accumulate, void* ws, size_t ws_bytes, void* stream,
+                            const ClipOut* clip) {
+  if (!A || !G || !P || !n) return DPRC_ERR_NULL;
+  dprc_status st = check_common(dtype, B, T, d, p);
+  if (st != DPRC_OK) return st;
+  if (k < 1 || k > 256) return DPRC_ERR_SHAPE;
+  if (!aligned16(A) || !aligned16(G) || !aligned16(P) || !aligned16(n)) return DPRC_ERR_ALIGN;
+  if (clip != nullptr) {
+    if (!clip->c) return DPRC_ERR_NULL;
+    if (!(clip->C > 0.f) || !(clip->C < __builtin_inff())) return DPRC_ERR_SHAPE;
+    if (!aligned16(clip->c)) return DPRC_ERR_ALIGN;
+  }
+  if (!ws) return DPRC_ERR_WORKSPACE;
+  if (!aligned16(ws)) return DPRC_ERR_ALIGN;
+  if (!device_ok()) return DPRC_ERR_DEVICE;
+  if (ws_bytes < hutch_ws(dtype, B, T, d, p, k)) return DPRC_ERR_WORKSPACE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char* w = static_cast<char*>(ws);
+  auto clip_after = [&](cudaError_t e) -> dprc_status {
+    if (e == cudaSuccess && clip != nullptr) e = launch_clip(n, B, clip->C, clip->c, clip->nonfinite, s);
+    return cuda_status(e);
+  };
+  mark(0, s);
+  if (narrow_proj_supported(dtype, d, p, k)) {
+    // p <= 64: X_i = A_i^T G_i in one pass, each row of it times P in the epilogue
+    const cudaError_t e =
+        launch_narrow_hutch(A, G, P, B, T, d, p, k, 1.0f, 0, 0,
+                            reinterpret_cast<float*>(w + narrow_part_off(B)), n, accumulate, s);
+    mark(1, s);
+    mark(2, s);
+    return clip_after(e);
+  }
+  if (tc_path_supported(dtype, B, T, d, p, k, false) && fused_hutch_supported(k)) {
+    // one launch: sketch and projection as two phases of one kernel (and the
+    // clip factors in its finishing step)
+    const TcPlan t = plan_tc(DPRC_OP_HUTCH, B, T, d, p, k);
+    bool launched = false;
+    const cudaError_t e = launch_tc_hutch_layers(1, &A, &G, &P, &d, &p, B, T, k,
+                                                 fused_scratch(t, w), n, accumulate, s, &launched,
+                                                 clip);
+    if (launched) {
+      mark(1, s);
+      mark(2, s);
+      return cuda_status(e);
+    }
+    if (e != cudaSuccess) (void)cudaGetLastError();  // not launched: two kernels below
+  }
+  return clip_after(hutch_kernels(A, G, P, dtype, B, T, d, p, k, n, accumulate, w,
+                                  static_cast<int>(k), 1.0f, s));
+}
+}  // namespace
+
 extern "C" {
 
 int dprc_abi_version(void) { return DPRC_ABI_VERSION; }
@@ -464,45 +521,24 @@ dprc_status dprc_set_phase_events(void** events, int n_events) {
   return DPRC_OK;
 }
 
+
 dprc_status dprc_norm_hutch(const void* A, const void* G, const void* P, dprc_dtype dtype,
                             int64_t B, int64_t T, int64_t d, int64_t p, int64_t k, float* n,
                             int accumulate, void* ws, size_t ws_bytes, void* stream) {
-  if (!A || !G || !P || !n) return DPRC_ERR_NULL;
-  dprc_status st = check_common(dtype, B, T, d, p);
-  if (st != DPRC_OK) return st;
-  if (k < 1 || k > 256) return DPRC_ERR_SHAPE;
-  if (!aligned16(A) || !aligned16(G) || !aligned16(P) || !aligned16(n)) return DPRC_ERR_ALIGN;
-  if (!ws) return DPRC_ERR_WORKSPACE;
-  if (!aligned16(ws)) return DPRC_ERR_ALIGN;
-  if (!device_ok()) return DPRC_ERR_DEVICE;
-  if (ws_bytes < hutch_ws(dtype, B, T, d, p, k)) return DPRC_ERR_WORKSPACE;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  char* w = static_cast<char*>(ws);
-  mark(0, s);
-  if (narrow_proj_supported(dtype, d, p, k)) {
-    // p <= 64: X_i = A_i^T G_i in one pass, each row of it times P in the epilogue
-    const cudaError_t e =
-        launch_narrow_hutch(A, G, P, B, T, d, p, k, 1.0f, 0, 0,
-                            reinterpret_cast<float*>(w + narrow_part_off(B)), n, accumulate, s);
-    mark(1, s);
-    mark(2, s);
-    return cuda_status(e);
-  }
-  if (tc_path_supported(dtype, B, T, d, p, k, false) && fused_hutch_supported(k)) {
-    // one launch: sketch and projection as two phases of one kernel
-    const TcPlan t = plan_tc(DPRC_OP_HUTCH, B, T, d, p, k);
-    bool launched = false;
-    const cudaError_t e = launch_tc_hutch_layers(1, &A, &G, &P, &d, &p, B, T, k,
-                                                 fused_scratch(t, w), n, accumulate, s, &launched);
-    if (launched) {
-      mark(1, s);
-      mark(2, s);
-      return cuda_status(e);
-    }
-    if (e != cudaSuccess) (void)cudaGetLastError();  // not launched: two kernels below
-  }
-  return cuda_status(hutch_kernels(A, G, P, dtype, B, T, d, p, k, n, accumulate, w,
-                                   static_cast<int>(k), 1.0f, s));
+  return norm_hutch_impl(A, G, P, dtype, B, T, d, p, k, n, accumulate, ws, ws_bytes, stream,
+                         nullptr);
+}
+
+dprc_status dprc_norm_hutch_clip(const void* A, const void* G, const void* P, dprc_dtype dtype,
+                                 int64_t B, int64_t T, int64_t d, int64_t p, int64_t k, float* n,
+                                 int accumulate, float C, float* c, int32_t* nonfinite, void* ws,
+                                 size_t ws_bytes, void* stream) {
+  ClipOut clip;
+  clip.C = C;
+  clip.c = c;
+  clip.nonfinite = nonfinite;
+  return norm_hutch_impl(A, G, P, dtype, B, T, d, p, k, n, accumulate, ws, ws_bytes, stream,
+                         &clip);
 }
 
 dprc_status dprc_norm_hutch_pm1(const void* A, const void* G, uint64_t seed, uint64_t step,

@@ -401,6 +401,19 @@ __device__ __forceinline__ uint4 philox_block(uint64_t j, uint64_t step, const R
 }
 
 
+// Clip factor of one squared norm v ("Method > Overall framework" of the
+// notes: c = min(1, C / sqrt(n))): 1 for v = 0; 0 for a non-finite or negative
+// v (an unknown norm: the sample contributes nothing), with `bad` set.
+__device__ __forceinline__ float clip_factor(float v, float C, bool& bad) {
+  bad = false;
+  if (!isfinite(v) || v < 0.f) {
+    bad = true;
+    return 0.f;
+  }
+  if (v == 0.f) return 1.f;
+  return fminf(1.f, C / sqrtf(v));
+}
+
 // Round a shared-memory pointer up to the 1024-byte alignment that 128-byte
 // swizzled tiles need.
 __device__ __forceinline__ uint8_t* align_1024(uint8_t* p) {

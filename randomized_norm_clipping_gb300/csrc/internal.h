@@ -174,10 +174,18 @@ bool fused_hutch_supported(int64_t k);
 // Whether a dprc_norm_hutch call with these sizes takes the fused kernel on
 // the current device (the same decision the launcher makes).
 bool fused_hutch_planned(int64_t B, int64_t T, int64_t d, int64_t p, int64_t k);
+// Optional clip epilogue: c[i] = min(1, C / sqrt(n_out[i])) (the rule of
+// dprc_clip_factors) once n_out[i] is final.
+struct ClipOut {
+  float C = 0.f;
+  float* c = nullptr;
+  int32_t* nonfinite = nullptr;
+};
 cudaError_t launch_tc_hutch_layers(int L, const void* const* A, const void* const* G,
                                    const void* const* P, const int64_t* d, const int64_t* p,
                                    int64_t B, int64_t T, int64_t k, const FusedScratch& ws,
-                                   float* n_out, int accumulate, cudaStream_t s, bool* launched);
+                                   float* n_out, int accumulate, cudaStream_t s, bool* launched,
+                                   const ClipOut* clip = nullptr);
 // The +-1 projection variant on the fused kernel (bf16, k = 16 or 32, one
 // layer): the signs are generated in the kernel from (seed, step); the norm is
 // scaled by 1/k.  *launched false: not possible here (use the signs below).

@@ -145,17 +145,9 @@ __global__ void clip_kernel(const float* __restrict__ n, long long B, float C,
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (i >= B) return;
-  const float v = n[i];
-  float out;
-  if (!isfinite(v) || v < 0.f) {
-    out = 0.f;  // unknown norm: the sample contributes nothing
-    if (nonfinite != nullptr) atomicAdd(nonfinite, 1);
-  } else if (v == 0.f) {
-    out = 1.f;
-  } else {
-    out = fminf(1.f, C / sqrtf(v));
-  }
-  c[i] = out;
+  bool bad;
+  c[i] = clip_factor(n[i], C, bad);
+  if (bad && nonfinite != nullptr) atomicAdd(nonfinite, 1);
 }
 
 int grid_for(long long work, int threads, int ctas_per_sm = 8) {

@@ -242,6 +242,9 @@ struct HParams {
   float* n_out;
   int accumulate;
   float norm_scale;                // 1, or 1/k for the +-1 projection
+  float clip_C;                    // clip epilogue (c_out non-null): c = min(1, C / sqrt(n))
+  float* c_out;
+  int32_t* nonfinite;
   unsigned long long seed, step;   // +-1 projection: its Philox stream
   LayerDesc layer[CAP];     // CAP = 1 for single-layer calls: a small parameter block
 };
@@ -765,7 +768,13 @@ __global__ void __launch_bounds__(hutch_threads<PM1>(), 1)
                 a.ready[li] = 0;
                 if (CAP == 1) {
                   // one layer: no layer sum to wait for
-                  a.n_out[i] = (a.accumulate ? a.n_out[i] : 0.f) + sum;
+                  const float nv = (a.accumulate ? a.n_out[i] : 0.f) + sum;
+                  a.n_out[i] = nv;
+                  if (a.c_out != nullptr) {
+                    bool bad;
+                    a.c_out[i] = clip_factor(nv, a.clip_C, bad);
+                    if (bad && a.nonfinite != nullptr) atomicAdd(a.nonfinite, 1);
+                  }
                 } else {
                   a.nl[li] = sum;
                   __threadfence();
@@ -781,8 +790,14 @@ __global__ void __launch_bounds__(hutch_threads<PM1>(), 1)
 #pragma unroll
                 for (int off = 16; off > 0; off >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, off);
                 if (lane == 0) {
-                  a.n_out[i] = (a.accumulate ? a.n_out[i] : 0.f) + tot;
+                  const float nv = (a.accumulate ? a.n_out[i] : 0.f) + tot;
+                  a.n_out[i] = nv;
                   a.lticket[i] = 0;
+                  if (a.c_out != nullptr) {
+                    bool bad;
+                    a.c_out[i] = clip_factor(nv, a.clip_C, bad);
+                    if (bad && a.nonfinite != nullptr) atomicAdd(a.nonfinite, 1);
+                  }
                 }
               }
             }
@@ -997,7 +1012,8 @@ template <int CAP, bool PM1>
 cudaError_t launch_cap(int L, const void* const* A, const void* const* G, const void* const* P,
                        const int64_t* d, const int64_t* p, int64_t B, int64_t T, int64_t k,
                        const FusedScratch& ws, float* n_out, int accumulate, uint64_t seed,
-                       uint64_t step, cudaStream_t s, bool* launched) {
+                       uint64_t step, cudaStream_t s, bool* launched,
+                       const ClipOut* clip) {
   static thread_local HParams<CAP> a;  // up to ~26 KB: kept off the stack
   int grid = 0;
   if (!plan_fused<CAP, PM1>(L, d, p, B, T, k, a, grid)) return cudaSuccess;
@@ -1015,6 +1031,9 @@ cudaError_t launch_cap(int L, const void* const* A, const void* const* G, const 
   a.n_out = n_out;
   a.accumulate = accumulate;
   a.norm_scale = PM1 ? 1.0f / static_cast<float>(k) : 1.0f;
+  a.clip_C = clip != nullptr ? clip->C : 0.f;
+  a.c_out = clip != nullptr ? clip->c : nullptr;
+  a.nonfinite = clip != nullptr ? clip->nonfinite : nullptr;
   a.seed = seed;
   a.step = step;
   for (int b = 0; b < 2; ++b)
@@ -1047,13 +1066,13 @@ cudaError_t launch_tc_hutch_layers(int L, const void* const* A, const void* cons
                                    const void* const* P, const int64_t* d, const int64_t* p,
                                    int64_t B, int64_t T, int64_t k, const FusedScratch& ws,
                                    float* n_out, int accumulate, cudaStream_t s,
-                                   bool* launched) {
+                                   bool* launched, const ClipOut* clip) {
   *launched = false;
   if (L == 1)
     return launch_cap<1, false>(L, A, G, P, d, p, B, T, k, ws, n_out, accumulate, 0, 0, s,
-                                launched);
+                                launched, clip);
   return launch_cap<kMaxFusedLayers, false>(L, A, G, P, d, p, B, T, k, ws, n_out, accumulate, 0,
-                                            0, s, launched);
+                                            0, s, launched, clip);
 }
 
 cudaError_t launch_tc_hutch_pm1(const void* A, const void* G, int64_t B, int64_t T, int64_t d,
@@ -1063,7 +1082,7 @@ cudaError_t launch_tc_hutch_pm1(const void* A, const void* G, int64_t B, int64_t
   *launched = false;
   const void* P = nullptr;
   return launch_cap<1, true>(1, &A, &G, &P, &d, &p, B, T, k, ws, n_out, accumulate, seed, step, s,
-                             launched);
+                             launched, nullptr);
 }
 
 }  // namespace dprc

@@ -15,7 +15,8 @@
 
 `RandomizedClippingStep` does steps 2-5 around the caller's forward pass.
 Steps 3-5 run in libdprc (dprc_norm_hutch or dprc_norm_hutchpp with
-accumulation for the layer sum, dprc_clip_factors, dprc_add_noise); PyTorch
+accumulation for the layer sum, the last Hutchinson layer through
+dprc_norm_hutch_clip, else dprc_clip_factors; dprc_add_noise); PyTorch
 provides the forward and backward passes and the memory.  The first backward
 asks autograd only for the gradients with respect to the recorded layer
 outputs, so no weight gradient is formed before the clip factors are known.
@@ -141,6 +142,8 @@ class RandomizedClippingStep:
         proj = self.projections(step) if projections is None else projections
         # step 3: layerwise sum of the per-sample estimates
         n = torch.zeros(B, dtype=torch.float32, device=losses.device)
+        c = torch.empty_like(n)
+        last = len(self.layers) - 1
         for j, (m, G) in enumerate(zip(self.layers, grads)):
             A = self._acts[m]
             # (B, ..., d): every position between batch and features is a token
@@ -150,14 +153,17 @@ class RandomizedClippingStep:
             p = G.shape[-1]
             if self.method == "hutch":
                 ws = self._workspace(rnc.DPRC_OP_HUTCH, A, Bt, T, d, p)
-                rnc.dprc_norm_hutch(A, G, proj[j], n, accumulate=j > 0, ws=ws)
+                if j == last:  # step 4's clip factors come with the last layer's norms
+                    rnc.dprc_norm_hutch_clip(A, G, proj[j], n, self.C, c, accumulate=j > 0, ws=ws)
+                else:
+                    rnc.dprc_norm_hutch(A, G, proj[j], n, accumulate=j > 0, ws=ws)
             else:
                 S, P = proj[j]
                 ws = self._workspace(rnc.DPRC_OP_HUTCHPP, A, Bt, T, d, p)
                 rnc.dprc_norm_hutchpp(A, G, S, P, n, accumulate=j > 0, ws=ws)
-        # step 4: clip factors and the rescaled second backward
-        c = torch.empty_like(n)
-        rnc.dprc_clip_factors(n, self.C, c)
+        # step 4: clip factors (Hutch++: here) and the rescaled second backward
+        if self.method != "hutch":
+            rnc.dprc_clip_factors(n, self.C, c)
         for m in self.layers:
             m.weight.grad = None
         (c.to(losses.dtype) * losses).sum().backward()

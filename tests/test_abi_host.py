@@ -107,6 +107,14 @@ def test_argument_errors_return_before_device_work(lib):
     e = lib.dprc_exact_norm
     assert e(_vp(A16), None, 1, 1, 1, 8, 8, _vp(A16), 0, _vp(A16), ws, None) == 1
     assert e(_vp(A16), _vp(A16), 1, 1, 1, 8, 8, _vp(A16), 0, _vp(A16), 0, None) == 5
+    hc = lib.dprc_norm_hutch_clip
+    f32 = ctypes.c_float
+    assert hc(_vp(A16), _vp(A16), _vp(A16), 1, 1, 64, 8, 8, 8, _vp(A16), 0, f32(1.0), None, None,
+              _vp(A16), ws, None) == 1  # no c
+    assert hc(_vp(A16), _vp(A16), _vp(A16), 1, 1, 64, 8, 8, 8, _vp(A16), 0, f32(0.0), _vp(A16),
+              None, _vp(A16), ws, None) == 2  # C <= 0
+    assert hc(_vp(A16), _vp(A16), _vp(A16), 1, 1, 64, 8, 8, 8, _vp(A16), 0, f32(1.0), _vp(A16 + 4),
+              None, _vp(A16), ws, None) == 4  # misaligned c
     ef = lib.dprc_exact_norm_form
     assert ef(_vp(A16), _vp(A16), 1, 1, 1, 8, 8, 5, _vp(A16), 0, _vp(A16), ws, None) == 2  # form
     assert ef(_vp(A16), _vp(A16), 0, 1, 1, 8, 8, 3, _vp(A16), 0, _vp(A16), ws, None) == 2

@@ -89,6 +89,45 @@ def test_hutch_bf16_matches_oracle(B, T, d, p, k):
     assert _relerr(n.cpu(), ref) < RTOL
 
 
+# The norm call with the clip factors of the updated n: in the fused kernel's
+# finishing step (one launch), or the clip kernel after the other paths; bit
+# for bit the two-call sequence, both clip branches, a non-finite sample.
+@pytest.mark.parametrize("B,T,d,p,k,dtype", [
+    (6, 300, 256, 512, 32, torch.bfloat16),   # fused kernel: the clip in its finisher
+    (4, 200, 256, 256, 64, torch.bfloat16),   # two kernels, then the clip kernel
+    (4, 500, 1024, 16, 32, torch.bfloat16),   # narrow layer, then the clip kernel
+    (4, 128, 64, 64, 8, torch.float32),       # CUDA cores, then the clip kernel
+])
+def test_norm_hutch_clip_equals_norm_then_clip(B, T, d, p, k, dtype):
+    A, G, P = _hutch_case(B, T, d, p, k, dtype, seed=300 + T)
+    Ad, Gd, Pd = A.to(DEV), G.to(DEV), P.to(DEV)
+    ref = oracle.hutch_norm(to_f64(A), to_f64(G), to_f64(P))
+    C = float(np.median(np.sqrt(ref)))  # half the samples clip
+    n1 = torch.full((B,), 0.5, device=DEV)
+    c1 = torch.empty(B, device=DEV)
+    rnc.dprc_norm_hutch(Ad, Gd, Pd, n1, accumulate=True)
+    rnc.dprc_clip_factors(n1, C, c1)
+    n2 = torch.full((B,), 0.5, device=DEV)
+    c2 = torch.empty(B, device=DEV)
+    rnc.dprc_norm_hutch_clip(Ad, Gd, Pd, n2, C, c2, accumulate=True)
+    assert torch.equal(n1, n2) and torch.equal(c1, c2)
+    tol = 1e-5 if dtype == torch.float32 else RTOL
+    assert _relerr(n2.cpu(), ref + 0.5) < tol
+    assert _relerr(c2.cpu(), oracle.clip_factors(ref + 0.5, C)) < tol
+
+
+def test_norm_hutch_clip_zeroes_a_nonfinite_sample():
+    A, G, P = _hutch_case(3, 300, 256, 512, 32, torch.bfloat16, seed=77)
+    A[1, 5, 7] = float("nan")
+    n = torch.zeros(3, device=DEV)
+    c = torch.full((3,), 9.0, device=DEV)
+    bad = torch.zeros(1, dtype=torch.int32, device=DEV)
+    rnc.dprc_norm_hutch_clip(A.to(DEV), G.to(DEV), P.to(DEV), n, 1.0, c, nonfinite=bad)
+    assert torch.isnan(n[1]) and float(c[1]) == 0.0 and int(bad) == 1
+    ref = oracle.hutch_norm(to_f64(A[[0, 2]]), to_f64(G[[0, 2]]), to_f64(P))
+    assert _relerr(c[[0, 2]].cpu(), oracle.clip_factors(ref, 1.0)) < RTOL
+
+
 # Narrow layers (a width <= 64): X_i = A_i^T G_i in one tensor-core pass; the
 # exact norm for both orientations (the wide operand A or G), the estimate
 # ||X_i P||^2 from the rows of X_i when p <= 64 (d-narrow maps take the
