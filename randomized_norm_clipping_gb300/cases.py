@@ -24,12 +24,28 @@ from . import binding as rnc
 from . import workloads as wl
 
 
-def _hutch(name, layer=0):
+def _hutch(name, layer=0, clip=False):
     wk = wl.WORKLOADS[name]
     lay = wk.layers[layer]
     A, G, P = wl.layer_inputs(wk, layer, device="cuda")
     n = torch.zeros(wk.B, device="cuda")
+    c = torch.empty(wk.B, device="cuda")
     ws = rnc.workspace(rnc.DPRC_OP_HUTCH, A, wk.B, wk.T, lay.d, lay.p, wk.k)
+    if clip:
+        return lambda: rnc.dprc_norm_hutch_clip(A, G, P, n, wk.C, c, ws=ws)
+    return lambda: rnc.dprc_norm_hutch(A, G, P, n, ws=ws)
+
+
+def _lora(B, T, d, p, k, exact):
+    g = torch.Generator(device="cuda").manual_seed(5)
+    A = torch.randn(B, T, d, device="cuda", generator=g).to(torch.bfloat16)
+    G = (torch.randn(B, T, p, device="cuda", generator=g) * 0.02).to(torch.bfloat16)
+    P = (torch.randn(p, k, device="cuda", generator=g) / k ** 0.5).to(torch.bfloat16)
+    n = torch.zeros(B, device="cuda")
+    if exact:
+        ws = rnc.workspace(rnc.DPRC_OP_EXACT, A, B, T, d, p, 0)
+        return lambda: rnc.dprc_exact_norm(A, G, n, ws=ws)
+    ws = rnc.workspace(rnc.DPRC_OP_HUTCH, A, B, T, d, p, k)
     return lambda: rnc.dprc_norm_hutch(A, G, P, n, ws=ws)
 
 
@@ -85,6 +101,11 @@ def _clip():
 CASES = {
     # B8 T4096 d = p = 2048 k32 bf16 (268 MB of A and G)
     "hutch_q_proj": lambda: _hutch("hutch_q_proj_b8_t4096_k32_bf16"),
+    # the same with the clip factors in the launch (the benchmark's step)
+    "hutch_clip_q_proj": lambda: _hutch("hutch_q_proj_b8_t4096_k32_bf16", clip=True),
+    # rank-16 adapter maps of the q_proj batch (B8 T4096; 135 MB of A and G)
+    "lora_down_exact": lambda: _lora(8, 4096, 2048, 16, 32, True),
+    "lora_down_hutch": lambda: _lora(8, 4096, 2048, 16, 32, False),
     # B2 T32768 2048 -> 8192 and 8192 -> 2048, k32 bf16 (1.34 GB each)
     # the same batch with the +-1 projection generated in the kernel
     "hutch_pm1_q_proj": lambda: _hutch_pm1("hutch_q_proj_b8_t4096_k32_bf16"),
