@@ -106,6 +106,8 @@ CASES = {
     # rank-16 adapter maps of the q_proj batch (B8 T4096; 135 MB of A and G)
     "lora_down_exact": lambda: _lora(8, 4096, 2048, 16, 32, True),
     "lora_down_hutch": lambda: _lora(8, 4096, 2048, 16, 32, False),
+    "lora_up_exact": lambda: _lora(8, 4096, 16, 2048, 32, True),
+    "lora_up_hutch": lambda: _lora(8, 4096, 16, 2048, 32, False),
     # B2 T32768 2048 -> 8192 and 8192 -> 2048, k32 bf16 (1.34 GB each)
     # the same batch with the +-1 projection generated in the kernel
     "hutch_pm1_q_proj": lambda: _hutch_pm1("hutch_q_proj_b8_t4096_k32_bf16"),

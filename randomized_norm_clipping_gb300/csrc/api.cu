@@ -353,17 +353,17 @@ dprc_status check_common(dprc_dtype dt, int64_t B, int64_t T, int64_t d, int64_t
   return DPRC_OK;
 }
 
-// Narrow layers keep one fp32 partial per tile after the counter block.
+// Narrow layers keep their per-tile partials after the counter block.
 size_t narrow_part_off(int64_t B) { return align_up(ctrl_bytes(B), 1024); }
-size_t narrow_ws(int64_t B, int64_t d, int64_t p) {
-  return narrow_part_off(B) + align_up(static_cast<size_t>(narrow_partials(B, d, p)) * 4, 1024);
+size_t narrow_ws(int64_t B, int64_t d, int64_t p, int64_t k) {
+  return narrow_part_off(B) + align_up(narrow_hutch_scratch_bytes(B, d, p, k), 1024);
 }
 
 size_t hutch_ws(dprc_dtype dt, int64_t B, int64_t T, int64_t d, int64_t p, int64_t k) {
   const size_t base = tc_path_supported(dt, B, T, d, p, k, false)
                           ? plan_tc(DPRC_OP_HUTCH, B, T, d, p, k).total
                           : plan_simt(DPRC_OP_HUTCH, B, T, d, p, k).total;
-  return narrow_proj_supported(dt, d, p, k) ? std::max(base, narrow_ws(B, d, p)) : base;
+  return narrow_proj_supported(dt, d, p, k) ? std::max(base, narrow_ws(B, d, p, k)) : base;
 }
 
 size_t hutchpp_ws(dprc_dtype dt, int64_t B, int64_t T, int64_t d, int64_t p, int64_t r) {
@@ -443,9 +443,9 @@ dprc_status norm_hutch_impl(const void* A, const void* G, const void* P, dprc_dt
   };
   mark(0, s);
   if (narrow_proj_supported(dtype, d, p, k)) {
-    // p <= 64: X_i = A_i^T G_i in one pass, each row of it times P in the epilogue
+    // a width <= 64: X_i = A_i^T G_i in one pass, times P in the epilogue
     const cudaError_t e =
-        launch_narrow_hutch(A, G, P, B, T, d, p, k, 1.0f, 0, 0,
+        launch_narrow_hutch(A, G, P, B, T, d, p, k, 1.0f, 0, 0, reinterpret_cast<int*>(w),
                             reinterpret_cast<float*>(w + narrow_part_off(B)), n, accumulate, s);
     mark(1, s);
     mark(2, s);
@@ -557,10 +557,11 @@ dprc_status dprc_norm_hutch_pm1(const void* A, const void* G, uint64_t seed, uin
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   char* w = static_cast<char*>(ws);
   if (narrow_proj_supported(dtype, d, p, k)) {
-    // p <= 64: X_i = A_i^T G_i in one pass, then (1/k) ||X_i S||^2 with the
-    // signs generated in the kernel's shared memory
+    // a width <= 64: X_i = A_i^T G_i in one pass, then (1/k) ||X_i S||^2
+    // with the signs generated in the kernel's shared memory
     return cuda_status(launch_narrow_hutch(A, G, nullptr, B, T, d, p, k,
                                            1.0f / static_cast<float>(k), seed, step,
+                                           reinterpret_cast<int*>(w),
                                            reinterpret_cast<float*>(w + narrow_part_off(B)), n,
                                            accumulate, s));
   }
@@ -635,7 +636,7 @@ int dprc_norm_hutch_launches(dprc_dtype dtype, int64_t B, int64_t T, int64_t d, 
                              int64_t k) {
   if (check_common(dtype, B, T, d, p) != DPRC_OK || k < 1 || k > 256) return 0;
   if (!device_ok()) return 0;
-  if (narrow_proj_supported(dtype, d, p, k)) return 2;
+  if (narrow_proj_supported(dtype, d, p, k)) return 1;
   if (!tc_path_supported(dtype, B, T, d, p, k, false)) return 3;
   return fused_hutch_planned(B, T, d, p, k) ? 1 : 2;
 }
@@ -752,7 +753,9 @@ dprc_status dprc_exact_norm_form(const void* A, const void* G, dprc_dtype dtype,
       err = launch_tc_exact_ghost(A, G, B, T, d, p, e.W, ws, partials, n, accumulate, s);
       break;
     case ExactPlan::kNarrowTc:
-      err = launch_narrow_norm(A, G, B, T, d, p, partials, n, accumulate, s);
+      // per-sample tickets at the front of the zeroed counter block
+      err = launch_narrow_norm(A, G, B, T, d, p, static_cast<int*>(ws), partials, n, accumulate,
+                               s);
       break;
     default:
       err = launch_exact_ghost(A, G, dtype, B, T, d, p, partials, n, accumulate, s);

@@ -211,21 +211,23 @@ cudaError_t launch_tc_exact_ghost(const void* A, const void* G, int64_t B, int64
                                   float* n_out, int accumulate, cudaStream_t s);
 // Narrow layers (bf16, d and p multiples of 8, min(d, p) <= 64): the gradient
 // X_i = A_i^T G_i formed tile by tile in one streaming tensor-core pass.
-// launch_narrow_norm: n_out (+)= ||X_i||^2; launch_narrow_hutch (p <= 64,
-// 1 <= k <= 256): n_out (+)= scale ||X_i P||^2 with P [p][k] bf16, or with the
-// +-1 signs of (seed, step) when P is null.  Both use narrow_partials(B, d, p)
-// floats of partials.
+// launch_narrow_norm: n_out (+)= ||X_i||^2 (narrow_partials(B, d, p) floats
+// of scratch); launch_narrow_hutch (narrow_proj_supported): n_out (+)=
+// scale ||X_i P||^2 with P [p][k] bf16, or with the +-1 signs of (seed, step)
+// when P is null (narrow_hutch_scratch_bytes of scratch).
 bool narrow_supported(dprc_dtype dt, int64_t d, int64_t p);
 bool narrow_proj_supported(dprc_dtype dt, int64_t d, int64_t p, int64_t k);
 int64_t narrow_partials(int64_t B, int64_t d, int64_t p);
+size_t narrow_hutch_scratch_bytes(int64_t B, int64_t d, int64_t p, int64_t k);
 cudaError_t read_device_error_narrow(int32_t* out, bool reset);
+// tickets: int32 [B], zero on entry and zero again on exit (one launch).
 cudaError_t launch_narrow_norm(const void* A, const void* G, int64_t B, int64_t T, int64_t d,
-                               int64_t p, float* partials, float* n_out, int accumulate,
-                               cudaStream_t s);
+                               int64_t p, int* tickets, float* partials, float* n_out,
+                               int accumulate, cudaStream_t s);
 cudaError_t launch_narrow_hutch(const void* A, const void* G, const void* P, int64_t B,
                                 int64_t T, int64_t d, int64_t p, int64_t k, float scale,
-                                uint64_t seed, uint64_t step, float* partials, float* n_out,
-                                int accumulate, cudaStream_t s);
+                                uint64_t seed, uint64_t step, int* tickets, float* partials,
+                                float* n_out, int accumulate, cudaStream_t s);
 // n_out[i] (+)= sum of partials[i * per_sample .. (i + 1) * per_sample), fixed order.
 cudaError_t launch_partials_finish(const float* partials, int64_t B, int64_t per_sample,
                                    float* n_out, int accumulate, cudaStream_t s);

@@ -27,8 +27,9 @@
 // eight of them keep 144 to 192 KB per SM in flight.  The accumulator is
 // double buffered.  The epilogue (one TMEM lane, i.e. one row of the tile, per
 // thread) squares and sums the row, or first multiplies it by P (staged in
-// shared memory in bf16), and writes one partial per tile; a finishing kernel
-// sums a sample's partials in index order.
+// shared memory in bf16), and writes one partial per tile; the CTA that
+// completes a sample's last tile (a per-sample ticket) adds the sample's
+// partials in tile order: one launch, deterministic.
 
 #include <atomic>
 
@@ -57,7 +58,9 @@ struct NwCfg {
   static_assert(kStage % 1024 == 0, "stages keep the 1024-byte alignment of swizzled tiles");
 };
 
-enum NwMode { kNwNorm = 0, kNwProj = 1 };
+// kNwNorm: ||rows||^2; kNwProj: ||row P||^2 (p narrow, rows = d);
+// kNwProjT: the tile's part of X_i P (d narrow, rows = p), X_tile^T P_tile.
+enum NwMode { kNwNorm = 0, kNwProj = 1, kNwProjT = 2 };
 
 struct NwArgs {
   int T;
@@ -70,7 +73,88 @@ struct NwArgs {
   int k, kp;          // kp: k rounded up to a multiple of 16 (shared-memory rows)
   float scale;
   uint64_t seed, step;  // the signs' Philox stream when P is null
+  float* ypart;         // kNwProjT: [ntiles][narrow * k] partial products
+  // the last tile of a sample adds its parts into n_out (tickets: zero on
+  // entry, zero again on exit)
+  int* tickets;         // [B]
+  float* n_out;
+  int accumulate;
 };
+
+// Copies `total` consecutive entries of a row-major [.][k] matrix into rows of
+// kp entries in shared memory, by the 128 epilogue threads (index et), with
+// four independent loads in flight per thread.
+template <typename TP>
+__device__ __forceinline__ void stage_rows(const TP* __restrict__ src, int total, int k, int kp,
+                                           TP* dst, int et) {
+  for (int e0 = et; e0 < total; e0 += 4 * 128) {
+    TP v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int e = e0 + 128 * u;
+      v[u] = e < total ? src[e] : static_cast<TP>(0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int e = e0 + 128 * u;
+      if (e < total) dst[(e / k) * kp + e % k] = v[u];
+    }
+  }
+}
+
+// Outputs o = et + 128 m (m < nm <= NM) of a tile's part of X_i P when k
+// divides 128: they share the column c = et % k and take rows
+// a = et / k + m 128 / k of X; each is a sum over the tile's rows in order.
+template <int NM, typename TP>
+__device__ __forceinline__ void shared_col_outputs(const float* Xs, int nx, const TP* Pt, int kp,
+                                                   int k, int rows, int et, int nm, float* dst) {
+  const int c = et % k, a0 = et / k, astep = kNwM / k;
+  float y[NM];
+#pragma unroll
+  for (int m = 0; m < NM; ++m) y[m] = 0.f;
+  for (int r = 0; r < rows; ++r) {
+    const float pv = static_cast<float>(Pt[r * kp + c]);
+    const float* xr = Xs + r * nx + a0;
+#pragma unroll
+    for (int m = 0; m < NM; ++m)
+      if (m < nm) y[m] = fmaf(xr[m * astep], pv, y[m]);
+  }
+  if (dst != nullptr) {
+#pragma unroll
+    for (int m = 0; m < NM; ++m)
+      if (m < nm) dst[et + m * kNwM] = y[m];
+  }
+}
+
+// Rows [p0, p0 + rows) of P (or of the +-1 signs, entry e = r k + c of the
+// Philox stream of (seed, step)) into Pt [128][kp], by the 128 epilogue
+// threads.
+template <typename TP, typename Args>
+__device__ __forceinline__ void stage_p_tile(const Args& a, int p0, int rows, TP* Pt, int et) {
+  if (a.P != nullptr) {
+    // one contiguous run of P: coalesced loads, four in flight per thread
+    stage_rows(static_cast<const TP*>(a.P) + static_cast<size_t>(p0) * a.k, rows * a.k, a.k,
+               a.kp, Pt, et);
+    return;
+  }
+  const RoundKeys rk = round_keys(a.seed);
+  const long long e0 = static_cast<long long>(p0) * a.k;
+  const long long e1 = e0 + static_cast<long long>(rows) * a.k;
+  for (long long jb = e0 / 128 + et; jb * 128 < e1; jb += 128) {
+    const uint4 w = philox_block(static_cast<uint64_t>(jb), a.step, rk);
+    const uint32_t words[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int wq = 0; wq < 4; ++wq)
+      for (int b = 0; b < 32; ++b) {
+        const long long e = jb * 128 + wq * 32 + b;
+        if (e >= e0 && e < e1) {
+          const int r = static_cast<int>((e - e0) / a.k);
+          const int c = static_cast<int>((e - e0) - static_cast<long long>(r) * a.k);
+          Pt[r * a.kp + c] = static_cast<TP>(((words[wq] >> b) & 1u) ? -1.0f : 1.0f);
+        }
+      }
+  }
+}
 
 template <int N, int MODE, typename TP>
 __global__ void __launch_bounds__(192, 1)
@@ -79,6 +163,7 @@ __global__ void __launch_bounds__(192, 1)
   using Cfg = NwCfg<N>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ float s_red[4];
+  __shared__ int s_last;
 
   uint8_t* ring = align_1024(smem_raw);
   TP* Ps = reinterpret_cast<TP*>(ring + kNwStages * Cfg::kStage + Cfg::kCtrl);
@@ -199,8 +284,7 @@ __global__ void __launch_bounds__(192, 1)
       for (int e = et; e < a.narrow * a.kp; e += 128) Ps[e] = static_cast<TP>(0.f);
       named_bar_sync(1, 128);
       if (a.P != nullptr) {
-        const TP* P = static_cast<const TP*>(a.P);
-        for (int e = et; e < pk; e += 128) Ps[(e / a.k) * a.kp + e % a.k] = P[e];
+        stage_rows(static_cast<const TP*>(a.P), pk, a.k, a.kp, Ps, et);
       } else {
         // entry e of S: bit (e & 31) of word ((e >> 5) & 3) of block e >> 7
         const RoundKeys rk = round_keys(a.seed);
@@ -223,6 +307,15 @@ __global__ void __launch_bounds__(192, 1)
     for (long long j = 0; j < my_tiles; ++j) {
       const long long tile = blockIdx.x + j * gridDim.x;
       const int abuf = static_cast<int>(j & 1);
+      if (MODE == kNwProjT) {
+        // the tile's rows of P do not depend on X: staged while the MMAs run
+        const int i = static_cast<int>(tile / a.mt);
+        const int p0 = static_cast<int>(tile - static_cast<long long>(i) * a.mt) * kNwM;
+        const int rows = a.wide - p0 < kNwM ? a.wide - p0 : kNwM;
+        TP* Pt = reinterpret_cast<TP*>(reinterpret_cast<float*>(Ps) + kNwM * (N + 1));
+        stage_p_tile(a, p0, rows, Pt, et);
+        named_bar_sync(1, 128);
+      }
       bool live = ok && mbar_wait(&accf[abuf], static_cast<uint32_t>((j >> 1) & 1),
                                   DPRC_DEVERR_ACCUM) &&
                   *abort_flag == 0;
@@ -243,6 +336,57 @@ __global__ void __launch_bounds__(192, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&acce[abuf]);
+      if (MODE == kNwProjT) {
+        // rows of the tile are p indices p0 + r: the tile's part of X_i P is
+        // sum_r x_r^T P[p0 + r] (d x k).  The rows go to shared memory (Xs,
+        // fp32 [128][N + 1]) beside the tile's rows of P (Pt, staged above),
+        // then each thread forms d k / 128 entries, each summed over r in
+        // a fixed order.
+        constexpr int NX = N + 1;  // padded row: conflict-free column writes
+        float* Xs = reinterpret_cast<float*>(Ps);
+        TP* Pt = reinterpret_cast<TP*>(Xs + kNwM * NX);
+        const int i = static_cast<int>(tile / a.mt);
+        const int p0 = static_cast<int>(tile - static_cast<long long>(i) * a.mt) * kNwM;
+        const int rows = a.wide - p0 < kNwM ? a.wide - p0 : kNwM;
+        const int row = q * 32 + lane;
+#pragma unroll
+        for (int c = 0; c < N; ++c) Xs[row * NX + c] = live ? v[c] : 0.f;
+        named_bar_sync(1, 128);
+        const bool lok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        const int dk = a.narrow * a.k;
+        if (kNwM % a.k == 0 && dk <= 32 * kNwM) {
+          // k divides 128: this thread's outputs et + 128 m share the column
+          // c = et % k, so each P element is loaded once per row
+          const int nm = (dk - et + kNwM - 1) / kNwM;
+          float* dst = lok ? a.ypart + tile * dk : nullptr;
+          if (nm <= 4)
+            shared_col_outputs<4>(Xs, NX, Pt, a.kp, a.k, rows, et, nm, dst);
+          else if (nm <= 8)
+            shared_col_outputs<8>(Xs, NX, Pt, a.kp, a.k, rows, et, nm, dst);
+          else if (nm <= 16)
+            shared_col_outputs<16>(Xs, NX, Pt, a.kp, a.k, rows, et, nm, dst);
+          else
+            shared_col_outputs<32>(Xs, NX, Pt, a.kp, a.k, rows, et, nm, dst);
+        } else {
+          for (int o = et; o < dk; o += 128) {
+            const int ad = o / a.k, c = o - (o / a.k) * a.k;
+            // eight partial sums over r (r mod 8; rows is a multiple of 8),
+            // added in a fixed order
+            float y[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) y[u] = 0.f;
+            for (int r = 0; r < rows; r += 8) {
+#pragma unroll
+              for (int u = 0; u < 8; ++u)
+                y[u] = fmaf(Xs[(r + u) * NX + ad], static_cast<float>(Pt[(r + u) * a.kp + c]),
+                            y[u]);
+            }
+            const float t = ((y[0] + y[1]) + (y[2] + y[3])) + ((y[4] + y[5]) + (y[6] + y[7]));
+            if (lok) a.ypart[tile * dk + o] = t;
+          }
+        }
+        named_bar_sync(1, 128);  // Xs and Pt are rewritten by the next tile
+      } else {
       float sq = 0.f;
       if (live) {
         if (MODE == kNwNorm) {
@@ -292,6 +436,49 @@ __global__ void __launch_bounds__(192, 1)
       if (ew == 0 && lane == 0 && ok)
         a.partials[tile] = (s_red[0] + s_red[1]) + (s_red[2] + s_red[3]);
       named_bar_sync(1, 128);
+      }  // MODE != kNwProjT
+      // the CTA that completes a sample's last tile adds the sample's parts,
+      // in tile order, into n_out
+      const int is = static_cast<int>(tile / a.mt);
+      __threadfence();  // this thread's partial writes, before the ticket
+      named_bar_sync(1, 128);
+      if (et == 0) s_last = atomicAdd(&a.tickets[is], 1) == a.mt - 1;
+      named_bar_sync(1, 128);
+      if (s_last) {
+        __threadfence();
+        float acc = 0.f;
+        if (MODE == kNwProjT) {
+          const int dk = a.narrow * a.k;
+          const float* yi = a.ypart + static_cast<size_t>(is) * a.mt * dk;
+          for (int e = et; e < dk; e += 128) {
+            float y = 0.f;
+            int m = 0;
+            for (; m + 8 <= a.mt; m += 8) {
+              float t[8];
+#pragma unroll
+              for (int u = 0; u < 8; ++u) t[u] = __ldcg(yi + static_cast<size_t>(m + u) * dk + e);
+#pragma unroll
+              for (int u = 0; u < 8; ++u) y += t[u];
+            }
+            for (; m < a.mt; ++m) y += __ldcg(yi + static_cast<size_t>(m) * dk + e);
+            acc = fmaf(y, y, acc);
+          }
+          acc *= a.scale;
+        } else if (ew == 0) {
+          for (int m = lane; m < a.mt; m += 32)
+            acc += __ldcg(a.partials + static_cast<size_t>(is) * a.mt + m);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (lane == 0) s_red[ew] = acc;
+        named_bar_sync(1, 128);
+        if (et == 0) {
+          const float tot = (s_red[0] + s_red[1]) + (s_red[2] + s_red[3]);
+          a.n_out[is] = (a.accumulate ? a.n_out[is] : 0.f) + tot;
+          a.tickets[is] = 0;
+        }
+        named_bar_sync(1, 128);
+      }
     }
   }
 
@@ -354,6 +541,10 @@ bool narrow_setup(const void* A, const void* G, int64_t B, int64_t T, int64_t d,
   a.k = a.kp = 0;
   a.scale = 1.f;
   a.seed = a.step = 0;
+  a.ypart = nullptr;
+  a.tickets = nullptr;
+  a.n_out = nullptr;
+  a.accumulate = 0;
   return true;
 }
 
@@ -368,7 +559,10 @@ bool narrow_supported(dprc_dtype dt, int64_t d, int64_t p) {
 }
 
 bool narrow_proj_supported(dprc_dtype dt, int64_t d, int64_t p, int64_t k) {
-  return dt == DPRC_BF16 && d % 8 == 0 && p % 8 == 0 && p <= 64 && k >= 1 && k <= 256;
+  if (dt != DPRC_BF16 || d % 8 != 0 || p % 8 != 0 || k < 1) return false;
+  // rows of X_i P from rows of X_i (p narrow), or per-tile parts of it (d
+  // narrow: the tile's rows and P's rows in shared memory next to the ring)
+  return (p <= 64 && k <= 256) || (d <= 32 && p > 64 && k <= 128);
 }
 
 int64_t narrow_partials(int64_t B, int64_t d, int64_t p) {
@@ -376,39 +570,53 @@ int64_t narrow_partials(int64_t B, int64_t d, int64_t p) {
   return B * ((wide + kNwM - 1) / kNwM);
 }
 
+size_t narrow_hutch_scratch_bytes(int64_t B, int64_t d, int64_t p, int64_t k) {
+  const bool swap = d <= 64 && p > 64;
+  const int64_t per = swap ? d * k : 1;  // floats per tile
+  return static_cast<size_t>(narrow_partials(B, d, p) * per) * 4;
+}
+
 cudaError_t launch_narrow_norm(const void* A, const void* G, int64_t B, int64_t T, int64_t d,
-                               int64_t p, float* partials, float* n_out, int accumulate,
-                               cudaStream_t s) {
+                               int64_t p, int* tickets, float* partials, float* n_out,
+                               int accumulate, cudaStream_t s) {
   CUtensorMap mw, mn;
   NwArgs a;
   int N = 16;
   if (!narrow_setup(A, G, B, T, d, p, mw, mn, a, N)) return cudaErrorInvalidValue;
   a.partials = partials;
-  const cudaError_t e = launch_mode<kNwNorm, float>(N, mw, mn, a, 0, s);
-  if (e != cudaSuccess) return e;
-  return launch_partials_finish(partials, B, a.mt, n_out, accumulate, s);
+  a.tickets = tickets;
+  a.n_out = n_out;
+  a.accumulate = accumulate;
+  return launch_mode<kNwNorm, float>(N, mw, mn, a, 0, s);
 }
 
 cudaError_t launch_narrow_hutch(const void* A, const void* G, const void* P, int64_t B,
                                 int64_t T, int64_t d, int64_t p, int64_t k, float scale,
-                                uint64_t seed, uint64_t step, float* partials, float* n_out,
-                                int accumulate, cudaStream_t s) {
-  if (p > 64 || k < 1 || k > 256) return cudaErrorInvalidValue;
+                                uint64_t seed, uint64_t step, int* tickets, float* partials,
+                                float* n_out, int accumulate, cudaStream_t s) {
+  if (!narrow_proj_supported(DPRC_BF16, d, p, k)) return cudaErrorInvalidValue;
   CUtensorMap mw, mn;
   NwArgs a;
   int N = 16;
   if (!narrow_setup(A, G, B, T, d, p, mw, mn, a, N)) return cudaErrorInvalidValue;
-  a.partials = partials;
   a.P = P;
   a.k = static_cast<int>(k);
   a.kp = static_cast<int>((k + 15) / 16 * 16);
   a.scale = scale;
   a.seed = seed;
   a.step = step;
-  const int proj_bytes = static_cast<int>(p * a.kp * 2);
-  const cudaError_t e = launch_mode<kNwProj, __nv_bfloat16>(N, mw, mn, a, proj_bytes, s);
-  if (e != cudaSuccess) return e;
-  return launch_partials_finish(partials, B, a.mt, n_out, accumulate, s);
+  a.tickets = tickets;
+  a.n_out = n_out;
+  a.accumulate = accumulate;
+  if (p <= 64) {
+    a.partials = partials;
+    const int proj_bytes = static_cast<int>(p * a.kp * 2);
+    return launch_mode<kNwProj, __nv_bfloat16>(N, mw, mn, a, proj_bytes, s);
+  }
+  // d narrow: per-tile parts of X_i P (scratch: narrow_hutch_scratch_bytes)
+  a.ypart = partials;
+  const int proj_bytes = kNwM * (N + 1) * 4 + kNwM * a.kp * 2;
+  return launch_mode<kNwProjT, __nv_bfloat16>(N, mw, mn, a, proj_bytes, s);
 }
 
 }  // namespace dprc

@@ -130,8 +130,8 @@ def test_norm_hutch_clip_zeroes_a_nonfinite_sample():
 
 # Narrow layers (a width <= 64): X_i = A_i^T G_i in one tensor-core pass; the
 # exact norm for both orientations (the wide operand A or G), the estimate
-# ||X_i P||^2 from the rows of X_i when p <= 64 (d-narrow maps take the
-# sketch path).  Both widths narrow, narrow widths padded to 16, 32 and 64
+# ||X_i P||^2 from the rows of X_i when p <= 64, from per-tile parts of X_i P
+# when d <= 32 < p and k <= 128 (other d-narrow maps take the sketch path).  Both widths narrow, narrow widths padded to 16, 32 and 64
 # columns, ragged T, k from 8 to 256 (P up to 64 x 256 in shared memory).
 NARROW_SHAPES = [
     (3, 1000, 2048, 16, 32),   # adapter down map: p narrow
@@ -142,6 +142,8 @@ NARROW_SHAPES = [
     (4, 300, 64, 64, 256),     # both narrow; P 64 x 256 in shared memory
     (1, 640, 32, 16, 128),     # both narrow, d > p
     (5, 257, 1024, 64, 32),
+    (2, 333, 32, 520, 128),    # d narrow: a 128 x 128 P tile per 128 p rows; last tile 8 rows
+    (3, 200, 8, 4096, 24),     # d narrow, k not a multiple of 16
 ]
 
 
@@ -238,10 +240,11 @@ def test_launch_count_query_matches_the_path():
     # fp32 or widths that are not multiples of 8: the CUDA-core path
     assert rnc.dprc_norm_hutch_launches(DPRC_F32, 4, 128, 64, 64, 8) == 3
     assert rnc.dprc_norm_hutch_launches(DPRC_BF16, 2, 100, 97, 64, 32) == 3
-    # p <= 64: X = A^T G formed in one pass with its rows times P, then the
-    # per-sample sum of the tile partials
-    assert rnc.dprc_norm_hutch_launches(DPRC_BF16, 8, 4096, 2048, 16, 32) == 2
-    assert rnc.dprc_norm_hutch_launches(DPRC_BF16, 8, 4096, 64, 48, 256) == 2
+    # a width <= 64: X = A^T G formed in one pass, times P in the epilogue, the
+    # per-sample sum by the CTA that completes the sample's last tile
+    assert rnc.dprc_norm_hutch_launches(DPRC_BF16, 8, 4096, 2048, 16, 32) == 1
+    assert rnc.dprc_norm_hutch_launches(DPRC_BF16, 8, 4096, 64, 48, 256) == 1
+    assert rnc.dprc_norm_hutch_launches(DPRC_BF16, 8, 4096, 16, 2048, 32) == 1
 
 
 def test_hutch_identity_projection_gives_exact_norm():
@@ -571,7 +574,8 @@ def test_hutch_layers_repeats_bitwise_and_reuses_its_workspace():
     (3, 77, 30, 17, 8, torch.float32),        # fp32: CUDA cores
     (2, 90, 37, 45, 24, torch.bfloat16),      # odd widths: CUDA cores
     (4, 1000, 2048, 16, 32, torch.bfloat16),  # adapter down map: X = A^T G, then X S
-    (4, 1000, 16, 2048, 32, torch.bfloat16),  # adapter up map, d narrow
+    (4, 1000, 16, 2048, 32, torch.bfloat16),  # adapter up map, d narrow: signs per P tile
+    (2, 300, 8, 1000, 16, torch.bfloat16),    # d narrow, ragged last tile
 ])
 def test_pm1_projection_matches_oracle(B, T, d, p, k, dtype):
     A = _rand((B, T, d), 500 + T, dtype)
