@@ -144,6 +144,8 @@ NARROW_SHAPES = [
     (5, 257, 1024, 64, 32),
     (2, 333, 32, 520, 128),    # d narrow: a 128 x 128 P tile per 128 p rows; last tile 8 rows
     (3, 200, 8, 4096, 24),     # d narrow, k not a multiple of 16
+    (20, 64, 2048, 16, 32),    # 320 tiles: several per CTA (double-buffered accumulator)
+    (20, 64, 16, 2048, 32),    # the same, d narrow (P tile restaged per tile)
 ]
 
 
@@ -341,7 +343,8 @@ def test_exact_norm_full_size_samples():
 EXACT_FORMS = [rnc.DPRC_EXACT_DIRECT, rnc.DPRC_EXACT_GHOST_N128, rnc.DPRC_EXACT_GHOST_N256]
 EXACT_FORM_SHAPES = [(1, 1, 8, 8), (2, 100, 64, 72), (2, 129, 96, 40), (3, 257, 200, 136),
                      (2, 384, 64, 64), (2, 1000, 392, 600), (1, 2048, 128, 256),
-                     (4, 640, 2048, 16), (4, 640, 16, 2048)]
+                     (4, 640, 2048, 16), (4, 640, 16, 2048),
+                     (2, 8192, 72, 64)]  # 64 blocks: 1056 ghost units per sample in the queue
 
 
 @pytest.mark.parametrize("form", EXACT_FORMS)
