@@ -362,6 +362,27 @@ __global__ void __launch_bounds__(hutch_threads<PM1>(), 1)
     fence_mbar_init();
     *abort_flag = 0;
   }
+  // The producer (thread 0, which initialised the barriers) issues the first
+  // ring slots of its first sketch block before the CTA barrier, so their
+  // DRAM round trip overlaps the TMEM allocation and the barrier.
+  int pre = 0;
+  if (threadIdx.x == 0) {
+    const LayerDesc& L0 = a.layer[0];
+    const Mine m1 = mine(L0.ph1, cl, rank);
+    if (count_blocks(L0.ph1, m1) > 0) {
+      const long long b = m1.first;
+      const int i = static_cast<int>(b / a.mtiles);
+      const int t0 = static_cast<int>(b - static_cast<long long>(i) * a.mtiles) * kTok;
+      for (int u = m1.ulo; u < m1.uhi && pre < kStages; ++u, ++pre) {
+        uint8_t* slot = ring + pre * Cfg::kSlot;
+        mbar_arrive_expect_tx(&full[pre], PM1 ? Cfg::kRowG : Cfg::kRowStage);
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+          tma_load_3d(slot + h * Cfg::kRowGBox, &L0.mg, &full[pre], u * kCol + h * 64, t0, i);
+        if (!PM1) tma_load_3d(slot + Cfg::kRowG, &L0.mp, &full[pre], 0, u * kCol, 0);
+      }
+    }
+  }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&a.mw[0]);
     tma_prefetch_desc(&a.mw[1]);
@@ -410,6 +431,10 @@ __global__ void __launch_bounds__(hutch_threads<PM1>(), 1)
           const int i = static_cast<int>(b / a.mtiles);
           const int t0 = static_cast<int>(b - static_cast<long long>(i) * a.mtiles) * kTok;
           for (int u = m1.ulo; u < m1.uhi; ++u) {
+            if (it < pre) {  // issued before the CTA barrier
+              ++it;
+              continue;
+            }
             const int s = take_slot(it);
             if (!ok) break;
             uint8_t* slot = ring + s * Cfg::kSlot;
