@@ -179,6 +179,19 @@ __global__ void __launch_bounds__(192, 1)
   const long long my_tiles =
       a.ntiles > blockIdx.x ? (a.ntiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
 
+  // stage u of the tile at (sample i, wide tile m) into ring slot s
+  auto load_stage = [&](int i, int m, int u, int s) {
+    uint8_t* st = ring + s * Cfg::kStage;
+    mbar_arrive_expect_tx(&full[s], Cfg::kStage);
+#pragma unroll
+    for (int h = 0; h < kNwM / 64; ++h)
+      tma_load_3d(st + h * kNwBox, &map_w, &full[s], m * kNwM + h * 64, u * kNwK, i);
+    tma_load_3d(st + kNwWide, &map_n, &full[s], 0, u * kNwK, i);
+  };
+  // the producer (thread 0) issues the first stages of its first tile right
+  // after initialising the barriers: their DRAM round trip overlaps the TMEM
+  // allocation and the CTA barrier
+  const int pre = my_tiles > 0 ? (nu < kNwStages ? nu : kNwStages) : 0;
   if (threadIdx.x == 0) {
     for (int s = 0; s < kNwStages; ++s) {
       mbar_init(&full[s], 1);
@@ -190,6 +203,9 @@ __global__ void __launch_bounds__(192, 1)
     }
     fence_mbar_init();
     *abort_flag = 0;
+    const int i0 = static_cast<int>(blockIdx.x / a.mt);
+    const int m0 = static_cast<int>(blockIdx.x - static_cast<long long>(i0) * a.mt);
+    for (int u = 0; u < pre; ++u) load_stage(i0, m0, u, u);
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&map_w);
@@ -213,6 +229,7 @@ __global__ void __launch_bounds__(192, 1)
         const int i = static_cast<int>(tile / a.mt);
         const int m = static_cast<int>(tile - static_cast<long long>(i) * a.mt);
         for (int u = 0; u < nu; ++u, ++it) {
+          if (it < pre) continue;  // issued before the CTA barrier
           const int s = static_cast<int>(it % kNwStages);
           const uint32_t ph = static_cast<uint32_t>(it / kNwStages) & 1;
           if (!mbar_wait(&empty[s], ph ^ 1, DPRC_DEVERR_PIPE_EMPTY)) {
@@ -220,12 +237,7 @@ __global__ void __launch_bounds__(192, 1)
             ok = false;
             break;
           }
-          uint8_t* st = ring + s * Cfg::kStage;
-          mbar_arrive_expect_tx(&full[s], Cfg::kStage);
-#pragma unroll
-          for (int h = 0; h < kNwM / 64; ++h)
-            tma_load_3d(st + h * kNwBox, &map_w, &full[s], m * kNwM + h * 64, u * kNwK, i);
-          tma_load_3d(st + kNwWide, &map_n, &full[s], 0, u * kNwK, i);
+          load_stage(i, m, u, s);
         }
       }
       // let the copies this thread issued land before the CTA can exit

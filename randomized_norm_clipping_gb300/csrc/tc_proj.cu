@@ -231,9 +231,24 @@ __global__ void __launch_bounds__(192, 2)
   xs.norms = reinterpret_cast<float*>(tmem_slot + 2);
   xs.recv = reinterpret_cast<float*>(smem + Cfg::kBase - 1024);
 
+  // the producer (thread 0) issues the first stages right after initialising
+  // the barriers, so their DRAM round trip overlaps the TMEM allocation and the
+  // CTA barrier
+  auto load_stage = [&](long long it, int s) {
+    const long long b = wk.b0 + it / nu;
+    const int kc = wk.ulo + static_cast<int>(it % nu);
+    const int i = static_cast<int>(b / a.mtiles);
+    const int t0 = static_cast<int>(b - static_cast<long long>(i) * a.mtiles) * kRowTile;
+    mbar_arrive_expect_tx(&full[s], Cfg::kStageBytes);
+    tma_load_3d(sx + s * Cfg::kXBytes, &map_x, &full[s], kc * kTileC, t0, i);
+    tma_load_3d(sr + s * Cfg::kRBytes, &map_r, &full[s], 0, kc * kTileC, a.r_batched ? i : 0);
+  };
+  const long long total_units = wk.b1 > wk.b0 ? (wk.b1 - wk.b0) * nu : 0;
+  const int pre = static_cast<int>(total_units < Cfg::kStages ? total_units : Cfg::kStages);
   if (threadIdx.x == 0) {
     init_barriers<Cfg::kStages>(full, empty, accf, acce, xs, sc.cl);
     *abort_flag = 0;
+    for (int it = 0; it < pre; ++it) load_stage(it, it);
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&map_x);
@@ -257,6 +272,7 @@ __global__ void __launch_bounds__(192, 2)
         const int i = static_cast<int>(b / a.mtiles);
         const int t0 = static_cast<int>(b - static_cast<long long>(i) * a.mtiles) * kRowTile;
         for (int kc = wk.ulo; kc < wk.uhi; ++kc, ++it) {
+          if (it < pre) continue;  // issued before the CTA barrier
           const int s = static_cast<int>(it % Cfg::kStages);
           const uint32_t ph = static_cast<uint32_t>(it / Cfg::kStages) & 1;
           if (!mbar_wait(&empty[s], ph ^ 1, DPRC_DEVERR_PIPE_EMPTY)) {
@@ -427,10 +443,33 @@ __global__ void __launch_bounds__(192, ColCfg<NMMA>::kCtasPerSm)
   xs.recv = reinterpret_cast<float*>(smem + Cfg::kBase - 1024);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long total = (wk.b1 - wk.b0) * nu;  // units of this CTA
+  auto unit = [&](long long it, int& i, int& ch, int& kt) {
+    const long long b = wk.b0 + it / nu;
+    kt = wk.ulo + static_cast<int>(it % nu);
+    i = static_cast<int>(b / a.nchunks);
+    ch = static_cast<int>(b - static_cast<long long>(i) * a.nchunks);
+  };
+  auto load_x = [&](long long it, int s) {
+    int i, ch, kt;
+    unit(it, i, ch, kt);
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+      tma_load_3d(sx + s * Cfg::kXBytes + h * Cfg::kXBoxBytes, &map_x, &full[s],
+                  ch * kColChunk + h * 64, kt * kTileT, i);
+  };
+  const int pre = static_cast<int>(total < Cfg::kStages ? total : Cfg::kStages);
 
   if (threadIdx.x == 0) {
     init_barriers<Cfg::kStages>(full, empty, accf, acce, xs, sc.cl);
     *abort_flag = 0;
+    // the producer (this thread) issues the X boxes of the first stages now:
+    // X does not depend on the previous kernel, and their DRAM round trip
+    // overlaps the TMEM allocation and the CTA barrier
+    for (int it = 0; it < pre; ++it) {
+      mbar_arrive_expect_tx(&full[it], Cfg::kStageBytes);
+      load_x(it, it);
+    }
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&map_x);
@@ -445,24 +484,9 @@ __global__ void __launch_bounds__(192, ColCfg<NMMA>::kCtasPerSm)
   if (sc.cl > 1) cluster_sync_all();  // peers' barriers exist before any remote arrive
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const long long total = (wk.b1 - wk.b0) * nu;  // units of this CTA
 
   if (warp == 0) {
     if (lane == 0 && total > 0) {
-      auto unit = [&](long long it, int& i, int& ch, int& kt) {
-        const long long b = wk.b0 + it / nu;
-        kt = wk.ulo + static_cast<int>(it % nu);
-        i = static_cast<int>(b / a.nchunks);
-        ch = static_cast<int>(b - static_cast<long long>(i) * a.nchunks);
-      };
-      auto load_x = [&](long long it, int s) {
-        int i, ch, kt;
-        unit(it, i, ch, kt);
-#pragma unroll
-        for (int h = 0; h < 2; ++h)
-          tma_load_3d(sx + s * Cfg::kXBytes + h * Cfg::kXBoxBytes, &map_x, &full[s],
-                      ch * kColChunk + h * 64, kt * kTileT, i);
-      };
       auto load_w = [&](long long it, int s) {
         int i, ch, kt;
         unit(it, i, ch, kt);
@@ -471,11 +495,6 @@ __global__ void __launch_bounds__(192, ColCfg<NMMA>::kCtasPerSm)
           tma_load_3d(sw + s * Cfg::kWBytes + h * Cfg::kWBoxBytes, &map_w, &full[s],
                       kt * kTileT + h * 64, 0, i);
       };
-      const int pre = static_cast<int>(total < Cfg::kStages ? total : Cfg::kStages);
-      for (int it = 0; it < pre; ++it) {
-        mbar_arrive_expect_tx(&full[it], Cfg::kStageBytes);
-        load_x(it, it);
-      }
       pdl_wait();  // the sketch is written by the previous kernel
       for (int it = 0; it < pre; ++it) load_w(it, it);
       long long issued = pre;
