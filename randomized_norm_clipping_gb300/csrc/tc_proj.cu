@@ -498,6 +498,11 @@ __global__ void __launch_bounds__(192, ColCfg<NMMA>::kCtasPerSm)
       pdl_wait();  // the sketch is written by the previous kernel
       for (int it = 0; it < pre; ++it) load_w(it, it);
       long long issued = pre;
+      // the unit of stage `it` by an incremental cursor (one division per
+      // block, none per stage: this thread paces the pipeline)
+      int ci, cch, ckt;
+      if (pre < total) unit(pre, ci, cch, ckt);
+      long long cb = wk.b0 + pre / nu;
       for (long long it = pre; it < total; ++it) {
         const int s = static_cast<int>(it % Cfg::kStages);
         const uint32_t ph = static_cast<uint32_t>(it / Cfg::kStages) & 1;
@@ -506,9 +511,21 @@ __global__ void __launch_bounds__(192, ColCfg<NMMA>::kCtasPerSm)
           break;
         }
         mbar_arrive_expect_tx(&full[s], Cfg::kStageBytes);
-        load_x(it, s);
-        load_w(it, s);
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+          tma_load_3d(sx + s * Cfg::kXBytes + h * Cfg::kXBoxBytes, &map_x, &full[s],
+                      cch * kColChunk + h * 64, ckt * kTileT, ci);
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+          tma_load_3d(sw + s * Cfg::kWBytes + h * Cfg::kWBoxBytes, &map_w, &full[s],
+                      ckt * kTileT + h * 64, 0, ci);
         ++issued;
+        if (++ckt == wk.uhi) {
+          ckt = wk.ulo;
+          ++cb;
+          ci = static_cast<int>(cb / a.nchunks);
+          cch = static_cast<int>(cb - static_cast<long long>(ci) * a.nchunks);
+        }
       }
       for (long long k = issued - 1; k >= 0 && k >= issued - Cfg::kStages; --k)
         mbar_wait(&full[k % Cfg::kStages], (k / Cfg::kStages) & 1, DPRC_DEVERR_PIPE_FULL);
