@@ -116,8 +116,8 @@ class RandomizedClippingStep:
                 out.append((S, P))
         return out
 
-    def _workspace(self, op, A, B, T, d, p):
-        need = rnc.dprc_workspace_bytes(op, rnc._dtype_code(A), B, T, d, p, self.k)
+    def _workspace(self, op, A, B, T, d, p, k):
+        need = rnc.dprc_workspace_bytes(op, rnc._dtype_code(A), B, T, d, p, k)
         key = (A.device, op)
         ws = self._ws.get(key)
         if ws is None or ws.numel() < need:
@@ -152,14 +152,14 @@ class RandomizedClippingStep:
             Bt, T, d = A.shape
             p = G.shape[-1]
             if self.method == "hutch":
-                ws = self._workspace(rnc.DPRC_OP_HUTCH, A, Bt, T, d, p)
+                ws = self._workspace(rnc.DPRC_OP_HUTCH, A, Bt, T, d, p, proj[j].shape[1])
                 if j == last:  # step 4's clip factors come with the last layer's norms
                     rnc.dprc_norm_hutch_clip(A, G, proj[j], n, self.C, c, accumulate=j > 0, ws=ws)
                 else:
                     rnc.dprc_norm_hutch(A, G, proj[j], n, accumulate=j > 0, ws=ws)
             else:
                 S, P = proj[j]
-                ws = self._workspace(rnc.DPRC_OP_HUTCHPP, A, Bt, T, d, p)
+                ws = self._workspace(rnc.DPRC_OP_HUTCHPP, A, Bt, T, d, p, S.shape[1])
                 rnc.dprc_norm_hutchpp(A, G, S, P, n, accumulate=j > 0, ws=ws)
         # step 4: clip factors (Hutch++: here) and the rescaled second backward
         if self.method != "hutch":

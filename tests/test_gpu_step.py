@@ -81,6 +81,99 @@ def test_identity_projection_reproduces_per_sample_clipping():
     step.close()
 
 
+class _Block(torch.nn.Module):
+    """A pre-norm transformer block: causal self-attention (q, k, v, o) and a
+    SiLU MLP (up, down), every projection a bias-free nn.Linear; the norms are
+    frozen (their per-sample norms are outside the method)."""
+
+    def __init__(self, dm=64, heads=4, hidden=128):
+        super().__init__()
+        self.heads = heads
+        self.n1 = torch.nn.LayerNorm(dm, elementwise_affine=False)
+        self.q = torch.nn.Linear(dm, dm, bias=False)
+        self.k = torch.nn.Linear(dm, dm, bias=False)
+        self.v = torch.nn.Linear(dm, dm, bias=False)
+        self.o = torch.nn.Linear(dm, dm, bias=False)
+        self.n2 = torch.nn.LayerNorm(dm, elementwise_affine=False)
+        self.up = torch.nn.Linear(dm, hidden, bias=False)
+        self.down = torch.nn.Linear(hidden, dm, bias=False)
+
+    def forward(self, x):
+        B, T, dm = x.shape
+        h = self.n1(x)
+        split = lambda t: t.view(B, T, self.heads, dm // self.heads).transpose(1, 2)  # noqa: E731
+        att = torch.nn.functional.scaled_dot_product_attention(
+            split(self.q(h)), split(self.k(h)), split(self.v(h)), is_causal=True)
+        x = x + self.o(att.transpose(1, 2).reshape(B, T, dm))
+        return x + self.down(torch.nn.functional.silu(self.up(self.n2(x))))
+
+
+@pytest.mark.gpu
+def test_transformer_block_step_reproduces_per_sample_clipping():
+    # with P = I for every layer the estimate is exact, so the step must equal
+    # per-sample clipping of the block's six projections computed by a loop
+    torch.manual_seed(3)
+    block = _Block().to(DEV)
+    x = torch.randn(4, 24, 64, device=DEV, generator=torch.Generator(DEV).manual_seed(4))
+    ws = [m.weight for m in (block.q, block.k, block.v, block.o, block.up, block.down)]
+
+    def losses(inp):
+        return (block(inp) ** 2).mean(dim=(1, 2))
+
+    norms, grads = [], []
+    for i in range(x.shape[0]):
+        gi = torch.autograd.grad(losses(x[i:i + 1]).sum(), ws)
+        norms.append(sum(float((g.double() ** 2).sum()) for g in gi))
+        grads.append([g.double() for g in gi])
+    n_ref = np.array(norms)
+    C = float(np.median(np.sqrt(n_ref)))
+    c_ref = np.minimum(1.0, C / np.sqrt(n_ref))
+    step = RandomizedClippingStep(block, C=C, sigma=0.0, k=64)
+    assert [m.weight for m in step.layers] == ws  # module order
+    eye = [torch.eye(m.out_features, device=DEV) for m in step.layers]
+    out = step(losses(x), step=0, projections=eye)
+    assert np.allclose(out["n"].cpu().numpy(), n_ref, rtol=1e-4)
+    assert np.allclose(out["c"].cpu().numpy(), c_ref, rtol=1e-4)
+    for j, w in enumerate(ws):
+        ref = sum(c_ref[i] * grads[i][j] for i in range(x.shape[0]))
+        assert torch.allclose(w.grad.double(), ref, rtol=1e-4, atol=1e-7 * float(ref.abs().max()))
+    step.close()
+
+
+@pytest.mark.gpu
+def test_bf16_transformer_block_step_matches_oracle():
+    # bf16 block: q, k, v, o, down (p = 64) take the narrow kernel, up (64 -> 128)
+    # the fused sketch kernel; the layer sum and clip factors against the oracle
+    # on the same activations, gradients and projections
+    torch.manual_seed(5)
+    block = _Block().to(DEV, torch.bfloat16)
+    x = torch.randn(3, 100, 64, device=DEV,
+                    generator=torch.Generator(DEV).manual_seed(6)).to(torch.bfloat16)
+
+    def losses(inp):
+        return (block(inp).float() ** 2).mean(dim=(1, 2))
+
+    step = RandomizedClippingStep(block, C=1.0, sigma=0.0, k=32, seed=2)
+    out = step(losses(x), step=11)
+    proj = step.projections(11)
+    acts, outs = [], []
+    hooks = [m.register_forward_hook(lambda mod, inp, o: (acts.append(inp[0]), outs.append(o))
+                                     and None) for m in step.layers]
+    loss = losses(x).sum()
+    for h in hooks:
+        h.remove()
+    gs = torch.autograd.grad(loss, outs)
+    ref = 0.0
+    for a_, g_, pr in zip(acts, gs, proj):
+        A = a_.detach().reshape(3, -1, a_.shape[-1])
+        G = g_.detach().reshape(3, -1, g_.shape[-1]).to(A.dtype)
+        ref = ref + oracle.hutch_norm(to_f64(A), to_f64(G), to_f64(pr))
+    got = out["n"].cpu().numpy().astype(np.float64)
+    assert np.max(np.abs(got - ref) / ref) < 1e-3
+    assert np.allclose(out["c"].cpu().numpy(), oracle.clip_factors(ref, 1.0), rtol=1e-3)
+    step.close()
+
+
 @pytest.mark.gpu
 @pytest.mark.parametrize("method,k", [("hutch", 32), ("hutchpp", 16)])
 def test_bf16_step_matches_oracle(method, k):
