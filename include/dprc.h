@@ -107,6 +107,9 @@ size_t dprc_workspace_bytes(dprc_op op, dprc_dtype dtype, int64_t B, int64_t T,
  *  n  device float [B]: n[i] = (accumulate ? n[i] : 0) + n_hat_i.
  *  Sizes: B >= 1, T >= 1, d >= 1, p >= 1, 1 <= k <= 256.
  *  Arithmetic: products and sums in fp32 (bf16 inputs are exact in fp32).
+ *  For bf16 layers with one width <= 64 (adapter maps: p <= 64, or d <= 32
+ *  with k <= 128) the small gradient X_i = A_i^T G_i is formed tile by tile in
+ *  one pass and n_hat_i = ||X_i P||_F^2, the same quantity up to rounding.
  *  All pointers 16-byte aligned.  The result is deterministic for fixed
  *  inputs, sizes and device.
  */
@@ -121,9 +124,10 @@ dprc_status dprc_norm_hutch(const void* A, const void* G, const void* P, dprc_dt
  * with the rule of dprc_clip_factors (n = 0 gives 1; a non-finite or
  * negative n gives 0 and is counted in *nonfinite, which may be NULL).  Use
  * it for the last layer of a step.  When dprc_norm_hutch_launches reports one
- * launch, the clip factors are written by that launch's finishing step (no
- * second kernel); otherwise the clip kernel follows on the same stream.  The
- * results equal dprc_norm_hutch then dprc_clip_factors bit for bit.
+ * launch, the clip factors are written by that launch's per-sample finishing
+ * step (no second kernel); otherwise the clip kernel follows on the same
+ * stream.  The results equal dprc_norm_hutch then dprc_clip_factors bit for
+ * bit.
  *  c device float [B], 16-byte aligned; C > 0 and finite.  Other arguments,
  *  the workspace and errors as dprc_norm_hutch.
  */
@@ -174,9 +178,9 @@ dprc_status dprc_norm_hutch_layers(int64_t L, const void* const* A, const void* 
 /*
  * Number of kernels one dprc_norm_hutch call with these arguments enqueues on
  * the current device: 1 (bf16, k = 16 or 32: sketch and projection as two
- * phases of one cooperative launch), 2 (other tensor-core shapes: a sketch
- * kernel and a projection kernel) or 3 (the CUDA-core path: sketch,
- * projection, reduction).  0 for arguments dprc_norm_hutch would reject or
+ * phases of one cooperative launch; or the one-pass kernel of a narrow
+ * layer), 2 (other tensor-core shapes: a sketch kernel and a projection
+ * kernel) or 3 (the CUDA-core path: sketch, projection, reduction).  0 for arguments dprc_norm_hutch would reject or
  * when no sm_103 device is current.  Enqueues nothing; for launch accounting
  * and graph builders.  No counterpart on the pages (a library property).
  */

@@ -444,12 +444,14 @@ dprc_status norm_hutch_impl(const void* A, const void* G, const void* P, dprc_dt
   mark(0, s);
   if (narrow_proj_supported(dtype, d, p, k)) {
     // a width <= 64: X_i = A_i^T G_i in one pass, times P in the epilogue
+    // (and the clip factors in the same launch)
     const cudaError_t e =
         launch_narrow_hutch(A, G, P, B, T, d, p, k, 1.0f, 0, 0, reinterpret_cast<int*>(w),
-                            reinterpret_cast<float*>(w + narrow_part_off(B)), n, accumulate, s);
+                            reinterpret_cast<float*>(w + narrow_part_off(B)), n, accumulate, s,
+                            clip);
     mark(1, s);
     mark(2, s);
-    return clip_after(e);
+    return cuda_status(e);
   }
   if (tc_path_supported(dtype, B, T, d, p, k, false) && fused_hutch_supported(k)) {
     // one launch: sketch and projection as two phases of one kernel (and the

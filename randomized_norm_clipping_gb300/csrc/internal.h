@@ -224,10 +224,12 @@ cudaError_t read_device_error_narrow(int32_t* out, bool reset);
 cudaError_t launch_narrow_norm(const void* A, const void* G, int64_t B, int64_t T, int64_t d,
                                int64_t p, int* tickets, float* partials, float* n_out,
                                int accumulate, cudaStream_t s);
+// clip: the clip factors of the final n_out, written in the same launch
 cudaError_t launch_narrow_hutch(const void* A, const void* G, const void* P, int64_t B,
                                 int64_t T, int64_t d, int64_t p, int64_t k, float scale,
                                 uint64_t seed, uint64_t step, int* tickets, float* partials,
-                                float* n_out, int accumulate, cudaStream_t s);
+                                float* n_out, int accumulate, cudaStream_t s,
+                                const ClipOut* clip = nullptr);
 // n_out[i] (+)= sum of partials[i * per_sample .. (i + 1) * per_sample), fixed order.
 cudaError_t launch_partials_finish(const float* partials, int64_t B, int64_t per_sample,
                                    float* n_out, int accumulate, cudaStream_t s);

@@ -79,6 +79,10 @@ struct NwArgs {
   int* tickets;         // [B]
   float* n_out;
   int accumulate;
+  // optional clip factors of the final n_out (c_out non-null)
+  float clip_C;
+  float* c_out;
+  int32_t* nonfinite;
 };
 
 // Copies `total` consecutive entries of a row-major [.][k] matrix into rows of
@@ -486,8 +490,14 @@ __global__ void __launch_bounds__(192, 1)
         named_bar_sync(1, 128);
         if (et == 0) {
           const float tot = (s_red[0] + s_red[1]) + (s_red[2] + s_red[3]);
-          a.n_out[is] = (a.accumulate ? a.n_out[is] : 0.f) + tot;
+          const float nv = (a.accumulate ? a.n_out[is] : 0.f) + tot;
+          a.n_out[is] = nv;
           a.tickets[is] = 0;
+          if (a.c_out != nullptr) {
+            bool bad;
+            a.c_out[is] = clip_factor(nv, a.clip_C, bad);
+            if (bad && a.nonfinite != nullptr) atomicAdd(a.nonfinite, 1);
+          }
         }
         named_bar_sync(1, 128);
       }
@@ -557,6 +567,9 @@ bool narrow_setup(const void* A, const void* G, int64_t B, int64_t T, int64_t d,
   a.tickets = nullptr;
   a.n_out = nullptr;
   a.accumulate = 0;
+  a.clip_C = 0.f;
+  a.c_out = nullptr;
+  a.nonfinite = nullptr;
   return true;
 }
 
@@ -605,7 +618,8 @@ cudaError_t launch_narrow_norm(const void* A, const void* G, int64_t B, int64_t 
 cudaError_t launch_narrow_hutch(const void* A, const void* G, const void* P, int64_t B,
                                 int64_t T, int64_t d, int64_t p, int64_t k, float scale,
                                 uint64_t seed, uint64_t step, int* tickets, float* partials,
-                                float* n_out, int accumulate, cudaStream_t s) {
+                                float* n_out, int accumulate, cudaStream_t s,
+                                const ClipOut* clip) {
   if (!narrow_proj_supported(DPRC_BF16, d, p, k)) return cudaErrorInvalidValue;
   CUtensorMap mw, mn;
   NwArgs a;
@@ -620,6 +634,11 @@ cudaError_t launch_narrow_hutch(const void* A, const void* G, const void* P, int
   a.tickets = tickets;
   a.n_out = n_out;
   a.accumulate = accumulate;
+  if (clip != nullptr) {
+    a.clip_C = clip->C;
+    a.c_out = clip->c;
+    a.nonfinite = clip->nonfinite;
+  }
   if (p <= 64) {
     a.partials = partials;
     const int proj_bytes = static_cast<int>(p * a.kp * 2);
