@@ -176,6 +176,23 @@ dprc_status dprc_norm_hutch_layers(int64_t L, const void* const* A, const void* 
                                    int accumulate, void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * dprc_norm_hutch_layers followed by the clip factors of the layer sum:
+ *     n[i] (+)= sum_l || A_l,i^T (G_l,i P_l) ||_F^2,   c[i] = min(1, C / sqrt(n[i]))
+ * (papernotes.org, "Method > Overall framework": the layerwise sum sets the
+ * clip factor), with the rule of dprc_clip_factors.  The launch that adds the
+ * last layer writes c in its per-sample finishing step; calls that take the
+ * layers one at a time end with the clip kernel.  Arguments, workspace and
+ * errors as dprc_norm_hutch_layers, plus C, c and nonfinite as
+ * dprc_norm_hutch_clip.
+ */
+dprc_status dprc_norm_hutch_layers_clip(int64_t L, const void* const* A, const void* const* G,
+                                        const void* const* P, const int64_t* d, const int64_t* p,
+                                        dprc_dtype dtype, int64_t B, int64_t T, int64_t k,
+                                        float* n, int accumulate, float C, float* c,
+                                        int32_t* nonfinite, void* ws, size_t ws_bytes,
+                                        void* stream);
+
+/*
  * Number of kernels one dprc_norm_hutch call with these arguments enqueues on
  * the current device: 1 (bf16, k = 16 or 32: sketch and projection as two
  * phases of one cooperative launch; or the one-pass kernel of a narrow

@@ -59,6 +59,10 @@ _PROTOS = [
      [_c.c_int64, _c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_int,
       _c.c_int64, _c.c_int64, _c.c_int64, _c.c_void_p, _c.c_int, _c.c_void_p, _c.c_size_t,
       _c.c_void_p]),
+    ("dprc_norm_hutch_layers_clip", _c.c_int,
+     [_c.c_int64, _c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_int,
+      _c.c_int64, _c.c_int64, _c.c_int64, _c.c_void_p, _c.c_int, _c.c_float, _c.c_void_p,
+      _c.c_void_p, _c.c_void_p, _c.c_size_t, _c.c_void_p]),
     ("dprc_norm_hutch_launches", _c.c_int,
      [_c.c_int, _c.c_int64, _c.c_int64, _c.c_int64, _c.c_int64, _c.c_int64]),
     ("dprc_exact_norm_form", _c.c_int,
@@ -192,8 +196,13 @@ def dprc_norm_hutch_pm1(A, G, k, seed, step, n, accumulate=False, ws=None, strea
     return n
 
 
-def dprc_norm_hutch_layers(As, Gs, Ps, n, accumulate=False, ws=None, stream=None):
-    """n[i] (+)= sum_l ||A_l,i^T (G_l,i P_l)||_F^2 over the layers (see include/dprc.h)."""
+def dprc_norm_hutch_layers(As, Gs, Ps, n, accumulate=False, ws=None, stream=None, C=None,
+                           c=None, nonfinite=None):
+    """n[i] (+)= sum_l ||A_l,i^T (G_l,i P_l)||_F^2 over the layers (see
+    include/dprc.h); with C and c also c[i] = min(1, C / sqrt(n[i])) of the sum
+    (dprc_norm_hutch_layers_clip)."""
+    if (C is None) != (c is None):
+        raise ValueError("give both C and c, or neither")
     L = len(As)
     if not (L == len(Gs) == len(Ps)) or L == 0:
         raise ValueError("As, Gs and Ps must be non-empty lists of the same length")
@@ -207,11 +216,19 @@ def dprc_norm_hutch_layers(As, Gs, Ps, n, accumulate=False, ws=None, stream=None
     pp = (ctypes.c_void_p * L)(*[_ptr(x) for x in Ps])
     if ws is None:
         ws = workspace(DPRC_OP_HUTCH_LAYERS, As[0], B, T, max(d), max(p), k)
-    st = lib().dprc_norm_hutch_layers(L, ap, gp, pp, d, p, _dtype_code(As[0]), B, T, k, _ptr(n),
-                                      int(bool(accumulate)), _ptr(ws), ws.numel(),
-                                      _stream(As[0], stream))
-    _check("dprc_norm_hutch_layers", st)
-    return n
+    if C is None:
+        st = lib().dprc_norm_hutch_layers(L, ap, gp, pp, d, p, _dtype_code(As[0]), B, T, k,
+                                          _ptr(n), int(bool(accumulate)), _ptr(ws), ws.numel(),
+                                          _stream(As[0], stream))
+        _check("dprc_norm_hutch_layers", st)
+        return n
+    _need_cuda(c, nonfinite)
+    st = lib().dprc_norm_hutch_layers_clip(L, ap, gp, pp, d, p, _dtype_code(As[0]), B, T, k,
+                                           _ptr(n), int(bool(accumulate)), float(C), _ptr(c),
+                                           _ptr(nonfinite) if nonfinite is not None else None,
+                                           _ptr(ws), ws.numel(), _stream(As[0], stream))
+    _check("dprc_norm_hutch_layers_clip", st)
+    return n, c
 
 
 def dprc_norm_hutch_launches(dtype_code, B, T, d, p, k):

@@ -473,6 +473,68 @@ dprc_status norm_hutch_impl(const void* A, const void* G, const void* P, dprc_dt
 }
 }  // namespace
 
+namespace {
+// dprc_norm_hutch_layers, with the clip factors of the final layer sum when
+// `clip` is set (in the launch that adds the last layer).
+dprc_status norm_hutch_layers_impl(int64_t L, const void* const* A, const void* const* G,
+                                   const void* const* P, const int64_t* d, const int64_t* p,
+                                   dprc_dtype dtype, int64_t B, int64_t T, int64_t k, float* n,
+                                   int accumulate, void* ws, size_t ws_bytes, void* stream,
+                                   const ClipOut* clip) {
+  if (!A || !G || !P || !d || !p || !n) return DPRC_ERR_NULL;
+  if (clip != nullptr) {
+    if (!clip->c) return DPRC_ERR_NULL;
+    if (!(clip->C > 0.f) || !(clip->C < __builtin_inff())) return DPRC_ERR_SHAPE;
+    if (!aligned16(clip->c)) return DPRC_ERR_ALIGN;
+  }
+  if (L < 1 || L > (int64_t(1) << 20)) return DPRC_ERR_SHAPE;
+  if (k < 1 || k > 256) return DPRC_ERR_SHAPE;
+  int64_t dmax = 0, pmax = 0;
+  bool fused = fused_hutch_supported(k);
+  for (int64_t l = 0; l < L; ++l) {
+    if (!A[l] || !G[l] || !P[l]) return DPRC_ERR_NULL;
+    const dprc_status st = check_common(dtype, B, T, d[l], p[l]);
+    if (st != DPRC_OK) return st;
+    if (!aligned16(A[l]) || !aligned16(G[l]) || !aligned16(P[l])) return DPRC_ERR_ALIGN;
+    dmax = std::max(dmax, d[l]);
+    pmax = std::max(pmax, p[l]);
+    fused = fused && tc_path_supported(dtype, B, T, d[l], p[l], k, false);
+  }
+  if (!aligned16(n)) return DPRC_ERR_ALIGN;
+  if (!ws) return DPRC_ERR_WORKSPACE;
+  if (!aligned16(ws)) return DPRC_ERR_ALIGN;
+  if (ws_bytes < dprc_workspace_bytes(DPRC_OP_HUTCH_LAYERS, dtype, B, T, dmax, pmax, k))
+    return DPRC_ERR_WORKSPACE;
+  if (!device_ok()) return DPRC_ERR_DEVICE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int64_t l0 = 0;
+  if (fused) {
+    const TcPlan t = plan_tc(DPRC_OP_HUTCH, B, T, dmax, pmax, k, kMaxFusedLayers);
+    const FusedScratch f = fused_scratch(t, static_cast<char*>(ws));
+    for (; l0 < L; l0 += kMaxFusedLayers) {
+      const int Lc = static_cast<int>(std::min<int64_t>(kMaxFusedLayers, L - l0));
+      bool launched = false;
+      const cudaError_t e = launch_tc_hutch_layers(Lc, A + l0, G + l0, P + l0, d + l0, p + l0, B,
+                                                   T, k, f, n, accumulate || l0 > 0, s,
+                                                   &launched, l0 + Lc == L ? clip : nullptr);
+      if (!launched) {
+        if (e != cudaSuccess) (void)cudaGetLastError();
+        break;  // the remaining layers one call at a time
+      }
+    }
+  }
+  for (int64_t l = l0; l < L; ++l) {
+    const dprc_status st = norm_hutch_impl(A[l], G[l], P[l], dtype, B, T, d[l], p[l], k, n,
+                                           accumulate || l > 0, ws, ws_bytes, stream,
+                                           l == L - 1 ? clip : nullptr);
+    if (st != DPRC_OK) return st;
+  }
+  return DPRC_OK;
+}
+}  // namespace
+
+
+
 extern "C" {
 
 int dprc_abi_version(void) { return DPRC_ABI_VERSION; }
@@ -508,10 +570,16 @@ size_t dprc_workspace_bytes(dprc_op op, dprc_dtype dtype, int64_t B, int64_t T, 
     case DPRC_OP_HUTCH_PM1:
       if (k < 1 || k > 256) return 0;
       return pm1_ws(dtype, B, T, d, p, k);
-    case DPRC_OP_HUTCH_LAYERS:
+    case DPRC_OP_HUTCH_LAYERS: {
       if (k < 1 || k > 256) return 0;
-      return std::max(hutch_ws(dtype, B, T, d, p, k),
-                      plan_tc(DPRC_OP_HUTCH, B, T, d, p, k, kMaxFusedLayers).total);
+      // any layer with widths up to (d, p), including narrow ones taken one
+      // call at a time
+      size_t w = std::max(hutch_ws(dtype, B, T, d, p, k),
+                          plan_tc(DPRC_OP_HUTCH, B, T, d, p, k, kMaxFusedLayers).total);
+      w = std::max(w, narrow_ws(B, std::min<int64_t>(d, 32), p, k));
+      w = std::max(w, narrow_ws(B, d, std::min<int64_t>(p, 64), k));
+      return w;
+    }
   }
   return 0;
 }
@@ -529,6 +597,28 @@ dprc_status dprc_norm_hutch(const void* A, const void* G, const void* P, dprc_dt
                             int accumulate, void* ws, size_t ws_bytes, void* stream) {
   return norm_hutch_impl(A, G, P, dtype, B, T, d, p, k, n, accumulate, ws, ws_bytes, stream,
                          nullptr);
+}
+
+dprc_status dprc_norm_hutch_layers(int64_t L, const void* const* A, const void* const* G,
+                                   const void* const* P, const int64_t* d, const int64_t* p,
+                                   dprc_dtype dtype, int64_t B, int64_t T, int64_t k, float* n,
+                                   int accumulate, void* ws, size_t ws_bytes, void* stream) {
+  return norm_hutch_layers_impl(L, A, G, P, d, p, dtype, B, T, k, n, accumulate, ws, ws_bytes,
+                                stream, nullptr);
+}
+
+dprc_status dprc_norm_hutch_layers_clip(int64_t L, const void* const* A, const void* const* G,
+                                        const void* const* P, const int64_t* d, const int64_t* p,
+                                        dprc_dtype dtype, int64_t B, int64_t T, int64_t k,
+                                        float* n, int accumulate, float C, float* c,
+                                        int32_t* nonfinite, void* ws, size_t ws_bytes,
+                                        void* stream) {
+  ClipOut clip;
+  clip.C = C;
+  clip.c = c;
+  clip.nonfinite = nonfinite;
+  return norm_hutch_layers_impl(L, A, G, P, d, p, dtype, B, T, k, n, accumulate, ws, ws_bytes,
+                                stream, &clip);
 }
 
 dprc_status dprc_norm_hutch_clip(const void* A, const void* G, const void* P, dprc_dtype dtype,
@@ -583,55 +673,6 @@ dprc_status dprc_norm_hutch_pm1(const void* A, const void* G, uint64_t seed, uin
   if (e != cudaSuccess) return DPRC_ERR_CUDA;
   return cuda_status(hutch_kernels(A, G, S, dtype, B, T, d, p, k, n, accumulate, w, 0,
                                    1.0f / static_cast<float>(k), s));
-}
-
-dprc_status dprc_norm_hutch_layers(int64_t L, const void* const* A, const void* const* G,
-                                   const void* const* P, const int64_t* d, const int64_t* p,
-                                   dprc_dtype dtype, int64_t B, int64_t T, int64_t k, float* n,
-                                   int accumulate, void* ws, size_t ws_bytes, void* stream) {
-  if (!A || !G || !P || !d || !p || !n) return DPRC_ERR_NULL;
-  if (L < 1 || L > (int64_t(1) << 20)) return DPRC_ERR_SHAPE;
-  if (k < 1 || k > 256) return DPRC_ERR_SHAPE;
-  int64_t dmax = 0, pmax = 0;
-  bool fused = fused_hutch_supported(k);
-  for (int64_t l = 0; l < L; ++l) {
-    if (!A[l] || !G[l] || !P[l]) return DPRC_ERR_NULL;
-    const dprc_status st = check_common(dtype, B, T, d[l], p[l]);
-    if (st != DPRC_OK) return st;
-    if (!aligned16(A[l]) || !aligned16(G[l]) || !aligned16(P[l])) return DPRC_ERR_ALIGN;
-    dmax = std::max(dmax, d[l]);
-    pmax = std::max(pmax, p[l]);
-    fused = fused && tc_path_supported(dtype, B, T, d[l], p[l], k, false);
-  }
-  if (!aligned16(n)) return DPRC_ERR_ALIGN;
-  if (!ws) return DPRC_ERR_WORKSPACE;
-  if (!aligned16(ws)) return DPRC_ERR_ALIGN;
-  if (ws_bytes < dprc_workspace_bytes(DPRC_OP_HUTCH_LAYERS, dtype, B, T, dmax, pmax, k))
-    return DPRC_ERR_WORKSPACE;
-  if (!device_ok()) return DPRC_ERR_DEVICE;
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  int64_t l0 = 0;
-  if (fused) {
-    const TcPlan t = plan_tc(DPRC_OP_HUTCH, B, T, dmax, pmax, k, kMaxFusedLayers);
-    const FusedScratch f = fused_scratch(t, static_cast<char*>(ws));
-    for (; l0 < L; l0 += kMaxFusedLayers) {
-      const int Lc = static_cast<int>(std::min<int64_t>(kMaxFusedLayers, L - l0));
-      bool launched = false;
-      const cudaError_t e = launch_tc_hutch_layers(Lc, A + l0, G + l0, P + l0, d + l0, p + l0, B,
-                                                   T, k, f, n, accumulate || l0 > 0, s,
-                                                   &launched);
-      if (!launched) {
-        if (e != cudaSuccess) (void)cudaGetLastError();
-        break;  // the remaining layers one call at a time
-      }
-    }
-  }
-  for (int64_t l = l0; l < L; ++l) {
-    const dprc_status st = dprc_norm_hutch(A[l], G[l], P[l], dtype, B, T, d[l], p[l], k, n,
-                                           accumulate || l > 0, ws, ws_bytes, stream);
-    if (st != DPRC_OK) return st;
-  }
-  return DPRC_OK;
 }
 
 int dprc_norm_hutch_launches(dprc_dtype dtype, int64_t B, int64_t T, int64_t d, int64_t p,

@@ -14,9 +14,10 @@
   5. Gaussian noise sigma C N(0, I) added to that aggregated gradient.
 
 `RandomizedClippingStep` does steps 2-5 around the caller's forward pass.
-Steps 3-5 run in libdprc (dprc_norm_hutch or dprc_norm_hutchpp with
-accumulation for the layer sum, the last Hutchinson layer through
-dprc_norm_hutch_clip, else dprc_clip_factors; dprc_add_noise); PyTorch
+Steps 3-5 run in libdprc (Hutchinson: every layer and the clip factors of
+the layer sum in one dprc_norm_hutch_layers_clip call; Hutch++: a
+dprc_norm_hutchpp call per layer with accumulation, then dprc_clip_factors;
+dprc_add_noise); PyTorch
 provides the forward and backward passes and the memory.  The first backward
 asks autograd only for the gradients with respect to the recorded layer
 outputs, so no weight gradient is formed before the clip factors are known.
@@ -116,6 +117,19 @@ class RandomizedClippingStep:
                 out.append((S, P))
         return out
 
+    def _layers_workspace(self, As, Gs, proj):
+        B, T = As[0].shape[0], As[0].shape[1]
+        k = max(P.shape[1] for P in proj)
+        need = rnc.dprc_workspace_bytes(rnc.DPRC_OP_HUTCH_LAYERS, rnc._dtype_code(As[0]), B, T,
+                                        max(A.shape[2] for A in As), max(G.shape[2] for G in Gs),
+                                        k)
+        key = (As[0].device, rnc.DPRC_OP_HUTCH_LAYERS)
+        ws = self._ws.get(key)
+        if ws is None or ws.numel() < need:
+            ws = torch.zeros(need, dtype=torch.uint8, device=As[0].device)  # zeroed once
+            self._ws[key] = ws
+        return ws
+
     def _workspace(self, op, A, B, T, d, p, k):
         need = rnc.dprc_workspace_bytes(op, rnc._dtype_code(A), B, T, d, p, k)
         key = (A.device, op)
@@ -143,24 +157,35 @@ class RandomizedClippingStep:
         # step 3: layerwise sum of the per-sample estimates
         n = torch.zeros(B, dtype=torch.float32, device=losses.device)
         c = torch.empty_like(n)
-        last = len(self.layers) - 1
-        for j, (m, G) in enumerate(zip(self.layers, grads)):
+        As, Gs = [], []
+        for m, G in zip(self.layers, grads):
             A = self._acts[m]
             # (B, ..., d): every position between batch and features is a token
-            A = A.detach().reshape(B, -1, A.shape[-1]).contiguous()
-            G = G.detach().reshape(B, -1, G.shape[-1]).to(A.dtype).contiguous()
-            Bt, T, d = A.shape
-            p = G.shape[-1]
-            if self.method == "hutch":
-                ws = self._workspace(rnc.DPRC_OP_HUTCH, A, Bt, T, d, p, proj[j].shape[1])
-                if j == last:  # step 4's clip factors come with the last layer's norms
-                    rnc.dprc_norm_hutch_clip(A, G, proj[j], n, self.C, c, accumulate=j > 0, ws=ws)
+            As.append(A.detach().reshape(B, -1, A.shape[-1]).contiguous())
+            Gs.append(G.detach().reshape(B, -1, G.shape[-1]).to(A.dtype).contiguous())
+        one_call = (self.method == "hutch" and len({A.shape[1] for A in As}) == 1
+                    and len({P.shape[1] for P in proj}) == 1 and len({A.dtype for A in As}) == 1)
+        if one_call:
+            # every layer in one call (persistent launches of up to 56 layers),
+            # the clip factors of the layer sum in the same call (step 4)
+            ws = self._layers_workspace(As, Gs, proj)
+            rnc.dprc_norm_hutch_layers(As, Gs, proj, n, ws=ws, C=self.C, c=c)
+        else:
+            last = len(self.layers) - 1
+            for j, (A, G) in enumerate(zip(As, Gs)):
+                Bt, T, d = A.shape
+                p = G.shape[-1]
+                if self.method == "hutch":
+                    ws = self._workspace(rnc.DPRC_OP_HUTCH, A, Bt, T, d, p, proj[j].shape[1])
+                    if j == last:  # step 4's clip factors come with the last layer's norms
+                        rnc.dprc_norm_hutch_clip(A, G, proj[j], n, self.C, c, accumulate=j > 0,
+                                                 ws=ws)
+                    else:
+                        rnc.dprc_norm_hutch(A, G, proj[j], n, accumulate=j > 0, ws=ws)
                 else:
-                    rnc.dprc_norm_hutch(A, G, proj[j], n, accumulate=j > 0, ws=ws)
-            else:
-                S, P = proj[j]
-                ws = self._workspace(rnc.DPRC_OP_HUTCHPP, A, Bt, T, d, p, S.shape[1])
-                rnc.dprc_norm_hutchpp(A, G, S, P, n, accumulate=j > 0, ws=ws)
+                    S, P = proj[j]
+                    ws = self._workspace(rnc.DPRC_OP_HUTCHPP, A, Bt, T, d, p, S.shape[1])
+                    rnc.dprc_norm_hutchpp(A, G, S, P, n, accumulate=j > 0, ws=ws)
         # step 4: clip factors (Hutch++: here) and the rescaled second backward
         if self.method != "hutch":
             rnc.dprc_clip_factors(n, self.C, c)

@@ -128,6 +128,29 @@ def test_norm_hutch_clip_zeroes_a_nonfinite_sample():
     assert _relerr(c[[0, 2]].cpu(), oracle.clip_factors(ref, 1.0)) < RTOL
 
 
+@pytest.mark.parametrize("shapes,B,T,k", [
+    ([(128, 64), (64, 128)] * 31, 2, 130, 16),        # 62 layers: two launches, clip in the second
+    ([(256, 256), (256, 512), (512, 256)], 3, 200, 64),  # k = 64: one call per layer, then the clip
+])
+def test_norm_hutch_layers_clip_equals_layers_then_clip(shapes, B, T, k):
+    As, Gs, Ps = [], [], []
+    for j, (d, p) in enumerate(shapes):
+        A, G, P = _hutch_case(B, T, d, p, k, torch.bfloat16, seed=900 + 3 * j)
+        As.append(A.to(DEV))
+        Gs.append(G.to(DEV))
+        Ps.append(P.to(DEV))
+    n1 = torch.zeros(B, device=DEV)
+    c1 = torch.empty(B, device=DEV)
+    rnc.dprc_norm_hutch_layers(As, Gs, Ps, n1)
+    C = float(torch.sqrt(n1).median())
+    rnc.dprc_clip_factors(n1, C, c1)
+    n2 = torch.zeros(B, device=DEV)
+    c2 = torch.empty(B, device=DEV)
+    rnc.dprc_norm_hutch_layers(As, Gs, Ps, n2, C=C, c=c2)
+    assert torch.equal(n1, n2) and torch.equal(c1, c2)
+    assert float(c2.min()) < 1.0 <= float(c2.max())  # both branches
+
+
 # Narrow layers (a width <= 64): X_i = A_i^T G_i in one tensor-core pass; the
 # exact norm for both orientations (the wide operand A or G), the estimate
 # ||X_i P||^2 from the rows of X_i when p <= 64, from per-tile parts of X_i P
