@@ -78,7 +78,8 @@ typedef enum {
     DPRC_OP_HUTCHPP = 2,
     DPRC_OP_EXACT = 3,
     DPRC_OP_HUTCH_LAYERS = 4,
-    DPRC_OP_HUTCH_PM1 = 5
+    DPRC_OP_HUTCH_PM1 = 5,
+    DPRC_OP_HUTCH_HOST = 6   /* the stage buffer of dprc_norm_hutch_clip_host */
 } dprc_op;
 
 /* Version of this ABI (DPRC_ABI_VERSION of the built library). */
@@ -135,6 +136,36 @@ dprc_status dprc_norm_hutch_clip(const void* A, const void* G, const void* P, dp
                                  int64_t B, int64_t T, int64_t d, int64_t p, int64_t k,
                                  float* n, int accumulate, float C, float* c,
                                  int32_t* nonfinite, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * dprc_norm_hutch_clip (accumulate = 0) for inputs that are in HOST memory,
+ * with the results written back to host memory: the whole per-sample norm and
+ * clip step of one layer, from the host's tensors to the host's clip factors.
+ *     n[i] = || A_i^T (G_i P) ||_F^2,   c[i] = min(1, C / sqrt(n[i]))
+ *  A host [B][T][d], G host [B][T][p], P host [p][k], all `dtype`; n, c host
+ *  float [B]; n may be NULL (the norms are then not copied back).  Use
+ *  page-locked (pinned) host memory: the copies are then asynchronous and run
+ *  at the host link's rate; pageable memory works, but its copies block the
+ *  calling thread.
+ *  The samples go to the device in chunks (the fewest samples that make at
+ *  least 64 MB of A and G) on two internal copy streams (A and G side by
+ *  side), through two slots of the stage buffer; each chunk's norms and clip
+ *  factors are computed on `stream` as soon as its copies have landed, while
+ *  the next chunk is copied, so only the last chunk's kernels do not hide
+ *  under a copy.  n and c are copied back at the end, on
+ *  `stream`: they are valid once `stream` reaches that point (synchronise it
+ *  before reading them).  The per-sample results equal dprc_norm_hutch_clip
+ *  on the device copies of a chunk bit for bit.
+ *  stage: device buffer of dprc_workspace_bytes(DPRC_OP_HUTCH_HOST, dtype, B,
+ *  T, d, p, k) bytes, 16-byte aligned; zero it once before its first use (it
+ *  holds a workspace).  One call at a time may use a stage buffer.
+ *  C > 0 and finite.  Errors as dprc_norm_hutch; a failed copy returns
+ *  DPRC_ERR_CUDA.  No counterpart on the pages (the host side of one step).
+ */
+dprc_status dprc_norm_hutch_clip_host(const void* A, const void* G, const void* P,
+                                      dprc_dtype dtype, int64_t B, int64_t T, int64_t d,
+                                      int64_t p, int64_t k, float C, float* n, float* c,
+                                      void* stage, size_t stage_bytes, void* stream);
 
 /*
  * Hutchinson estimate with a +-1 projection generated from a seed (the {-1, +1}

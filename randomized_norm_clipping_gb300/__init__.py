@@ -17,6 +17,7 @@ from .binding import (  # noqa: F401
     DPRC_F32,
     DPRC_OP_EXACT,
     DPRC_OP_HUTCH,
+    DPRC_OP_HUTCH_HOST,
     DPRC_OP_HUTCH_LAYERS,
     DPRC_OP_HUTCH_PM1,
     DPRC_OP_HUTCHPP,
@@ -30,6 +31,7 @@ from .binding import (  # noqa: F401
     dprc_exact_norm_plan,
     dprc_norm_hutch,
     dprc_norm_hutch_clip,
+    dprc_norm_hutch_clip_host,
     dprc_norm_hutch_launches,
     dprc_norm_hutch_layers,
     dprc_norm_hutch_pm1,
@@ -38,6 +40,7 @@ from .binding import (  # noqa: F401
     dprc_philox_words,
     dprc_set_phase_events,
     dprc_workspace_bytes,
+    host_stage,
     lib,
     workspace,
 )

@@ -19,8 +19,8 @@ PKG_DIR = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG_DIR, "libdprc.so")
 
 DPRC_F32, DPRC_BF16 = 0, 1
-DPRC_OP_HUTCH, DPRC_OP_HUTCHPP, DPRC_OP_EXACT, DPRC_OP_HUTCH_LAYERS, DPRC_OP_HUTCH_PM1 = (
-    1, 2, 3, 4, 5)
+(DPRC_OP_HUTCH, DPRC_OP_HUTCHPP, DPRC_OP_EXACT, DPRC_OP_HUTCH_LAYERS, DPRC_OP_HUTCH_PM1,
+ DPRC_OP_HUTCH_HOST) = (1, 2, 3, 4, 5, 6)
 (DPRC_EXACT_AUTO, DPRC_EXACT_DIRECT, DPRC_EXACT_GHOST, DPRC_EXACT_GHOST_N128,
  DPRC_EXACT_GHOST_N256) = (0, 1, 2, 3, 4)
 STATUS = {0: "ok", 1: "null pointer", 2: "shape", 3: "dtype", 4: "alignment",
@@ -70,6 +70,10 @@ _PROTOS = [
       _c.c_int, _c.c_void_p, _c.c_int, _c.c_void_p, _c.c_size_t, _c.c_void_p]),
     ("dprc_exact_norm_plan", _c.c_int,
      [_c.c_int, _c.c_int64, _c.c_int64, _c.c_int64, _c.c_int64, _c.c_int]),
+    ("dprc_norm_hutch_clip_host", _c.c_int,
+     [_c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_int, _c.c_int64, _c.c_int64, _c.c_int64,
+      _c.c_int64, _c.c_int64, _c.c_float, _c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_size_t,
+      _c.c_void_p]),
     ("dprc_norm_hutch_clip", _c.c_int,
      [_c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_int, _c.c_int64, _c.c_int64, _c.c_int64,
       _c.c_int64, _c.c_int64, _c.c_void_p, _c.c_int, _c.c_float, _c.c_void_p, _c.c_void_p,
@@ -177,6 +181,41 @@ def dprc_norm_hutch_clip(A, G, P, n, C, c, accumulate=False, nonfinite=None, ws=
                                     _ptr(nonfinite) if nonfinite is not None else None,
                                     _ptr(ws), ws.numel(), _stream(A, stream))
     _check("dprc_norm_hutch_clip", st)
+    return n, c
+
+
+def host_stage(A, T, d, p, k, B=None, device=None):
+    """A zeroed device stage buffer for dprc_norm_hutch_clip_host with the
+    sizes of host tensor A ([B][T][d]) and P [p][k]."""
+    B = A.shape[0] if B is None else B
+    n = dprc_workspace_bytes(DPRC_OP_HUTCH_HOST, _dtype_code(A), B, T, d, p, k)
+    if n == 0:
+        raise DprcError("dprc_workspace_bytes", 2)
+    return torch.zeros(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def dprc_norm_hutch_clip_host(A, G, P, C, n, c, stage=None, stream=None):
+    """Host tensors A [B][T][d], G [B][T][p], P [p][k] (pinned for asynchronous
+    copies) -> host float32 n, c [B]: n[i] = ||A_i^T (G_i P)||_F^2 and
+    c[i] = min(1, C / sqrt(n[i])), copied back at the end of the work enqueued
+    on the stream (see include/dprc.h); n may be None.  Synchronise the
+    stream before reading n and c."""
+    ts = [t for t in (A, G, P, n, c) if t is not None]
+    for t in ts:
+        if t.is_cuda:
+            raise ValueError("dprc_norm_hutch_clip_host takes host tensors")
+        if not t.is_contiguous():
+            raise ValueError("host tensors must be contiguous")
+    if (n is not None and n.dtype != torch.float32) or c.dtype != torch.float32:
+        raise ValueError("n and c must be float32")
+    B, T, d = A.shape
+    p, k = P.shape
+    if stage is None:
+        stage = host_stage(A, T, d, p, k)
+    st = lib().dprc_norm_hutch_clip_host(_ptr(A), _ptr(G), _ptr(P), _dtype_code(A), B, T, d, p, k,
+                                         float(C), _ptr(n), _ptr(c), _ptr(stage), stage.numel(),
+                                         _stream(stage, stream))
+    _check("dprc_norm_hutch_clip_host", st)
     return n, c
 
 

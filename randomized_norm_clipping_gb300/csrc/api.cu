@@ -13,6 +13,7 @@
 
 #include <algorithm>
 #include <atomic>
+#include <mutex>
 
 #include "dprc.h"
 #include "internal.h"
@@ -412,6 +413,63 @@ size_t pm1_ws(dprc_dtype dt, int64_t B, int64_t T, int64_t d, int64_t p, int64_t
          align_up(static_cast<size_t>(p) * k * (dt == DPRC_F32 ? 4 : 2), 1024);
 }
 
+// Device buffer of dprc_norm_hutch_clip_host: the workspace of one chunk's
+// call, the per-chunk n and c (16-byte aligned per chunk), P, and two slots
+// that each hold one chunk of samples of A and G.  A chunk is the fewest
+// samples that make at least 64 MB of A and G: fewer, larger copies keep the
+// host link busy (each copy costs a few microseconds of set-up), while the
+// kernel of the last chunk is all that does not hide under a copy.
+struct HostStage {
+  int64_t chunk = 0, nchunks = 0, pitch = 0;  // samples per chunk; n/c floats per chunk
+  size_t ws_off = 0, ws_bytes = 0, n_off = 0, c_off = 0, p_off = 0;
+  size_t slot_off[2] = {0, 0}, a_bytes = 0, g_bytes = 0, total = 0;
+};
+
+HostStage plan_host_stage(dprc_dtype dt, int64_t B, int64_t T, int64_t d, int64_t p, int64_t k) {
+  HostStage h;
+  const size_t eb = dt == DPRC_F32 ? 4 : 2;
+  const size_t sample = static_cast<size_t>(T) * (d + p) * eb;
+  const size_t want = size_t(64) << 20;
+  h.chunk = std::min<int64_t>(B, static_cast<int64_t>((want + sample - 1) / sample));
+  h.nchunks = (B + h.chunk - 1) / h.chunk;
+  h.pitch = (h.chunk + 3) / 4 * 4;
+  h.ws_bytes = hutch_ws(dt, h.chunk, T, d, p, k);
+  size_t off = 0;
+  h.ws_off = off;
+  off = align_up(off + h.ws_bytes, 1024);
+  h.n_off = off;
+  off = align_up(off + static_cast<size_t>(h.nchunks) * h.pitch * 4, 1024);
+  h.c_off = off;
+  off = align_up(off + static_cast<size_t>(h.nchunks) * h.pitch * 4, 1024);
+  h.p_off = off;
+  off = align_up(off + static_cast<size_t>(p) * k * eb, 1024);
+  h.a_bytes = static_cast<size_t>(h.chunk) * T * d * eb;
+  h.g_bytes = static_cast<size_t>(h.chunk) * T * p * eb;
+  for (int sl = 0; sl < 2; ++sl) {
+    h.slot_off[sl] = off;
+    off = align_up(off + align_up(h.a_bytes, 1024) + h.g_bytes, 1024);
+  }
+  h.total = off;
+  return h;
+}
+
+// Two copy streams per device for the host-input entry (A and G of a chunk
+// travel side by side, so one copy's set-up overlaps the other's transfer),
+// created on first use.
+constexpr int kMaxCopyDev = 64;
+cudaStream_t g_copy_stream[kMaxCopyDev][2];
+std::mutex g_copy_mu;
+
+cudaStream_t copy_stream(int which) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxCopyDev) return nullptr;
+  std::lock_guard<std::mutex> lock(g_copy_mu);
+  cudaStream_t& cs = g_copy_stream[dev][which];
+  if (cs == nullptr && cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking) != cudaSuccess)
+    cs = nullptr;
+  return cs;
+}
+
 }  // namespace
 
 namespace {
@@ -570,6 +628,9 @@ size_t dprc_workspace_bytes(dprc_op op, dprc_dtype dtype, int64_t B, int64_t T, 
     case DPRC_OP_HUTCH_PM1:
       if (k < 1 || k > 256) return 0;
       return pm1_ws(dtype, B, T, d, p, k);
+    case DPRC_OP_HUTCH_HOST:
+      if (k < 1 || k > 256) return 0;
+      return plan_host_stage(dtype, B, T, d, p, k).total;
     case DPRC_OP_HUTCH_LAYERS: {
       if (k < 1 || k > 256) return 0;
       // any layer with widths up to (d, p), including narrow ones taken one
@@ -631,6 +692,89 @@ dprc_status dprc_norm_hutch_clip(const void* A, const void* G, const void* P, dp
   clip.nonfinite = nonfinite;
   return norm_hutch_impl(A, G, P, dtype, B, T, d, p, k, n, accumulate, ws, ws_bytes, stream,
                          &clip);
+}
+
+dprc_status dprc_norm_hutch_clip_host(const void* A, const void* G, const void* P,
+                                      dprc_dtype dtype, int64_t B, int64_t T, int64_t d,
+                                      int64_t p, int64_t k, float C, float* n, float* c,
+                                      void* stage, size_t stage_bytes, void* stream) {
+  if (!A || !G || !P || !c) return DPRC_ERR_NULL;
+  dprc_status st = check_common(dtype, B, T, d, p);
+  if (st != DPRC_OK) return st;
+  if (k < 1 || k > 256) return DPRC_ERR_SHAPE;
+  if (!(C > 0.f) || !(C < __builtin_inff())) return DPRC_ERR_SHAPE;
+  if (!stage) return DPRC_ERR_WORKSPACE;
+  if (!aligned16(stage)) return DPRC_ERR_ALIGN;
+  const HostStage h = plan_host_stage(dtype, B, T, d, p, k);
+  if (stage_bytes < h.total) return DPRC_ERR_WORKSPACE;
+  if (!device_ok()) return DPRC_ERR_DEVICE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaStream_t cs[2] = {copy_stream(0), copy_stream(1)};
+  if (cs[0] == nullptr || cs[1] == nullptr) return DPRC_ERR_CUDA;
+  char* w = static_cast<char*>(stage);
+  const size_t eb = dtype == DPRC_F32 ? 4 : 2;
+  float* nd = reinterpret_cast<float*>(w + h.n_off);
+  float* cd = reinterpret_cast<float*>(w + h.c_off);
+  void* Pd = w + h.p_off;
+  // events: [0] start; per slot: A copied, G copied, slot free again
+  constexpr int kEv = 7;
+  cudaEvent_t ev[kEv] = {};
+  cudaError_t e = cudaSuccess;
+  for (int q = 0; q < kEv && e == cudaSuccess; ++q)
+    e = cudaEventCreateWithFlags(&ev[q], cudaEventDisableTiming);
+  cudaEvent_t start = ev[0];
+  auto copied = [&](int operand, int sl) { return ev[1 + 2 * sl + operand]; };
+  auto freed = [&](int sl) { return ev[5 + sl]; };
+  // the copies follow the work already on the caller's stream (which may use
+  // the stage buffer); chunk j's copies wait until the kernels of chunk j - 2
+  // are done with its slot; chunk j's kernels wait for both copies
+  if (e == cudaSuccess) e = cudaEventRecord(start, s);
+  for (int q = 0; q < 2 && e == cudaSuccess; ++q) e = cudaStreamWaitEvent(cs[q], start, 0);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(Pd, P, static_cast<size_t>(p) * k * eb, cudaMemcpyHostToDevice, cs[1]);
+  for (int64_t j = 0; j < h.nchunks && e == cudaSuccess && st == DPRC_OK; ++j) {
+    const int sl = static_cast<int>(j & 1);
+    const int64_t i0 = j * h.chunk;
+    const int64_t bc = std::min<int64_t>(h.chunk, B - i0);
+    char* Ad = w + h.slot_off[sl];
+    char* Gd = Ad + align_up(h.a_bytes, 1024);
+    for (int q = 0; q < 2 && e == cudaSuccess; ++q) {
+      const int64_t wq = q == 0 ? d : p;
+      if (j >= 2) e = cudaStreamWaitEvent(cs[q], freed(sl), 0);
+      if (e == cudaSuccess)
+        e = cudaMemcpyAsync(q == 0 ? Ad : Gd,
+                            static_cast<const char*>(q == 0 ? A : G) +
+                                static_cast<size_t>(i0) * T * wq * eb,
+                            static_cast<size_t>(bc) * T * wq * eb, cudaMemcpyHostToDevice, cs[q]);
+      if (e == cudaSuccess) e = cudaEventRecord(copied(q, sl), cs[q]);
+      if (e == cudaSuccess) e = cudaStreamWaitEvent(s, copied(q, sl), 0);
+    }
+    if (e != cudaSuccess) break;
+    ClipOut clip;
+    clip.C = C;
+    clip.c = cd + j * h.pitch;
+    st = norm_hutch_impl(Ad, Gd, Pd, dtype, bc, T, d, p, k, nd + j * h.pitch, 0, w + h.ws_off,
+                         h.ws_bytes, s, &clip);
+    if (st == DPRC_OK) e = cudaEventRecord(freed(sl), s);
+  }
+  // n and c back to the host: chunk j's values sit at j * pitch
+  const int64_t full = B / h.chunk, rest = B - full * h.chunk;
+  for (int q = n ? 0 : 1; q < 2 && e == cudaSuccess && st == DPRC_OK; ++q) {
+    float* dst = q == 0 ? n : c;
+    const float* src = q == 0 ? nd : cd;
+    if (full > 0)
+      e = cudaMemcpy2DAsync(dst, static_cast<size_t>(h.chunk) * 4, src,
+                            static_cast<size_t>(h.pitch) * 4, static_cast<size_t>(h.chunk) * 4,
+                            static_cast<size_t>(full), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess && rest > 0)
+      e = cudaMemcpyAsync(dst + full * h.chunk, src + full * h.pitch,
+                          static_cast<size_t>(rest) * 4, cudaMemcpyDeviceToHost, s);
+  }
+  // (events are released once the work recorded on them completes)
+  for (int q = 0; q < kEv; ++q)
+    if (ev[q]) cudaEventDestroy(ev[q]);
+  if (st != DPRC_OK) return st;
+  return cuda_status(e);
 }
 
 dprc_status dprc_norm_hutch_pm1(const void* A, const void* G, uint64_t seed, uint64_t step,

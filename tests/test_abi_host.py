@@ -68,7 +68,17 @@ def test_workspace_bytes_host_only(lib):
     assert b.dprc_workspace_bytes(b.DPRC_OP_EXACT, b.DPRC_BF16, 3, 1000, 64, 16, 0) >= 3 * 8 * 9 // 2 * 4
     assert b.dprc_workspace_bytes(b.DPRC_OP_EXACT, b.DPRC_F32, 2, 4096, 64, 64, 0) >= 2 * 128 * 128 * 4
     assert b.dprc_workspace_bytes(b.DPRC_OP_EXACT, b.DPRC_BF16, 2, 4096, 63, 64, 0) >= 2 * 128 * 128 * 4
+    # host-input stage: a chunk's workspace, P and two slots of a chunk each (two
+    # 33.5 MB samples make the 64 MB chunk)
+    hs = b.dprc_workspace_bytes(b.DPRC_OP_HUTCH_HOST, b.DPRC_BF16, 8, 4096, 2048, 2048, 32)
+    two = b.dprc_workspace_bytes(b.DPRC_OP_HUTCH, b.DPRC_BF16, 2, 4096, 2048, 2048, 32)
+    assert hs >= two + 2 * 2 * 4096 * 4096 * 2 + 2048 * 32 * 2
+    assert hs < two + 2 * 2 * 4096 * 4096 * 2 + (1 << 20)
+    # small samples go 4 (or a multiple of 4) to a chunk
+    assert (b.dprc_workspace_bytes(b.DPRC_OP_HUTCH_HOST, b.DPRC_BF16, 64, 128, 256, 256, 16)
+            >= 2 * 64 * 128 * 512 * 2)
     # invalid sizes give 0
+    assert b.dprc_workspace_bytes(b.DPRC_OP_HUTCH_HOST, b.DPRC_BF16, 8, 4096, 2048, 2048, 0) == 0
     assert b.dprc_workspace_bytes(b.DPRC_OP_HUTCH, b.DPRC_BF16, 0, 4096, 2048, 2048, 32) == 0
     assert b.dprc_workspace_bytes(b.DPRC_OP_HUTCH, b.DPRC_BF16, 1, 4096, 2048, 2048, 0) == 0
     assert b.dprc_workspace_bytes(b.DPRC_OP_HUTCH, b.DPRC_BF16, 1, 4096, 2048, 2048, 257) == 0
@@ -146,6 +156,22 @@ def test_argument_errors_return_before_device_work(lib):
     assert hl(2, ptrs, bad, ptrs, sizes, sizes, 1, 1, 1, 16, _vp(A16), 0, _vp(A16), ws, None) == 4
     assert hl(2, ptrs, ptrs, ptrs, I2(8, 0), sizes, 1, 1, 1, 16, _vp(A16), 0, _vp(A16), ws, None) == 2
     assert hl(2, ptrs, ptrs, ptrs, sizes, sizes, 1, 1, 1, 16, _vp(A16), 0, _vp(A16), 16, None) == 5
+    hh = lib.dprc_norm_hutch_clip_host
+    big = 1 << 40
+    assert hh(_vp(A16), None, _vp(A16), 1, 2, 64, 8, 8, 8, f32(1.0), _vp(A16), _vp(A16),
+              _vp(A16), big, None) == 1  # no G
+    assert hh(_vp(A16), _vp(A16), _vp(A16), 1, 2, 64, 8, 8, 8, f32(1.0), _vp(A16), None,
+              _vp(A16), big, None) == 1  # no c
+    assert hh(_vp(A16), _vp(A16), _vp(A16), 1, 2, 64, 8, 8, 0, f32(1.0), _vp(A16), _vp(A16),
+              _vp(A16), big, None) == 2  # k = 0
+    assert hh(_vp(A16), _vp(A16), _vp(A16), 1, 2, 64, 8, 8, 8, f32(float("inf")), _vp(A16),
+              _vp(A16), _vp(A16), big, None) == 2  # C not finite
+    assert hh(_vp(A16), _vp(A16), _vp(A16), 1, 2, 64, 8, 8, 8, f32(1.0), _vp(A16), _vp(A16),
+              _vp(A16 + 8), big, None) == 4  # misaligned stage
+    assert hh(_vp(A16), _vp(A16), _vp(A16), 1, 2, 64, 8, 8, 8, f32(1.0), _vp(A16), _vp(A16),
+              None, big, None) == 5  # no stage
+    assert hh(_vp(A16), _vp(A16), _vp(A16), 1, 2, 64, 8, 8, 8, f32(1.0), _vp(A16), _vp(A16),
+              _vp(A16), 1024, None) == 5  # stage too small
     w = lib.dprc_philox_words
     assert w(None, 4, 0, 1, 1, None) == 1
     assert w(None, 0, 0, 1, 1, None) == 0

@@ -272,6 +272,52 @@ def test_launch_count_query_matches_the_path():
     assert rnc.dprc_norm_hutch_launches(DPRC_BF16, 8, 4096, 16, 2048, 32) == 1
 
 
+def _host_chunk(B, T, d, p, esize):
+    # the chunk rule of dprc_norm_hutch_clip_host (include/dprc.h): the fewest
+    # samples that make at least 64 MB of A and G
+    sample = T * (d + p) * esize
+    return min(B, -(-(64 << 20) // sample))
+
+
+@pytest.mark.parametrize("B,T,d,p,k,dtype", [
+    (5, 4096, 2048, 2048, 32, torch.bfloat16),   # chunks of 2, 2 and 1: both slots reused
+    (40, 1024, 1024, 1024, 16, torch.bfloat16),  # chunks of 16, 16 and 8 samples
+    (5, 100, 40, 24, 8, torch.float32),          # one chunk
+])
+def test_norm_hutch_clip_host_matches_device_calls_and_oracle(B, T, d, p, k, dtype):
+    A = _rand((B, T, d), 60 + B, dtype)
+    G = _rand((B, T, p), 61 + B, dtype, 0.05)
+    P = _rand((p, k), 62 + B, dtype, k ** -0.5)
+    Ah, Gh, Ph = (x.pin_memory() for x in (A, G, P))
+    nh = torch.full((B,), -1.0).pin_memory()
+    ch = torch.full((B,), -1.0).pin_memory()
+    ref = oracle.hutch_norm(to_f64(A), to_f64(G), to_f64(P))
+    C = float(np.median(ref)) ** 0.5  # some samples clipped, some not
+    stage = rnc.host_stage(Ah, T, d, p, k)
+    rnc.dprc_norm_hutch_clip_host(Ah, Gh, Ph, C, nh, ch, stage=stage)
+    torch.cuda.synchronize()
+    assert _relerr(nh, ref) < (1e-5 if dtype == torch.float32 else RTOL)
+    # the same chunks through the device entry: bit for bit
+    step = _host_chunk(B, T, d, p, A.element_size())
+    nd = torch.empty(B)
+    cd = torch.empty(B)
+    for i0 in range(0, B, step):
+        sl = slice(i0, min(B, i0 + step))
+        m = sl.stop - sl.start
+        n1 = torch.zeros(m, device=DEV)
+        c1 = torch.empty(m, device=DEV)
+        rnc.dprc_norm_hutch_clip(A[sl].to(DEV), G[sl].to(DEV), P.to(DEV), n1, C, c1)
+        nd[sl], cd[sl] = n1.cpu(), c1.cpu()
+    assert torch.equal(nh, nd) and torch.equal(ch, cd)
+    assert (ch < 1).any() and (ch == 1).any()  # both branches of the clip rule
+    # a second call through the same stage buffer agrees; without n only c comes back
+    ch2 = torch.zeros(B).pin_memory()
+    rnc.dprc_norm_hutch_clip_host(Ah, Gh, Ph, C, None, ch2, stage=stage)
+    torch.cuda.synchronize()
+    assert torch.equal(ch, ch2)
+    assert rnc.dprc_device_error() == 0
+
+
 def test_hutch_identity_projection_gives_exact_norm():
     # P = I_p (k = p = 32) turns the estimate into the exact norm
     A, G, _ = _hutch_case(2, 300, 128, 32, 32, torch.bfloat16, seed=3)
