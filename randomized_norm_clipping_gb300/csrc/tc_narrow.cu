@@ -464,20 +464,32 @@ __global__ void __launch_bounds__(192, 1)
         __threadfence();
         float acc = 0.f;
         if (MODE == kNwProjT) {
+          // entry e of the sample's X_i P is the sum over its tiles m, in m
+          // order; four entries at a time, eight tiles per batch of loads, so
+          // 32 loads are in flight (this runs at the very end of the launch)
           const int dk = a.narrow * a.k;
           const float* yi = a.ypart + static_cast<size_t>(is) * a.mt * dk;
-          for (int e = et; e < dk; e += 128) {
-            float y = 0.f;
-            int m = 0;
-            for (; m + 8 <= a.mt; m += 8) {
-              float t[8];
+          for (int e0 = et; e0 < dk; e0 += 4 * 128) {
+            float y[4] = {0.f, 0.f, 0.f, 0.f};
+            for (int m = 0; m < a.mt; m += 8) {
+              float t[8][4];
 #pragma unroll
-              for (int u = 0; u < 8; ++u) t[u] = __ldcg(yi + static_cast<size_t>(m + u) * dk + e);
+              for (int u = 0; u < 8; ++u)
 #pragma unroll
-              for (int u = 0; u < 8; ++u) y += t[u];
+                for (int q2 = 0; q2 < 4; ++q2) {
+                  const int e = e0 + q2 * 128;
+                  t[u][q2] = (m + u < a.mt && e < dk)
+                                 ? __ldcg(yi + static_cast<size_t>(m + u) * dk + e)
+                                 : 0.f;
+                }
+#pragma unroll
+              for (int u = 0; u < 8; ++u)
+#pragma unroll
+                for (int q2 = 0; q2 < 4; ++q2)
+                  if (m + u < a.mt) y[q2] += t[u][q2];
             }
-            for (; m < a.mt; ++m) y += __ldcg(yi + static_cast<size_t>(m) * dk + e);
-            acc = fmaf(y, y, acc);
+#pragma unroll
+            for (int q2 = 0; q2 < 4; ++q2) acc = fmaf(y[q2], y[q2], acc);
           }
           acc *= a.scale;
         } else if (ew == 0) {
