@@ -120,6 +120,18 @@ __device__ __forceinline__ Mine mine(const Phase& ph, int cl, int rank) {
   return m;
 }
 
+// Sketch unit of the u-th stage of a block: the CTA's units [ulo, uhi) in an
+// order rotated by the CTA index, so that CTAs streaming at the same moment
+// read different 256-byte column ranges of their rows of G (a different
+// column range of a row lives in other HBM channels).  The sum over the
+// block's units is the same; only its order differs (fixed per CTA).
+__device__ __forceinline__ int rot_unit(const Mine& m, int u) {
+  const int n = m.uhi - m.ulo;
+  const int r = static_cast<int>(blockIdx.x % static_cast<unsigned>(n));
+  const int v = u - m.ulo + r;
+  return m.ulo + (v >= n ? v - n : v);
+}
+
 __device__ __forceinline__ long long count_blocks(const Phase& ph, const Mine& m) {
   return ph.nblocks > m.first ? (ph.nblocks - 1 - m.first) / m.step + 1 : 0;
 }
@@ -378,8 +390,9 @@ __global__ void __launch_bounds__(hutch_threads<PM1>(), 1)
         mbar_arrive_expect_tx(&full[pre], PM1 ? Cfg::kRowG : Cfg::kRowStage);
 #pragma unroll
         for (int h = 0; h < 2; ++h)
-          tma_load_3d(slot + h * Cfg::kRowGBox, &L0.mg, &full[pre], u * kCol + h * 64, t0, i);
-        if (!PM1) tma_load_3d(slot + Cfg::kRowG, &L0.mp, &full[pre], 0, u * kCol, 0);
+          tma_load_3d(slot + h * Cfg::kRowGBox, &L0.mg, &full[pre], rot_unit(m1, u) * kCol + h * 64,
+                      t0, i);
+        if (!PM1) tma_load_3d(slot + Cfg::kRowG, &L0.mp, &full[pre], 0, rot_unit(m1, u) * kCol, 0);
       }
     }
   }
@@ -442,8 +455,9 @@ __global__ void __launch_bounds__(hutch_threads<PM1>(), 1)
             mbar_arrive_expect_tx(&full[s], PM1 ? Cfg::kRowG : Cfg::kRowStage);
 #pragma unroll
             for (int h = 0; h < 2; ++h)
-              tma_load_3d(slot + h * Cfg::kRowGBox, &Ld.mg, &full[s], u * kCol + h * 64, t0, i);
-            if (!PM1) tma_load_3d(slot + Cfg::kRowG, &Ld.mp, &full[s], 0, u * kCol, 0);
+              tma_load_3d(slot + h * Cfg::kRowGBox, &Ld.mg, &full[s], rot_unit(m1, u) * kCol + h * 64,
+                          t0, i);
+            if (!PM1) tma_load_3d(slot + Cfg::kRowG, &Ld.mp, &full[s], 0, rot_unit(m1, u) * kCol, 0);
             ++it;
           }
         }
@@ -626,7 +640,8 @@ __global__ void __launch_bounds__(hutch_threads<PM1>(), 1)
                               DPRC_DEVERR_PIPE_EMPTY);
         ok = __shfl_sync(0xffffffffu, free_ok ? 1 : 0, 0) != 0 && *abort_flag == 0;
         if (!ok) break;
-        gen_sign_tile<K>(ring + s * Cfg::kSlot + Cfg::kRowG, u, lane, warp - 6, rk, a.step);
+        gen_sign_tile<K>(ring + s * Cfg::kSlot + Cfg::kRowG, rot_unit(m1, u), lane, warp - 6, rk,
+                         a.step);
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
         if (lane == 0) mbar_arrive(&full[s]);
