@@ -25,10 +25,12 @@
  *    `ws` (see dprc_workspace_bytes).  Zero a workspace once before its first
  *    use (e.g. cudaMemsetAsync): it starts with a block of per-sample
  *    counters that must read zero when a call begins.  Every call that ends
- *    without a device error (dprc_device_error) leaves that block zero again,
- *    so one workspace serves any sequence of calls of any sizes that fit it;
- *    after a device error, zero it again.  The rest of its contents are
- *    scratch.
+ *    without a device error (dprc_device_error) leaves that block zero again.
+ *    The block has one size for every B <= 256, so one workspace serves any
+ *    sequence of calls with B <= 256 and sizes that fit it.  Above 256 samples
+ *    the block grows with B: zero the workspace again before a call with
+ *    B > 256 unless the previous call on it had the same B.  After a device
+ *    error, zero it again.  The rest of its contents are scratch.
  *  - `stream` is a cudaStream_t passed as void*; NULL means the legacy default
  *    stream.  Calls only enqueue work and return; results are ready when the
  *    stream reaches them.  Calls on different streams may run concurrently
@@ -148,7 +150,7 @@ dprc_status dprc_norm_hutch_clip(const void* A, const void* G, const void* P, dp
  *  at the host link's rate; pageable memory works, but its copies block the
  *  calling thread.
  *  The samples go to the device in chunks (the fewest samples that make at
- *  least 64 MB of A and G) on two internal copy streams (A and G side by
+ *  least 128 MB of A and G) on two internal copy streams (A and G side by
  *  side), through two slots of the stage buffer; each chunk's norms and clip
  *  factors are computed on `stream` as soon as its copies have landed, while
  *  the next chunk is copied, so only the last chunk's kernels do not hide

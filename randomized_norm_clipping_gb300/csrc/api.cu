@@ -126,9 +126,14 @@ bool tc_path_supported(dprc_dtype dt, int64_t B, int64_t T, int64_t d, int64_t p
 // counters per (layer slot, sample), layers finished per sample, projection
 // blocks finished per layer slot, and one CTA-exit count.  Calls leave it
 // zeroed; the fused Hutchinson kernel relies on that, so no other buffer may
-// overlap it.
+// overlap it.  Where the counters sit inside the block depends on B, so the
+// block has one size for every B up to kCtrlFixedB: a call with fewer samples
+// must not place its scratch where a call with more keeps counters (one
+// workspace then serves calls with any B up to that bound).
+constexpr int64_t kCtrlFixedB = 256;
 size_t ctrl_bytes(int64_t B) {
-  const size_t ints = 2 * static_cast<size_t>(kMaxFusedLayers) * B + B + kMaxFusedLayers + 1;
+  const int64_t Bc = B > kCtrlFixedB ? B : kCtrlFixedB;
+  const size_t ints = 2 * static_cast<size_t>(kMaxFusedLayers) * Bc + Bc + kMaxFusedLayers + 1;
   return align_up(ints * 4, 256);
 }
 
@@ -416,12 +421,13 @@ size_t pm1_ws(dprc_dtype dt, int64_t B, int64_t T, int64_t d, int64_t p, int64_t
 // Device buffer of dprc_norm_hutch_clip_host: the workspace of one chunk's
 // call, the per-chunk n and c (16-byte aligned per chunk), P, and two slots
 // that each hold one chunk of samples of A and G.  A chunk is the fewest
-// samples that make at least 64 MB of A and G: fewer, larger copies keep the
+// samples that make at least 128 MB of A and G: fewer, larger copies keep the
 // host link busy (each copy costs a few microseconds of set-up), while the
 // kernel of the last chunk is all that does not hide under a copy.
 struct HostStage {
   int64_t chunk = 0, nchunks = 0, pitch = 0;  // samples per chunk; n/c floats per chunk
   size_t ws_off = 0, ws_bytes = 0, n_off = 0, c_off = 0, p_off = 0;
+  size_t rest_ws_off = 0, rest_ws_bytes = 0;  // the last chunk's own workspace when it is short
   size_t slot_off[2] = {0, 0}, a_bytes = 0, g_bytes = 0, total = 0;
 };
 
@@ -429,7 +435,7 @@ HostStage plan_host_stage(dprc_dtype dt, int64_t B, int64_t T, int64_t d, int64_
   HostStage h;
   const size_t eb = dt == DPRC_F32 ? 4 : 2;
   const size_t sample = static_cast<size_t>(T) * (d + p) * eb;
-  const size_t want = size_t(64) << 20;
+  const size_t want = size_t(128) << 20;
   h.chunk = std::min<int64_t>(B, static_cast<int64_t>((want + sample - 1) / sample));
   h.nchunks = (B + h.chunk - 1) / h.chunk;
   h.pitch = (h.chunk + 3) / 4 * 4;
@@ -437,6 +443,15 @@ HostStage plan_host_stage(dprc_dtype dt, int64_t B, int64_t T, int64_t d, int64_
   size_t off = 0;
   h.ws_off = off;
   off = align_up(off + h.ws_bytes, 1024);
+  // a shorter last chunk gets a workspace of its own: its counter block and
+  // scratch are laid out for another B, and a workspace is shared only by
+  // calls whose counter blocks coincide
+  const int64_t rest = B % h.chunk;
+  if (rest > 0) {
+    h.rest_ws_bytes = hutch_ws(dt, rest, T, d, p, k);
+    h.rest_ws_off = off;
+    off = align_up(off + h.rest_ws_bytes, 1024);
+  }
   h.n_off = off;
   off = align_up(off + static_cast<size_t>(h.nchunks) * h.pitch * 4, 1024);
   h.c_off = off;
@@ -753,8 +768,10 @@ dprc_status dprc_norm_hutch_clip_host(const void* A, const void* G, const void* 
     ClipOut clip;
     clip.C = C;
     clip.c = cd + j * h.pitch;
-    st = norm_hutch_impl(Ad, Gd, Pd, dtype, bc, T, d, p, k, nd + j * h.pitch, 0, w + h.ws_off,
-                         h.ws_bytes, s, &clip);
+    const bool short_chunk = bc < h.chunk;
+    st = norm_hutch_impl(Ad, Gd, Pd, dtype, bc, T, d, p, k, nd + j * h.pitch, 0,
+                         w + (short_chunk ? h.rest_ws_off : h.ws_off),
+                         short_chunk ? h.rest_ws_bytes : h.ws_bytes, s, &clip);
     if (st == DPRC_OK) e = cudaEventRecord(freed(sl), s);
   }
   // n and c back to the host: chunk j's values sit at j * pitch

@@ -68,12 +68,12 @@ def test_workspace_bytes_host_only(lib):
     assert b.dprc_workspace_bytes(b.DPRC_OP_EXACT, b.DPRC_BF16, 3, 1000, 64, 16, 0) >= 3 * 8 * 9 // 2 * 4
     assert b.dprc_workspace_bytes(b.DPRC_OP_EXACT, b.DPRC_F32, 2, 4096, 64, 64, 0) >= 2 * 128 * 128 * 4
     assert b.dprc_workspace_bytes(b.DPRC_OP_EXACT, b.DPRC_BF16, 2, 4096, 63, 64, 0) >= 2 * 128 * 128 * 4
-    # host-input stage: a chunk's workspace, P and two slots of a chunk each (two
-    # 33.5 MB samples make the 64 MB chunk)
+    # host-input stage: a chunk's workspace, P and two slots of a chunk each (four
+    # 33.5 MB samples make the 128 MB chunk)
     hs = b.dprc_workspace_bytes(b.DPRC_OP_HUTCH_HOST, b.DPRC_BF16, 8, 4096, 2048, 2048, 32)
-    two = b.dprc_workspace_bytes(b.DPRC_OP_HUTCH, b.DPRC_BF16, 2, 4096, 2048, 2048, 32)
-    assert hs >= two + 2 * 2 * 4096 * 4096 * 2 + 2048 * 32 * 2
-    assert hs < two + 2 * 2 * 4096 * 4096 * 2 + (1 << 20)
+    four = b.dprc_workspace_bytes(b.DPRC_OP_HUTCH, b.DPRC_BF16, 4, 4096, 2048, 2048, 32)
+    assert hs >= four + 2 * 4 * 4096 * 4096 * 2 + 2048 * 32 * 2
+    assert hs < four + 2 * 4 * 4096 * 4096 * 2 + (1 << 20)
     # small samples go 4 (or a multiple of 4) to a chunk
     assert (b.dprc_workspace_bytes(b.DPRC_OP_HUTCH_HOST, b.DPRC_BF16, 64, 128, 256, 256, 16)
             >= 2 * 64 * 128 * 512 * 2)

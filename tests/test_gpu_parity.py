@@ -272,16 +272,39 @@ def test_launch_count_query_matches_the_path():
     assert rnc.dprc_norm_hutch_launches(DPRC_BF16, 8, 4096, 16, 2048, 32) == 1
 
 
+def test_one_workspace_serves_calls_with_different_batch_sizes():
+    # a call with fewer samples must not leave scratch where a call with more
+    # keeps its counters (they share one fixed counter block for B <= 256)
+    T, d, p, k = 1024, 1024, 1024, 16
+    ws = rnc.workspace(rnc.DPRC_OP_HUTCH, torch.empty(1, dtype=torch.bfloat16, device=DEV),
+                       32, T, d, p, k)
+    runs = []
+    for B in (32, 6, 32, 6):
+        A = _rand((B, T, d), 70 + B, torch.bfloat16).to(DEV)
+        G = _rand((B, T, p), 71 + B, torch.bfloat16, 0.05).to(DEV)
+        P = _rand((p, k), 72, torch.bfloat16, k ** -0.5).to(DEV)
+        n = torch.zeros(B, device=DEV)
+        c = torch.empty(B, device=DEV)
+        rnc.dprc_norm_hutch_clip(A, G, P, n, 1.0, c, ws=ws)
+        fresh = torch.zeros(B, device=DEV)
+        rnc.dprc_norm_hutch(A, G, P, fresh)  # its own zeroed workspace
+        runs.append((n, fresh))
+        torch.cuda.synchronize()
+        assert rnc.dprc_device_error() == 0
+    for n, fresh in runs:
+        assert torch.equal(n, fresh)
+
+
 def _host_chunk(B, T, d, p, esize):
     # the chunk rule of dprc_norm_hutch_clip_host (include/dprc.h): the fewest
-    # samples that make at least 64 MB of A and G
+    # samples that make at least 128 MB of A and G
     sample = T * (d + p) * esize
-    return min(B, -(-(64 << 20) // sample))
+    return min(B, -(-(128 << 20) // sample))
 
 
 @pytest.mark.parametrize("B,T,d,p,k,dtype", [
-    (5, 4096, 2048, 2048, 32, torch.bfloat16),   # chunks of 2, 2 and 1: both slots reused
-    (40, 1024, 1024, 1024, 16, torch.bfloat16),  # chunks of 16, 16 and 8 samples
+    (9, 4096, 2048, 2048, 32, torch.bfloat16),   # chunks of 4, 4 and 1: a slot reused
+    (70, 1024, 1024, 1024, 16, torch.bfloat16),  # chunks of 32, 32 and 6 samples
     (5, 100, 40, 24, 8, torch.float32),          # one chunk
 ])
 def test_norm_hutch_clip_host_matches_device_calls_and_oracle(B, T, d, p, k, dtype):
