@@ -160,7 +160,9 @@ dprc_status dprc_norm_hutch_clip(const void* A, const void* G, const void* P, dp
  *  on the device copies of a chunk bit for bit.
  *  stage: device buffer of dprc_workspace_bytes(DPRC_OP_HUTCH_HOST, dtype, B,
  *  T, d, p, k) bytes, 16-byte aligned; zero it once before its first use (it
- *  holds a workspace).  One call at a time may use a stage buffer.
+ *  holds workspaces, placed by the sizes).  Calls with the same sizes may reuse
+ *  it as it is; zero it again before a call with other sizes.  One call at a
+ *  time may use a stage buffer.
  *  C > 0 and finite.  Errors as dprc_norm_hutch; a failed copy returns
  *  DPRC_ERR_CUDA.  No counterpart on the pages (the host side of one step).
  */
