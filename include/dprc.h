@@ -91,9 +91,12 @@ int dprc_abi_version(void);
 const char* dprc_status_string(dprc_status s);
 
 /*
- * Scratch bytes needed by one call of `op` with these sizes (k is the
- * projection width for DPRC_OP_HUTCH, the sketch width r for
- * DPRC_OP_HUTCHPP, ignored for DPRC_OP_EXACT).  Returns 0 for invalid sizes.
+ * Scratch bytes needed by one call of `op` with these sizes.  k is the
+ * projection width for DPRC_OP_HUTCH, DPRC_OP_HUTCH_PM1 and
+ * DPRC_OP_HUTCH_HOST, the sketch width r for DPRC_OP_HUTCHPP, and ignored
+ * for DPRC_OP_EXACT.  For DPRC_OP_HUTCH_LAYERS, d and p are the largest
+ * widths of the layer list.  DPRC_OP_HUTCH_HOST gives the size of the device
+ * stage buffer of dprc_norm_hutch_clip_host.  Returns 0 for invalid sizes.
  * The size depends on the current device's SM count.
  */
 size_t dprc_workspace_bytes(dprc_op op, dprc_dtype dtype, int64_t B, int64_t T,
@@ -232,9 +235,10 @@ dprc_status dprc_norm_hutch_layers_clip(int64_t L, const void* const* A, const v
  * the current device: 1 (bf16, k = 16 or 32: sketch and projection as two
  * phases of one cooperative launch; or the one-pass kernel of a narrow
  * layer), 2 (other tensor-core shapes: a sketch kernel and a projection
- * kernel) or 3 (the CUDA-core path: sketch, projection, reduction).  0 for arguments dprc_norm_hutch would reject or
- * when no sm_103 device is current.  Enqueues nothing; for launch accounting
- * and graph builders.  No counterpart on the pages (a library property).
+ * kernel) or 3 (the CUDA-core path: sketch, projection, reduction).  0 for
+ * arguments dprc_norm_hutch would reject or when no sm_103 device is current.
+ * Enqueues nothing; for launch accounting and graph builders.  No counterpart
+ * on the pages (a library property).
  */
 int dprc_norm_hutch_launches(dprc_dtype dtype, int64_t B, int64_t T, int64_t d, int64_t p,
                              int64_t k);
