@@ -401,18 +401,122 @@ def run_native(args, rank, ws, local):
     which = set() if args.rows == "none" else (
         {"c3", "c4", "c5", "noise", "exact", "step", "pm1", "lora"} if args.rows == "all"
         else set(args.rows.split(",")))
-    if which:
-        out["rows"] = measure_rows(which, device, peak, measured_tflops(), 7919 * rank)
+    rows = measure_rows(which, device, peak, measured_tflops(), 7919 * rank) if which else {}
     if rank == 0 and not args.no_cpu_baseline:
         rate, done, el = cpu_oracle_rate(A.cpu(), G.cpu(), P.cpu(), wk.C)
         out["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": os.cpu_count(),
                                "kind": "oracle",
                                "sample": f"{done} whole samples (T={T}) of the same batch, "
                                          f"{el:.1f} s, float64 numpy (BLAS threads = cores)"}
+        if rows:
+            cpu_oracle_subsets(rows, device)
+    if rows:
+        # the full rows first; the line ends with a compact summary of them,
+        # ordered so the 112-layer step, the noise, Hutch++ and the training
+        # step come last (a reader of only the line's tail still sees them)
+        out["rows_detail"] = rows
+        out["rows"] = compact_rows(rows)
     return out
 
 
 # ---------------------------------------------------------------- other rows
+
+def _sig(x, digits=4):
+    return float(f"{x:.{digits}g}") if isinstance(x, (int, float)) and x is not None else x
+
+
+# compact summary: which fields of each row, in print order (the most
+# important rows last)
+_COMPACT = (
+    ("exact_q_proj_b32_t1024", None),
+    ("exact_c2", ("ms", "frac")),
+    ("lora_down_r16", ("ms", "frac", "exact_ms", "exact_frac")),
+    ("lora_up_r16", ("ms", "frac", "exact_ms", "exact_frac")),
+    ("pm1_q_proj", ("ms", "frac")),
+    ("c5_up_proj", ("ms", "frac", "tokens_per_s", "cpu_tokens_per_s")),
+    ("c5_down_proj", ("ms", "frac", "tokens_per_s", "cpu_tokens_per_s")),
+    ("c4_hutchpp", ("ms", "frac", "tokens_per_s", "cpu_tokens_per_s")),
+    ("noise_1.24e9", ("ms", "frac", "cpu_ms")),
+    ("dpsgd_rc_step_mlp", ("ms", "plain_backward_ms", "overhead")),
+    ("c3_112layers", ("ms", "frac", "norms_ms", "norms_frac", "tokens_per_s_per_layer",
+                      "cpu_tokens_per_s_per_layer", "clip_fraction")),
+)
+
+
+def compact_rows(rows):
+    out = {}
+    for name, fields in _COMPACT:
+        if name not in rows:
+            continue
+        r = rows[name]
+        if name == "exact_q_proj_b32_t1024":
+            out[name] = {"auto": r["auto"], **{f"{k}_ms": _sig(v["ms"]) for k, v in r["forms"].items()},
+                         **{f"{k}_frac": _sig(v["frac"], 3) for k, v in r["forms"].items()}}
+            continue
+        flat = dict(r)
+        if "norms" in r:
+            flat["norms_ms"] = r["norms"]["ms"]
+            flat["norms_frac"] = r["norms"]["frac"]
+        if "cpu_oracle" in r:
+            flat.update({k: v for k, v in r["cpu_oracle"].items() if k != "sample"})
+        out[name] = {k: _sig(flat[k], 3 if "frac" in k else 4) for k in fields if k in flat}
+    return out
+
+
+def cpu_oracle_subsets(rows, device):
+    """The float64 oracle on the host cores on a stated subset of each row's
+    workload, extrapolated linearly in samples and layers (the oracle's time
+    per sample grows with T (d + p)); added to the rows as "cpu_oracle"."""
+    import oracle
+
+    def one_sample(wk, li):
+        A, G, P = wl.layer_inputs(wk, li, device=device)
+        if isinstance(P, tuple):
+            args = (wl.to_f64(A[:1]), wl.to_f64(G[:1]), *[wl.to_f64(x) for x in P])
+            fn = oracle.hutchpp_norm
+        else:
+            args = (wl.to_f64(A[:1]), wl.to_f64(G[:1]), wl.to_f64(P))
+            fn = oracle.hutch_norm
+        del A, G, P
+        t0 = time.perf_counter()
+        fn(*args)
+        return time.perf_counter() - t0
+
+    if "c4_hutchpp" in rows:
+        wk = wl.WORKLOADS["hutchpp_q_proj_b8_t4096_r16_bf16"]
+        t = one_sample(wk, 0)
+        rows["c4_hutchpp"]["cpu_oracle"] = {
+            "cpu_tokens_per_s": wk.T / t, "cores": os.cpu_count(),
+            "sample": f"one sample (T={wk.T}) of the batch, {t:.2f} s"}
+    for i, name in enumerate(("c5_up_proj", "c5_down_proj")):
+        if name in rows:
+            wk = wl.WORKLOADS["hutch_long_b2_t32768_up_down_k32_bf16"]
+            t = one_sample(wk, i)
+            rows[name]["cpu_oracle"] = {
+                "cpu_tokens_per_s": wk.T / t, "cores": os.cpu_count(),
+                "sample": f"one sample (T={wk.T}) of the B=2 batch, {t:.2f} s"}
+    if "noise_1.24e9" in rows or "c3_112layers" in rows:
+        wk = wl.WORKLOADS["hutch_llama32_1b_112layers_b4_t4096_k32_bf16"]
+        sub = 1 << 20
+        g = np.zeros(sub)
+        t0 = time.perf_counter()
+        oracle.add_noise(g, wk.sigma, wk.C, 1234, 1)
+        t_noise = (time.perf_counter() - t0) * wk.noise_elems / sub
+        if "noise_1.24e9" in rows:
+            rows["noise_1.24e9"]["cpu_oracle"] = {
+                "cpu_ms": 1e3 * t_noise, "cores": os.cpu_count(),
+                "sample": f"{sub} elements, scaled to {wk.noise_elems}"}
+        if "c3_112layers" in rows:
+            nblock = len(wl.LLAMA32_1B_BLOCK)
+            per_sample = sum(one_sample(wk, j) for j in range(nblock))
+            t_norms = per_sample * wk.B * wl.LLAMA32_1B_BLOCKS
+            rows["c3_112layers"]["cpu_oracle"] = {
+                "cpu_tokens_per_s_per_layer": wk.B * wk.T * len(wk.layers) / t_norms,
+                "cpu_step_ms": 1e3 * (t_norms + t_noise), "cores": os.cpu_count(),
+                "sample": f"one sample of each of the {nblock} layer shapes of a block "
+                          f"({per_sample:.2f} s), scaled by {wk.B} samples x "
+                          f"{wl.LLAMA32_1B_BLOCKS} blocks; the noise on {sub} elements, "
+                          f"scaled to {wk.noise_elems}"}
 
 def graph_ms(fn, device, reps, warmup=3):
     """Mean device time of fn captured as one CUDA graph and replayed reps times

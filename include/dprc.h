@@ -352,16 +352,53 @@ dprc_status dprc_philox_words(uint32_t* out, int64_t n_blocks, uint64_t first_bl
 
 /*
  * Reads (and, if reset != 0, clears) the device error word of the current
- * device.  Nonzero means a bounded in-kernel wait ran out (the value encodes
- * which: see DPRC_DEVERR_*); the affected outputs are invalid.  This call
- * synchronizes with the device.
+ * device.  Nonzero means a bounded in-kernel wait ran out, or a kernel
+ * refused a launch shape it was not planned for (the value encodes which: see
+ * DPRC_DEVERR_*); the affected outputs are invalid, and the workspace of the
+ * call must be zeroed again before its next use.  The first error since the
+ * last reset is kept.  This call synchronizes with the device.
  */
 #define DPRC_DEVERR_PIPE_FULL 1   /* consumer waited too long for a tile */
 #define DPRC_DEVERR_PIPE_EMPTY 2  /* producer waited too long for a free stage */
 #define DPRC_DEVERR_ACCUM 3       /* epilogue waited too long for the accumulator */
 #define DPRC_DEVERR_CLUSTER 4     /* a CTA waited too long for its cluster peers' partials */
 #define DPRC_DEVERR_READY 5       /* the projection waited too long for a sample's sketch */
+#define DPRC_DEVERR_LAUNCH 6      /* a kernel found its launch's cluster shape other than
+                                     planned and returned before doing anything */
 dprc_status dprc_device_error(int32_t* out, int reset);
+
+/*
+ * Failure-detection test of the one-launch Hutchinson kernel (a check of this
+ * library's own promise that every wait inside a kernel is bounded; the pages
+ * have no counterpart).  The layers are given as for dprc_norm_hutch_layers
+ * (bf16, k = 16 or 32, 1 <= L <= 56, widths multiples of 8, none narrow); the
+ * launch is planned exactly as dprc_norm_hutch_layers (L > 1) or
+ * dprc_norm_hutch (L = 1) plans it, with accumulate = 0, and then altered:
+ *   mode 0: every sketch-ready target is set one above what the sketch phase
+ *           adds, so no projection block's wait for its sample's sketch can
+ *           succeed.  Each such wait runs out after wait_ns, sets
+ *           DPRC_DEVERR_READY, and the launch unwinds: the other roles of a
+ *           CTA stop at their next wait, the MMAs and copies already issued
+ *           complete, the tensor memory is freed and the kernel returns.  n
+ *           is not written.  The workspace's counters are left nonzero: zero
+ *           it before its next use.
+ *   mode 1: a plan without clusters is launched with clusters of 2; the
+ *           kernel finds the cluster shape it was not planned for, sets
+ *           DPRC_DEVERR_LAUNCH and returns before touching any memory (n and
+ *           the workspace are unchanged).
+ *  wait_ns: limit of the launch's waits on other CTAs' progress, 1e3 .. 2e9
+ *           ns (the default is 2e9); waits inside a CTA or its cluster get
+ *           twice that, so the wait that is the cause runs out first.
+ *  Workspace: dprc_workspace_bytes(L > 1 ? DPRC_OP_HUTCH_LAYERS :
+ *  DPRC_OP_HUTCH, ...).  Returns DPRC_ERR_SHAPE when the layers do not take
+ *  the one-launch kernel on this device, or (mode 1) when its plan already
+ *  uses clusters.  Other errors as dprc_norm_hutch_layers.  Read the result
+ *  with dprc_device_error(&v, 1).
+ */
+dprc_status dprc_test_hutch_fault(int mode, uint64_t wait_ns, int64_t L, const void* const* A,
+                                  const void* const* G, const void* const* P, const int64_t* d,
+                                  const int64_t* p, int64_t B, int64_t T, int64_t k, float* n,
+                                  void* ws, size_t ws_bytes, void* stream);
 
 /*
  * Timing hook.  With events != NULL, every later call made by this host
@@ -388,8 +425,10 @@ dprc_status dprc_set_phase_events(void** events, int n_events);
  * device memory (a file-scope __device__ array), held on every GPU that loads
  * the library until the process exits.  Calls whose dprc_workspace_bytes
  * (DPRC_OP_HUTCH, ...) exceeds that size return DPRC_ERR_TOO_LARGE before
- * any device work.  The call itself allocates nothing (no cudaMalloc,
- * cudaFree or allocating library routine).
+ * any device work, as do argument errors (the checks and codes of
+ * dprc_norm_hutch) and DPRC_ERR_DEVICE when the current device is not an
+ * sm_103 GPU.  The call itself allocates nothing (no cudaMalloc, cudaFree or
+ * allocating library routine).
  *
  * Set-up: the first call on each device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current and caches it, so make the

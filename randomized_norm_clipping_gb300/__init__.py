@@ -39,6 +39,7 @@ from .binding import (  # noqa: F401
     dprc_norm_hutchpp,
     dprc_philox_words,
     dprc_set_phase_events,
+    dprc_test_hutch_fault,
     dprc_workspace_bytes,
     host_stage,
     lib,

@@ -81,6 +81,10 @@ _PROTOS = [
     ("dprc_norm_hutch_noalloc", _c.c_int,
      [_c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_int, _c.c_int64, _c.c_int64, _c.c_int64,
       _c.c_int64, _c.c_int64, _c.c_void_p, _c.c_int, _c.c_void_p]),
+    ("dprc_test_hutch_fault", _c.c_int,
+     [_c.c_int, _c.c_uint64, _c.c_int64, _c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p,
+      _c.c_void_p, _c.c_int64, _c.c_int64, _c.c_int64, _c.c_void_p, _c.c_void_p, _c.c_size_t,
+      _c.c_void_p]),
 ]
 EXPORTED = tuple(name for name, _, _ in _PROTOS)
 
@@ -313,6 +317,35 @@ def dprc_norm_hutch_noalloc(A, G, P, n, accumulate=False, stream=None):
     st = lib().dprc_norm_hutch_noalloc(_ptr(A), _ptr(G), _ptr(P), _dtype_code(A), B, T, d, p, k,
                                        _ptr(n), int(bool(accumulate)), _stream(A, stream))
     _check("dprc_norm_hutch_noalloc", st)
+    return n
+
+
+# Device error codes (DPRC_DEVERR_* of include/dprc.h).
+(DPRC_DEVERR_PIPE_FULL, DPRC_DEVERR_PIPE_EMPTY, DPRC_DEVERR_ACCUM, DPRC_DEVERR_CLUSTER,
+ DPRC_DEVERR_READY, DPRC_DEVERR_LAUNCH) = (1, 2, 3, 4, 5, 6)
+FAULT_READY_NEVER_MET, FAULT_CLUSTER_SHAPE = 0, 1
+
+
+def dprc_test_hutch_fault(mode, wait_ns, As, Gs, Ps, n, ws, stream=None):
+    """Failure-detection test of the one-launch Hutchinson kernel (see
+    include/dprc.h): mode FAULT_READY_NEVER_MET makes every projection's wait
+    for its sample's sketch run out after wait_ns; mode FAULT_CLUSTER_SHAPE
+    launches a plan without clusters as clusters of 2.  Read the outcome with
+    dprc_device_error(reset=True)."""
+    L = len(As)
+    if not (L == len(Gs) == len(Ps)) or L == 0:
+        raise ValueError("As, Gs and Ps must be non-empty lists of the same length")
+    _need_cuda(*As, *Gs, *Ps, n, ws)
+    B, T = As[0].shape[0], As[0].shape[1]
+    k = Ps[0].shape[1]
+    d = (ctypes.c_int64 * L)(*[a.shape[2] for a in As])
+    p = (ctypes.c_int64 * L)(*[g.shape[2] for g in Gs])
+    ap = (ctypes.c_void_p * L)(*[_ptr(a) for a in As])
+    gp = (ctypes.c_void_p * L)(*[_ptr(g) for g in Gs])
+    pp = (ctypes.c_void_p * L)(*[_ptr(x) for x in Ps])
+    st = lib().dprc_test_hutch_fault(int(mode), int(wait_ns), L, ap, gp, pp, d, p, B, T, k,
+                                     _ptr(n), _ptr(ws), ws.numel(), _stream(As[0], stream))
+    _check("dprc_test_hutch_fault", st)
     return n
 
 

@@ -487,6 +487,21 @@ cudaStream_t copy_stream(int which) {
 
 }  // namespace
 
+namespace dprc {
+dprc_status check_hutch_args(const void* A, const void* G, const void* P, dprc_dtype dtype,
+                             int64_t B, int64_t T, int64_t d, int64_t p, int64_t k,
+                             const float* n) {
+  if (!A || !G || !P || !n) return DPRC_ERR_NULL;
+  const dprc_status st = check_common(dtype, B, T, d, p);
+  if (st != DPRC_OK) return st;
+  if (k < 1 || k > 256) return DPRC_ERR_SHAPE;
+  if (!aligned16(A) || !aligned16(G) || !aligned16(P) || !aligned16(n)) return DPRC_ERR_ALIGN;
+  return DPRC_OK;
+}
+
+bool current_device_supported() { return device_ok(); }
+}  // namespace dprc
+
 namespace {
 // dprc_norm_hutch, with the clip factors of the updated n when `clip` is set
 // (in the fused kernel's finishing step, else by the clip kernel afterwards).
@@ -494,11 +509,8 @@ dprc_status norm_hutch_impl(const void* A, const void* G, const void* P, dprc_dt
                             int64_t B, int64_t T, int64_t d, int64_t p, int64_t k, float* n,
                             int accumulate, void* ws, size_t ws_bytes, void* stream,
                             const ClipOut* clip) {
-  if (!A || !G || !P || !n) return DPRC_ERR_NULL;
-  dprc_status st = check_common(dtype, B, T, d, p);
+  const dprc_status st = check_hutch_args(A, G, P, dtype, B, T, d, p, k, n);
   if (st != DPRC_OK) return st;
-  if (k < 1 || k > 256) return DPRC_ERR_SHAPE;
-  if (!aligned16(A) || !aligned16(G) || !aligned16(P) || !aligned16(n)) return DPRC_ERR_ALIGN;
   if (clip != nullptr) {
     if (!clip->c) return DPRC_ERR_NULL;
     if (!(clip->C > 0.f) || !(clip->C < __builtin_inff())) return DPRC_ERR_SHAPE;
@@ -1024,6 +1036,48 @@ dprc_status dprc_philox_words(uint32_t* out, int64_t n_blocks, uint64_t first_bl
   if (!device_ok()) return DPRC_ERR_DEVICE;
   return cuda_status(launch_philox_words(out, n_blocks, first_block, seed, step,
                                          static_cast<cudaStream_t>(stream)));
+}
+
+dprc_status dprc_test_hutch_fault(int mode, uint64_t wait_ns, int64_t L, const void* const* A,
+                                  const void* const* G, const void* const* P, const int64_t* d,
+                                  const int64_t* p, int64_t B, int64_t T, int64_t k, float* n,
+                                  void* ws, size_t ws_bytes, void* stream) {
+  if (!A || !G || !P || !d || !p || !n) return DPRC_ERR_NULL;
+  if (mode != kFaultReadyNeverMet && mode != kFaultClusterShape) return DPRC_ERR_SHAPE;
+  constexpr uint64_t kMaxWaitNs = 2000000000ull;  // the kernels' own limit
+  if (wait_ns < 1000 || wait_ns > kMaxWaitNs) return DPRC_ERR_SHAPE;
+  if (L < 1 || L > kMaxFusedLayers) return DPRC_ERR_SHAPE;
+  if (!fused_hutch_supported(k)) return DPRC_ERR_SHAPE;
+  int64_t dmax = 0, pmax = 0;
+  for (int64_t l = 0; l < L; ++l) {
+    if (!A[l] || !G[l] || !P[l]) return DPRC_ERR_NULL;
+    const dprc_status st = check_common(DPRC_BF16, B, T, d[l], p[l]);
+    if (st != DPRC_OK) return st;
+    if (!tc_path_supported(DPRC_BF16, B, T, d[l], p[l], k, false)) return DPRC_ERR_SHAPE;
+    if (!aligned16(A[l]) || !aligned16(G[l]) || !aligned16(P[l])) return DPRC_ERR_ALIGN;
+    dmax = std::max(dmax, d[l]);
+    pmax = std::max(pmax, p[l]);
+  }
+  if (!aligned16(n)) return DPRC_ERR_ALIGN;
+  if (!ws) return DPRC_ERR_WORKSPACE;
+  if (!aligned16(ws)) return DPRC_ERR_ALIGN;
+  const int layers = L > 1 ? kMaxFusedLayers : 1;
+  const TcPlan t = plan_tc(DPRC_OP_HUTCH, B, T, dmax, pmax, k, layers);
+  if (ws_bytes < t.total) return DPRC_ERR_WORKSPACE;
+  if (!device_ok()) return DPRC_ERR_DEVICE;
+  HutchFaultTest test;
+  test.mode = mode;
+  test.wait_ns = wait_ns;
+  bool launched = false;
+  const cudaError_t e =
+      launch_tc_hutch_fault_test(static_cast<int>(L), A, G, P, d, p, B, T, k,
+                                 fused_scratch(t, static_cast<char*>(ws)), n, test,
+                                 static_cast<cudaStream_t>(stream), &launched);
+  if (!launched) {
+    if (e != cudaSuccess) (void)cudaGetLastError();
+    return e == cudaSuccess ? DPRC_ERR_SHAPE : DPRC_ERR_CUDA;
+  }
+  return cuda_status(e);
 }
 
 dprc_status dprc_device_error(int32_t* out, int reset) {

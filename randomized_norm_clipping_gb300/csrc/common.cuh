@@ -102,12 +102,42 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int co
   }
 }
 
+// Like mbar_wait, with the time limit given by the caller, and giving up
+// early (false, nothing recorded: the CTA is already unwinding) once another
+// role of the CTA has set `abort` (may be null).  For the pipeline waits of a
+// kernel whose roles stop at the first failure of any of them.
+__device__ __forceinline__ bool mbar_wait_lim(uint64_t* bar, uint32_t parity, int code,
+                                              unsigned long long limit_ns,
+                                              const volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer_ns();
+  while (true) {
+    for (int spin = 0; spin < 64; ++spin)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (abort != nullptr && *abort != 0) return false;
+    if (globaltimer_ns() - t0 > limit_ns) {
+      record_error(code);
+      return false;
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------
 // Thread-block clusters: ranks, distributed shared memory, remote arrivals.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+
+// CTAs in this CTA's cluster as launched (1 for a launch without clusters).
+// A kernel whose plan splits work over clusters compares it with the planned
+// size before any distributed shared memory access: with another shape, a
+// peer rank it would address does not exist.
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
   return r;
 }
 
@@ -168,14 +198,15 @@ __device__ __forceinline__ bool mbar_try_wait_acq_cluster(uint64_t* bar, uint32_
 }
 
 // Bounded wait for data that peers in the cluster published with
-// mbar_arrive_remote; false (and `code` recorded) on time-out.
-__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, int code) {
+// mbar_arrive_remote; false (and `code` recorded) after limit_ns.
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, int code,
+                                                  unsigned long long limit_ns = kWaitLimitNs) {
   if (mbar_try_wait_acq_cluster(bar, parity)) return true;
   const unsigned long long t0 = globaltimer_ns();
   while (true) {
     for (int spin = 0; spin < 64; ++spin)
       if (mbar_try_wait_acq_cluster(bar, parity)) return true;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+    if (globaltimer_ns() - t0 > limit_ns) {
       record_error(code);
       return false;
     }
@@ -242,6 +273,15 @@ __device__ __forceinline__ void umma_commit(uint64_t* bar) {
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
           smem_u32(bar))
       : "memory");
+}
+
+// Waits until every MMA this thread has issued is complete: a commit to
+// `bar` (a barrier of count 1 used for nothing else, phase 0) and a bounded
+// wait on it.  The MMA thread calls it last, on every path out of its loop,
+// so that no MMA still writes the tensor memory the CTA releases at exit.
+__device__ __forceinline__ void umma_drain(uint64_t* bar, unsigned long long limit_ns) {
+  umma_commit(bar);
+  mbar_wait_lim(bar, 0, DPRC_DEVERR_ACCUM, limit_ns, nullptr);
 }
 
 // 32 TMEM lanes x 32 columns of 32-bit: thread l of the warp receives lane

@@ -61,6 +61,13 @@ struct SimtPlan {
 };
 
 int device_sm_count();
+// Argument checks of dprc_norm_hutch that need no device (pointers, sizes,
+// alignment); DPRC_OK or the status the call returns.
+dprc_status check_hutch_args(const void* A, const void* G, const void* P, dprc_dtype dtype,
+                             int64_t B, int64_t T, int64_t d, int64_t p, int64_t k,
+                             const float* n);
+// Whether the current device is an sm_103 GPU (cached per device).
+bool current_device_supported();
 int rowproj_ctas_per_sm();
 int colproj_ctas_per_sm(int nmma);
 int colproj_stage_chunk();
@@ -186,6 +193,22 @@ cudaError_t launch_tc_hutch_layers(int L, const void* const* A, const void* cons
                                    int64_t B, int64_t T, int64_t k, const FusedScratch& ws,
                                    float* n_out, int accumulate, cudaStream_t s, bool* launched,
                                    const ClipOut* clip = nullptr);
+// Failure-detection test of the fused kernel (dprc_test_hutch_fault): mode
+// kFaultReadyNeverMet plans the launch as usual but raises every sketch-ready
+// target by one, so the projection's waits cannot succeed; mode
+// kFaultClusterShape launches a plan without clusters as clusters of 2.  Every
+// wait in the launch is limited to wait_ns.  *launched false: these layers do
+// not take the fused kernel (or, for the second mode, their plan has clusters).
+enum { kFaultReadyNeverMet = 0, kFaultClusterShape = 1 };
+struct HutchFaultTest {
+  int mode = kFaultReadyNeverMet;
+  unsigned long long wait_ns = 0;
+};
+cudaError_t launch_tc_hutch_fault_test(int L, const void* const* A, const void* const* G,
+                                       const void* const* P, const int64_t* d, const int64_t* p,
+                                       int64_t B, int64_t T, int64_t k, const FusedScratch& ws,
+                                       float* n_out, const HutchFaultTest& test, cudaStream_t s,
+                                       bool* launched);
 // The +-1 projection variant on the fused kernel (bf16, k = 16 or 32, one
 // layer): the signs are generated in the kernel from (seed, step); the norm is
 // scaled by 1/k.  *launched false: not possible here (use the signs below).

@@ -39,8 +39,10 @@ dprc_status scratch_address(void** out) {
   std::lock_guard<std::mutex> lock(g_mu);
   if (g_scratch_addr[dev] == nullptr) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+      (void)cudaGetLastError();  // leave no sticky error behind for the caller
       return DPRC_ERR_CUDA;
+    }
     g_scratch_addr[dev] = p;
   }
   *out = g_scratch_addr[dev];
@@ -53,12 +55,16 @@ extern "C" dprc_status dprc_norm_hutch_noalloc(const void* A, const void* G, con
                                                dprc_dtype dtype, int64_t B, int64_t T,
                                                int64_t d, int64_t p, int64_t k, float* n,
                                                int accumulate, void* stream) {
+  // every check that needs no device first: an argument error returns before
+  // the scratch is looked up or its counters are cleared
+  dprc_status st = dprc::check_hutch_args(A, G, P, dtype, B, T, d, p, k, n);
+  if (st != DPRC_OK) return st;
   const size_t need = dprc_workspace_bytes(DPRC_OP_HUTCH, dtype, B, T, d, p, k);
-  if (need == 0)  // invalid arguments: let the checks of dprc_norm_hutch name the error
-    return dprc_norm_hutch(A, G, P, dtype, B, T, d, p, k, n, accumulate, nullptr, 0, stream);
+  if (need == 0) return DPRC_ERR_SHAPE;
   if (need > static_cast<size_t>(DPRC_NOALLOC_SCRATCH_BYTES)) return DPRC_ERR_TOO_LARGE;
+  if (!dprc::current_device_supported()) return DPRC_ERR_DEVICE;
   void* ws = nullptr;
-  const dprc_status st = scratch_address(&ws);
+  st = scratch_address(&ws);
   if (st != DPRC_OK) return st;
   // the counters at the front of the scratch must start at zero
   if (cudaMemsetAsync(ws, 0, dprc::ctrl_bytes(B), static_cast<cudaStream_t>(stream)) !=

@@ -148,6 +148,12 @@ __global__ void __launch_bounds__(kCt, 1)
   extern __shared__ float stage[];  // Q rows then P rows: [kCt * RPT][17] each
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // Each sample's rows are spread over one cluster of kCl CTAs; a launch of
+  // any other cluster shape would address ranks that do not exist: refuse it.
+  if (cluster_nctarank() != static_cast<uint32_t>(kCl)) {
+    if (tid == 0) record_error(DPRC_DEVERR_LAUNCH);
+    return;
+  }
   const int rank = static_cast<int>(cluster_ctarank());
   const int i = blockIdx.x / kCl;
   const float* m_i = M + static_cast<size_t>(i) * p * kR;

@@ -64,7 +64,8 @@ __global__ void __launch_bounds__(192, 1)
   uint64_t* empty = full + kFgcStages;
   uint64_t* accf = empty + kFgcStages;  // [2]
   uint64_t* acce = accf + 2;            // [2]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acce + 2);
+  uint64_t* drain = acce + 2;           // MMA thread: all its MMAs complete
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acce + 3);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -82,6 +83,7 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(&accf[b], 1);
       mbar_init(&acce[b], 4);
     }
+    mbar_init(drain, 1);
     fence_mbar_init();
     *abort_flag = 0;
   }
@@ -134,7 +136,7 @@ __global__ void __launch_bounds__(192, 1)
     if (lane == 0 && my_tiles > 0) {
       constexpr uint32_t idesc = make_idesc_bf16(kFgcM, kFgcN, true, true);
       long long it = 0;
-      bool ok = true;
+      bool ok = true, issued = false;
       for (long long j = 0; j < my_tiles && ok; ++j) {
         const int abuf = static_cast<int>(j & 1);
         if (!mbar_wait(&acce[abuf], static_cast<uint32_t>((j >> 1) & 1) ^ 1, DPRC_DEVERR_ACCUM)) {
@@ -163,9 +165,13 @@ __global__ void __launch_bounds__(192, 1)
             umma_bf16(tmem + abuf * kFgcN, ad, bd, idesc, (u == 0 && kk == 0) ? 0u : 1u);
           }
           umma_commit(&empty[s]);
+          issued = true;
         }
         if (ok) umma_commit(&accf[abuf]);
       }
+      // on every path out of the loop: no MMA still writes the tensor memory
+      // the CTA releases
+      if (issued) umma_drain(drain, kWaitLimitNs);
     }
   } else {
     // ---------------- epilogue warps 2..5 ----------------
@@ -324,7 +330,8 @@ __global__ void __launch_bounds__(kGhThreads, 1)
   uint64_t* g_full = a_free + 1;            // S_G complete
   uint64_t* g_free = g_full + 1;            // S_G consumed
   uint64_t* mail = g_free + 1;              // [2] epilogue mailbox filled
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mail + 2);
+  uint64_t* drain = mail + 2;               // MMA thread: all its MMAs complete
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(mail + 3);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -341,6 +348,7 @@ __global__ void __launch_bounds__(kGhThreads, 1)
     mbar_init(g_free, kGhEpiWarps);
     mbar_init(&mail[0], 1);
     mbar_init(&mail[1], 1);
+    mbar_init(drain, 1);
     fence_mbar_init();
     *abort_flag = 0;
     epi_stop = 0;
@@ -408,6 +416,7 @@ __global__ void __launch_bounds__(kGhThreads, 1)
       constexpr uint32_t idesc_w = make_idesc_bf16(kGhRows, Cfg::kN, false, false);
       constexpr uint32_t idesc_1 = make_idesc_bf16(kGhRows, kGhRows, false, false);
       long long it = 0;
+      bool issued = false;
       for (long long j = 0;; ++j) {
         // the unit's first stage names it
         const int s0 = static_cast<int>(it % Cfg::kStages);
@@ -452,6 +461,7 @@ __global__ void __launch_bounds__(kGhThreads, 1)
               umma_bf16(dst, ad, bd, idesc, (f == f0 && kk == 0) ? 0u : 1u);
             }
             umma_commit(&empty[s]);
+            issued = true;
           }
           if (ok) umma_commit(part == 0 ? a_full : g_full);
         }
@@ -460,6 +470,9 @@ __global__ void __launch_bounds__(kGhThreads, 1)
           break;
         }
       }
+      // on every path out of the loop: no MMA still writes the tensor memory
+      // the CTA releases
+      if (issued) umma_drain(drain, kWaitLimitNs);
     }
   } else {
     // ---------------- epilogue warps 2 .. 9 ----------------

@@ -27,10 +27,14 @@
 // n_l[l][i]; the last layer to finish sample i adds them in layer order
 // (deterministic) into n_i.
 //
-// The cross-CTA waits are safe because the launch is cooperative (every CTA
-// is resident) and every wait is on work that comes earlier in the one order
-// all CTAs follow (layer, then phase); every wait is bounded (2 s) and
-// records a code in the device error word when it runs out.
+// The cross-CTA waits are safe because every CTA is resident (the grid is at
+// most what fits on the device at once; a launch without clusters is
+// cooperative) and every wait is on work that comes earlier in the one order
+// all CTAs follow (layer, then phase).  Every wait is bounded (2 s, or the
+// limit a test gives) and records a code in the device error word when it
+// runs out; the CTA's other roles then stop at their next wait, the MMA
+// thread waits for the MMAs it issued and the producer for its copies, and
+// the CTA frees its tensor memory and returns.
 //
 // Each phase assigns blocks either whole, strided over the CTAs, or one at a
 // time to a thread-block cluster whose CTAs split the block's units and
@@ -38,8 +42,8 @@
 // the receive buffer reusable across blocks, phases and layers).
 //
 // Counters (ready, tickets, per-sample layer tickets, per-layer projection
-// counts) are reset by their last user, so they are zero after every call and
-// must be zero before the first.
+// counts) are reset by their last user, so they are zero after every call that
+// ends without a device error, and must be zero before the first.
 //
 // One CTA per SM: the driver counts tensor-memory kernels at one CTA per SM,
 // and a cooperative launch cannot exceed that.  The shared-memory ring has 4
@@ -83,7 +87,7 @@ struct HCfg {
   static constexpr int kAccR = K < 32 ? 32 : K;
   static constexpr int kColAcc0 = 2 * kAccR;
   static constexpr int kTmemCols = 256;
-  static constexpr int kBars = 2 * kStages + 8 + 4;  // ring, accumulators, exchange
+  static constexpr int kBars = 2 * kStages + 8 + 1 + 4;  // ring, accumulators, drain, exchange
   static constexpr int xchg(int cl) { return cl <= 1 ? 0 : (cl - 1) * (kRows / cl) * K * 4; }
   static constexpr int kCtrl = 1024;  // barriers, TMEM slot, flags, norms
   static constexpr int smem(int cl) { return 1024 + kRing + kCtrl + xchg(cl); }
@@ -146,15 +150,18 @@ __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
-// Bounded wait until *p >= target (acquire); false (error recorded) on timeout.
-__device__ __forceinline__ bool wait_geq(const int* p, int target) {
+// Bounded wait until *p >= target (acquire); false on timeout (error
+// recorded) or once the CTA's abort flag is set (nothing recorded).
+__device__ __forceinline__ bool wait_geq(const int* p, int target, unsigned long long limit_ns,
+                                         const volatile int* abort) {
   if (ld_acquire(p) >= target) return true;
   const unsigned long long t0 = globaltimer_ns();
   unsigned ns = 64;
   while (true) {
     __nanosleep(ns);
     if (ld_acquire(p) >= target) return true;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+    if (*abort != 0) return false;
+    if (globaltimer_ns() - t0 > limit_ns) {
       record_error(DPRC_DEVERR_READY);
       return false;
     }
@@ -177,14 +184,16 @@ struct Xchg {
 // end with the sum over ranks in rank order and return true.
 template <int K>
 __device__ __forceinline__ bool xchg_rows(const Xchg& xs, int cl, int rank, int row, int rnd,
-                                          bool last, float (&y)[K], bool& ok) {
+                                          bool last, float (&y)[K], bool& ok,
+                                          unsigned long long limit_ns) {
   const int R = kRows / cl;
   const int owner = row / R;
   const int r_in = row - owner * R;
   bool mine_row = owner == rank;
   if (!mine_row) {
     // the owner must have read our rows of the previous round
-    if (rnd > 0 && !mbar_wait(xs.free_bar, static_cast<uint32_t>(rnd - 1) & 1, DPRC_DEVERR_CLUSTER))
+    if (rnd > 0 && !mbar_wait_lim(xs.free_bar, static_cast<uint32_t>(rnd - 1) & 1,
+                                  DPRC_DEVERR_CLUSTER, limit_ns, nullptr))
       ok = false;
     const int slot = rank < owner ? rank : rank - 1;
     const uint32_t dst = map_to_rank(xs.recv + (static_cast<size_t>(slot) * R + r_in) * K, owner);
@@ -193,7 +202,8 @@ __device__ __forceinline__ bool xchg_rows(const Xchg& xs, int cl, int rank, int 
       st_cluster_f4(dst + 16 * c4, make_float4(y[4 * c4], y[4 * c4 + 1], y[4 * c4 + 2], y[4 * c4 + 3]));
     mbar_arrive_remote(map_to_rank(xs.recv_bar, owner));
   } else {
-    if (!mbar_wait_cluster(xs.recv_bar, static_cast<uint32_t>(rnd) & 1, DPRC_DEVERR_CLUSTER))
+    if (!mbar_wait_cluster(xs.recv_bar, static_cast<uint32_t>(rnd) & 1, DPRC_DEVERR_CLUSTER,
+                           limit_ns))
       ok = false;
     float acc[K];
 #pragma unroll
@@ -258,6 +268,7 @@ struct HParams {
   float* c_out;
   int32_t* nonfinite;
   unsigned long long seed, step;   // +-1 projection: its Philox stream
+  unsigned long long wait_ns;      // limit of every wait in the launch
   LayerDesc layer[CAP];     // CAP = 1 for single-layer calls: a small parameter block
 };
 
@@ -329,6 +340,14 @@ __global__ void __launch_bounds__(hutch_threads<PM1>(), 1)
   extern __shared__ uint8_t smem_raw[];
   __shared__ float s_red[4];
 
+  // The schedule (block split, exchange partners, ready targets) is planned
+  // for clusters of a.cl CTAs.  A launch of any other cluster shape would make
+  // the exchange address ranks that do not exist: do nothing and say so.
+  if (cluster_nctarank() != static_cast<uint32_t>(a.cl)) {
+    if (threadIdx.x == 0) record_error(DPRC_DEVERR_LAUNCH);
+    return;
+  }
+
   uint8_t* ring = align_1024(smem_raw);
   uint64_t* bars = reinterpret_cast<uint64_t*>(ring + Cfg::kRing);
   uint64_t* full = bars;                  // [kStages]
@@ -337,10 +356,11 @@ __global__ void __launch_bounds__(hutch_threads<PM1>(), 1)
   uint64_t* acce_r = accf_r + 2;          // [2]
   uint64_t* accf_c = acce_r + 2;          // [2]
   uint64_t* acce_c = accf_c + 2;          // [2]
+  uint64_t* drain = acce_c + 2;           // MMA thread: all its MMAs complete
   Xchg xs;
-  xs.recv_bar = acce_c + 2;
-  xs.free_bar = acce_c + 3;
-  xs.norm_bar = acce_c + 4;  // [2]
+  xs.recv_bar = acce_c + 3;
+  xs.free_bar = acce_c + 4;
+  xs.norm_bar = acce_c + 5;  // [2]
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + Cfg::kBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   xs.norms = reinterpret_cast<float*>(bars + Cfg::kBars + 2);  // [2][8]
@@ -367,6 +387,7 @@ __global__ void __launch_bounds__(hutch_threads<PM1>(), 1)
       mbar_init(&acce_c[s], 4);
       mbar_init(&xs.norm_bar[s], cl > 1 ? cl - 1 : 1);
     }
+    mbar_init(drain, 1);
     if (cl > 1) {
       mbar_init(xs.recv_bar, (cl - 1) * (kRows / cl));
       mbar_init(xs.free_bar, cl - 1);
@@ -415,6 +436,17 @@ __global__ void __launch_bounds__(hutch_threads<PM1>(), 1)
   if (cl > 1) cluster_sync_all();  // peers' barriers exist before any remote arrive
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // The waits on other CTAs' progress (sketch ready, sketch buffer free) end
+  // within a.wait_ns; every wait inside the CTA or its cluster within twice
+  // that.  Those are downstream of the former (a tile waits for the sketch
+  // its W half needs, a peer's partials for the peer's tiles) and may start
+  // earlier, so the longer limit lets the wait that is the cause run out
+  // first and record its code.  The pipeline waits also end as soon as
+  // another role has set abort_flag, so after the first failure the roles
+  // unwind without each running out its own limit; the exchange waits do not
+  // (both ranks of a cluster always run the same exchanges).
+  const unsigned long long lim = a.wait_ns;
+  const unsigned long long lim2 = 2 * a.wait_ns;
 
   if (warp == 0) {
     // ---------------- TMA producer ----------------
@@ -423,8 +455,8 @@ __global__ void __launch_bounds__(hutch_threads<PM1>(), 1)
       long long it = 0;  // stages issued (both phases, all layers)
       auto take_slot = [&](long long i) -> int {
         const int s = static_cast<int>(i % kStages);
-        if (!mbar_wait(&empty[s], (static_cast<uint32_t>(i / kStages) & 1) ^ 1,
-                       DPRC_DEVERR_PIPE_EMPTY))
+        if (!mbar_wait_lim(&empty[s], (static_cast<uint32_t>(i / kStages) & 1) ^ 1,
+                           DPRC_DEVERR_PIPE_EMPTY, lim2, abort_flag))
           ok = false;
         return s;
       };
@@ -517,7 +549,7 @@ __global__ void __launch_bounds__(hutch_threads<PM1>(), 1)
           }
           if (w_done >= it - base) break;  // nothing left to complete (after an error)
           if (need_wait) {
-            if (wait_geq(&a.ready[l * a.B + cw.i], Ld.ready_target)) {
+            if (wait_geq(&a.ready[l * a.B + cw.i], Ld.ready_target, lim, abort_flag)) {
               fence_proxy_async_global();
               ready_i = cw.i;
             } else {
@@ -536,22 +568,26 @@ __global__ void __launch_bounds__(hutch_threads<PM1>(), 1)
         }
       }
       if (!ok) *abort_flag = 1;
-      // let every copy this thread issued land before the CTA can exit
+      // Let every copy this thread issued land before the CTA can exit.  Only
+      // the last kStages stages can be in flight: each earlier one was
+      // consumed (its slot was freed) before its slot was refilled.
       for (long long k = it - 1; k >= 0 && k >= it - kStages; --k)
-        mbar_wait(&full[k % kStages], static_cast<uint32_t>(k / kStages) & 1,
-                  DPRC_DEVERR_PIPE_FULL);
+        mbar_wait_lim(&full[k % kStages], static_cast<uint32_t>(k / kStages) & 1,
+                      DPRC_DEVERR_PIPE_FULL, lim2, nullptr);
     }
   } else if (warp == 1) {
     // ---------------- MMA issuer ----------------
     if (lane == 0) {
       bool ok = true;
+      bool issued = false;  // any MMA issued (to drain before the CTA exits)
       long long it = 0, seg1 = 0, seg2 = 0;
       constexpr uint32_t idesc1 = make_idesc_bf16(128, Cfg::kNR, false, true);
       constexpr uint32_t p_swz = swz_code_for_bytes(2 * Cfg::kNR);
       constexpr uint32_t idesc2 = make_idesc_bf16(128, Cfg::kNC, true, false);
       auto wait_full = [&](long long i) -> int {
         const int s = static_cast<int>(i % kStages);
-        if (!mbar_wait(&full[s], static_cast<uint32_t>(i / kStages) & 1, DPRC_DEVERR_PIPE_FULL))
+        if (!mbar_wait_lim(&full[s], static_cast<uint32_t>(i / kStages) & 1,
+                           DPRC_DEVERR_PIPE_FULL, lim2, abort_flag))
           ok = false;
         return s;
       };
@@ -561,8 +597,8 @@ __global__ void __launch_bounds__(hutch_threads<PM1>(), 1)
         const long long nb1 = count_blocks(Ld.ph1, m1);
         for (long long j = 0; j < nb1 && ok; ++j, ++seg1) {
           const int abuf = static_cast<int>(seg1 & 1);
-          if (!mbar_wait(&acce_r[abuf], (static_cast<uint32_t>(seg1 >> 1) & 1) ^ 1,
-                         DPRC_DEVERR_ACCUM)) {
+          if (!mbar_wait_lim(&acce_r[abuf], (static_cast<uint32_t>(seg1 >> 1) & 1) ^ 1,
+                             DPRC_DEVERR_ACCUM, lim2, abort_flag)) {
             ok = false;
             break;
           }
@@ -583,6 +619,7 @@ __global__ void __launch_bounds__(hutch_threads<PM1>(), 1)
               umma_bf16(tmem + abuf * Cfg::kAccR, ad, bd, idesc1,
                         (u == m1.ulo && kk == 0) ? 0u : 1u);
             }
+            issued = true;
             umma_commit(&empty[s]);
           }
           if (ok) umma_commit(&accf_r[abuf]);
@@ -591,8 +628,8 @@ __global__ void __launch_bounds__(hutch_threads<PM1>(), 1)
         const long long nb2 = count_blocks(Ld.ph2, m2);
         for (long long j = 0; j < nb2 && ok; ++j, ++seg2) {
           const int abuf = static_cast<int>(seg2 & 1);
-          if (!mbar_wait(&acce_c[abuf], (static_cast<uint32_t>(seg2 >> 1) & 1) ^ 1,
-                         DPRC_DEVERR_ACCUM)) {
+          if (!mbar_wait_lim(&acce_c[abuf], (static_cast<uint32_t>(seg2 >> 1) & 1) ^ 1,
+                             DPRC_DEVERR_ACCUM, lim2, abort_flag)) {
             ok = false;
             break;
           }
@@ -613,12 +650,16 @@ __global__ void __launch_bounds__(hutch_threads<PM1>(), 1)
               umma_bf16(tmem + Cfg::kColAcc0 + abuf * Cfg::kNC, ad, bd, idesc2,
                         (u == m2.ulo && kk == 0) ? 0u : 1u);
             }
+            issued = true;
             umma_commit(&empty[s]);
           }
           if (ok) umma_commit(&accf_c[abuf]);
         }
       }
       if (!ok) *abort_flag = 1;
+      // On every path (a wait that gave up skips the accumulator commits): no
+      // MMA may still write tensor memory once the CTA releases it.
+      if (issued) umma_drain(drain, lim2);
     }
   } else if (PM1 && warp >= 6) {
     // ---------------- sign-tile writers (+-1 projection, one layer) ----------------
@@ -636,8 +677,8 @@ __global__ void __launch_bounds__(hutch_threads<PM1>(), 1)
         const int s = static_cast<int>(it % kStages);
         bool free_ok = true;
         if (lane == 0)
-          free_ok = mbar_wait(&empty[s], (static_cast<uint32_t>(it / kStages) & 1) ^ 1,
-                              DPRC_DEVERR_PIPE_EMPTY);
+          free_ok = mbar_wait_lim(&empty[s], (static_cast<uint32_t>(it / kStages) & 1) ^ 1,
+                                  DPRC_DEVERR_PIPE_EMPTY, lim2, abort_flag);
         ok = __shfl_sync(0xffffffffu, free_ok ? 1 : 0, 0) != 0 && *abort_flag == 0;
         if (!ok) break;
         gen_sign_tile<K>(ring + s * Cfg::kSlot + Cfg::kRowG, rot_unit(m1, u), lane, warp - 6, rk,
@@ -674,15 +715,16 @@ __global__ void __launch_bounds__(hutch_threads<PM1>(), 1)
       if (CAP > 1 && nb1 > 0 && l >= 2) {
         // the previous user of this sketch buffer (layer l - 2) must be done
         if (threadIdx.x == 64 && ok &&
-            !wait_geq(&a.done2[l - 2], static_cast<int>(a.layer[CAP == 1 ? 0 : l - 2].ph2.nblocks)))
+            !wait_geq(&a.done2[l - 2], static_cast<int>(a.layer[CAP == 1 ? 0 : l - 2].ph2.nblocks),
+                      lim, abort_flag))
           *abort_flag = 1;
         named_bar_sync(1, 128);
       }
       for (long long j = 0; j < nb1; ++j, ++seg1) {
         const int abuf = static_cast<int>(seg1 & 1);
         bool live = ok &&
-                    mbar_wait(&accf_r[abuf], static_cast<uint32_t>(seg1 >> 1) & 1,
-                              DPRC_DEVERR_ACCUM) &&
+                    mbar_wait_lim(&accf_r[abuf], static_cast<uint32_t>(seg1 >> 1) & 1,
+                                  DPRC_DEVERR_ACCUM, lim2, abort_flag) &&
                     *abort_flag == 0;
         live = __all_sync(0xffffffffu, live);  // keep the warp's TMEM loads convergent
         if (!live) ok = false;
@@ -696,7 +738,7 @@ __global__ void __launch_bounds__(hutch_threads<PM1>(), 1)
         if (lane == 0) mbar_arrive(&acce_r[abuf]);
         bool mine_row = true;
         if (Ld.ph1.split) {
-          mine_row = xchg_rows<K>(xs, cl, rank, row, rnd, rnd + 1 == rounds, y, ok);
+          mine_row = xchg_rows<K>(xs, cl, rank, row, rnd, rnd + 1 == rounds, y, ok, lim2);
           ++rnd;
         }
         const long long b = m1.first + j * m1.step;
@@ -725,8 +767,8 @@ __global__ void __launch_bounds__(hutch_threads<PM1>(), 1)
       for (long long j = 0; j < nb2; ++j, ++seg2) {
         const int abuf = static_cast<int>(seg2 & 1);
         bool live = ok &&
-                    mbar_wait(&accf_c[abuf], static_cast<uint32_t>(seg2 >> 1) & 1,
-                              DPRC_DEVERR_ACCUM) &&
+                    mbar_wait_lim(&accf_c[abuf], static_cast<uint32_t>(seg2 >> 1) & 1,
+                                  DPRC_DEVERR_ACCUM, lim2, abort_flag) &&
                     *abort_flag == 0;
         live = __all_sync(0xffffffffu, live);
         if (!live) ok = false;
@@ -747,7 +789,7 @@ __global__ void __launch_bounds__(hutch_threads<PM1>(), 1)
         if (lane == 0) mbar_arrive(&acce_c[abuf]);
         bool mine_row = true;
         if (Ld.ph2.split) {
-          mine_row = xchg_rows<K>(xs, cl, rank, row, rnd, rnd + 1 == rounds, y, ok);
+          mine_row = xchg_rows<K>(xs, cl, rank, row, rnd, rnd + 1 == rounds, y, ok, lim2);
           ++rnd;
         }
         const long long b = m2.first + j * m2.step;
@@ -777,7 +819,8 @@ __global__ void __launch_bounds__(hutch_threads<PM1>(), 1)
               leader = 0;
             } else {
               if (!mbar_wait_cluster(&xs.norm_bar[nsplit2 & 1],
-                                     static_cast<uint32_t>(nsplit2 >> 1) & 1, DPRC_DEVERR_CLUSTER))
+                                     static_cast<uint32_t>(nsplit2 >> 1) & 1, DPRC_DEVERR_CLUSTER,
+                                     lim2))
                 ok = false;
               nb[0] = part;
               chunk = 0.f;
@@ -924,27 +967,37 @@ int resident_ctas(int cl) {
   return v;
 }
 
+// Launch of a planned schedule.  Without clusters the launch is cooperative:
+// the driver then guarantees that every CTA is resident at once, which the
+// cross-CTA waits rely on.  With clusters it is a plain cluster launch of at
+// most the number of clusters that fit on the device at once (the occupancy
+// query of resident_ctas), so on a device it has to itself every CTA is
+// resident too; when other work holds SMs, a waiting CTA's wait ends within
+// its limit with DPRC_DEVERR_READY instead of hanging.  Cooperative and
+// cluster attributes are never combined: that combination is the one launch
+// form of this kernel that faulted the GPU (under a profiler's replay).
+// `test_cl` > 0 (failure-detection test only): launch with clusters of that
+// size whatever the plan says.
 template <int K, int CAP, bool PM1>
-cudaError_t launch_k(const HParams<CAP>& a, int grid, cudaStream_t s) {
+cudaError_t launch_k(const HParams<CAP>& a, int grid, cudaStream_t s, int test_cl = 0) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(hutch_threads<PM1>());
   cfg.dynamicSmemBytes = HCfg<K>::smem(a.cl);
   cfg.stream = s;
-  cudaLaunchAttribute attr[2];
-  int na = 0;
-  attr[na].id = cudaLaunchAttributeCooperative;
-  attr[na].val.cooperative = 1;
-  ++na;
-  if (a.cl > 1) {
-    attr[na].id = cudaLaunchAttributeClusterDimension;
-    attr[na].val.clusterDim.x = a.cl;
-    attr[na].val.clusterDim.y = 1;
-    attr[na].val.clusterDim.z = 1;
-    ++na;
+  const int cl = test_cl > 0 ? test_cl : a.cl;
+  cudaLaunchAttribute attr[1];
+  if (cl > 1) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cl;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+  } else {
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
   }
   cfg.attrs = attr;
-  cfg.numAttrs = na;
+  cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, tc_hutch_kernel<K, CAP, PM1>, a);
 }
 
@@ -1053,10 +1106,22 @@ cudaError_t launch_cap(int L, const void* const* A, const void* const* G, const 
                        const int64_t* d, const int64_t* p, int64_t B, int64_t T, int64_t k,
                        const FusedScratch& ws, float* n_out, int accumulate, uint64_t seed,
                        uint64_t step, cudaStream_t s, bool* launched,
-                       const ClipOut* clip) {
+                       const ClipOut* clip, const HutchFaultTest* test = nullptr) {
   static thread_local HParams<CAP> a;  // up to ~26 KB: kept off the stack
   int grid = 0;
   if (!plan_fused<CAP, PM1>(L, d, p, B, T, k, a, grid)) return cudaSuccess;
+  int test_cl = 0;
+  a.wait_ns = kWaitLimitNs;
+  if (test != nullptr) {
+    a.wait_ns = test->wait_ns;
+    if (test->mode == kFaultReadyNeverMet) {
+      for (int l = 0; l < L; ++l) a.layer[l].ready_target += 1;  // one more than phase 1 adds
+    } else {
+      if (a.cl != 1) return cudaSuccess;  // needs a plan without clusters
+      test_cl = 2;
+      grid += grid & 1;  // a whole number of clusters
+    }
+  }
   const int ik = static_cast<int>(k);
   a.tpad = ws.tpad;
   a.W[0] = static_cast<__nv_bfloat16*>(ws.W[0]);
@@ -1087,8 +1152,8 @@ cudaError_t launch_cap(int L, const void* const* A, const void* const* G, const 
         !make_tmap_3d_bf16(&Ld.ma, A[l], d[l], T, B, d[l], T * d[l], 64, kTok, 128))
       return cudaErrorInvalidValue;
   }
-  const cudaError_t e =
-      ik == 16 ? launch_k<16, CAP, PM1>(a, grid, s) : launch_k<32, CAP, PM1>(a, grid, s);
+  const cudaError_t e = ik == 16 ? launch_k<16, CAP, PM1>(a, grid, s, test_cl)
+                                 : launch_k<32, CAP, PM1>(a, grid, s, test_cl);
   if (e == cudaSuccess) {
     *launched = true;
   } else if (e == cudaErrorCooperativeLaunchTooLarge || e == cudaErrorNotSupported ||
@@ -1113,6 +1178,19 @@ cudaError_t launch_tc_hutch_layers(int L, const void* const* A, const void* cons
                                 launched, clip);
   return launch_cap<kMaxFusedLayers, false>(L, A, G, P, d, p, B, T, k, ws, n_out, accumulate, 0,
                                             0, s, launched, clip);
+}
+
+cudaError_t launch_tc_hutch_fault_test(int L, const void* const* A, const void* const* G,
+                                       const void* const* P, const int64_t* d, const int64_t* p,
+                                       int64_t B, int64_t T, int64_t k, const FusedScratch& ws,
+                                       float* n_out, const HutchFaultTest& test, cudaStream_t s,
+                                       bool* launched) {
+  *launched = false;
+  if (L == 1)
+    return launch_cap<1, false>(L, A, G, P, d, p, B, T, k, ws, n_out, 0, 0, 0, s, launched,
+                                nullptr, &test);
+  return launch_cap<kMaxFusedLayers, false>(L, A, G, P, d, p, B, T, k, ws, n_out, 0, 0, 0, s,
+                                            launched, nullptr, &test);
 }
 
 cudaError_t launch_tc_hutch_pm1(const void* A, const void* G, int64_t B, int64_t T, int64_t d,

@@ -175,7 +175,8 @@ __global__ void __launch_bounds__(192, 1)
   uint64_t* empty = full + kNwStages;
   uint64_t* accf = empty + kNwStages;  // [2]
   uint64_t* acce = accf + 2;           // [2]
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acce + 2);
+  uint64_t* drain = acce + 2;          // MMA thread: all its MMAs complete
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acce + 3);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -205,6 +206,7 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(&accf[b], 1);
       mbar_init(&acce[b], 4);
     }
+    mbar_init(drain, 1);
     fence_mbar_init();
     *abort_flag = 0;
     const int i0 = static_cast<int>(blockIdx.x / a.mt);
@@ -253,7 +255,7 @@ __global__ void __launch_bounds__(192, 1)
       constexpr uint32_t idesc = make_idesc_bf16(kNwM, N, true, true);
       constexpr uint32_t nswz = swz_code_for_bytes(2 * N);
       long long it = 0;
-      bool ok = true;
+      bool ok = true, issued = false;
       for (long long j = 0; j < my_tiles && ok; ++j) {
         const int abuf = static_cast<int>(j & 1);
         if (!mbar_wait(&acce[abuf], static_cast<uint32_t>((j >> 1) & 1) ^ 1, DPRC_DEVERR_ACCUM)) {
@@ -284,9 +286,13 @@ __global__ void __launch_bounds__(192, 1)
             umma_bf16(tmem + abuf * N, ad, bd, idesc, (u == 0 && kk == 0) ? 0u : 1u);
           }
           umma_commit(&empty[s]);
+          issued = true;
         }
         if (ok) umma_commit(&accf[abuf]);
       }
+      // on every path out of the loop: no MMA still writes the tensor memory
+      // the CTA releases
+      if (issued) umma_drain(drain, kWaitLimitNs);
     }
   } else {
     // ---------------- epilogue warps 2..5 ----------------

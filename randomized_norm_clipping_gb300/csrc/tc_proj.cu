@@ -137,10 +137,12 @@ __device__ __forceinline__ bool cluster_reduce_rows(const XchgSmem& xs, int cl, 
   return true;
 }
 
-// Shared prologue of both kernels: pipeline barriers, cluster barriers, TMEM.
+// Shared prologue of both kernels: pipeline barriers, the MMA drain barrier,
+// cluster barriers.
 template <int kStages>
 __device__ __forceinline__ void init_barriers(uint64_t* full, uint64_t* empty, uint64_t* accf,
-                                              uint64_t* acce, const XchgSmem& xs, int cl) {
+                                              uint64_t* acce, uint64_t* drain, const XchgSmem& xs,
+                                              int cl) {
   for (int s = 0; s < kStages; ++s) {
     mbar_init(&full[s], 1);
     mbar_init(&empty[s], 1);
@@ -149,6 +151,7 @@ __device__ __forceinline__ void init_barriers(uint64_t* full, uint64_t* empty, u
     mbar_init(&accf[b], 1);
     mbar_init(&acce[b], 4);
   }
+  mbar_init(drain, 1);
   if (cl > 1) {
     mbar_init(xs.recv_bar, (cl - 1) * (128 / cl));
     mbar_init(xs.norm_bar, cl - 1);
@@ -209,6 +212,12 @@ __global__ void __launch_bounds__(192, 2)
 
   const Sched& sc = a.sched;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // The schedule splits blocks over clusters of sc.cl CTAs; a launch of any
+  // other cluster shape would address ranks that do not exist: refuse it.
+  if (cluster_nctarank() != static_cast<uint32_t>(sc.cl)) {
+    if (threadIdx.x == 0) record_error(DPRC_DEVERR_LAUNCH);
+    return;
+  }
   // The whole grid fits at once: the next kernel may start its prologue.
   pdl_launch_dependents();
   if (blockIdx.x == 0 && a.zero_ptr != nullptr)
@@ -226,7 +235,8 @@ __global__ void __launch_bounds__(192, 2)
   XchgSmem xs;
   xs.recv_bar = acce + 2;
   xs.norm_bar = acce + 3;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acce + 4);
+  uint64_t* drain = acce + 4;  // MMA thread: all its MMAs complete
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acce + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   xs.norms = reinterpret_cast<float*>(tmem_slot + 2);
   xs.recv = reinterpret_cast<float*>(smem + Cfg::kBase - 1024);
@@ -246,7 +256,7 @@ __global__ void __launch_bounds__(192, 2)
   const long long total_units = wk.b1 > wk.b0 ? (wk.b1 - wk.b0) * nu : 0;
   const int pre = static_cast<int>(total_units < Cfg::kStages ? total_units : Cfg::kStages);
   if (threadIdx.x == 0) {
-    init_barriers<Cfg::kStages>(full, empty, accf, acce, xs, sc.cl);
+    init_barriers<Cfg::kStages>(full, empty, accf, acce, drain, xs, sc.cl);
     *abort_flag = 0;
     for (int it = 0; it < pre; ++it) load_stage(it, it);
   }
@@ -296,7 +306,7 @@ __global__ void __launch_bounds__(192, 2)
       constexpr uint32_t r_swz = swz_code_for_bytes(2 * NMMA);
       long long it = 0;
       int seg = 0;
-      bool ok = true;
+      bool ok = true, issued = false;
       for (long long b = wk.b0; b < wk.b1 && ok; ++b, ++seg) {
         const int abuf = seg & 1;
         if (!mbar_wait(&acce[abuf], ((seg >> 1) & 1) ^ 1, DPRC_DEVERR_ACCUM)) {
@@ -326,9 +336,13 @@ __global__ void __launch_bounds__(192, 2)
                       (kc == wk.ulo && kk == 0) ? 0u : 1u);
           }
           umma_commit(&empty[s]);
+          issued = true;
         }
         if (ok) umma_commit(&accf[abuf]);
       }
+      // on every path out of the loop: no MMA still writes the tensor memory
+      // the CTA releases
+      if (issued) umma_drain(drain, kWaitLimitNs);
     }
   } else {
     // ---------------- epilogue warps 2..5 ----------------
@@ -374,6 +388,9 @@ __global__ void __launch_bounds__(192, 2)
     tc_fence_after();
     tmem_dealloc(tmem, Cfg::kTmemCols);
   }
+  // every distributed shared memory access of the cluster is complete before
+  // any of its CTAs exits
+  if (sc.cl > 1) cluster_sync_all();
 }
 
 // ===========================================================================
@@ -424,6 +441,12 @@ __global__ void __launch_bounds__(192, ColCfg<NMMA>::kCtasPerSm)
   __shared__ float s_red[4];
 
   const Sched& sc = a.sched;
+  // The schedule splits blocks over clusters of sc.cl CTAs; a launch of any
+  // other cluster shape would address ranks that do not exist: refuse it.
+  if (cluster_nctarank() != static_cast<uint32_t>(sc.cl)) {
+    if (threadIdx.x == 0) record_error(DPRC_DEVERR_LAUNCH);
+    return;
+  }
   const CtaWork wk = cta_work(sc);
   const int nu = wk.uhi - wk.ulo;
 
@@ -437,7 +460,8 @@ __global__ void __launch_bounds__(192, ColCfg<NMMA>::kCtasPerSm)
   XchgSmem xs;
   xs.recv_bar = acce + 2;
   xs.norm_bar = acce + 3;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acce + 4);
+  uint64_t* drain = acce + 4;  // MMA thread: all its MMAs complete
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acce + 5);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   xs.norms = reinterpret_cast<float*>(tmem_slot + 2);
   xs.recv = reinterpret_cast<float*>(smem + Cfg::kBase - 1024);
@@ -461,7 +485,7 @@ __global__ void __launch_bounds__(192, ColCfg<NMMA>::kCtasPerSm)
   const int pre = static_cast<int>(total < Cfg::kStages ? total : Cfg::kStages);
 
   if (threadIdx.x == 0) {
-    init_barriers<Cfg::kStages>(full, empty, accf, acce, xs, sc.cl);
+    init_barriers<Cfg::kStages>(full, empty, accf, acce, drain, xs, sc.cl);
     *abort_flag = 0;
     // the producer (this thread) issues the X boxes of the first stages now:
     // X does not depend on the previous kernel, and their DRAM round trip
@@ -535,7 +559,7 @@ __global__ void __launch_bounds__(192, ColCfg<NMMA>::kCtasPerSm)
       constexpr uint32_t idesc = make_idesc_bf16(128, NMMA, true, false);
       long long it = 0;
       int seg = 0;
-      bool ok = true;
+      bool ok = true, issued = false;
       for (long long b = wk.b0; b < wk.b1 && ok; ++b, ++seg) {
         const int abuf = seg & 1;
         if (!mbar_wait(&acce[abuf], ((seg >> 1) & 1) ^ 1, DPRC_DEVERR_ACCUM)) {
@@ -565,9 +589,13 @@ __global__ void __launch_bounds__(192, ColCfg<NMMA>::kCtasPerSm)
             umma_bf16(tmem + abuf * Cfg::kAcc, ad, bd, idesc, (u == 0 && kk == 0) ? 0u : 1u);
           }
           umma_commit(&empty[s]);
+          issued = true;
         }
         if (ok) umma_commit(&accf[abuf]);
       }
+      // on every path out of the loop: no MMA still writes the tensor memory
+      // the CTA releases
+      if (issued) umma_drain(drain, kWaitLimitNs);
     }
   } else {
     // ---------------- epilogue warps 2..5 ----------------
@@ -679,6 +707,9 @@ __global__ void __launch_bounds__(192, ColCfg<NMMA>::kCtasPerSm)
     tc_fence_after();
     tmem_dealloc(tmem, Cfg::kTmemCols);
   }
+  // every distributed shared memory access of the cluster is complete before
+  // any of its CTAs exits
+  if (sc.cl > 1) cluster_sync_all();
 }
 
 // Raises a kernel's dynamic shared memory limit once per device (the attribute

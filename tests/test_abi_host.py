@@ -175,6 +175,25 @@ def test_argument_errors_return_before_device_work(lib):
     w = lib.dprc_philox_words
     assert w(None, 4, 0, 1, 1, None) == 1
     assert w(None, 0, 0, 1, 1, None) == 0
+    na = lib.dprc_norm_hutch_noalloc
+    assert na(None, _vp(A16), _vp(A16), 1, 1, 64, 8, 8, 8, _vp(A16), 0, None) == 1
+    assert na(_vp(A16), _vp(A16), _vp(A16), 1, 1, 64, 8, 8, 0, _vp(A16), 0, None) == 2
+    assert na(_vp(A16), _vp(A16 + 2), _vp(A16), 1, 1, 64, 8, 8, 8, _vp(A16), 0, None) == 4
+    # beyond the built-in scratch: refused before any device is needed
+    assert na(_vp(A16), _vp(A16), _vp(A16), 1, 64, 32768, 8192, 8192, 32, _vp(A16), 0,
+              None) == 9
+    tf = lib.dprc_test_hutch_fault
+    one = ctypes.c_void_p * 1
+    p1, s1 = one(A16), (ctypes.c_int64 * 1)(256)
+    args = (1, p1, p1, p1, s1, s1, 2, 256, 32, _vp(A16), _vp(A16), big, None)
+    assert tf(0, 1000000, *args[:1], None, *args[2:]) == 1       # no A list
+    assert tf(7, 1000000, *args) == 2                            # unknown mode
+    assert tf(0, 10, *args) == 2                                 # wait limit too short
+    assert tf(0, 3000000000, *args) == 2                         # beyond the kernels' own limit
+    assert tf(0, 1000000, 57, *args[1:]) == 2                    # more layers than one launch
+    assert tf(0, 1000000, *args[:8], 64, *args[9:]) == 2         # k not 16 or 32
+    assert tf(0, 1000000, *args[:1], one(A16 + 2), *args[2:]) == 4  # misaligned A
+    assert tf(0, 1000000, *args[:10], None, big, None) == 5      # no workspace
 
 
 def test_valid_calls_without_a_gpu_fail_loudly(lib):
@@ -184,6 +203,9 @@ def test_valid_calls_without_a_gpu_fail_loudly(lib):
     st = lib.dprc_norm_hutch(_vp(A16), _vp(A16), _vp(A16), 1, 1, 1, 8, 8, 16, _vp(A16), 0,
                              _vp(A16), 1 << 30, None)
     assert st == 8  # DPRC_ERR_DEVICE: nothing was launched
+    st = lib.dprc_norm_hutch_noalloc(_vp(A16), _vp(A16), _vp(A16), 1, 1, 64, 8, 8, 8, _vp(A16),
+                                     0, None)
+    assert st == 8  # the device check comes before the scratch lookup
     # the launch-count query enqueues nothing and reports 0 without a device
     assert lib.dprc_norm_hutch_launches(1, 8, 4096, 2048, 2048, 32) == 0
 

@@ -2,8 +2,9 @@
 
 It serves callers that cannot allocate device memory where they need the
 norm; its scratch is a fixed array inside the library.  Checked through the C
-ABI against dprc_norm_hutch on the same inputs, on two calls in a row (the
-second with other sizes, so the array's leftover contents must not matter).
+ABI against dprc_norm_hutch on the same inputs, on calls in a row with other
+sizes (larger after smaller and smaller after larger, so the array's leftover
+contents must not matter) and with accumulate set on repeated calls.
 This file is collected last so a failure here cannot hide another test.
 """
 
@@ -41,12 +42,12 @@ def _vp(t):
     return ctypes.c_void_p(t.data_ptr())
 
 
-def _noalloc(lib, A, G, P, n):
+def _noalloc(lib, A, G, P, n, accumulate=0):
     B, T, d = A.shape
     p, k = P.shape
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
-    return lib.dprc_norm_hutch_noalloc(_vp(A), _vp(G), _vp(P), 1, B, T, d, p, k, _vp(n), 0,
-                                       stream)
+    return lib.dprc_norm_hutch_noalloc(_vp(A), _vp(G), _vp(P), 1, B, T, d, p, k, _vp(n),
+                                       accumulate, stream)
 
 
 def _with_workspace(lib, A, G, P, n):
@@ -72,6 +73,31 @@ def test_noalloc_matches_workspace_entry_on_two_calls(lib):
         ref = n_ref.cpu().double().numpy()
         got = n_new.cpu().double().numpy()
         assert np.all(np.abs(got - ref) <= RTOL * np.abs(ref)), (got, ref)
+
+
+def test_noalloc_small_after_large_and_accumulate(lib):
+    # the array keeps the last call's contents: a smaller call after a larger
+    # one (other sketch stride and offsets) must not see them, and two calls
+    # in a row with accumulate = 1 must add on the caller's n
+    big = (8, 4096, 2048, 2048, 32)
+    Ab, Gb, Pb = _case(*big, 3)
+    nb = torch.zeros(big[0], device=DEV)
+    assert _noalloc(lib, Ab, Gb, Pb, nb) == 0
+    small = (4, 1000, 512, 768, 32)
+    A, G, P = _case(*small, 4)
+    n_ref = torch.zeros(small[0], device=DEV)
+    assert _with_workspace(lib, A, G, P, n_ref) == 0
+    ref = n_ref.cpu().double().numpy()
+    n_new = torch.full((small[0],), -1.0, device=DEV)
+    assert _noalloc(lib, A, G, P, n_new, accumulate=0) == 0
+    torch.cuda.synchronize()
+    got = n_new.cpu().double().numpy()
+    assert np.all(np.abs(got - ref) <= RTOL * np.abs(ref)), (got, ref)
+    for times in (2, 3):
+        assert _noalloc(lib, A, G, P, n_new, accumulate=1) == 0
+        torch.cuda.synchronize()
+        got = n_new.cpu().double().numpy()
+        assert np.all(np.abs(got - times * ref) <= RTOL * times * np.abs(ref)), (times, got, ref)
 
 
 def test_noalloc_rejects_calls_beyond_its_scratch(lib):
