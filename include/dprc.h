@@ -340,6 +340,23 @@ dprc_status dprc_add_noise(float* grad, int64_t N, float sigma, float C, uint64_
                            uint64_t step, void* stream);
 
 /*
+ * dprc_add_noise on one piece of a gradient that the caller keeps in several
+ * buffers (one per weight, say), without gathering them into one: the pieces
+ * laid end to end form the aggregated gradient, and the piece that starts at
+ * element first_element of it gets the same noise as that range would get
+ * from dprc_add_noise on the whole (papernotes.org, "Method > Overall
+ * framework": sigma*C*N(0, I) on the aggregated gradient):
+ *     grad[i] += sigma * C * z_{first_element + i},   0 <= i < N
+ * with z_e as in dprc_add_noise.  dtype DPRC_F32 or DPRC_BF16: a bf16
+ * gradient gets its sum formed in fp32 and rounded once to nearest.
+ *  grad device [N] of dtype, in place, 16-byte aligned; N >= 0;
+ *  first_element + N must not exceed 2^64.  Errors as dprc_add_noise, plus
+ *  DPRC_ERR_DTYPE.
+ */
+dprc_status dprc_add_noise_at(void* grad, dprc_dtype dtype, int64_t N, uint64_t first_element,
+                              float sigma, float C, uint64_t seed, uint64_t step, void* stream);
+
+/*
  * The raw Philox4x32-10 stream behind dprc_add_noise (Salmon et al.,
  * "Parallel Random Numbers: As Easy as 1, 2, 3", SC'11): block j is the
  * generator applied to the counter (j_lo, j_hi, step_lo, step_hi) under the
@@ -365,6 +382,9 @@ dprc_status dprc_philox_words(uint32_t* out, int64_t n_blocks, uint64_t first_bl
 #define DPRC_DEVERR_READY 5       /* the projection waited too long for a sample's sketch */
 #define DPRC_DEVERR_LAUNCH 6      /* a kernel found its launch's cluster shape other than
                                      planned and returned before doing anything */
+#define DPRC_DEVERR_BOUNDS 7      /* bounds-checked build only (libdprc_debug.so): an index
+                                     failed its check and the access was skipped; the
+                                     word's bits above the low 8 hold the source line */
 dprc_status dprc_device_error(int32_t* out, int reset);
 
 /*

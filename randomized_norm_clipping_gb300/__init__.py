@@ -25,6 +25,7 @@ from .binding import (  # noqa: F401
     DprcError,
     dprc_abi_version,
     dprc_add_noise,
+    dprc_add_noise_at,
     dprc_clip_factors,
     dprc_device_error,
     dprc_exact_norm,

@@ -16,7 +16,11 @@ import threading
 import torch
 
 PKG_DIR = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(PKG_DIR, "libdprc.so")
+# DPRC_LIBRARY=debug loads the bounds-checked build (libdprc_debug.so: every
+# computed index checked before its access, failures recorded in the device
+# error word as DPRC_DEVERR_BOUNDS); anything else, the release build.
+LIB_PATH = os.path.join(
+    PKG_DIR, "libdprc_debug.so" if os.environ.get("DPRC_LIBRARY") == "debug" else "libdprc.so")
 
 DPRC_F32, DPRC_BF16 = 0, 1
 (DPRC_OP_HUTCH, DPRC_OP_HUTCHPP, DPRC_OP_EXACT, DPRC_OP_HUTCH_LAYERS, DPRC_OP_HUTCH_PM1,
@@ -47,6 +51,9 @@ _PROTOS = [
      [_c.c_void_p, _c.c_int64, _c.c_float, _c.c_void_p, _c.c_void_p, _c.c_void_p]),
     ("dprc_add_noise", _c.c_int,
      [_c.c_void_p, _c.c_int64, _c.c_float, _c.c_float, _c.c_uint64, _c.c_uint64, _c.c_void_p]),
+    ("dprc_add_noise_at", _c.c_int,
+     [_c.c_void_p, _c.c_int, _c.c_int64, _c.c_uint64, _c.c_float, _c.c_float, _c.c_uint64,
+      _c.c_uint64, _c.c_void_p]),
     ("dprc_philox_words", _c.c_int,
      [_c.c_void_p, _c.c_int64, _c.c_uint64, _c.c_uint64, _c.c_uint64, _c.c_void_p]),
     ("dprc_device_error", _c.c_int, [_c.c_void_p, _c.c_int]),
@@ -322,7 +329,7 @@ def dprc_norm_hutch_noalloc(A, G, P, n, accumulate=False, stream=None):
 
 # Device error codes (DPRC_DEVERR_* of include/dprc.h).
 (DPRC_DEVERR_PIPE_FULL, DPRC_DEVERR_PIPE_EMPTY, DPRC_DEVERR_ACCUM, DPRC_DEVERR_CLUSTER,
- DPRC_DEVERR_READY, DPRC_DEVERR_LAUNCH) = (1, 2, 3, 4, 5, 6)
+ DPRC_DEVERR_READY, DPRC_DEVERR_LAUNCH, DPRC_DEVERR_BOUNDS) = (1, 2, 3, 4, 5, 6, 7)
 FAULT_READY_NEVER_MET, FAULT_CLUSTER_SHAPE = 0, 1
 
 
@@ -395,6 +402,19 @@ def dprc_add_noise(grad, sigma, C, seed, step, stream=None):
                               int(seed) & (2**64 - 1), int(step) & (2**64 - 1),
                               _stream(grad, stream))
     _check("dprc_add_noise", st)
+    return grad
+
+
+def dprc_add_noise_at(grad, first_element, sigma, C, seed, step, stream=None):
+    """grad += sigma * C * z[first_element : first_element + grad.numel()], in
+    place (float32 or bfloat16): the noise of one piece of a gradient kept in
+    several buffers (see include/dprc.h)."""
+    _need_cuda(grad)
+    st = lib().dprc_add_noise_at(_ptr(grad), _dtype_code(grad), grad.numel(),
+                                 int(first_element) & (2**64 - 1), float(sigma), float(C),
+                                 int(seed) & (2**64 - 1), int(step) & (2**64 - 1),
+                                 _stream(grad, stream))
+    _check("dprc_add_noise_at", st)
     return grad
 
 

@@ -1,7 +1,12 @@
-"""Builds libdprc.so in-tree from the CUDA sources in csrc/ (sm_103a only).
+"""Builds libdprc.so in-tree from the CUDA sources in csrc/ (sm_103a only),
+and its bounds-checked variant libdprc_debug.so (the same sources with
+DPRC_DEBUG defined: every computed global or distributed-shared-memory index
+is checked before its access, a failed check is recorded in the device error
+word and the access skipped).
 
-Each translation unit is compiled in parallel, then linked into one shared
-library next to this file.  Run ``python -m randomized_norm_clipping_gb300.build``.
+Every translation unit of both variants is compiled in parallel, then each
+variant is linked into one shared library next to this file.  Run
+``python -m randomized_norm_clipping_gb300.build``.
 """
 
 from __future__ import annotations
@@ -19,9 +24,11 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIB_NAME = "libdprc.so"
 LIB_PATH = os.path.join(PKG_DIR, LIB_NAME)
+DEBUG_LIB_PATH = os.path.join(PKG_DIR, "libdprc_debug.so")
 
 SOURCES = ["api.cu", "tc_proj.cu", "tc_exact.cu", "tc_narrow.cu", "tc_hutch.cu", "simt.cu", "qr.cu", "qr_cluster.cu", "noise.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+VARIANTS = {"release": ([], LIB_PATH), "debug": (["-DDPRC_DEBUG"], DEBUG_LIB_PATH)}
 
 
 def _nvcc():
@@ -36,28 +43,39 @@ def _flags():
             "-I" + INCLUDE, "-I" + CSRC]
 
 
-def _compile(src):
-    obj = os.path.join(BUILD_DIR, os.path.splitext(src)[0] + ".o")
-    cmd = [_nvcc(), *_flags(), "-c", os.path.join(CSRC, src), "-o", obj]
+def _compile(job):
+    variant, src = job
+    out_dir = os.path.join(BUILD_DIR, variant)
+    obj = os.path.join(out_dir, os.path.splitext(src)[0] + ".o")
+    cmd = [_nvcc(), *_flags(), *VARIANTS[variant][0], "-c", os.path.join(CSRC, src), "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
-        raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")
+        raise RuntimeError(f"nvcc failed on {src} ({variant}):\n{r.stdout}\n{r.stderr}")
     return obj
 
 
-def build(verbose=False):
-    """Compiles every translation unit and links libdprc.so; returns its path."""
-    os.makedirs(BUILD_DIR, exist_ok=True)
-    with concurrent.futures.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        objs = list(ex.map(_compile, SOURCES))
-    tmp = LIB_PATH + ".tmp"
+def _link(objs, path):
+    tmp = path + ".tmp"
     cmd = [_nvcc(), *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB_PATH)
-    if verbose:
-        print("built", LIB_PATH)
+    os.replace(tmp, path)
+
+
+def build(verbose=False, variants=("release", "debug")):
+    """Compiles every translation unit of the given variants and links each
+    into its shared library; returns the release library's path."""
+    for v in variants:
+        os.makedirs(os.path.join(BUILD_DIR, v), exist_ok=True)
+    jobs = [(v, src) for v in variants for src in SOURCES]
+    workers = min(len(jobs), max(4, os.cpu_count() or 4))
+    with concurrent.futures.ThreadPoolExecutor(max_workers=workers) as ex:
+        objs = list(ex.map(_compile, jobs))
+    for v in variants:
+        _link([o for (vv, _), o in zip(jobs, objs) if vv == v], VARIANTS[v][1])
+        if verbose:
+            print("built", VARIANTS[v][1])
     return LIB_PATH
 
 

@@ -1027,6 +1027,25 @@ dprc_status dprc_add_noise(float* grad, int64_t N, float sigma, float C, uint64_
   return cuda_status(e);
 }
 
+dprc_status dprc_add_noise_at(void* grad, dprc_dtype dtype, int64_t N, uint64_t first_element,
+                             float sigma, float C, uint64_t seed, uint64_t step, void* stream) {
+  if (dtype != DPRC_F32 && dtype != DPRC_BF16) return DPRC_ERR_DTYPE;
+  if (N < 0) return DPRC_ERR_SHAPE;
+  if (N > 0 && !grad) return DPRC_ERR_NULL;
+  if (!(sigma >= 0.f) || !(sigma < __builtin_inff()) || !(C >= 0.f) || !(C < __builtin_inff()))
+    return DPRC_ERR_SHAPE;
+  // the stream has 2^66 elements; the call's range must not wrap
+  if (static_cast<uint64_t>(N) > ~uint64_t(0) - first_element) return DPRC_ERR_SHAPE;
+  if (N > 0 && !aligned16(grad)) return DPRC_ERR_ALIGN;
+  if (N == 0) return DPRC_OK;
+  if (!device_ok()) return DPRC_ERR_DEVICE;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  mark(0, s);
+  const cudaError_t e = launch_noise_at(grad, dtype, N, first_element, sigma, C, seed, step, s);
+  mark(1, s);
+  return cuda_status(e);
+}
+
 dprc_status dprc_philox_words(uint32_t* out, int64_t n_blocks, uint64_t first_block,
                               uint64_t seed, uint64_t step, void* stream) {
   if (n_blocks < 0) return DPRC_ERR_SHAPE;

@@ -49,6 +49,22 @@ __device__ __forceinline__ void record_error(int code) {
   atomicCAS(&g_device_error, 0, code);
 }
 
+// Bounds-checked build (DPRC_DEBUG, built as libdprc_debug.so): every
+// computed global or distributed-shared-memory index is checked before its
+// access with DPRC_IN(cond).  A failed check records DPRC_DEVERR_BOUNDS with
+// the source line in the bits above the code (first writer wins) and the
+// access is skipped: no trap, the context stays usable and the host reads
+// where it happened.  Release builds compile the checks away.
+#ifdef DPRC_DEBUG
+__device__ __forceinline__ bool dbg_in(bool ok, int line) {
+  if (!ok) atomicCAS(&g_device_error, 0, DPRC_DEVERR_BOUNDS | (line << 8));
+  return ok;
+}
+#define DPRC_IN(cond) ::dprc::dbg_in(static_cast<bool>(cond), __LINE__)
+#else
+#define DPRC_IN(cond) true
+#endif
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

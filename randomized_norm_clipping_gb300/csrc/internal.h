@@ -266,6 +266,10 @@ cudaError_t launch_clip(const float* n, int64_t B, float C, float* c, int32_t* n
                         cudaStream_t s);
 cudaError_t launch_noise(float* grad, int64_t N, float sigma, float C, uint64_t seed,
                          uint64_t step, cudaStream_t s);
+// grad[i] += sigma C z_{first_element + i}, grad fp32 or bf16 (sum in fp32,
+// rounded once).
+cudaError_t launch_noise_at(void* grad, dprc_dtype dt, int64_t N, uint64_t first_element,
+                            float sigma, float C, uint64_t seed, uint64_t step, cudaStream_t s);
 cudaError_t launch_philox_words(uint32_t* out, int64_t n_blocks, uint64_t first_block,
                                 uint64_t seed, uint64_t step, cudaStream_t s);
 

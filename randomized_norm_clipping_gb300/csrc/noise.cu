@@ -75,8 +75,11 @@ __device__ __forceinline__ float4 add_noise4(float4 g, uint4 w, float scale) {
 constexpr int kNoiseUnroll = 2;
 constexpr int kNoiseCtasPerSm = 64;
 
+// grad[i] += scale z_{4 blk0 + i}: the fp32 buffer starts at a block boundary
+// of the stream (blk0 = 0 for a whole gradient).
 __global__ void __launch_bounds__(256) noise_kernel(float* __restrict__ grad, long long n,
-                                                    float scale, uint64_t seed, uint64_t step) {
+                                                    float scale, uint64_t seed, uint64_t step,
+                                                    uint64_t blk0) {
   const RoundKeys rk = round_keys(seed);
   const long long nblk = n >> 2;
   float4* g4 = reinterpret_cast<float4*>(grad);
@@ -93,16 +96,73 @@ __global__ void __launch_bounds__(256) noise_kernel(float* __restrict__ grad, lo
     for (int u = 0; u < kNoiseUnroll; ++u) {
       const long long j = base + u * blockDim.x + threadIdx.x;
       if (j < nblk)
-        __stcs(g4 + j, add_noise4(g[u], philox_block(static_cast<uint64_t>(j), step, rk), scale));
+        __stcs(g4 + j,
+               add_noise4(g[u], philox_block(blk0 + static_cast<uint64_t>(j), step, rk), scale));
     }
   }
   // ragged tail: the last n & 3 elements, one thread
   if (blockIdx.x == 0 && threadIdx.x == 0 && (n & 3) != 0) {
-    const uint4 w = philox_block(static_cast<uint64_t>(nblk), step, rk);
+    const uint4 w = philox_block(blk0 + static_cast<uint64_t>(nblk), step, rk);
     const float2 z01 = box_muller(w.x, w.y);
     const float2 z23 = box_muller(w.z, w.w);
     const float z[4] = {z01.x, z01.y, z23.x, z23.y};
     for (long long e = nblk * 4; e < n; ++e) grad[e] = fmaf(scale, z[e - nblk * 4], grad[e]);
+  }
+}
+
+// The four normals of stream block q (words 0..3 as elements 4q .. 4q + 3).
+__device__ __forceinline__ void block_normals(uint64_t q, uint64_t step, const RoundKeys& rk,
+                                              float* z) {
+  const uint4 w = philox_block(q, step, rk);
+  const float2 z01 = box_muller(w.x, w.y);
+  const float2 z23 = box_muller(w.z, w.w);
+  z[0] = z01.x;
+  z[1] = z01.y;
+  z[2] = z23.x;
+  z[3] = z23.y;
+}
+
+__device__ __forceinline__ float load_f(const float* p) { return *p; }
+__device__ __forceinline__ float load_f(const __nv_bfloat16* p) { return __bfloat162float(*p); }
+__device__ __forceinline__ void store_f(float* p, float v) { *p = v; }
+__device__ __forceinline__ void store_f(__nv_bfloat16* p, float v) { *p = __float2bfloat16_rn(v); }
+
+// grad[i] += scale z_{e0 + i} for any element type TG (fp32 or bf16) and any
+// stream offset e0 with e0 & 3 == R: a thread owns V consecutive elements (16
+// bytes), whose stream positions span NB Philox blocks; the sum is formed in
+// fp32 and rounded once to TG.  The last n mod V elements: one thread.
+template <typename TG, int R>
+__global__ void __launch_bounds__(256) noise_at_kernel(TG* __restrict__ grad, long long n,
+                                                       float scale, uint64_t seed, uint64_t step,
+                                                       uint64_t e0) {
+  constexpr int V = 16 / static_cast<int>(sizeof(TG));
+  constexpr int NB = (R + V + 3) / 4;
+  const RoundKeys rk = round_keys(seed);
+  const long long nvec = n / V;
+  const uint64_t q0 = e0 >> 2;  // block of element 0
+  uint4* g16 = reinterpret_cast<uint4*>(grad);
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long j = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; j < nvec;
+       j += stride) {
+    uint4 raw = __ldcs(g16 + j);
+    TG* v = reinterpret_cast<TG*>(&raw);
+    float z[4 * NB];
+#pragma unroll
+    for (int b = 0; b < NB; ++b)
+      block_normals(q0 + static_cast<uint64_t>(j) * (V / 4) + b, step, rk, z + 4 * b);
+#pragma unroll
+    for (int t = 0; t < V; ++t) store_f(v + t, fmaf(scale, z[R + t], load_f(v + t)));
+    __stcs(g16 + j, raw);
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    for (long long i = nvec * V; i < n; ++i) {
+      float z[4];
+      const uint64_t e = e0 + static_cast<uint64_t>(i);
+      block_normals(e >> 2, step, rk, z);
+      const int w = static_cast<int>(e & 3);
+      const float ze = w == 0 ? z[0] : (w == 1 ? z[1] : (w == 2 ? z[2] : z[3]));
+      store_f(grad + i, fmaf(scale, ze, load_f(grad + i)));
+    }
   }
 }
 
@@ -165,8 +225,40 @@ cudaError_t launch_noise(float* grad, int64_t N, float sigma, float C, uint64_t 
                          uint64_t step, cudaStream_t s) {
   if (N == 0) return cudaSuccess;
   noise_kernel<<<grid_for(N / 4 / kNoiseUnroll + 1, 256, kNoiseCtasPerSm), 256, 0, s>>>(
-      grad, N, sigma * C, seed, step);
+      grad, N, sigma * C, seed, step, 0);
   return cudaGetLastError();
+}
+
+namespace {
+template <typename TG>
+cudaError_t launch_noise_at_t(TG* grad, int64_t N, uint64_t e0, float scale, uint64_t seed,
+                              uint64_t step, cudaStream_t s) {
+  constexpr int V = 16 / static_cast<int>(sizeof(TG));
+  const int grid = grid_for(N / V + 1, 256, kNoiseCtasPerSm);
+  switch (e0 & 3) {
+    case 0: noise_at_kernel<TG, 0><<<grid, 256, 0, s>>>(grad, N, scale, seed, step, e0); break;
+    case 1: noise_at_kernel<TG, 1><<<grid, 256, 0, s>>>(grad, N, scale, seed, step, e0); break;
+    case 2: noise_at_kernel<TG, 2><<<grid, 256, 0, s>>>(grad, N, scale, seed, step, e0); break;
+    default: noise_at_kernel<TG, 3><<<grid, 256, 0, s>>>(grad, N, scale, seed, step, e0);
+  }
+  return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_noise_at(void* grad, dprc_dtype dt, int64_t N, uint64_t first_element,
+                            float sigma, float C, uint64_t seed, uint64_t step, cudaStream_t s) {
+  if (N == 0) return cudaSuccess;
+  if (dt == DPRC_F32 && (first_element & 3) == 0) {
+    // a block boundary: the whole-gradient kernel with its block offset
+    noise_kernel<<<grid_for(N / 4 / kNoiseUnroll + 1, 256, kNoiseCtasPerSm), 256, 0, s>>>(
+        static_cast<float*>(grad), N, sigma * C, seed, step, first_element >> 2);
+    return cudaGetLastError();
+  }
+  if (dt == DPRC_F32)
+    return launch_noise_at_t(static_cast<float*>(grad), N, first_element, sigma * C, seed, step,
+                             s);
+  return launch_noise_at_t(static_cast<__nv_bfloat16*>(grad), N, first_element, sigma * C, seed,
+                           step, s);
 }
 
 cudaError_t launch_philox_words(uint32_t* out, int64_t n_blocks, uint64_t first_block,

@@ -209,7 +209,7 @@ __global__ void __launch_bounds__(192, 1)
       for (int off = 16; off > 0; off >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, off);
       if (lane == 0) s_red[ew] = sq;
       named_bar_sync(1, 128);
-      if (ew == 0 && lane == 0 && ok)
+      if (ew == 0 && lane == 0 && ok && DPRC_IN(blockIdx.x + j * gridDim.x < a.ntiles))
         a.partials[blockIdx.x + j * gridDim.x] = (s_red[0] + s_red[1]) + (s_red[2] + s_red[3]);
       named_bar_sync(1, 128);
     }
@@ -540,7 +540,7 @@ __global__ void __launch_bounds__(kGhThreads, 1)
       }
       named_bar_sync(1, 32 * kGhEpiWarps);
       const bool stop = epi_stop != 0;
-      if (ew == 0 && lane == 0 && !stop) {
+      if (ew == 0 && lane == 0 && !stop && DPRC_IN(g >= 0 && g < a.nunits)) {
         float tot = 0.f;
 #pragma unroll
         for (int e = 0; e < kGhEpiWarps; ++e) tot += s_red[e];

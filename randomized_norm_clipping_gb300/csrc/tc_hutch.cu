@@ -196,11 +196,15 @@ __device__ __forceinline__ bool xchg_rows(const Xchg& xs, int cl, int rank, int 
                                   DPRC_DEVERR_CLUSTER, limit_ns, nullptr))
       ok = false;
     const int slot = rank < owner ? rank : rank - 1;
-    const uint32_t dst = map_to_rank(xs.recv + (static_cast<size_t>(slot) * R + r_in) * K, owner);
+    if (DPRC_IN(owner < cl && slot >= 0 && slot < cl - 1 && r_in < R)) {
+      const uint32_t dst =
+          map_to_rank(xs.recv + (static_cast<size_t>(slot) * R + r_in) * K, owner);
 #pragma unroll
-    for (int c4 = 0; c4 < K / 4; ++c4)
-      st_cluster_f4(dst + 16 * c4, make_float4(y[4 * c4], y[4 * c4 + 1], y[4 * c4 + 2], y[4 * c4 + 3]));
-    mbar_arrive_remote(map_to_rank(xs.recv_bar, owner));
+      for (int c4 = 0; c4 < K / 4; ++c4)
+        st_cluster_f4(dst + 16 * c4,
+                      make_float4(y[4 * c4], y[4 * c4 + 1], y[4 * c4 + 2], y[4 * c4 + 3]));
+      mbar_arrive_remote(map_to_rank(xs.recv_bar, owner));
+    }
   } else {
     if (!mbar_wait_cluster(xs.recv_bar, static_cast<uint32_t>(rnd) & 1, DPRC_DEVERR_CLUSTER,
                            limit_ns))
@@ -214,6 +218,7 @@ __device__ __forceinline__ bool xchg_rows(const Xchg& xs, int cl, int rank, int 
         for (int t = 0; t < K; ++t) acc[t] += y[t];
       } else {
         const int slot = s < rank ? s : s - 1;
+        if (!DPRC_IN(slot >= 0 && slot < cl - 1 && r_in < R)) continue;
         const float4* src =
             reinterpret_cast<const float4*>(xs.recv + (static_cast<size_t>(slot) * R + r_in) * K);
 #pragma unroll
@@ -233,7 +238,7 @@ __device__ __forceinline__ bool xchg_rows(const Xchg& xs, int cl, int rank, int 
   named_bar_sync(1, 128);
   if (!last && threadIdx.x == 64) {  // first epilogue thread
     for (int s = 0; s < cl; ++s)
-      if (s != rank) mbar_arrive_remote(map_to_rank(xs.free_bar, s));
+      if (s != rank && DPRC_IN(cl <= 8)) mbar_arrive_remote(map_to_rank(xs.free_bar, s));
   }
   return mine_row;
 }
@@ -548,7 +553,8 @@ __global__ void __launch_bounds__(hutch_threads<PM1>(), 1)
             advance(ca);
           }
           if (w_done >= it - base) break;  // nothing left to complete (after an error)
-          if (need_wait) {
+          if (need_wait && !DPRC_IN(cw.i >= 0 && cw.i < a.B && l < a.L)) ok = false;
+          if (need_wait && ok) {
             if (wait_geq(&a.ready[l * a.B + cw.i], Ld.ready_target, lim, abort_flag)) {
               fence_proxy_async_global();
               ready_i = cw.i;
@@ -715,8 +721,10 @@ __global__ void __launch_bounds__(hutch_threads<PM1>(), 1)
       if (CAP > 1 && nb1 > 0 && l >= 2) {
         // the previous user of this sketch buffer (layer l - 2) must be done
         if (threadIdx.x == 64 && ok &&
-            !wait_geq(&a.done2[l - 2], static_cast<int>(a.layer[CAP == 1 ? 0 : l - 2].ph2.nblocks),
-                      lim, abort_flag))
+            (!DPRC_IN(l < a.L) ||
+             !wait_geq(&a.done2[l - 2],
+                       static_cast<int>(a.layer[CAP == 1 ? 0 : l - 2].ph2.nblocks), lim,
+                       abort_flag)))
           *abort_flag = 1;
         named_bar_sync(1, 128);
       }
@@ -744,7 +752,7 @@ __global__ void __launch_bounds__(hutch_threads<PM1>(), 1)
         const long long b = m1.first + j * m1.step;
         const int i = static_cast<int>(b / a.mtiles);
         const int t = static_cast<int>(b - static_cast<long long>(i) * a.mtiles) * kTok + row;
-        if (mine_row && ok && t < a.T) {
+        if (mine_row && ok && t < a.T && DPRC_IN(i >= 0 && i < a.B && t < a.tpad)) {
           __nv_bfloat16* wi = W + static_cast<size_t>(i) * 2 * K * a.tpad + t;
 #pragma unroll
           for (int c = 0; c < K; ++c) {
@@ -756,7 +764,7 @@ __global__ void __launch_bounds__(hutch_threads<PM1>(), 1)
         }
         fence_proxy_async_global();  // these rows are read by TMA (async proxy)
         named_bar_sync(1, 128);
-        if (ew == 0 && lane == 0 && ok) {
+        if (ew == 0 && lane == 0 && ok && DPRC_IN(i >= 0 && i < a.B && l < a.L)) {
           __threadfence();
           atomicAdd(&a.ready[l * a.B + i], 1);
         }
@@ -814,8 +822,10 @@ __global__ void __launch_bounds__(hutch_threads<PM1>(), 1)
           if (lane == 0 && Ld.ph2.split) {
             float* nb = xs.norms + (nsplit2 & 1) * 8;
             if (rank != 0) {
-              st_cluster_f32(map_to_rank(nb + rank, 0), part);
-              mbar_arrive_remote(map_to_rank(&xs.norm_bar[nsplit2 & 1], 0));
+              if (DPRC_IN(rank < 8)) {
+                st_cluster_f32(map_to_rank(nb + rank, 0), part);
+                mbar_arrive_remote(map_to_rank(&xs.norm_bar[nsplit2 & 1], 0));
+              }
               leader = 0;
             } else {
               if (!mbar_wait_cluster(&xs.norm_bar[nsplit2 & 1],
@@ -830,7 +840,8 @@ __global__ void __launch_bounds__(hutch_threads<PM1>(), 1)
           leader = __shfl_sync(0xffffffffu, leader, 0);
           const bool lok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
           if (!lok) ok = false;
-          if (leader && lok) {
+          if (leader && lok &&
+              DPRC_IN(i >= 0 && i < a.B && ch >= 0 && ch < Ld.nchunks && Ld.nchunks <= a.maxch)) {
             const size_t li = static_cast<size_t>(l) * a.B + i;
             int last = 0;
             if (lane == 0) {
@@ -885,7 +896,7 @@ __global__ void __launch_bounds__(hutch_threads<PM1>(), 1)
               }
             }
             // this block no longer reads the sketch buffer of layer l
-            if (CAP > 1 && lane == 0) atomicAdd(&a.done2[l], 1);
+            if (CAP > 1 && lane == 0 && DPRC_IN(l < a.L)) atomicAdd(&a.done2[l], 1);
           }
         }
         named_bar_sync(1, 128);

@@ -380,7 +380,7 @@ __global__ void __launch_bounds__(192, 1)
           // k divides 128: this thread's outputs et + 128 m share the column
           // c = et % k, so each P element is loaded once per row
           const int nm = (dk - et + kNwM - 1) / kNwM;
-          float* dst = lok ? a.ypart + tile * dk : nullptr;
+          float* dst = lok && DPRC_IN(tile < a.ntiles) ? a.ypart + tile * dk : nullptr;
           if (nm <= 4)
             shared_col_outputs<4>(Xs, NX, Pt, a.kp, a.k, rows, et, nm, dst);
           else if (nm <= 8)
@@ -404,7 +404,7 @@ __global__ void __launch_bounds__(192, 1)
                             y[u]);
             }
             const float t = ((y[0] + y[1]) + (y[2] + y[3])) + ((y[4] + y[5]) + (y[6] + y[7]));
-            if (lok) a.ypart[tile * dk + o] = t;
+            if (lok && DPRC_IN(tile < a.ntiles)) a.ypart[tile * dk + o] = t;
           }
         }
         named_bar_sync(1, 128);  // Xs and Pt are rewritten by the next tile
@@ -455,7 +455,7 @@ __global__ void __launch_bounds__(192, 1)
       for (int off = 16; off > 0; off >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, off);
       if (lane == 0) s_red[ew] = sq;
       named_bar_sync(1, 128);
-      if (ew == 0 && lane == 0 && ok)
+      if (ew == 0 && lane == 0 && ok && DPRC_IN(tile < a.ntiles))
         a.partials[tile] = (s_red[0] + s_red[1]) + (s_red[2] + s_red[3]);
       named_bar_sync(1, 128);
       }  // MODE != kNwProjT
@@ -464,7 +464,8 @@ __global__ void __launch_bounds__(192, 1)
       const int is = static_cast<int>(tile / a.mt);
       __threadfence();  // this thread's partial writes, before the ticket
       named_bar_sync(1, 128);
-      if (et == 0) s_last = atomicAdd(&a.tickets[is], 1) == a.mt - 1;
+      if (et == 0)
+        s_last = DPRC_IN(tile < a.ntiles) && atomicAdd(&a.tickets[is], 1) == a.mt - 1;
       named_bar_sync(1, 128);
       if (s_last) {
         __threadfence();

@@ -103,6 +103,7 @@ __device__ __forceinline__ bool cluster_reduce_rows(const XchgSmem& xs, int cl, 
   const int r_in = row - owner * R;
   if (owner != rank) {
     const int slot = rank < owner ? rank : rank - 1;  // sender index at the owner
+    if (!DPRC_IN(owner < cl && slot >= 0 && slot < cl - 1 && r_in < R)) return false;
     const uint32_t dst = map_to_rank(xs.recv + (static_cast<size_t>(slot) * R + r_in) * N, owner);
 #pragma unroll
     for (int c4 = 0; c4 < N / 4; ++c4)
@@ -374,7 +375,7 @@ __global__ void __launch_bounds__(192, 2)
       if (sc.cl > 1) mine = cluster_reduce_rows<kN>(xs, sc.cl, wk.rank, row, y, ok);
       const int i = static_cast<int>(b / a.mtiles);
       const int t = static_cast<int>(b - static_cast<long long>(i) * a.mtiles) * kRowTile + row;
-      if (mine && ok && t < a.T)
+      if (mine && ok && t < a.T && DPRC_IN(b < sc.nblocks && t < a.tpad))
         write_sketch_row<NMMA, HILO_IN>(a.W + static_cast<size_t>(i) * 2 * kN * a.tpad + t,
                                         a.tpad, y);
     }
@@ -650,8 +651,10 @@ __global__ void __launch_bounds__(192, ColCfg<NMMA>::kCtasPerSm)
           int leader = 1;
           if (lane == 0 && sc.cl > 1) {
             if (wk.rank != 0) {
-              st_cluster_f32(map_to_rank(xs.norms + wk.rank, 0), part);
-              mbar_arrive_remote(map_to_rank(xs.norm_bar, 0));
+              if (DPRC_IN(wk.rank < 8)) {
+                st_cluster_f32(map_to_rank(xs.norms + wk.rank, 0), part);
+                mbar_arrive_remote(map_to_rank(xs.norm_bar, 0));
+              }
               leader = 0;
             } else {
               if (!mbar_wait_cluster(xs.norm_bar, 0, DPRC_DEVERR_CLUSTER)) ok = false;
@@ -663,7 +666,7 @@ __global__ void __launch_bounds__(192, ColCfg<NMMA>::kCtasPerSm)
           leader = __shfl_sync(0xffffffffu, leader, 0);
           const bool lok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
           if (!lok) ok = false;
-          if (leader && lok) {
+          if (leader && lok && DPRC_IN(b < sc.nblocks)) {
             int last = 0;
             if (lane == 0) {
               a.chunk_norms[b] = chunk;
@@ -685,7 +688,7 @@ __global__ void __launch_bounds__(192, ColCfg<NMMA>::kCtasPerSm)
           }
         }
         named_bar_sync(1, 128);
-      } else if (mine && ok && grow < a.c) {
+      } else if (mine && ok && grow < a.c && DPRC_IN(b < sc.nblocks)) {
         if (a.mode == kColprojF32) {
           float4* d4 = reinterpret_cast<float4*>(a.y_f32 + (static_cast<size_t>(i) * a.c + grow) * kN);
 #pragma unroll

@@ -17,7 +17,7 @@
 Steps 3-5 run in libdprc (Hutchinson: every layer and the clip factors of
 the layer sum in one dprc_norm_hutch_layers_clip call; Hutch++: a
 dprc_norm_hutchpp call per layer with accumulation, then dprc_clip_factors;
-dprc_add_noise); PyTorch
+dprc_add_noise_at on each weight's gradient in place); PyTorch
 provides the forward and backward passes and the memory.  The first backward
 asks autograd only for the gradients with respect to the recorded layer
 outputs, so no weight gradient is formed before the clip factors are known.
@@ -192,16 +192,17 @@ class RandomizedClippingStep:
         for m in self.layers:
             m.weight.grad = None
         (c.to(losses.dtype) * losses).sum().backward()
-        # step 5: noise on the aggregated gradient (one buffer, one call)
+        # step 5: noise on the aggregated gradient, in place: the weights'
+        # gradients laid end to end in layer order are that gradient, and each
+        # gets the stretch of the one noise stream its position there selects
         if self.sigma > 0.0:
-            ws_ = [m.weight for m in self.layers]
-            flat = torch.cat([w.grad.reshape(-1).float() for w in ws_])
-            rnc.dprc_add_noise(flat, self.sigma, self.C, _seed(self.seed, 2), step)
             off = 0
-            for w in ws_:
-                cnt = w.grad.numel()
-                w.grad.copy_(flat[off:off + cnt].view_as(w.grad))
-                off += cnt
+            for m in self.layers:
+                g = m.weight.grad
+                if not g.is_contiguous():
+                    raise RuntimeError("weight gradients must be contiguous")
+                rnc.dprc_add_noise_at(g, off, self.sigma, self.C, _seed(self.seed, 2), step)
+                off += g.numel()
         self._acts.clear()
         self._outs.clear()
         return {"n": n, "c": c}

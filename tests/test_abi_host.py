@@ -40,6 +40,16 @@ def test_library_exports_every_declared_symbol(lib):
     assert set(binding.EXPORTED) == set(_declared())
 
 
+def test_bounds_checked_build_exports_the_same_symbols(lib):
+    # libdprc_debug.so: the same sources with every computed index checked
+    from randomized_norm_clipping_gb300 import build
+    if not os.path.exists(build.DEBUG_LIB_PATH):
+        build.build(variants=("debug",))
+    dbg = ctypes.CDLL(build.DEBUG_LIB_PATH)
+    for name in _declared():
+        assert hasattr(dbg, name), name
+
+
 def test_abi_version_and_status_strings(lib):
     assert lib.dprc_abi_version() == 1
     for code in range(9):
@@ -172,6 +182,14 @@ def test_argument_errors_return_before_device_work(lib):
               None, big, None) == 5  # no stage
     assert hh(_vp(A16), _vp(A16), _vp(A16), 1, 2, 64, 8, 8, 8, f32(1.0), _vp(A16), _vp(A16),
               _vp(A16), 1024, None) == 5  # stage too small
+    na_ = lib.dprc_add_noise_at
+    one = ctypes.c_float(1.0)
+    assert na_(_vp(A16), 5, 10, 0, one, one, 1, 1, None) == 3            # unknown dtype
+    assert na_(None, 0, 10, 0, one, one, 1, 1, None) == 1                 # no gradient
+    assert na_(_vp(A16 + 4), 1, 10, 0, one, one, 1, 1, None) == 4         # misaligned
+    assert na_(_vp(A16), 0, 10, 2**64 - 5, one, one, 1, 1, None) == 2     # range wraps
+    assert na_(_vp(A16), 0, 10, 0, ctypes.c_float(-1.0), one, 1, 1, None) == 2
+    assert na_(None, 1, 0, 123, one, one, 1, 1, None) == 0                # empty: no-op
     w = lib.dprc_philox_words
     assert w(None, 4, 0, 1, 1, None) == 1
     assert w(None, 0, 0, 1, 1, None) == 0

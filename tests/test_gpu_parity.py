@@ -590,6 +590,50 @@ def test_noise_matches_oracle(N):
     assert np.all(err <= _noise_tol(z, grad.double().numpy(), sigma, C))
 
 
+def _z_and_radius_at(first, N, seed, step):
+    """z_e and its Box-Muller pair radius for e in [first, first + N)."""
+    base = first & ~3
+    z = oracle.noise_normals(first - base + N, seed, step, first_element=base)
+    r = _pair_radius(z)  # pairs are (4j, 4j + 1), (4j + 2, 4j + 3): base is a multiple of 4
+    return z[first - base:], r[first - base:]
+
+
+@pytest.mark.parametrize("first,N", [(0, 1001), (4, 1003), (5, 4096), (6, 7), (7, 65539),
+                                     ((1 << 33) + 1, 999), (1_235_814_397, 12)])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_noise_at_offset_matches_oracle(first, N, dtype):
+    # a piece of a gradient kept in several buffers: element i gets z_{first + i}
+    grad = wl.gradient_buffer(N, seed=N + 1).to(dtype)
+    out = grad.to(DEV)
+    sigma, C = 1.3, 0.7
+    rnc.dprc_add_noise_at(out, first, sigma, C, seed=99, step=4)
+    g = grad.double().numpy()
+    z, r = _z_and_radius_at(first, N, 99, 4)
+    ref = g + sigma * C * z
+    got = out.cpu().double().numpy()
+    tol = _noise_tol(z, g, sigma, C, r)
+    if dtype == torch.bfloat16:
+        # the fp32 sum is rounded once to bf16: one bf16 unit in the last place
+        tol = tol + np.abs(ref) * 2.0 ** -7
+    assert np.all(np.abs(got - ref) <= tol)
+
+
+def test_noise_pieces_equal_the_whole_bitwise():
+    # the training step's use: weight gradients laid end to end, each given
+    # its stretch of the one stream, equal dprc_add_noise on the concatenation
+    sizes = [4096, 1000, 3, 5, 8192, 12, 1]
+    grad = wl.gradient_buffer(sum(sizes), seed=5).to(DEV)
+    whole = grad.clone()
+    rnc.dprc_add_noise(whole, 0.9, 1.1, seed=7, step=3)
+    off, parts = 0, []
+    for n in sizes:
+        piece = grad[off:off + n].clone()  # its own (16-byte aligned) buffer
+        rnc.dprc_add_noise_at(piece, off, 0.9, 1.1, seed=7, step=3)
+        parts.append(piece)
+        off += n
+    assert torch.equal(torch.cat(parts), whole)
+
+
 def test_noise_same_seed_step_reproduces_and_differs_otherwise():
     a = torch.zeros(10000, device=DEV)
     b = torch.zeros(10000, device=DEV)

@@ -66,12 +66,17 @@ def _gaussian_draws(A, G, k, seed):
     p = G.shape[2]
     g = torch.Generator(device=DEV).manual_seed(seed)
     Ps = (torch.randn(DRAWS, p, k, generator=g, device=DEV) / math.sqrt(k)).to(A.dtype)
-    out = torch.zeros(DRAWS, B, device=DEV)
+    out = _rows(B)
     ws = rnc.workspace(rnc.DPRC_OP_HUTCH, A, B, T, d, p, k)
     for j in range(DRAWS):
-        rnc.dprc_norm_hutch(A, G, Ps[j], out[j], ws=ws)
+        rnc.dprc_norm_hutch(A, G, Ps[j], out[j, :B], ws=ws)
     torch.cuda.synchronize()
-    return out.double().cpu().numpy(), Ps
+    return out[:, :B].double().cpu().numpy(), Ps
+
+
+def _rows(B):
+    """[DRAWS][B] outputs, each row 16-byte aligned (the library's rule)."""
+    return torch.zeros(DRAWS, (B + 3) // 4 * 4, device=DEV)
 
 
 def _fp32_case(T=None, seed_shift=0):
@@ -148,12 +153,12 @@ def test_plus_minus_one_estimate_is_unbiased_with_its_variance_law(path):
         k = 32
     B, T, d = A.shape
     p = G.shape[2]
-    out = torch.zeros(DRAWS, B, device=DEV)
+    out = _rows(B)
     ws = rnc.workspace(rnc.DPRC_OP_HUTCH_PM1, A, B, T, d, p, k)
     for j in range(DRAWS):
-        rnc.dprc_norm_hutch_pm1(A, G, k, 4242, j, out[j], ws=ws)
+        rnc.dprc_norm_hutch_pm1(A, G, k, 4242, j, out[j, :B], ws=ws)
     torch.cuda.synchronize()
-    x = out.double().cpu().numpy()
+    x = out[:, :B].double().cpu().numpy()
     _check_unbiased(x, _gram(A, G),
                     lambda O: 2.0 / k * (np.sum(O * O) - np.sum(np.diag(O) ** 2)), var_tol=0.15)
 

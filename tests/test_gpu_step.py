@@ -214,6 +214,28 @@ def test_noise_is_sigma_c_times_the_philox_normals():
     assert torch.allclose(diff, scale * z, atol=tol, rtol=1e-5)
 
 
+@pytest.mark.gpu
+def test_noise_in_place_on_bf16_weight_gradients():
+    # the step adds the noise to each weight's bf16 gradient in place (its
+    # stretch of the one stream); the result is the fp32 sum rounded once
+    x = torch.randn(4, 16, 64, device=DEV,
+                    generator=torch.Generator(DEV).manual_seed(5)).to(torch.bfloat16)
+    grads = []
+    for sigma in (0.0, 0.7):
+        model = _model(torch.bfloat16, widths=(64, 96, 40), seed=12)
+        step = RandomizedClippingStep(model, C=2.0, sigma=sigma, k=32, seed=9)
+        step(_losses(model, x), step=6)
+        grads.append(torch.cat([m.weight.grad.reshape(-1) for m in model
+                                if isinstance(m, torch.nn.Linear)]).float())
+        step.close()
+    z = torch.zeros_like(grads[0])
+    rnc.dprc_add_noise(z, 1.0, 1.0, _noise_seed(9), 6)
+    want = grads[0] + 1.4 * z
+    # one bf16 rounding of the sum (2^-8 relative), plus the normals' bound
+    tol = (want.abs() * 2.0 ** -8 + 1.4 * 1e-5).to(want.dtype)
+    assert torch.all((grads[1] - want).abs() <= tol)
+
+
 def _noise_seed(seed):
     from randomized_norm_clipping_gb300.step import _seed
     return _seed(seed, 2)
