@@ -254,11 +254,13 @@ def run_native(args, rank, ws, local):
     torch.cuda.synchronize(device)
     eager_ms = ev0.elapsed_time(ev1) / args.steps
 
-    # The step captured once as a CUDA graph and replayed: the GPU runs the
-    # kernels back to back; this is the timed region.
+    # The K timed steps captured as one CUDA graph (the way a training loop
+    # captures its step): the GPU runs the K launches back to back, each a
+    # programmatic dependent of the one before; one replay is the timed region.
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
-        step()
+        for _ in range(args.steps):
+            step()
     for _ in range(args.warmup):
         graph.replay()
     torch.cuda.synchronize(device)
@@ -267,15 +269,14 @@ def run_native(args, rank, ws, local):
     with ClockSampler(local) as clk:
         t_soak = time.perf_counter()
         while time.perf_counter() - t_soak < 1.5:
-            for _ in range(500):
+            for _ in range(max(1, 500 // args.steps)):
                 graph.replay()
             torch.cuda.synchronize(device)
         barrier(ws)
         torch.cuda.synchronize(device)
-        torch.cuda._sleep(2_000_000)  # queue the replays behind ~1 ms of GPU work
+        torch.cuda._sleep(2_000_000)  # queue the replay behind ~1 ms of GPU work
         ev0.record(stream)
-        for _ in range(args.steps):
-            graph.replay()
+        graph.replay()
         ev1.record(stream)
         torch.cuda.synchronize(device)
         barrier(ws)
@@ -318,10 +319,10 @@ def run_native(args, rank, ws, local):
     k2 = float(np.mean(k2_ms))
     peak, peak_kind = measured_peaks()
     if norm_launches == 1:
-        # one kernel streams G, P and A: its average launch duration is the
-        # event-timed run of back-to-back calls (no event inside the run)
+        # one kernel streams G, P and A, once per step: its average launch
+        # duration is the timed region divided by the K launches in it
         dom, dom_ms, dom_bytes, dom_key = ("tc_hutch_kernel (sketch G P + projection "
-                                           "A^T W, ||Y||^2, one launch)", call_ms,
+                                           "A^T W, ||Y||^2, one launch)", ms_local / args.steps,
                                            sk_bytes + pj_bytes, "fused")
     elif k2 >= k1:
         dom, dom_ms, dom_bytes, dom_key = "colproj (A^T W, ||Y||^2)", k2, pj_bytes, "colproj"
@@ -378,7 +379,7 @@ def run_native(args, rank, ws, local):
             "global_batch": ws * B, "seq_len": T, "d": d, "p": p, "k": k,
             "parallelism": f"replicas x{ws} (samples sharded, no collective)",
             "l2": "inputs (268 MB per rank) larger than the 126 MB L2; no flush",
-            "timed": "step captured as a CUDA graph, K replays queued back to back",
+            "timed": "the K steps captured as one CUDA graph (one launch each), one replay",
             "eager_ms_per_step": eager_ms,
         },
         "roofline": {
@@ -387,7 +388,8 @@ def run_native(args, rank, ws, local):
             "traffic": traffic, "ms": dom_ms, "algorithmic_bytes": dom_bytes,
         },
         "roofline_op": {
-            "what": "dprc_norm_hutch call (both kernels), algorithmic bytes A + G + P",
+            "what": "dprc_norm_hutch_clip called eagerly 20 times back to back (host launch "
+                    "cost hidden behind a GPU sleep), algorithmic bytes A + G + P",
             "achieved": op_achieved, "peak": peak, "unit": "GB/s", "frac": op_achieved / peak,
             "ms": call_ms,
             "kernel_ms": ({"fused": k1} if norm_launches == 1 else {"rowproj": k1, "colproj": k2}),
@@ -519,23 +521,22 @@ def cpu_oracle_subsets(rows, device):
                           f"scaled to {wk.noise_elems}"}
 
 def graph_ms(fn, device, reps, warmup=3):
-    """Mean device time of fn captured as one CUDA graph and replayed reps times
-    back to back (queued behind a GPU sleep so host launch gaps are hidden)."""
+    """Mean device time of fn: reps calls captured as one CUDA graph, replayed
+    once (queued behind a GPU sleep so host launch gaps are hidden)."""
     for _ in range(warmup):
         fn()
     torch.cuda.synchronize(device)
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g):
-        fn()
-    for _ in range(warmup):
-        g.replay()
+        for _ in range(reps):
+            fn()
+    g.replay()
     torch.cuda.synchronize(device)
     stream = torch.cuda.current_stream(device)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda._sleep(5_000_000)
     e0.record(stream)
-    for _ in range(reps):
-        g.replay()
+    g.replay()
     e1.record(stream)
     torch.cuda.synchronize(device)
     del g

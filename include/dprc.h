@@ -233,7 +233,7 @@ dprc_status dprc_norm_hutch_layers_clip(int64_t L, const void* const* A, const v
 /*
  * Number of kernels one dprc_norm_hutch call with these arguments enqueues on
  * the current device: 1 (bf16, k = 16 or 32: sketch and projection as two
- * phases of one cooperative launch; or the one-pass kernel of a narrow
+ * phases of one persistent launch; or the one-pass kernel of a narrow
  * layer), 2 (other tensor-core shapes: a sketch kernel and a projection
  * kernel) or 3 (the CUDA-core path: sketch, projection, reduction).  0 for
  * arguments dprc_norm_hutch would reject or when no sm_103 device is current.

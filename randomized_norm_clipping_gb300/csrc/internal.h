@@ -160,7 +160,7 @@ cudaError_t launch_qr_project(const float* M, int64_t B, int64_t p, int r, const
 // order into n_out.  bf16, d and p multiples of 8.
 int64_t fgc_partials(int64_t B, int64_t d, int64_t p);
 // Fused Hutchinson: sketch and projection of 1..kMaxFusedLayers layers as
-// phases of one cooperative launch (bf16, k = 16 or 32, one B and T for all
+// phases of one persistent launch (bf16, k = 16 or 32, one B and T for all
 // layers).  n_out (+)= the layer sum.  Returns cudaSuccess with *launched
 // false when the kernel cannot run with these shapes on this device (the
 // caller then uses the two-kernel path); the counters must be zero and are

@@ -7,8 +7,8 @@
 // its squared Frobenius norm; "Overall framework": the layerwise sum).
 //
 // Each layer is two contractions (those of tc_proj.cu): the sketch
-// W_i = G_i P and the projection Y_i = A_i^T W_i.  One persistent cooperative
-// kernel runs them as phases, layer after layer:
+// W_i = G_i P and the projection Y_i = A_i^T W_i.  One persistent kernel,
+// every CTA resident at once, runs them as phases, layer after layer:
 //
 //   phase 1 (sketch)      CTAs take blocks of 128 tokens of one sample and write
 //                         W_i as bf16 hi/lo planes; each block then adds one to
@@ -28,9 +28,8 @@
 // (deterministic) into n_i.
 //
 // The cross-CTA waits are safe because every CTA is resident (the grid is at
-// most what fits on the device at once; a launch without clusters is
-// cooperative) and every wait is on work that comes earlier in the one order
-// all CTAs follow (layer, then phase).  Every wait is bounded (2 s, or the
+// most what fits on the device at once) and every wait is on work that comes
+// earlier in the one order all CTAs follow (layer, then phase).  Every wait is bounded (2 s, or the
 // limit a test gives) and records a code in the device error word when it
 // runs out; the CTA's other roles then stop at their next wait, the MMA
 // thread waits for the MMAs it issued and the producer for its copies, and
@@ -45,8 +44,8 @@
 // counts) are reset by their last user, so they are zero after every call that
 // ends without a device error, and must be zero before the first.
 //
-// One CTA per SM: the driver counts tensor-memory kernels at one CTA per SM,
-// and a cooperative launch cannot exceed that.  The shared-memory ring has 4
+// One CTA per SM (the 192 KB ring leaves room for no second one).  The
+// shared-memory ring has 4
 // slots of 48 KB used by both phases: a sketch stage is 128 tokens x 128 p of
 // G (two TMA boxes, 256 contiguous bytes per row) plus 128 rows of P; a
 // projection stage 128 tokens x 128 d of A plus the matching 128 tokens of the
@@ -372,8 +371,8 @@ __global__ void __launch_bounds__(hutch_threads<PM1>(), 1)
   xs.recv = reinterpret_cast<float*>(ring + Cfg::kRing + Cfg::kCtrl);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // a dependent launch (the clip factors) may start now; it waits for this
-  // grid's completion before reading anything
+  // a dependent launch (the clip factors, or the next call) may start now;
+  // it waits for this grid's completion before touching memory
   pdl_launch_dependents();
   const int nlayers = CAP == 1 ? 1 : a.L;  // a constant for single-layer launches
   const int cl = a.cl;
@@ -402,8 +401,14 @@ __global__ void __launch_bounds__(hutch_threads<PM1>(), 1)
   }
   // The producer (thread 0, which initialised the barriers) issues the first
   // ring slots of its first sketch block before the CTA barrier, so their
-  // DRAM round trip overlaps the TMEM allocation and the barrier.
+  // DRAM round trip overlaps the TMEM allocation and the barrier.  Launched as
+  // a programmatic dependent of the previous kernel in the stream, this grid
+  // may start while that one finishes: thread 0 first waits until it has
+  // completed and its writes are visible (every other thread touches memory
+  // only after the CTA barrier below, behind this wait); the barrier set-up
+  // above and the TMEM allocation overlap the previous grid's tail.
   int pre = 0;
+  if (threadIdx.x == 0) pdl_wait();
   if (threadIdx.x == 0) {
     const LayerDesc& L0 = a.layer[0];
     const Mine m1 = mine(L0.ph1, cl, rank);
@@ -937,9 +942,9 @@ cudaError_t set_smem_once() {
   return e;
 }
 
-// CTAs of this kernel that may run at once in one cooperative launch with
-// clusters of cl: the driver's occupancy figures (one CTA per SM: the
-// tensor-memory kernels are counted as such), cached per device and cl.
+// CTAs of this kernel that may run at once in one launch with clusters of
+// cl: the driver's occupancy figures (one CTA per SM), cached per device and
+// cl.
 template <int K, int CAP, bool PM1>
 int resident_ctas(int cl) {
   constexpr int kMaxDev = 64;
@@ -978,15 +983,20 @@ int resident_ctas(int cl) {
   return v;
 }
 
-// Launch of a planned schedule.  Without clusters the launch is cooperative:
-// the driver then guarantees that every CTA is resident at once, which the
-// cross-CTA waits rely on.  With clusters it is a plain cluster launch of at
-// most the number of clusters that fit on the device at once (the occupancy
-// query of resident_ctas), so on a device it has to itself every CTA is
-// resident too; when other work holds SMs, a waiting CTA's wait ends within
-// its limit with DPRC_DEVERR_READY instead of hanging.  Cooperative and
-// cluster attributes are never combined: that combination is the one launch
-// form of this kernel that faulted the GPU (under a profiler's replay).
+// Launch of a planned schedule.  The grid is at most what fits on the device
+// at once (one CTA per SM; with clusters, the clusters the occupancy query of
+// resident_ctas counts), so every CTA is resident together, which the
+// cross-CTA waits rely on; when other work holds SMs, a waiting CTA's wait
+// ends within its limit with DPRC_DEVERR_READY instead of hanging.  Without
+// clusters the launch is a programmatic dependent of the previous kernel in
+// the stream: its CTAs may start on SMs that kernel has released, set up, and
+// wait for its completion (griddepcontrol.wait) before any memory access.
+// Every CTA of the previous grid is already resident when this one starts
+// (its CTAs allow the dependent launch only once all of them run), so the
+// early CTAs cannot keep it from finishing.  With clusters the launch is a
+// plain cluster launch.  Cooperative and cluster attributes are never
+// combined: that combination is the one launch form of this kernel that
+// faulted the GPU (under a profiler's replay).
 // `test_cl` > 0 (failure-detection test only): launch with clusters of that
 // size whatever the plan says.
 template <int K, int CAP, bool PM1>
@@ -1004,8 +1014,8 @@ cudaError_t launch_k(const HParams<CAP>& a, int grid, cudaStream_t s, int test_c
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
   } else {
-    attr[0].id = cudaLaunchAttributeCooperative;
-    attr[0].val.cooperative = 1;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
   }
   cfg.attrs = attr;
   cfg.numAttrs = 1;
@@ -1022,8 +1032,8 @@ int want_cl(long long nblocks, int upb, int slots) {
   return cl;
 }
 
-// Devices on which the cooperative launch was refused once keep using the
-// two-kernel path.
+// Devices on which the launch was refused once keep using the two-kernel
+// path.
 constexpr int kMaxDevices = 64;
 std::atomic<int> g_refused[kMaxDevices];
 
