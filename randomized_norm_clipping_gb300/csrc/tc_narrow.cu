@@ -32,6 +32,7 @@
 // partials in tile order: one launch, deterministic.
 
 #include <atomic>
+#include <type_traits>
 
 #include "common.cuh"
 #include "internal.h"
@@ -45,6 +46,10 @@ constexpr int kNwK = 64;                     // tokens per stage
 constexpr int kNwStages = 8;
 constexpr int kNwBox = kNwK * 64 * 2;        // 64 tokens x 64 wide columns, 8 KB
 constexpr int kNwWide = (kNwM / 64) * kNwBox;  // 16 KB
+
+// Row stride (floats) of the tile's X rows in shared memory in the d-narrow
+// estimate: a multiple of four, so each row starts on a 16-byte boundary.
+__host__ __device__ constexpr int nx_of(int n) { return n + 4; }
 
 template <int N>
 struct NwCfg {
@@ -127,6 +132,73 @@ __device__ __forceinline__ void shared_col_outputs(const float* Xs, int nx, cons
 #pragma unroll
     for (int m = 0; m < NM; ++m)
       if (m < nm) dst[et + m * kNwM] = y[m];
+  }
+}
+
+// A tile's part of X_i P (d narrow, rows = p indices) with the outputs in
+// register blocks: thread et owns rows 4 dq .. 4 dq + 3 of X^T P against
+// columns 2 kq, 2 kq + 1, over one of `parts` equal ranges of the tile's rows,
+// so each row costs one 16-byte load of X and one 4-byte load of P for eight
+// products, and the eight sums are independent.  Needs k even and
+// (narrow / 4) (k / 2) dividing 128 (blocked_fits).  The parts are then added
+// in part order through shared memory (Xs, once every thread is done with
+// it) and the sums written row-major [narrow][k] to dst (skipped if null).
+__device__ __forceinline__ bool blocked_fits(int narrow, int k) {
+  if ((k & 1) != 0 || (narrow & 3) != 0) return false;
+  const int items = (narrow >> 2) * (k >> 1);
+  return items > 0 && kNwM % items == 0;
+}
+
+__device__ __forceinline__ void blocked_outputs(float* Xs, int nx, const __nv_bfloat16* Pt,
+                                                int kp, int k, int narrow, int rows, int et,
+                                                float* dst) {
+  const int nk2 = k >> 1, items = (narrow >> 2) * nk2, parts = kNwM / items;
+  const int h = et / items, it = et - h * items;
+  const int dq = it / nk2, kq = it - dq * nk2;
+  const int rlen = kNwM / parts;
+  const int r0 = h * rlen, r1 = r0 + rlen < rows ? r0 + rlen : rows;
+  float acc[4][2];
+#pragma unroll
+  for (int m = 0; m < 4; ++m) acc[m][0] = acc[m][1] = 0.f;
+#pragma unroll 4
+  for (int r = r0; r < r1; ++r) {
+    const float4 x = *reinterpret_cast<const float4*>(Xs + r * nx + 4 * dq);
+    const float2 pv = __bfloat1622float2(
+        *reinterpret_cast<const __nv_bfloat162*>(Pt + r * kp + 2 * kq));
+    acc[0][0] = fmaf(x.x, pv.x, acc[0][0]);
+    acc[0][1] = fmaf(x.x, pv.y, acc[0][1]);
+    acc[1][0] = fmaf(x.y, pv.x, acc[1][0]);
+    acc[1][1] = fmaf(x.y, pv.y, acc[1][1]);
+    acc[2][0] = fmaf(x.z, pv.x, acc[2][0]);
+    acc[2][1] = fmaf(x.z, pv.y, acc[2][1]);
+    acc[3][0] = fmaf(x.w, pv.x, acc[3][0]);
+    acc[3][1] = fmaf(x.w, pv.y, acc[3][1]);
+  }
+  named_bar_sync(1, 128);  // every part is done reading Xs
+  if (h > 0) {
+    float* red = Xs + ((h - 1) * items + it) * 8;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      red[2 * m] = acc[m][0];
+      red[2 * m + 1] = acc[m][1];
+    }
+  }
+  named_bar_sync(1, 128);
+  if (h == 0 && dst != nullptr) {
+    for (int hh = 1; hh < parts; ++hh) {
+      const float* red = Xs + ((hh - 1) * items + it) * 8;
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        acc[m][0] += red[2 * m];
+        acc[m][1] += red[2 * m + 1];
+      }
+    }
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      float* o = dst + (4 * dq + m) * k + 2 * kq;
+      o[0] = acc[m][0];
+      o[1] = acc[m][1];
+    }
   }
 }
 
@@ -334,7 +406,7 @@ __global__ void __launch_bounds__(192, 1)
         const int i = static_cast<int>(tile / a.mt);
         const int p0 = static_cast<int>(tile - static_cast<long long>(i) * a.mt) * kNwM;
         const int rows = a.wide - p0 < kNwM ? a.wide - p0 : kNwM;
-        TP* Pt = reinterpret_cast<TP*>(reinterpret_cast<float*>(Ps) + kNwM * (N + 1));
+        TP* Pt = reinterpret_cast<TP*>(reinterpret_cast<float*>(Ps) + kNwM * nx_of(N));
         stage_p_tile(a, p0, rows, Pt, et);
         named_bar_sync(1, 128);
       }
@@ -364,7 +436,7 @@ __global__ void __launch_bounds__(192, 1)
         // fp32 [128][N + 1]) beside the tile's rows of P (Pt, staged above),
         // then each thread forms d k / 128 entries, each summed over r in
         // a fixed order.
-        constexpr int NX = N + 1;  // padded row: conflict-free column writes
+        constexpr int NX = nx_of(N);  // rows 16-byte aligned
         float* Xs = reinterpret_cast<float*>(Ps);
         TP* Pt = reinterpret_cast<TP*>(Xs + kNwM * NX);
         const int i = static_cast<int>(tile / a.mt);
@@ -376,7 +448,16 @@ __global__ void __launch_bounds__(192, 1)
         named_bar_sync(1, 128);
         const bool lok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         const int dk = a.narrow * a.k;
-        if (kNwM % a.k == 0 && dk <= 32 * kNwM) {
+        bool blocked = false;
+        if constexpr (std::is_same<TP, __nv_bfloat16>::value) {
+          if (blocked_fits(a.narrow, a.k)) {
+            blocked_outputs(Xs, NX, Pt, a.kp, a.k, a.narrow, rows, et,
+                            lok && DPRC_IN(tile < a.ntiles) ? a.ypart + tile * dk : nullptr);
+            blocked = true;
+          }
+        }
+        if (blocked) {
+        } else if (kNwM % a.k == 0 && dk <= 32 * kNwM) {
           // k divides 128: this thread's outputs et + 128 m share the column
           // c = et % k, so each P element is loaded once per row
           const int nm = (dk - et + kNwM - 1) / kNwM;
@@ -665,7 +746,7 @@ cudaError_t launch_narrow_hutch(const void* A, const void* G, const void* P, int
   }
   // d narrow: per-tile parts of X_i P (scratch: narrow_hutch_scratch_bytes)
   a.ypart = partials;
-  const int proj_bytes = kNwM * (N + 1) * 4 + kNwM * a.kp * 2;
+  const int proj_bytes = kNwM * nx_of(N) * 4 + kNwM * a.kp * 2;
   return launch_mode<kNwProjT, __nv_bfloat16>(N, mw, mn, a, proj_bytes, s);
 }
 
