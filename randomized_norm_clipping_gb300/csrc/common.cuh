@@ -470,10 +470,13 @@ __device__ __forceinline__ float clip_factor(float v, float C, bool& bad) {
   return fminf(1.f, C / sqrtf(v));
 }
 
-// Round a shared-memory pointer up to the 1024-byte alignment that 128-byte
-// swizzled tiles need.
+// Round a shared-memory pointer up to the 1024-byte alignment (of its
+// shared-window address) that 128-byte swizzled tiles need.  The result is p
+// plus an offset, not an integer turned back into a pointer, so the compiler
+// still knows it points to shared memory and accesses through it stay
+// shared-memory instructions rather than generic ones.
 __device__ __forceinline__ uint8_t* align_1024(uint8_t* p) {
-  return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+  return p + ((1024u - (smem_u32(p) & 1023u)) & 1023u);
 }
 
 // Loads `NC` consecutive fp32 TMEM columns of this thread's lane.

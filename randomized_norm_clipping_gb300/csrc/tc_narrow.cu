@@ -160,11 +160,7 @@ __device__ __forceinline__ void blocked_outputs(float* Xs, int nx, const __nv_bf
   float acc[4][2];
 #pragma unroll
   for (int m = 0; m < 4; ++m) acc[m][0] = acc[m][1] = 0.f;
-#pragma unroll 4
-  for (int r = r0; r < r1; ++r) {
-    const float4 x = *reinterpret_cast<const float4*>(Xs + r * nx + 4 * dq);
-    const float2 pv = __bfloat1622float2(
-        *reinterpret_cast<const __nv_bfloat162*>(Pt + r * kp + 2 * kq));
+  auto row = [&](const float4& x, const float2& pv) {
     acc[0][0] = fmaf(x.x, pv.x, acc[0][0]);
     acc[0][1] = fmaf(x.x, pv.y, acc[0][1]);
     acc[1][0] = fmaf(x.y, pv.x, acc[1][0]);
@@ -173,7 +169,24 @@ __device__ __forceinline__ void blocked_outputs(float* Xs, int nx, const __nv_bf
     acc[2][1] = fmaf(x.z, pv.y, acc[2][1]);
     acc[3][0] = fmaf(x.w, pv.x, acc[3][0]);
     acc[3][1] = fmaf(x.w, pv.y, acc[3][1]);
+  };
+  // one warp per scheduler runs this, so nothing else hides the load
+  // latency: eight rows' loads are issued before their products
+  int r = r0;
+  for (; r + 8 <= r1; r += 8) {
+    float4 x[8];
+    __nv_bfloat162 pb[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      x[u] = *reinterpret_cast<const float4*>(Xs + (r + u) * nx + 4 * dq);
+      pb[u] = *reinterpret_cast<const __nv_bfloat162*>(Pt + (r + u) * kp + 2 * kq);
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) row(x[u], __bfloat1622float2(pb[u]));
   }
+  for (; r < r1; ++r)
+    row(*reinterpret_cast<const float4*>(Xs + r * nx + 4 * dq),
+        __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(Pt + r * kp + 2 * kq)));
   named_bar_sync(1, 128);  // every part is done reading Xs
   if (h > 0) {
     float* red = Xs + ((h - 1) * items + it) * 8;
@@ -553,16 +566,16 @@ __global__ void __launch_bounds__(192, 1)
         float acc = 0.f;
         if (MODE == kNwProjT) {
           // entry e of the sample's X_i P is the sum over its tiles m, in m
-          // order; four entries at a time, eight tiles per batch of loads, so
-          // 32 loads are in flight (this runs at the very end of the launch)
+          // order; four entries at a time, sixteen tiles per batch of loads, so
+          // 64 loads are in flight (this runs at the very end of the launch)
           const int dk = a.narrow * a.k;
           const float* yi = a.ypart + static_cast<size_t>(is) * a.mt * dk;
           for (int e0 = et; e0 < dk; e0 += 4 * 128) {
             float y[4] = {0.f, 0.f, 0.f, 0.f};
-            for (int m = 0; m < a.mt; m += 8) {
-              float t[8][4];
+            for (int m = 0; m < a.mt; m += 16) {
+              float t[16][4];
 #pragma unroll
-              for (int u = 0; u < 8; ++u)
+              for (int u = 0; u < 16; ++u)
 #pragma unroll
                 for (int q2 = 0; q2 < 4; ++q2) {
                   const int e = e0 + q2 * 128;
@@ -571,7 +584,7 @@ __global__ void __launch_bounds__(192, 1)
                                  : 0.f;
                 }
 #pragma unroll
-              for (int u = 0; u < 8; ++u)
+              for (int u = 0; u < 16; ++u)
 #pragma unroll
                 for (int q2 = 0; q2 < 4; ++q2)
                   if (m + u < a.mt) y[q2] += t[u][q2];
