@@ -26,7 +26,7 @@ LIB_NAME = "libdprc.so"
 LIB_PATH = os.path.join(PKG_DIR, LIB_NAME)
 DEBUG_LIB_PATH = os.path.join(PKG_DIR, "libdprc_debug.so")
 
-SOURCES = ["api.cu", "tc_proj.cu", "tc_exact.cu", "tc_narrow.cu", "tc_hutch.cu", "simt.cu", "qr.cu", "qr_cluster.cu", "noise.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "tc_proj.cu", "tc_exact.cu", "tc_narrow.cu", "tc_hutch.cu", "simt.cu", "qr.cu", "qr_cluster.cu", "hutchpp.cu", "noise.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 VARIANTS = {"release": ([], LIB_PATH), "debug": (["-DDPRC_DEBUG"], DEBUG_LIB_PATH)}
 

@@ -170,6 +170,12 @@ TcPlan plan_tc(dprc_op op, int64_t B, int64_t T, int64_t d, int64_t p, int64_t k
     off = align_up(off + static_cast<size_t>(B) * p * 4 * r * 2, 1024);
     t.qscratch_off = off;
     off = align_up(off + static_cast<size_t>(B) * p * r * 4 * 2, 1024);
+    t.sp_off = off;
+    off = align_up(off + static_cast<size_t>(p) * 2 * r * 2, 1024);
+    t.yp_off = off;
+    off = align_up(off + static_cast<size_t>(B) * d * r * 4, 1024);
+    t.rc_off = off;
+    off = align_up(off + static_cast<size_t>(B) * qr_factor_floats() * 4, 1024);
   }
   t.total = off;
   return t;
@@ -883,6 +889,47 @@ dprc_status dprc_norm_hutchpp(const void* A, const void* G, const void* S, const
     float* M = reinterpret_cast<float*>(w + t.m_off);
     void* QP = w + t.qp_off;
     const bool pdl = t_events == nullptr;
+    if (qr_cluster_supported(p, ir)) {
+      // the QR runs beside the third pass, which streams X M instead of X Q
+      // (hutchpp.cu): X Q = (X M) diag(s) R^-1, X P' = X P - (X Q) C
+      void* SP = w + t.sp_off;
+      float* YP = reinterpret_cast<float*>(w + t.yp_off);
+      float* RC = reinterpret_cast<float*>(w + t.rc_off);
+      void* MH = QP;  // M as bf16 hi/lo [B][p][2r], the third pass's sketch operand
+      mark(0, s);
+      cudaError_t e = launch_pack_cols(S, P, SP, p, ir, s);
+      // pass 1: [Z | X P] = A^T (G [S | P]); Z as hi/lo for pass 2, X P in fp32
+      if (e == cudaSuccess)
+        e = launch_tc_rowproj(G, B, T, p, SP, false, 2 * ir, false, W, t.tpad,
+                              rowproj_sched(B, T, p, 2 * ir), stick, B, s);
+      if (e == cudaSuccess)
+        e = launch_tc_colproj(A, B, T, d, W, t.tpad, 2 * ir, colproj_sched(B, T, d, 4 * ir),
+                              stick, cnorm, kColprojSplit, nullptr, 0, ir, 1.0f, YP, Z, pdl, s,
+                              ir);
+      mark(1, s);
+      // pass 2: M = G^T (A Z) = O S, fp32 for the QR and hi/lo for pass 3
+      if (e == cudaSuccess)
+        e = launch_tc_rowproj(A, B, T, d, Z, true, 2 * ir, true, W, t.tpad,
+                              rowproj_sched(B, T, d, 2 * ir), stick, B, s);
+      if (e == cudaSuccess)
+        e = launch_tc_colproj(G, B, T, p, W, t.tpad, ir, colproj_sched(B, T, p, 2 * ir), stick,
+                              cnorm, kColprojF32Hilo, nullptr, 0, ir, 1.0f, M, MH, pdl, s);
+      mark(2, s);
+      // the QR's factors (R, column scales, C = Q^T P) ...
+      if (e == cudaSuccess) e = launch_qr_cluster(M, B, p, P, dtype, nullptr, true, s, RC);
+      mark(3, s);
+      // ... while pass 3 streams X M = A^T (G M); its epilogue forms
+      // n (+)= ||X Q||^2 + ||X P'||^2 / r row by row from X M, X P and them
+      if (e == cudaSuccess)
+        e = launch_tc_rowproj(G, B, T, p, MH, true, 2 * ir, true, W, t.tpad,
+                              rowproj_sched(B, T, p, 2 * ir), stick, B, s, pdl);
+      if (e == cudaSuccess)
+        e = launch_tc_colproj(A, B, T, d, W, t.tpad, ir, colproj_sched(B, T, d, 2 * ir), stick,
+                              cnorm, kColprojHpp, n, accumulate, ir, 1.0f, nullptr, nullptr, pdl,
+                              s, 0, RC, YP);
+      mark(4, s);
+      return cuda_status(e);
+    }
     mark(0, s);
     // pass 1: Z = A^T (G S)
     cudaError_t e = launch_tc_rowproj(G, B, T, p, S, false, ir, false, W, t.tpad,

@@ -407,6 +407,30 @@ __device__ __forceinline__ void split_hilo(float x, __nv_bfloat16& hi, __nv_bflo
   lo = __float2bfloat16_rn(x - __bfloat162float(hi));
 }
 
+// A row y[0..N) as bf16 hi/lo planes [hi_0 .. hi_N-1 | lo_0 .. lo_N-1] at dst
+// (16-byte aligned), 16 bytes per store.
+template <int N>
+__device__ __forceinline__ void store_hilo_row(__nv_bfloat16* dst, const float (&y)[N]) {
+  static_assert(N % 8 == 0, "whole 16-byte chunks");
+  uint32_t h[N / 2], l[N / 2];
+#pragma unroll
+  for (int t = 0; t < N / 2; ++t) {
+    __nv_bfloat16 h0, l0, h1, l1;
+    split_hilo(y[2 * t], h0, l0);
+    split_hilo(y[2 * t + 1], h1, l1);
+    const __nv_bfloat162 hh = __halves2bfloat162(h0, h1);
+    const __nv_bfloat162 ll = __halves2bfloat162(l0, l1);
+    h[t] = *reinterpret_cast<const uint32_t*>(&hh);
+    l[t] = *reinterpret_cast<const uint32_t*>(&ll);
+  }
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int c = 0; c < N / 8; ++c) {
+    d4[c] = make_uint4(h[4 * c], h[4 * c + 1], h[4 * c + 2], h[4 * c + 3]);
+    d4[N / 8 + c] = make_uint4(l[4 * c], l[4 * c + 1], l[4 * c + 2], l[4 * c + 3]);
+  }
+}
+
 // ---------------------------------------------------------------------------
 // Philox4x32-10 (Salmon, Moraes, Dror and Shaw, "Parallel Random Numbers: As
 // Easy as 1, 2, 3", SC'11), written from that paper's definition.  Block j of

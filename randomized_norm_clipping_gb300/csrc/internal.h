@@ -46,6 +46,10 @@ struct TcPlan {
   size_t m_off = 0;           // Hutch++: M = O S fp32 [B][p][r]
   size_t qp_off = 0;          // Hutch++: [Q | P'] hi/lo bf16 [B][p][4r]
   size_t qscratch_off = 0;    // Hutch++: QR work space fp32 [B][p][r] * 2
+  // Hutch++ with the QR beside the third pass (r = 16, cluster QR):
+  size_t sp_off = 0;          // [S | P] bf16 [p][2r]
+  size_t yp_off = 0;          // X P fp32 [B][d][r]
+  size_t rc_off = 0;          // QR factors fp32 [B][qr_factor_floats()]
   size_t total = 0;
 };
 
@@ -114,12 +118,33 @@ bool make_tmap_3d_bf16(CUtensorMap* map, const void* base, uint64_t dim0, uint64
 // column halves of R are the hi and lo parts of one fp32 matrix and are
 // summed.  W is written as bf16 hi/lo planes [B][2n][tpad].  CTA 0 also
 // clears `zero_ints` int32 words at `zero_ptr` (the next kernel's tickets).
+// beside_previous: a programmatic dependent launch that runs while the
+// previous kernel in the stream (which must let it start early) still runs;
+// X and R must not be written by that kernel.  CTA 0 waits for it before
+// exiting, so this kernel completes after it.
 cudaError_t launch_tc_rowproj(const void* X, int64_t B, int64_t T, int64_t c, const void* R,
                               bool r_batched, int nmma, bool hilo_in, void* W, int64_t tpad,
                               const BlockSched& bs, int* zero_ptr, size_t zero_ints,
-                              cudaStream_t s);
+                              cudaStream_t s, bool beside_previous = false);
 
-enum ColprojMode { kColprojNorm = 0, kColprojF32 = 1, kColprojHilo = 2 };
+// kColprojSplit: the first n_split = n / 2 columns of Y as bf16 hi/lo
+// [B][c][n], the rest fp32 [B][c][n / 2]; kColprojF32Hilo: Y both ways;
+// kColprojHpp (n = 16): Y = X M of Hutch++, whose head and tail
+// ||Y_Q||^2 + ||Y_P - Y_Q C||^2 / 16 (Y_Q = Y diag(s) R^-1, hutchpp.cu) are
+// added into n_out like kColprojNorm's squares, from the QR factors hpp_rc and
+// Y_P = X P (fp32 [B][c][16]).
+enum ColprojMode {
+  kColprojNorm = 0,
+  kColprojF32 = 1,
+  kColprojHilo = 2,
+  kColprojSplit = 3,
+  kColprojF32Hilo = 4,
+  kColprojHpp = 5
+};
+
+// Hutch++ combining step: a column j of R with |R_jj| at most this fraction of
+// its column norm is left out of X Q (hutchpp.cu says why).
+constexpr float kHppDropTau = 1e-3f;
 
 // Column projection on tensor cores, reduced over T: Y[i] = X[i]^T W[i] with
 // X [B][T][c] bf16 and W the hi/lo sketch [B][2n][tpad].  Mode kColprojNorm
@@ -131,7 +156,8 @@ cudaError_t launch_tc_colproj(const void* X, int64_t B, int64_t T, int64_t c, co
                               int64_t tpad, int n, const BlockSched& bs, int* sample_tickets,
                               float* chunk_norms, ColprojMode mode, float* n_out, int accumulate,
                               int n_head, float w_tail, float* y_f32, void* y_hilo, bool pdl,
-                              cudaStream_t s);
+                              cudaStream_t s, int n_split = 0, const float* hpp_rc = nullptr,
+                              const float* hpp_yp = nullptr);
 
 // SIMT (fp32 CUDA-core) building blocks; Xdt is the dtype of X, Rdt of R.
 cudaError_t launch_simt_rowproj(const void* X, dprc_dtype xdt, int64_t B, int64_t T, int64_t c,
@@ -148,8 +174,18 @@ cudaError_t launch_simt_norm_finish(const float* Y, int64_t B, int64_t c, int n,
 // Cluster QR (r = 16, 16 <= p <= 4096): one cluster of 8 CTAs per sample;
 // same output as launch_qr_project.
 bool qr_cluster_supported(int64_t p, int r);
+// With rc set, also writes per sample (rc + i qr_factor_floats()) the R of the
+// column-scaled M (16 x 16 row-major), the 16 column scales s (M diag(s) =
+// Q R) and C = Q^T P (16 x 16); out may then be null (no [Q | P'] written).
+// The launch lets the next kernel start at once (see launch_tc_rowproj).
 cudaError_t launch_qr_cluster(const float* M, int64_t B, int64_t p, const void* P, dprc_dtype pdt,
-                              void* out, bool hilo, cudaStream_t s);
+                              void* out, bool hilo, cudaStream_t s, float* rc = nullptr);
+int qr_factor_floats();
+
+// Hutch++ with the QR beside the third pass (hutchpp.cu): SP = [S | P] row by
+// row (bf16 [p][2r], r a multiple of 8), the first pass's sketch operand.
+cudaError_t launch_pack_cols(const void* S, const void* P, void* SP, int64_t p, int r,
+                             cudaStream_t s);
 cudaError_t launch_qr_project(const float* M, int64_t B, int64_t p, int r, const void* P,
                               dprc_dtype pdt, float* scratch, void* out, bool hilo,
                               cudaStream_t s);

@@ -26,6 +26,12 @@
 // and the compact-WY factor T, so Q = E - V (T V_top^T) and P' need no
 // further exchange.  Sums run in a fixed order (deterministic).
 //
+// With `rc` set, rank 0 of each cluster also writes the sample's factors for
+// a caller that forms X Q as (X M) R^-1: R of the scaled M (its rows fall out
+// of the step totals), the column scales and C.  The kernel lets the next
+// kernel in the stream start at once (programmatic dependent launch); that
+// one must not read what this kernel writes before it completes.
+//
 // Householder QR stays orthonormal when M is rank deficient (a zero reflector
 // is the identity), which is exactly the low-rank case where Hutch++ is exact;
 // the columns are first scaled by their largest magnitude (span unchanged).
@@ -49,6 +55,7 @@ constexpr int kEpt = kCt >= kE ? 1 : kE / kCt;       // of them per thread
 constexpr int kCrows = kR / kCw > 0 ? kR / kCw : 1;  // rows of C = Q^T P per warp
 static_assert((kCt >= kE || kE % kCt == 0) && (kR % kCw == 0 || kCw % kR == 0), "CTA size");
 constexpr int kXch = 256;    // floats per rank slot of the exchange buffer
+constexpr int kRC = 2 * kE + kR;  // factors per sample: R (row-major), column scales, C
 
 template <typename TP>
 __device__ __forceinline__ float ld_elem(const TP* p);
@@ -135,7 +142,7 @@ __device__ __forceinline__ bool xch_wait(const Exchange& x, int rnd) {
 template <int RPT, typename TP>
 __global__ void __launch_bounds__(kCt, 1)
     qr_cluster_kernel(const float* __restrict__ M, int p, const TP* __restrict__ P,
-                      void* __restrict__ out, int hilo) {
+                      void* __restrict__ out, int hilo, float* __restrict__ rc) {
   __shared__ float xbuf[2][kCl][kXch];
   __shared__ __align__(8) uint64_t xbar[2];
   __shared__ float part[kCw][kR];
@@ -145,6 +152,8 @@ __global__ void __launch_bounds__(kCt, 1)
   __shared__ float Tm[kR][kR];
   __shared__ float Km[kR][kR];
   __shared__ float Cm[kR * kR];
+  __shared__ float Rsm[kR][kR];  // R of the scaled M
+  __shared__ float scm[kR];      // column scales
   extern __shared__ float stage[];  // Q rows then P rows: [kCt * RPT][17] each
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -154,6 +163,7 @@ __global__ void __launch_bounds__(kCt, 1)
     if (tid == 0) record_error(DPRC_DEVERR_LAUNCH);
     return;
   }
+  pdl_launch_dependents();  // the next kernel reads nothing this one writes before it ends
   const int rank = static_cast<int>(cluster_ctarank());
   const int i = blockIdx.x / kCl;
   const float* m_i = M + static_cast<size_t>(i) * p * kR;
@@ -219,6 +229,7 @@ __global__ void __launch_bounds__(kCt, 1)
     if (lane < kR)
       for (int r = 0; r < kCl; ++r) tot = fmaxf(tot, xbuf[0][r][lane]);
     const float sc = tot > 0.f ? 1.f / tot : 1.f;
+    if (warp == 0 && lane < kR) scm[lane] = sc;
 #pragma unroll
     for (int l = 0; l < kR; ++l) {
       const float s_l = __shfl_sync(0xffffffffu, sc, l);
@@ -287,6 +298,8 @@ __global__ void __launch_bounds__(kCt, 1)
       } else {
         vtop[j][lane] = 0.f;
       }
+      // row j of R: alpha on the diagonal, the pivot row after the reflector right of it
+      Rsm[j][lane] = lane < j ? 0.f : (lane == j ? alpha : fmaf(-cf_lane, xj - alpha, pv));
     }
     float cf[kR];
 #pragma unroll
@@ -441,12 +454,22 @@ __global__ void __launch_bounds__(kCt, 1)
       if (tid < kE) Cm[tid + kCt * m] = t[m];
   }
   __syncthreads();
+  if (rc != nullptr && rank == 0 && ok) {
+    float* f = rc + static_cast<size_t>(i) * kRC;
+#pragma unroll
+    for (int m = 0; m < kEpt; ++m)
+      if (tid < kE) {
+        f[tid + kCt * m] = (&Rsm[0][0])[tid + kCt * m];
+        f[kE + kR + tid + kCt * m] = Cm[tid + kCt * m];
+      }
+    if (tid < kR) f[kE + tid] = scm[tid];
+  }
 
   // P' = P - Q C and the output rows
 #pragma unroll
   for (int k = 0; k < RPT; ++k) {
     const int row = row_of(k);
-    if (row >= p) continue;
+    if (row >= p || out == nullptr) continue;
     const int loc = k * kCt + tid;
     float q[kR], pp[kR];
 #pragma unroll
@@ -494,7 +517,7 @@ __global__ void __launch_bounds__(kCt, 1)
 
 template <int RPT, typename TP>
 cudaError_t launch_rpt(const float* M, int64_t B, int64_t p, const void* P, void* out, bool hilo,
-                       cudaStream_t s) {
+                       float* rc, cudaStream_t s) {
   auto kern = qr_cluster_kernel<RPT, TP>;
   const int smem = 2 * kCt * RPT * 17 * 4;
   constexpr int kMaxDev = 64;
@@ -524,14 +547,14 @@ cudaError_t launch_rpt(const float* M, int64_t B, int64_t p, const void* P, void
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kern, M, static_cast<int>(p), static_cast<const TP*>(P), out,
-                            hilo ? 1 : 0);
+                            hilo ? 1 : 0, rc);
 }
 
 template <int RPT>
 cudaError_t launch_dt(const float* M, int64_t B, int64_t p, const void* P, dprc_dtype pdt,
-                      void* out, bool hilo, cudaStream_t s) {
-  return pdt == DPRC_F32 ? launch_rpt<RPT, float>(M, B, p, P, out, hilo, s)
-                         : launch_rpt<RPT, __nv_bfloat16>(M, B, p, P, out, hilo, s);
+                      void* out, bool hilo, float* rc, cudaStream_t s) {
+  return pdt == DPRC_F32 ? launch_rpt<RPT, float>(M, B, p, P, out, hilo, rc, s)
+                         : launch_rpt<RPT, __nv_bfloat16>(M, B, p, P, out, hilo, rc, s);
 }
 
 }  // namespace
@@ -542,10 +565,12 @@ cudaError_t read_device_error_qr(int32_t* out, bool reset) {
 
 bool qr_cluster_supported(int64_t p, int r) { return r == kR && p >= kR && p <= 2 * kCl * kCt; }
 
+int qr_factor_floats() { return kRC; }
+
 cudaError_t launch_qr_cluster(const float* M, int64_t B, int64_t p, const void* P, dprc_dtype pdt,
-                              void* out, bool hilo, cudaStream_t s) {
-  if (p <= kCl * kCt) return launch_dt<1>(M, B, p, P, pdt, out, hilo, s);
-  return launch_dt<2>(M, B, p, P, pdt, out, hilo, s);
+                              void* out, bool hilo, cudaStream_t s, float* rc) {
+  if (p <= kCl * kCt) return launch_dt<1>(M, B, p, P, pdt, out, hilo, rc, s);
+  return launch_dt<2>(M, B, p, P, pdt, out, hilo, rc, s);
 }
 
 }  // namespace dprc

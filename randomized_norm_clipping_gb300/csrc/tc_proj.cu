@@ -174,6 +174,11 @@ struct RowArgs {
   long long tpad;
   int* zero_ptr;
   int zero_ints;
+  // launched as a programmatic dependent that runs beside the previous
+  // kernel (its inputs are older): CTA 0 waits for that kernel to complete
+  // before it exits, so this kernel's completion implies the other's (the
+  // other CTAs leave as they finish and free their slots)
+  int wait_end;
 };
 
 template <int NMMA, bool HILO_IN>
@@ -392,6 +397,7 @@ __global__ void __launch_bounds__(192, 2)
   // every distributed shared memory access of the cluster is complete before
   // any of its CTAs exits
   if (sc.cl > 1) cluster_sync_all();
+  if (a.wait_end && blockIdx.x == 0 && threadIdx.x == 0) pdl_wait();
 }
 
 // ===========================================================================
@@ -413,7 +419,53 @@ struct ColArgs {
   float w_tail;
   float* y_f32;
   __nv_bfloat16* y_hilo;
+  int n_split;  // kColprojSplit: columns [0, n_split) to y_hilo, the rest to y_f32
+  // kColprojHpp: the QR factors [B][hpp_rcs] and X P fp32 [B][c][16]
+  const float* hpp_rc;
+  const float* hpp_yp;
+  int hpp_rcs;
 };
+
+// Hutch++ head and tail of one row of d from Y_M = X M (y) and Y_P = X P
+// (yp): Y_Q = (y diag(s)) R^-1 by forward substitution (rinv[j] = 0 leaves
+// column j out), ||Y_Q||^2 + ||Y_P - Y_Q C||^2 / 16.  f: R (row-major), s,
+// C, rinv, in shared memory.
+__device__ __forceinline__ float hpp_row(const float (&y)[16], const float* __restrict__ yp,
+                                         const float* f) {
+  const float* R = f;
+  const float* sc = f + 256;
+  const float* C = f + 272;
+  const float* rinv = f + 528;
+  float yq[16];
+  float head = 0.f;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    float t = y[j] * sc[j];
+#pragma unroll
+    for (int a2 = 0; a2 < j; ++a2) t = fmaf(-yq[a2], R[a2 * 16 + j], t);
+    yq[j] = t * rinv[j];
+    head = fmaf(yq[j], yq[j], head);
+  }
+  float ypr[16];
+  const float4* p4 = reinterpret_cast<const float4*>(yp);
+#pragma unroll
+  for (int c4 = 0; c4 < 4; ++c4) {
+    const float4 v = p4[c4];
+    ypr[4 * c4] = v.x;
+    ypr[4 * c4 + 1] = v.y;
+    ypr[4 * c4 + 2] = v.z;
+    ypr[4 * c4 + 3] = v.w;
+  }
+  float tail = 0.f;
+#pragma unroll
+  for (int l = 0; l < 16; ++l) {
+    float t = ypr[l];
+#pragma unroll
+    for (int a2 = 0; a2 < 16; ++a2) t = fmaf(-yq[a2], C[a2 * 16 + l], t);
+    tail = fmaf(t, t, tail);
+  }
+  return head + tail * (1.f / 16.f);
+}
 
 template <int NMMA>
 struct ColCfg {
@@ -440,6 +492,7 @@ __global__ void __launch_bounds__(192, ColCfg<NMMA>::kCtasPerSm)
   constexpr int kN = Cfg::kN;
   extern __shared__ uint8_t smem_raw[];
   __shared__ float s_red[4];
+  __shared__ __align__(16) float s_hf[kN == 16 ? 544 : 1];  // Hutch++ factors (kColprojHpp)
 
   const Sched& sc = a.sched;
   // The schedule splits blocks over clusters of sc.cl CTAs; a launch of any
@@ -632,10 +685,29 @@ __global__ void __launch_bounds__(192, ColCfg<NMMA>::kCtasPerSm)
       const int i = static_cast<int>(b / a.nchunks);
       const int ch = static_cast<int>(b - static_cast<long long>(i) * a.nchunks);
       const int grow = ch * kColChunk + row;
-      if (a.mode == kColprojNorm) {
-        // this CTA's rows: weighted squares, then a fixed-order reduction
+      if (a.mode == kColprojNorm || a.mode == kColprojHpp) {
+        // this CTA's rows: weighted squares (or the Hutch++ head and tail),
+        // then a fixed-order reduction
         float sq = 0.f;
-        if (mine && ok && grow < a.c) {
+        if (a.mode == kColprojHpp) {
+          if constexpr (kN == 16) {
+            // sample i's factors, then 1 / R_jj of the columns kept
+            const float* f = a.hpp_rc + static_cast<size_t>(i) * a.hpp_rcs;
+            const int et = threadIdx.x - 64;
+            for (int e = et; e < 528; e += 128) s_hf[e] = f[e];
+            named_bar_sync(1, 128);
+            if (et < 16) {
+              float cn = 0.f;
+              for (int a2 = 0; a2 <= et; ++a2) cn = fmaf(s_hf[a2 * 16 + et], s_hf[a2 * 16 + et], cn);
+              const float rjj = s_hf[et * 16 + et];
+              s_hf[528 + et] = rjj * rjj > kHppDropTau * kHppDropTau * cn ? 1.f / rjj : 0.f;
+            }
+            named_bar_sync(1, 128);
+            if (mine && ok && grow < a.c && DPRC_IN(b < sc.nblocks))
+              sq = hpp_row(y, a.hpp_yp + (static_cast<size_t>(i) * a.c + grow) * 16, s_hf);
+            named_bar_sync(1, 128);  // s_hf is rewritten for the next block
+          }
+        } else if (mine && ok && grow < a.c) {
 #pragma unroll
           for (int t = 0; t < kN; ++t) sq += (t < a.n_head ? 1.f : a.w_tail) * y[t] * y[t];
         }
@@ -689,15 +761,27 @@ __global__ void __launch_bounds__(192, ColCfg<NMMA>::kCtasPerSm)
         }
         named_bar_sync(1, 128);
       } else if (mine && ok && grow < a.c && DPRC_IN(b < sc.nblocks)) {
-        if (a.mode == kColprojF32) {
-          float4* d4 = reinterpret_cast<float4*>(a.y_f32 + (static_cast<size_t>(i) * a.c + grow) * kN);
+        const size_t yrow = static_cast<size_t>(i) * a.c + grow;
+        if (a.mode == kColprojF32 || a.mode == kColprojF32Hilo) {
+          float4* d4 = reinterpret_cast<float4*>(a.y_f32 + yrow * kN);
 #pragma unroll
           for (int c4 = 0; c4 < kN / 4; ++c4)
             d4[c4] = make_float4(y[4 * c4], y[4 * c4 + 1], y[4 * c4 + 2], y[4 * c4 + 3]);
-        } else {
-          __nv_bfloat16* dst = a.y_hilo + (static_cast<size_t>(i) * a.c + grow) * 2 * kN;
+        }
+        if (a.mode == kColprojHilo || a.mode == kColprojF32Hilo)
+          store_hilo_row<kN>(a.y_hilo + yrow * 2 * kN, y);
+        if (a.mode == kColprojSplit) {
+          // the first half as hi/lo rows of kN values, the second as fp32 rows
+          constexpr int kH = kN / 2;
+          float yh[kH];
 #pragma unroll
-          for (int t = 0; t < kN; ++t) split_hilo(y[t], dst[t], dst[kN + t]);
+          for (int t = 0; t < kH; ++t) yh[t] = y[t];
+          store_hilo_row<kH>(a.y_hilo + yrow * 2 * kH, yh);
+          float4* f4 = reinterpret_cast<float4*>(a.y_f32 + yrow * kH);
+#pragma unroll
+          for (int c4 = 0; c4 < kH / 4; ++c4)
+            f4[c4] = make_float4(y[kH + 4 * c4], y[kH + 4 * c4 + 1], y[kH + 4 * c4 + 2],
+                                 y[kH + 4 * c4 + 3]);
         }
       }
     }
@@ -782,7 +866,7 @@ cudaError_t read_device_error_proj(int32_t* out, bool reset) {
 cudaError_t launch_tc_rowproj(const void* X, int64_t B, int64_t T, int64_t c, const void* R,
                               bool r_batched, int nmma, bool hilo_in, void* W, int64_t tpad,
                               const BlockSched& bs, int* zero_ptr, size_t zero_ints,
-                              cudaStream_t s) {
+                              cudaStream_t s, bool beside_previous) {
   CUtensorMap mx, mr;
   if (!make_tmap_3d_bf16(&mx, X, c, T, B, c, T * c, kTileC, kRowTile, 128))
     return cudaErrorInvalidValue;
@@ -799,12 +883,12 @@ cudaError_t launch_tc_rowproj(const void* X, int64_t B, int64_t T, int64_t c, co
   a.tpad = tpad;
   a.zero_ptr = zero_ptr;
   a.zero_ints = static_cast<int>(zero_ints);
-#define DPRC_ROW(NM, HL)                                                                 \
-  if (nmma == NM && hilo_in == HL)                                                       \
-    return launch_sched<tc_rowproj_kernel<NM, HL>>(bs.grid, bs.cl,                       \
-                                                   RowCfg<NM, HL>::smem(bs.cl),          \
-                                                   RowCfg<NM, HL>::smem(8), false, s, mx, \
-                                                   mr, a);
+  a.wait_end = beside_previous ? 1 : 0;
+#define DPRC_ROW(NM, HL)                                                              \
+  if (nmma == NM && hilo_in == HL)                                                    \
+    return launch_sched<tc_rowproj_kernel<NM, HL>>(                                   \
+        bs.grid, bs.cl, RowCfg<NM, HL>::smem(bs.cl), RowCfg<NM, HL>::smem(8),         \
+        beside_previous, s, mx, mr, a);
   DPRC_ROW(16, false)
   DPRC_ROW(32, false)
   DPRC_ROW(64, false)
@@ -818,8 +902,12 @@ cudaError_t launch_tc_colproj(const void* X, int64_t B, int64_t T, int64_t c, co
                               int64_t tpad, int n, const BlockSched& bs, int* sample_tickets,
                               float* chunk_norms, ColprojMode mode, float* n_out, int accumulate,
                               int n_head, float w_tail, float* y_f32, void* y_hilo, bool pdl,
-                              cudaStream_t s) {
+                              cudaStream_t s, int n_split, const float* hpp_rc,
+                              const float* hpp_yp) {
   const int nmma = 2 * n;
+  if (mode == kColprojSplit && 2 * n_split != n) return cudaErrorInvalidValue;
+  if (mode == kColprojHpp && (n != 16 || hpp_rc == nullptr || hpp_yp == nullptr))
+    return cudaErrorInvalidValue;
   CUtensorMap mx, mw;
   if (!make_tmap_3d_bf16(&mx, X, c, T, B, c, T * c, 64, kTileT, 128))
     return cudaErrorInvalidValue;
@@ -839,6 +927,10 @@ cudaError_t launch_tc_colproj(const void* X, int64_t B, int64_t T, int64_t c, co
   a.w_tail = w_tail;
   a.y_f32 = y_f32;
   a.y_hilo = static_cast<__nv_bfloat16*>(y_hilo);
+  a.n_split = n_split;
+  a.hpp_rc = hpp_rc;
+  a.hpp_yp = hpp_yp;
+  a.hpp_rcs = qr_factor_floats();
 #define DPRC_COL(NM)                                                                        \
   if (nmma == NM)                                                                           \
     return launch_sched<tc_colproj_kernel<NM>>(bs.grid, bs.cl, ColCfg<NM>::smem(bs.cl),     \

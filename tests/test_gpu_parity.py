@@ -352,8 +352,12 @@ def test_hutch_identity_projection_gives_exact_norm():
 
 # ------------------------------------------------------------------ Hutch++
 
+# the cluster QR with one row per thread (p <= 2048, 2040 with a ragged last
+# CTA) and two (2056 .. 4096, up to its bound); past it (4200) the one-CTA QR
+# and the three passes in sequence
 @pytest.mark.parametrize("B,T,d,p", [(2, 200, 256, 256), (3, 77, 136, 64), (2, 1100, 512, 1024),
-                                     (2, 300, 256, 3000)])
+                                     (2, 300, 256, 3000), (2, 150, 136, 128), (2, 300, 128, 2040),
+                                     (2, 300, 128, 2056), (1, 200, 128, 4096), (1, 120, 128, 4200)])
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 def test_hutchpp_matches_oracle(B, T, d, p, dtype):
     r = 16
@@ -363,6 +367,25 @@ def test_hutchpp_matches_oracle(B, T, d, p, dtype):
     G = (torch.bmm(U, V.transpose(1, 2)) / np.sqrt(8) + 0.05 * torch.randn(B, T, p, generator=g)).to(dtype)
     S = _rand((p, r), 42, dtype)
     P = _rand((p, r), 43, dtype)
+    n = torch.zeros(B, device=DEV)
+    rnc.dprc_norm_hutchpp(A.to(DEV), G.to(DEV), S.to(DEV), P.to(DEV), n)
+    ref = oracle.hutchpp_norm(to_f64(A), to_f64(G), to_f64(S), to_f64(P))
+    assert _relerr(n.cpu(), ref) < RTOL
+
+
+@pytest.mark.parametrize("tail", [1e-2, 1e-3, 1e-5, 0.0])
+def test_hutchpp_near_rank_deficient_sketch(tail):
+    # G = rank 8 + a small tail: M = O S has 8 strong columns and 8 at the
+    # tail's level, down to rounding noise (tail 0).  The combining step
+    # forms X Q as (X M) R^-1 and drops columns of R at noise level; the
+    # result must still be the oracle's (Householder Q) within RTOL
+    B, T, d, p, r = 2, 300, 256, 512, 16
+    A = _rand((B, T, d), 60, torch.bfloat16)
+    g = torch.Generator(device="cpu").manual_seed(61)
+    U, V = torch.randn(B, T, 8, generator=g), torch.randn(B, p, 8, generator=g)
+    G = (torch.bmm(U, V.transpose(1, 2)) / np.sqrt(8) + tail * torch.randn(B, T, p, generator=g))
+    G = G.to(torch.bfloat16)
+    S, P = _rand((p, r), 62, torch.bfloat16), _rand((p, r), 63, torch.bfloat16)
     n = torch.zeros(B, device=DEV)
     rnc.dprc_norm_hutchpp(A.to(DEV), G.to(DEV), S.to(DEV), P.to(DEV), n)
     ref = oracle.hutchpp_norm(to_f64(A), to_f64(G), to_f64(S), to_f64(P))
