@@ -428,43 +428,76 @@ struct ColArgs {
 
 // Hutch++ head and tail of one row of d from Y_M = X M (y) and Y_P = X P
 // (yp): Y_Q = (y diag(s)) R^-1 by forward substitution (rinv[j] = 0 leaves
-// column j out), ||Y_Q||^2 + ||Y_P - Y_Q C||^2 / 16.  f: R (row-major), s,
-// C, rinv, in shared memory.
+// column j out), ||Y_Q||^2 + ||Y_P - Y_Q C||^2 / 16.  f, in shared memory:
+// R^T and C^T (so each column's coefficients are 16 contiguous floats, read
+// 4 at a time), s, rinv.
+constexpr int kHppF = 2 * 256 + 2 * 16;  // floats of f
 __device__ __forceinline__ float hpp_row(const float (&y)[16], const float* __restrict__ yp,
                                          const float* f) {
-  const float* R = f;
-  const float* sc = f + 256;
-  const float* C = f + 272;
+  const float* RT = f;
+  const float* CT = f + 256;
+  const float* sc = f + 512;
   const float* rinv = f + 528;
   float yq[16];
   float head = 0.f;
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
     float t = y[j] * sc[j];
+    const float4* r4 = reinterpret_cast<const float4*>(RT + j * 16);
 #pragma unroll
-    for (int a2 = 0; a2 < j; ++a2) t = fmaf(-yq[a2], R[a2 * 16 + j], t);
+    for (int q4 = 0; q4 < (j + 3) / 4; ++q4) {
+      const float4 c = r4[q4];
+      const float cs[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (4 * q4 + u < j) t = fmaf(-yq[4 * q4 + u], cs[u], t);
+    }
     yq[j] = t * rinv[j];
     head = fmaf(yq[j], yq[j], head);
   }
-  float ypr[16];
   const float4* p4 = reinterpret_cast<const float4*>(yp);
-#pragma unroll
-  for (int c4 = 0; c4 < 4; ++c4) {
-    const float4 v = p4[c4];
-    ypr[4 * c4] = v.x;
-    ypr[4 * c4 + 1] = v.y;
-    ypr[4 * c4 + 2] = v.z;
-    ypr[4 * c4 + 3] = v.w;
-  }
   float tail = 0.f;
 #pragma unroll
-  for (int l = 0; l < 16; ++l) {
-    float t = ypr[l];
+  for (int l4 = 0; l4 < 4; ++l4) {
+    const float4 pv = p4[l4];
+    const float ps[4] = {pv.x, pv.y, pv.z, pv.w};
 #pragma unroll
-    for (int a2 = 0; a2 < 16; ++a2) t = fmaf(-yq[a2], C[a2 * 16 + l], t);
-    tail = fmaf(t, t, tail);
+    for (int u = 0; u < 4; ++u) {
+      const int l = 4 * l4 + u;
+      float t = ps[u];
+      const float4* c4 = reinterpret_cast<const float4*>(CT + l * 16);
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        const float4 c = c4[q4];
+        t = fmaf(-yq[4 * q4], c.x, t);
+        t = fmaf(-yq[4 * q4 + 1], c.y, t);
+        t = fmaf(-yq[4 * q4 + 2], c.z, t);
+        t = fmaf(-yq[4 * q4 + 3], c.w, t);
+      }
+      tail = fmaf(t, t, tail);
+    }
   }
   return head + tail * (1.f / 16.f);
+}
+
+// Stages sample i's Hutch++ factors (R, s, C from the QR: row-major R, then s,
+// then row-major C) into f as hpp_row reads them, by the 128 epilogue threads
+// (index et), then 1 / R_jj of the columns kept.
+__device__ __forceinline__ void hpp_stage(const float* __restrict__ rc, float* f, int et) {
+  for (int e = et; e < 256; e += 128) {
+    const int a2 = e >> 4, j = e & 15;
+    f[j * 16 + a2] = rc[e];              // R^T
+    f[256 + j * 16 + a2] = rc[272 + e];  // C^T
+  }
+  if (et < 16) f[512 + et] = rc[256 + et];
+  named_bar_sync(1, 128);
+  if (et < 16) {
+    float cn = 0.f;
+    for (int a2 = 0; a2 <= et; ++a2) cn = fmaf(f[et * 16 + a2], f[et * 16 + a2], cn);
+    const float rjj = f[et * 16 + et];
+    f[528 + et] = rjj * rjj > kHppDropTau * kHppDropTau * cn ? 1.f / rjj : 0.f;
+  }
+  named_bar_sync(1, 128);
 }
 
 template <int NMMA>
@@ -492,7 +525,7 @@ __global__ void __launch_bounds__(192, ColCfg<NMMA>::kCtasPerSm)
   constexpr int kN = Cfg::kN;
   extern __shared__ uint8_t smem_raw[];
   __shared__ float s_red[4];
-  __shared__ __align__(16) float s_hf[kN == 16 ? 544 : 1];  // Hutch++ factors (kColprojHpp)
+  __shared__ __align__(16) float s_hf[kN == 16 ? kHppF : 4];  // Hutch++ factors (kColprojHpp)
 
   const Sched& sc = a.sched;
   // The schedule splits blocks over clusters of sc.cl CTAs; a launch of any
@@ -659,6 +692,15 @@ __global__ void __launch_bounds__(192, ColCfg<NMMA>::kCtasPerSm)
     const int row = q * 32 + lane;  // row of the 128-row chunk = TMEM lane
     bool ok = true;
     int seg = 0;
+    int hpp_i = -1;  // sample whose Hutch++ factors s_hf holds
+    if constexpr (kN == 16) {
+      // the factors do not depend on this kernel's accumulators: the first
+      // block's are staged while its tiles stream
+      if (a.mode == kColprojHpp && wk.b0 < wk.b1) {
+        hpp_i = static_cast<int>(wk.b0 / a.nchunks);
+        hpp_stage(a.hpp_rc + static_cast<size_t>(hpp_i) * a.hpp_rcs, s_hf, threadIdx.x - 64);
+      }
+    }
     for (long long b = wk.b0; b < wk.b1; ++b, ++seg) {
       const int abuf = seg & 1;
       bool live = ok && mbar_wait(&accf[abuf], (seg >> 1) & 1, DPRC_DEVERR_ACCUM) &&
@@ -691,21 +733,13 @@ __global__ void __launch_bounds__(192, ColCfg<NMMA>::kCtasPerSm)
         float sq = 0.f;
         if (a.mode == kColprojHpp) {
           if constexpr (kN == 16) {
-            // sample i's factors, then 1 / R_jj of the columns kept
-            const float* f = a.hpp_rc + static_cast<size_t>(i) * a.hpp_rcs;
-            const int et = threadIdx.x - 64;
-            for (int e = et; e < 528; e += 128) s_hf[e] = f[e];
-            named_bar_sync(1, 128);
-            if (et < 16) {
-              float cn = 0.f;
-              for (int a2 = 0; a2 <= et; ++a2) cn = fmaf(s_hf[a2 * 16 + et], s_hf[a2 * 16 + et], cn);
-              const float rjj = s_hf[et * 16 + et];
-              s_hf[528 + et] = rjj * rjj > kHppDropTau * kHppDropTau * cn ? 1.f / rjj : 0.f;
+            if (i != hpp_i) {  // a block of the next sample: its factors
+              named_bar_sync(1, 128);  // every thread is done with the last ones
+              hpp_i = i;
+              hpp_stage(a.hpp_rc + static_cast<size_t>(i) * a.hpp_rcs, s_hf, threadIdx.x - 64);
             }
-            named_bar_sync(1, 128);
             if (mine && ok && grow < a.c && DPRC_IN(b < sc.nblocks))
               sq = hpp_row(y, a.hpp_yp + (static_cast<size_t>(i) * a.c + grow) * 16, s_hf);
-            named_bar_sync(1, 128);  // s_hf is rewritten for the next block
           }
         } else if (mine && ok && grow < a.c) {
 #pragma unroll
