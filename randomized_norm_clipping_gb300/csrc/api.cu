@@ -689,6 +689,7 @@ dprc_status dprc_set_phase_events(void** events, int n_events) {
 dprc_status dprc_norm_hutch(const void* A, const void* G, const void* P, dprc_dtype dtype,
                             int64_t B, int64_t T, int64_t d, int64_t p, int64_t k, float* n,
                             int accumulate, void* ws, size_t ws_bytes, void* stream) {
+  DPRC_NVTX_RANGE();
   return norm_hutch_impl(A, G, P, dtype, B, T, d, p, k, n, accumulate, ws, ws_bytes, stream,
                          nullptr);
 }
@@ -697,6 +698,7 @@ dprc_status dprc_norm_hutch_layers(int64_t L, const void* const* A, const void* 
                                    const void* const* P, const int64_t* d, const int64_t* p,
                                    dprc_dtype dtype, int64_t B, int64_t T, int64_t k, float* n,
                                    int accumulate, void* ws, size_t ws_bytes, void* stream) {
+  DPRC_NVTX_RANGE();
   return norm_hutch_layers_impl(L, A, G, P, d, p, dtype, B, T, k, n, accumulate, ws, ws_bytes,
                                 stream, nullptr);
 }
@@ -707,6 +709,7 @@ dprc_status dprc_norm_hutch_layers_clip(int64_t L, const void* const* A, const v
                                         float* n, int accumulate, float C, float* c,
                                         int32_t* nonfinite, void* ws, size_t ws_bytes,
                                         void* stream) {
+  DPRC_NVTX_RANGE();
   ClipOut clip;
   clip.C = C;
   clip.c = c;
@@ -719,6 +722,7 @@ dprc_status dprc_norm_hutch_clip(const void* A, const void* G, const void* P, dp
                                  int64_t B, int64_t T, int64_t d, int64_t p, int64_t k, float* n,
                                  int accumulate, float C, float* c, int32_t* nonfinite, void* ws,
                                  size_t ws_bytes, void* stream) {
+  DPRC_NVTX_RANGE();
   ClipOut clip;
   clip.C = C;
   clip.c = c;
@@ -731,6 +735,7 @@ dprc_status dprc_norm_hutch_clip_host(const void* A, const void* G, const void* 
                                       dprc_dtype dtype, int64_t B, int64_t T, int64_t d,
                                       int64_t p, int64_t k, float C, float* n, float* c,
                                       void* stage, size_t stage_bytes, void* stream) {
+  DPRC_NVTX_RANGE();
   if (!A || !G || !P || !c) return DPRC_ERR_NULL;
   dprc_status st = check_common(dtype, B, T, d, p);
   if (st != DPRC_OK) return st;
@@ -816,6 +821,7 @@ dprc_status dprc_norm_hutch_pm1(const void* A, const void* G, uint64_t seed, uin
                                 dprc_dtype dtype, int64_t B, int64_t T, int64_t d, int64_t p,
                                 int64_t k, float* n, int accumulate, void* ws, size_t ws_bytes,
                                 void* stream) {
+  DPRC_NVTX_RANGE();
   if (!A || !G || !n) return DPRC_ERR_NULL;
   dprc_status st = check_common(dtype, B, T, d, p);
   if (st != DPRC_OK) return st;
@@ -867,6 +873,7 @@ dprc_status dprc_norm_hutchpp(const void* A, const void* G, const void* S, const
                               dprc_dtype dtype, int64_t B, int64_t T, int64_t d, int64_t p,
                               int64_t r, float* n, int accumulate, void* ws, size_t ws_bytes,
                               void* stream) {
+  DPRC_NVTX_RANGE();
   if (!A || !G || !S || !P || !n) return DPRC_ERR_NULL;
   dprc_status st = check_common(dtype, B, T, d, p);
   if (st != DPRC_OK) return st;
@@ -993,6 +1000,7 @@ dprc_status dprc_norm_hutchpp(const void* A, const void* G, const void* S, const
 dprc_status dprc_exact_norm_form(const void* A, const void* G, dprc_dtype dtype, int64_t B,
                                  int64_t T, int64_t d, int64_t p, int form, float* n,
                                  int accumulate, void* ws, size_t ws_bytes, void* stream) {
+  DPRC_NVTX_RANGE();
   if (!A || !G || !n) return DPRC_ERR_NULL;
   dprc_status st = check_common(dtype, B, T, d, p);
   if (st != DPRC_OK) return st;
@@ -1050,6 +1058,7 @@ int dprc_exact_norm_plan(dprc_dtype dtype, int64_t B, int64_t T, int64_t d, int6
 
 dprc_status dprc_clip_factors(const float* n, int64_t B, float C, float* c, int32_t* nonfinite,
                               void* stream) {
+  DPRC_NVTX_RANGE();
   if (!n || !c) return DPRC_ERR_NULL;
   if (B < 1 || B > (int64_t(1) << 31)) return DPRC_ERR_SHAPE;
   if (!(C > 0.f) || !(C < __builtin_inff())) return DPRC_ERR_SHAPE;
@@ -1060,6 +1069,7 @@ dprc_status dprc_clip_factors(const float* n, int64_t B, float C, float* c, int3
 
 dprc_status dprc_add_noise(float* grad, int64_t N, float sigma, float C, uint64_t seed,
                            uint64_t step, void* stream) {
+  DPRC_NVTX_RANGE();
   if (N < 0) return DPRC_ERR_SHAPE;
   if (N > 0 && !grad) return DPRC_ERR_NULL;
   if (!(sigma >= 0.f) || !(sigma < __builtin_inff()) || !(C >= 0.f) || !(C < __builtin_inff()))
@@ -1076,6 +1086,7 @@ dprc_status dprc_add_noise(float* grad, int64_t N, float sigma, float C, uint64_
 
 dprc_status dprc_add_noise_at(void* grad, dprc_dtype dtype, int64_t N, uint64_t first_element,
                              float sigma, float C, uint64_t seed, uint64_t step, void* stream) {
+  DPRC_NVTX_RANGE();
   if (dtype != DPRC_F32 && dtype != DPRC_BF16) return DPRC_ERR_DTYPE;
   if (N < 0) return DPRC_ERR_SHAPE;
   if (N > 0 && !grad) return DPRC_ERR_NULL;
@@ -1095,6 +1106,7 @@ dprc_status dprc_add_noise_at(void* grad, dprc_dtype dtype, int64_t N, uint64_t 
 
 dprc_status dprc_philox_words(uint32_t* out, int64_t n_blocks, uint64_t first_block,
                               uint64_t seed, uint64_t step, void* stream) {
+  DPRC_NVTX_RANGE();
   if (n_blocks < 0) return DPRC_ERR_SHAPE;
   if (n_blocks > 0 && !out) return DPRC_ERR_NULL;
   if (n_blocks > 0 && !aligned16(out)) return DPRC_ERR_ALIGN;
@@ -1108,6 +1120,7 @@ dprc_status dprc_test_hutch_fault(int mode, uint64_t wait_ns, int64_t L, const v
                                   const void* const* G, const void* const* P, const int64_t* d,
                                   const int64_t* p, int64_t B, int64_t T, int64_t k, float* n,
                                   void* ws, size_t ws_bytes, void* stream) {
+  DPRC_NVTX_RANGE();
   if (!A || !G || !P || !d || !p || !n) return DPRC_ERR_NULL;
   if (mode != kFaultReadyNeverMet && mode != kFaultClusterShape) return DPRC_ERR_SHAPE;
   constexpr uint64_t kMaxWaitNs = 2000000000ull;  // the kernels' own limit

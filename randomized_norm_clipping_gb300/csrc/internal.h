@@ -7,7 +7,21 @@
 
 #include "dprc.h"
 
+#include <nvtx3/nvToolsExt.h>
+
 namespace dprc {
+
+// One NVTX range per C-ABI call, named after the call, so the kernels of a
+// call group under its name in a profiler's timeline (ncu --nvtx).  With no
+// tool attached a push or pop is a check of an unset function pointer.
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
+#define DPRC_NVTX_RANGE() ::dprc::NvtxRange dprc_nvtx_range_(__func__)
+
 
 // ---- block schedules --------------------------------------------------------
 // How one tensor-core launch assigns its blocks (128 output rows, `upb` units

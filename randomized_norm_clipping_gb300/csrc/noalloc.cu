@@ -55,6 +55,7 @@ extern "C" dprc_status dprc_norm_hutch_noalloc(const void* A, const void* G, con
                                                dprc_dtype dtype, int64_t B, int64_t T,
                                                int64_t d, int64_t p, int64_t k, float* n,
                                                int accumulate, void* stream) {
+  DPRC_NVTX_RANGE();
   // every check that needs no device first: an argument error returns before
   // the scratch is looked up or its counters are cleared
   dprc_status st = dprc::check_hutch_args(A, G, P, dtype, B, T, d, p, k, n);
