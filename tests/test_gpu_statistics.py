@@ -15,7 +15,9 @@ the tested seeds and fail these.
     or (2/k)(||O||_F^2 - sum_j O_jj^2) (the +-1 projection), and the sample
     variance matches that law;
   - the chi^2(k) law for a rank-one O (T = 1), by a Kolmogorov-Smirnov test,
-    with chi^2(k - 1) and chi^2(2k) rejected.
+    with chi^2(k - 1) and chi^2(2k) rejected;
+  - Hutch++ over fresh P for a fixed S: the mean is trace(O) and the variance
+    2 ||O_res||_F^2 / r, O_res the part of O outside the head's span.
 
 Shapes: the single-layer fp32 configuration (B4 T128 d = p = 64, k = 8:
 CUDA-core path) and a bf16 layer that takes the one-launch tensor-core kernel
@@ -171,3 +173,41 @@ def test_draws_are_independent_of_each_other():
     for i in range(x.shape[1]):
         c = np.corrcoef(x[:-1, i], x[1:, i])[0, 1]
         assert abs(c) < 4.0 / math.sqrt(DRAWS), (i, c)
+
+
+def test_hutchpp_tail_is_unbiased_given_the_head():
+    # Hutch++ (papernotes.org, "Key design > Hutch++ head-tail decomposition"):
+    # for a fixed S the head ||X Q||^2 is exact and the tail (1/r)||X P'||^2,
+    # P' = (I - Q Q^T) P with P ~ N(0, 1), is unbiased for trace(O_res),
+    # O_res = (I - Q Q^T) O (I - Q Q^T), with variance 2 ||O_res||_F^2 / r.  So
+    # over fresh P the estimates average to trace(O) = ||A^T G||_F^2 exactly.
+    # Run through the tensor-core path whose third pass streams X M and forms
+    # X Q = (X M) R^-1 in its epilogue: a wrong factor, scale or C in that
+    # step would bias the mean or change the variance.
+    B, T, d, p, r = 2, 256, 256, 256, 16
+    g = torch.Generator(device=DEV).manual_seed(37)
+    A = torch.randn(B, T, d, generator=g, device=DEV).to(torch.bfloat16)
+    U = torch.randn(B, T, 8, generator=g, device=DEV)
+    V = torch.randn(B, p, 8, generator=g, device=DEV)
+    G = (torch.bmm(U, V.transpose(1, 2)) / math.sqrt(8)
+         + 0.3 * torch.randn(B, T, p, generator=g, device=DEV)).to(torch.bfloat16)
+    S = torch.randn(p, r, generator=g, device=DEV).to(torch.bfloat16)
+    draws = 4000
+    Ps = torch.randn(draws, p, r, generator=g, device=DEV).to(torch.bfloat16)
+    out = _rows(B)[:draws]
+    ws = rnc.workspace(rnc.DPRC_OP_HUTCHPP, A, B, T, d, p, r)
+    for j in range(draws):
+        rnc.dprc_norm_hutchpp(A, G, S, Ps[j], out[j, :B], ws=ws)
+    torch.cuda.synchronize()
+    x = out[:, :B].double().cpu().numpy()
+    Af, Gf, Sf = to_f64(A), to_f64(G), to_f64(S)
+    for i in range(B):
+        X = Af[i].T @ Gf[i]
+        O = X.T @ X
+        Q, _ = np.linalg.qr(O @ Sf)
+        Pr = np.eye(p) - Q @ Q.T
+        Ores = Pr @ O @ Pr
+        var = 2.0 * np.sum(Ores * Ores) / r
+        se = math.sqrt(var / draws)
+        assert abs(x[:, i].mean() - np.trace(O)) < 4.0 * se, (i, x[:, i].mean(), np.trace(O), se)
+        assert abs(x[:, i].var() / var - 1.0) < 0.15, (i, x[:, i].var(), var)
