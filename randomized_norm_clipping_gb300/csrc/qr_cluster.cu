@@ -528,6 +528,11 @@ cudaError_t launch_rpt(const float* M, int64_t B, int64_t p, const void* P, void
   if (dev < 0 || dev >= kMaxDev || !done[dev].load(std::memory_order_acquire)) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
+    // an SM that takes a QR CTA keeps its largest shared-memory carve-out, so
+    // two sketch CTAs of the pass that runs beside the QR fit next to it
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
     if (kCl > 8) {
       e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
       if (e != cudaSuccess) return e;
