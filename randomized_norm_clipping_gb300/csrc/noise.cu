@@ -46,9 +46,14 @@ __device__ __forceinline__ float neg2log_u1(uint32_t a) {
 // u2 = (b >> 8) 2^-24 in [0, 1):  (r cos 2 pi u2, r sin 2 pi u2),
 // r = sqrt(-2 ln u1).  The angle is taken as x + pi with x = 2 pi (u2 - 1/2)
 // in [-pi, pi), where the hardware sine and cosine have absolute error
-// <= 2^-21.41, hence |error| <= 2e-6 + 1e-6 r for each normal.
+// <= 2^-21.41, hence |error| <= 2e-6 + 1e-6 r for each normal.  r is taken as
+// q rsqrt(q), q = -2 ln u1 (rsqrtf within 2 ulp: relative 2.5e-7 in r, inside
+// that bound; a few instructions fewer than the correctly rounded sqrtf in a
+// kernel whose instruction issue sits close to its memory time); q = 0
+// (u1 = 1) gives r = 0.
 __device__ __forceinline__ float2 box_muller(uint32_t a, uint32_t b) {
-  const float rad = sqrtf(neg2log_u1(a));
+  const float q = neg2log_u1(a);
+  const float rad = q > 0.f ? q * rsqrtf(q) : 0.f;
   const float t = static_cast<float>(b >> 8) * 5.9604644775390625e-8f - 0.5f;  // exact
   float s, c;
   __sincosf(6.283185307179586f * t, &s, &c);
