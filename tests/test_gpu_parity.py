@@ -357,7 +357,8 @@ def test_hutch_identity_projection_gives_exact_norm():
 # and the three passes in sequence
 @pytest.mark.parametrize("B,T,d,p", [(2, 200, 256, 256), (3, 77, 136, 64), (2, 1100, 512, 1024),
                                      (2, 300, 256, 3000), (2, 150, 136, 128), (2, 300, 128, 2040),
-                                     (2, 300, 128, 2056), (1, 200, 128, 4096), (1, 120, 128, 4200)])
+                                     (2, 300, 128, 2056), (1, 200, 128, 4096), (1, 120, 128, 4200),
+                                     (1, 50, 8, 16), (2, 1, 16, 24)])
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 def test_hutchpp_matches_oracle(B, T, d, p, dtype):
     r = 16
@@ -390,6 +391,20 @@ def test_hutchpp_near_rank_deficient_sketch(tail):
     rnc.dprc_norm_hutchpp(A.to(DEV), G.to(DEV), S.to(DEV), P.to(DEV), n)
     ref = oracle.hutchpp_norm(to_f64(A), to_f64(G), to_f64(S), to_f64(P))
     assert _relerr(n.cpu(), ref) < RTOL
+
+
+def test_hutchpp_accumulates():
+    # n (+)= the estimate: a second call with accumulate adds the same value
+    B, T, d, p, r = 2, 200, 136, 256, 16
+    A = _rand((B, T, d), 70, torch.bfloat16)
+    G = _rand((B, T, p), 71, torch.bfloat16, 0.1)
+    S, P = _rand((p, r), 72, torch.bfloat16), _rand((p, r), 73, torch.bfloat16)
+    ref = oracle.hutchpp_norm(to_f64(A), to_f64(G), to_f64(S), to_f64(P))
+    n = torch.full((B,), 5.0, device=DEV)
+    rnc.dprc_norm_hutchpp(A.to(DEV), G.to(DEV), S.to(DEV), P.to(DEV), n)
+    assert _relerr(n.cpu(), ref) < RTOL
+    rnc.dprc_norm_hutchpp(A.to(DEV), G.to(DEV), S.to(DEV), P.to(DEV), n, accumulate=True)
+    assert _relerr(n.cpu(), 2.0 * ref) < RTOL
 
 
 def test_hutchpp_exact_on_low_rank_gradients():
