@@ -27,7 +27,8 @@
 // eight of them keep 144 to 192 KB per SM in flight.  The accumulator is
 // double buffered.  The epilogue (one TMEM lane, i.e. one row of the tile, per
 // thread) squares and sums the row, or first multiplies it by P (staged in
-// shared memory in bf16), and writes one partial per tile; the CTA that
+// shared memory in bf16; for p <= 16 on the tensor cores, the rows of X as
+// bf16 hi/lo against P), and writes one partial per tile; the CTA that
 // completes a sample's last tile (a per-sample ticket) adds the sample's
 // partials in tile order: one launch, deterministic.
 
@@ -245,6 +246,37 @@ __device__ __forceinline__ void stage_p_tile(const Args& a, int p0, int rows, TP
   }
 }
 
+// p narrow (<= 16), kp = 16, 32 or 64: the rows of X_i P come from the tensor
+// cores.  Each epilogue thread writes its row of X as bf16 hi and lo into two
+// A tiles (128 rows x 16, K-major, 32-byte swizzle: 16-byte chunk c of row r
+// at c ^ ((r >> 2) & 1)); P sits once per CTA in a B tile (16 rows x kp,
+// MN-major, 2 kp-byte swizzle); one thread issues X_hi P and X_lo P into
+// kp TMEM columns after the accumulators, and every thread squares its row of
+// the product.
+__host__ __device__ __forceinline__ bool rows_mma_fits(int N, int kp) {
+  return N == 16 && (kp == 16 || kp == 32 || kp == 64);
+}
+constexpr int kNwRowsExtra = 1024 + 2048 + 2 * 4096;  // alignment, B tile, A tiles hi/lo
+constexpr int kNwResCol = 32;                         // first TMEM column of X P
+
+// chunk of a 16-byte chunk c in row r of a tile of `bytes`-wide swizzled rows
+__device__ __forceinline__ int swz_chunk(int c, int r, int bytes) {
+  return bytes == 128 ? (c ^ (r & 7)) : (bytes == 64 ? (c ^ ((r >> 1) & 3)) : (c ^ ((r >> 2) & 1)));
+}
+
+template <int KP>
+__device__ __forceinline__ float rows_mma_square(uint32_t taddr) {
+  float y[KP];
+  tmem_ld_cols<KP>(taddr, y);
+  float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+  for (int c = 0; c < KP; c += 2) {
+    s0 = fmaf(y[c], y[c], s0);
+    s1 = fmaf(y[c + 1], y[c + 1], s1);
+  }
+  return s0 + s1;
+}
+
 template <int N, int MODE, typename TP>
 __global__ void __launch_bounds__(192, 1)
     tc_narrow_kernel(const __grid_constant__ CUtensorMap map_w,
@@ -253,6 +285,7 @@ __global__ void __launch_bounds__(192, 1)
   extern __shared__ uint8_t smem_raw[];
   __shared__ float s_red[4];
   __shared__ int s_last;
+  __shared__ int s_live[4];
 
   uint8_t* ring = align_1024(smem_raw);
   TP* Ps = reinterpret_cast<TP*>(ring + kNwStages * Cfg::kStage + Cfg::kCtrl);
@@ -263,6 +296,11 @@ __global__ void __launch_bounds__(192, 1)
   uint64_t* drain = acce + 2;          // MMA thread: all its MMAs complete
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(acce + 3);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  uint64_t* pbar = acce + 4;           // the epilogue's X P products complete
+  uint64_t* edrain = acce + 5;         // the epilogue's issuer: all its MMAs complete
+  // the row products on tensor cores (kNwProj, p <= 16): TMEM for them too
+  constexpr int kTmemAlloc = MODE == kNwProj && N == 16 ? 128 : Cfg::kTmemCols;
+  const bool rows_mma = MODE == kNwProj && rows_mma_fits(N, a.kp);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nu = (a.T + kNwK - 1) / kNwK;  // stages per tile
@@ -292,6 +330,8 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(&acce[b], 4);
     }
     mbar_init(drain, 1);
+    mbar_init(pbar, 1);
+    mbar_init(edrain, 1);
     fence_mbar_init();
     *abort_flag = 0;
     const int i0 = static_cast<int>(blockIdx.x / a.mt);
@@ -303,7 +343,7 @@ __global__ void __launch_bounds__(192, 1)
     tma_prefetch_desc(&map_n);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, Cfg::kTmemCols);
+    tmem_alloc(tmem_slot, kTmemAlloc);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -410,6 +450,25 @@ __global__ void __launch_bounds__(192, 1)
       }
       named_bar_sync(1, 128);
     }
+    // the row products' tiles (rows_mma): B = P as 16 swizzled rows of kp,
+    // then the A tiles of X hi and lo
+    uint8_t* mbase = align_1024(reinterpret_cast<uint8_t*>(Ps) + 2048);
+    uint8_t* PB = mbase;
+    uint8_t* XAh = mbase + 2048;
+    uint8_t* XAl = mbase + 2048 + 4096;
+    if (rows_mma) {
+      const int wb = 2 * a.kp, cpr = wb / 16;
+      for (int e = et; e < 16 * cpr; e += 128) {
+        const int b = e / cpr, c = e - b * cpr;
+        uint4 v4 = make_uint4(0u, 0u, 0u, 0u);
+        if (b < a.narrow) v4 = *reinterpret_cast<const uint4*>(Ps + b * a.kp + 8 * c);
+        *reinterpret_cast<uint4*>(PB + b * wb + 16 * swz_chunk(c, b, wb)) = v4;
+      }
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      named_bar_sync(1, 128);
+    }
+    uint32_t pphase = 0;    // parity of the next product batch
+    bool e_issued = false;  // thread et 0 issued products (drained before exit)
     bool ok = true;
     for (long long j = 0; j < my_tiles; ++j) {
       const long long tile = blockIdx.x + j * gridDim.x;
@@ -504,7 +563,62 @@ __global__ void __launch_bounds__(192, 1)
         named_bar_sync(1, 128);  // Xs and Pt are rewritten by the next tile
       } else {
       float sq = 0.f;
-      if (live) {
+      if (MODE == kNwProj && rows_mma) {
+        // X row -> bf16 hi/lo A rows; every epilogue thread takes part in the
+        // barriers, and the products are issued only if every warp is live
+        const int row = q * 32 + lane;
+        if (live) {
+          uint32_t hw[8], lw[8];
+#pragma unroll
+          for (int t2 = 0; t2 < 8; ++t2) {
+            __nv_bfloat16 h0, l0, h1, l1;
+            split_hilo(v[2 * t2], h0, l0);
+            split_hilo(v[2 * t2 + 1], h1, l1);
+            const __nv_bfloat162 hh = __halves2bfloat162(h0, h1);
+            const __nv_bfloat162 ll = __halves2bfloat162(l0, l1);
+            hw[t2] = *reinterpret_cast<const uint32_t*>(&hh);
+            lw[t2] = *reinterpret_cast<const uint32_t*>(&ll);
+          }
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            const int pc = swz_chunk(c, row, 32);
+            *reinterpret_cast<uint4*>(XAh + row * 32 + 16 * pc) =
+                make_uint4(hw[4 * c], hw[4 * c + 1], hw[4 * c + 2], hw[4 * c + 3]);
+            *reinterpret_cast<uint4*>(XAl + row * 32 + 16 * pc) =
+                make_uint4(lw[4 * c], lw[4 * c + 1], lw[4 * c + 2], lw[4 * c + 3]);
+          }
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        if (lane == 0) s_live[ew] = live ? 1 : 0;
+        named_bar_sync(1, 128);
+        const bool go = s_live[0] && s_live[1] && s_live[2] && s_live[3];
+        if (go) {
+          if (et == 0) {
+            tc_fence_after();
+            const uint32_t idesc = make_idesc_bf16(128, a.kp, false, true);
+            const uint64_t bd =
+                make_sdesc(smem_u32(PB), 16, 16 * a.kp, swz_code_for_bytes(2 * a.kp));
+            umma_bf16(tmem + kNwResCol, make_sdesc(smem_u32(XAh), 16, 256, kSwz32), bd, idesc, 0u);
+            umma_bf16(tmem + kNwResCol, make_sdesc(smem_u32(XAl), 16, 256, kSwz32), bd, idesc, 1u);
+            umma_commit(pbar);
+            e_issued = true;
+          }
+          bool done = mbar_wait(pbar, pphase, DPRC_DEVERR_ACCUM);
+          pphase ^= 1u;
+          done = __all_sync(0xffffffffu, done);
+          tc_fence_after();
+          if (done) {
+            const uint32_t tr = tmem + (static_cast<uint32_t>(q * 32) << 16) + kNwResCol;
+            sq = a.kp == 16 ? rows_mma_square<16>(tr)
+                            : (a.kp == 32 ? rows_mma_square<32>(tr) : rows_mma_square<64>(tr));
+            sq *= a.scale;
+          } else {
+            ok = false;
+          }
+        }
+        tc_fence_before();
+        named_bar_sync(1, 128);  // the A tiles and the product columns are reused next tile
+      } else if (live) {
         if (MODE == kNwNorm) {
           float s0 = 0.f, s1 = 0.f;
 #pragma unroll
@@ -615,6 +729,9 @@ __global__ void __launch_bounds__(192, 1)
         named_bar_sync(1, 128);
       }
     }
+    // the products this thread issued are complete before the TMEM is freed
+    // (after a failed wait above they may still run)
+    if (e_issued) umma_drain(edrain, kWaitLimitNs);
   }
 
   __syncwarp();  // reconverge each warp before the CTA barrier
@@ -622,7 +739,7 @@ __global__ void __launch_bounds__(192, 1)
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, Cfg::kTmemCols);
+    tmem_dealloc(tmem, kTmemAlloc);
   }
 }
 
@@ -754,7 +871,10 @@ cudaError_t launch_narrow_hutch(const void* A, const void* G, const void* P, int
   }
   if (p <= 64) {
     a.partials = partials;
-    const int proj_bytes = static_cast<int>(p * a.kp * 2);
+    int proj_bytes = static_cast<int>(p * a.kp * 2);
+    // P's rows for the CUDA-core product, or (p <= 16) room for the tensor
+    // cores' tiles after them
+    if (rows_mma_fits(N, a.kp)) proj_bytes = (proj_bytes > 2048 ? proj_bytes : 2048) + kNwRowsExtra;
     return launch_mode<kNwProj, __nv_bfloat16>(N, mw, mn, a, proj_bytes, s);
   }
   // d narrow: per-tile parts of X_i P (scratch: narrow_hutch_scratch_bytes)

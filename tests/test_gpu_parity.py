@@ -156,6 +156,8 @@ def test_norm_hutch_layers_clip_equals_layers_then_clip(shapes, B, T, k):
 # ||X_i P||^2 from the rows of X_i when p <= 64, from per-tile parts of X_i P
 # when d <= 32 < p and k <= 128 (other d-narrow maps take the sketch path).  Both widths narrow, narrow widths padded to 16, 32 and 64
 # columns, ragged T, k from 8 to 256 (P up to 64 x 256 in shared memory).
+# With p <= 16 and k rounded up to 16, 32 or 64, the rows of X_i P come from
+# the tensor cores (X as bf16 hi/lo against P).
 NARROW_SHAPES = [
     (3, 1000, 2048, 16, 32),   # adapter down map: p narrow
     (3, 1000, 16, 2048, 32),   # adapter up map: d narrow, G is the wide operand
@@ -169,6 +171,8 @@ NARROW_SHAPES = [
     (3, 200, 8, 4096, 24),     # d narrow, k not a multiple of 16
     (20, 64, 2048, 16, 32),    # 320 tiles: several per CTA (double-buffered accumulator)
     (20, 64, 16, 2048, 32),    # the same, d narrow (P tile restaged per tile)
+    (2, 300, 256, 8, 64),      # p <= 16, kp = 64: rows of X P on the tensor cores
+    (2, 300, 512, 16, 40),     # p <= 16, kp = 48: rows of X P on CUDA cores
 ]
 
 
