@@ -316,6 +316,11 @@ __global__ void __launch_bounds__(192, 1)
       tma_load_3d(st + h * kNwBox, &map_w, &full[s], m * kNwM + h * 64, u * kNwK, i);
     tma_load_3d(st + kNwWide, &map_n, &full[s], 0, u * kNwK, i);
   };
+  // The launch is a programmatic dependent of the previous kernel in the
+  // stream: the next launch may set up now, and this one's threads wait for
+  // the previous grid's completion before they touch global memory (thread 0
+  // before its first loads, the epilogue before P and its outputs).
+  pdl_launch_dependents();
   // the producer (thread 0) issues the first stages of its first tile right
   // after initialising the barriers: their DRAM round trip overlaps the TMEM
   // allocation and the CTA barrier
@@ -336,6 +341,7 @@ __global__ void __launch_bounds__(192, 1)
     *abort_flag = 0;
     const int i0 = static_cast<int>(blockIdx.x / a.mt);
     const int m0 = static_cast<int>(blockIdx.x - static_cast<long long>(i0) * a.mt);
+    pdl_wait();
     for (int u = 0; u < pre; ++u) load_stage(i0, m0, u, u);
   }
   if (warp == 0 && lane == 0) {
@@ -424,6 +430,7 @@ __global__ void __launch_bounds__(192, 1)
     const int ew = warp - 2;
     const int q = warp & 3;  // TMEM lane quadrant this warp may read
     const int et = threadIdx.x - 64;
+    pdl_wait();
     if (MODE == kNwProj) {
       // P (or the +-1 signs) into shared memory, once
       // rows of kp = k rounded up to 16 columns, zeros past k
@@ -759,8 +766,17 @@ cudaError_t launch_n(const CUtensorMap& mw, const CUtensorMap& mn, const NwArgs&
     if (dev >= 0 && dev < kMaxDev) done[dev].store(smem, std::memory_order_release);
   }
   const long long grid = a.ntiles < device_sm_count() ? a.ntiles : device_sm_count();
-  kern<<<static_cast<unsigned>(grid), 192, smem, s>>>(mw, mn, a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(192);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, mw, mn, a);
 }
 
 template <int MODE, typename TP>
