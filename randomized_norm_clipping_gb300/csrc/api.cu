@@ -903,37 +903,50 @@ dprc_status dprc_norm_hutchpp(const void* A, const void* G, const void* S, const
       float* YP = reinterpret_cast<float*>(w + t.yp_off);
       float* RC = reinterpret_cast<float*>(w + t.rc_off);
       void* MH = QP;  // M as bf16 hi/lo [B][p][2r], the third pass's sketch operand
+      // Each projection streams a sample as soon as the sample's sketch is
+      // written (per-sample counts, rows 1, 2 and 0 of the block of counts for
+      // passes 1, 2 and 3) instead of after the sketch kernel's end; only its
+      // epilogue waits for that end.  The third pass's last blocks zero all three.
+      int* ready = pdl ? reinterpret_cast<int*>(w + t.ready_off) : nullptr;
+      int* ready1 = ready ? ready + B : nullptr;
+      int* ready2 = ready ? ready + 2 * B : nullptr;
+      const int ready_target = static_cast<int>((T + 127) / 128);
       mark(0, s);
       cudaError_t e = launch_pack_cols(S, P, SP, p, ir, s);
       // pass 1: [Z | X P] = A^T (G [S | P]); Z as hi/lo for pass 2, X P in fp32
+      const BlockSched rs1 = rowproj_sched(B, T, p, 2 * ir);
       if (e == cudaSuccess)
-        e = launch_tc_rowproj(G, B, T, p, SP, false, 2 * ir, false, W, t.tpad,
-                              rowproj_sched(B, T, p, 2 * ir), stick, B, s);
+        e = launch_tc_rowproj(G, B, T, p, SP, false, 2 * ir, false, W, t.tpad, rs1, stick, B, s,
+                              false, ready1);
       if (e == cudaSuccess)
         e = launch_tc_colproj(A, B, T, d, W, t.tpad, 2 * ir, colproj_sched(B, T, d, 4 * ir),
                               stick, cnorm, kColprojSplit, nullptr, 0, ir, 1.0f, YP, Z, pdl, s,
-                              ir);
+                              ir, nullptr, nullptr, ready1, ready_target * rs1.cl);
       mark(1, s);
       // pass 2: M = G^T (A Z) = O S, fp32 for the QR and hi/lo for pass 3
+      const BlockSched rs2 = rowproj_sched(B, T, d, 2 * ir);
       if (e == cudaSuccess)
-        e = launch_tc_rowproj(A, B, T, d, Z, true, 2 * ir, true, W, t.tpad,
-                              rowproj_sched(B, T, d, 2 * ir), stick, B, s);
+        e = launch_tc_rowproj(A, B, T, d, Z, true, 2 * ir, true, W, t.tpad, rs2, stick, B, s,
+                              false, ready2);
       if (e == cudaSuccess)
         e = launch_tc_colproj(G, B, T, p, W, t.tpad, ir, colproj_sched(B, T, p, 2 * ir), stick,
-                              cnorm, kColprojF32Hilo, nullptr, 0, ir, 1.0f, M, MH, pdl, s);
+                              cnorm, kColprojF32Hilo, nullptr, 0, ir, 1.0f, M, MH, pdl, s, 0,
+                              nullptr, nullptr, ready2, ready_target * rs2.cl);
       mark(2, s);
       // the QR's factors (R, column scales, C = Q^T P) ...
       if (e == cudaSuccess) e = launch_qr_cluster(M, B, p, P, dtype, nullptr, true, s, RC);
       mark(3, s);
       // ... while pass 3 streams X M = A^T (G M); its epilogue forms
       // n (+)= ||X Q||^2 + ||X P'||^2 / r row by row from X M, X P and them
+      // (the sketch kernel's end waits for the QR)
+      const BlockSched rs3 = rowproj_sched(B, T, p, 2 * ir);
       if (e == cudaSuccess)
-        e = launch_tc_rowproj(G, B, T, p, MH, true, 2 * ir, true, W, t.tpad,
-                              rowproj_sched(B, T, p, 2 * ir), stick, B, s, pdl);
+        e = launch_tc_rowproj(G, B, T, p, MH, true, 2 * ir, true, W, t.tpad, rs3, stick, B, s,
+                              pdl, ready);
       if (e == cudaSuccess)
         e = launch_tc_colproj(A, B, T, d, W, t.tpad, ir, colproj_sched(B, T, d, 2 * ir), stick,
                               cnorm, kColprojHpp, n, accumulate, ir, 1.0f, nullptr, nullptr, pdl,
-                              s, 0, RC, YP);
+                              s, 0, RC, YP, ready, ready_target * rs3.cl, 3);
       mark(4, s);
       return cuda_status(e);
     }

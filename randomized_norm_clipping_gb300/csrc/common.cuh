@@ -139,6 +139,40 @@ __device__ __forceinline__ bool mbar_wait_lim(uint64_t* bar, uint32_t parity, in
 }
 
 // ---------------------------------------------------------------------------
+// Counters in global memory written by other CTAs (a release add after the
+// data it announces) and waited on with acquire loads.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int ld_acquire(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Bounded wait until *p >= target (acquire); false on timeout (error
+// recorded) or once the CTA's abort flag is set (nothing recorded).
+__device__ __forceinline__ bool wait_geq(const int* p, int target, unsigned long long limit_ns,
+                                         const volatile int* abort) {
+  if (ld_acquire(p) >= target) return true;
+  const unsigned long long t0 = globaltimer_ns();
+  unsigned ns = 64;
+  while (true) {
+    __nanosleep(ns);
+    if (ld_acquire(p) >= target) return true;
+    if (*abort != 0) return false;
+    if (globaltimer_ns() - t0 > limit_ns) {
+      record_error(DPRC_DEVERR_READY);
+      return false;
+    }
+    if (ns < 512) ns *= 2;
+  }
+}
+
+
+// ---------------------------------------------------------------------------
 // Thread-block clusters: ranks, distributed shared memory, remote arrivals.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t cluster_ctarank() {
@@ -162,6 +196,16 @@ __device__ __forceinline__ uint32_t cluster_nctarank() {
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
                ::: "memory");
+}
+
+// The two halves of cluster_sync_all, for a thread that has work to do
+// before it needs its peers to have arrived (every thread of the cluster
+// arrives once, then waits once, before it arrives again).
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 // Address of the same shared-memory object in the CTA of rank `rank`.

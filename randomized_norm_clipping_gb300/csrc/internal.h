@@ -136,10 +136,14 @@ bool make_tmap_3d_bf16(CUtensorMap* map, const void* base, uint64_t dim0, uint64
 // previous kernel in the stream (which must let it start early) still runs;
 // X and R must not be written by that kernel.  CTA 0 waits for it before
 // exiting, so this kernel completes after it.
+// ready (may be null): int32 [B], zero on entry; every CTA adds one to
+// ready[i] after each of its blocks of sample i is in memory (release), so a
+// sample's count reaches ceil(T / 128) * bs.cl.
 cudaError_t launch_tc_rowproj(const void* X, int64_t B, int64_t T, int64_t c, const void* R,
                               bool r_batched, int nmma, bool hilo_in, void* W, int64_t tpad,
                               const BlockSched& bs, int* zero_ptr, size_t zero_ints,
-                              cudaStream_t s, bool beside_previous = false);
+                              cudaStream_t s, bool beside_previous = false,
+                              int* ready = nullptr);
 
 // kColprojSplit: the first n_split = n / 2 columns of Y as bf16 hi/lo
 // [B][c][n], the rest fp32 [B][c][n / 2]; kColprojF32Hilo: Y both ways;
@@ -166,12 +170,20 @@ constexpr float kHppDropTau = 1e-3f;
 // n_out (per-block squares in chunk_norms, combined in block order by the
 // last block of each sample, found with sample_tickets, which must be zero);
 // kColprojF32 writes Y [B][c][n]; kColprojHilo writes Y as bf16 hi/lo [B][c][2n].
+// ready (may be null): the counts of a launch_tc_rowproj with the same
+// `ready` just before this one in the stream (pdl set): the loads of sample
+// i's sketch wait for ready[i] >= ready_target instead of that kernel's end,
+// so a sample's projection starts as soon as its sketch is written.  With
+// ready_rows > 0 (kColprojNorm and kColprojHpp only) the sample's last block
+// sets ready[r * B + i] back to zero for r < ready_rows, once every block is
+// past its wait; counts of earlier launches may share that block of rows.
 cudaError_t launch_tc_colproj(const void* X, int64_t B, int64_t T, int64_t c, const void* W,
                               int64_t tpad, int n, const BlockSched& bs, int* sample_tickets,
                               float* chunk_norms, ColprojMode mode, float* n_out, int accumulate,
                               int n_head, float w_tail, float* y_f32, void* y_hilo, bool pdl,
                               cudaStream_t s, int n_split = 0, const float* hpp_rc = nullptr,
-                              const float* hpp_yp = nullptr);
+                              const float* hpp_yp = nullptr, int* ready = nullptr,
+                              int ready_target = 0, int ready_rows = 0);
 
 // SIMT (fp32 CUDA-core) building blocks; Xdt is the dtype of X, Rdt of R.
 cudaError_t launch_simt_rowproj(const void* X, dprc_dtype xdt, int64_t B, int64_t T, int64_t c,

@@ -154,7 +154,7 @@ __global__ void __launch_bounds__(kCt, 1)
   __shared__ float Cm[kR * kR];
   __shared__ float Rsm[kR][kR];  // R of the scaled M
   __shared__ float scm[kR];      // column scales
-  extern __shared__ float stage[];  // Q rows then P rows: [kCt * RPT][17] each
+  __shared__ float cpart[kCw][kE];  // per-warp parts of this CTA's part of C
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   // Each sample's rows are spread over one cluster of kCl CTAs; a launch of
@@ -383,55 +383,56 @@ __global__ void __launch_bounds__(kCt, 1)
   }
   __syncthreads();
 
-  // Q rows = [I; 0] rows - V rows K, staged with the P rows for C = Q^T P
-  float* Qs = stage;
-  float* Ps = stage + kCt * RPT * 17;
+  // this thread's rows of P; its rows of Q = [I; 0] - V K are formed from V
+  // and K when needed (entry a of row `row`: [row == a] - sum over the
+  // reflectors b <= row of v_b K[b][a])
+  float pk[RPT][kR];
 #pragma unroll
   for (int k = 0; k < RPT; ++k) {
     const int row = row_of(k);
-    float q[kR];
 #pragma unroll
-    for (int l = 0; l < kR; ++l) q[l] = row == l ? 1.f : 0.f;
+    for (int l = 0; l < kR; ++l)
+      pk[k][l] = row < p ? ld_elem(P + static_cast<size_t>(row) * kR + l) : 0.f;
+  }
+  auto q_entry = [&](int k, int a) {
+    const int row = row_of(k);
+    float q = row == a ? 1.f : 0.f;
 #pragma unroll
-    for (int a = 0; a < kR; ++a) {
-      const float va = (row < p && row >= a) ? v[k][a] : 0.f;
-#pragma unroll
-      for (int l = 0; l < kR; ++l) q[l] = fmaf(-va, Km[a][l], q[l]);
+    for (int b = 0; b < kR; ++b) {
+      const float vb = (row < p && row >= b) ? v[k][b] : 0.f;
+      q = fmaf(-vb, Km[b][a], q);
     }
-    const int loc = k * kCt + tid;
+    return row < p ? q : 0.f;
+  };
+
+  // this CTA's part of C = Q^T P: for each row a of C the warp reduce-scatters
+  // its rows' products q_a p_l (lanes 2c, 2c+1 then hold the warp's total of
+  // one column), and the warps' totals are added in warp order
+#pragma unroll 1
+  for (int a = 0; a < kR; ++a) {
+    float qa[RPT];
+#pragma unroll
+    for (int k = 0; k < RPT; ++k) qa[k] = q_entry(k, a);
+    float c[kR];
 #pragma unroll
     for (int l = 0; l < kR; ++l) {
-      Qs[loc * 17 + l] = row < p ? q[l] : 0.f;
-      Ps[loc * 17 + l] = row < p ? ld_elem(P + static_cast<size_t>(row) * kR + l) : 0.f;
+      c[l] = 0.f;
+#pragma unroll
+      for (int k = 0; k < RPT; ++k) c[l] = fmaf(qa[k], pk[k][l], c[l]);
     }
+    int idx;
+    const float w = warp_scatter16<false>(c, lane, idx);
+    if ((lane & 1) == 0) cpart[warp][a * kR + idx] = w;
   }
   __syncthreads();
-
-  // this CTA's part of C = Q^T P: warp w owns rows kCrows w .. of C
-  if (warp * kCrows < kR) {
-    float c[kCrows][kR];
 #pragma unroll
-    for (int x2 = 0; x2 < kCrows; ++x2)
+  for (int m = 0; m < kEpt; ++m)
+    if (tid + kCt * m < kE) {
+      float t = 0.f;
 #pragma unroll
-      for (int l = 0; l < kR; ++l) c[x2][l] = 0.f;
-    for (int loc = lane; loc < kCt * RPT; loc += 32) {
-      float qa[kCrows];
-#pragma unroll
-      for (int x2 = 0; x2 < kCrows; ++x2) qa[x2] = Qs[loc * 17 + kCrows * warp + x2];
-#pragma unroll
-      for (int l = 0; l < kR; ++l) {
-        const float pl = Ps[loc * 17 + l];
-#pragma unroll
-        for (int x2 = 0; x2 < kCrows; ++x2) c[x2][l] = fmaf(qa[x2], pl, c[x2][l]);
-      }
+      for (int w2 = 0; w2 < kCw; ++w2) t += cpart[w2][tid + kCt * m];
+      Cm[tid + kCt * m] = t;
     }
-#pragma unroll
-    for (int x2 = 0; x2 < kCrows; ++x2) {
-      int idx;
-      const float w = warp_scatter16<false>(c[x2], lane, idx);
-      if ((lane & 1) == 0) Cm[(kCrows * warp + x2) * kR + idx] = w;
-    }
-  }
   __syncthreads();
   // round 17: all-gather the 256 partials; every thread sums its entries
 #pragma unroll
@@ -470,12 +471,11 @@ __global__ void __launch_bounds__(kCt, 1)
   for (int k = 0; k < RPT; ++k) {
     const int row = row_of(k);
     if (row >= p || out == nullptr) continue;
-    const int loc = k * kCt + tid;
     float q[kR], pp[kR];
 #pragma unroll
     for (int l = 0; l < kR; ++l) {
-      q[l] = Qs[loc * 17 + l];
-      pp[l] = Ps[loc * 17 + l];
+      q[l] = q_entry(k, l);
+      pp[l] = pk[k][l];
     }
 #pragma unroll
     for (int a = 0; a < kR; ++a)
@@ -519,17 +519,15 @@ template <int RPT, typename TP>
 cudaError_t launch_rpt(const float* M, int64_t B, int64_t p, const void* P, void* out, bool hilo,
                        float* rc, cudaStream_t s) {
   auto kern = qr_cluster_kernel<RPT, TP>;
-  const int smem = 2 * kCt * RPT * 17 * 4;
   constexpr int kMaxDev = 64;
   static std::atomic<int> done[kMaxDev];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDev || !done[dev].load(std::memory_order_acquire)) {
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    // an SM that takes a QR CTA keeps its largest shared-memory carve-out, so
-    // two sketch CTAs of the pass that runs beside the QR fit next to it
+    // an SM that takes a QR CTA (about 31 KB of shared memory) keeps its
+    // largest shared-memory carve-out, so two CTAs of the sketch or the
+    // projection of the pass that runs beside the QR fit next to it
     e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
                              cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
@@ -542,7 +540,7 @@ cudaError_t launch_rpt(const float* M, int64_t B, int64_t p, const void* P, void
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(B * kCl));
   cfg.blockDim = dim3(kCt);
-  cfg.dynamicSmemBytes = smem;
+  cfg.dynamicSmemBytes = 0;
   cfg.stream = s;
   cudaLaunchAttribute attr;
   attr.id = cudaLaunchAttributeClusterDimension;

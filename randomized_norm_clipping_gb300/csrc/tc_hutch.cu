@@ -139,35 +139,6 @@ __device__ __forceinline__ long long count_blocks(const Phase& ph, const Mine& m
   return ph.nblocks > m.first ? (ph.nblocks - 1 - m.first) / m.step + 1 : 0;
 }
 
-__device__ __forceinline__ int ld_acquire(const int* p) {
-  int v;
-  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ void fence_proxy_async_global() {
-  asm volatile("fence.proxy.async.global;" ::: "memory");
-}
-
-// Bounded wait until *p >= target (acquire); false on timeout (error
-// recorded) or once the CTA's abort flag is set (nothing recorded).
-__device__ __forceinline__ bool wait_geq(const int* p, int target, unsigned long long limit_ns,
-                                         const volatile int* abort) {
-  if (ld_acquire(p) >= target) return true;
-  const unsigned long long t0 = globaltimer_ns();
-  unsigned ns = 64;
-  while (true) {
-    __nanosleep(ns);
-    if (ld_acquire(p) >= target) return true;
-    if (*abort != 0) return false;
-    if (globaltimer_ns() - t0 > limit_ns) {
-      record_error(DPRC_DEVERR_READY);
-      return false;
-    }
-    if (ns < 512) ns *= 2;
-  }
-}
-
 // Cluster exchange state of one CTA.
 struct Xchg {
   float* recv;          // [cl-1][128/cl][K] rows sent to this rank

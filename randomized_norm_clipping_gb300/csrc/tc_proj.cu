@@ -179,6 +179,10 @@ struct RowArgs {
   // before it exits, so this kernel's completion implies the other's (the
   // other CTAs leave as they finish and free their slots)
   int wait_end;
+  // if set, ready[i] counts the blocks of sample i whose sketch rows are in
+  // memory: after a block's rows, one add with release (the column projection
+  // launched after this kernel waits on it instead of this kernel's end)
+  int* ready;
 };
 
 template <int NMMA, bool HILO_IN>
@@ -383,6 +387,14 @@ __global__ void __launch_bounds__(192, 2)
       if (mine && ok && t < a.T && DPRC_IN(b < sc.nblocks && t < a.tpad))
         write_sketch_row<NMMA, HILO_IN>(a.W + static_cast<size_t>(i) * 2 * kN * a.tpad + t,
                                         a.tpad, y);
+      if (a.ready != nullptr) {
+        fence_proxy_async_global();  // the rows are read by TMA (async proxy)
+        named_bar_sync(1, 128);
+        if (ew == 0 && lane == 0 && ok && DPRC_IN(b < sc.nblocks)) {
+          __threadfence();
+          atomicAdd(&a.ready[i], 1);
+        }
+      }
     }
     (void)ew;
   }
@@ -424,6 +436,15 @@ struct ColArgs {
   const float* hpp_rc;
   const float* hpp_yp;
   int hpp_rcs;
+  // if set, the producer waits for ready[i] >= ready_target (the sketch
+  // kernel's per-sample count) instead of the sketch kernel's end; the
+  // epilogue still waits for the end before anything it reads or writes.  In
+  // the modes with tickets the sample's last block then sets
+  // ready[r * ready_stride + i] = 0 for r < ready_rows.
+  int* ready;
+  int ready_target;
+  int ready_rows;
+  int ready_stride;
 };
 
 // Hutch++ head and tail of one row of d from Y_M = X M (y) and Y_P = X P
@@ -509,6 +530,10 @@ struct ColCfg {
   static constexpr int kStageBytes = kXBytes + kWBytes;
   static constexpr int kStages = NMMA >= 128 ? 3 : 2;
   static constexpr int kCtasPerSm = NMMA >= 128 ? 1 : 2;
+  // registers per thread: at most what kCtasPerSm CTAs leave of the SM's
+  // 64 K, and for NMMA = 32 (the Hutch++ passes beside the QR) few enough
+  // that two CTAs fit next to a QR CTA (256 threads x 96 registers)
+  static constexpr int kMaxRegs = NMMA >= 128 ? 255 : (NMMA == 64 ? 168 : 104);
   static constexpr int kN = NMMA / 2;
   static constexpr int kAcc = NMMA;
   static constexpr int kTmemCols = 2 * kAcc;
@@ -518,7 +543,7 @@ struct ColCfg {
 };
 
 template <int NMMA>
-__global__ void __launch_bounds__(192, ColCfg<NMMA>::kCtasPerSm)
+__global__ void __launch_bounds__(192) __maxnreg__(ColCfg<NMMA>::kMaxRegs)
     tc_colproj_kernel(const __grid_constant__ CUtensorMap map_x,
                       const __grid_constant__ CUtensorMap map_w, const ColArgs a) {
   using Cfg = ColCfg<NMMA>;
@@ -592,7 +617,9 @@ __global__ void __launch_bounds__(192, ColCfg<NMMA>::kCtasPerSm)
   }
   tc_fence_before();
   __syncthreads();
-  if (sc.cl > 1) cluster_sync_all();  // peers' barriers exist before any remote arrive
+  // the peers' barriers must exist before this CTA's first remote arrive,
+  // which comes only in the epilogue: arrive now, wait there
+  if (sc.cl > 1) cluster_arrive();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
@@ -606,8 +633,27 @@ __global__ void __launch_bounds__(192, ColCfg<NMMA>::kCtasPerSm)
           tma_load_3d(sw + s * Cfg::kWBytes + h * Cfg::kWBoxBytes, &map_w, &full[s],
                       kt * kTileT + h * 64, 0, i);
       };
-      pdl_wait();  // the sketch is written by the previous kernel
-      for (int it = 0; it < pre; ++it) load_w(it, it);
+      // the sketch is written by the previous kernel: wait for its end, or
+      // for each sample's count before the sample's first W tile
+      int ready_i = -1;
+      bool ready_ok = true;
+      auto await_w = [&](int i) {
+        if (a.ready == nullptr || i == ready_i || !ready_ok) return;
+        if (wait_geq(&a.ready[i], a.ready_target, kWaitLimitNs, abort_flag)) {
+          fence_proxy_async_global();
+        } else {
+          ready_ok = false;  // W is still loaded so the issued stages complete; results are void
+          *abort_flag = 1;
+        }
+        ready_i = i;
+      };
+      if (a.ready == nullptr) pdl_wait();
+      for (int it = 0; it < pre; ++it) {
+        int i, ch, kt;
+        unit(it, i, ch, kt);
+        await_w(i);
+        load_w(it, it);
+      }
       long long issued = pre;
       // the unit of stage `it` by an incremental cursor (one division per
       // block, none per stage: this thread paces the pipeline)
@@ -626,6 +672,7 @@ __global__ void __launch_bounds__(192, ColCfg<NMMA>::kCtasPerSm)
         for (int h = 0; h < 2; ++h)
           tma_load_3d(sx + s * Cfg::kXBytes + h * Cfg::kXBoxBytes, &map_x, &full[s],
                       cch * kColChunk + h * 64, ckt * kTileT, ci);
+        await_w(ci);
 #pragma unroll
         for (int h = 0; h < 2; ++h)
           tma_load_3d(sw + s * Cfg::kWBytes + h * Cfg::kWBoxBytes, &map_w, &full[s],
@@ -687,6 +734,7 @@ __global__ void __launch_bounds__(192, ColCfg<NMMA>::kCtasPerSm)
   } else {
     // ---------------- epilogue warps 2..5 ----------------
     pdl_wait();  // the sample tickets are cleared by the previous kernel
+    if (sc.cl > 1) cluster_wait();
     const int ew = warp - 2;
     const int q = warp & 3;
     const int row = q * 32 + lane;  // row of the 128-row chunk = TMEM lane
@@ -789,6 +837,10 @@ __global__ void __launch_bounds__(192, ColCfg<NMMA>::kCtasPerSm)
               if (lane == 0) {
                 a.n_out[i] = (a.accumulate ? a.n_out[i] : 0.f) + sum;
                 a.sample_tickets[i] = 0;
+                // every block of the sample is past its wait on the count
+                // (and those of earlier launches that share the block of counts)
+                if (a.ready != nullptr)
+                  for (int r = 0; r < a.ready_rows; ++r) a.ready[r * a.ready_stride + i] = 0;
               }
             }
           }
@@ -822,6 +874,7 @@ __global__ void __launch_bounds__(192, ColCfg<NMMA>::kCtasPerSm)
   }
 
   __syncwarp();  // reconverge each warp before the CTA barrier
+  if (sc.cl > 1 && warp < 2) cluster_wait();  // the epilogue waited before its first remote access
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -900,7 +953,7 @@ cudaError_t read_device_error_proj(int32_t* out, bool reset) {
 cudaError_t launch_tc_rowproj(const void* X, int64_t B, int64_t T, int64_t c, const void* R,
                               bool r_batched, int nmma, bool hilo_in, void* W, int64_t tpad,
                               const BlockSched& bs, int* zero_ptr, size_t zero_ints,
-                              cudaStream_t s, bool beside_previous) {
+                              cudaStream_t s, bool beside_previous, int* ready) {
   CUtensorMap mx, mr;
   if (!make_tmap_3d_bf16(&mx, X, c, T, B, c, T * c, kTileC, kRowTile, 128))
     return cudaErrorInvalidValue;
@@ -918,6 +971,7 @@ cudaError_t launch_tc_rowproj(const void* X, int64_t B, int64_t T, int64_t c, co
   a.zero_ptr = zero_ptr;
   a.zero_ints = static_cast<int>(zero_ints);
   a.wait_end = beside_previous ? 1 : 0;
+  a.ready = ready;
 #define DPRC_ROW(NM, HL)                                                              \
   if (nmma == NM && hilo_in == HL)                                                    \
     return launch_sched<tc_rowproj_kernel<NM, HL>>(                                   \
@@ -937,8 +991,11 @@ cudaError_t launch_tc_colproj(const void* X, int64_t B, int64_t T, int64_t c, co
                               float* chunk_norms, ColprojMode mode, float* n_out, int accumulate,
                               int n_head, float w_tail, float* y_f32, void* y_hilo, bool pdl,
                               cudaStream_t s, int n_split, const float* hpp_rc,
-                              const float* hpp_yp) {
+                              const float* hpp_yp, int* ready, int ready_target,
+                              int ready_rows) {
   const int nmma = 2 * n;
+  if (ready_rows > 0 && mode != kColprojNorm && mode != kColprojHpp)
+    return cudaErrorInvalidValue;
   if (mode == kColprojSplit && 2 * n_split != n) return cudaErrorInvalidValue;
   if (mode == kColprojHpp && (n != 16 || hpp_rc == nullptr || hpp_yp == nullptr))
     return cudaErrorInvalidValue;
@@ -965,6 +1022,10 @@ cudaError_t launch_tc_colproj(const void* X, int64_t B, int64_t T, int64_t c, co
   a.hpp_rc = hpp_rc;
   a.hpp_yp = hpp_yp;
   a.hpp_rcs = qr_factor_floats();
+  a.ready = ready;
+  a.ready_target = ready_target;
+  a.ready_rows = ready_rows;
+  a.ready_stride = static_cast<int>(B);
 #define DPRC_COL(NM)                                                                        \
   if (nmma == NM)                                                                           \
     return launch_sched<tc_colproj_kernel<NM>>(bs.grid, bs.cl, ColCfg<NM>::smem(bs.cl),     \
