@@ -411,6 +411,33 @@ def test_hutchpp_accumulates():
     assert _relerr(n.cpu(), 2.0 * ref) < RTOL
 
 
+def test_hutchpp_leaves_the_counter_block_zero_for_other_calls():
+    # Hutch++ counts its sketch rows per sample in three rows of the counter
+    # block that the fused Hutchinson kernel also uses (one row per layer);
+    # the third pass zeroes them, so one workspace serves both calls in turn
+    B, T, d, p, r, k = 3, 300, 136, 256, 16, 32
+    A = _rand((B, T, d), 80, torch.bfloat16).to(DEV)
+    G = _rand((B, T, p), 81, torch.bfloat16, 0.1).to(DEV)
+    S, Pp = _rand((p, r), 82, torch.bfloat16).to(DEV), _rand((p, r), 83, torch.bfloat16).to(DEV)
+    P = _rand((p, k), 84, torch.bfloat16).to(DEV)
+    nbytes = max(rnc.dprc_workspace_bytes(rnc.DPRC_OP_HUTCHPP, rnc._dtype_code(A), B, T, d, p, r),
+                 rnc.dprc_workspace_bytes(rnc.DPRC_OP_HUTCH_LAYERS, rnc._dtype_code(A), B, T, d, p,
+                                          k))
+    ws = torch.zeros(nbytes, dtype=torch.uint8, device=DEV)
+    ref_pp = oracle.hutchpp_norm(to_f64(A.cpu()), to_f64(G.cpu()), to_f64(S.cpu()), to_f64(Pp.cpu()))
+    ref_h = oracle.hutch_norm(to_f64(A.cpu()), to_f64(G.cpu()), to_f64(P.cpu()))
+    for _ in range(2):
+        n = torch.zeros(B, device=DEV)
+        rnc.dprc_norm_hutchpp(A, G, S, Pp, n, ws=ws)
+        assert _relerr(n.cpu(), ref_pp) < RTOL
+        layers = [(A, G, P)] * 3
+        n = torch.zeros(B, device=DEV)
+        rnc.dprc_norm_hutch_layers([x[0] for x in layers], [x[1] for x in layers],
+                                   [x[2] for x in layers], n, ws=ws)
+        assert _relerr(n.cpu(), 3.0 * ref_h) < RTOL
+    assert rnc.dprc_device_error(reset=True) == 0
+
+
 def test_hutchpp_exact_on_low_rank_gradients():
     B, T, d, p, r = 2, 256, 256, 512, 16
     A = _rand((B, T, d), 50, torch.bfloat16)
