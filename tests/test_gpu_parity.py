@@ -420,9 +420,8 @@ def test_hutchpp_leaves_the_counter_block_zero_for_other_calls():
     G = _rand((B, T, p), 81, torch.bfloat16, 0.1).to(DEV)
     S, Pp = _rand((p, r), 82, torch.bfloat16).to(DEV), _rand((p, r), 83, torch.bfloat16).to(DEV)
     P = _rand((p, k), 84, torch.bfloat16).to(DEV)
-    nbytes = max(rnc.dprc_workspace_bytes(rnc.DPRC_OP_HUTCHPP, rnc._dtype_code(A), B, T, d, p, r),
-                 rnc.dprc_workspace_bytes(rnc.DPRC_OP_HUTCH_LAYERS, rnc._dtype_code(A), B, T, d, p,
-                                          k))
+    nbytes = max(rnc.workspace(rnc.DPRC_OP_HUTCHPP, A, B, T, d, p, r).numel(),
+                 rnc.workspace(rnc.DPRC_OP_HUTCH_LAYERS, A, B, T, d, p, k).numel())
     ws = torch.zeros(nbytes, dtype=torch.uint8, device=DEV)
     ref_pp = oracle.hutchpp_norm(to_f64(A.cpu()), to_f64(G.cpu()), to_f64(S.cpu()), to_f64(Pp.cpu()))
     ref_h = oracle.hutch_norm(to_f64(A.cpu()), to_f64(G.cpu()), to_f64(P.cpu()))
