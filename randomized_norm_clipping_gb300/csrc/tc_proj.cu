@@ -639,7 +639,8 @@ __global__ void __launch_bounds__(192) __maxnreg__(ColCfg<NMMA>::kMaxRegs)
       bool ready_ok = true;
       auto await_w = [&](int i) {
         if (a.ready == nullptr || i == ready_i || !ready_ok) return;
-        if (wait_geq(&a.ready[i], a.ready_target, kWaitLimitNs, abort_flag)) {
+        if (DPRC_IN(i >= 0 && i < a.ready_stride) &&
+            wait_geq(&a.ready[i], a.ready_target, kWaitLimitNs, abort_flag)) {
           fence_proxy_async_global();
         } else {
           ready_ok = false;  // W is still loaded so the issued stages complete; results are void
