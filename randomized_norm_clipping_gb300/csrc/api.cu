@@ -155,9 +155,11 @@ TcPlan plan_tc(dprc_op op, int64_t B, int64_t T, int64_t d, int64_t p, int64_t k
   t.w_bytes = static_cast<size_t>(B) * (op == DPRC_OP_HUTCH ? 2 * k : 4 * k) * t.tpad * 2;
   t.w_off = off;
   off = align_up(off + t.w_bytes, 1024);
-  t.w2_off = t.w_off;
+  t.w2_off = t.w3_off = t.w_off;
   if (layers > 1) {
     t.w2_off = off;
+    off = align_up(off + t.w_bytes, 1024);
+    t.w3_off = off;
     off = align_up(off + t.w_bytes, 1024);
   }
   if (op == DPRC_OP_HUTCHPP) {
@@ -185,6 +187,7 @@ FusedScratch fused_scratch(const TcPlan& t, char* w) {
   FusedScratch f;
   f.W[0] = w + t.w_off;
   f.W[1] = w + t.w2_off;
+  f.W[2] = w + t.w3_off;
   f.tpad = t.tpad;
   f.tickets = reinterpret_cast<int*>(w + t.stick_off);
   f.ready = reinterpret_cast<int*>(w + t.ready_off);

@@ -55,7 +55,8 @@ struct TcPlan {
   size_t cnorm_off = 0;       // per-block squared norms fp32 [layers][B][chunks]
   size_t nl_off = 0;          // per-layer norms fp32 [layers][B]
   size_t w_off = 0, w_bytes = 0;  // sketch G P (or G S, A Z, G [Q|P']) hi/lo bf16
-  size_t w2_off = 0;          // second sketch buffer (multi-layer calls; = w_off otherwise)
+  size_t w2_off = 0;          // second and third sketch buffers (multi-layer calls; = w_off
+  size_t w3_off = 0;          // otherwise)
   size_t z_off = 0;           // Hutch++: Z hi/lo bf16 [B][d][2r]
   size_t m_off = 0;           // Hutch++: M = O S fp32 [B][p][r]
   size_t qp_off = 0;          // Hutch++: [Q | P'] hi/lo bf16 [B][p][4r]
@@ -228,7 +229,7 @@ int64_t fgc_partials(int64_t B, int64_t d, int64_t p);
 // caller then uses the two-kernel path); the counters must be zero and are
 // zero again afterwards.
 struct FusedScratch {
-  void* W[2];           // sketch buffers (layer parity); W[1] may equal W[0] for one layer
+  void* W[3];           // sketch buffers (layer l uses W[l % 3]); all equal for one layer
   int64_t tpad;
   int* ready;           // [kMaxFusedLayers][B]
   int* tickets;         // [kMaxFusedLayers][B]

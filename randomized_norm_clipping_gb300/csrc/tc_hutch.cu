@@ -8,7 +8,7 @@
 //
 // Each layer is two contractions (those of tc_proj.cu): the sketch
 // W_i = G_i P and the projection Y_i = A_i^T W_i.  One persistent kernel,
-// every CTA resident at once, runs them as phases, layer after layer:
+// every CTA resident at once, runs them as phases:
 //
 //   phase 1 (sketch)      CTAs take blocks of 128 tokens of one sample and write
 //                         W_i as bf16 hi/lo planes; each block then adds one to
@@ -19,17 +19,18 @@
 //                         epilogue squares Y and a per-(layer, sample) ticket
 //                         sums the blocks in order.
 //
-// A CTA that finishes its share of layer l moves straight on to layer l + 1,
-// so one layer's start-up and tail overlap its neighbours' streaming.  The
-// sketch is double-buffered by layer parity: before phase 1 of layer l writes
-// buffer l % 2, it waits until every projection block of layer l - 2 (the
-// previous user of that buffer) has finished.  Per-layer results go to
-// n_l[l][i]; the last layer to finish sample i adds them in layer order
-// (deterministic) into n_i.
+// With several layers a CTA runs the sketch of layer l + 1 before the
+// projection of layer l (S0, S1, P0, S2, P1, ...; phase_at), so by the time
+// it projects layer l the other CTAs have long written that layer's sketch,
+// and one layer's start-up and tail overlap its neighbours' streaming.  The
+// sketch has three buffers: before phase 1 of layer l writes buffer l % 3, it
+// waits until every projection block of layer l - 3 (the previous user of
+// that buffer) has finished.  Per-layer results go to n_l[l][i]; the last
+// layer to finish sample i adds them in layer order (deterministic) into n_i.
 //
 // The cross-CTA waits are safe because every CTA is resident (the grid is at
 // most what fits on the device at once) and every wait is on work that comes
-// earlier in the one order all CTAs follow (layer, then phase).  Every wait is bounded (2 s, or the
+// earlier in the one order all CTAs follow (phase_at).  Every wait is bounded (2 s, or the
 // limit a test gives) and records a code in the device error word when it
 // runs out; the CTA's other roles then stop at their next wait, the MMA
 // thread waits for the MMAs it issued and the producer for its copies, and
@@ -223,12 +224,12 @@ struct LayerDesc {
 
 template <int CAP>
 struct HParams {
-  CUtensorMap mw[2];       // the two sketch buffers, [B][2k][T_pad]
+  CUtensorMap mw[3];       // the sketch buffers, [B][2k][T_pad] (layer l: l % 3)
   int L, B, T, mtiles;     // layers; batch; tokens; sketch blocks per sample
   int cl;                  // cluster size of the launch
   int maxch;               // stride of chunk_norms per (layer, sample)
   long long tpad;
-  __nv_bfloat16* W[2];
+  __nv_bfloat16* W[3];
   int* ready;              // [L][B]
   int* tickets;            // [L][B]
   int* lticket;            // [B]   layers finished per sample
@@ -306,6 +307,36 @@ __device__ __forceinline__ void gen_sign_tile(uint8_t* tile, int u, int lane, in
 // +-1 projection two more warps that write the sign tiles.
 template <bool PM1>
 constexpr int hutch_threads() { return PM1 ? 256 : 192; }
+
+// Step ps (0 <= ps < 2L) of the one order in which every role of every CTA
+// walks the phases of a launch: the sketch of layer 0, then the sketch of
+// layer l + 1 before the projection of layer l, and the last projection at
+// the end,
+//   S0, S1, P0, S2, P1, ..., S(L-1), P(L-2), P(L-1).
+// A CTA reaches the projection of layer l one sketch after its own sketch
+// blocks of l, so the other CTAs' blocks of l are normally done by then and
+// the projection seldom waits.  Every wait is still on a phase that comes
+// earlier in this order on every CTA: P(l) on S(l), and S(l), which writes
+// sketch buffer l % 3, on P(l - 3), the buffer's previous reader.
+template <int CAP>
+__device__ __forceinline__ void phase_at(int ps, int L, int& l, bool& sketch) {
+  if (CAP == 1) {  // one layer: S0, P0
+    l = 0;
+    sketch = ps == 0;
+  } else if (ps == 0) {
+    l = 0;
+    sketch = true;
+  } else if (ps == 2 * L - 1) {
+    l = L - 1;
+    sketch = false;
+  } else if (ps & 1) {
+    l = (ps + 1) >> 1;
+    sketch = true;
+  } else {
+    l = (ps >> 1) - 1;
+    sketch = false;
+  }
+}
 
 template <int K, int CAP, bool PM1>
 __global__ void __launch_bounds__(hutch_threads<PM1>(), 1)
@@ -400,7 +431,10 @@ __global__ void __launch_bounds__(hutch_threads<PM1>(), 1)
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&a.mw[0]);
-    tma_prefetch_desc(&a.mw[1]);
+    if (CAP > 1) {
+      tma_prefetch_desc(&a.mw[1]);
+      tma_prefetch_desc(&a.mw[2]);
+    }
     for (int l = 0; l < nlayers && l < 4; ++l) {
       const LayerDesc& Ld = a.layer[CAP == 1 ? 0 : l];
       tma_prefetch_desc(&Ld.mg);
@@ -441,112 +475,119 @@ __global__ void __launch_bounds__(hutch_threads<PM1>(), 1)
           ok = false;
         return s;
       };
-      for (int l = 0; l < nlayers && ok; ++l) {
+      #pragma unroll(CAP == 1 ? 2 : 1)
+      for (int ps = 0; ps < 2 * nlayers && ok; ++ps) {
+        int l;
+        bool sketch;
+        phase_at<CAP>(ps, nlayers, l, sketch);
         const LayerDesc& Ld = a.layer[CAP == 1 ? 0 : l];
-        if (CAP > 1 && l + 4 < nlayers) {
-          const LayerDesc& Ln = a.layer[CAP == 1 ? 0 : l + 4];
-          tma_prefetch_desc(&Ln.mg);
-          tma_prefetch_desc(&Ln.mp);
-          tma_prefetch_desc(&Ln.ma);
-        }
-        // phase 1: G and P tiles
-        const Mine m1 = mine(Ld.ph1, cl, rank);
-        const long long nb1 = count_blocks(Ld.ph1, m1);
-        for (long long j = 0; j < nb1 && ok; ++j) {
-          const long long b = m1.first + j * m1.step;
-          const int i = static_cast<int>(b / a.mtiles);
-          const int t0 = static_cast<int>(b - static_cast<long long>(i) * a.mtiles) * kTok;
-          for (int u = m1.ulo; u < m1.uhi; ++u) {
-            if (it < pre) {  // issued before the CTA barrier
+        if (sketch) {
+          if (CAP > 1 && l + 4 < nlayers) {
+            const LayerDesc& Ln = a.layer[CAP == 1 ? 0 : l + 4];
+            tma_prefetch_desc(&Ln.mg);
+            tma_prefetch_desc(&Ln.mp);
+            tma_prefetch_desc(&Ln.ma);
+          }
+          // phase 1: G and P tiles
+          const Mine m1 = mine(Ld.ph1, cl, rank);
+          const long long nb1 = count_blocks(Ld.ph1, m1);
+          for (long long j = 0; j < nb1 && ok; ++j) {
+            const long long b = m1.first + j * m1.step;
+            const int i = static_cast<int>(b / a.mtiles);
+            const int t0 = static_cast<int>(b - static_cast<long long>(i) * a.mtiles) * kTok;
+            for (int u = m1.ulo; u < m1.uhi; ++u) {
+              if (it < pre) {  // issued before the CTA barrier
+                ++it;
+                continue;
+              }
+              const int s = take_slot(it);
+              if (!ok) break;
+              uint8_t* slot = ring + s * Cfg::kSlot;
+              // (+-1 projection: the sign tile comes from the generator warp)
+              mbar_arrive_expect_tx(&full[s], PM1 ? Cfg::kRowG : Cfg::kRowStage);
+  #pragma unroll
+              for (int h = 0; h < 2; ++h)
+                tma_load_3d(slot + h * Cfg::kRowGBox, &Ld.mg, &full[s], rot_unit(m1, u) * kCol + h * 64,
+                            t0, i);
+              if (!PM1) tma_load_3d(slot + Cfg::kRowG, &Ld.mp, &full[s], 0, rot_unit(m1, u) * kCol, 0);
               ++it;
-              continue;
             }
-            const int s = take_slot(it);
-            if (!ok) break;
+          }
+        } else {
+          // phase 2: A tiles, then, once sample i's sketch is complete, W tiles.
+          // Before waiting for a new sample's sketch, up to kStages stages of A
+          // go out; otherwise the A and W tiles of a stage go out together.  Two
+          // cursors walk the stages (one division per block: this thread paces
+          // the whole pipeline).
+          const Mine m2 = mine(Ld.ph2, cl, rank);
+          const long long nb2 = count_blocks(Ld.ph2, m2);
+          const int nu2 = m2.uhi - m2.ulo;
+          const long long total2 = nb2 * nu2;
+          struct Cursor {
+            long long j = 0;
+            int u = 0, i = 0, ch = 0;
+          };
+          auto seek = [&](Cursor& c) {
+            const long long b = m2.first + c.j * m2.step;
+            c.i = static_cast<int>(b / Ld.nchunks);
+            c.ch = static_cast<int>(b - static_cast<long long>(c.i) * Ld.nchunks);
+          };
+          auto advance = [&](Cursor& c) {
+            if (++c.u == m2.uhi) {
+              c.u = m2.ulo;
+              ++c.j;
+              if (c.j < nb2) seek(c);
+            }
+          };
+          Cursor ca, cw;
+          ca.u = cw.u = m2.ulo;
+          if (nb2 > 0) {
+            seek(ca);
+            seek(cw);
+          }
+          const long long base = it;     // global index of this phase's first stage
+          long long w_done = 0;          // stages of this phase with W issued
+          int ready_i = -1;
+          while (w_done < total2) {
+            const bool need_wait = ok && cw.i != ready_i;
+            const long long ahead = need_wait ? kStages : 1;
+            const long long a_to = w_done + ahead < total2 ? w_done + ahead : total2;
+            while (ok && it - base < a_to) {
+              const int s = take_slot(it);
+              if (!ok) break;
+              uint8_t* slot = ring + s * Cfg::kSlot;
+              mbar_arrive_expect_tx(&full[s], Cfg::kColStage);
+              if (PM1) {  // no sign tile in a projection stage
+                mbar_arrive(&full[s]);
+                mbar_arrive(&full[s]);
+              }
+  #pragma unroll
+              for (int h = 0; h < 2; ++h)
+                tma_load_3d(slot + h * Cfg::kColABox, &Ld.ma, &full[s], ca.ch * kRows + h * 64,
+                            ca.u * kTok, ca.i);
+              ++it;
+              advance(ca);
+            }
+            if (w_done >= it - base) break;  // nothing left to complete (after an error)
+            if (need_wait && !DPRC_IN(cw.i >= 0 && cw.i < a.B && l < a.L)) ok = false;
+            if (need_wait && ok) {
+              if (wait_geq(&a.ready[l * a.B + cw.i], Ld.ready_target, lim, abort_flag)) {
+                fence_proxy_async_global();
+                ready_i = cw.i;
+              } else {
+                ok = false;  // still load W so the issued stages complete; results are void
+              }
+            }
+            const long long g = base + w_done;
+            const int s = static_cast<int>(g % kStages);
             uint8_t* slot = ring + s * Cfg::kSlot;
-            // (+-1 projection: the sign tile comes from the generator warp)
-            mbar_arrive_expect_tx(&full[s], PM1 ? Cfg::kRowG : Cfg::kRowStage);
-#pragma unroll
+  #pragma unroll
             for (int h = 0; h < 2; ++h)
-              tma_load_3d(slot + h * Cfg::kRowGBox, &Ld.mg, &full[s], rot_unit(m1, u) * kCol + h * 64,
-                          t0, i);
-            if (!PM1) tma_load_3d(slot + Cfg::kRowG, &Ld.mp, &full[s], 0, rot_unit(m1, u) * kCol, 0);
-            ++it;
+              tma_load_3d(slot + Cfg::kColA + h * Cfg::kColWBox, &a.mw[l % 3], &full[s],
+                          cw.u * kTok + h * 64, 0, cw.i);
+            ++w_done;
+            advance(cw);
           }
-        }
-        // phase 2: A tiles, then, once sample i's sketch is complete, W tiles.
-        // Before waiting for a new sample's sketch, up to kStages stages of A
-        // go out; otherwise the A and W tiles of a stage go out together.  Two
-        // cursors walk the stages (one division per block: this thread paces
-        // the whole pipeline).
-        const Mine m2 = mine(Ld.ph2, cl, rank);
-        const long long nb2 = count_blocks(Ld.ph2, m2);
-        const int nu2 = m2.uhi - m2.ulo;
-        const long long total2 = nb2 * nu2;
-        struct Cursor {
-          long long j = 0;
-          int u = 0, i = 0, ch = 0;
-        };
-        auto seek = [&](Cursor& c) {
-          const long long b = m2.first + c.j * m2.step;
-          c.i = static_cast<int>(b / Ld.nchunks);
-          c.ch = static_cast<int>(b - static_cast<long long>(c.i) * Ld.nchunks);
-        };
-        auto advance = [&](Cursor& c) {
-          if (++c.u == m2.uhi) {
-            c.u = m2.ulo;
-            ++c.j;
-            if (c.j < nb2) seek(c);
-          }
-        };
-        Cursor ca, cw;
-        ca.u = cw.u = m2.ulo;
-        if (nb2 > 0) {
-          seek(ca);
-          seek(cw);
-        }
-        const long long base = it;     // global index of this phase's first stage
-        long long w_done = 0;          // stages of this phase with W issued
-        int ready_i = -1;
-        while (w_done < total2) {
-          const bool need_wait = ok && cw.i != ready_i;
-          const long long ahead = need_wait ? kStages : 1;
-          const long long a_to = w_done + ahead < total2 ? w_done + ahead : total2;
-          while (ok && it - base < a_to) {
-            const int s = take_slot(it);
-            if (!ok) break;
-            uint8_t* slot = ring + s * Cfg::kSlot;
-            mbar_arrive_expect_tx(&full[s], Cfg::kColStage);
-            if (PM1) {  // no sign tile in a projection stage
-              mbar_arrive(&full[s]);
-              mbar_arrive(&full[s]);
-            }
-#pragma unroll
-            for (int h = 0; h < 2; ++h)
-              tma_load_3d(slot + h * Cfg::kColABox, &Ld.ma, &full[s], ca.ch * kRows + h * 64,
-                          ca.u * kTok, ca.i);
-            ++it;
-            advance(ca);
-          }
-          if (w_done >= it - base) break;  // nothing left to complete (after an error)
-          if (need_wait && !DPRC_IN(cw.i >= 0 && cw.i < a.B && l < a.L)) ok = false;
-          if (need_wait && ok) {
-            if (wait_geq(&a.ready[l * a.B + cw.i], Ld.ready_target, lim, abort_flag)) {
-              fence_proxy_async_global();
-              ready_i = cw.i;
-            } else {
-              ok = false;  // still load W so the issued stages complete; results are void
-            }
-          }
-          const long long g = base + w_done;
-          const int s = static_cast<int>(g % kStages);
-          uint8_t* slot = ring + s * Cfg::kSlot;
-#pragma unroll
-          for (int h = 0; h < 2; ++h)
-            tma_load_3d(slot + Cfg::kColA + h * Cfg::kColWBox, &a.mw[l & 1], &full[s],
-                        cw.u * kTok + h * 64, 0, cw.i);
-          ++w_done;
-          advance(cw);
         }
       }
       if (!ok) *abort_flag = 1;
@@ -573,69 +614,76 @@ __global__ void __launch_bounds__(hutch_threads<PM1>(), 1)
           ok = false;
         return s;
       };
-      for (int l = 0; l < nlayers && ok; ++l) {
+      #pragma unroll(CAP == 1 ? 2 : 1)
+      for (int ps = 0; ps < 2 * nlayers && ok; ++ps) {
+        int l;
+        bool sketch;
+        phase_at<CAP>(ps, nlayers, l, sketch);
         const LayerDesc& Ld = a.layer[CAP == 1 ? 0 : l];
-        const Mine m1 = mine(Ld.ph1, cl, rank);
-        const long long nb1 = count_blocks(Ld.ph1, m1);
-        for (long long j = 0; j < nb1 && ok; ++j, ++seg1) {
-          const int abuf = static_cast<int>(seg1 & 1);
-          if (!mbar_wait_lim(&acce_r[abuf], (static_cast<uint32_t>(seg1 >> 1) & 1) ^ 1,
-                             DPRC_DEVERR_ACCUM, lim2, abort_flag)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          for (int u = m1.ulo; u < m1.uhi; ++u, ++it) {
-            const int s = wait_full(it);
-            if (!ok) break;
-            tc_fence_after();
-            const uint32_t ga = smem_u32(ring + s * Cfg::kSlot);
-            const uint32_t pa = ga + Cfg::kRowG;
-#pragma unroll
-            for (int kk = 0; kk < kCol / 16; ++kk) {
-              // G: two boxes of 128 token rows x 64 p, K-major, 128-byte swizzle.
-              const uint64_t ad =
-                  make_sdesc(ga + (kk >> 2) * Cfg::kRowGBox + (kk & 3) * 32, 16, 1024, kSwz128);
-              // P: 128 p rows x K columns, MN-major, one swizzle atom wide.
-              const uint64_t bd = make_sdesc(pa + kk * 32 * Cfg::kNR, 16, 16 * Cfg::kNR, p_swz);
-              umma_bf16(tmem + abuf * Cfg::kAccR, ad, bd, idesc1,
-                        (u == m1.ulo && kk == 0) ? 0u : 1u);
+        if (sketch) {
+          const Mine m1 = mine(Ld.ph1, cl, rank);
+          const long long nb1 = count_blocks(Ld.ph1, m1);
+          for (long long j = 0; j < nb1 && ok; ++j, ++seg1) {
+            const int abuf = static_cast<int>(seg1 & 1);
+            if (!mbar_wait_lim(&acce_r[abuf], (static_cast<uint32_t>(seg1 >> 1) & 1) ^ 1,
+                               DPRC_DEVERR_ACCUM, lim2, abort_flag)) {
+              ok = false;
+              break;
             }
-            issued = true;
-            umma_commit(&empty[s]);
-          }
-          if (ok) umma_commit(&accf_r[abuf]);
-        }
-        const Mine m2 = mine(Ld.ph2, cl, rank);
-        const long long nb2 = count_blocks(Ld.ph2, m2);
-        for (long long j = 0; j < nb2 && ok; ++j, ++seg2) {
-          const int abuf = static_cast<int>(seg2 & 1);
-          if (!mbar_wait_lim(&acce_c[abuf], (static_cast<uint32_t>(seg2 >> 1) & 1) ^ 1,
-                             DPRC_DEVERR_ACCUM, lim2, abort_flag)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          for (int u = m2.ulo; u < m2.uhi; ++u, ++it) {
-            const int s = wait_full(it);
-            if (!ok) break;
             tc_fence_after();
-            const uint32_t xa = smem_u32(ring + s * Cfg::kSlot);
-            const uint32_t wa = xa + Cfg::kColA;
-#pragma unroll
-            for (int kk = 0; kk < kTok / 16; ++kk) {
-              // A^T: 128 d (two 64-d atoms, LBO = one box) x 16 tokens (SBO 1 KB).
-              const uint64_t ad = make_sdesc(xa + kk * 2048, Cfg::kColABox, 1024, kSwz128);
-              // Sketch: 2K rows x 64 tokens per box, K-major, 128-byte swizzle.
-              const uint64_t bd =
-                  make_sdesc(wa + (kk >> 2) * Cfg::kColWBox + (kk & 3) * 32, 16, 1024, kSwz128);
-              umma_bf16(tmem + Cfg::kColAcc0 + abuf * Cfg::kNC, ad, bd, idesc2,
-                        (u == m2.ulo && kk == 0) ? 0u : 1u);
+            for (int u = m1.ulo; u < m1.uhi; ++u, ++it) {
+              const int s = wait_full(it);
+              if (!ok) break;
+              tc_fence_after();
+              const uint32_t ga = smem_u32(ring + s * Cfg::kSlot);
+              const uint32_t pa = ga + Cfg::kRowG;
+  #pragma unroll
+              for (int kk = 0; kk < kCol / 16; ++kk) {
+                // G: two boxes of 128 token rows x 64 p, K-major, 128-byte swizzle.
+                const uint64_t ad =
+                    make_sdesc(ga + (kk >> 2) * Cfg::kRowGBox + (kk & 3) * 32, 16, 1024, kSwz128);
+                // P: 128 p rows x K columns, MN-major, one swizzle atom wide.
+                const uint64_t bd = make_sdesc(pa + kk * 32 * Cfg::kNR, 16, 16 * Cfg::kNR, p_swz);
+                umma_bf16(tmem + abuf * Cfg::kAccR, ad, bd, idesc1,
+                          (u == m1.ulo && kk == 0) ? 0u : 1u);
+              }
+              issued = true;
+              umma_commit(&empty[s]);
             }
-            issued = true;
-            umma_commit(&empty[s]);
+            if (ok) umma_commit(&accf_r[abuf]);
           }
-          if (ok) umma_commit(&accf_c[abuf]);
+        } else {
+          const Mine m2 = mine(Ld.ph2, cl, rank);
+          const long long nb2 = count_blocks(Ld.ph2, m2);
+          for (long long j = 0; j < nb2 && ok; ++j, ++seg2) {
+            const int abuf = static_cast<int>(seg2 & 1);
+            if (!mbar_wait_lim(&acce_c[abuf], (static_cast<uint32_t>(seg2 >> 1) & 1) ^ 1,
+                               DPRC_DEVERR_ACCUM, lim2, abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            for (int u = m2.ulo; u < m2.uhi; ++u, ++it) {
+              const int s = wait_full(it);
+              if (!ok) break;
+              tc_fence_after();
+              const uint32_t xa = smem_u32(ring + s * Cfg::kSlot);
+              const uint32_t wa = xa + Cfg::kColA;
+  #pragma unroll
+              for (int kk = 0; kk < kTok / 16; ++kk) {
+                // A^T: 128 d (two 64-d atoms, LBO = one box) x 16 tokens (SBO 1 KB).
+                const uint64_t ad = make_sdesc(xa + kk * 2048, Cfg::kColABox, 1024, kSwz128);
+                // Sketch: 2K rows x 64 tokens per box, K-major, 128-byte swizzle.
+                const uint64_t bd =
+                    make_sdesc(wa + (kk >> 2) * Cfg::kColWBox + (kk & 3) * 32, 16, 1024, kSwz128);
+                umma_bf16(tmem + Cfg::kColAcc0 + abuf * Cfg::kNC, ad, bd, idesc2,
+                          (u == m2.ulo && kk == 0) ? 0u : 1u);
+              }
+              issued = true;
+              umma_commit(&empty[s]);
+            }
+            if (ok) umma_commit(&accf_c[abuf]);
+          }
         }
       }
       if (!ok) *abort_flag = 1;
@@ -688,195 +736,202 @@ __global__ void __launch_bounds__(hutch_threads<PM1>(), 1)
       if (Ld.ph1.split) rounds += static_cast<int>(count_blocks(Ld.ph1, mine(Ld.ph1, cl, rank)));
       if (Ld.ph2.split) rounds += static_cast<int>(count_blocks(Ld.ph2, mine(Ld.ph2, cl, rank)));
     }
-    for (int l = 0; l < nlayers; ++l) {
+    #pragma unroll(CAP == 1 ? 2 : 1)
+    for (int ps = 0; ps < 2 * nlayers; ++ps) {
+      int l;
+      bool sketch;
+      phase_at<CAP>(ps, nlayers, l, sketch);
       const LayerDesc& Ld = a.layer[CAP == 1 ? 0 : l];
-      __nv_bfloat16* W = a.W[l & 1];
-      // phase 1: sketch rows -> W hi/lo, then count the block done
-      const Mine m1 = mine(Ld.ph1, cl, rank);
-      const long long nb1 = count_blocks(Ld.ph1, m1);
-      if (CAP > 1 && nb1 > 0 && l >= 2) {
-        // the previous user of this sketch buffer (layer l - 2) must be done
-        if (threadIdx.x == 64 && ok &&
-            (!DPRC_IN(l < a.L) ||
-             !wait_geq(&a.done2[l - 2],
-                       static_cast<int>(a.layer[CAP == 1 ? 0 : l - 2].ph2.nblocks), lim,
-                       abort_flag)))
-          *abort_flag = 1;
-        named_bar_sync(1, 128);
-      }
-      for (long long j = 0; j < nb1; ++j, ++seg1) {
-        const int abuf = static_cast<int>(seg1 & 1);
-        bool live = ok &&
-                    mbar_wait_lim(&accf_r[abuf], static_cast<uint32_t>(seg1 >> 1) & 1,
-                                  DPRC_DEVERR_ACCUM, lim2, abort_flag) &&
-                    *abort_flag == 0;
-        live = __all_sync(0xffffffffu, live);  // keep the warp's TMEM loads convergent
-        if (!live) ok = false;
-        tc_fence_after();
-        float y[K];
-#pragma unroll
-        for (int t = 0; t < K; ++t) y[t] = 0.f;
-        if (live) tmem_ld_cols<K>(tmem + lane_base + abuf * Cfg::kAccR, y);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&acce_r[abuf]);
-        bool mine_row = true;
-        if (Ld.ph1.split) {
-          mine_row = xchg_rows<K>(xs, cl, rank, row, rnd, rnd + 1 == rounds, y, ok, lim2);
-          ++rnd;
+      if (sketch) {
+        __nv_bfloat16* W = a.W[l % 3];
+        // phase 1: sketch rows -> W hi/lo, then count the block done
+        const Mine m1 = mine(Ld.ph1, cl, rank);
+        const long long nb1 = count_blocks(Ld.ph1, m1);
+        if (CAP > 1 && nb1 > 0 && l >= 3) {
+          // the previous user of this sketch buffer (layer l - 3) must be done
+          if (threadIdx.x == 64 && ok &&
+              (!DPRC_IN(l < a.L) ||
+               !wait_geq(&a.done2[l - 3],
+                         static_cast<int>(a.layer[CAP == 1 ? 0 : l - 3].ph2.nblocks), lim,
+                         abort_flag)))
+            *abort_flag = 1;
+          named_bar_sync(1, 128);
         }
-        const long long b = m1.first + j * m1.step;
-        const int i = static_cast<int>(b / a.mtiles);
-        const int t = static_cast<int>(b - static_cast<long long>(i) * a.mtiles) * kTok + row;
-        if (mine_row && ok && t < a.T && DPRC_IN(i >= 0 && i < a.B && t < a.tpad)) {
-          __nv_bfloat16* wi = W + static_cast<size_t>(i) * 2 * K * a.tpad + t;
-#pragma unroll
-          for (int c = 0; c < K; ++c) {
-            __nv_bfloat16 hi, lo;
-            split_hilo(y[c], hi, lo);
-            wi[static_cast<size_t>(c) * a.tpad] = hi;
-            wi[static_cast<size_t>(K + c) * a.tpad] = lo;
+        for (long long j = 0; j < nb1; ++j, ++seg1) {
+          const int abuf = static_cast<int>(seg1 & 1);
+          bool live = ok &&
+                      mbar_wait_lim(&accf_r[abuf], static_cast<uint32_t>(seg1 >> 1) & 1,
+                                    DPRC_DEVERR_ACCUM, lim2, abort_flag) &&
+                      *abort_flag == 0;
+          live = __all_sync(0xffffffffu, live);  // keep the warp's TMEM loads convergent
+          if (!live) ok = false;
+          tc_fence_after();
+          float y[K];
+  #pragma unroll
+          for (int t = 0; t < K; ++t) y[t] = 0.f;
+          if (live) tmem_ld_cols<K>(tmem + lane_base + abuf * Cfg::kAccR, y);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acce_r[abuf]);
+          bool mine_row = true;
+          if (Ld.ph1.split) {
+            mine_row = xchg_rows<K>(xs, cl, rank, row, rnd, rnd + 1 == rounds, y, ok, lim2);
+            ++rnd;
+          }
+          const long long b = m1.first + j * m1.step;
+          const int i = static_cast<int>(b / a.mtiles);
+          const int t = static_cast<int>(b - static_cast<long long>(i) * a.mtiles) * kTok + row;
+          if (mine_row && ok && t < a.T && DPRC_IN(i >= 0 && i < a.B && t < a.tpad)) {
+            __nv_bfloat16* wi = W + static_cast<size_t>(i) * 2 * K * a.tpad + t;
+  #pragma unroll
+            for (int c = 0; c < K; ++c) {
+              __nv_bfloat16 hi, lo;
+              split_hilo(y[c], hi, lo);
+              wi[static_cast<size_t>(c) * a.tpad] = hi;
+              wi[static_cast<size_t>(K + c) * a.tpad] = lo;
+            }
+          }
+          fence_proxy_async_global();  // these rows are read by TMA (async proxy)
+          named_bar_sync(1, 128);
+          if (ew == 0 && lane == 0 && ok && DPRC_IN(i >= 0 && i < a.B && l < a.L)) {
+            __threadfence();
+            atomicAdd(&a.ready[l * a.B + i], 1);
           }
         }
-        fence_proxy_async_global();  // these rows are read by TMA (async proxy)
-        named_bar_sync(1, 128);
-        if (ew == 0 && lane == 0 && ok && DPRC_IN(i >= 0 && i < a.B && l < a.L)) {
-          __threadfence();
-          atomicAdd(&a.ready[l * a.B + i], 1);
-        }
-      }
-      // phase 2: squared norms of the projection blocks
-      const Mine m2 = mine(Ld.ph2, cl, rank);
-      const long long nb2 = count_blocks(Ld.ph2, m2);
-      for (long long j = 0; j < nb2; ++j, ++seg2) {
-        const int abuf = static_cast<int>(seg2 & 1);
-        bool live = ok &&
-                    mbar_wait_lim(&accf_c[abuf], static_cast<uint32_t>(seg2 >> 1) & 1,
-                                  DPRC_DEVERR_ACCUM, lim2, abort_flag) &&
-                    *abort_flag == 0;
-        live = __all_sync(0xffffffffu, live);
-        if (!live) ok = false;
-        tc_fence_after();
-        float y[K];
-#pragma unroll
-        for (int t = 0; t < K; ++t) y[t] = 0.f;
-        if (live) {
-          const uint32_t tb = tmem + lane_base + Cfg::kColAcc0 + abuf * Cfg::kNC;
-          float hi[K], lo[K];
-          tmem_ld_cols<K>(tb, hi);
-          tmem_ld_cols<K>(tb + K, lo);
-#pragma unroll
-          for (int t = 0; t < K; ++t) y[t] = hi[t] + lo[t];
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&acce_c[abuf]);
-        bool mine_row = true;
-        if (Ld.ph2.split) {
-          mine_row = xchg_rows<K>(xs, cl, rank, row, rnd, rnd + 1 == rounds, y, ok, lim2);
-          ++rnd;
-        }
-        const long long b = m2.first + j * m2.step;
-        const int i = static_cast<int>(b / Ld.nchunks);
-        const int ch = static_cast<int>(b - static_cast<long long>(i) * Ld.nchunks);
-        float sq = 0.f;
-        if (mine_row && ok && ch * kRows + row < Ld.d) {
-#pragma unroll
-          for (int t = 0; t < K; ++t) sq = fmaf(y[t], y[t], sq);
-          sq *= a.norm_scale;  // 1, or 1/k (a power of two: exact)
-        }
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, off);
-        if (lane == 0) s_red[ew] = sq;
-        named_bar_sync(1, 128);
-        if (ew == 0) {
-          // warp 2: lane 0 gathers the block's norm; the whole warp finishes
-          // a sample (the chunk and layer sums read many L2 lines: one per lane)
-          const float part = (s_red[0] + s_red[1]) + (s_red[2] + s_red[3]);
-          float chunk = part;
-          int leader = 1;
-          if (lane == 0 && Ld.ph2.split) {
-            float* nb = xs.norms + (nsplit2 & 1) * 8;
-            if (rank != 0) {
-              if (DPRC_IN(rank < 8)) {
-                st_cluster_f32(map_to_rank(nb + rank, 0), part);
-                mbar_arrive_remote(map_to_rank(&xs.norm_bar[nsplit2 & 1], 0));
+      } else {
+        // phase 2: squared norms of the projection blocks
+        const Mine m2 = mine(Ld.ph2, cl, rank);
+        const long long nb2 = count_blocks(Ld.ph2, m2);
+        for (long long j = 0; j < nb2; ++j, ++seg2) {
+          const int abuf = static_cast<int>(seg2 & 1);
+          bool live = ok &&
+                      mbar_wait_lim(&accf_c[abuf], static_cast<uint32_t>(seg2 >> 1) & 1,
+                                    DPRC_DEVERR_ACCUM, lim2, abort_flag) &&
+                      *abort_flag == 0;
+          live = __all_sync(0xffffffffu, live);
+          if (!live) ok = false;
+          tc_fence_after();
+          float y[K];
+  #pragma unroll
+          for (int t = 0; t < K; ++t) y[t] = 0.f;
+          if (live) {
+            const uint32_t tb = tmem + lane_base + Cfg::kColAcc0 + abuf * Cfg::kNC;
+            float hi[K], lo[K];
+            tmem_ld_cols<K>(tb, hi);
+            tmem_ld_cols<K>(tb + K, lo);
+  #pragma unroll
+            for (int t = 0; t < K; ++t) y[t] = hi[t] + lo[t];
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acce_c[abuf]);
+          bool mine_row = true;
+          if (Ld.ph2.split) {
+            mine_row = xchg_rows<K>(xs, cl, rank, row, rnd, rnd + 1 == rounds, y, ok, lim2);
+            ++rnd;
+          }
+          const long long b = m2.first + j * m2.step;
+          const int i = static_cast<int>(b / Ld.nchunks);
+          const int ch = static_cast<int>(b - static_cast<long long>(i) * Ld.nchunks);
+          float sq = 0.f;
+          if (mine_row && ok && ch * kRows + row < Ld.d) {
+  #pragma unroll
+            for (int t = 0; t < K; ++t) sq = fmaf(y[t], y[t], sq);
+            sq *= a.norm_scale;  // 1, or 1/k (a power of two: exact)
+          }
+  #pragma unroll
+          for (int off = 16; off > 0; off >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, off);
+          if (lane == 0) s_red[ew] = sq;
+          named_bar_sync(1, 128);
+          if (ew == 0) {
+            // warp 2: lane 0 gathers the block's norm; the whole warp finishes
+            // a sample (the chunk and layer sums read many L2 lines: one per lane)
+            const float part = (s_red[0] + s_red[1]) + (s_red[2] + s_red[3]);
+            float chunk = part;
+            int leader = 1;
+            if (lane == 0 && Ld.ph2.split) {
+              float* nb = xs.norms + (nsplit2 & 1) * 8;
+              if (rank != 0) {
+                if (DPRC_IN(rank < 8)) {
+                  st_cluster_f32(map_to_rank(nb + rank, 0), part);
+                  mbar_arrive_remote(map_to_rank(&xs.norm_bar[nsplit2 & 1], 0));
+                }
+                leader = 0;
+              } else {
+                if (!mbar_wait_cluster(&xs.norm_bar[nsplit2 & 1],
+                                       static_cast<uint32_t>(nsplit2 >> 1) & 1, DPRC_DEVERR_CLUSTER,
+                                       lim2))
+                  ok = false;
+                nb[0] = part;
+                chunk = 0.f;
+                for (int s = 0; s < cl; ++s) chunk += nb[s];
               }
-              leader = 0;
-            } else {
-              if (!mbar_wait_cluster(&xs.norm_bar[nsplit2 & 1],
-                                     static_cast<uint32_t>(nsplit2 >> 1) & 1, DPRC_DEVERR_CLUSTER,
-                                     lim2))
-                ok = false;
-              nb[0] = part;
-              chunk = 0.f;
-              for (int s = 0; s < cl; ++s) chunk += nb[s];
             }
-          }
-          leader = __shfl_sync(0xffffffffu, leader, 0);
-          const bool lok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-          if (!lok) ok = false;
-          if (leader && lok &&
-              DPRC_IN(i >= 0 && i < a.B && ch >= 0 && ch < Ld.nchunks && Ld.nchunks <= a.maxch)) {
-            const size_t li = static_cast<size_t>(l) * a.B + i;
-            int last = 0;
-            if (lane == 0) {
-              a.chunk_norms[li * a.maxch + ch] = chunk;
-              __threadfence();
-              last = atomicAdd(&a.tickets[li], 1) == Ld.nchunks - 1;
-            }
-            if (__shfl_sync(0xffffffffu, last, 0)) {
-              // last block of (layer l, sample i): its norm, summed in a fixed order
-              __threadfence();
-              float sum = 0.f;
-              for (int c = lane; c < Ld.nchunks; c += 32) sum += __ldcg(&a.chunk_norms[li * a.maxch + c]);
-#pragma unroll
-              for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-              int final_layer = 0;
+            leader = __shfl_sync(0xffffffffu, leader, 0);
+            const bool lok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+            if (!lok) ok = false;
+            if (leader && lok &&
+                DPRC_IN(i >= 0 && i < a.B && ch >= 0 && ch < Ld.nchunks && Ld.nchunks <= a.maxch)) {
+              const size_t li = static_cast<size_t>(l) * a.B + i;
+              int last = 0;
               if (lane == 0) {
-                a.tickets[li] = 0;
-                a.ready[li] = 0;
-                if (CAP == 1) {
-                  // one layer: no layer sum to wait for
-                  const float nv = (a.accumulate ? a.n_out[i] : 0.f) + sum;
-                  a.n_out[i] = nv;
-                  if (a.c_out != nullptr) {
-                    bool bad;
-                    a.c_out[i] = clip_factor(nv, a.clip_C, bad);
-                    if (bad && a.nonfinite != nullptr) atomicAdd(a.nonfinite, 1);
-                  }
-                } else {
-                  a.nl[li] = sum;
-                  __threadfence();
-                  final_layer = atomicAdd(&a.lticket[i], 1) == a.L - 1;
-                }
-              }
-              if (CAP > 1 && __shfl_sync(0xffffffffu, final_layer, 0)) {
-                // last layer of sample i: the layer sum, in a fixed order
+                a.chunk_norms[li * a.maxch + ch] = chunk;
                 __threadfence();
-                float tot = 0.f;
-                for (int ll = lane; ll < a.L; ll += 32)
-                  tot += __ldcg(&a.nl[static_cast<size_t>(ll) * a.B + i]);
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, off);
+                last = atomicAdd(&a.tickets[li], 1) == Ld.nchunks - 1;
+              }
+              if (__shfl_sync(0xffffffffu, last, 0)) {
+                // last block of (layer l, sample i): its norm, summed in a fixed order
+                __threadfence();
+                float sum = 0.f;
+                for (int c = lane; c < Ld.nchunks; c += 32) sum += __ldcg(&a.chunk_norms[li * a.maxch + c]);
+  #pragma unroll
+                for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+                int final_layer = 0;
                 if (lane == 0) {
-                  const float nv = (a.accumulate ? a.n_out[i] : 0.f) + tot;
-                  a.n_out[i] = nv;
-                  a.lticket[i] = 0;
-                  if (a.c_out != nullptr) {
-                    bool bad;
-                    a.c_out[i] = clip_factor(nv, a.clip_C, bad);
-                    if (bad && a.nonfinite != nullptr) atomicAdd(a.nonfinite, 1);
+                  a.tickets[li] = 0;
+                  a.ready[li] = 0;
+                  if (CAP == 1) {
+                    // one layer: no layer sum to wait for
+                    const float nv = (a.accumulate ? a.n_out[i] : 0.f) + sum;
+                    a.n_out[i] = nv;
+                    if (a.c_out != nullptr) {
+                      bool bad;
+                      a.c_out[i] = clip_factor(nv, a.clip_C, bad);
+                      if (bad && a.nonfinite != nullptr) atomicAdd(a.nonfinite, 1);
+                    }
+                  } else {
+                    a.nl[li] = sum;
+                    __threadfence();
+                    final_layer = atomicAdd(&a.lticket[i], 1) == a.L - 1;
+                  }
+                }
+                if (CAP > 1 && __shfl_sync(0xffffffffu, final_layer, 0)) {
+                  // last layer of sample i: the layer sum, in a fixed order
+                  __threadfence();
+                  float tot = 0.f;
+                  for (int ll = lane; ll < a.L; ll += 32)
+                    tot += __ldcg(&a.nl[static_cast<size_t>(ll) * a.B + i]);
+  #pragma unroll
+                  for (int off = 16; off > 0; off >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, off);
+                  if (lane == 0) {
+                    const float nv = (a.accumulate ? a.n_out[i] : 0.f) + tot;
+                    a.n_out[i] = nv;
+                    a.lticket[i] = 0;
+                    if (a.c_out != nullptr) {
+                      bool bad;
+                      a.c_out[i] = clip_factor(nv, a.clip_C, bad);
+                      if (bad && a.nonfinite != nullptr) atomicAdd(a.nonfinite, 1);
+                    }
                   }
                 }
               }
+              // this block no longer reads the sketch buffer of layer l
+              if (CAP > 1 && lane == 0 && DPRC_IN(l < a.L)) atomicAdd(&a.done2[l], 1);
             }
-            // this block no longer reads the sketch buffer of layer l
-            if (CAP > 1 && lane == 0 && DPRC_IN(l < a.L)) atomicAdd(&a.done2[l], 1);
           }
+          named_bar_sync(1, 128);
+          if (Ld.ph2.split) ++nsplit2;
         }
-        named_bar_sync(1, 128);
-        if (Ld.ph2.split) ++nsplit2;
       }
     }
   }
@@ -1116,8 +1171,7 @@ cudaError_t launch_cap(int L, const void* const* A, const void* const* G, const 
   }
   const int ik = static_cast<int>(k);
   a.tpad = ws.tpad;
-  a.W[0] = static_cast<__nv_bfloat16*>(ws.W[0]);
-  a.W[1] = static_cast<__nv_bfloat16*>(ws.W[1]);
+  for (int b = 0; b < 3; ++b) a.W[b] = static_cast<__nv_bfloat16*>(ws.W[b]);
   a.ready = ws.ready;
   a.tickets = ws.tickets;
   a.lticket = ws.lticket;
@@ -1133,7 +1187,7 @@ cudaError_t launch_cap(int L, const void* const* A, const void* const* G, const 
   a.nonfinite = clip != nullptr ? clip->nonfinite : nullptr;
   a.seed = seed;
   a.step = step;
-  for (int b = 0; b < 2; ++b)
+  for (int b = 0; b < 3; ++b)
     if (!make_tmap_3d_bf16(&a.mw[b], ws.W[b], T, 2 * ik, B, ws.tpad, 2 * ik * ws.tpad, 64,
                            2 * ik, 128))
       return cudaErrorInvalidValue;
