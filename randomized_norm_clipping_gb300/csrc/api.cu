@@ -916,25 +916,32 @@ dprc_status dprc_norm_hutchpp(const void* A, const void* G, const void* S, const
       const int ready_target = static_cast<int>((T + 127) / 128);
       mark(0, s);
       cudaError_t e = launch_pack_cols(S, P, SP, p, ir, s);
-      // pass 1: [Z | X P] = A^T (G [S | P]); Z as hi/lo for pass 2, X P in fp32
-      const BlockSched rs1 = rowproj_sched(B, T, p, 2 * ir);
-      if (e == cudaSuccess)
+      // passes 1 and 2 as one persistent launch of the fused kernel (pass 2's
+      // sketch of a sample starts when pass 1 has written that sample's Z)
+      bool fused12 = false;
+      if (e == cudaSuccess && pdl)
+        e = launch_tc_hutchpp12(A, G, SP, B, T, d, p, fused_scratch(t, w), Z, YP, M, MH, s,
+                                &fused12);
+      if (e == cudaSuccess && !fused12) {
+        // pass 1: [Z | X P] = A^T (G [S | P]); Z as hi/lo for pass 2, X P in fp32
+        const BlockSched rs1 = rowproj_sched(B, T, p, 2 * ir);
         e = launch_tc_rowproj(G, B, T, p, SP, false, 2 * ir, false, W, t.tpad, rs1, stick, B, s,
                               false, ready1);
-      if (e == cudaSuccess)
-        e = launch_tc_colproj(A, B, T, d, W, t.tpad, 2 * ir, colproj_sched(B, T, d, 4 * ir),
-                              stick, cnorm, kColprojSplit, nullptr, 0, ir, 1.0f, YP, Z, pdl, s,
-                              ir, nullptr, nullptr, ready1, ready_target * rs1.cl);
-      mark(1, s);
-      // pass 2: M = G^T (A Z) = O S, fp32 for the QR and hi/lo for pass 3
-      const BlockSched rs2 = rowproj_sched(B, T, d, 2 * ir);
-      if (e == cudaSuccess)
-        e = launch_tc_rowproj(A, B, T, d, Z, true, 2 * ir, true, W, t.tpad, rs2, stick, B, s,
-                              false, ready2);
-      if (e == cudaSuccess)
-        e = launch_tc_colproj(G, B, T, p, W, t.tpad, ir, colproj_sched(B, T, p, 2 * ir), stick,
-                              cnorm, kColprojF32Hilo, nullptr, 0, ir, 1.0f, M, MH, pdl, s, 0,
-                              nullptr, nullptr, ready2, ready_target * rs2.cl);
+        if (e == cudaSuccess)
+          e = launch_tc_colproj(A, B, T, d, W, t.tpad, 2 * ir, colproj_sched(B, T, d, 4 * ir),
+                                stick, cnorm, kColprojSplit, nullptr, 0, ir, 1.0f, YP, Z, pdl, s,
+                                ir, nullptr, nullptr, ready1, ready_target * rs1.cl);
+        mark(1, s);
+        // pass 2: M = G^T (A Z) = O S, fp32 for the QR and hi/lo for pass 3
+        const BlockSched rs2 = rowproj_sched(B, T, d, 2 * ir);
+        if (e == cudaSuccess)
+          e = launch_tc_rowproj(A, B, T, d, Z, true, 2 * ir, true, W, t.tpad, rs2, stick, B, s,
+                                false, ready2);
+        if (e == cudaSuccess)
+          e = launch_tc_colproj(G, B, T, p, W, t.tpad, ir, colproj_sched(B, T, p, 2 * ir), stick,
+                                cnorm, kColprojF32Hilo, nullptr, 0, ir, 1.0f, M, MH, pdl, s, 0,
+                                nullptr, nullptr, ready2, ready_target * rs2.cl);
+      }
       mark(2, s);
       // the QR's factors (R, column scales, C = Q^T P) ...
       if (e == cudaSuccess) e = launch_qr_cluster(M, B, p, P, dtype, nullptr, true, s, RC);

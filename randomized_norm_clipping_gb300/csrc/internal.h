@@ -240,6 +240,16 @@ struct FusedScratch {
   float* nl;            // [layers][B]
 };
 FusedScratch fused_scratch(const TcPlan& t, char* ws);
+// The first two passes of Hutch++ (r = 16) as one persistent launch of the
+// fused kernel: pass 1 sketches G with SP = [S | P] and writes Z = A^T G S as
+// bf16 hi/lo [B][d][32] and X P = A^T G P fp32 [B][d][16]; pass 2 sketches A
+// with Z_i as soon as all of Z_i is written and writes M = G^T A Z fp32
+// [B][p][16] and hi/lo [B][p][32].  *launched is false when the shapes do not
+// fit its plan (the caller then runs the passes as separate kernels).
+cudaError_t launch_tc_hutchpp12(const void* A, const void* G, const void* SP, int64_t B,
+                                int64_t T, int64_t d, int64_t p, const FusedScratch& ws, void* Z,
+                                float* YP, float* M, void* MH, cudaStream_t s, bool* launched);
+
 bool fused_hutch_supported(int64_t k);
 // Whether a dprc_norm_hutch call with these sizes takes the fused kernel on
 // the current device (the same decision the launcher makes).

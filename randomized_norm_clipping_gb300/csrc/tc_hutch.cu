@@ -245,8 +245,23 @@ struct HParams {
   int32_t* nonfinite;
   unsigned long long seed, step;   // +-1 projection: its Philox stream
   unsigned long long wait_ns;      // limit of every wait in the launch
+  // The first two passes of Hutch++ (CAP == kHppCap, see hpp_launch): layer 0
+  // is pass 1 (sketch G [S | P], projection A^T W written as Z hi/lo and X P),
+  // layer 1 pass 2 (sketch A Z_i, Z_i per sample and summed from its hi/lo
+  // halves; projection G^T W written as M fp32 and hi/lo).
+  __nv_bfloat16* hz;       // Z hi/lo [B][d][32]
+  float* hyp;              // X P [B][d][16]
+  float* hm;               // M [B][p][16]
+  __nv_bfloat16* hmh;      // M hi/lo [B][p][32]
+  int* zdone;              // [B] pass-1 projection blocks written per sample
+  int zdone_target;        // their number per sample
+  int mdone_target;        // pass-2 projection blocks per sample
   LayerDesc layer[CAP];     // CAP = 1 for single-layer calls: a small parameter block
 };
+
+// CAP of the launch that runs the first two passes of Hutch++ (no
+// Hutchinson launch has two layer slots: those have 1 or kMaxFusedLayers).
+constexpr int kHppCap = 2;
 
 // The +-1 projection (reading of papernotes.org, "Experiments > Ablation": a
 // {-1, +1} one-bit P instead of a Gaussian one): rows [128 u, 128 u + 128) of
@@ -323,6 +338,11 @@ __device__ __forceinline__ void phase_at(int ps, int L, int& l, bool& sketch) {
   if (CAP == 1) {  // one layer: S0, P0
     l = 0;
     sketch = ps == 0;
+  } else if (CAP == kHppCap) {
+    // Hutch++ passes 1 and 2: the sketch of pass 2 reads pass 1's projection,
+    // so the phases go in order, S0, P0, S1, P1
+    l = ps >> 1;
+    sketch = (ps & 1) == 0;
   } else if (ps == 0) {
     l = 0;
     sketch = true;
@@ -491,10 +511,24 @@ __global__ void __launch_bounds__(hutch_threads<PM1>(), 1)
           // phase 1: G and P tiles
           const Mine m1 = mine(Ld.ph1, cl, rank);
           const long long nb1 = count_blocks(Ld.ph1, m1);
+          // Hutch++ pass 2: the operand Z_i is per sample (its batch coordinate)
+          // and written by pass 1's projection, waited for per sample
+          const bool zbatched = CAP == kHppCap && l == 1;
+          int z_i = -1;
           for (long long j = 0; j < nb1 && ok; ++j) {
             const long long b = m1.first + j * m1.step;
             const int i = static_cast<int>(b / a.mtiles);
             const int t0 = static_cast<int>(b - static_cast<long long>(i) * a.mtiles) * kTok;
+            if (zbatched && i != z_i) {
+              if (DPRC_IN(i >= 0 && i < a.B) &&
+                  wait_geq(&a.zdone[i], a.zdone_target, lim, abort_flag)) {
+                fence_proxy_async_global();
+              } else {
+                ok = false;
+                break;
+              }
+              z_i = i;
+            }
             for (int u = m1.ulo; u < m1.uhi; ++u) {
               if (it < pre) {  // issued before the CTA barrier
                 ++it;
@@ -509,7 +543,9 @@ __global__ void __launch_bounds__(hutch_threads<PM1>(), 1)
               for (int h = 0; h < 2; ++h)
                 tma_load_3d(slot + h * Cfg::kRowGBox, &Ld.mg, &full[s], rot_unit(m1, u) * kCol + h * 64,
                             t0, i);
-              if (!PM1) tma_load_3d(slot + Cfg::kRowG, &Ld.mp, &full[s], 0, rot_unit(m1, u) * kCol, 0);
+              if (!PM1)
+                tma_load_3d(slot + Cfg::kRowG, &Ld.mp, &full[s], 0, rot_unit(m1, u) * kCol,
+                            zbatched ? i : 0);
               ++it;
             }
           }
@@ -778,6 +814,17 @@ __global__ void __launch_bounds__(hutch_threads<PM1>(), 1)
             mine_row = xchg_rows<K>(xs, cl, rank, row, rnd, rnd + 1 == rounds, y, ok, lim2);
             ++rnd;
           }
+          if (CAP == kHppCap && l == 1) {
+            // Hutch++ pass 2: the operand's columns are Z_hi | Z_lo, so the
+            // sketch is the sum of the two halves; the other half stays zero
+            // (rows K/2..K-1 of each plane of W, which the projection's MMA
+            // reads as zero columns)
+  #pragma unroll
+            for (int c = 0; c < K / 2; ++c) {
+              y[c] += y[K / 2 + c];
+              y[K / 2 + c] = 0.f;
+            }
+          }
           const long long b = m1.first + j * m1.step;
           const int i = static_cast<int>(b / a.mtiles);
           const int t = static_cast<int>(b - static_cast<long long>(i) * a.mtiles) * kTok + row;
@@ -833,6 +880,44 @@ __global__ void __launch_bounds__(hutch_threads<PM1>(), 1)
           const long long b = m2.first + j * m2.step;
           const int i = static_cast<int>(b / Ld.nchunks);
           const int ch = static_cast<int>(b - static_cast<long long>(i) * Ld.nchunks);
+          if constexpr (CAP == kHppCap) {
+            // Hutch++ passes 1 and 2: this rank's rows of the projection go to
+            // memory (pass 1: Z = columns 0..15 as hi/lo, X P = 16..31 in
+            // fp32; pass 2: M in fp32 and hi/lo), then one count per block
+            constexpr int H = K / 2;
+            const int grow = ch * kRows + row;
+            if (mine_row && ok && grow < Ld.d && DPRC_IN(i >= 0 && i < a.B)) {
+              const size_t yrow = static_cast<size_t>(i) * Ld.d + grow;
+              float yh[H];
+  #pragma unroll
+              for (int c = 0; c < H; ++c) yh[c] = y[c];
+              float4* f4 = reinterpret_cast<float4*>((l == 0 ? a.hyp : a.hm) + yrow * H);
+  #pragma unroll
+              for (int c4 = 0; c4 < H / 4; ++c4) {
+                const int c = (l == 0 ? H : 0) + 4 * c4;
+                f4[c4] = make_float4(y[c], y[c + 1], y[c + 2], y[c + 3]);
+              }
+              store_hilo_row<H>((l == 0 ? a.hz : a.hmh) + yrow * K, yh);
+            }
+            fence_proxy_async_global();  // Z is read by TMA in pass 2's sketch
+            named_bar_sync(1, 128);
+            if (threadIdx.x == 64 && ok && DPRC_IN(i >= 0 && i < a.B)) {
+              __threadfence();
+              if (l == 0) {
+                // the sample's last pass-1 block: every block of the sample has
+                // passed its wait on ready[0][i]
+                if (atomicAdd(&a.zdone[i], 1) == a.zdone_target - 1) a.ready[i] = 0;
+              } else if (atomicAdd(&a.tickets[a.B + i], 1) == a.mdone_target - 1) {
+                // the sample's last pass-2 block: every block of pass 2 has
+                // passed its waits, on zdone[i] (sketch) and ready[1][i]
+                a.tickets[a.B + i] = 0;
+                a.ready[a.B + i] = 0;
+                a.zdone[i] = 0;
+              }
+            }
+            named_bar_sync(1, 128);
+            continue;
+          }
           float sq = 0.f;
           if (mine_row && ok && ch * kRows + row < Ld.d) {
   #pragma unroll
@@ -1237,6 +1322,60 @@ cudaError_t launch_tc_hutch_fault_test(int L, const void* const* A, const void* 
                                 nullptr, &test);
   return launch_cap<kMaxFusedLayers, false>(L, A, G, P, d, p, B, T, k, ws, n_out, 0, 0, 0, s,
                                             launched, nullptr, &test);
+}
+
+cudaError_t launch_tc_hutchpp12(const void* A, const void* G, const void* SP, int64_t B,
+                                int64_t T, int64_t d, int64_t p, const FusedScratch& ws, void* Z,
+                                float* YP, float* M, void* MH, cudaStream_t s, bool* launched) {
+  *launched = false;
+  static thread_local HParams<kHppCap> a;
+  // pass 1 projects onto the rows of d (A) and sketches p (G); pass 2 the
+  // other way round
+  const int64_t dd[2] = {d, p};
+  const int64_t pp[2] = {p, d};
+  int grid = 0;
+  if (!plan_fused<kHppCap, false>(2, dd, pp, B, T, 32, a, grid)) return cudaSuccess;
+  a.wait_ns = kWaitLimitNs;
+  a.tpad = ws.tpad;
+  // One sketch buffer serves both passes: pass 2's sketch of sample i starts
+  // only once every pass-1 projection block of sample i has finished.
+  for (int b = 0; b < 3; ++b) a.W[b] = static_cast<__nv_bfloat16*>(ws.W[0]);
+  a.ready = ws.ready;
+  a.tickets = ws.tickets;
+  a.lticket = ws.lticket;
+  a.done2 = ws.done2;
+  a.exit_count = ws.exit_count;
+  a.chunk_norms = ws.chunk_norms;
+  a.nl = ws.nl;
+  a.n_out = nullptr;
+  a.accumulate = 0;
+  a.norm_scale = 1.0f;
+  a.clip_C = 0.f;
+  a.c_out = nullptr;
+  a.nonfinite = nullptr;
+  a.seed = a.step = 0;
+  a.hz = static_cast<__nv_bfloat16*>(Z);
+  a.hyp = YP;
+  a.hm = M;
+  a.hmh = static_cast<__nv_bfloat16*>(MH);
+  a.zdone = ws.lticket;
+  a.zdone_target = a.layer[0].nchunks * (a.layer[0].ph2.split ? a.cl : 1);
+  a.mdone_target = a.layer[1].nchunks * (a.layer[1].ph2.split ? a.cl : 1);
+  for (int b = 0; b < 3; ++b)
+    if (!make_tmap_3d_bf16(&a.mw[b], ws.W[0], T, 64, B, ws.tpad, 64 * ws.tpad, 64, 64, 128))
+      return cudaErrorInvalidValue;
+  LayerDesc& L0 = a.layer[0];
+  LayerDesc& L1 = a.layer[1];
+  if (!make_tmap_3d_bf16(&L0.mg, G, p, T, B, p, T * p, 64, kTok, 128) ||
+      !make_tmap_3d_bf16(&L0.mp, SP, 32, p, 1, 32, p * 32, 32, kCol, 64) ||
+      !make_tmap_3d_bf16(&L0.ma, A, d, T, B, d, T * d, 64, kTok, 128) ||
+      !make_tmap_3d_bf16(&L1.mg, A, d, T, B, d, T * d, 64, kTok, 128) ||
+      !make_tmap_3d_bf16(&L1.mp, Z, 32, d, B, 32, d * 32, 32, kCol, 64) ||
+      !make_tmap_3d_bf16(&L1.ma, G, p, T, B, p, T * p, 64, kTok, 128))
+    return cudaErrorInvalidValue;
+  const cudaError_t e = launch_k<32, kHppCap, false>(a, grid, s);
+  if (e == cudaSuccess) *launched = true;
+  return e;
 }
 
 cudaError_t launch_tc_hutch_pm1(const void* A, const void* G, int64_t B, int64_t T, int64_t d,
