@@ -253,8 +253,10 @@ int dprc_norm_hutch_launches(dprc_dtype dtype, int64_t B, int64_t T, int64_t d, 
  *  per-sample Householder QR in fp32.  Sizes as dprc_norm_hutch with
  *  1 <= r <= 64.  Other arguments as dprc_norm_hutch.
  *  For bf16 with r = 16 and p <= 4096 the call enqueues the pack of [S | P],
- *  three (sketch, projection) pairs and the QR, which runs beside the third
- *  sketch: that pass streams A_i^T G_i M_i (M_i = O_i S) and its epilogue
+ *  three (sketch, projection) pairs (the first two in one launch where its
+ *  plan fits, pass 2 of a sample starting once pass 1 has written it) and the
+ *  QR, which runs beside the third sketch: that pass streams
+ *  A_i^T G_i M_i (M_i = O_i S) and its epilogue
  *  forms A_i^T G_i Q_i = (A_i^T G_i M_i) diag(s) R^-1 from the QR of the
  *  column-scaled M_i, leaving out a column of R whose diagonal is at most
  *  1e-3 of its norm (M_i numerically rank deficient there; the estimate then
