@@ -244,6 +244,20 @@ int dprc_norm_hutch_launches(dprc_dtype dtype, int64_t B, int64_t T, int64_t d, 
                              int64_t k);
 
 /*
+ * Number of kernels one dprc_norm_hutchpp call with these arguments enqueues
+ * on the current device: 5 (bf16, r = 16, p <= 4096 and sizes that fit the
+ * fused kernel's plan: the pack of [S | P], passes 1 and 2 in one launch, the
+ * cluster QR, the third pass's sketch and its projection), 8 (the same shapes
+ * with passes 1 and 2 as four kernels; or the CUDA-core path: three sketch and
+ * projection pairs, the QR and a reduction) or 7 (other tensor-core shapes:
+ * three pairs and the QR between the second and the third).  0 for arguments
+ * dprc_norm_hutchpp would reject or when no sm_103 device is current.
+ * Enqueues nothing.  No counterpart on the pages (a library property).
+ */
+int dprc_norm_hutchpp_launches(dprc_dtype dtype, int64_t B, int64_t T, int64_t d, int64_t p,
+                               int64_t r);
+
+/*
  * Hutch++ head/tail estimate for one layer (papernotes.org, "Key design >
  * Hutch++ head-tail decomposition"; gist.science, "Kernmechanisme" item 2):
  *     Q_i     = orthonormal basis of Col(O_i S)          (p x r, thin QR)

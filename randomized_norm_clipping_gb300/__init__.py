@@ -38,6 +38,7 @@ from .binding import (  # noqa: F401
     dprc_norm_hutch_pm1,
     dprc_norm_hutch_noalloc,
     dprc_norm_hutchpp,
+    dprc_norm_hutchpp_launches,
     dprc_philox_words,
     dprc_set_phase_events,
     dprc_test_hutch_fault,

@@ -72,6 +72,8 @@ _PROTOS = [
       _c.c_void_p, _c.c_void_p, _c.c_size_t, _c.c_void_p]),
     ("dprc_norm_hutch_launches", _c.c_int,
      [_c.c_int, _c.c_int64, _c.c_int64, _c.c_int64, _c.c_int64, _c.c_int64]),
+    ("dprc_norm_hutchpp_launches", _c.c_int,
+     [_c.c_int, _c.c_int64, _c.c_int64, _c.c_int64, _c.c_int64, _c.c_int64]),
     ("dprc_exact_norm_form", _c.c_int,
      [_c.c_void_p, _c.c_void_p, _c.c_int, _c.c_int64, _c.c_int64, _c.c_int64, _c.c_int64,
       _c.c_int, _c.c_void_p, _c.c_int, _c.c_void_p, _c.c_size_t, _c.c_void_p]),
@@ -285,6 +287,12 @@ def dprc_norm_hutch_launches(dtype_code, B, T, d, p, k):
     """Kernels one dprc_norm_hutch call with these sizes enqueues on the
     current device (1 fused, 2 sketch + projection, 3 CUDA cores; 0 invalid)."""
     return int(lib().dprc_norm_hutch_launches(dtype_code, B, T, d, p, k))
+
+
+def dprc_norm_hutchpp_launches(dtype_code, B, T, d, p, r):
+    """Kernels one dprc_norm_hutchpp call with these sizes enqueues on the
+    current device (5 with passes 1 and 2 fused, 7 or 8 otherwise; 0 invalid)."""
+    return int(lib().dprc_norm_hutchpp_launches(dtype_code, B, T, d, p, r))
 
 
 def dprc_norm_hutch(A, G, P, n, accumulate=False, ws=None, stream=None):

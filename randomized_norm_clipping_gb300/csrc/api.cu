@@ -872,6 +872,15 @@ int dprc_norm_hutch_launches(dprc_dtype dtype, int64_t B, int64_t T, int64_t d, 
   return fused_hutch_planned(B, T, d, p, k) ? 1 : 2;
 }
 
+int dprc_norm_hutchpp_launches(dprc_dtype dtype, int64_t B, int64_t T, int64_t d, int64_t p,
+                               int64_t r) {
+  if (check_common(dtype, B, T, d, p) != DPRC_OK || r < 1 || r > 64 || r > p) return 0;
+  if (!device_ok()) return 0;
+  if (!tc_path_supported(dtype, B, T, d, p, r, true)) return 8;
+  if (!qr_cluster_supported(p, static_cast<int>(r))) return 7;
+  return hutchpp12_planned(B, T, d, p) ? 5 : 8;
+}
+
 dprc_status dprc_norm_hutchpp(const void* A, const void* G, const void* S, const void* P,
                               dprc_dtype dtype, int64_t B, int64_t T, int64_t d, int64_t p,
                               int64_t r, float* n, int accumulate, void* ws, size_t ws_bytes,

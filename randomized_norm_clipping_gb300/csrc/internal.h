@@ -254,6 +254,8 @@ bool fused_hutch_supported(int64_t k);
 // Whether a dprc_norm_hutch call with these sizes takes the fused kernel on
 // the current device (the same decision the launcher makes).
 bool fused_hutch_planned(int64_t B, int64_t T, int64_t d, int64_t p, int64_t k);
+// Whether launch_tc_hutchpp12 would launch for these sizes on the current device.
+bool hutchpp12_planned(int64_t B, int64_t T, int64_t d, int64_t p);
 // Optional clip epilogue: c[i] = min(1, C / sqrt(n_out[i])) (the rule of
 // dprc_clip_factors) once n_out[i] is final.
 struct ClipOut {

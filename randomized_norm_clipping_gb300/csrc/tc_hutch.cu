@@ -1324,6 +1324,14 @@ cudaError_t launch_tc_hutch_fault_test(int L, const void* const* A, const void* 
                                             launched, nullptr, &test);
 }
 
+bool hutchpp12_planned(int64_t B, int64_t T, int64_t d, int64_t p) {
+  HParams<kHppCap> a;
+  const int64_t dd[2] = {d, p};
+  const int64_t pp[2] = {p, d};
+  int grid = 0;
+  return plan_fused<kHppCap, false>(2, dd, pp, B, T, 32, a, grid);
+}
+
 cudaError_t launch_tc_hutchpp12(const void* A, const void* G, const void* SP, int64_t B,
                                 int64_t T, int64_t d, int64_t p, const FusedScratch& ws, void* Z,
                                 float* YP, float* M, void* MH, cudaStream_t s, bool* launched) {

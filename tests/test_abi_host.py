@@ -226,6 +226,7 @@ def test_valid_calls_without_a_gpu_fail_loudly(lib):
     assert st == 8  # the device check comes before the scratch lookup
     # the launch-count query enqueues nothing and reports 0 without a device
     assert lib.dprc_norm_hutch_launches(1, 8, 4096, 2048, 2048, 32) == 0
+    assert lib.dprc_norm_hutchpp_launches(1, 8, 4096, 2048, 2048, 16) == 0
 
 
 def test_launch_count_query_rejects_bad_arguments(lib):
@@ -234,6 +235,11 @@ def test_launch_count_query_rejects_bad_arguments(lib):
     assert q(1, 0, 4096, 2048, 2048, 32) == 0   # empty batch
     assert q(1, 8, 4096, 2048, 2048, 0) == 0    # k = 0
     assert q(1, 8, 4096, 2048, 2048, 300) == 0  # k > 256
+    q = lib.dprc_norm_hutchpp_launches
+    assert q(5, 8, 4096, 2048, 2048, 16) == 0   # unknown dtype
+    assert q(1, 8, 4096, 2048, 2048, 0) == 0    # r = 0
+    assert q(1, 8, 4096, 2048, 2048, 65) == 0   # r > 64
+    assert q(1, 8, 4096, 2048, 16, 32) == 0     # r > p
 
 
 def test_binding_raises_when_library_missing(monkeypatch, tmp_path):

@@ -276,6 +276,21 @@ def test_launch_count_query_matches_the_path():
     assert rnc.dprc_norm_hutch_launches(DPRC_BF16, 8, 4096, 16, 2048, 32) == 1
 
 
+def test_hutchpp_launch_count_query_matches_the_path():
+    from randomized_norm_clipping_gb300 import DPRC_BF16, DPRC_F32
+    q = rnc.dprc_norm_hutchpp_launches
+    # bf16 r = 16, p <= 4096: pack, passes 1 and 2 fused, cluster QR, pass 3
+    assert q(DPRC_BF16, 8, 4096, 2048, 2048, 16) == 5
+    assert q(DPRC_BF16, 3, 300, 136, 256, 16) == 5
+    # p > 4096: three sketch and projection pairs and the one-CTA QR
+    assert q(DPRC_BF16, 2, 256, 64, 8192, 16) == 7
+    # fp32, r != 16 or widths that are not multiples of 8: the CUDA-core path
+    assert q(DPRC_F32, 4, 128, 64, 64, 8) == 8
+    assert q(DPRC_BF16, 4, 128, 64, 64, 8) == 8
+    assert q(DPRC_BF16, 2, 100, 97, 64, 16) == 8
+    assert q(DPRC_BF16, 8, 4096, 2048, 2048, 65) == 0
+
+
 def test_one_workspace_serves_calls_with_different_batch_sizes():
     # a call with fewer samples must not leave scratch where a call with more
     # keeps its counters (they share one fixed counter block for B <= 256)
