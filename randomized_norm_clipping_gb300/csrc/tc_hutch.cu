@@ -263,6 +263,20 @@ struct HParams {
 // Hutchinson launch has two layer slots: those have 1 or kMaxFusedLayers).
 constexpr int kHppCap = 2;
 
+// A tile of a streamed operand (G in a sketch phase, A in a projection phase).
+// A Hutchinson launch reads each once, so its lines carry the evict-first L2
+// policy and the sketch written between the phases, and P, keep their place
+// in L2.  The Hutch++ launch leaves them at the default: its second sketch
+// reads the A that the first projection has just streamed, part of it from L2.
+template <int CAP>
+__device__ __forceinline__ void load_streamed(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                              int c0, int c1, int c2, uint64_t pol) {
+  if constexpr (CAP == kHppCap)
+    tma_load_3d(dst, map, bar, c0, c1, c2);
+  else
+    tma_load_3d_hint(dst, map, bar, c0, c1, c2, pol);
+}
+
 // The +-1 projection (reading of papernotes.org, "Experiments > Ablation": a
 // {-1, +1} one-bit P instead of a Gaussian one): rows [128 u, 128 u + 128) of
 // S [p][K] written by one warp as bf16 +-1 into the P tile of a sketch stage,
@@ -434,6 +448,7 @@ __global__ void __launch_bounds__(hutch_threads<PM1>(), 1)
   if (threadIdx.x == 0) {
     const LayerDesc& L0 = a.layer[0];
     const Mine m1 = mine(L0.ph1, cl, rank);
+    const uint64_t pol = l2_policy_evict_first();
     if (count_blocks(L0.ph1, m1) > 0) {
       const long long b = m1.first;
       const int i = static_cast<int>(b / a.mtiles);
@@ -443,8 +458,8 @@ __global__ void __launch_bounds__(hutch_threads<PM1>(), 1)
         mbar_arrive_expect_tx(&full[pre], PM1 ? Cfg::kRowG : Cfg::kRowStage);
 #pragma unroll
         for (int h = 0; h < 2; ++h)
-          tma_load_3d(slot + h * Cfg::kRowGBox, &L0.mg, &full[pre], rot_unit(m1, u) * kCol + h * 64,
-                      t0, i);
+          load_streamed<CAP>(slot + h * Cfg::kRowGBox, &L0.mg, &full[pre],
+                             rot_unit(m1, u) * kCol + h * 64, t0, i, pol);
         if (!PM1) tma_load_3d(slot + Cfg::kRowG, &L0.mp, &full[pre], 0, rot_unit(m1, u) * kCol, 0);
       }
     }
@@ -488,6 +503,7 @@ __global__ void __launch_bounds__(hutch_threads<PM1>(), 1)
     if (lane == 0) {
       bool ok = true;
       long long it = 0;  // stages issued (both phases, all layers)
+      const uint64_t pol = l2_policy_evict_first();
       auto take_slot = [&](long long i) -> int {
         const int s = static_cast<int>(i % kStages);
         if (!mbar_wait_lim(&empty[s], (static_cast<uint32_t>(i / kStages) & 1) ^ 1,
@@ -541,8 +557,8 @@ __global__ void __launch_bounds__(hutch_threads<PM1>(), 1)
               mbar_arrive_expect_tx(&full[s], PM1 ? Cfg::kRowG : Cfg::kRowStage);
   #pragma unroll
               for (int h = 0; h < 2; ++h)
-                tma_load_3d(slot + h * Cfg::kRowGBox, &Ld.mg, &full[s], rot_unit(m1, u) * kCol + h * 64,
-                            t0, i);
+                load_streamed<CAP>(slot + h * Cfg::kRowGBox, &Ld.mg, &full[s],
+                                   rot_unit(m1, u) * kCol + h * 64, t0, i, pol);
               if (!PM1)
                 tma_load_3d(slot + Cfg::kRowG, &Ld.mp, &full[s], 0, rot_unit(m1, u) * kCol,
                             zbatched ? i : 0);
@@ -599,8 +615,8 @@ __global__ void __launch_bounds__(hutch_threads<PM1>(), 1)
               }
   #pragma unroll
               for (int h = 0; h < 2; ++h)
-                tma_load_3d(slot + h * Cfg::kColABox, &Ld.ma, &full[s], ca.ch * kRows + h * 64,
-                            ca.u * kTok, ca.i);
+                load_streamed<CAP>(slot + h * Cfg::kColABox, &Ld.ma, &full[s], ca.ch * kRows + h * 64,
+                                   ca.u * kTok, ca.i, pol);
               ++it;
               advance(ca);
             }
