@@ -266,12 +266,14 @@ constexpr int kHppCap = 2;
 // A tile of a streamed operand (G in a sketch phase, A in a projection phase).
 // A Hutchinson launch reads each once, so its lines carry the evict-first L2
 // policy and the sketch written between the phases, and P, keep their place
-// in L2.  The Hutch++ launch leaves them at the default: its second sketch
-// reads the A that the first projection has just streamed, part of it from L2.
+// in L2.  The Hutch++ launch does the same in its sketch phases, but its
+// projections leave their operand at the default: the next pass starts by
+// reading that operand again (pass 2's sketch the A of pass 1's projection,
+// pass 3's sketch the G of pass 2's) and finds its most recent part in L2.
 template <int CAP>
 __device__ __forceinline__ void load_streamed(void* dst, const CUtensorMap* map, uint64_t* bar,
-                                              int c0, int c1, int c2, uint64_t pol) {
-  if constexpr (CAP == kHppCap)
+                                              int c0, int c1, int c2, uint64_t pol, bool sketch) {
+  if (CAP == kHppCap && !sketch)
     tma_load_3d(dst, map, bar, c0, c1, c2);
   else
     tma_load_3d_hint(dst, map, bar, c0, c1, c2, pol);
@@ -459,7 +461,7 @@ __global__ void __launch_bounds__(hutch_threads<PM1>(), 1)
 #pragma unroll
         for (int h = 0; h < 2; ++h)
           load_streamed<CAP>(slot + h * Cfg::kRowGBox, &L0.mg, &full[pre],
-                             rot_unit(m1, u) * kCol + h * 64, t0, i, pol);
+                             rot_unit(m1, u) * kCol + h * 64, t0, i, pol, true);
         if (!PM1) tma_load_3d(slot + Cfg::kRowG, &L0.mp, &full[pre], 0, rot_unit(m1, u) * kCol, 0);
       }
     }
@@ -558,7 +560,7 @@ __global__ void __launch_bounds__(hutch_threads<PM1>(), 1)
   #pragma unroll
               for (int h = 0; h < 2; ++h)
                 load_streamed<CAP>(slot + h * Cfg::kRowGBox, &Ld.mg, &full[s],
-                                   rot_unit(m1, u) * kCol + h * 64, t0, i, pol);
+                                   rot_unit(m1, u) * kCol + h * 64, t0, i, pol, true);
               if (!PM1)
                 tma_load_3d(slot + Cfg::kRowG, &Ld.mp, &full[s], 0, rot_unit(m1, u) * kCol,
                             zbatched ? i : 0);
@@ -616,7 +618,7 @@ __global__ void __launch_bounds__(hutch_threads<PM1>(), 1)
   #pragma unroll
               for (int h = 0; h < 2; ++h)
                 load_streamed<CAP>(slot + h * Cfg::kColABox, &Ld.ma, &full[s], ca.ch * kRows + h * 64,
-                                   ca.u * kTok, ca.i, pol);
+                                   ca.u * kTok, ca.i, pol, false);
               ++it;
               advance(ca);
             }

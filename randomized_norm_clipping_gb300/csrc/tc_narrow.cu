@@ -307,13 +307,16 @@ __global__ void __launch_bounds__(192, 1)
   const long long my_tiles =
       a.ntiles > blockIdx.x ? (a.ntiles - 1 - blockIdx.x) / gridDim.x + 1 : 0;
 
-  // stage u of the tile at (sample i, wide tile m) into ring slot s
+  // stage u of the tile at (sample i, wide tile m) into ring slot s.  Each
+  // wide tile is read once, with the evict-first L2 policy; the narrow rows
+  // are read again by every tile of the sample and keep the default.
   auto load_stage = [&](int i, int m, int u, int s) {
     uint8_t* st = ring + s * Cfg::kStage;
     mbar_arrive_expect_tx(&full[s], Cfg::kStage);
+    const uint64_t pol = l2_policy_evict_first();
 #pragma unroll
     for (int h = 0; h < kNwM / 64; ++h)
-      tma_load_3d(st + h * kNwBox, &map_w, &full[s], m * kNwM + h * 64, u * kNwK, i);
+      tma_load_3d_hint(st + h * kNwBox, &map_w, &full[s], m * kNwM + h * 64, u * kNwK, i, pol);
     tma_load_3d(st + kNwWide, &map_n, &full[s], 0, u * kNwK, i);
   };
   // The launch is a programmatic dependent of the previous kernel in the

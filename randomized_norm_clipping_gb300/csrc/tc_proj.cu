@@ -254,13 +254,17 @@ __global__ void __launch_bounds__(192, 2)
   // the producer (thread 0) issues the first stages right after initialising
   // the barriers, so their DRAM round trip overlaps the TMEM allocation and the
   // CTA barrier
+  // X is streamed once per launch (the operand after it in every sequence of
+  // this library is the other one): its tiles carry the evict-first L2 policy,
+  // so the sketch operand and the outputs keep their place in L2
   auto load_stage = [&](long long it, int s) {
     const long long b = wk.b0 + it / nu;
     const int kc = wk.ulo + static_cast<int>(it % nu);
     const int i = static_cast<int>(b / a.mtiles);
     const int t0 = static_cast<int>(b - static_cast<long long>(i) * a.mtiles) * kRowTile;
     mbar_arrive_expect_tx(&full[s], Cfg::kStageBytes);
-    tma_load_3d(sx + s * Cfg::kXBytes, &map_x, &full[s], kc * kTileC, t0, i);
+    tma_load_3d_hint(sx + s * Cfg::kXBytes, &map_x, &full[s], kc * kTileC, t0, i,
+                     l2_policy_evict_first());
     tma_load_3d(sr + s * Cfg::kRBytes, &map_r, &full[s], 0, kc * kTileC, a.r_batched ? i : 0);
   };
   const long long total_units = wk.b1 > wk.b0 ? (wk.b1 - wk.b0) * nu : 0;
@@ -288,6 +292,7 @@ __global__ void __launch_bounds__(192, 2)
     if (lane == 0 && wk.b1 > wk.b0) {
       long long it = 0;
       bool ok = true;
+      const uint64_t pol = l2_policy_evict_first();
       for (long long b = wk.b0; b < wk.b1 && ok; ++b) {
         const int i = static_cast<int>(b / a.mtiles);
         const int t0 = static_cast<int>(b - static_cast<long long>(i) * a.mtiles) * kRowTile;
@@ -301,7 +306,7 @@ __global__ void __launch_bounds__(192, 2)
             break;
           }
           mbar_arrive_expect_tx(&full[s], Cfg::kStageBytes);
-          tma_load_3d(sx + s * Cfg::kXBytes, &map_x, &full[s], kc * kTileC, t0, i);
+          tma_load_3d_hint(sx + s * Cfg::kXBytes, &map_x, &full[s], kc * kTileC, t0, i, pol);
           tma_load_3d(sr + s * Cfg::kRBytes, &map_r, &full[s], 0, kc * kTileC,
                       a.r_batched ? i : 0);
         }
@@ -586,13 +591,24 @@ __global__ void __launch_bounds__(192) __maxnreg__(ColCfg<NMMA>::kMaxRegs)
     i = static_cast<int>(b / a.nchunks);
     ch = static_cast<int>(b - static_cast<long long>(i) * a.nchunks);
   };
+  // X is streamed with the evict-first L2 policy when this projection ends the
+  // sequence (the norm modes), so the sketch W keeps its place in L2; a
+  // projection whose output feeds a next Hutch++ pass leaves X at the default,
+  // since that pass starts by reading X again and finds its latest part in L2
+  const bool x_last = a.mode == kColprojNorm || a.mode == kColprojHpp;
+  auto copy_x = [&](int s, int h, int c0, int c1, int i, uint64_t pol) {
+    uint8_t* dst = sx + s * Cfg::kXBytes + h * Cfg::kXBoxBytes;
+    if (x_last)
+      tma_load_3d_hint(dst, &map_x, &full[s], c0, c1, i, pol);
+    else
+      tma_load_3d(dst, &map_x, &full[s], c0, c1, i);
+  };
   auto load_x = [&](long long it, int s) {
     int i, ch, kt;
     unit(it, i, ch, kt);
+    const uint64_t pol = l2_policy_evict_first();
 #pragma unroll
-    for (int h = 0; h < 2; ++h)
-      tma_load_3d(sx + s * Cfg::kXBytes + h * Cfg::kXBoxBytes, &map_x, &full[s],
-                  ch * kColChunk + h * 64, kt * kTileT, i);
+    for (int h = 0; h < 2; ++h) copy_x(s, h, ch * kColChunk + h * 64, kt * kTileT, i, pol);
   };
   const int pre = static_cast<int>(total < Cfg::kStages ? total : Cfg::kStages);
 
@@ -656,6 +672,7 @@ __global__ void __launch_bounds__(192) __maxnreg__(ColCfg<NMMA>::kMaxRegs)
         load_w(it, it);
       }
       long long issued = pre;
+      const uint64_t pol = l2_policy_evict_first();
       // the unit of stage `it` by an incremental cursor (one division per
       // block, none per stage: this thread paces the pipeline)
       int ci, cch, ckt;
@@ -670,9 +687,7 @@ __global__ void __launch_bounds__(192) __maxnreg__(ColCfg<NMMA>::kMaxRegs)
         }
         mbar_arrive_expect_tx(&full[s], Cfg::kStageBytes);
 #pragma unroll
-        for (int h = 0; h < 2; ++h)
-          tma_load_3d(sx + s * Cfg::kXBytes + h * Cfg::kXBoxBytes, &map_x, &full[s],
-                      cch * kColChunk + h * 64, ckt * kTileT, ci);
+        for (int h = 0; h < 2; ++h) copy_x(s, h, cch * kColChunk + h * 64, ckt * kTileT, ci, pol);
         await_w(ci);
 #pragma unroll
         for (int h = 0; h < 2; ++h)
